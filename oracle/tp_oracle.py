@@ -1,0 +1,371 @@
+"""fp64 CPU oracle of the tensor-parallel transformer block (TEST INFRASTRUCTURE).
+
+This module is test infrastructure.  Only the tests, ``__graft_entry__.smoke()``
+and the ``cpu_baseline`` / reference leg of ``bench.py`` may import it; the
+product path (the CUDA library and its binding) never does, and shares no code
+with it.  It is plain numpy in float64: every function writes out the
+definition the pages give, in their order and notation, with a library matmul
+as the only primitive.  No blocking, fusion or reordering beyond the pages'.
+
+Pages cited (titles as used throughout this repository):
+  [Walkthrough]  "Megatron" distributed-training walkthrough
+                 (formulaic.cloudchewie.com, docs/.../5-megatron)
+  [TP notes]     "Megatron tensor / model parallelism" notes
+                 (amentiraz.github.io, posts/Megtron张量/模型并行)
+  [Study notes]  Megatron / ZeRO study notes (baty7811.com blog)
+  [Core DDP]     megatron.core.distributed overview (zwxr.cn news 246059)
+
+Notation: M = b*s tokens, h hidden size, h' = FFN width, N shards.  Column
+shard i holds W_i (h'/N, h) (torch ``weight`` layout, so A_i = W_i^T); row
+shard i holds U_i (h, h'/N) (B_i = U_i^T).  Every matrix is row-major.
+
+Readings where the pages are silent or garbled (each also listed in the design doc):
+  * GELU is the exact erf form (the pages' formula is an image).
+  * The row-parallel bias is added once, after the shard sum.
+  * The second vocabulary range of the 300-word example is [150, 300).
+  * An id that falls in no range yields a zero row (masked sum), not an error.
+  * The oracle keeps every intermediate in fp64; it does not mimic bf16
+    rounding of saved activations (the tolerance absorbs it).
+
+Parity status per function is stated in its docstring: "pinned by ..." names
+the tests that tie it to something other than itself.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+from scipy.special import erf as _erf
+
+_SQRT2 = math.sqrt(2.0)
+_INV_SQRT_2PI = 1.0 / math.sqrt(2.0 * math.pi)
+
+
+# --------------------------------------------------------------------------
+# GELU
+# --------------------------------------------------------------------------
+def gelu(z):
+    """GELU(z) = z * Phi(z) = z/2 * (1 + erf(z / sqrt 2)), exact erf form.
+
+    [TP notes] §MLP层: GELU is the non-linear activation between A and B (its
+    formula is an image on the page; the erf form is taken).
+    Pinned by: special values (gelu(0)=0, gelu(x)-gelu(-x)=x, gelu(x)/x->1),
+    math.erf on sample points, torch float64 F.gelu(approximate='none').
+    """
+    z = np.asarray(z, dtype=np.float64)
+    return 0.5 * z * (1.0 + _erf(z / _SQRT2))
+
+
+def gelu_prime(z):
+    """dGELU/dz = Phi(z) + z * phi(z), phi the standard normal density.
+
+    Derivative of the form above.  Pinned by: gelu_prime(0)=1/2 and central
+    finite differences of ``gelu``.
+    """
+    z = np.asarray(z, dtype=np.float64)
+    return 0.5 * (1.0 + _erf(z / _SQRT2)) + z * np.exp(-0.5 * z * z) * _INV_SQRT_2PI
+
+
+# --------------------------------------------------------------------------
+# Column-parallel linear (A split by columns) and row-parallel linear
+# --------------------------------------------------------------------------
+def column_parallel_fwd(X, W_shards, a_shards=None):
+    """Y_i = GELU(X A_i + a_i) per shard, with A_i = W_i^T.
+
+    [Walkthrough] §ColumnParallelLinear: f is the identity in forward, each
+    shard computes F.linear(X, W_i, a_i) = X W_i^T + a_i, and the output stays
+    split (no gather) because [TP notes] §MLP层 feeds Y_i straight into the
+    row-split B.  Returns (Z_i list, Y_i list).
+    Pinned by: unsharded equality, N=1 vs torch float64, finite differences.
+    """
+    Z, Y = [], []
+    for i, W in enumerate(W_shards):
+        Zi = X @ W.T
+        if a_shards is not None:
+            Zi = Zi + a_shards[i][None, :]
+        Z.append(Zi)
+        Y.append(gelu(Zi))
+    return Z, Y
+
+
+def row_parallel_fwd(Y_shards, U_shards, b=None):
+    """Out = sum_i Y_i B_i + b with B_i = U_i^T.
+
+    [Walkthrough] §RowParallelLinear: each shard computes F.linear(Y_i, U_i)
+    without bias; g is the all-reduce (sum) over shards in forward; the bias,
+    which is not split, is added once after the reduction.
+    Pinned by: unsharded equality (sharded sum == XA->GELU->B), bias-once test.
+    """
+    Out = None
+    for Yi, Ui in zip(Y_shards, U_shards):
+        Pi = Yi @ Ui.T
+        Out = Pi if Out is None else Out + Pi
+    if b is not None:
+        Out = Out + b[None, :]
+    return Out
+
+
+def mlp_fwd(X, W_shards, a_shards, U_shards, b):
+    """Tensor-parallel MLP forward: A column-split -> GELU -> B row-split.
+
+    [TP notes] §MLP层 (A by columns, B by rows, one all-reduce in forward).
+    Returns Z (M,h') and Y (M,h') with shard i in columns [i h'/N, (i+1) h'/N),
+    and Out (M,h).
+    """
+    Z, Y = column_parallel_fwd(X, W_shards, a_shards)
+    Out = row_parallel_fwd(Y, U_shards, b)
+    return np.concatenate(Z, axis=1), np.concatenate(Y, axis=1), Out
+
+
+def mlp_bwd(dOut, X, W_shards, a_shards, U_shards):
+    """Tensor-parallel MLP backward.
+
+    [Walkthrough] §RowParallelLinear: g backward is the identity, so every
+    shard sees the whole dOut;  §ColumnParallelLinear: f backward is an
+    all-reduce, so dX is the sum over shards.  Per shard i:
+        dY_i = dOut U_i,  dZ_i = dY_i * GELU'(Z_i)
+        dU_i = dOut^T Y_i,  dW_i = dZ_i^T X
+        da_i = column sums of dZ_i,  db = column sums of dOut
+        dX   = sum_i dZ_i W_i
+    Z_i, Y_i are recomputed here in fp64 from X (the oracle never takes values
+    from the device).  Returns a dict of fp64 arrays (dW, dU, da are lists).
+    Pinned by: central finite differences on tiny shapes, unsharded dX.
+    """
+    Z, Y = column_parallel_fwd(X, W_shards, a_shards)
+    dW, dU, da = [], [], []
+    dX = None
+    for i in range(len(W_shards)):
+        dYi = dOut @ U_shards[i]
+        dZi = dYi * gelu_prime(Z[i])
+        dU.append(dOut.T @ Y[i])
+        dW.append(dZi.T @ X)
+        da.append(dZi.sum(axis=0))
+        part = dZi @ W_shards[i]
+        dX = part if dX is None else dX + part
+    out = dict(dX=dX, dW=dW, dU=dU, da=da, db=dOut.sum(axis=0))
+    return out
+
+
+def mlp_bwd_sampled(dOut, X, W_shards, a_shards, U_shards, rows, units):
+    """The same definitions as ``mlp_bwd``, evaluated only where asked.
+
+    ``rows``: token indices r for which dX[r] is formed (dX is row-local).
+    ``units``: per shard, the FFN units j for which column j of dZ_i is formed
+    over all tokens, giving row j of dW_i, column j of dU_i and da_i[j].
+    Used at full workload sizes where the whole fp64 backward is too slow.
+    """
+    # dX rows: dZ_i[r] needs only X[r] and dOut[r]
+    Xr, dOr = X[rows], dOut[rows]
+    Zr, _ = column_parallel_fwd(Xr, W_shards, a_shards)
+    dXr = None
+    for i in range(len(W_shards)):
+        dZr = (dOr @ U_shards[i]) * gelu_prime(Zr[i])
+        part = dZr @ W_shards[i]
+        dXr = part if dXr is None else dXr + part
+    dW, dU, da = [], [], []
+    for i, J in enumerate(units):
+        Wj = W_shards[i][J]
+        Zj = X @ Wj.T
+        if a_shards is not None:
+            Zj = Zj + a_shards[i][J][None, :]
+        dZj = (dOut @ U_shards[i][:, J]) * gelu_prime(Zj)
+        dW.append(dZj.T @ X)
+        dU.append(dOut.T @ gelu(Zj))
+        da.append(dZj.sum(axis=0))
+    return dict(dX_rows=dXr, dW_rows=dW, dU_cols=dU, da=da, db=dOut.sum(axis=0))
+
+
+# --------------------------------------------------------------------------
+# Head-split attention projections
+# --------------------------------------------------------------------------
+def attn_proj_fwd(X, Wqkv_shards, bqkv_shards, C, Wo_shards, bo):
+    """QKV projection split by heads (column split) and output projection
+    split by rows, with the sum over shards.
+
+    [TP notes] §Self-Attention层: Q, K, V are split by columns, one or more
+    heads per shard; the output linear B is split by rows exactly like the MLP.
+    [Walkthrough] §ParallelSelfAttention: QKV outputs are not reduced; the
+    output projection's result is all-reduced.
+        QKV_i = X Wqkv_i^T + bqkv_i   (shard-major [Q_i K_i V_i] columns)
+        O     = sum_i C_i Wo_i^T + bo,  C_i = C[:, i h/N:(i+1) h/N]
+    C is the attention context (the attention core is not part of the block).
+    Pinned by: unsharded equality with a single (3h,h)/(h,h) projection.
+    """
+    N = len(Wqkv_shards)
+    d = C.shape[1] // N
+    QKV = []
+    for i in range(N):
+        q = X @ Wqkv_shards[i].T
+        if bqkv_shards is not None:
+            q = q + bqkv_shards[i][None, :]
+        QKV.append(q)
+    O = None
+    for i in range(N):
+        part = C[:, i * d:(i + 1) * d] @ Wo_shards[i].T
+        O = part if O is None else O + part
+    if bo is not None:
+        O = O + bo[None, :]
+    return np.concatenate(QKV, axis=1), O
+
+
+def attn_proj_bwd(dQKV, dO, X, C, Wqkv_shards, Wo_shards):
+    """Backward of ``attn_proj_fwd`` ([TP notes] §Self-Attention层: same
+    forward/backward principle as the MLP).
+        dWqkv_i = dQKV_i^T X,  dbqkv_i = column sums of dQKV_i
+        dX      = sum_i dQKV_i Wqkv_i            (f backward: sum over shards)
+        dWo_i   = dO^T C_i,    dbo = column sums of dO
+        dC_i    = dO Wo_i                        (g backward: identity)
+    Pinned by: central finite differences on tiny shapes.
+    """
+    N = len(Wqkv_shards)
+    w = dQKV.shape[1] // N
+    d = C.shape[1] // N
+    dWqkv, dbqkv, dWo, dC = [], [], [], []
+    dX = None
+    for i in range(N):
+        g = dQKV[:, i * w:(i + 1) * w]
+        dWqkv.append(g.T @ X)
+        dbqkv.append(g.sum(axis=0))
+        part = g @ Wqkv_shards[i]
+        dX = part if dX is None else dX + part
+        dWo.append(dO.T @ C[:, i * d:(i + 1) * d])
+        dC.append(dO @ Wo_shards[i])
+    return dict(dX=dX, dWqkv=dWqkv, dbqkv=dbqkv, dWo=dWo, dbo=dO.sum(axis=0),
+                dC=np.concatenate(dC, axis=1))
+
+
+# --------------------------------------------------------------------------
+# Vocab-parallel embedding
+# --------------------------------------------------------------------------
+def vocab_mask(ids, start, end):
+    """Mask and shift of one vocabulary range.
+
+    [Walkthrough] §VocabParallelEmbedding: input_mask = (id < start) | (id >= end);
+    masked_input = id - start, with masked positions set to 0.
+    Returns (masked_input, input_mask).
+    Pinned by: the page's own example ids [2,7,1,5], range [0,3) -> [2,0,1,0].
+    """
+    ids = np.asarray(ids, dtype=np.int64)
+    mask = (ids < start) | (ids >= end)
+    masked = ids - start
+    masked[mask] = 0
+    return masked, mask
+
+
+def vocab_parallel_embed_partials(ids, E_shards, range_starts):
+    """Per-range partial lookups: each range looks up the ids it owns and
+    writes zero rows elsewhere ([Walkthrough] §VocabParallelEmbedding;
+    [TP notes] §输入层Embedding).  Returns a list of (T,h) fp64 partials."""
+    parts = []
+    for r, Er in enumerate(E_shards):
+        masked, mask = vocab_mask(ids, range_starts[r], range_starts[r + 1])
+        out = np.asarray(Er, dtype=np.float64)[masked]
+        out[mask, :] = 0.0
+        parts.append(out)
+    return parts
+
+
+def vocab_parallel_embed(ids, E_shards, range_starts):
+    """out[t] = sum_r partial_r[t]: the all-reduce (sum) over ranges of the
+    masked lookups.  Pinned by: the 300-word two-range example, brute force
+    over every id on small vocabularies, equality with the full lookup."""
+    parts = vocab_parallel_embed_partials(ids, E_shards, range_starts)
+    out = parts[0].copy()
+    for p in parts[1:]:
+        out += p
+    return out
+
+
+def vocab_logits(X, E_shards):
+    """Per-range logits L_r = X E_r^T ([Walkthrough] §_VocabParallelCrossEntropy:
+    the output layer uses the transpose of the input word embedding; each
+    range holds its own block of columns).  Pinned by: equality with the
+    unsharded X E^T."""
+    return [X @ np.asarray(Er, dtype=np.float64).T for Er in E_shards]
+
+
+def embed_sort(ids, V):
+    """Tokens grouped by id, stable in token order: (offsets (V+1), perm).
+
+    perm lists the token positions t with 0 <= id_t < V sorted by (id_t, t);
+    offsets[v]..offsets[v+1] is the segment of id v.  This is the grouping the
+    scatter-add of the embedding gradient runs over.  Pinned by: brute force
+    (every segment is exactly the increasing list of positions holding v).
+    """
+    ids = np.asarray(ids, dtype=np.int64)
+    valid = np.nonzero((ids >= 0) & (ids < V))[0]
+    order = valid[np.argsort(ids[valid], kind="stable")]
+    counts = np.bincount(ids[valid], minlength=V) if len(valid) else np.zeros(V, np.int64)
+    offsets = np.zeros(V + 1, dtype=np.int64)
+    offsets[1:] = np.cumsum(counts)
+    return offsets, order
+
+
+def embed_scatter_grad(ids, dEmb, V):
+    """Input-side gradient of the word embedding: dE_in[v] = sum over tokens
+    t with id_t = v of dEmb[t] (backward of the lookup; an id outside [0,V)
+    contributes nothing, as its forward row was masked to zero).  A brute
+    force loop over tokens.  Pinned by: column sums equal sum_t dEmb[t] over
+    valid tokens; per-id brute force on small vocabularies."""
+    ids = np.asarray(ids, dtype=np.int64)
+    out = np.zeros((V, dEmb.shape[1]), dtype=np.float64)
+    for t in range(len(ids)):
+        v = int(ids[t])
+        if 0 <= v < V:
+            out[v] += dEmb[t]
+    return out
+
+
+def tied_embed_grad(ids, dEmb, X, dLogits_shards, range_starts, V):
+    """Gradient of the tied word embedding = input-side scatter-add + output
+    side dLogits^T X, kept separately and then summed.
+
+    [TP notes] §输出层Embedding: the input and output layers share one word
+    embedding, and the update must use the sum of both gradients.
+    Returns a list of per-range (|r|, h) fp64 blocks.
+    Pinned by: the decomposition, the dLogits=0 and dEmb=0 reductions.
+    """
+    scatter = embed_scatter_grad(ids, dEmb, V)
+    out = []
+    for r, dL in enumerate(dLogits_shards):
+        s, e = range_starts[r], range_starts[r + 1]
+        gemm = dL.T @ X
+        out.append(scatter[s:e] + gemm)
+    return out
+
+
+def tied_embed_grad_rows(ids, dEmb, X, dLogits_full, vocab_rows):
+    """``tied_embed_grad`` for a subset of vocabulary rows (global ids),
+    dLogits given unsharded (T, V).  Row v = sum_{t: id_t = v} dEmb[t] +
+    dLogits[:, v]^T X."""
+    ids = np.asarray(ids, dtype=np.int64)
+    rows = []
+    for v in vocab_rows:
+        acc = dLogits_full[:, v] @ X
+        sel = np.nonzero(ids == v)[0]
+        for t in sel:
+            acc = acc + dEmb[t]
+        rows.append(acc)
+    return np.stack(rows) if rows else np.zeros((0, X.shape[1]))
+
+
+# --------------------------------------------------------------------------
+# Closed forms the pages state
+# --------------------------------------------------------------------------
+def param_count(H, L, V):
+    """(12 H^2 + 4 H) L + 2 H V: per layer 3H^2 (QKV) + H^2 (attention output)
+    + 4H^2 + 4H^2 (MLP up/down) + 2*(2H) (two LayerNorms), plus the input
+    embedding and output projection, 2 H V ([Walkthrough], model set-up
+    paragraph after model_provider).  Pinned by: the page's 2,827,821,056."""
+    return (12 * H * H + 4 * H) * L + 2 * H * V
+
+
+def tp_block_comm_volume(b, s, h):
+    """Communication of one MLP (or attention) block under tensor parallelism:
+    one all-reduce in forward and one in backward, each a reduce-scatter plus
+    an all-gather of phi = b*s*h elements, so 2*phi each and 4*phi in all
+    ([TP notes] §MLP层的通讯量分析, §Self-Attention层的通讯量分析).
+    Returns (phi, number of shard sums, total volume)."""
+    phi = b * s * h
+    n_sums = 2
+    return phi, n_sums, n_sums * 2 * phi

@@ -1,0 +1,170 @@
+"""Seeded synthetic inputs for the tensor-parallel block.
+
+This module is shared by the tests, ``bench.py`` and ``smoke()``: it holds the
+workload shapes, the seeds and the random draws, and nothing of the block's
+arithmetic (no GEMM, no activation, no masking, no reduction).  The same bytes
+feed both the CUDA path and the fp64 oracle.
+
+Recipe (one rule for every tensor):
+  * every tensor is drawn in full (unsharded) from its own PCG64 stream,
+    ``numpy.random.Generator(PCG64([seed, stream_id]))``, as float32 normals
+    scaled by the tensor's standard deviation, then rounded once to the
+    workload's dtype (bf16 by round-to-nearest-even through torch);
+  * the full tensor is then split into its shards, so a sharded and an
+    unsharded computation see identical values (init-then-split);
+  * weights ~ N(0, 0.02), activations and upstream gradients ~ N(0, 1),
+    biases are zero unless a test asks for N(0, bias_std);
+  * token ids are uniform integers in [0, V) drawn from their own stream.
+
+No public dataset is involved: the pages name none for this path.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+__all__ = ["WORKLOADS", "normal", "uniform_ids", "mlp_inputs", "attn_inputs",
+           "embed_inputs", "split_rows", "split_cols"]
+
+# Workloads: shapes and seeds only.  Names state the sizes.
+WORKLOADS = {
+    # tiny fp32 MLP: b=1, s=8, h=64, h'=4h=256, N=2
+    "mlp_tiny_f32": dict(kind="mlp", dtype="f32", b=1, s=8, h=64, hp=256, N=2, seed=1000),
+    # tiny fp32 vocab-parallel embedding: V=300, h=16, two ranges, ids [0,212,7,9]
+    "embed_tiny_f32": dict(kind="embed", dtype="f32", V=300, h=16, b=1, s=4,
+                           ranges=[0, 150, 300], ids=[0, 212, 7, 9], seed=1000),
+    # bf16 MLP: b=4, s=1024, h=1024, h'=4096, N=4
+    "mlp_b4_s1024_h1024_hp4096_N4": dict(kind="mlp", dtype="bf16", b=4, s=1024, h=1024,
+                                         hp=4096, N=4, seed=1001),
+    # bf16 MLP at model width: b=2, s=2048, h=4096, h'=16384, N=2
+    "mlp_b2_s2048_h4096_hp16384_N2": dict(kind="mlp", dtype="bf16", b=2, s=2048, h=4096,
+                                          hp=16384, N=2, seed=1002),
+    # bf16 head-split attention projections: b=1, s=2048, h=4096, 8 heads of 512, N=8
+    "attn_b1_s2048_h4096_heads8_N8": dict(kind="attn", dtype="bf16", b=1, s=2048, h=4096,
+                                          n_heads=8, N=8, seed=1003),
+    # bf16 vocab-parallel tied embedding: V=50257, h=4096, b=4, s=2048, two ranges
+    "embed_tied_V50257_h4096_T8192": dict(kind="embed", dtype="bf16", V=50257, h=4096, b=4,
+                                          s=2048, ranges=[0, 25129, 50257], seed=1004),
+}
+
+_TORCH_DTYPE = {"f32": torch.float32, "bf16": torch.bfloat16}
+
+
+def _gen(seed: int, stream: int) -> np.random.Generator:
+    return np.random.Generator(np.random.PCG64([int(seed), int(stream)]))
+
+
+def normal(seed: int, stream: int, shape, std: float, dtype: str) -> torch.Tensor:
+    """N(0, std^2) draw, float32 then rounded once to ``dtype``; CPU tensor."""
+    g = _gen(seed, stream)
+    a = g.standard_normal(size=shape, dtype=np.float32)
+    if std != 1.0:
+        a *= np.float32(std)
+    return torch.from_numpy(a).to(_TORCH_DTYPE[dtype])
+
+
+def uniform_ids(seed: int, stream: int, T: int, V: int) -> torch.Tensor:
+    """T token ids uniform in [0, V) as int64; CPU tensor."""
+    g = _gen(seed, stream)
+    return torch.from_numpy(g.integers(0, V, size=T, dtype=np.int64))
+
+
+def split_rows(t: torch.Tensor, N: int):
+    """Contiguous copies of N equal row blocks of ``t``."""
+    n = t.shape[0] // N
+    return [t[i * n:(i + 1) * n].contiguous() for i in range(N)]
+
+
+def split_cols(t: torch.Tensor, N: int):
+    """Contiguous copies of N equal column blocks of ``t``."""
+    n = t.shape[1] // N
+    return [t[:, i * n:(i + 1) * n].contiguous() for i in range(N)]
+
+
+def mlp_inputs(cfg: dict, bias_std: float = 0.0, M: int | None = None) -> dict:
+    """Inputs of the column->GELU->row MLP block.
+
+    Returns full tensors and their shards:
+      X (M,h), dOut (M,h) ~ N(0,1);
+      W (h',h) ~ N(0,0.02), split by rows into W_i (h'/N,h)  [column-parallel A];
+      U (h,h') ~ N(0,0.02), split by columns into U_i (h,h'/N) [row-parallel B];
+      a (h') and b (h) biases (zero unless ``bias_std`` > 0).
+    """
+    dt, seed, N = cfg["dtype"], cfg["seed"], cfg["N"]
+    h, hp = cfg["h"], cfg["hp"]
+    M = cfg["b"] * cfg["s"] if M is None else M
+    X = normal(seed, 1, (M, h), 1.0, dt)
+    W = normal(seed, 2, (hp, h), 0.02, dt)
+    U = normal(seed, 3, (h, hp), 0.02, dt)
+    dOut = normal(seed, 4, (M, h), 1.0, dt)
+    if bias_std > 0:
+        a = normal(seed, 5, (hp,), bias_std, dt)
+        b = normal(seed, 6, (h,), bias_std, dt)
+    else:
+        a = torch.zeros(hp, dtype=_TORCH_DTYPE[dt])
+        b = torch.zeros(h, dtype=_TORCH_DTYPE[dt])
+    return dict(M=M, h=h, hp=hp, N=N, dtype=dt, X=X, W=W, U=U, a=a, b=b, dOut=dOut,
+                W_shards=split_rows(W, N), U_shards=split_cols(U, N),
+                a_shards=[x.contiguous() for x in a.chunk(N)])
+
+
+def attn_inputs(cfg: dict, bias_std: float = 0.0, M: int | None = None) -> dict:
+    """Inputs of the head-split attention projections.
+
+    Wqkv (3h,h) is stored in the global [Q; K; V] order; shard i gathers the rows
+    of its heads from each of Q, K and V, giving (3h/N, h) = [Q_i; K_i; V_i].
+    Wo (h,h) is split by columns into Wo_i (h, h/N).  C is the attention context
+    that feeds the output projection (the attention core is not part of the
+    block), ~N(0,1), as are X and the upstream gradients dQKV, dO.
+    """
+    dt, seed, N = cfg["dtype"], cfg["seed"], cfg["N"]
+    h = cfg["h"]
+    M = cfg["b"] * cfg["s"] if M is None else M
+    X = normal(seed, 11, (M, h), 1.0, dt)
+    Wqkv = normal(seed, 12, (3 * h, h), 0.02, dt)
+    Wo = normal(seed, 13, (h, h), 0.02, dt)
+    C = normal(seed, 14, (M, h), 1.0, dt)
+    dQKV = normal(seed, 15, (M, 3 * h), 1.0, dt)
+    dO = normal(seed, 16, (M, h), 1.0, dt)
+    if bias_std > 0:
+        bqkv = normal(seed, 17, (3 * h,), bias_std, dt)
+        bo = normal(seed, 18, (h,), bias_std, dt)
+    else:
+        bqkv = torch.zeros(3 * h, dtype=_TORCH_DTYPE[dt])
+        bo = torch.zeros(h, dtype=_TORCH_DTYPE[dt])
+    d = h // N
+    Wqkv_shards, bqkv_shards = [], []
+    for i in range(N):
+        rows = [Wqkv[j * h + i * d: j * h + (i + 1) * d] for j in range(3)]
+        Wqkv_shards.append(torch.cat(rows, 0).contiguous())
+        bqkv_shards.append(torch.cat([bqkv[j * h + i * d: j * h + (i + 1) * d] for j in range(3)]).contiguous())
+    return dict(M=M, h=h, N=N, n_heads=cfg["n_heads"], dtype=dt, X=X, Wqkv=Wqkv, Wo=Wo, C=C,
+                dQKV=dQKV, dO=dO, bqkv=bqkv, bo=bo, Wqkv_shards=Wqkv_shards,
+                bqkv_shards=bqkv_shards, Wo_shards=split_cols(Wo, N))
+
+
+def embed_inputs(cfg: dict, T: int | None = None) -> dict:
+    """Inputs of the vocab-parallel embedding and its tied output layer.
+
+    E (V,h) ~ N(0,0.02) for bf16 workloads (N(0,1) for the tiny fp32 one),
+    split by the vocabulary ranges into E_r (|r|, h).  ids uniform in [0,V)
+    unless the workload fixes them.  X (the last hidden state feeding the
+    output layer), dEmb (gradient reaching the embedding output) and dLogits
+    (gradient of the logits) ~ N(0,1).  dLogits is stored per range, (T, |r|).
+    """
+    dt, seed, V, h = cfg["dtype"], cfg["seed"], cfg["V"], cfg["h"]
+    ranges = list(cfg["ranges"])
+    if "ids" in cfg and T is None:
+        ids = torch.tensor(cfg["ids"], dtype=torch.int64)
+    else:
+        T = cfg["b"] * cfg["s"] if T is None else T
+        ids = uniform_ids(seed, 21, T, V)
+    T = ids.numel()
+    E = normal(seed, 22, (V, h), 1.0 if dt == "f32" else 0.02, dt)
+    X = normal(seed, 23, (T, h), 1.0, dt)
+    dEmb = normal(seed, 24, (T, h), 1.0, dt)
+    dLogits = normal(seed, 25, (T, V), 1.0, dt)
+    E_shards = [E[ranges[r]:ranges[r + 1]].contiguous() for r in range(len(ranges) - 1)]
+    dL_shards = [dLogits[:, ranges[r]:ranges[r + 1]].contiguous() for r in range(len(ranges) - 1)]
+    return dict(T=T, V=V, h=h, N=len(ranges) - 1, dtype=dt, ranges=ranges, ids=ids, E=E,
+                E_shards=E_shards, X=X, dEmb=dEmb, dLogits=dLogits, dLogits_shards=dL_shards)

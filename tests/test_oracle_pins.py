@@ -1,0 +1,492 @@
+"""Pins of the fp64 oracle to what the pages and the mathematics fix.
+
+Each check is written as a function of the oracle module so that the
+planted-mistake tests at the bottom can re-run it against a deliberately
+broken oracle (on the CPU) and show that the pin catches the mistake.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+import oracle.tp_oracle as O
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def golden(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+def rng(seed=0):
+    return np.random.default_rng(seed)
+
+
+def tiny_mlp(seed=0, M=3, h=4, hp=8, N=2, bias=True):
+    g = rng(seed)
+    X = g.standard_normal((M, h))
+    W = g.standard_normal((hp, h)) * 0.5
+    U = g.standard_normal((h, hp)) * 0.5
+    a = g.standard_normal(hp) * 0.3 if bias else np.zeros(hp)
+    b = g.standard_normal(h) * 0.3 if bias else np.zeros(h)
+    dOut = g.standard_normal((M, h))
+    n = hp // N
+    return dict(X=X, W=W, U=U, a=a, b=b, dOut=dOut, N=N,
+                Ws=[W[i * n:(i + 1) * n] for i in range(N)],
+                Us=[U[:, i * n:(i + 1) * n] for i in range(N)],
+                As=[a[i * n:(i + 1) * n] for i in range(N)])
+
+
+# ----------------------------------------------------------------------------
+# GELU
+# ----------------------------------------------------------------------------
+def check_gelu(mod):
+    xs = np.linspace(-6, 6, 97)
+    errs = []
+    # math.erf (C library) as an independent routine
+    ref = np.array([0.5 * x * (1 + math.erf(x / math.sqrt(2))) for x in xs])
+    errs.append(np.max(np.abs(mod.gelu(xs) - ref)))
+    # torch float64 exact GELU, a third implementation
+    t = F.gelu(torch.tensor(xs, dtype=torch.float64), approximate="none").numpy()
+    errs.append(np.max(np.abs(mod.gelu(xs) - t)))
+    # special values and the odd-part identity gelu(x) - gelu(-x) = x
+    errs.append(abs(mod.gelu(0.0)))
+    errs.append(np.max(np.abs(mod.gelu(xs) - mod.gelu(-xs) - xs)))
+    errs.append(abs(mod.gelu(30.0) / 30.0 - 1.0))
+    # textbook normal-table values: gelu(x) = x Phi(x)
+    gd = golden("gelu_row_split.json")
+    # (the table has 10 digits, so it is held to 1e-9, scaled into the 1e-12 gate)
+    errs.append(abs(mod.gelu(1.0) - gd["Phi_1"]) * 1e-3)
+    errs.append(abs(mod.gelu(2.0) - 2 * gd["Phi_2"]) * 1e-3)
+    return max(errs)
+
+
+def check_gelu_prime(mod):
+    xs = np.linspace(-5, 5, 41)
+    eps = 1e-6
+    fd = (mod.gelu(xs + eps) - mod.gelu(xs - eps)) / (2 * eps)
+    e1 = np.max(np.abs(mod.gelu_prime(xs) - fd))
+    e2 = abs(mod.gelu_prime(0.0) - 0.5)
+    # torch autograd of the exact GELU
+    t = torch.tensor(xs, dtype=torch.float64, requires_grad=True)
+    F.gelu(t, approximate="none").sum().backward()
+    e3 = np.max(np.abs(mod.gelu_prime(xs) - t.grad.numpy()))
+    return max(e1, e2, e3)
+
+
+def test_gelu_pinned():
+    assert check_gelu(O) < 1e-12
+
+
+def test_gelu_prime_pinned():
+    assert check_gelu_prime(O) < 1e-8
+
+
+def test_gelu_row_split_differs_closed_form():
+    gd = golden("gelu_row_split.json")
+    assert round(float(O.gelu(2.0)), 4) == gd["gelu_2"]
+    assert round(float(2 * O.gelu(1.0)), 4) == gd["two_gelu_1"]
+
+
+# ----------------------------------------------------------------------------
+# MLP forward: sharded == unsharded, row split differs, bias once
+# ----------------------------------------------------------------------------
+def torch_mlp(X, W, a, U, b):
+    """Unsharded X A -> GELU -> B with torch float64 library routines."""
+    t = lambda x: torch.tensor(x, dtype=torch.float64)
+    Z = F.linear(t(X), t(W), t(a))
+    return F.linear(F.gelu(Z, approximate="none"), t(U), t(b)).numpy()
+
+
+def check_mlp_fwd_unsharded(mod):
+    worst = 0.0
+    g = rng(1)
+    M, h, hp = 5, 16, 64
+    X = g.standard_normal((M, h))
+    W = g.standard_normal((hp, h)) * 0.3
+    U = g.standard_normal((h, hp)) * 0.3
+    a = g.standard_normal(hp) * 0.2
+    b = g.standard_normal(h) * 0.2
+    ref = torch_mlp(X, W, a, U, b)
+    for N in (1, 2, 4, 8):
+        n = hp // N
+        Z, Y, Out = mod.mlp_fwd(X, [W[i * n:(i + 1) * n] for i in range(N)],
+                                [a[i * n:(i + 1) * n] for i in range(N)],
+                                [U[:, i * n:(i + 1) * n] for i in range(N)], b)
+        worst = max(worst, np.max(np.abs(Out - ref)))
+        Zref = X @ W.T + a
+        worst = max(worst, np.max(np.abs(Z - Zref)))
+    return worst
+
+
+def test_mlp_sharded_equals_unsharded():
+    assert check_mlp_fwd_unsharded(O) < 1e-12
+
+
+def test_row_split_before_gelu_differs():
+    """Splitting A by rows (X by columns) and applying GELU to the partials
+    gives a different result; the difference is far above any tolerance."""
+    g = rng(2)
+    M, h, hp, N = 8, 32, 64, 2
+    X = g.standard_normal((M, h))
+    A = g.standard_normal((h, hp)) * 0.3
+    k = h // N
+    row_split = sum(O.gelu(X[:, i * k:(i + 1) * k] @ A[i * k:(i + 1) * k]) for i in range(N))
+    correct = O.gelu(X @ A)
+    rel = np.max(np.abs(row_split - correct)) / np.max(np.abs(correct))
+    assert rel > 10 * 2e-2
+
+
+def test_bias_added_once_after_shard_sum():
+    d = tiny_mlp(3, M=4, h=8, hp=16, N=4)
+    _, _, out_b = O.mlp_fwd(d["X"], d["Ws"], d["As"], d["Us"], d["b"])
+    _, _, out_0 = O.mlp_fwd(d["X"], d["Ws"], d["As"], d["Us"], np.zeros_like(d["b"]))
+    assert np.max(np.abs((out_b - out_0) - d["b"][None, :])) < 1e-12
+
+
+# ----------------------------------------------------------------------------
+# MLP backward: central finite differences in fp64, torch autograd
+# ----------------------------------------------------------------------------
+def mlp_loss(mod, d, X=None, Ws=None, As=None, Us=None, b=None):
+    _, _, Out = mod.mlp_fwd(d["X"] if X is None else X, d["Ws"] if Ws is None else Ws,
+                            d["As"] if As is None else As, d["Us"] if Us is None else Us,
+                            d["b"] if b is None else b)
+    return float(np.sum(Out * d["dOut"]))
+
+
+def fd_grad(f, x, eps=1e-6):
+    g = np.zeros_like(x)
+    it = np.nditer(x, flags=["multi_index"])
+    for _ in it:
+        idx = it.multi_index
+        old = x[idx]
+        x[idx] = old + eps
+        fp = f()
+        x[idx] = old - eps
+        fm = f()
+        x[idx] = old
+        g[idx] = (fp - fm) / (2 * eps)
+    return g
+
+
+def check_mlp_bwd_fd(mod):
+    d = tiny_mlp(4)
+    grads = mod.mlp_bwd(d["dOut"], d["X"], d["Ws"], d["As"], d["Us"])
+    worst = 0.0
+    X = d["X"].copy()
+    worst = max(worst, np.max(np.abs(grads["dX"] - fd_grad(lambda: mlp_loss(mod, d, X=X), X))))
+    for i in range(d["N"]):
+        Ws = [w.copy() for w in d["Ws"]]
+        worst = max(worst, np.max(np.abs(grads["dW"][i] - fd_grad(lambda: mlp_loss(mod, d, Ws=Ws), Ws[i]))))
+        Us = [u.copy() for u in d["Us"]]
+        worst = max(worst, np.max(np.abs(grads["dU"][i] - fd_grad(lambda: mlp_loss(mod, d, Us=Us), Us[i]))))
+        As = [a.copy() for a in d["As"]]
+        worst = max(worst, np.max(np.abs(grads["da"][i] - fd_grad(lambda: mlp_loss(mod, d, As=As), As[i]))))
+    b = d["b"].copy()
+    worst = max(worst, np.max(np.abs(grads["db"] - fd_grad(lambda: mlp_loss(mod, d, b=b), b))))
+    return worst
+
+
+def test_mlp_bwd_finite_differences():
+    assert check_mlp_bwd_fd(O) < 1e-7
+
+
+def test_mlp_bwd_matches_torch_autograd_unsharded():
+    d = tiny_mlp(5, M=6, h=8, hp=32, N=4)
+    t = lambda x: torch.tensor(x, dtype=torch.float64, requires_grad=True)
+    X, W, a, U, b = t(d["X"]), t(d["W"]), t(d["a"]), t(d["U"]), t(d["b"])
+    out = F.linear(F.gelu(F.linear(X, W, a), approximate="none"), U, b)
+    (out * torch.tensor(d["dOut"])).sum().backward()
+    g = O.mlp_bwd(d["dOut"], d["X"], d["Ws"], d["As"], d["Us"])
+    assert np.max(np.abs(g["dX"] - X.grad.numpy())) < 1e-12
+    assert np.max(np.abs(np.concatenate(g["dW"], 0) - W.grad.numpy())) < 1e-12
+    assert np.max(np.abs(np.concatenate(g["dU"], 1) - U.grad.numpy())) < 1e-12
+    assert np.max(np.abs(np.concatenate(g["da"]) - a.grad.numpy())) < 1e-12
+    assert np.max(np.abs(g["db"] - b.grad.numpy())) < 1e-12
+
+
+def test_mlp_bwd_sampled_equals_full():
+    d = tiny_mlp(6, M=10, h=8, hp=32, N=4)
+    full = O.mlp_bwd(d["dOut"], d["X"], d["Ws"], d["As"], d["Us"])
+    rows = [0, 3, 9]
+    units = [[0, 5], [1], [2, 3, 7], [6]]
+    s = O.mlp_bwd_sampled(d["dOut"], d["X"], d["Ws"], d["As"], d["Us"], rows, units)
+    assert np.max(np.abs(s["dX_rows"] - full["dX"][rows])) < 1e-12
+    for i, J in enumerate(units):
+        assert np.max(np.abs(s["dW_rows"][i] - full["dW"][i][J])) < 1e-12
+        assert np.max(np.abs(s["dU_cols"][i] - full["dU"][i][:, J])) < 1e-12
+        assert np.max(np.abs(s["da"][i] - full["da"][i][J])) < 1e-12
+
+
+def test_comm_volume_4phi():
+    phi, n_sums, vol = O.tp_block_comm_volume(4, 1024, 1024)
+    assert phi == 4 * 1024 * 1024 and n_sums == 2 and vol == 4 * phi
+
+
+# ----------------------------------------------------------------------------
+# Attention projections
+# ----------------------------------------------------------------------------
+def tiny_attn(seed=7, M=3, h=8, N=2):
+    g = rng(seed)
+    d = h // N
+    X = g.standard_normal((M, h))
+    Wqkv = g.standard_normal((3 * h, h)) * 0.5
+    Wo = g.standard_normal((h, h)) * 0.5
+    bqkv = g.standard_normal(3 * h) * 0.3
+    bo = g.standard_normal(h) * 0.3
+    C = g.standard_normal((M, h))
+    Ws = [np.concatenate([Wqkv[j * h + i * d: j * h + (i + 1) * d] for j in range(3)]) for i in range(N)]
+    Bs = [np.concatenate([bqkv[j * h + i * d: j * h + (i + 1) * d] for j in range(3)]) for i in range(N)]
+    Wos = [Wo[:, i * d:(i + 1) * d] for i in range(N)]
+    return dict(X=X, Wqkv=Wqkv, Wo=Wo, bqkv=bqkv, bo=bo, C=C, Ws=Ws, Bs=Bs, Wos=Wos, N=N, h=h, d=d,
+                dQKV=g.standard_normal((M, 3 * h)), dO=g.standard_normal((M, h)))
+
+
+def test_attn_proj_sharded_equals_unsharded():
+    a = tiny_attn(M=5, h=16, N=4)
+    QKV, Oo = O.attn_proj_fwd(a["X"], a["Ws"], a["Bs"], a["C"], a["Wos"], a["bo"])
+    full = torch.nn.functional.linear(torch.tensor(a["X"]), torch.tensor(a["Wqkv"]), torch.tensor(a["bqkv"])).numpy()
+    h, d, N = a["h"], a["d"], a["N"]
+    for i in range(N):
+        for j in range(3):
+            got = QKV[:, i * 3 * d + j * d: i * 3 * d + (j + 1) * d]
+            ref = full[:, j * h + i * d: j * h + (i + 1) * d]
+            assert np.max(np.abs(got - ref)) < 1e-12
+    Oref = F.linear(torch.tensor(a["C"]), torch.tensor(a["Wo"]), torch.tensor(a["bo"])).numpy()
+    assert np.max(np.abs(Oo - Oref)) < 1e-12
+
+
+def check_attn_bwd_fd(mod):
+    a = tiny_attn()
+
+    def loss(X=None, Ws=None, C=None, Wos=None):
+        QKV, Oo = mod.attn_proj_fwd(a["X"] if X is None else X, a["Ws"] if Ws is None else Ws,
+                                    a["Bs"], a["C"] if C is None else C,
+                                    a["Wos"] if Wos is None else Wos, a["bo"])
+        return float(np.sum(QKV * a["dQKV"]) + np.sum(Oo * a["dO"]))
+
+    g = mod.attn_proj_bwd(a["dQKV"], a["dO"], a["X"], a["C"], a["Ws"], a["Wos"])
+    worst = 0.0
+    X = a["X"].copy()
+    worst = max(worst, np.max(np.abs(g["dX"] - fd_grad(lambda: loss(X=X), X))))
+    C = a["C"].copy()
+    worst = max(worst, np.max(np.abs(g["dC"] - fd_grad(lambda: loss(C=C), C))))
+    for i in range(a["N"]):
+        Ws = [w.copy() for w in a["Ws"]]
+        worst = max(worst, np.max(np.abs(g["dWqkv"][i] - fd_grad(lambda: loss(Ws=Ws), Ws[i]))))
+        Wos = [w.copy() for w in a["Wos"]]
+        worst = max(worst, np.max(np.abs(g["dWo"][i] - fd_grad(lambda: loss(Wos=Wos), Wos[i]))))
+    worst = max(worst, np.max(np.abs(g["dbo"] - a["dO"].sum(0))))
+    return worst
+
+
+def test_attn_bwd_finite_differences():
+    assert check_attn_bwd_fd(O) < 1e-7
+
+
+# ----------------------------------------------------------------------------
+# Vocab-parallel embedding
+# ----------------------------------------------------------------------------
+def test_vocab_mask_page_example():
+    gd = golden("vocab_mask_example.json")
+    masked, mask = O.vocab_mask(gd["ids"], gd["start"], gd["end"])
+    assert masked.tolist() == gd["masked_input"]
+    assert mask.tolist() == gd["input_mask"]
+
+
+def check_vocab300(mod):
+    gd = golden("vocab300_two_ranges.json")
+    V, rs, ids = gd["V"], gd["range_starts"], gd["ids"]
+    E = rng(8).standard_normal((V, 16))
+    Es = [E[rs[r]:rs[r + 1]] for r in range(2)]
+    parts = mod.vocab_parallel_embed_partials(ids, Es, rs)
+    ok = True
+    for r in range(2):
+        zero_rows = [t for t in range(len(ids)) if not np.any(parts[r][t])]
+        ok &= zero_rows == gd["zero_rows_per_range"][r]
+    out = mod.vocab_parallel_embed(ids, Es, rs)
+    ok &= bool(np.array_equal(out, E[ids]))
+    return ok
+
+
+def test_vocab300_two_range_example():
+    assert check_vocab300(O)
+
+
+def test_vocab_embed_brute_force_small_vocab():
+    g = rng(9)
+    for V in (1, 7, 64):
+        for N in (1, 2, 3):
+            if N > V:
+                continue
+            cuts = sorted(g.choice(np.arange(1, V), size=N - 1, replace=False).tolist()) if N > 1 else []
+            rs = [0] + cuts + [V]
+            E = g.standard_normal((V, 5))
+            Es = [E[rs[r]:rs[r + 1]] for r in range(N)]
+            ids = list(range(V)) + [-1, V, V + 3, -7]
+            out = O.vocab_parallel_embed(ids, Es, rs)
+            for t, v in enumerate(ids):
+                if 0 <= v < V:
+                    assert np.array_equal(out[t], E[v])
+                else:
+                    assert not np.any(out[t])
+            # torch F.embedding on the valid ids
+            valid = [v for v in ids if 0 <= v < V]
+            te = F.embedding(torch.tensor(valid), torch.tensor(E)).numpy()
+            assert np.array_equal(out[:len(valid)], te)
+
+
+def test_vocab_logits_equals_unsharded():
+    g = rng(10)
+    V, h, T = 37, 6, 5
+    rs = [0, 11, 20, 37]
+    E = g.standard_normal((V, h))
+    X = g.standard_normal((T, h))
+    Ls = O.vocab_logits(X, [E[rs[r]:rs[r + 1]] for r in range(3)])
+    ref = F.linear(torch.tensor(X), torch.tensor(E)).numpy()
+    assert np.max(np.abs(np.concatenate(Ls, 1) - ref)) < 1e-12
+
+
+# ----------------------------------------------------------------------------
+# Tied embedding gradient
+# ----------------------------------------------------------------------------
+def tied_case(seed=11, V=23, h=4, T=40, rs=(0, 9, 23)):
+    g = rng(seed)
+    ids = g.integers(-2, V + 2, size=T)
+    ids[:6] = 5  # a repeated id
+    return dict(ids=ids, V=V, rs=list(rs), dEmb=g.standard_normal((T, h)), X=g.standard_normal((T, h)),
+                dL=g.standard_normal((T, V)))
+
+
+def check_scatter(mod):
+    c = tied_case()
+    s = mod.embed_scatter_grad(c["ids"], c["dEmb"], c["V"])
+    ref = np.zeros_like(s)
+    valid = (c["ids"] >= 0) & (c["ids"] < c["V"])
+    np.add.at(ref, c["ids"][valid], c["dEmb"][valid])
+    e1 = np.max(np.abs(s - ref))
+    e2 = np.max(np.abs(s.sum(0) - c["dEmb"][valid].sum(0)))
+    # torch autograd of F.embedding on the valid tokens
+    Et = torch.zeros((c["V"], c["dEmb"].shape[1]), dtype=torch.float64, requires_grad=True)
+    out = F.embedding(torch.tensor(c["ids"][valid]), Et)
+    (out * torch.tensor(c["dEmb"][valid])).sum().backward()
+    e3 = np.max(np.abs(s - Et.grad.numpy()))
+    return max(e1, e2, e3)
+
+
+def test_scatter_grad_pinned():
+    assert check_scatter(O) < 1e-12
+
+
+def test_tied_grad_is_sum_of_both_contributions():
+    c = tied_case()
+    rs, V = c["rs"], c["V"]
+    dLs = [c["dL"][:, rs[r]:rs[r + 1]] for r in range(2)]
+    tg = np.concatenate(O.tied_embed_grad(c["ids"], c["dEmb"], c["X"], dLs, rs, V), 0)
+    scatter = O.embed_scatter_grad(c["ids"], c["dEmb"], V)
+    assert np.max(np.abs(tg - (scatter + c["dL"].T @ c["X"]))) < 1e-12
+    # dLogits = 0 reduces to the embedding backward; dEmb = 0 to dLogits^T X
+    z = [np.zeros_like(x) for x in dLs]
+    t0 = np.concatenate(O.tied_embed_grad(c["ids"], c["dEmb"], c["X"], z, rs, V), 0)
+    assert np.max(np.abs(t0 - scatter)) < 1e-12
+    t1 = np.concatenate(O.tied_embed_grad(c["ids"], np.zeros_like(c["dEmb"]), c["X"], dLs, rs, V), 0)
+    ref = F.linear(torch.tensor(c["dL"].T.copy()), torch.tensor(c["X"].T.copy())).numpy()
+    assert np.max(np.abs(t1 - ref)) < 1e-12
+    rows = [0, 5, 9, 22]
+    tr = O.tied_embed_grad_rows(c["ids"], c["dEmb"], c["X"], c["dL"], rows)
+    assert np.max(np.abs(tr - tg[rows])) < 1e-12
+
+
+def test_embed_sort_brute_force():
+    c = tied_case(12, V=17, T=60)
+    offs, perm = O.embed_sort(c["ids"], c["V"])
+    for v in range(c["V"]):
+        seg = perm[offs[v]:offs[v + 1]].tolist()
+        assert seg == [t for t in range(len(c["ids"])) if c["ids"][t] == v]
+    assert offs[-1] == np.sum((c["ids"] >= 0) & (c["ids"] < c["V"]))
+
+
+# ----------------------------------------------------------------------------
+# Closed forms
+# ----------------------------------------------------------------------------
+def test_param_count_page_value():
+    gd = golden("param_count.json")
+    total = O.param_count(gd["H"], gd["L"], gd["V"])
+    assert total == gd["total"]
+    body = (12 * gd["H"] ** 2 + 4 * gd["H"]) * gd["L"]
+    assert round(body / 1e9, 1) == gd["body_approx_billions"]
+
+
+# ----------------------------------------------------------------------------
+# Planted mistakes: each pin must catch a plausible error in the oracle
+# ----------------------------------------------------------------------------
+def _tanh_gelu(z):
+    z = np.asarray(z, dtype=np.float64)
+    return 0.5 * z * (1 + np.tanh(math.sqrt(2 / math.pi) * (z + 0.044715 * z ** 3)))
+
+
+def test_planted_tanh_gelu_is_caught(monkeypatch):
+    monkeypatch.setattr(O, "gelu", _tanh_gelu)
+    assert check_gelu(O) > 1e-6
+
+
+def test_planted_gelu_prime_dropped_term_is_caught(monkeypatch):
+    monkeypatch.setattr(O, "gelu_prime", lambda z: 0.5 * (1 + O._erf(np.asarray(z) / math.sqrt(2))))
+    assert check_gelu_prime(O) > 1e-3
+    assert check_mlp_bwd_fd(O) > 1e-3
+
+
+def test_planted_sign_error_in_dx_is_caught(monkeypatch):
+    real = O.mlp_bwd
+
+    def broken(*args, **kw):
+        g = real(*args, **kw)
+        g["dX"] = -g["dX"]
+        return g
+    monkeypatch.setattr(O, "mlp_bwd", broken)
+    assert check_mlp_bwd_fd(O) > 1e-3
+
+
+def test_planted_transposed_operand_is_caught(monkeypatch):
+    def broken_row(Y_shards, U_shards, b=None):
+        out = sum(Yi @ Ui[:, ::-1].T for Yi, Ui in zip(Y_shards, U_shards))
+        return out + b[None, :] if b is not None else out
+    monkeypatch.setattr(O, "row_parallel_fwd", broken_row)
+    assert check_mlp_fwd_unsharded(O) > 1e-3
+
+
+def test_planted_bias_per_shard_is_caught(monkeypatch):
+    def broken_row(Y_shards, U_shards, b=None):
+        out = 0
+        for Yi, Ui in zip(Y_shards, U_shards):
+            out = out + Yi @ Ui.T + (b[None, :] if b is not None else 0)
+        return out
+    monkeypatch.setattr(O, "row_parallel_fwd", broken_row)
+    assert check_mlp_fwd_unsharded(O) > 1e-3
+
+
+def test_planted_unmasked_lookup_is_caught(monkeypatch):
+    def broken_parts(ids, E_shards, range_starts):
+        parts = []
+        for r, Er in enumerate(E_shards):
+            masked, mask = O.vocab_mask(ids, range_starts[r], range_starts[r + 1])
+            parts.append(np.asarray(Er, dtype=np.float64)[masked])  # zeroing dropped
+        return parts
+    monkeypatch.setattr(O, "vocab_parallel_embed_partials", broken_parts)
+    assert not check_vocab300(O)
+
+
+def test_planted_scatter_off_by_one_is_caught(monkeypatch):
+    def broken(ids, dEmb, V):
+        out = np.zeros((V, dEmb.shape[1]))
+        for t, v in enumerate(ids):
+            if 0 <= v < V - 1:
+                out[v + 1] += dEmb[t]
+        return out
+    monkeypatch.setattr(O, "embed_scatter_grad", broken)
+    assert check_scatter(O) > 1e-3
