@@ -1,0 +1,265 @@
+/*
+ * tp.h -- C ABI of the GB300 (sm_103a) tensor-parallel block library (libtp.so).
+ *
+ * One GPU computes the tensor-parallel transformer block with its N shards laid
+ * out logically in device memory: the column -> GELU -> row MLP, the head-split
+ * attention projections, the vocab-parallel word embedding and the gradient of
+ * the tied input/output embedding.  The all-reduces of the multi-GPU method
+ * become on-chip sums over shards in a fixed shard order.
+ *
+ * Pages cited:
+ *   [Walkthrough] "Megatron" distributed-training walkthrough
+ *                 (formulaic.cloudchewie.com, docs/.../5-megatron)
+ *   [TP notes]    "Megatron tensor / model parallelism" notes
+ *                 (amentiraz.github.io, posts/Megtron张量/模型并行)
+ *   [Core DDP]    megatron.core.distributed overview (zwxr.cn news 246059)
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Matrices are row-major with a row pitch equal to their column count
+ *    unless a pitch argument says otherwise.  M = b*s tokens, h hidden size,
+ *    hp = h' the FFN width, N the number of shards (1 <= N <= 8; vocabulary
+ *    ranges 1 <= N <= 64).
+ *  - "Shard arrays" (const void* const* X_shards) are HOST arrays of N DEVICE
+ *    pointers; shard i is its own contiguous buffer.  Every other pointer is a
+ *    device pointer unless marked (host).
+ *  - dtype TP_BF16: bf16 inputs and activations, fp32 accumulation, fp32 weight
+ *    and embedding gradients.  dtype TP_F32: everything fp32 (fp32 FMA, no
+ *    tensor-core rounding).  Weight-gradient outputs are fp32 in both cases
+ *    (the fp32 main_grad of [Core DDP] §3.2, grad_reduce_in_fp32).
+ *  - bf16 operands of the tensor-core path must start on 16-byte boundaries and
+ *    have row pitches that are multiples of 8 elements (TMA); violations return
+ *    TP_ERR_ALIGN before anything is launched.  M (and T) may be any value >= 0.
+ *  - Ownership: the caller allocates and owns every buffer, including the
+ *    workspace.  The library keeps only a device error word (a static device
+ *    variable) and never frees caller memory.
+ *  - Execution: work is enqueued asynchronously on `stream` (a cudaStream_t
+ *    passed as void*; NULL = legacy default stream).  Argument errors return
+ *    synchronously before any launch.  Device-side errors (a bounded wait that
+ *    expired) are reported by tp_get_status().
+ *  - accumulate: 0 = overwrite the gradient outputs, 1 = add into them.
+ */
+#ifndef TP_H_
+#define TP_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define TP_API __attribute__((visibility("default")))
+#else
+#define TP_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  TP_OK = 0,
+  TP_ERR_INVALID = 1,     /* bad size, null pointer, N out of range, bad vocab ranges */
+  TP_ERR_UNSUPPORTED = 2, /* dtype/op combination not provided */
+  TP_ERR_CUDA = 3,        /* a CUDA runtime/driver call failed */
+  TP_ERR_TIMEOUT = 4,     /* a bounded device wait expired; the kernel exited early */
+  TP_ERR_WORKSPACE = 5,   /* workspace null or smaller than the *_workspace_size query */
+  TP_ERR_ALIGN = 6        /* pointer or pitch violates the 16-byte / 8-element TMA rule */
+} tp_status;
+
+typedef enum { TP_F32 = 0, TP_BF16 = 1 } tp_dtype;
+
+/* ------------------------------------------------------------------------ */
+/* MLP block: ColumnParallelLinear -> GELU -> RowParallelLinear              */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * tp_mlp_fwd -- forward of the tensor-parallel MLP.
+ * [TP notes] §MLP层 (A split by columns, B by rows); [Walkthrough]
+ * §ColumnParallelLinear (f = identity, F.linear(X, W_i, a_i), no gather) and
+ * §RowParallelLinear (F.linear(Y_i, U_i), g = sum over shards, then + b).
+ *   Z[:, i] = X W_i^T + a_i ;  Y = GELU(Z) (erf form) ;  Out = sum_i Y_i U_i^T + b
+ * Arguments:
+ *   X   (M, h)                 input
+ *   W   shard array, W_i (hp/N, h)   column-parallel weight (torch layout)
+ *   a   shard array or NULL, a_i (hp/N)  column bias
+ *   U   shard array, U_i (h, hp/N)   row-parallel weight
+ *   b   (h) or NULL            row bias, added once after the shard sum
+ *   Z, Y (M, hp) out           pre-activation and activation, shard i in
+ *                              columns [i hp/N, (i+1) hp/N); saved for backward
+ *   Out (M, h) out
+ * hp % N == 0 (TP_ERR_INVALID otherwise).
+ */
+TP_API tp_status tp_mlp_fwd(tp_dtype dt, int64_t M, int64_t h, int64_t hp, int N,
+                     const void* X, const void* const* W, const void* const* a,
+                     const void* const* U, const void* b,
+                     void* Z, void* Y, void* Out, void* stream);
+
+/*
+ * tp_mlp_bwd -- backward of the tensor-parallel MLP.
+ * [Walkthrough] §RowParallelLinear (g backward = identity: every shard sees
+ * dOut) and §ColumnParallelLinear (f backward = all-reduce: dX sums shards).
+ *   dZ_i = (dOut U_i) * GELU'(Z_i)      dU_i = dOut^T Y_i    dW_i = dZ_i^T X
+ *   da_i = colsum(dZ_i)   db = colsum(dOut)   dX = sum_i dZ_i W_i
+ * Arguments:
+ *   dOut (M, h), X (M, h), W, U as in tp_mlp_fwd, Z, Y (M, hp) from tp_mlp_fwd
+ *   dZ  (M, hp) out            activation-gradient buffer (bf16/f32 like Z);
+ *                              holds dZ on return
+ *   dX  (M, h) out
+ *   dW  shard array, dW_i (hp/N, h) fp32 out
+ *   da  shard array or NULL, da_i (hp/N) fp32 out
+ *   dU  shard array, dU_i (h, hp/N) fp32 out
+ *   db  (h) fp32 out or NULL
+ *   workspace, ws_bytes        >= tp_mlp_bwd_workspace_size(M, h, hp); may be
+ *                              NULL when da and db are both NULL
+ */
+TP_API tp_status tp_mlp_bwd(tp_dtype dt, int64_t M, int64_t h, int64_t hp, int N,
+                     const void* dOut, const void* X, const void* const* W,
+                     const void* const* U, const void* Z, const void* Y,
+                     void* dZ, void* dX, void* const* dW, void* const* da,
+                     void* const* dU, void* db, int accumulate,
+                     void* workspace, size_t ws_bytes, void* stream);
+
+/* Bytes of device workspace tp_mlp_bwd needs for the bias column sums. */
+TP_API size_t tp_mlp_bwd_workspace_size(int64_t M, int64_t h, int64_t hp);
+
+/* ------------------------------------------------------------------------ */
+/* Head-split attention projections                                          */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * tp_attn_proj_fwd -- QKV projection split by heads, output projection split
+ * by rows with the sum over shards.
+ * [TP notes] §Self-Attention层 (Q, K, V split by columns, one or more heads
+ * per shard, n_heads % N == 0; the output linear split by rows like the MLP's
+ * B); [Walkthrough] §ParallelSelfAttention (QKV outputs not reduced, the output
+ * projection all-reduced).
+ *   QKV[:, i*3h/N : (i+1)*3h/N] = X Wqkv_i^T + bqkv_i       (= [Q_i K_i V_i])
+ *   O = sum_i C_i Wo_i^T + bo,   C_i = C[:, i h/N : (i+1) h/N]
+ * Arguments:
+ *   X (M, h); Wqkv shard array, Wqkv_i (3h/N, h) = rows [Q_i; K_i; V_i];
+ *   bqkv shard array or NULL, (3h/N); C (M, h) attention context;
+ *   Wo shard array, Wo_i (h, h/N); bo (h) or NULL;
+ *   QKV (M, 3h) out (shard-major); O (M, h) out.
+ */
+TP_API tp_status tp_attn_proj_fwd(tp_dtype dt, int64_t M, int64_t h, int n_heads, int N,
+                           const void* X, const void* const* Wqkv, const void* const* bqkv,
+                           const void* C, const void* const* Wo, const void* bo,
+                           void* QKV, void* O, void* stream);
+
+/*
+ * tp_attn_proj_bwd -- backward of tp_attn_proj_fwd ([TP notes] §Self-Attention层:
+ * forward/backward as for the MLP).
+ *   dWqkv_i = dQKV_i^T X   dbqkv_i = colsum(dQKV_i)   dX = sum_i dQKV_i Wqkv_i
+ *   dWo_i = dO^T C_i       dbo = colsum(dO)           dC_i = dO Wo_i
+ * Arguments: dQKV (M, 3h) shard-major as QKV; dO (M, h); X, C (M, h);
+ *   Wqkv, Wo shard arrays; dX (M, h) out; dC (M, h) out;
+ *   dWqkv shard array (3h/N, h) fp32 out; dbqkv shard array (3h/N) fp32 or NULL;
+ *   dWo shard array (h, h/N) fp32 out; dbo (h) fp32 or NULL;
+ *   workspace >= tp_attn_proj_bwd_workspace_size(M, h) (NULL if no bias grads).
+ */
+TP_API tp_status tp_attn_proj_bwd(tp_dtype dt, int64_t M, int64_t h, int n_heads, int N,
+                           const void* dQKV, const void* dO, const void* X, const void* C,
+                           const void* const* Wqkv, const void* const* Wo,
+                           void* dX, void* dC, void* const* dWqkv, void* const* dbqkv,
+                           void* const* dWo, void* dbo, int accumulate,
+                           void* workspace, size_t ws_bytes, void* stream);
+
+TP_API size_t tp_attn_proj_bwd_workspace_size(int64_t M, int64_t h);
+
+/* ------------------------------------------------------------------------ */
+/* Vocab-parallel word embedding and tied output layer                       */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * vocab_parallel_embed -- masked lookup in every vocabulary range plus the
+ * sum over ranges.
+ * [Walkthrough] §VocabParallelEmbedding (mask ids outside [start, end), shift
+ * by start, F.embedding, zero the masked rows, all-reduce); [TP notes]
+ * §输入层Embedding (300-word, two-range example).
+ *   out[t] = sum_r [s_r <= id_t < s_{r+1}] E_r[id_t - s_r]
+ * Exactly one range owns an id in [0, V), so the sum is a select; an id outside
+ * [0, V) gives a zero row (status TP_OK).  Bit-exact copy of the owning row.
+ * Arguments:
+ *   ids (T) int64; E shard array, E_r (s_{r+1} - s_r, h);
+ *   range_starts (host) int64[N+1], range_starts[0] = 0, strictly increasing,
+ *   range_starts[N] = V; out (T, h).
+ */
+TP_API tp_status vocab_parallel_embed(tp_dtype dt, int64_t T, int64_t h, int64_t V, int N,
+                               const int64_t* ids, const void* const* E,
+                               const int64_t* range_starts, void* out, void* stream);
+
+/*
+ * tp_vocab_logits -- logits of the tied output layer per vocabulary range.
+ * [Walkthrough] §_VocabParallelCrossEntropy (the output layer uses WE^T; each
+ * range yields its own column block); [TP notes] §输出层Embedding.
+ *   L_r = X E_r^T      (T, s_{r+1} - s_r), stored with row pitch ld_logits[r]
+ * Arguments: X (T, h); E shard array; range_starts (host) as above;
+ *   logits shard array, L_r with pitch ld_logits[r] (host int64[N],
+ *   >= s_{r+1} - s_r; a multiple of 8 for bf16).
+ */
+TP_API tp_status tp_vocab_logits(tp_dtype dt, int64_t T, int64_t h, int64_t V, int N,
+                          const void* X, const void* const* E, const int64_t* range_starts,
+                          void* const* logits, const int64_t* ld_logits, void* stream);
+
+/*
+ * tied_embed_grad -- gradient of the word embedding shared by the input and
+ * output layers: the sum of both contributions ([TP notes] §输出层Embedding).
+ *   dE[v] = sum_{t : id_t = v} dEmb[t]  +  sum_t dLogits[t, v] X[t, :]
+ * The scatter part is deterministic: tokens are grouped by id with a counting
+ * sort that is stable in token order, and each row sums its tokens in that
+ * order in fp32 before it is added to the GEMM part.
+ * Arguments:
+ *   ids (T) int64 (ids outside [0, V) contribute nothing); dEmb (T, h);
+ *   X (T, h); dLogits shard array, (T, s_{r+1} - s_r) with pitch ld_dlogits[r]
+ *   (host int64[N]), or NULL for the input-side part alone;
+ *   range_starts (host) as above; dE shard array, dE_r (s_{r+1} - s_r, h) fp32 out;
+ *   workspace >= tied_embed_grad_workspace_size(T, V).  On return the
+ *   workspace starts with the grouping: int32 offsets[V + 1] (segment of id v
+ *   is offsets[v] .. offsets[v+1]) followed by int32 perm[T] (token positions
+ *   sorted by (id, position); entries past offsets[V] are unspecified).
+ */
+TP_API tp_status tied_embed_grad(tp_dtype dt, int64_t T, int64_t h, int64_t V, int N,
+                          const int64_t* ids, const void* dEmb, const void* X,
+                          const void* const* dLogits, const int64_t* ld_dlogits,
+                          const int64_t* range_starts, void* const* dE, int accumulate,
+                          void* workspace, size_t ws_bytes, void* stream);
+
+TP_API size_t tied_embed_grad_workspace_size(int64_t T, int64_t V);
+
+/* ------------------------------------------------------------------------ */
+/* Status, profiling and debugging                                           */
+/* ------------------------------------------------------------------------ */
+
+/* Synchronises `stream`, then reads and clears the device error word of the
+ * current device: TP_OK, TP_ERR_TIMEOUT (a bounded wait expired), or
+ * TP_ERR_CUDA (a CUDA error, sticky or not). */
+TP_API tp_status tp_get_status(void* stream);
+
+/* Human-readable name of a status code (static string). */
+TP_API const char* tp_status_string(tp_status s);
+
+/* Number of SMs the persistent kernels size their grids for (current device). */
+TP_API int tp_num_sms(void);
+
+/* Per-kernel timing.  When enabled, every launch the library makes is
+ * bracketed by CUDA events on its stream; tp_profile_read() synchronises
+ * the device and returns, per kernel kind, the launch count and total device
+ * milliseconds since the last reset.  Disabled by default (no events). */
+TP_API void tp_profile_enable(int on);
+TP_API void tp_profile_reset(void);
+/* Fills up to `cap` entries; returns the number of kernel kinds recorded.
+ * names[i] points at a static string. */
+TP_API int tp_profile_read(const char** names, int64_t* launches, double* total_ms, int cap);
+
+/* Fault injection for testing the bounded waits (host-controlled; never
+ * faults the GPU).  kind 1: the TMA producer of the next tensor-core GEMM
+ * launch skips its first stage, so the consumer's bounded wait expires and
+ * the kernel returns early with TP_ERR_TIMEOUT recorded.  kind 0: off.
+ * wait_limit_ms sets the bounded-wait limit (default 1000 ms). */
+TP_API void tp_debug_inject_fault(int kind);
+TP_API void tp_debug_set_wait_limit_ms(int ms);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TP_H_ */

@@ -1,0 +1,316 @@
+"""Python binding of libtp.so, the GB300 tensor-parallel block library.
+
+Argument marshalling only: every function here has the name of a C-ABI entry
+point (include/tp.h), checks that the torch tensors it is given live on the
+GPU and are contiguous, passes their device pointers and the current CUDA
+stream to the library, and raises ``TPError`` on a non-OK status.  No step of
+the computation runs in Python and there is no CPU path: if libtp.so is
+missing or fails to load, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+import torch
+
+__all__ = [
+    "TPError", "lib", "LIB_PATH", "TP_OK", "TP_ERR_INVALID", "TP_ERR_UNSUPPORTED", "TP_ERR_CUDA",
+    "TP_ERR_TIMEOUT", "TP_ERR_WORKSPACE", "TP_ERR_ALIGN", "TP_F32", "TP_BF16",
+    "tp_mlp_fwd", "tp_mlp_bwd", "tp_mlp_bwd_workspace_size", "tp_attn_proj_fwd",
+    "tp_attn_proj_bwd", "tp_attn_proj_bwd_workspace_size", "vocab_parallel_embed",
+    "tp_vocab_logits", "tied_embed_grad", "tied_embed_grad_workspace_size", "tp_get_status",
+    "tp_status_string", "tp_num_sms", "tp_profile_enable", "tp_profile_reset", "tp_profile_read",
+    "tp_debug_inject_fault", "tp_debug_set_wait_limit_ms", "logits_pitch",
+]
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libtp.so")
+
+TP_OK, TP_ERR_INVALID, TP_ERR_UNSUPPORTED, TP_ERR_CUDA, TP_ERR_TIMEOUT, TP_ERR_WORKSPACE, TP_ERR_ALIGN = range(7)
+TP_F32, TP_BF16 = 0, 1
+
+_c_void_p, _i64, _int, _size_t = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
+_PP = ctypes.POINTER(ctypes.c_void_p)
+_PI64 = ctypes.POINTER(ctypes.c_int64)
+
+_SIGNATURES = {
+    "tp_mlp_fwd": (_int, [_int, _i64, _i64, _i64, _int, _c_void_p, _PP, _PP, _PP, _c_void_p,
+                          _c_void_p, _c_void_p, _c_void_p, _c_void_p]),
+    "tp_mlp_bwd": (_int, [_int, _i64, _i64, _i64, _int, _c_void_p, _c_void_p, _PP, _PP, _c_void_p,
+                          _c_void_p, _c_void_p, _c_void_p, _PP, _PP, _PP, _c_void_p, _int,
+                          _c_void_p, _size_t, _c_void_p]),
+    "tp_mlp_bwd_workspace_size": (_size_t, [_i64, _i64, _i64]),
+    "tp_attn_proj_fwd": (_int, [_int, _i64, _i64, _int, _int, _c_void_p, _PP, _PP, _c_void_p, _PP,
+                                _c_void_p, _c_void_p, _c_void_p, _c_void_p]),
+    "tp_attn_proj_bwd": (_int, [_int, _i64, _i64, _int, _int, _c_void_p, _c_void_p, _c_void_p,
+                                _c_void_p, _PP, _PP, _c_void_p, _c_void_p, _PP, _PP, _PP,
+                                _c_void_p, _int, _c_void_p, _size_t, _c_void_p]),
+    "tp_attn_proj_bwd_workspace_size": (_size_t, [_i64, _i64]),
+    "vocab_parallel_embed": (_int, [_int, _i64, _i64, _i64, _int, _c_void_p, _PP, _PI64,
+                                    _c_void_p, _c_void_p]),
+    "tp_vocab_logits": (_int, [_int, _i64, _i64, _i64, _int, _c_void_p, _PP, _PI64, _PP, _PI64,
+                               _c_void_p]),
+    "tied_embed_grad": (_int, [_int, _i64, _i64, _i64, _int, _c_void_p, _c_void_p, _c_void_p, _PP,
+                               _PI64, _PI64, _PP, _int, _c_void_p, _size_t, _c_void_p]),
+    "tied_embed_grad_workspace_size": (_size_t, [_i64, _i64]),
+    "tp_get_status": (_int, [_c_void_p]),
+    "tp_status_string": (ctypes.c_char_p, [_int]),
+    "tp_num_sms": (_int, []),
+    "tp_profile_enable": (None, [_int]),
+    "tp_profile_reset": (None, []),
+    "tp_profile_read": (_int, [ctypes.POINTER(ctypes.c_char_p), _PI64,
+                               ctypes.POINTER(ctypes.c_double), _int]),
+    "tp_debug_inject_fault": (None, [_int]),
+    "tp_debug_set_wait_limit_ms": (None, [_int]),
+}
+
+_LIB: Optional[ctypes.CDLL] = None
+
+
+class TPError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        super().__init__(f"{where}: {_status_name(status)} ({status})")
+        self.status = status
+
+
+def _status_name(s: int) -> str:
+    names = ["TP_OK", "TP_ERR_INVALID", "TP_ERR_UNSUPPORTED", "TP_ERR_CUDA", "TP_ERR_TIMEOUT",
+             "TP_ERR_WORKSPACE", "TP_ERR_ALIGN"]
+    return names[s] if 0 <= s < len(names) else f"status {s}"
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libtp.so (raises if it is missing: there is no fallback)."""
+    global _LIB
+    if _LIB is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"libtp.so not built ({LIB_PATH}); run "
+                              "`python -m megatron_tensor_transformer_tp_gb300.build_lib`")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGNATURES.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _LIB = L
+    return _LIB
+
+
+# ----------------------------------------------------------------------------
+# marshalling helpers
+# ----------------------------------------------------------------------------
+def _check(status: int, where: str):
+    if status != TP_OK:
+        raise TPError(status, where)
+
+
+def _dev(t: Optional[torch.Tensor], name: str) -> Optional[int]:
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (the library has no CPU path)")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def _ptrs(ts: Optional[Sequence[torch.Tensor]], name: str):
+    if ts is None:
+        return None
+    arr = (ctypes.c_void_p * len(ts))(*[_dev(t, f"{name}[{i}]") for i, t in enumerate(ts)])
+    return ctypes.cast(arr, _PP), arr  # keep arr alive with the cast
+
+
+def _pp(x):
+    return None if x is None else x[0]
+
+
+def _i64s(vals):
+    arr = (ctypes.c_int64 * len(vals))(*[int(v) for v in vals])
+    return arr
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _dtype(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return TP_BF16
+    if t.dtype == torch.float32:
+        return TP_F32
+    raise TypeError(f"unsupported dtype {t.dtype} (bf16 or fp32)")
+
+
+def logits_pitch(n_cols: int, dtype: torch.dtype) -> int:
+    """Row pitch (elements) for a logits block of ``n_cols`` columns: a
+    multiple of 16 bytes, as the tensor-core path needs for TMA."""
+    per = 16 // (2 if dtype == torch.bfloat16 else 4)
+    return (n_cols + per - 1) // per * per
+
+
+# ----------------------------------------------------------------------------
+# MLP block
+# ----------------------------------------------------------------------------
+def tp_mlp_fwd(X, W, a, U, b, Z, Y, Out, stream=None):
+    """Z, Y, Out <- column-parallel linear + GELU + row-parallel linear (shard sum)."""
+    M, h = X.shape
+    N = len(W)
+    hp = Z.shape[1]
+    w, u = _ptrs(W, "W"), _ptrs(U, "U")
+    av = _ptrs(a, "a")
+    _check(lib().tp_mlp_fwd(_dtype(X), M, h, hp, N, _dev(X, "X"), w[0], _pp(av), u[0], _dev(b, "b"),
+                            _dev(Z, "Z"), _dev(Y, "Y"), _dev(Out, "Out"), _stream(stream)),
+           "tp_mlp_fwd")
+
+
+def tp_mlp_bwd_workspace_size(M, h, hp) -> int:
+    return int(lib().tp_mlp_bwd_workspace_size(M, h, hp))
+
+
+def tp_mlp_bwd(dOut, X, W, U, Z, Y, dZ, dX, dW, da, dU, db, accumulate=False, workspace=None,
+               stream=None):
+    M, h = X.shape
+    N = len(W)
+    hp = Z.shape[1]
+    w, u, dw, du = _ptrs(W, "W"), _ptrs(U, "U"), _ptrs(dW, "dW"), _ptrs(dU, "dU")
+    dav = _ptrs(da, "da")
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(lib().tp_mlp_bwd(_dtype(X), M, h, hp, N, _dev(dOut, "dOut"), _dev(X, "X"), w[0], u[0],
+                            _dev(Z, "Z"), _dev(Y, "Y"), _dev(dZ, "dZ"), _dev(dX, "dX"), dw[0],
+                            _pp(dav), du[0], _dev(db, "db"), int(bool(accumulate)),
+                            _dev(workspace, "workspace"), ws_bytes, _stream(stream)),
+           "tp_mlp_bwd")
+
+
+# ----------------------------------------------------------------------------
+# Attention projections
+# ----------------------------------------------------------------------------
+def tp_attn_proj_fwd(X, Wqkv, bqkv, C, Wo, bo, QKV, O, n_heads, stream=None):
+    M, h = X.shape
+    N = len(Wqkv)
+    wq, wo = _ptrs(Wqkv, "Wqkv"), _ptrs(Wo, "Wo")
+    bq = _ptrs(bqkv, "bqkv")
+    _check(lib().tp_attn_proj_fwd(_dtype(X), M, h, n_heads, N, _dev(X, "X"), wq[0], _pp(bq),
+                                  _dev(C, "C"), wo[0], _dev(bo, "bo"), _dev(QKV, "QKV"),
+                                  _dev(O, "O"), _stream(stream)),
+           "tp_attn_proj_fwd")
+
+
+def tp_attn_proj_bwd_workspace_size(M, h) -> int:
+    return int(lib().tp_attn_proj_bwd_workspace_size(M, h))
+
+
+def tp_attn_proj_bwd(dQKV, dO, X, C, Wqkv, Wo, dX, dC, dWqkv, dbqkv, dWo, dbo, n_heads,
+                     accumulate=False, workspace=None, stream=None):
+    M, h = X.shape
+    N = len(Wqkv)
+    wq, wo, dwq, dwo = _ptrs(Wqkv, "Wqkv"), _ptrs(Wo, "Wo"), _ptrs(dWqkv, "dWqkv"), _ptrs(dWo, "dWo")
+    dbq = _ptrs(dbqkv, "dbqkv")
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(lib().tp_attn_proj_bwd(_dtype(X), M, h, n_heads, N, _dev(dQKV, "dQKV"), _dev(dO, "dO"),
+                                  _dev(X, "X"), _dev(C, "C"), wq[0], wo[0], _dev(dX, "dX"),
+                                  _dev(dC, "dC"), dwq[0], _pp(dbq), dwo[0], _dev(dbo, "dbo"),
+                                  int(bool(accumulate)), _dev(workspace, "workspace"), ws_bytes,
+                                  _stream(stream)),
+           "tp_attn_proj_bwd")
+
+
+# ----------------------------------------------------------------------------
+# Vocab-parallel embedding, logits, tied gradient
+# ----------------------------------------------------------------------------
+def vocab_parallel_embed(ids, E, range_starts, out, stream=None):
+    T = ids.numel()
+    N = len(E)
+    h = out.shape[1]
+    V = int(range_starts[-1])
+    if ids.dtype != torch.int64:
+        raise TypeError("ids must be int64")
+    e = _ptrs(E, "E")
+    rs = _i64s(range_starts)
+    _check(lib().vocab_parallel_embed(_dtype(out), T, h, V, N, _dev(ids, "ids"), e[0], rs,
+                                      _dev(out, "out"), _stream(stream)),
+           "vocab_parallel_embed")
+
+
+def tp_vocab_logits(X, E, range_starts, logits, stream=None):
+    """logits: per-range tensors (T, pitch_r); columns [0, |r|) are written."""
+    T, h = X.shape
+    N = len(E)
+    V = int(range_starts[-1])
+    e, lg = _ptrs(E, "E"), _ptrs(logits, "logits")
+    rs = _i64s(range_starts)
+    ld = _i64s([t.shape[1] for t in logits])
+    _check(lib().tp_vocab_logits(_dtype(X), T, h, V, N, _dev(X, "X"), e[0], rs, lg[0], ld,
+                                 _stream(stream)),
+           "tp_vocab_logits")
+
+
+def tied_embed_grad_workspace_size(T, V) -> int:
+    return int(lib().tied_embed_grad_workspace_size(T, V))
+
+
+def tied_embed_grad(ids, dEmb, X, dLogits, range_starts, dE, accumulate=False, workspace=None,
+                    stream=None):
+    """dLogits: per-range tensors (T, pitch_r) or None (input-side part only)."""
+    T = ids.numel()
+    N = len(dE)
+    h = dEmb.shape[1]
+    V = int(range_starts[-1])
+    if ids.dtype != torch.int64:
+        raise TypeError("ids must be int64")
+    dl = _ptrs(dLogits, "dLogits")
+    ld = _i64s([t.shape[1] for t in dLogits]) if dLogits is not None else None
+    de = _ptrs(dE, "dE")
+    rs = _i64s(range_starts)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(lib().tied_embed_grad(_dtype(dEmb), T, h, V, N, _dev(ids, "ids"), _dev(dEmb, "dEmb"),
+                                 _dev(X, "X"), _pp(dl), ld, rs, de[0], int(bool(accumulate)),
+                                 _dev(workspace, "workspace"), ws_bytes, _stream(stream)),
+           "tied_embed_grad")
+
+
+# ----------------------------------------------------------------------------
+# status, profiling, debugging
+# ----------------------------------------------------------------------------
+def tp_get_status(stream=None) -> int:
+    return int(lib().tp_get_status(_stream(stream)))
+
+
+def tp_status_string(s: int) -> str:
+    return lib().tp_status_string(s).decode()
+
+
+def tp_num_sms() -> int:
+    return int(lib().tp_num_sms())
+
+
+def tp_profile_enable(on: bool = True):
+    lib().tp_profile_enable(int(bool(on)))
+
+
+def tp_profile_reset():
+    lib().tp_profile_reset()
+
+
+def tp_profile_read(cap: int = 64) -> dict:
+    """{kernel kind: (launches, total device ms)} since the last reset."""
+    names = (ctypes.c_char_p * cap)()
+    launches = (ctypes.c_int64 * cap)()
+    ms = (ctypes.c_double * cap)()
+    n = lib().tp_profile_read(names, launches, ms, cap)
+    return {names[i].decode(): (int(launches[i]), float(ms[i])) for i in range(min(n, cap))}
+
+
+def tp_debug_inject_fault(kind: int):
+    lib().tp_debug_inject_fault(int(kind))
+
+
+def tp_debug_set_wait_limit_ms(ms: int):
+    lib().tp_debug_set_wait_limit_ms(int(ms))

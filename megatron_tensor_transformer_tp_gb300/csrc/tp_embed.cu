@@ -1,0 +1,314 @@
+// HBM-bound kernels of the block: the vocab-parallel embedding gather, the
+// deterministic grouping of tokens by id (counting sort, stable in token
+// order), the input-side embedding gradient as ordered segment sums, and
+// deterministic column sums for bias gradients.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "tp_device.cuh"
+#include "tp_internal.h"
+
+namespace tp {
+namespace {
+
+// ---------------------------------------------------------------------------
+// Vocab-parallel embedding gather ("Megatron" walkthrough, section
+// VocabParallelEmbedding: each range looks up the ids it owns and zeroes the
+// others, then the ranges are summed).  Exactly one range owns an id in
+// [0, V), so the sum over ranges is the owner's row: one 16-byte vectorised,
+// bit-exact copy per row chunk.  One warp per token row.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ const uint8_t* owner_row(const RangeTable& rt, int64_t id,
+                                                    int64_t row_bytes) {
+  if (id < rt.start[0] || id >= rt.start[rt.n]) return nullptr;
+  int lo = 0, hi = rt.n - 1;  // find r with start[r] <= id < start[r+1]
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (rt.start[mid] <= id) lo = mid; else hi = mid - 1;
+  }
+  return static_cast<const uint8_t*>(rt.ptr[lo]) + (id - rt.start[lo]) * row_bytes;
+}
+
+constexpr int GATHER_UNROLL = 4;
+
+__global__ void __launch_bounds__(256) embed_gather_vec16(const int64_t* __restrict__ ids, int64_t T,
+                                                          int64_t row_bytes,
+                                                          const __grid_constant__ RangeTable rt,
+                                                          uint8_t* __restrict__ out) {
+  const int lane = threadIdx.x & 31;
+  const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+  const int64_t nvec = row_bytes >> 4;
+  for (int64_t t = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; t < T;
+       t += nwarps) {
+    const uint8_t* src = owner_row(rt, __ldg(ids + t), row_bytes);
+    const uint4* s4 = reinterpret_cast<const uint4*>(src);
+    uint4* d4 = reinterpret_cast<uint4*>(out + t * row_bytes);
+    for (int64_t i = lane; i < nvec; i += 32 * GATHER_UNROLL) {
+      uint4 v[GATHER_UNROLL];
+#pragma unroll
+      for (int u = 0; u < GATHER_UNROLL; ++u) {
+        const int64_t j = i + 32 * u;
+        v[u] = (src != nullptr && j < nvec) ? __ldg(s4 + j) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int u = 0; u < GATHER_UNROLL; ++u) {
+        const int64_t j = i + 32 * u;
+        if (j < nvec) __stcs(d4 + j, v[u]);
+      }
+    }
+  }
+}
+
+// Byte-granular fallback for rows that are not 16-byte multiples or aligned.
+__global__ void embed_gather_bytes(const int64_t* __restrict__ ids, int64_t T, int64_t row_bytes,
+                                   const __grid_constant__ RangeTable rt, uint8_t* __restrict__ out) {
+  const int lane = threadIdx.x & 31;
+  const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+  for (int64_t t = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; t < T;
+       t += nwarps) {
+    const uint8_t* src = owner_row(rt, ids[t], row_bytes);
+    for (int64_t j = lane; j < row_bytes; j += 32) out[t * row_bytes + j] = src ? src[j] : 0;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Grouping of tokens by id: offsets[V+1] and perm[T] such that the tokens of
+// id v are perm[offsets[v] .. offsets[v+1]) in increasing position.
+// ---------------------------------------------------------------------------
+__global__ void sort_histogram(const int64_t* __restrict__ ids, int64_t T, int64_t V,
+                               int* __restrict__ counts) {
+  for (int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; t < T;
+       t += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t v = ids[t];
+    if (v >= 0 && v < V) atomicAdd(counts + v, 1);
+  }
+}
+
+// Single-CTA exclusive scan of counts[0..V) into offsets[0..V]; counts is
+// reset to zero for reuse as the scatter cursor.
+constexpr int SCAN_THREADS = 1024;
+__global__ void __launch_bounds__(SCAN_THREADS) sort_scan(int* __restrict__ counts, int64_t V,
+                                                          int* __restrict__ offsets) {
+  __shared__ int warp_sums[SCAN_THREADS / 32];
+  const int64_t per = (V + SCAN_THREADS - 1) / SCAN_THREADS;
+  const int64_t b = threadIdx.x * per;
+  const int64_t e = b + per < V ? b + per : V;
+  int local = 0;
+  for (int64_t v = b; v < e; ++v) local += counts[v];
+  // block-wide exclusive scan of `local`
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  int incl = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) warp_sums[w] = incl;
+  __syncthreads();
+  if (w == 0) {
+    int x = warp_sums[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    warp_sums[lane] = x;  // inclusive over warps
+  }
+  __syncthreads();
+  int run = incl - local + (w > 0 ? warp_sums[w - 1] : 0);
+  for (int64_t v = b; v < e; ++v) {
+    offsets[v] = run;
+    run += counts[v];
+    counts[v] = 0;
+  }
+  if (threadIdx.x == SCAN_THREADS - 1) offsets[V] = warp_sums[SCAN_THREADS / 32 - 1];
+}
+
+__global__ void sort_scatter(const int64_t* __restrict__ ids, int64_t T, int64_t V,
+                             const int* __restrict__ offsets, int* __restrict__ cursor,
+                             int* __restrict__ perm) {
+  for (int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; t < T;
+       t += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t v = ids[t];
+    if (v >= 0 && v < V) perm[offsets[v] + atomicAdd(cursor + v, 1)] = static_cast<int>(t);
+  }
+}
+
+// The scatter placed each segment's tokens in arbitrary order; sorting each
+// segment by position makes the result unique (hence deterministic).
+__global__ void sort_segments(const int* __restrict__ offsets, int64_t V, int* __restrict__ perm) {
+  for (int64_t v = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; v < V;
+       v += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int b = offsets[v], e = offsets[v + 1];
+    for (int i = b + 1; i < e; ++i) {
+      const int x = perm[i];
+      int j = i - 1;
+      while (j >= b && perm[j] > x) {
+        perm[j + 1] = perm[j];
+        --j;
+      }
+      perm[j + 1] = x;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Input-side embedding gradient alone (no output-layer term): one warp per
+// vocabulary row; the row's tokens are summed in position order in fp32.
+// ---------------------------------------------------------------------------
+__global__ void segment_sum_rows(const int* __restrict__ offsets, const int* __restrict__ perm,
+                                 int64_t V, const void* __restrict__ dEmb, int in_f32, int64_t h,
+                                 const __grid_constant__ RangeTable dE, int accumulate) {
+  const int lane = threadIdx.x & 31;
+  const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+  for (int64_t v = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; v < V;
+       v += nwarps) {
+    int r = 0;
+    while (v >= dE.start[r + 1]) ++r;
+    float* row = static_cast<float*>(const_cast<void*>(dE.ptr[r])) + (v - dE.start[r]) * h;
+    const int b = offsets[v], e = offsets[v + 1];
+    for (int64_t c = lane; c < h; c += 32) {
+      float s = 0.f;
+      for (int t = b; t < e; ++t) {
+        const int64_t idx = static_cast<int64_t>(perm[t]) * h + c;
+        s += in_f32 ? static_cast<const float*>(dEmb)[idx]
+                    : bf2f(static_cast<const __nv_bfloat16*>(dEmb)[idx]);
+      }
+      row[c] = accumulate ? row[c] + s : s;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Deterministic column sums: partial sums over 256-row chunks in a fixed
+// order, then the chunks summed in order.
+// ---------------------------------------------------------------------------
+constexpr int CS_ROWS = 256;
+constexpr int CS_COLS = 64;
+__global__ void __launch_bounds__(256) colsum_partial(const void* __restrict__ src, int in_f32,
+                                                      int64_t M, int64_t ncols, int64_t ld,
+                                                      float* __restrict__ partial) {
+  __shared__ float red[4][CS_COLS];
+  const int tx = threadIdx.x & 63, ty = threadIdx.x >> 6;
+  const int64_t col = static_cast<int64_t>(blockIdx.x) * CS_COLS + tx;
+  const int64_t r0 = static_cast<int64_t>(blockIdx.y) * CS_ROWS;
+  float s = 0.f;
+  if (col < ncols) {
+    for (int64_t r = r0 + ty; r < r0 + CS_ROWS && r < M; r += 4) {
+      const int64_t idx = r * ld + col;
+      s += in_f32 ? static_cast<const float*>(src)[idx]
+                  : bf2f(static_cast<const __nv_bfloat16*>(src)[idx]);
+    }
+  }
+  red[ty][tx] = s;
+  __syncthreads();
+  if (ty == 0 && col < ncols)
+    partial[static_cast<int64_t>(blockIdx.y) * ncols + col] =
+        ((red[0][tx] + red[1][tx]) + red[2][tx]) + red[3][tx];
+}
+
+__global__ void colsum_final(const float* __restrict__ partial, int64_t chunks, int64_t ncols,
+                             const __grid_constant__ ShardOut out, int accumulate) {
+  for (int64_t c = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; c < ncols;
+       c += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    float s = 0.f;
+    for (int64_t k = 0; k < chunks; ++k) s += partial[k * ncols + c];
+    const int64_t sh = c / out.cols_per_shard;
+    float* o = out.p[sh] + (c - sh * out.cols_per_shard);
+    *o = accumulate ? *o + s : s;
+  }
+}
+
+__global__ void colsum_zero_rows(int64_t ncols, const __grid_constant__ ShardOut out) {
+  for (int64_t c = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; c < ncols;
+       c += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t sh = c / out.cols_per_shard;
+    out.p[sh][c - sh * out.cols_per_shard] = 0.f;
+  }
+}
+
+inline int blocks_for(int64_t n, int threads, int cap = 65535 * 8) {
+  int64_t b = (n + threads - 1) / threads;
+  if (b < 1) b = 1;
+  if (b > cap) b = cap;
+  return static_cast<int>(b);
+}
+
+inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+}  // namespace
+
+cudaError_t launch_embed_gather(const int64_t* ids, int64_t T, int64_t row_bytes,
+                                const RangeTable& rt, void* out, cudaStream_t s) {
+  if (T <= 0 || row_bytes <= 0) return cudaSuccess;
+  bool vec = (row_bytes % 16) == 0 && (reinterpret_cast<uintptr_t>(out) % 16) == 0;
+  for (int r = 0; r < rt.n; ++r) vec = vec && (reinterpret_cast<uintptr_t>(rt.ptr[r]) % 16) == 0;
+  const int blocks = blocks_for(T * 32, 256);
+  if (vec)
+    embed_gather_vec16<<<blocks, 256, 0, s>>>(ids, T, row_bytes, rt, static_cast<uint8_t*>(out));
+  else
+    embed_gather_bytes<<<blocks, 256, 0, s>>>(ids, T, row_bytes, rt, static_cast<uint8_t*>(out));
+  return cudaGetLastError();
+}
+
+size_t sort_workspace_bytes(int64_t T, int64_t V) {
+  return align256(static_cast<size_t>(V + 1) * 4) + align256(static_cast<size_t>(T > 0 ? T : 1) * 4) +
+         align256(static_cast<size_t>(V) * 4);
+}
+
+int* sort_offsets(void* ws) { return static_cast<int*>(ws); }
+int* sort_perm(void* ws, int64_t V) {
+  return reinterpret_cast<int*>(static_cast<uint8_t*>(ws) + align256(static_cast<size_t>(V + 1) * 4));
+}
+static int* sort_counts(void* ws, int64_t T, int64_t V) {
+  return reinterpret_cast<int*>(static_cast<uint8_t*>(ws) + align256(static_cast<size_t>(V + 1) * 4) +
+                                align256(static_cast<size_t>(T > 0 ? T : 1) * 4));
+}
+
+cudaError_t launch_embed_sort(const int64_t* ids, int64_t T, int64_t V, void* ws, cudaStream_t s) {
+  int* offsets = sort_offsets(ws);
+  int* perm = sort_perm(ws, V);
+  int* counts = sort_counts(ws, T, V);
+  cudaError_t e = cudaMemsetAsync(counts, 0, static_cast<size_t>(V) * 4, s);
+  if (e != cudaSuccess) return e;
+  if (T > 0) sort_histogram<<<blocks_for(T, 256), 256, 0, s>>>(ids, T, V, counts);
+  sort_scan<<<1, SCAN_THREADS, 0, s>>>(counts, V, offsets);
+  if (T > 0) {
+    sort_scatter<<<blocks_for(T, 256), 256, 0, s>>>(ids, T, V, offsets, counts, perm);
+    sort_segments<<<blocks_for(V, 256), 256, 0, s>>>(offsets, V, perm);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_segment_sum(const void* ws, int64_t V, int64_t T, const void* dEmb, int in_f32,
+                               int64_t h, const RangeTable& dE, int accumulate, cudaStream_t s) {
+  (void)T;
+  const int* offsets = sort_offsets(const_cast<void*>(ws));
+  const int* perm = sort_perm(const_cast<void*>(ws), V);
+  segment_sum_rows<<<blocks_for(V * 32, 256), 256, 0, s>>>(offsets, perm, V, dEmb, in_f32, h, dE,
+                                                           accumulate);
+  return cudaGetLastError();
+}
+
+size_t colsum_workspace_bytes(int64_t M, int64_t ncols) {
+  const int64_t chunks = (M + CS_ROWS - 1) / CS_ROWS;
+  return align256(static_cast<size_t>(chunks > 0 ? chunks : 1) * ncols * 4);
+}
+
+cudaError_t launch_colsum(const void* src, int in_f32, int64_t M, int64_t ncols, int64_t ld,
+                          const ShardOut& out, int accumulate, void* ws, cudaStream_t s) {
+  if (ncols <= 0) return cudaSuccess;
+  if (M <= 0) {
+    if (!accumulate) colsum_zero_rows<<<blocks_for(ncols, 256), 256, 0, s>>>(ncols, out);
+    return cudaGetLastError();
+  }
+  const int64_t chunks = (M + CS_ROWS - 1) / CS_ROWS;
+  float* partial = static_cast<float*>(ws);
+  dim3 grid(static_cast<unsigned>((ncols + CS_COLS - 1) / CS_COLS), static_cast<unsigned>(chunks));
+  colsum_partial<<<grid, 256, 0, s>>>(src, in_f32, M, ncols, ld, partial);
+  colsum_final<<<blocks_for(ncols, 256), 256, 0, s>>>(partial, chunks, ncols, out, accumulate);
+  return cudaGetLastError();
+}
+
+}  // namespace tp

@@ -1,0 +1,555 @@
+// Tensor-core GEMM engine for sm_103a: tcgen05.mma with fp32 accumulators in
+// TMEM, operands staged in shared memory by TMA (128-byte swizzle), persistent
+// CTAs, one elected thread issuing the MMAs.
+//
+// One launch computes a list of "groups"; each group is an output matrix
+//     D (M x N) = sum over its segments s of A_s B_s^T
+// followed by a fused epilogue.  The segments of a group are the shards of a
+// tensor-parallel reduction: the row-parallel linear's forward sum over shards
+// (g operator) and the column-parallel linear's backward sum (f operator) run
+// as one fp32 accumulation in TMEM in fixed shard order, so the per-shard
+// partial products never reach HBM ("Megatron" walkthrough, sections
+// ColumnParallelLinear and RowParallelLinear; "Megatron tensor / model
+// parallelism" notes, section MLP层的通讯量分析).
+//
+// CTA layout (192 threads):
+//   warp 0      TMA producer (one lane)
+//   warp 1      TMEM allocator + MMA issuer (one lane)
+//   warps 2..5  epilogue: TMEM -> registers -> fused op -> global
+// Tile 128 x 256 x 64, 4-stage smem ring, two TMEM accumulators (2 x 256
+// columns) so the epilogue of one tile overlaps the main loop of the next.
+// Every wait is bounded: after the limit the thread records a timeout in the
+// device error word, raises a CTA-wide abort flag and the CTA winds down
+// (in-flight copies and MMAs drained, TMEM freed) instead of hanging.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "tp_device.cuh"
+#include "tp_internal.h"
+
+namespace tp {
+namespace {
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 64;
+constexpr int STAGES = 4;
+constexpr int A_TILE_BYTES = BM * BK * 2;  // 16 KB
+constexpr int B_TILE_BYTES = BN * BK * 2;  // 32 KB
+constexpr int STAGE_BYTES = A_TILE_BYTES + B_TILE_BYTES;
+constexpr int TMEM_COLS = 2 * BN;  // two fp32 accumulators
+constexpr int NUM_THREADS = 192;
+constexpr int MN_BOX_BYTES = 64 * BK * 2;  // one 64(MN) x 64(K) box: 8 KB
+constexpr int BAR_BYTES = 256;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + BAR_BYTES + 1024;  // + alignment slack
+
+// ---------------------------------------------------------------------------
+// PTX wrappers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+struct WaitCtx {
+  volatile int* abort_flag;
+  unsigned* err;
+  unsigned long long limit_ns;
+};
+
+// Bounded wait on an mbarrier phase.  Returns false on abort or timeout.
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const WaitCtx& w) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = global_ns();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*w.abort_flag) return false;
+    if (global_ns() - t0 > w.limit_ns) {
+      *w.abort_flag = 1;
+      atomicOr(w.err, kErrTimeout);
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int c0, int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1)
+      : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor (tcgen05 format): start address, leading and
+// stride byte offsets (16-byte units), version 1 at bit 46, 128-byte swizzle.
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(2) << 61;  // SWIZZLE_128B
+  return d;
+}
+
+// Instruction descriptor of tcgen05.mma kind::f16: D f32, A and B bf16,
+// transpose bits select MN-major operands, N >> 3 at bit 17, M >> 4 at bit 24.
+__device__ __forceinline__ uint32_t idesc_bf16(int a_mn, int b_mn) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(a_mn) << 15) |
+         (static_cast<uint32_t>(b_mn) << 16) | (static_cast<uint32_t>(BN >> 3) << 17) |
+         (static_cast<uint32_t>(BM >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
+// Tile decode (identical sequence for all three roles)
+// ---------------------------------------------------------------------------
+struct TileCoord {
+  int g, m0, n0;
+};
+
+__device__ __forceinline__ TileCoord decode_tile(const TcGemmParams& p, int tile) {
+  int g = 0;
+  while (g + 1 < p.num_groups && tile >= p.grp[g + 1].tile_begin) ++g;
+  const GemmGroup& G = p.grp[g];
+  const int local = tile - G.tile_begin;
+  TileCoord c;
+  c.g = g;
+  c.m0 = (local % G.tiles_m) * BM;
+  c.n0 = (local / G.tiles_m) * BN;
+  return c;
+}
+
+// ---------------------------------------------------------------------------
+// Epilogue of one 32-column chunk of one row
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void store_chunk(void* base, int out_type, int64_t ld, int row, int n,
+                                            const float* v, int ncols, bool vec) {
+  if (out_type == OUT_BF16) {
+    __nv_bfloat16* o = static_cast<__nv_bfloat16*>(base) + static_cast<int64_t>(row) * ld + n;
+    if (vec) {
+      uint4* o4 = reinterpret_cast<uint4*>(o);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        uint4 w;
+        w.x = pack_bf16x2(v[8 * q + 0], v[8 * q + 1]);
+        w.y = pack_bf16x2(v[8 * q + 2], v[8 * q + 3]);
+        w.z = pack_bf16x2(v[8 * q + 4], v[8 * q + 5]);
+        w.w = pack_bf16x2(v[8 * q + 6], v[8 * q + 7]);
+        o4[q] = w;
+      }
+    } else {
+      _Pragma("unroll") for (int j = 0; j < 32; ++j) if (j < ncols) o[j] = __float2bfloat16_rn(v[j]);
+    }
+  } else {
+    float* o = static_cast<float*>(base) + static_cast<int64_t>(row) * ld + n;
+    if (vec) {
+      float4* o4 = reinterpret_cast<float4*>(o);
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        o4[q] = make_float4(v[4 * q + 0], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+    } else {
+      _Pragma("unroll") for (int j = 0; j < 32; ++j) if (j < ncols) o[j] = v[j];
+    }
+  }
+}
+
+__device__ __forceinline__ void load_bf16_chunk(const __nv_bfloat16* src, float* v, int ncols,
+                                                bool vec) {
+  if (vec) {
+    const uint4* s4 = reinterpret_cast<const uint4*>(src);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint4 w = __ldg(s4 + q);
+      unpack_bf16x2(w.x, v[8 * q + 0], v[8 * q + 1]);
+      unpack_bf16x2(w.y, v[8 * q + 2], v[8 * q + 3]);
+      unpack_bf16x2(w.z, v[8 * q + 4], v[8 * q + 5]);
+      unpack_bf16x2(w.w, v[8 * q + 6], v[8 * q + 7]);
+    }
+  } else {
+    _Pragma("unroll") for (int j = 0; j < 32; ++j) v[j] = j < ncols ? bf2f(src[j]) : 0.f;
+  }
+}
+
+__device__ __forceinline__ void epilogue_chunk(const GemmGroup& G, int row, int n, float* v) {
+  if (row >= G.M) return;
+  const int ncols = min(32, G.N - n);
+  const bool vec = (ncols == 32) && G.vec_ok;
+  switch (G.epi) {
+    case EPI_STORE:
+    case EPI_BIAS_GELU: {
+      if (G.bias != nullptr) {
+        const __nv_bfloat16* b = static_cast<const __nv_bfloat16*>(G.bias) + n;
+        _Pragma("unroll") for (int j = 0; j < 32; ++j) if (j < ncols) v[j] += bf2f(b[j]);
+      }
+      store_chunk(G.out, G.out_type, G.ldo, row, n, v, ncols, vec);
+      if (G.epi == EPI_BIAS_GELU) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = gelu_f(v[j]);
+        store_chunk(G.out2, G.out_type, G.ldo, row, n, v, ncols, vec);
+      }
+      break;
+    }
+    case EPI_DGELU: {
+      float z[32];
+      const __nv_bfloat16* zp =
+          static_cast<const __nv_bfloat16*>(G.aux) + static_cast<int64_t>(row) * G.ld_aux + n;
+      load_bf16_chunk(zp, z, ncols, vec);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) v[j] *= gelu_grad_f(z[j]);
+      store_chunk(G.out, G.out_type, G.ldo, row, n, v, ncols, vec);
+      break;
+    }
+    case EPI_F32:
+    case EPI_SEGSUM: {
+      if (G.epi == EPI_SEGSUM) {
+        const int64_t id = G.seg_row0 + row;
+        const int b = G.seg_offsets[id], e = G.seg_offsets[id + 1];
+        if (b < e) {
+          float s[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) s[j] = 0.f;
+          for (int t = b; t < e; ++t) {
+            float x[32];
+            const __nv_bfloat16* src = static_cast<const __nv_bfloat16*>(G.seg_src) +
+                                       static_cast<int64_t>(G.seg_perm[t]) * G.ld_seg + n;
+            load_bf16_chunk(src, x, ncols, vec);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) s[j] += x[j];
+          }
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] += s[j];
+        }
+      }
+      float* o = static_cast<float*>(G.out) + static_cast<int64_t>(row) * G.ldo + n;
+      if (G.accumulate) {
+        if (vec) {
+          const float4* o4 = reinterpret_cast<const float4*>(o);
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const float4 w = o4[q];
+            v[4 * q + 0] += w.x;
+            v[4 * q + 1] += w.y;
+            v[4 * q + 2] += w.z;
+            v[4 * q + 3] += w.w;
+          }
+        } else {
+          _Pragma("unroll") for (int j = 0; j < 32; ++j) if (j < ncols) v[j] += o[j];
+        }
+      }
+      store_chunk(G.out, OUT_F32, G.ldo, row, n, v, ncols, vec);
+      break;
+    }
+    default:
+      break;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// The kernel
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_constant__ TcGemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  // bars: full[0..3], empty[4..7], tfull[8..9], tempty[10..11], drain[12]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 17);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t bar0 = smem_addr(bars);
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+  auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
+  auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(tfull_bar(b), 1);
+      mbar_init(tempty_bar(b), 128);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_addr(tmem_slot)),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const WaitCtx wctx{abort_flag, p.err, p.wait_limit_ns};
+  const uint32_t tiles_base = smem_addr(smem);
+
+  if (warp == 0 && lane == 0) {
+    // ------------------------------ TMA producer ------------------------------
+    for (int s = 0; s < p.num_segs; ++s) {
+      prefetch_tmap(&p.mapA[s]);
+      prefetch_tmap(&p.mapB[s]);
+    }
+    int stage = 0;
+    uint32_t phase = 0;
+    int pending_phase[STAGES];
+    for (int s = 0; s < STAGES; ++s) pending_phase[s] = -1;
+    bool first = true;
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < p.total_tiles; tile += gridDim.x) {
+      const TileCoord tc = decode_tile(p, tile);
+      const GemmGroup& G = p.grp[tc.g];
+      for (int s = G.seg_begin; ok && s < G.seg_end; ++s) {
+        const TcSeg& S = p.seg[s];
+        const int nk = (S.K + BK - 1) / BK;
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!wait_bounded(empty_bar(stage), phase ^ 1u, wctx)) {
+            ok = false;
+            break;
+          }
+          const uint32_t a_dst = tiles_base + stage * STAGE_BYTES;
+          const uint32_t b_dst = a_dst + A_TILE_BYTES;
+          if (first && p.fault_skip) {
+            // Injected fault: this stage is never filled, so the consumer's
+            // bounded wait on it expires.
+          } else {
+            mbar_arrive_expect_tx(full_bar(stage), STAGE_BYTES);
+            pending_phase[stage] = static_cast<int>(phase);
+            const int k0 = kb * BK;
+            if (S.a_mn) {
+              tma_load_2d(a_dst, &p.mapA[s], full_bar(stage), tc.m0, k0);
+              tma_load_2d(a_dst + MN_BOX_BYTES, &p.mapA[s], full_bar(stage), tc.m0 + 64, k0);
+            } else {
+              tma_load_2d(a_dst, &p.mapA[s], full_bar(stage), k0, tc.m0);
+            }
+            if (S.b_mn) {
+#pragma unroll
+              for (int j = 0; j < BN / 64; ++j)
+                tma_load_2d(b_dst + j * MN_BOX_BYTES, &p.mapB[s], full_bar(stage), tc.n0 + 64 * j,
+                            k0);
+            } else {
+              tma_load_2d(b_dst, &p.mapB[s], full_bar(stage), k0, tc.n0);
+            }
+          }
+          first = false;
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+    }
+    if (*abort_flag) {
+      // Drain: wait (bounded) until every copy this thread issued has landed.
+      WaitCtx drain_ctx{abort_flag, p.err, p.wait_limit_ns};
+      for (int s = 0; s < STAGES; ++s) {
+        if (pending_phase[s] < 0) continue;
+        const unsigned long long t0 = global_ns();
+        while (!mbar_try_wait(full_bar(s), static_cast<uint32_t>(pending_phase[s]))) {
+          if (global_ns() - t0 > drain_ctx.limit_ns) break;
+        }
+      }
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ------------------------------- MMA issuer -------------------------------
+    int stage = 0;
+    uint32_t phase = 0;
+    int lt = 0;
+    bool ok = true;
+    bool issued_any = false;
+    for (int tile = blockIdx.x; ok && tile < p.total_tiles; tile += gridDim.x, ++lt) {
+      const TileCoord tc = decode_tile(p, tile);
+      const GemmGroup& G = p.grp[tc.g];
+      const int buf = lt & 1;
+      const uint32_t tphase = static_cast<uint32_t>(lt >> 1) & 1u;
+      if (!wait_bounded(tempty_bar(buf), tphase ^ 1u, wctx)) break;
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
+      uint32_t acc = 0;
+      for (int s = G.seg_begin; ok && s < G.seg_end; ++s) {
+        const TcSeg& S = p.seg[s];
+        const int nk = (S.K + BK - 1) / BK;
+        const uint32_t idesc = idesc_bf16(S.a_mn, S.b_mn);
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!wait_bounded(full_bar(stage), phase, wctx)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_base = tiles_base + stage * STAGE_BYTES;
+          const uint32_t b_base = a_base + A_TILE_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            // K-major: 16 K elements = 32 bytes along the swizzled row.
+            // MN-major: 16 K rows = 2 swizzle atoms of 8 rows x 128 bytes.
+            const uint64_t ad = S.a_mn ? sdesc(a_base + kk * 2048, MN_BOX_BYTES, 1024)
+                                       : sdesc(a_base + kk * 32, 16, 1024);
+            const uint64_t bd = S.b_mn ? sdesc(b_base + kk * 2048, MN_BOX_BYTES, 1024)
+                                       : sdesc(b_base + kk * 32, 16, 1024);
+            mma_bf16(d_tmem, ad, bd, idesc, acc);
+            acc = 1;
+          }
+          issued_any = true;
+          mma_commit(empty_bar(stage));
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) break;
+      mma_commit(tfull_bar(buf));
+    }
+    if (*abort_flag && issued_any) {
+      // Drain: the commit arrives once every MMA issued so far has completed.
+      mma_commit(drain_bar);
+      const unsigned long long t0 = global_ns();
+      while (!mbar_try_wait(drain_bar, 0)) {
+        if (global_ns() - t0 > p.wait_limit_ns) break;
+      }
+    }
+  } else if (warp >= 2) {
+    // -------------------------------- Epilogue --------------------------------
+    const int quarter = warp & 3;  // TMEM lanes this warp may access
+    int lt = 0;
+    for (int tile = blockIdx.x; tile < p.total_tiles; tile += gridDim.x, ++lt) {
+      const TileCoord tc = decode_tile(p, tile);
+      const GemmGroup& G = p.grp[tc.g];
+      const int buf = lt & 1;
+      const uint32_t tphase = static_cast<uint32_t>(lt >> 1) & 1u;
+      if (!wait_bounded(tfull_bar(buf), tphase, wctx)) break;
+      tc_fence_after();
+      const int row = tc.m0 + quarter * 32 + lane;
+      const uint32_t taddr =
+          tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(buf * BN);
+      for (int c = 0; c < BN / 32; ++c) {
+        const int n = tc.n0 + c * 32;
+        if (n >= G.N) break;  // warp-uniform
+        uint32_t r[32];
+        float v[32];
+        if (G.k_empty) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] = 0.f;
+        } else {
+          tmem_ld32(taddr + static_cast<uint32_t>(c * 32), r);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+        }
+        epilogue_chunk(G, row, n, v);
+      }
+      tc_fence_before();
+      mbar_arrive(tempty_bar(buf));
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                 "r"(TMEM_COLS)
+                 : "memory");
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_tc_gemm(const TcGemmParams& p, int num_sms, cudaStream_t s) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e =
+        cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  if (p.total_tiles <= 0) return cudaSuccess;
+  const int grid = p.total_tiles < num_sms ? p.total_tiles : num_sms;
+  tc_gemm_kernel<<<grid, NUM_THREADS, SMEM_BYTES, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace tp

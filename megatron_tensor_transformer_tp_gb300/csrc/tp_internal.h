@@ -1,0 +1,116 @@
+// Internal declarations shared by the library's translation units (not part of the ABI).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace tp {
+
+constexpr int kMaxGroups = 32;    // independent output matrices in one GEMM launch
+constexpr int kMaxSegs = 32;      // (A, B) operand pairs summed into the outputs
+constexpr int kMaxRanges = 64;    // vocabulary ranges
+
+// Error bits of the device error word.
+constexpr unsigned kErrTimeout = 1u;
+
+// Epilogue kinds of the GEMM engines.
+enum Epi : int {
+  EPI_STORE = 0,      // out = acc (+ bias[n]); bf16 or f32
+  EPI_BIAS_GELU = 1,  // z = acc + bias[n]; out = z, out2 = GELU(z)
+  EPI_DGELU = 2,      // out = acc * GELU'(aux[m, n])
+  EPI_F32 = 3,        // out (f32) = acc (+ out if accumulate)
+  EPI_SEGSUM = 4      // out (f32) = acc + sum_{j in seg(row)} seg_src[perm[j], n] (+ out)
+};
+
+enum OutType : int { OUT_BF16 = 0, OUT_F32 = 1 };
+
+// One output matrix D (M x N) = sum over its segments of A_s B_s^T.
+struct GemmGroup {
+  int M, N;
+  int seg_begin, seg_end;
+  int epi, out_type, accumulate, vec_ok;
+  int tiles_m, tiles_n, tile_begin, k_empty;  // k_empty: no k-blocks, D = 0
+  void* out;            // D, row pitch ldo (elements)
+  void* out2;           // second output (GELU: Y), same pitch as out
+  const void* aux;      // DGELU: Z, row pitch ld_aux
+  const void* bias;     // column bias (length N) or null; same dtype as inputs
+  int64_t ldo, ld_aux;
+  // EPI_SEGSUM: row r of D is vocabulary id seg_row0 + r; its tokens are
+  // perm[offsets[id] .. offsets[id+1]); seg_src rows have pitch ld_seg.
+  const int* seg_offsets;
+  const int* seg_perm;
+  const void* seg_src;
+  int64_t ld_seg;
+  int64_t seg_row0;
+};
+
+// One operand pair of the tensor-core engine.  Operands are bf16.
+// A "K-major" operand is stored (rows = M or N, cols = K); "MN-major" is
+// stored (rows = K, cols = M or N).
+struct TcSeg {
+  int K;
+  int a_mn, b_mn;
+  int pad;
+};
+
+struct TcGemmParams {
+  CUtensorMap mapA[kMaxSegs];
+  CUtensorMap mapB[kMaxSegs];
+  TcSeg seg[kMaxSegs];
+  GemmGroup grp[kMaxGroups];
+  int num_groups, num_segs, total_tiles;
+  int fault_skip;        // fault injection: producer skips its first stage
+  unsigned* err;         // device error word
+  unsigned long long wait_limit_ns;
+  int pad;
+};
+
+// One operand pair of the fp32 SIMT engine: element (m, k) of A at
+// A[m*sam + k*sak], element (n, k) of B at B[n*sbn + k*sbk].
+struct SimtSeg {
+  const float* A;
+  const float* B;
+  int64_t sam, sak, sbn, sbk;
+  int K, pad;
+};
+
+struct SimtGemmParams {
+  SimtSeg seg[kMaxSegs];
+  GemmGroup grp[kMaxGroups];
+  int num_groups, num_segs, total_tiles, pad;
+};
+
+// Vocabulary range table.
+struct RangeTable {
+  int64_t start[kMaxRanges + 1];
+  const void* ptr[kMaxRanges];
+  int n;
+};
+
+// Shard pointer table for per-shard fp32 outputs of column sums.
+struct ShardOut {
+  float* p[kMaxGroups];
+  int64_t cols_per_shard;
+  int n;
+};
+
+// Launchers (each returns the launch error).
+cudaError_t launch_tc_gemm(const TcGemmParams& p, int num_sms, cudaStream_t s);
+cudaError_t launch_simt_gemm(const SimtGemmParams& p, cudaStream_t s);
+cudaError_t launch_embed_gather(const int64_t* ids, int64_t T, int64_t row_bytes,
+                                const RangeTable& rt, void* out, cudaStream_t s);
+// Grouping of tokens by id.  ws holds offsets[V+1], perm[T], counts[V].
+size_t sort_workspace_bytes(int64_t T, int64_t V);
+cudaError_t launch_embed_sort(const int64_t* ids, int64_t T, int64_t V, void* ws, cudaStream_t s);
+int* sort_offsets(void* ws);
+int* sort_perm(void* ws, int64_t V);
+// Input-side embedding gradient alone: dE_r rows = segment sums (+ old).
+cudaError_t launch_segment_sum(const void* ws, int64_t V, int64_t T, const void* dEmb, int in_f32,
+                               int64_t h, const RangeTable& dE, int accumulate, cudaStream_t s);
+// Deterministic column sums of src (M x ncols, pitch ld) into per-shard fp32 outputs.
+size_t colsum_workspace_bytes(int64_t M, int64_t ncols);
+cudaError_t launch_colsum(const void* src, int in_f32, int64_t M, int64_t ncols, int64_t ld,
+                          const ShardOut& out, int accumulate, void* ws, cudaStream_t s);
+
+}  // namespace tp

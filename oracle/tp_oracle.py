@@ -234,6 +234,23 @@ def attn_proj_bwd(dQKV, dO, X, C, Wqkv_shards, Wo_shards):
                 dC=np.concatenate(dC, axis=1))
 
 
+def attn_proj_bwd_weight_rows(dQKV, dO, X, C, N, qkv_rows, o_rows):
+    """Rows of the weight gradients of ``attn_proj_bwd`` (same definitions,
+    evaluated only where asked, for full-size workloads):
+    dWqkv_i[j] = dQKV_i[:, j]^T X for j in qkv_rows[i];
+    dWo_i[k]   = dO[:, k]^T C_i   for k in o_rows[i];
+    and the bias gradients in full (column sums of dQKV_i and of dO)."""
+    w = dQKV.shape[1] // N
+    d = C.shape[1] // N
+    dWqkv, dWo, dbqkv = [], [], []
+    for i in range(N):
+        g = dQKV[:, i * w:(i + 1) * w]
+        dWqkv.append(g[:, qkv_rows[i]].T @ X)
+        dWo.append(dO[:, o_rows[i]].T @ C[:, i * d:(i + 1) * d])
+        dbqkv.append(g.sum(axis=0))
+    return dWqkv, dWo, dbqkv, dO.sum(axis=0)
+
+
 # --------------------------------------------------------------------------
 # Vocab-parallel embedding
 # --------------------------------------------------------------------------
@@ -259,7 +276,7 @@ def vocab_parallel_embed_partials(ids, E_shards, range_starts):
     parts = []
     for r, Er in enumerate(E_shards):
         masked, mask = vocab_mask(ids, range_starts[r], range_starts[r + 1])
-        out = np.asarray(Er, dtype=np.float64)[masked]
+        out = np.asarray(Er)[masked].astype(np.float64)
         out[mask, :] = 0.0
         parts.append(out)
     return parts
