@@ -1,0 +1,646 @@
+"""Benchmark of the tensor-parallel block on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--no-rows]
+
+Prints ONE JSON line (rank 0).  The headline step is one forward + backward of
+the tensor-parallel MLP block (tp_mlp_fwd + tp_mlp_bwd) on the workload
+b=4, s=1024, h=1024, h'=4096, N=4 shards, bf16 with fp32 accumulation; the
+metric is its throughput in TFLOP/s (12*M*h*h' algorithmic FLOPs per step).
+Inputs are synthetic and seeded (synthetic_inputs.py) and resident in HBM when
+the timed region starts; L2 is flushed (a 256 MiB write) before every timed
+step and the flush is outside the per-step events.
+
+The same line carries: the roofline of the dominant kernel (per-launch CUDA
+events taken by the library on the launching stream during the timed region),
+the end-to-end number through the C ABI with host buffers (pinned host->device
+copies of the step's inputs and device->host reads of its outputs inside the
+timed region), the clocks sampled by nvidia-smi during the timed region, the
+other rows of the block (embedding gather GB/s, attention projections, the
+model-width MLP, logits, tied gradient), and the fp64 CPU oracle timed on a
+bounded sample as a reported baseline.
+
+Multi-GPU: the block runs on one GPU; under torchrun every rank runs an
+independent replica (no collective on the data path) and the line reports the
+units all ranks processed over the slowest rank's time ("scaling": "weak").
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import synthetic_inputs as SI  # noqa: E402
+
+METRIC = "TP-MLP fwd+bwd TFLOP/s (% BF16 peak); embed gather GB/s (% HBM)"
+DEFAULT_WORKLOAD = "mlp_b4_s1024_h1024_hp4096_N4"
+L2_FLUSH_BYTES = 256 << 20
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ----------------------------------------------------------------------------
+# distributed plumbing (replicas only)
+# ----------------------------------------------------------------------------
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def dist_init(backend):
+    import torch.distributed as dist
+    ws, rank, _ = dist_env()
+    if ws > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend=backend, rank=rank, world_size=ws)
+    return ws, rank
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+def reduce_max(x: float, device=None) -> float:
+    """Max over ranks (identity on one rank)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def reduce_sum(x: float, device=None) -> float:
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def aggregate_throughput(units_per_rank_sum: float, max_seconds: float) -> float:
+    """Whole-job throughput: units all ranks processed / slowest rank's time."""
+    return units_per_rank_sum / max_seconds if max_seconds > 0 else float("nan")
+
+
+# ----------------------------------------------------------------------------
+# measurement helpers
+# ----------------------------------------------------------------------------
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "megatron_tensor_transformer_tp_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def load_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, or
+    None when absent or taken on a different kernel source."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    if d.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    rec = d.get("kernels", {}).get(f"{workload}/{kernel}")
+    return None if rec is None else rec.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, period_ms: int = 100):
+        self.gpu = gpu_index
+        self.period = period_ms
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", f"-lms={self.period}"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, smax, reasons, power = [], None, set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm),
+                "power_w_max": max(power) if power else None}
+
+
+# ----------------------------------------------------------------------------
+# workloads: device state, one step, algorithmic work
+# ----------------------------------------------------------------------------
+class MLPBench:
+    kind = "mlp"
+
+    def __init__(self, name, tp, torch):
+        self.name, self.tp, self.torch = name, tp, torch
+        cfg = SI.WORKLOADS[name]
+        inp = SI.mlp_inputs(cfg)
+        d = lambda t: t.cuda().contiguous()
+        M, h, hp, N = inp["M"], inp["h"], inp["hp"], inp["N"]
+        self.M, self.h, self.hp, self.N = M, h, hp, N
+        bf, f = torch.bfloat16, torch.float32
+        self.X, self.dOut = d(inp["X"]), d(inp["dOut"])
+        self.W = [d(t) for t in inp["W_shards"]]
+        self.U = [d(t) for t in inp["U_shards"]]
+        self.a = [d(t) for t in inp["a_shards"]]
+        self.b = d(inp["b"])
+        self.Z = torch.empty(M, hp, dtype=bf, device="cuda")
+        self.Y = torch.empty_like(self.Z)
+        self.Out = torch.empty(M, h, dtype=bf, device="cuda")
+        self.dZ = torch.empty_like(self.Z)
+        self.dX = torch.empty(M, h, dtype=bf, device="cuda")
+        self.dW = [torch.empty(hp // N, h, dtype=f, device="cuda") for _ in range(N)]
+        self.dU = [torch.empty(h, hp // N, dtype=f, device="cuda") for _ in range(N)]
+        self.da = [torch.empty(hp // N, dtype=f, device="cuda") for _ in range(N)]
+        self.db = torch.empty(h, dtype=f, device="cuda")
+        self.ws = torch.empty(tp.tp_mlp_bwd_workspace_size(M, h, hp), dtype=torch.uint8, device="cuda")
+        # pinned host buffers for the end-to-end path
+        self.hX = inp["X"].pin_memory()
+        self.hdOut = inp["dOut"].pin_memory()
+        self.hOut = torch.empty(M, h, dtype=bf).pin_memory()
+        self.hdX = torch.empty(M, h, dtype=bf).pin_memory()
+
+    def step(self):
+        tp = self.tp
+        tp.tp_mlp_fwd(self.X, self.W, self.a, self.U, self.b, self.Z, self.Y, self.Out)
+        tp.tp_mlp_bwd(self.dOut, self.X, self.W, self.U, self.Z, self.Y, self.dZ, self.dX, self.dW,
+                      self.da, self.dU, self.db, workspace=self.ws)
+
+    def e2e_step(self):
+        self.X.copy_(self.hX, non_blocking=True)
+        self.dOut.copy_(self.hdOut, non_blocking=True)
+        self.step()
+        self.hOut.copy_(self.Out, non_blocking=True)
+        self.hdX.copy_(self.dX, non_blocking=True)
+
+    def e2e_bytes(self):
+        b = lambda t: t.numel() * t.element_size()
+        return b(self.hX) + b(self.hdOut), b(self.hOut) + b(self.hdX)
+
+    def units(self):
+        return 12.0 * self.M * self.h * self.hp, "TFLOP/s", 1e12
+
+    def kernel_work(self):
+        f = 2.0 * self.M * self.h * self.hp
+        return {"gemm_column_gelu": ("tensor", f), "gemm_row_shardsum": ("tensor", f),
+                "gemm_dU_dgelu": ("tensor", 2 * f), "gemm_dX_shardsum_dW": ("tensor", 2 * f),
+                "colsum_da": ("hbm", self.M * self.hp * 2.0), "colsum_db": ("hbm", self.M * self.h * 2.0)}
+
+
+class AttnBench:
+    kind = "attn"
+
+    def __init__(self, name, tp, torch):
+        self.name, self.tp, self.torch = name, tp, torch
+        inp = SI.attn_inputs(SI.WORKLOADS[name])
+        d = lambda t: t.cuda().contiguous()
+        M, h, N = inp["M"], inp["h"], inp["N"]
+        self.M, self.h, self.N, self.nh = M, h, N, inp["n_heads"]
+        bf, f = torch.bfloat16, torch.float32
+        self.X, self.C, self.dQKV, self.dO = d(inp["X"]), d(inp["C"]), d(inp["dQKV"]), d(inp["dO"])
+        self.Wq = [d(t) for t in inp["Wqkv_shards"]]
+        self.Wo = [d(t) for t in inp["Wo_shards"]]
+        self.bq = [d(t) for t in inp["bqkv_shards"]]
+        self.bo = d(inp["bo"])
+        dd = h // N
+        self.QKV = torch.empty(M, 3 * h, dtype=bf, device="cuda")
+        self.O = torch.empty(M, h, dtype=bf, device="cuda")
+        self.dX = torch.empty(M, h, dtype=bf, device="cuda")
+        self.dC = torch.empty(M, h, dtype=bf, device="cuda")
+        self.dWq = [torch.empty(3 * dd, h, dtype=f, device="cuda") for _ in range(N)]
+        self.dWo = [torch.empty(h, dd, dtype=f, device="cuda") for _ in range(N)]
+        self.dbq = [torch.empty(3 * dd, dtype=f, device="cuda") for _ in range(N)]
+        self.dbo = torch.empty(h, dtype=f, device="cuda")
+        self.ws = torch.empty(tp.tp_attn_proj_bwd_workspace_size(M, h), dtype=torch.uint8, device="cuda")
+
+    def step(self):
+        tp = self.tp
+        tp.tp_attn_proj_fwd(self.X, self.Wq, self.bq, self.C, self.Wo, self.bo, self.QKV, self.O, self.nh)
+        tp.tp_attn_proj_bwd(self.dQKV, self.dO, self.X, self.C, self.Wq, self.Wo, self.dX, self.dC,
+                            self.dWq, self.dbq, self.dWo, self.dbo, self.nh, workspace=self.ws)
+
+    def units(self):
+        return 24.0 * self.M * self.h * self.h, "TFLOP/s", 1e12
+
+    def kernel_work(self):
+        f = 8.0 * self.M * self.h * self.h
+        return {"gemm_attn_fwd": ("tensor", f), "gemm_attn_dW": ("tensor", f),
+                "gemm_attn_dX_dC": ("tensor", f), "colsum_dbqkv": ("hbm", self.M * 3 * self.h * 2.0),
+                "colsum_dbo": ("hbm", self.M * self.h * 2.0)}
+
+
+class EmbedBench:
+    """Vocab-parallel lookup, per-range logits and tied gradient."""
+    kind = "embed"
+
+    def __init__(self, name, tp, torch):
+        self.name, self.tp, self.torch = name, tp, torch
+        inp = SI.embed_inputs(SI.WORKLOADS[name])
+        d = lambda t: t.cuda().contiguous()
+        bf = torch.bfloat16
+        self.T, self.V, self.h, self.N, self.rs = inp["T"], inp["V"], inp["h"], inp["N"], inp["ranges"]
+        self.ids = d(inp["ids"])
+        self.unique = int(torch.unique(inp["ids"]).numel())
+        self.E = [d(t) for t in inp["E_shards"]]
+        self.X, self.dEmb = d(inp["X"]), d(inp["dEmb"])
+        self.out = torch.empty(self.T, self.h, dtype=bf, device="cuda")
+        widths = [self.rs[r + 1] - self.rs[r] for r in range(self.N)]
+        self.L = [torch.empty(self.T, tp.logits_pitch(w, bf), dtype=bf, device="cuda") for w in widths]
+        self.dL = []
+        for r, w in enumerate(widths):
+            buf = torch.zeros(self.T, tp.logits_pitch(w, bf), dtype=bf, device="cuda")
+            buf[:, :w] = inp["dLogits_shards"][r].cuda()
+            self.dL.append(buf)
+        self.dE = [torch.empty(w, self.h, dtype=torch.float32, device="cuda") for w in widths]
+        self.ws = torch.empty(tp.tied_embed_grad_workspace_size(self.T, self.V), dtype=torch.uint8,
+                              device="cuda")
+
+    def gather(self):
+        self.tp.vocab_parallel_embed(self.ids, self.E, self.rs, self.out)
+
+    def step(self):
+        tp = self.tp
+        self.gather()
+        tp.tp_vocab_logits(self.X, self.E, self.rs, self.L)
+        tp.tied_embed_grad(self.ids, self.dEmb, self.X, self.dL, self.rs, self.dE, workspace=self.ws)
+
+    def gather_bytes(self):
+        # unique rows read once + every output row written + the ids
+        return self.unique * self.h * 2.0 + self.T * self.h * 2.0 + self.T * 8.0
+
+    def units(self):
+        return 4.0 * self.T * self.V * self.h, "TFLOP/s", 1e12
+
+    def kernel_work(self):
+        f = 2.0 * self.T * self.V * self.h
+        return {"embed_gather": ("hbm", self.gather_bytes()), "gemm_logits": ("tensor", f),
+                "gemm_tied_grad_segsum": ("tensor", f),
+                "embed_sort": ("hbm", self.T * 8.0 + self.T * 4.0 + (self.V + 1) * 4.0)}
+
+
+BENCHES = {"mlp": MLPBench, "attn": AttnBench, "embed": EmbedBench}
+
+
+def time_steps(torch, fn, steps, warmup, flush):
+    """W untimed steps, then K steps each bracketed by CUDA events on the
+    current stream, with an L2 flush before every step outside the events.
+    Returns (per-step ms list, wall seconds of the bracketed loop)."""
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for e0, e1 in ev:
+        flush.fill_(1)
+        e0.record()
+        fn()
+        e1.record()
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    barrier()
+    return [e0.elapsed_time(e1) for e0, e1 in ev], wall
+
+
+def roofline_for(tp, bench, prof, peaks, peak_src, sustained=True):
+    """Dominant kernel (largest total device time) of the profiled region."""
+    work = bench.kernel_work()
+    rows = []
+    for name, (launches, ms) in prof.items():
+        if name not in work or launches == 0:
+            continue
+        bound, per_launch = work[name]
+        avg_s = ms / launches / 1e3
+        rows.append((ms, name, bound, per_launch, avg_s, launches))
+    if not rows:
+        return None, []
+    rows.sort(reverse=True)
+    out = []
+    for ms, name, bound, per_launch, avg_s, launches in rows:
+        if bound == "tensor":
+            ach, unit = per_launch / avg_s / 1e12, "TFLOP/s"
+            peak = peaks["bf16_tflops_sustained" if sustained else "bf16_tflops"]
+        else:
+            ach, unit = per_launch / avg_s / 1e9, "GB/s"
+            peak = peaks["hbm_gbs"]
+        out.append({"kernel": name, "bound": bound, "launches": launches, "avg_us": avg_s * 1e6,
+                    "achieved": ach, "peak": peak, "unit": unit, "frac": ach / peak,
+                    "share": ms / sum(r[0] for r in rows)})
+    top = dict(out[0])
+    top["traffic"] = load_traffic(top["kernel"], bench.name)
+    top["peak_source"] = (f"{peak_src} {'bf16_tflops_sustained' if sustained else 'bf16_tflops'}"
+                          if top["bound"] == "tensor" else f"{peak_src} hbm_gbs")
+    return top, out
+
+
+# ----------------------------------------------------------------------------
+# the oracle as CPU baseline / reference arm
+# ----------------------------------------------------------------------------
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+class OracleMLP:
+    """fp64 oracle forward + backward of the MLP block on the first tokens of a
+    workload (same weights as the GPU arm); inputs widened once."""
+
+    def __init__(self, workload: str, max_tokens: int):
+        import torch
+
+        import oracle.tp_oracle as O
+        self.O = O
+        cfg = SI.WORKLOADS[workload]
+        inp = SI.mlp_inputs(cfg, M=max_tokens)
+        f64 = lambda t: t.to(torch.float64).numpy()
+        self.X, self.dOut = f64(inp["X"]), f64(inp["dOut"])
+        self.W = [f64(t) for t in inp["W_shards"]]
+        self.U = [f64(t) for t in inp["U_shards"]]
+        self.a = [f64(t) for t in inp["a_shards"]]
+        self.b = f64(inp["b"])
+        self.h, self.hp, self.M_full = cfg["h"], cfg["hp"], cfg["b"] * cfg["s"]
+
+    def flops(self, tokens):
+        return 12.0 * tokens * self.h * self.hp
+
+    def run(self, tokens):
+        """One fwd+bwd on `tokens` tokens; returns seconds."""
+        X, dO = self.X[:tokens], self.dOut[:tokens]
+        t0 = time.perf_counter()
+        self.O.mlp_fwd(X, self.W, self.a, self.U, self.b)
+        self.O.mlp_bwd(dO, X, self.W, self.a, self.U)
+        return time.perf_counter() - t0
+
+
+def oracle_mlp_sample(workload: str, tokens: int, min_seconds: float, max_seconds: float):
+    """The oracle repeated on `tokens` tokens for at least `min_seconds`
+    (at most `max_seconds`).  Returns (TFLOP/s, seconds, repeats, tokens)."""
+    orc = OracleMLP(workload, tokens)
+    reps, el = 0, 0.0
+    while el < min_seconds and el < max_seconds:
+        el += orc.run(tokens)
+        reps += 1
+    return orc.flops(tokens) * reps / el / 1e12, el, reps, tokens
+
+
+def run_reference(args):
+    """The reference arm: the fp64 oracle, as it stands, on the host cores.
+    Every step is a bounded sample of the workload (the first `tokens` tokens,
+    same weights), sized so the whole run stays within about two minutes."""
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    wl = args.workload
+    cfg = SI.WORKLOADS[wl]
+    if cfg["kind"] != "mlp":
+        print(json.dumps({"impl": "reference", "unavailable":
+                          "the reference arm times the MLP workloads only"}))
+        return 0
+    orc = OracleMLP(wl, 512)
+    t64 = min(orc.run(64) for _ in range(2))
+    budget = 120.0 / (args.steps + args.warmup)
+    tokens = int(max(8, min(512, 64 * budget / max(t64, 1e-6))) // 8 * 8)
+    times = []
+    for i in range(args.warmup + args.steps):
+        el = orc.run(tokens)
+        if i >= args.warmup:
+            times.append(el)
+    ms = statistics.mean(times) * 1e3
+    value = orc.flops(tokens) / (ms / 1e3) / 1e12
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded normals; no dataset)",
+            "config": {"workload": wl, "b": cfg["b"], "s": cfg["s"], "h": cfg["h"], "hp": cfg["hp"],
+                       "N": cfg["N"], "sample_tokens": tokens},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
+                             "sample": f"fp64 numpy oracle MLP fwd+bwd on {tokens} of "
+                                       f"{orc.M_full} tokens per step, same weights"},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+# ----------------------------------------------------------------------------
+# main arm
+# ----------------------------------------------------------------------------
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--no-rows", action="store_true", help="skip the secondary rows")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+    ws, rank, local = dist_env()
+    if ws > 1:
+        torch.cuda.set_device(local)
+    dist_init("nccl" if ws > 1 else "gloo")
+    import megatron_tensor_transformer_tp_gb300 as tp
+    tp.lib()
+    peaks, peak_src = load_peaks()
+    cfg = SI.WORKLOADS[args.workload]
+    bench = BENCHES[cfg["kind"]](args.workload, tp, torch)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+
+    # ---- headline: device-resident inputs, profiled per launch --------------
+    tp.tp_profile_reset()
+    for _ in range(args.warmup):
+        bench.step()
+    assert tp.tp_get_status() == tp.TP_OK
+    sampler = ClockSampler(torch.cuda.current_device() if ws == 1 else local)
+    sampler.start()
+    time.sleep(0.3)
+    tp.tp_profile_reset()
+    tp.tp_profile_enable(True)
+    step_ms, wall = time_steps(torch, bench.step, args.steps, 0, flush)
+    tp.tp_profile_enable(False)
+    prof = tp.tp_profile_read()
+    clocks = sampler.stop()
+    st = tp.tp_get_status()
+    if st != tp.TP_OK:
+        raise SystemExit(f"device status {tp.tp_status_string(st)}")
+    units, unit, scale = bench.units()
+    my_seconds = sum(step_ms) / 1e3
+    max_seconds = reduce_max(my_seconds, device="cuda")
+    total_units = reduce_sum(units * args.steps, device="cuda")
+    value = aggregate_throughput(total_units, max_seconds) / scale
+    ms_per_step = max_seconds / args.steps * 1e3
+    launches = sum(n for n, _ in prof.values())
+    top, kernels = roofline_for(tp, bench, prof, peaks, peak_src, sustained=True)
+
+    # ---- end to end through the C ABI with host buffers ---------------------
+    e2e = None
+    if hasattr(bench, "e2e_step"):
+        e_ms, _ = time_steps(torch, bench.e2e_step, max(args.steps // 4, 10), 3, flush)
+        e_sec = reduce_max(sum(e_ms) / 1e3, device="cuda")
+        e_units = reduce_sum(units * len(e_ms), device="cuda")
+        h2d, d2h = bench.e2e_bytes()
+        e2e = {"value": aggregate_throughput(e_units, e_sec) / scale, "unit": unit,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": e_sec / len(e_ms) * 1e3}
+
+    # ---- secondary rows -----------------------------------------------------
+    rows = {}
+    if not args.no_rows and rank == 0:
+        rows = secondary_rows(tp, torch, flush, peaks, peak_src, args.workload)
+
+    # ---- CPU baseline: the oracle on a bounded sample ------------------------
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline and cfg["kind"] == "mlp":
+        tf, el, reps, tokens = oracle_mlp_sample(args.workload, 256, 10.0, 30.0)
+        cpu = {"value": tf, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
+               "sample": f"fp64 numpy oracle MLP fwd+bwd on {tokens} of {bench.M} tokens "
+                         f"(same weights), {reps} repeats in {el:.1f} s"}
+
+    if rank != 0:
+        return 0
+    gather = rows.get("embed_gather") if rows else None
+    line = {
+        "metric": METRIC, "value": value, "unit": unit, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded normals; no dataset)",
+        "config": {"workload": args.workload, **{k: v for k, v in cfg.items() if k not in ("kind", "seed")},
+                   "parallelism": f"replicas{ws}" if ws > 1 else "single-gpu, N logical shards",
+                   "l2": "flushed before every timed step (256 MiB write, outside the step events)",
+                   "flops_per_step": units},
+        "roofline": None if top is None else {
+            "bound": top["bound"], "achieved": top["achieved"], "peak": top["peak"],
+            "unit": top["unit"], "frac": top["frac"], "traffic": top["traffic"],
+            "kernel": top["kernel"], "peak_source": top["peak_source"],
+            "avg_launch_us": top["avg_us"]},
+        "kernels": kernels,
+        "peak_tensor_frac_step": (value / ws) / peaks["bf16_tflops_sustained"],
+        "embed_gather": gather,
+        "rows": {k: v for k, v in rows.items() if k != "embed_gather"},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": launches,
+        "clocks": clocks,
+        "wall_s_timed_loop": wall,
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def secondary_rows(tp, torch, flush, peaks, peak_src, main_workload):
+    """The other rows of the block, each on its own workload, a few timed steps."""
+    rows = {}
+    for name in ("embed_tied_V50257_h4096_T8192", "attn_b1_s2048_h4096_heads8_N8",
+                 "mlp_b2_s2048_h4096_hp16384_N2"):
+        if name == main_workload:
+            continue
+        cfg = SI.WORKLOADS[name]
+        b = BENCHES[cfg["kind"]](name, tp, torch)
+        if cfg["kind"] == "embed":
+            # the gather alone, HBM-bound
+            tp.tp_profile_reset()
+            tp.tp_profile_enable(True)
+            g_ms, _ = time_steps(torch, b.gather, 50, 5, flush)
+            tp.tp_profile_enable(False)
+            prof = tp.tp_profile_read()
+            n, ms = prof.get("embed_gather", (0, 0.0))
+            avg = ms / max(n, 1) / 1e3
+            gbs = b.gather_bytes() / avg / 1e9
+            rows["embed_gather"] = {
+                "workload": name, "value": gbs, "unit": "GB/s", "bound": "hbm", "achieved": gbs,
+                "peak": peaks["hbm_gbs"], "frac": gbs / peaks["hbm_gbs"],
+                "peak_source": f"{peak_src} hbm_gbs", "avg_launch_us": avg * 1e6,
+                "bytes_per_launch": b.gather_bytes(), "unique_rows": b.unique,
+                "traffic": load_traffic("embed_gather", name)}
+        tp.tp_profile_reset()
+        tp.tp_profile_enable(True)
+        s_ms, _ = time_steps(torch, b.step, 10, 3, flush)
+        tp.tp_profile_enable(False)
+        prof = tp.tp_profile_read()
+        units, unit, scale = b.units()
+        top, kernels = roofline_for(tp, b, prof, peaks, peak_src, sustained=True)
+        rows[name] = {"value": units / (statistics.mean(s_ms) / 1e3) / scale, "unit": unit,
+                      "ms_per_step": statistics.mean(s_ms), "kernels": kernels}
+        del b
+        torch.cuda.empty_cache()
+    assert tp.tp_get_status() == tp.TP_OK
+    return rows
+
+
+if __name__ == "__main__":
+    sys.exit(main())

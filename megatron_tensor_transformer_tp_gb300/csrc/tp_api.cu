@@ -217,11 +217,28 @@ bool group_vec_ok(const GemmGroup& g, int in_esize) {
 
 tp_status run_plan(Plan& pl, tp_dtype dt, const char* name, cudaStream_t s) {
   if (pl.overflow) return TP_ERR_INVALID;
-  // Host-side checks first: nothing below touches the GPU until they pass.
+  // Drop empty outputs; mark outputs with no k-blocks and the segments that
+  // kept outputs use.
+  GemmGroup groups[kMaxGroups];
+  bool used[kMaxSegs] = {};
+  int ng = 0;
+  for (int i = 0; i < pl.ng; ++i) {
+    GemmGroup g = pl.grp[i];
+    if (g.M <= 0 || g.N <= 0) continue;
+    int64_t ktot = 0;
+    for (int sidx = g.seg_begin; sidx < g.seg_end; ++sidx) {
+      ktot += pl.seg[sidx].K;
+      used[sidx] = pl.seg[sidx].K > 0;
+    }
+    g.k_empty = ktot == 0;
+    groups[ng++] = g;
+  }
+  if (ng == 0) return TP_OK;
+  // Host-side checks before anything touches the GPU.
   if (dt == TP_BF16) {
     for (int i = 0; i < pl.ns; ++i) {
+      if (!used[i]) continue;
       const Plan::Seg& S = pl.seg[i];
-      if (S.K == 0) continue;
       const Operand* ops[2] = {&S.A, &S.B};
       for (int j = 0; j < 2; ++j) {
         const Operand& o = *ops[j];
@@ -233,19 +250,6 @@ tp_status run_plan(Plan& pl, tp_dtype dt, const char* name, cudaStream_t s) {
   DeviceState* dev = nullptr;
   tp_status st = device_state(&dev);
   if (st != TP_OK) return st;
-
-  // Drop empty outputs; mark outputs with no k-blocks.
-  GemmGroup groups[kMaxGroups];
-  int ng = 0;
-  for (int i = 0; i < pl.ng; ++i) {
-    GemmGroup g = pl.grp[i];
-    if (g.M <= 0 || g.N <= 0) continue;
-    int64_t ktot = 0;
-    for (int sidx = g.seg_begin; sidx < g.seg_end; ++sidx) ktot += pl.seg[sidx].K;
-    g.k_empty = ktot == 0;
-    groups[ng++] = g;
-  }
-  if (ng == 0) return TP_OK;
 
   if (dt == TP_F32) {
     static SimtGemmParams p;
@@ -285,7 +289,7 @@ tp_status run_plan(Plan& pl, tp_dtype dt, const char* name, cudaStream_t s) {
     p.seg[i].K = static_cast<int>(S.K);
     p.seg[i].a_mn = S.A.mn;
     p.seg[i].b_mn = S.B.mn;
-    if (S.K == 0) continue;
+    if (!used[i]) continue;
     // K-major boxes are (64 K) x (128 or 256 rows); MN-major boxes (64 MN) x (64 K).
     if (!encode_map(&p.mapA[i], S.A.ptr, S.A.rows, S.A.cols, S.A.ld, S.A.mn ? 64 : 128))
       return TP_ERR_CUDA;
