@@ -225,6 +225,33 @@ TP_API tp_status tied_embed_grad(tp_dtype dt, int64_t T, int64_t h, int64_t V, i
 
 TP_API size_t tied_embed_grad_workspace_size(int64_t T, int64_t V);
 
+/*
+ * tied_embed_grad_noalloc -- tied_embed_grad without a caller workspace.
+ * The pages have no counterpart: this entry point exists for callers that
+ * cannot allocate device memory for the workspace, such as code running under
+ * a memory manager that owns every device allocation (a serving runtime that
+ * reserves HBM up front) or code that must not call cudaMalloc because it
+ * would synchronise the device.  It allocates nothing: the grouping scratch
+ * lives in a fixed 1.5 MiB static device array inside the library, which every
+ * GPU that loads the library holds until the process exits.
+ * Arguments, layouts and results are those of tied_embed_grad, minus the
+ * workspace.
+ * Limits and behaviour:
+ *  - tied_embed_grad_workspace_size(T, V) must not exceed 1.5 MiB (for
+ *    example V <= 131072 with T <= 65536); larger sizes return
+ *    TP_ERR_WORKSPACE before anything is launched.
+ *  - The first call on a device looks up the array's device address with that
+ *    device current; make that first call before any stream capture.
+ *  - All calls share the one array, which keeps the last call's contents: calls
+ *    that overlap on the GPU (different streams, no ordering between them) race
+ *    and give wrong results.  Order them on one stream or with events.
+ */
+TP_API tp_status tied_embed_grad_noalloc(tp_dtype dt, int64_t T, int64_t h, int64_t V, int N,
+                                         const int64_t* ids, const void* dEmb, const void* X,
+                                         const void* const* dLogits, const int64_t* ld_dlogits,
+                                         const int64_t* range_starts, void* const* dE,
+                                         int accumulate, void* stream);
+
 /* ------------------------------------------------------------------------ */
 /* Status, profiling and debugging                                           */
 /* ------------------------------------------------------------------------ */

@@ -20,7 +20,8 @@ __all__ = [
     "TP_ERR_TIMEOUT", "TP_ERR_WORKSPACE", "TP_ERR_ALIGN", "TP_F32", "TP_BF16",
     "tp_mlp_fwd", "tp_mlp_bwd", "tp_mlp_bwd_workspace_size", "tp_attn_proj_fwd",
     "tp_attn_proj_bwd", "tp_attn_proj_bwd_workspace_size", "vocab_parallel_embed",
-    "tp_vocab_logits", "tied_embed_grad", "tied_embed_grad_workspace_size", "tp_get_status",
+    "tp_vocab_logits", "tied_embed_grad", "tied_embed_grad_workspace_size",
+    "tied_embed_grad_noalloc", "tp_get_status",
     "tp_status_string", "tp_num_sms", "tp_profile_enable", "tp_profile_reset", "tp_profile_read",
     "tp_debug_inject_fault", "tp_debug_set_wait_limit_ms", "logits_pitch",
 ]
@@ -54,6 +55,8 @@ _SIGNATURES = {
     "tied_embed_grad": (_int, [_int, _i64, _i64, _i64, _int, _c_void_p, _c_void_p, _c_void_p, _PP,
                                _PI64, _PI64, _PP, _int, _c_void_p, _size_t, _c_void_p]),
     "tied_embed_grad_workspace_size": (_size_t, [_i64, _i64]),
+    "tied_embed_grad_noalloc": (_int, [_int, _i64, _i64, _i64, _int, _c_void_p, _c_void_p,
+                                       _c_void_p, _PP, _PI64, _PI64, _PP, _int, _c_void_p]),
     "tp_get_status": (_int, [_c_void_p]),
     "tp_status_string": (ctypes.c_char_p, [_int]),
     "tp_num_sms": (_int, []),
@@ -274,6 +277,28 @@ def tied_embed_grad(ids, dEmb, X, dLogits, range_starts, dE, accumulate=False, w
                                  _dev(X, "X"), _pp(dl), ld, rs, de[0], int(bool(accumulate)),
                                  _dev(workspace, "workspace"), ws_bytes, _stream(stream)),
            "tied_embed_grad")
+
+
+def tied_embed_grad_noalloc(ids, dEmb, X, dLogits, range_starts, dE, accumulate=False,
+                            stream=None):
+    """tied_embed_grad for callers that cannot allocate a device workspace: the
+    library uses its own fixed 1.5 MiB static device scratch (shared by all
+    calls; calls that overlap on the GPU race).  Sizes whose grouping needs
+    more scratch raise TPError(TP_ERR_WORKSPACE)."""
+    T = ids.numel()
+    N = len(dE)
+    h = dEmb.shape[1]
+    V = int(range_starts[-1])
+    if ids.dtype != torch.int64:
+        raise TypeError("ids must be int64")
+    dl = _ptrs(dLogits, "dLogits")
+    ld = _i64s([t.shape[1] for t in dLogits]) if dLogits is not None else None
+    de = _ptrs(dE, "dE")
+    rs = _i64s(range_starts)
+    _check(lib().tied_embed_grad_noalloc(_dtype(dEmb), T, h, V, N, _dev(ids, "ids"),
+                                         _dev(dEmb, "dEmb"), _dev(X, "X"), _pp(dl), ld, rs, de[0],
+                                         int(bool(accumulate)), _stream(stream)),
+           "tied_embed_grad_noalloc")
 
 
 # ----------------------------------------------------------------------------
