@@ -210,6 +210,7 @@ bool group_vec_ok(const GemmGroup& g, int in_esize) {
   const int oes = g.out_type == OUT_F32 ? 4 : 2;
   bool ok = al16(g.out) && (g.ldo * oes) % 16 == 0;
   if (g.out2) ok = ok && al16(g.out2);
+  if (g.bias) ok = ok && al16(g.bias);
   if (g.aux) ok = ok && al16(g.aux) && (g.ld_aux * in_esize) % 16 == 0;
   if (g.seg_src) ok = ok && al16(g.seg_src) && (g.ld_seg * in_esize) % 16 == 0;
   return ok;

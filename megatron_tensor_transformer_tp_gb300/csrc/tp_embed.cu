@@ -181,11 +181,57 @@ __global__ void segment_sum_rows(const int* __restrict__ offsets, const int* __r
 }
 
 // ---------------------------------------------------------------------------
-// Deterministic column sums: partial sums over 256-row chunks in a fixed
-// order, then the chunks summed in order.
+// Deterministic column sums: partial sums over 128-row chunks in a fixed
+// order, then the chunks summed in order.  The vector kernel gives each lane
+// 8 adjacent columns (one 16-byte load per row for bf16, two for fp32) and
+// each of the 8 warps 16 rows of the chunk; warps combine in fixed order.
 // ---------------------------------------------------------------------------
-constexpr int CS_ROWS = 256;
-constexpr int CS_COLS = 64;
+constexpr int CS_ROWS = 128;
+constexpr int CS_VCOLS = 256;  // columns per CTA of the vector kernel
+constexpr int CS_COLS = 64;    // columns per CTA of the scalar kernel
+
+__global__ void __launch_bounds__(256) colsum_partial_vec(const void* __restrict__ src, int in_f32,
+                                                          int64_t M, int64_t ncols, int64_t ld,
+                                                          float* __restrict__ partial) {
+  __shared__ float red[8][CS_VCOLS + 4];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int64_t c0 = static_cast<int64_t>(blockIdx.x) * CS_VCOLS + lane * 8;
+  const int64_t r0 = static_cast<int64_t>(blockIdx.y) * CS_ROWS;
+  float acc[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) acc[j] = 0.f;
+  if (c0 < ncols) {
+    const int64_t rend = r0 + CS_ROWS < M ? r0 + CS_ROWS : M;
+#pragma unroll 4
+    for (int64_t r = r0 + w; r < rend; r += 8) {
+      if (in_f32) {
+        const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(src) + r * ld + c0);
+        const float4 a = __ldg(p), b = __ldg(p + 1);
+        acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
+        acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
+      } else {
+        const uint4 u = __ldg(reinterpret_cast<const uint4*>(
+            static_cast<const __nv_bfloat16*>(src) + r * ld + c0));
+        float x0, x1;
+        unpack_bf16x2(u.x, x0, x1); acc[0] += x0; acc[1] += x1;
+        unpack_bf16x2(u.y, x0, x1); acc[2] += x0; acc[3] += x1;
+        unpack_bf16x2(u.z, x0, x1); acc[4] += x0; acc[5] += x1;
+        unpack_bf16x2(u.w, x0, x1); acc[6] += x0; acc[7] += x1;
+      }
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < 8; ++j) red[w][lane * 8 + j] = acc[j];
+  __syncthreads();
+  const int64_t col = static_cast<int64_t>(blockIdx.x) * CS_VCOLS + threadIdx.x;
+  if (col < ncols) {
+    float t = 0.f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) t += red[k][threadIdx.x];
+    partial[static_cast<int64_t>(blockIdx.y) * ncols + col] = t;
+  }
+}
+
 __global__ void __launch_bounds__(256) colsum_partial(const void* __restrict__ src, int in_f32,
                                                       int64_t M, int64_t ncols, int64_t ld,
                                                       float* __restrict__ partial) {
@@ -305,8 +351,16 @@ cudaError_t launch_colsum(const void* src, int in_f32, int64_t M, int64_t ncols,
   }
   const int64_t chunks = (M + CS_ROWS - 1) / CS_ROWS;
   float* partial = static_cast<float*>(ws);
-  dim3 grid(static_cast<unsigned>((ncols + CS_COLS - 1) / CS_COLS), static_cast<unsigned>(chunks));
-  colsum_partial<<<grid, 256, 0, s>>>(src, in_f32, M, ncols, ld, partial);
+  const int es = in_f32 ? 4 : 2;
+  const bool vec = (reinterpret_cast<uintptr_t>(src) % 16) == 0 && (ld * es) % 16 == 0 &&
+                   (ncols % 8) == 0;
+  if (vec) {
+    dim3 grid(static_cast<unsigned>((ncols + CS_VCOLS - 1) / CS_VCOLS), static_cast<unsigned>(chunks));
+    colsum_partial_vec<<<grid, 256, 0, s>>>(src, in_f32, M, ncols, ld, partial);
+  } else {
+    dim3 grid(static_cast<unsigned>((ncols + CS_COLS - 1) / CS_COLS), static_cast<unsigned>(chunks));
+    colsum_partial<<<grid, 256, 0, s>>>(src, in_f32, M, ncols, ld, partial);
+  }
   colsum_final<<<blocks_for(ncols, 256), 256, 0, s>>>(partial, chunks, ncols, out, accumulate);
   return cudaGetLastError();
 }

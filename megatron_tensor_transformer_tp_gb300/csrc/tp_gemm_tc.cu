@@ -12,12 +12,18 @@
 // ColumnParallelLinear and RowParallelLinear; "Megatron tensor / model
 // parallelism" notes, section MLP层的通讯量分析).
 //
-// CTA layout (192 threads):
-//   warp 0      TMA producer (one lane)
+// CTA layout (320 threads):
+//   warp 0      tile scheduler + TMA producer (one lane)
 //   warp 1      TMEM allocator + MMA issuer (one lane)
-//   warps 2..5  epilogue: TMEM -> registers -> fused op -> global
+//   warps 2..9  epilogue: TMEM -> registers -> fused op -> global; two warps
+//               per TMEM lane quarter, each taking half of the tile's columns
 // Tile 128 x 256 x 64, 4-stage smem ring, two TMEM accumulators (2 x 256
 // columns) so the epilogue of one tile overlaps the main loop of the next.
+// Tiles are handed out dynamically: each CTA starts with tile blockIdx.x and
+// then takes the next unclaimed tile from a global counter, so launches that
+// mix long-K and short-K outputs (listed longest first) balance across SMs.
+// The producer passes each tile id to the MMA and epilogue warps through a
+// small shared-memory ring.
 // Every wait is bounded: after the limit the thread records a timeout in the
 // device error word, raises a CTA-wide abort flag and the CTA winds down
 // (in-flight copies and MMAs drained, TMEM freed) instead of hanging.
@@ -40,10 +46,14 @@ constexpr int A_TILE_BYTES = BM * BK * 2;  // 16 KB
 constexpr int B_TILE_BYTES = BN * BK * 2;  // 32 KB
 constexpr int STAGE_BYTES = A_TILE_BYTES + B_TILE_BYTES;
 constexpr int TMEM_COLS = 2 * BN;  // two fp32 accumulators
-constexpr int NUM_THREADS = 192;
+constexpr int NUM_EPI_WARPS = 8;  // two per SM sub-partition, each half the columns
+constexpr int NUM_THREADS = 64 + 32 * NUM_EPI_WARPS;
+constexpr int TILE_RING = 4;      // tile ids handed from the producer to the other roles
 constexpr int MN_BOX_BYTES = 64 * BK * 2;  // one 64(MN) x 64(K) box: 8 KB
-constexpr int BAR_BYTES = 256;
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + BAR_BYTES + 1024;  // + alignment slack
+constexpr int BAR_BYTES = 512;
+constexpr int EPI_STAGE_BYTES = 32 * 32 * 4;  // per epilogue warp: one 32x32 fp32 chunk
+constexpr int SMEM_BYTES =
+    STAGES * STAGE_BYTES + BAR_BYTES + NUM_EPI_WARPS * EPI_STAGE_BYTES + 1024;  // + alignment slack
 
 // ---------------------------------------------------------------------------
 // PTX wrappers
@@ -244,38 +254,158 @@ __device__ __forceinline__ void load_bf16_chunk(const __nv_bfloat16* src, float*
   }
 }
 
-__device__ __forceinline__ void epilogue_chunk(const GemmGroup& G, int row, int n, float* v) {
-  if (row >= G.M) return;
+// ---------------------------------------------------------------------------
+// Coalesced row-block transfers.  After the TMEM load, lane l of a warp holds
+// row (row0 + l) of a 32 x 32 chunk.  Stores and loads of such a chunk go
+// through a per-warp shared-memory stage (16-byte units, XOR-swizzled so both
+// the row-per-lane side and the coalesced side are free of bank conflicts),
+// so each global access instruction of the warp covers whole 64-byte (bf16)
+// or 128-byte (fp32) row segments instead of 32 half-filled sectors.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void stage_store_rows(uint4* st, void* base, int out_type, int64_t ld,
+                                                 int row0, int M, int n, const float* v, int lane) {
+  if (out_type == OUT_BF16) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      uint4 w;
+      w.x = pack_bf16x2(v[8 * c + 0], v[8 * c + 1]);
+      w.y = pack_bf16x2(v[8 * c + 2], v[8 * c + 3]);
+      w.z = pack_bf16x2(v[8 * c + 4], v[8 * c + 5]);
+      w.w = pack_bf16x2(v[8 * c + 6], v[8 * c + 7]);
+      st[lane * 4 + (c ^ ((lane >> 1) & 3))] = w;
+    }
+    __syncwarp();
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int r = i * 8 + (lane >> 2), c = lane & 3;
+      const uint4 w = st[r * 4 + (c ^ ((r >> 1) & 3))];
+      if (row0 + r < M)
+        *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(base) +
+                                  static_cast<int64_t>(row0 + r) * ld + n + c * 8) = w;
+    }
+  } else {
+#pragma unroll
+    for (int c = 0; c < 8; ++c)
+      st[lane * 8 + (c ^ (lane & 7))] =
+          make_uint4(__float_as_uint(v[4 * c + 0]), __float_as_uint(v[4 * c + 1]),
+                     __float_as_uint(v[4 * c + 2]), __float_as_uint(v[4 * c + 3]));
+    __syncwarp();
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int r = i * 4 + (lane >> 3), c = lane & 7;
+      const uint4 w = st[r * 8 + (c ^ (r & 7))];
+      if (row0 + r < M)
+        *reinterpret_cast<uint4*>(static_cast<float*>(base) + static_cast<int64_t>(row0 + r) * ld +
+                                  n + c * 4) = w;
+    }
+  }
+  __syncwarp();
+}
+
+__device__ __forceinline__ void stage_load_rows_bf16(uint4* st, const void* base, int64_t ld,
+                                                     int row0, int M, int n, float* z, int lane) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int r = i * 8 + (lane >> 2), c = lane & 3;
+    uint4 w = make_uint4(0, 0, 0, 0);
+    if (row0 + r < M)
+      w = __ldg(reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(base) +
+                                               static_cast<int64_t>(row0 + r) * ld + n + c * 8));
+    st[r * 4 + (c ^ ((r >> 1) & 3))] = w;
+  }
+  __syncwarp();
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const uint4 w = st[lane * 4 + (c ^ ((lane >> 1) & 3))];
+    unpack_bf16x2(w.x, z[8 * c + 0], z[8 * c + 1]);
+    unpack_bf16x2(w.y, z[8 * c + 2], z[8 * c + 3]);
+    unpack_bf16x2(w.z, z[8 * c + 4], z[8 * c + 5]);
+    unpack_bf16x2(w.w, z[8 * c + 6], z[8 * c + 7]);
+  }
+  __syncwarp();
+}
+
+__device__ __forceinline__ void stage_add_rows_f32(uint4* st, const void* base, int64_t ld, int row0,
+                                                   int M, int n, float* v, int lane) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int r = i * 4 + (lane >> 3), c = lane & 7;
+    uint4 w = make_uint4(0, 0, 0, 0);
+    if (row0 + r < M)
+      w = *reinterpret_cast<const uint4*>(static_cast<const float*>(base) +
+                                          static_cast<int64_t>(row0 + r) * ld + n + c * 4);
+    st[r * 8 + (c ^ (r & 7))] = w;
+  }
+  __syncwarp();
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    const uint4 w = st[lane * 8 + (c ^ (lane & 7))];
+    v[4 * c + 0] += __uint_as_float(w.x);
+    v[4 * c + 1] += __uint_as_float(w.y);
+    v[4 * c + 2] += __uint_as_float(w.z);
+    v[4 * c + 3] += __uint_as_float(w.w);
+  }
+  __syncwarp();
+}
+
+// Epilogue of one 32 x 32 chunk: rows row0 .. row0+31 (lane l owns row0 + l),
+// columns n .. n+31.  Called by all 32 lanes of the warp (the staged paths
+// are warp-collective); rows >= M are computed but never stored.
+__device__ __forceinline__ void epilogue_chunk(const GemmGroup& G, uint4* st, int lane, int row0,
+                                               int n, float* v) {
+  const int row = row0 + lane;
+  const bool row_ok = row < G.M;
   const int ncols = min(32, G.N - n);
-  const bool vec = (ncols == 32) && G.vec_ok;
+  const bool coal = (ncols == 32) && G.vec_ok;  // warp-uniform
   switch (G.epi) {
     case EPI_STORE:
     case EPI_BIAS_GELU: {
       if (G.bias != nullptr) {
-        const __nv_bfloat16* b = static_cast<const __nv_bfloat16*>(G.bias) + n;
-        _Pragma("unroll") for (int j = 0; j < 32; ++j) if (j < ncols) v[j] += bf2f(b[j]);
+        float b[32];
+        load_bf16_chunk(static_cast<const __nv_bfloat16*>(G.bias) + n, b, ncols, coal);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] += b[j];
       }
-      store_chunk(G.out, G.out_type, G.ldo, row, n, v, ncols, vec);
+      if (coal) {
+        stage_store_rows(st, G.out, G.out_type, G.ldo, row0, G.M, n, v, lane);
+      } else if (row_ok) {
+        store_chunk(G.out, G.out_type, G.ldo, row, n, v, ncols, false);
+      }
       if (G.epi == EPI_BIAS_GELU) {
 #pragma unroll
         for (int j = 0; j < 32; ++j) v[j] = gelu_f(v[j]);
-        store_chunk(G.out2, G.out_type, G.ldo, row, n, v, ncols, vec);
+        if (coal) {
+          stage_store_rows(st, G.out2, G.out_type, G.ldo, row0, G.M, n, v, lane);
+        } else if (row_ok) {
+          store_chunk(G.out2, G.out_type, G.ldo, row, n, v, ncols, false);
+        }
       }
       break;
     }
     case EPI_DGELU: {
       float z[32];
-      const __nv_bfloat16* zp =
-          static_cast<const __nv_bfloat16*>(G.aux) + static_cast<int64_t>(row) * G.ld_aux + n;
-      load_bf16_chunk(zp, z, ncols, vec);
+      if (coal) {
+        stage_load_rows_bf16(st, G.aux, G.ld_aux, row0, G.M, n, z, lane);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) z[j] = 0.f;
+        if (row_ok)
+          load_bf16_chunk(static_cast<const __nv_bfloat16*>(G.aux) +
+                              static_cast<int64_t>(row) * G.ld_aux + n,
+                          z, ncols, false);
+      }
 #pragma unroll
       for (int j = 0; j < 32; ++j) v[j] *= gelu_grad_f(z[j]);
-      store_chunk(G.out, G.out_type, G.ldo, row, n, v, ncols, vec);
+      if (coal) {
+        stage_store_rows(st, G.out, G.out_type, G.ldo, row0, G.M, n, v, lane);
+      } else if (row_ok) {
+        store_chunk(G.out, G.out_type, G.ldo, row, n, v, ncols, false);
+      }
       break;
     }
     case EPI_F32:
     case EPI_SEGSUM: {
-      if (G.epi == EPI_SEGSUM) {
+      if (G.epi == EPI_SEGSUM && row_ok) {
         const int64_t id = G.seg_row0 + row;
         const int b = G.seg_offsets[id], e = G.seg_offsets[id + 1];
         if (b < e) {
@@ -286,7 +416,7 @@ __device__ __forceinline__ void epilogue_chunk(const GemmGroup& G, int row, int 
             float x[32];
             const __nv_bfloat16* src = static_cast<const __nv_bfloat16*>(G.seg_src) +
                                        static_cast<int64_t>(G.seg_perm[t]) * G.ld_seg + n;
-            load_bf16_chunk(src, x, ncols, vec);
+            load_bf16_chunk(src, x, ncols, coal);
 #pragma unroll
             for (int j = 0; j < 32; ++j) s[j] += x[j];
           }
@@ -294,29 +424,32 @@ __device__ __forceinline__ void epilogue_chunk(const GemmGroup& G, int row, int 
           for (int j = 0; j < 32; ++j) v[j] += s[j];
         }
       }
-      float* o = static_cast<float*>(G.out) + static_cast<int64_t>(row) * G.ldo + n;
-      if (G.accumulate) {
-        if (vec) {
-          const float4* o4 = reinterpret_cast<const float4*>(o);
+      if (coal) {
+        if (G.accumulate) stage_add_rows_f32(st, G.out, G.ldo, row0, G.M, n, v, lane);
+        stage_store_rows(st, G.out, OUT_F32, G.ldo, row0, G.M, n, v, lane);
+      } else if (row_ok) {
+        float* o = static_cast<float*>(G.out) + static_cast<int64_t>(row) * G.ldo + n;
+        if (G.accumulate) {
 #pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            const float4 w = o4[q];
-            v[4 * q + 0] += w.x;
-            v[4 * q + 1] += w.y;
-            v[4 * q + 2] += w.z;
-            v[4 * q + 3] += w.w;
-          }
-        } else {
-          _Pragma("unroll") for (int j = 0; j < 32; ++j) if (j < ncols) v[j] += o[j];
+          for (int j = 0; j < 32; ++j)
+            if (j < ncols) v[j] += o[j];
         }
+        store_chunk(G.out, OUT_F32, G.ldo, row, n, v, ncols, false);
       }
-      store_chunk(G.out, OUT_F32, G.ldo, row, n, v, ncols, vec);
       break;
     }
     default:
       break;
   }
 }
+
+// ---------------------------------------------------------------------------
+// Dynamic tile scheduling: one (next, done) counter pair per launch slot.  The
+// last CTA to finish resets its pair, so the next launch using the slot starts
+// from zero.  Launches rotate over the slots.
+// ---------------------------------------------------------------------------
+constexpr int kSchedSlots = 64;
+__device__ int g_sched[2 * kSchedSlots];
 
 // ---------------------------------------------------------------------------
 // The kernel
@@ -326,9 +459,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
-  // bars: full[0..3], empty[4..7], tfull[8..9], tempty[10..11], drain[12]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 17);
+  // bars: full[S], empty[S], tfull[2], tempty[2], drain, tile_full[R], tile_empty[R]
+  constexpr int kBarCount = 2 * STAGES + 5 + 2 * TILE_RING;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kBarCount);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + kBarCount + 1);
+  volatile int* tile_ids = reinterpret_cast<volatile int*>(bars + kBarCount + 2);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -338,6 +473,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
   auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
   auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
   const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
+  auto tile_full_bar = [&](int r) { return bar0 + 8u * (2 * STAGES + 5 + r); };
+  auto tile_empty_bar = [&](int r) { return bar0 + 8u * (2 * STAGES + 5 + TILE_RING + r); };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -346,9 +483,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(tfull_bar(b), 1);
-      mbar_init(tempty_bar(b), 128);
+      mbar_init(tempty_bar(b), NUM_EPI_WARPS);
     }
     mbar_init(drain_bar, 1);
+    for (int r = 0; r < TILE_RING; ++r) {
+      mbar_init(tile_full_bar(r), 1);
+      mbar_init(tile_empty_bar(r), 1 + NUM_EPI_WARPS);
+    }
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -366,9 +507,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
 
   const WaitCtx wctx{abort_flag, p.err, p.wait_limit_ns};
   const uint32_t tiles_base = smem_addr(smem);
+  int* sched = g_sched + 2 * p.sched_slot;
 
   if (warp == 0 && lane == 0) {
-    // ------------------------------ TMA producer ------------------------------
+    // ---------------------- tile scheduler + TMA producer ----------------------
     for (int s = 0; s < p.num_segs; ++s) {
       prefetch_tmap(&p.mapA[s]);
       prefetch_tmap(&p.mapB[s]);
@@ -379,8 +521,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
     for (int s = 0; s < STAGES; ++s) pending_phase[s] = -1;
     bool first = true;
     bool ok = true;
-    for (int tile = blockIdx.x; ok && tile < p.total_tiles; tile += gridDim.x) {
-      const TileCoord tc = decode_tile(p, tile);
+    int tile = blockIdx.x;
+    for (int i = 0; ok; ++i) {
+      // publish the tile id (or -1 = done) to the other roles
+      const int r = i % TILE_RING;
+      if (!wait_bounded(tile_empty_bar(r), static_cast<uint32_t>((i / TILE_RING) & 1) ^ 1u, wctx)) break;
+      const int t = tile < p.total_tiles ? tile : -1;
+      tile_ids[r] = t;
+      mbar_arrive(tile_full_bar(r));
+      if (t < 0) break;
+      const TileCoord tc = decode_tile(p, t);
       const GemmGroup& G = p.grp[tc.g];
       for (int s = G.seg_begin; ok && s < G.seg_end; ++s) {
         const TcSeg& S = p.seg[s];
@@ -421,15 +571,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
           }
         }
       }
+      // next tile: the first gridDim tiles are static, the rest claimed in order
+      tile = static_cast<int>(gridDim.x) + atomicAdd(sched, 1);
     }
     if (*abort_flag) {
       // Drain: wait (bounded) until every copy this thread issued has landed.
-      WaitCtx drain_ctx{abort_flag, p.err, p.wait_limit_ns};
       for (int s = 0; s < STAGES; ++s) {
         if (pending_phase[s] < 0) continue;
         const unsigned long long t0 = global_ns();
         while (!mbar_try_wait(full_bar(s), static_cast<uint32_t>(pending_phase[s]))) {
-          if (global_ns() - t0 > drain_ctx.limit_ns) break;
+          if (global_ns() - t0 > p.wait_limit_ns) break;
         }
       }
     }
@@ -437,10 +588,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
     // ------------------------------- MMA issuer -------------------------------
     int stage = 0;
     uint32_t phase = 0;
-    int lt = 0;
     bool ok = true;
     bool issued_any = false;
-    for (int tile = blockIdx.x; ok && tile < p.total_tiles; tile += gridDim.x, ++lt) {
+    for (int lt = 0; ok; ++lt) {
+      const int r = lt % TILE_RING;
+      if (!wait_bounded(tile_full_bar(r), static_cast<uint32_t>((lt / TILE_RING) & 1), wctx)) break;
+      const int tile = tile_ids[r];
+      mbar_arrive(tile_empty_bar(r));
+      if (tile < 0) break;
       const TileCoord tc = decode_tile(p, tile);
       const GemmGroup& G = p.grp[tc.g];
       const int buf = lt & 1;
@@ -493,35 +648,44 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
     }
   } else if (warp >= 2) {
     // -------------------------------- Epilogue --------------------------------
-    const int quarter = warp & 3;  // TMEM lanes this warp may access
-    int lt = 0;
-    for (int tile = blockIdx.x; tile < p.total_tiles; tile += gridDim.x, ++lt) {
+    const int quarter = warp & 3;              // TMEM lanes this warp may access
+    uint4* epi_stage = reinterpret_cast<uint4*>(smem + STAGES * STAGE_BYTES + BAR_BYTES +
+                                                (warp - 2) * EPI_STAGE_BYTES);
+    const int c_begin = ((warp - 2) >> 2) * (BN / 64);  // first of its 4 column chunks
+    for (int lt = 0;; ++lt) {
+      const int r = lt % TILE_RING;
+      if (!wait_bounded(tile_full_bar(r), static_cast<uint32_t>((lt / TILE_RING) & 1), wctx)) break;
+      const int tile = tile_ids[r];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tile_empty_bar(r));
+      if (tile < 0) break;
       const TileCoord tc = decode_tile(p, tile);
       const GemmGroup& G = p.grp[tc.g];
       const int buf = lt & 1;
       const uint32_t tphase = static_cast<uint32_t>(lt >> 1) & 1u;
       if (!wait_bounded(tfull_bar(buf), tphase, wctx)) break;
       tc_fence_after();
-      const int row = tc.m0 + quarter * 32 + lane;
+      const int row0 = tc.m0 + quarter * 32;
       const uint32_t taddr =
           tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(buf * BN);
-      for (int c = 0; c < BN / 32; ++c) {
+      for (int c = c_begin; c < c_begin + BN / 64; ++c) {
         const int n = tc.n0 + c * 32;
         if (n >= G.N) break;  // warp-uniform
-        uint32_t r[32];
+        uint32_t rr[32];
         float v[32];
         if (G.k_empty) {
 #pragma unroll
           for (int j = 0; j < 32; ++j) v[j] = 0.f;
         } else {
-          tmem_ld32(taddr + static_cast<uint32_t>(c * 32), r);
+          tmem_ld32(taddr + static_cast<uint32_t>(c * 32), rr);
 #pragma unroll
-          for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+          for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(rr[j]);
         }
-        epilogue_chunk(G, row, n, v);
+        epilogue_chunk(G, epi_stage, lane, row0, n, v);
       }
       tc_fence_before();
-      mbar_arrive(tempty_bar(buf));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty_bar(buf));
     }
   }
 
@@ -534,19 +698,30 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
                  "r"(TMEM_COLS)
                  : "memory");
   }
+  if (threadIdx.x == 0) {
+    // The last CTA to finish resets this launch slot's counters.
+    __threadfence();
+    if (atomicAdd(sched + 1, 1) == static_cast<int>(gridDim.x) - 1) {
+      atomicExch(sched, 0);
+      atomicExch(sched + 1, 0);
+    }
+  }
 }
 
 }  // namespace
 
-cudaError_t launch_tc_gemm(const TcGemmParams& p, int num_sms, cudaStream_t s) {
+cudaError_t launch_tc_gemm(const TcGemmParams& p_in, int num_sms, cudaStream_t s) {
   static bool attr_set = false;
+  static unsigned slot_seq = 0;
   if (!attr_set) {
     cudaError_t e =
         cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  if (p.total_tiles <= 0) return cudaSuccess;
+  if (p_in.total_tiles <= 0) return cudaSuccess;
+  TcGemmParams& p = const_cast<TcGemmParams&>(p_in);
+  p.sched_slot = static_cast<int>(slot_seq++ % kSchedSlots);
   const int grid = p.total_tiles < num_sms ? p.total_tiles : num_sms;
   tc_gemm_kernel<<<grid, NUM_THREADS, SMEM_BYTES, s>>>(p);
   return cudaGetLastError();

@@ -61,9 +61,9 @@ struct TcGemmParams {
   GemmGroup grp[kMaxGroups];
   int num_groups, num_segs, total_tiles;
   int fault_skip;        // fault injection: producer skips its first stage
+  int sched_slot;        // dynamic tile counter slot (set by the launcher)
   unsigned* err;         // device error word
   unsigned long long wait_limit_ns;
-  int pad;
 };
 
 // One operand pair of the fp32 SIMT engine: element (m, k) of A at
