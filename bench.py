@@ -219,7 +219,6 @@ class MLPBench:
         self.dU = [torch.empty(h, hp // N, dtype=f, device="cuda") for _ in range(N)]
         self.da = [torch.empty(hp // N, dtype=f, device="cuda") for _ in range(N)]
         self.db = torch.empty(h, dtype=f, device="cuda")
-        self.ws = torch.empty(tp.tp_mlp_bwd_workspace_size(M, h, hp), dtype=torch.uint8, device="cuda")
         # pinned host buffers for the end-to-end path
         self.hX = inp["X"].pin_memory()
         self.hdOut = inp["dOut"].pin_memory()
@@ -230,7 +229,7 @@ class MLPBench:
         tp = self.tp
         tp.tp_mlp_fwd(self.X, self.W, self.a, self.U, self.b, self.Z, self.Y, self.Out)
         tp.tp_mlp_bwd(self.dOut, self.X, self.W, self.U, self.Z, self.Y, self.dZ, self.dX, self.dW,
-                      self.da, self.dU, self.db, workspace=self.ws)
+                      self.da, self.dU, self.db)
 
     def e2e_step(self):
         self.X.copy_(self.hX, non_blocking=True)
@@ -247,10 +246,10 @@ class MLPBench:
         return 12.0 * self.M * self.h * self.hp, "TFLOP/s", 1e12
 
     def kernel_work(self):
+        # algorithmic FLOPs only: the bias column sums the backward also
+        # computes on the tensor cores are not counted
         f = 2.0 * self.M * self.h * self.hp
-        return {"gemm_column_gelu": ("tensor", f), "gemm_row_shardsum": ("tensor", f),
-                "gemm_dU_dgelu": ("tensor", 2 * f), "gemm_dX_shardsum_dW": ("tensor", 2 * f),
-                "colsum_da": ("hbm", self.M * self.hp * 2.0), "colsum_db": ("hbm", self.M * self.h * 2.0)}
+        return {"gemm_mlp_fwd": ("tensor", 2 * f), "gemm_mlp_bwd": ("tensor", 4 * f)}
 
 
 class AttnBench:
@@ -277,22 +276,19 @@ class AttnBench:
         self.dWo = [torch.empty(h, dd, dtype=f, device="cuda") for _ in range(N)]
         self.dbq = [torch.empty(3 * dd, dtype=f, device="cuda") for _ in range(N)]
         self.dbo = torch.empty(h, dtype=f, device="cuda")
-        self.ws = torch.empty(tp.tp_attn_proj_bwd_workspace_size(M, h), dtype=torch.uint8, device="cuda")
 
     def step(self):
         tp = self.tp
         tp.tp_attn_proj_fwd(self.X, self.Wq, self.bq, self.C, self.Wo, self.bo, self.QKV, self.O, self.nh)
         tp.tp_attn_proj_bwd(self.dQKV, self.dO, self.X, self.C, self.Wq, self.Wo, self.dX, self.dC,
-                            self.dWq, self.dbq, self.dWo, self.dbo, self.nh, workspace=self.ws)
+                            self.dWq, self.dbq, self.dWo, self.dbo, self.nh)
 
     def units(self):
         return 24.0 * self.M * self.h * self.h, "TFLOP/s", 1e12
 
     def kernel_work(self):
         f = 8.0 * self.M * self.h * self.h
-        return {"gemm_attn_fwd": ("tensor", f), "gemm_attn_dW": ("tensor", f),
-                "gemm_attn_dX_dC": ("tensor", f), "colsum_dbqkv": ("hbm", self.M * 3 * self.h * 2.0),
-                "colsum_dbo": ("hbm", self.M * self.h * 2.0)}
+        return {"gemm_attn_fwd": ("tensor", f), "gemm_attn_bwd": ("tensor", 2 * f)}
 
 
 class EmbedBench:
@@ -374,24 +370,25 @@ def roofline_for(tp, bench, prof, peaks, peak_src, sustained=True):
     """Dominant kernel (largest total device time) of the profiled region."""
     work = bench.kernel_work()
     rows = []
-    for name, (launches, ms) in prof.items():
-        if name not in work or launches == 0:
+    for name, (calls, kernels, ms) in prof.items():
+        if name not in work or calls == 0:
             continue
-        bound, per_launch = work[name]
-        avg_s = ms / launches / 1e3
-        rows.append((ms, name, bound, per_launch, avg_s, launches))
+        bound, per_call = work[name]
+        avg_s = ms / calls / 1e3
+        rows.append((ms, name, bound, per_call, avg_s, calls, kernels))
     if not rows:
         return None, []
     rows.sort(reverse=True)
     out = []
-    for ms, name, bound, per_launch, avg_s, launches in rows:
+    for ms, name, bound, per_call, avg_s, calls, kernels in rows:
         if bound == "tensor":
-            ach, unit = per_launch / avg_s / 1e12, "TFLOP/s"
+            ach, unit = per_call / avg_s / 1e12, "TFLOP/s"
             peak = peaks["bf16_tflops_sustained" if sustained else "bf16_tflops"]
         else:
-            ach, unit = per_launch / avg_s / 1e9, "GB/s"
+            ach, unit = per_call / avg_s / 1e9, "GB/s"
             peak = peaks["hbm_gbs"]
-        out.append({"kernel": name, "bound": bound, "launches": launches, "avg_us": avg_s * 1e6,
+        out.append({"kernel": name, "bound": bound, "launches": calls,
+                    "kernel_launches_per_call": kernels / calls, "avg_us": avg_s * 1e6,
                     "achieved": ach, "peak": peak, "unit": unit, "frac": ach / peak,
                     "share": ms / sum(r[0] for r in rows)})
     top = dict(out[0])
@@ -544,7 +541,7 @@ def main(argv=None):
     total_units = reduce_sum(units * args.steps, device="cuda")
     value = aggregate_throughput(total_units, max_seconds) / scale
     ms_per_step = max_seconds / args.steps * 1e3
-    launches = sum(n for n, _ in prof.values())
+    launches = sum(k for _, k, _ in prof.values())
     top, kernels = roofline_for(tp, bench, prof, peaks, peak_src, sustained=True)
 
     # ---- end to end through the C ABI with host buffers ---------------------
@@ -618,7 +615,7 @@ def secondary_rows(tp, torch, flush, peaks, peak_src, main_workload):
             g_ms, _ = time_steps(torch, b.gather, 50, 5, flush)
             tp.tp_profile_enable(False)
             prof = tp.tp_profile_read()
-            n, ms = prof.get("embed_gather", (0, 0.0))
+            n, _, ms = prof.get("embed_gather", (0, 0, 0.0))
             avg = ms / max(n, 1) / 1e3
             gbs = b.gather_bytes() / avg / 1e9
             rows["embed_gather"] = {

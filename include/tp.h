@@ -31,8 +31,11 @@
  *    have row pitches that are multiples of 8 elements (TMA); violations return
  *    TP_ERR_ALIGN before anything is launched.  M (and T) may be any value >= 0.
  *  - Ownership: the caller allocates and owns every buffer, including the
- *    workspace.  The library keeps only a device error word (a static device
- *    variable) and never frees caller memory.
+ *    workspace.  The library allocates nothing: its state is static device
+ *    memory (an error word, tile-scheduler and tile-completion counters, a
+ *    16 x 64 block of ones) and it never frees caller memory.  Launches
+ *    rotate over 64 counter slots, so at most 64 launches may be in flight
+ *    at the same time across all streams of a device.
  *  - Execution: work is enqueued asynchronously on `stream` (a cudaStream_t
  *    passed as void*; NULL = legacy default stream).  Argument errors return
  *    synchronously before any launch.  Device-side errors (a bounded wait that
@@ -77,6 +80,7 @@ typedef enum { TP_F32 = 0, TP_BF16 = 1 } tp_dtype;
  * §ColumnParallelLinear (f = identity, F.linear(X, W_i, a_i), no gather) and
  * §RowParallelLinear (F.linear(Y_i, U_i), g = sum over shards, then + b).
  *   Z[:, i] = X W_i^T + a_i ;  Y = GELU(Z) (erf form) ;  Out = sum_i Y_i U_i^T + b
+ * One launch: a row block of Out starts once all shards of its Y rows are stored.
  * Arguments:
  *   X   (M, h)                 input
  *   W   shard array, W_i (hp/N, h)   column-parallel weight (torch layout)
@@ -99,6 +103,9 @@ TP_API tp_status tp_mlp_fwd(tp_dtype dt, int64_t M, int64_t h, int64_t hp, int N
  * dOut) and §ColumnParallelLinear (f backward = all-reduce: dX sums shards).
  *   dZ_i = (dOut U_i) * GELU'(Z_i)      dU_i = dOut^T Y_i    dW_i = dZ_i^T X
  *   da_i = colsum(dZ_i)   db = colsum(dOut)   dX = sum_i dZ_i W_i
+ * All of it is one launch: a tile of dX, dW_i or da_i starts as soon as the
+ * dZ tiles it reads are stored.  The bias gradients are column sums computed
+ * on the tensor cores (A^T times a ones block), deterministic, no workspace.
  * Arguments:
  *   dOut (M, h), X (M, h), W, U as in tp_mlp_fwd, Z, Y (M, hp) from tp_mlp_fwd
  *   dZ  (M, hp) out            activation-gradient buffer (bf16/f32 like Z);
@@ -108,18 +115,12 @@ TP_API tp_status tp_mlp_fwd(tp_dtype dt, int64_t M, int64_t h, int64_t hp, int N
  *   da  shard array or NULL, da_i (hp/N) fp32 out
  *   dU  shard array, dU_i (h, hp/N) fp32 out
  *   db  (h) fp32 out or NULL
- *   workspace, ws_bytes        >= tp_mlp_bwd_workspace_size(M, h, hp); may be
- *                              NULL when da and db are both NULL
  */
 TP_API tp_status tp_mlp_bwd(tp_dtype dt, int64_t M, int64_t h, int64_t hp, int N,
                      const void* dOut, const void* X, const void* const* W,
                      const void* const* U, const void* Z, const void* Y,
                      void* dZ, void* dX, void* const* dW, void* const* da,
-                     void* const* dU, void* db, int accumulate,
-                     void* workspace, size_t ws_bytes, void* stream);
-
-/* Bytes of device workspace tp_mlp_bwd needs for the bias column sums. */
-TP_API size_t tp_mlp_bwd_workspace_size(int64_t M, int64_t h, int64_t hp);
+                     void* const* dU, void* db, int accumulate, void* stream);
 
 /* ------------------------------------------------------------------------ */
 /* Head-split attention projections                                          */
@@ -147,23 +148,19 @@ TP_API tp_status tp_attn_proj_fwd(tp_dtype dt, int64_t M, int64_t h, int n_heads
 
 /*
  * tp_attn_proj_bwd -- backward of tp_attn_proj_fwd ([TP notes] §Self-Attention层:
- * forward/backward as for the MLP).
+ * forward/backward as for the MLP).  One launch.
  *   dWqkv_i = dQKV_i^T X   dbqkv_i = colsum(dQKV_i)   dX = sum_i dQKV_i Wqkv_i
  *   dWo_i = dO^T C_i       dbo = colsum(dO)           dC_i = dO Wo_i
  * Arguments: dQKV (M, 3h) shard-major as QKV; dO (M, h); X, C (M, h);
  *   Wqkv, Wo shard arrays; dX (M, h) out; dC (M, h) out;
  *   dWqkv shard array (3h/N, h) fp32 out; dbqkv shard array (3h/N) fp32 or NULL;
- *   dWo shard array (h, h/N) fp32 out; dbo (h) fp32 or NULL;
- *   workspace >= tp_attn_proj_bwd_workspace_size(M, h) (NULL if no bias grads).
+ *   dWo shard array (h, h/N) fp32 out; dbo (h) fp32 or NULL.
  */
 TP_API tp_status tp_attn_proj_bwd(tp_dtype dt, int64_t M, int64_t h, int n_heads, int N,
                            const void* dQKV, const void* dO, const void* X, const void* C,
                            const void* const* Wqkv, const void* const* Wo,
                            void* dX, void* dC, void* const* dWqkv, void* const* dbqkv,
-                           void* const* dWo, void* dbo, int accumulate,
-                           void* workspace, size_t ws_bytes, void* stream);
-
-TP_API size_t tp_attn_proj_bwd_workspace_size(int64_t M, int64_t h);
+                           void* const* dWo, void* dbo, int accumulate, void* stream);
 
 /* ------------------------------------------------------------------------ */
 /* Vocab-parallel word embedding and tied output layer                       */
@@ -267,15 +264,24 @@ TP_API const char* tp_status_string(tp_status s);
 /* Number of SMs the persistent kernels size their grids for (current device). */
 TP_API int tp_num_sms(void);
 
-/* Per-kernel timing.  When enabled, every launch the library makes is
- * bracketed by CUDA events on its stream; tp_profile_read() synchronises
- * the device and returns, per kernel kind, the launch count and total device
- * milliseconds since the last reset.  Disabled by default (no events). */
+/* Timing of the library's device work.  When enabled, the device work of every
+ * library call is bracketed by CUDA events on its stream; tp_profile_read()
+ * synchronises the device and returns, per kind of work (the names the calls
+ * give it, e.g. "gemm_mlp_fwd", "embed_gather"), the number of calls, the
+ * number of kernels they launched and the total device milliseconds since the
+ * last reset.  Disabled by default (no events). */
 TP_API void tp_profile_enable(int on);
 TP_API void tp_profile_reset(void);
-/* Fills up to `cap` entries; returns the number of kernel kinds recorded.
- * names[i] points at a static string. */
-TP_API int tp_profile_read(const char** names, int64_t* launches, double* total_ms, int cap);
+/* Fills up to `cap` entries; returns the number of kinds recorded.
+ * names[i] points at a static string.  Any output array may be NULL. */
+TP_API int tp_profile_read(const char** names, int64_t* calls, int64_t* kernel_launches,
+                           double* total_ms, int cap);
+
+/* Evaluates, on the device, the GELU and GELU' that the GEMM epilogues use
+ * (GELU(z) = z Phi(z) with erf from Abramowitz & Stegun 7.1.26, |erf error|
+ * <= 1.5e-7).  z, y, dy: n fp32 device values; y or dy may be NULL.  A test
+ * hook for the device math ([TP notes] §MLP层). */
+TP_API tp_status tp_gelu_eval(const float* z, float* y, float* dy, int64_t n, void* stream);
 
 /* Fault injection for testing the bounded waits (host-controlled; never
  * faults the GPU).  kind 1: the TMA producer of the next tensor-core GEMM
@@ -283,6 +289,11 @@ TP_API int tp_profile_read(const char** names, int64_t* launches, double* total_
  * the kernel returns early with TP_ERR_TIMEOUT recorded.  kind 0: off.
  * wait_limit_ms sets the bounded-wait limit (default 1000 ms). */
 TP_API void tp_debug_inject_fault(int kind);
+/* Selects the tensor-core GEMM kernel for bf16 work: 1 (default) the two-SM
+ * kernel (CTA pairs computing 256 x 256 tiles with tcgen05 cta_group::2),
+ * 0 the one-SM kernel (128 x 256 tiles).  Both give the same results up to
+ * fp32 summation order; tests run both. */
+TP_API void tp_debug_set_gemm_kernel(int pair);
 TP_API void tp_debug_set_wait_limit_ms(int ms);
 
 #ifdef __cplusplus

@@ -18,12 +18,12 @@ import torch
 __all__ = [
     "TPError", "lib", "LIB_PATH", "TP_OK", "TP_ERR_INVALID", "TP_ERR_UNSUPPORTED", "TP_ERR_CUDA",
     "TP_ERR_TIMEOUT", "TP_ERR_WORKSPACE", "TP_ERR_ALIGN", "TP_F32", "TP_BF16",
-    "tp_mlp_fwd", "tp_mlp_bwd", "tp_mlp_bwd_workspace_size", "tp_attn_proj_fwd",
-    "tp_attn_proj_bwd", "tp_attn_proj_bwd_workspace_size", "vocab_parallel_embed",
+    "tp_mlp_fwd", "tp_mlp_bwd", "tp_attn_proj_fwd", "tp_attn_proj_bwd", "vocab_parallel_embed",
     "tp_vocab_logits", "tied_embed_grad", "tied_embed_grad_workspace_size",
     "tied_embed_grad_noalloc", "tp_get_status",
     "tp_status_string", "tp_num_sms", "tp_profile_enable", "tp_profile_reset", "tp_profile_read",
-    "tp_debug_inject_fault", "tp_debug_set_wait_limit_ms", "logits_pitch",
+    "tp_debug_inject_fault", "tp_debug_set_wait_limit_ms", "tp_debug_set_gemm_kernel",
+    "tp_gelu_eval", "logits_pitch",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libtp.so")
@@ -40,14 +40,12 @@ _SIGNATURES = {
                           _c_void_p, _c_void_p, _c_void_p, _c_void_p]),
     "tp_mlp_bwd": (_int, [_int, _i64, _i64, _i64, _int, _c_void_p, _c_void_p, _PP, _PP, _c_void_p,
                           _c_void_p, _c_void_p, _c_void_p, _PP, _PP, _PP, _c_void_p, _int,
-                          _c_void_p, _size_t, _c_void_p]),
-    "tp_mlp_bwd_workspace_size": (_size_t, [_i64, _i64, _i64]),
+                          _c_void_p]),
     "tp_attn_proj_fwd": (_int, [_int, _i64, _i64, _int, _int, _c_void_p, _PP, _PP, _c_void_p, _PP,
                                 _c_void_p, _c_void_p, _c_void_p, _c_void_p]),
     "tp_attn_proj_bwd": (_int, [_int, _i64, _i64, _int, _int, _c_void_p, _c_void_p, _c_void_p,
                                 _c_void_p, _PP, _PP, _c_void_p, _c_void_p, _PP, _PP, _PP,
-                                _c_void_p, _int, _c_void_p, _size_t, _c_void_p]),
-    "tp_attn_proj_bwd_workspace_size": (_size_t, [_i64, _i64]),
+                                _c_void_p, _int, _c_void_p]),
     "vocab_parallel_embed": (_int, [_int, _i64, _i64, _i64, _int, _c_void_p, _PP, _PI64,
                                     _c_void_p, _c_void_p]),
     "tp_vocab_logits": (_int, [_int, _i64, _i64, _i64, _int, _c_void_p, _PP, _PI64, _PP, _PI64,
@@ -62,9 +60,11 @@ _SIGNATURES = {
     "tp_num_sms": (_int, []),
     "tp_profile_enable": (None, [_int]),
     "tp_profile_reset": (None, []),
-    "tp_profile_read": (_int, [ctypes.POINTER(ctypes.c_char_p), _PI64,
+    "tp_profile_read": (_int, [ctypes.POINTER(ctypes.c_char_p), _PI64, _PI64,
                                ctypes.POINTER(ctypes.c_double), _int]),
     "tp_debug_inject_fault": (None, [_int]),
+    "tp_debug_set_gemm_kernel": (None, [_int]),
+    "tp_gelu_eval": (_int, [_c_void_p, _c_void_p, _c_void_p, _i64, _c_void_p]),
     "tp_debug_set_wait_limit_ms": (None, [_int]),
 }
 
@@ -173,22 +173,16 @@ def tp_mlp_fwd(X, W, a, U, b, Z, Y, Out, stream=None):
            "tp_mlp_fwd")
 
 
-def tp_mlp_bwd_workspace_size(M, h, hp) -> int:
-    return int(lib().tp_mlp_bwd_workspace_size(M, h, hp))
-
-
-def tp_mlp_bwd(dOut, X, W, U, Z, Y, dZ, dX, dW, da, dU, db, accumulate=False, workspace=None,
-               stream=None):
+def tp_mlp_bwd(dOut, X, W, U, Z, Y, dZ, dX, dW, da, dU, db, accumulate=False, stream=None):
     M, h = X.shape
     N = len(W)
     hp = Z.shape[1]
     w, u, dw, du = _ptrs(W, "W"), _ptrs(U, "U"), _ptrs(dW, "dW"), _ptrs(dU, "dU")
     dav = _ptrs(da, "da")
-    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     _check(lib().tp_mlp_bwd(_dtype(X), M, h, hp, N, _dev(dOut, "dOut"), _dev(X, "X"), w[0], u[0],
                             _dev(Z, "Z"), _dev(Y, "Y"), _dev(dZ, "dZ"), _dev(dX, "dX"), dw[0],
                             _pp(dav), du[0], _dev(db, "db"), int(bool(accumulate)),
-                            _dev(workspace, "workspace"), ws_bytes, _stream(stream)),
+                            _stream(stream)),
            "tp_mlp_bwd")
 
 
@@ -206,22 +200,16 @@ def tp_attn_proj_fwd(X, Wqkv, bqkv, C, Wo, bo, QKV, O, n_heads, stream=None):
            "tp_attn_proj_fwd")
 
 
-def tp_attn_proj_bwd_workspace_size(M, h) -> int:
-    return int(lib().tp_attn_proj_bwd_workspace_size(M, h))
-
-
 def tp_attn_proj_bwd(dQKV, dO, X, C, Wqkv, Wo, dX, dC, dWqkv, dbqkv, dWo, dbo, n_heads,
-                     accumulate=False, workspace=None, stream=None):
+                     accumulate=False, stream=None):
     M, h = X.shape
     N = len(Wqkv)
     wq, wo, dwq, dwo = _ptrs(Wqkv, "Wqkv"), _ptrs(Wo, "Wo"), _ptrs(dWqkv, "dWqkv"), _ptrs(dWo, "dWo")
     dbq = _ptrs(dbqkv, "dbqkv")
-    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     _check(lib().tp_attn_proj_bwd(_dtype(X), M, h, n_heads, N, _dev(dQKV, "dQKV"), _dev(dO, "dO"),
                                   _dev(X, "X"), _dev(C, "C"), wq[0], wo[0], _dev(dX, "dX"),
                                   _dev(dC, "dC"), dwq[0], _pp(dbq), dwo[0], _dev(dbo, "dbo"),
-                                  int(bool(accumulate)), _dev(workspace, "workspace"), ws_bytes,
-                                  _stream(stream)),
+                                  int(bool(accumulate)), _stream(stream)),
            "tp_attn_proj_bwd")
 
 
@@ -325,16 +313,29 @@ def tp_profile_reset():
 
 
 def tp_profile_read(cap: int = 64) -> dict:
-    """{kernel kind: (launches, total device ms)} since the last reset."""
+    """{kind: (calls, kernel launches, total device ms)} since the last reset."""
     names = (ctypes.c_char_p * cap)()
-    launches = (ctypes.c_int64 * cap)()
+    calls = (ctypes.c_int64 * cap)()
+    kernels = (ctypes.c_int64 * cap)()
     ms = (ctypes.c_double * cap)()
-    n = lib().tp_profile_read(names, launches, ms, cap)
-    return {names[i].decode(): (int(launches[i]), float(ms[i])) for i in range(min(n, cap))}
+    n = lib().tp_profile_read(names, calls, kernels, ms, cap)
+    return {names[i].decode(): (int(calls[i]), int(kernels[i]), float(ms[i]))
+            for i in range(min(n, cap))}
+
+
+def tp_gelu_eval(z, y=None, dy=None, stream=None):
+    """y, dy <- the device GELU and GELU' of fp32 z (test hook)."""
+    _check(lib().tp_gelu_eval(_dev(z, "z"), _dev(y, "y"), _dev(dy, "dy"), z.numel(), _stream(stream)),
+           "tp_gelu_eval")
 
 
 def tp_debug_inject_fault(kind: int):
     lib().tp_debug_inject_fault(int(kind))
+
+
+def tp_debug_set_gemm_kernel(pair: int):
+    """1: two-SM tensor-core kernel (default), 0: one-SM kernel."""
+    lib().tp_debug_set_gemm_kernel(int(pair))
 
 
 def tp_debug_set_wait_limit_ms(ms: int):

@@ -6,6 +6,7 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <atomic>
 #include <mutex>
 #include <vector>
 
@@ -18,6 +19,13 @@ using namespace tp;
 // expired.  A static device variable, so the library allocates nothing.
 __device__ unsigned int g_tp_error_word;
 
+// Ones operands for column sums computed as GEMMs (colsum(A) = A^T 1): a
+// 16 x 64 bf16 block of ones read by TMA for the tensor-core engine (every
+// k-block reads the same box), and one fp32 1.0 read with zero strides by the
+// fp32 engine.
+__device__ __align__(128) unsigned short g_ones_bf16[16 * 64];
+__device__ float g_one_f32 = 1.0f;
+
 namespace {
 
 // ---------------------------------------------------------------------------
@@ -28,11 +36,14 @@ struct DeviceState {
   bool ready = false;
   int num_sms = 0;
   unsigned* err = nullptr;
+  void* ones_bf16 = nullptr;
+  void* one_f32 = nullptr;
 };
 DeviceState g_dev[kMaxDevices];
 std::mutex g_mu;
 
 int g_fault_kind = 0;
+int g_use_pair = 1;  // 1: two-SM GEMM kernel for bf16, 0: one-SM kernel
 unsigned long long g_wait_limit_ns = 1000ull * 1000ull * 1000ull;
 
 tp_status device_state(DeviceState** out) {
@@ -46,6 +57,11 @@ tp_status device_state(DeviceState** out) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_tp_error_word) != cudaSuccess) return TP_ERR_CUDA;
     d.err = static_cast<unsigned*>(p);
+    if (cudaGetSymbolAddress(&d.ones_bf16, g_ones_bf16) != cudaSuccess) return TP_ERR_CUDA;
+    if (cudaGetSymbolAddress(&d.one_f32, g_one_f32) != cudaSuccess) return TP_ERR_CUDA;
+    unsigned short ones[16 * 64];
+    for (int i = 0; i < 16 * 64; ++i) ones[i] = 0x3F80;  // bf16 1.0
+    if (cudaMemcpyToSymbol(g_ones_bf16, ones, sizeof(ones)) != cudaSuccess) return TP_ERR_CUDA;
     d.ready = true;
   }
   *out = &d;
@@ -53,21 +69,24 @@ tp_status device_state(DeviceState** out) {
 }
 
 // ---------------------------------------------------------------------------
-// Profiling: optional CUDA events around every launch
+// Profiling: optional CUDA events around every library call's device work
 // ---------------------------------------------------------------------------
 struct ProfRec {
   const char* name;
   cudaEvent_t e0, e1;
+  long long kernels;
 };
 bool g_prof_on = false;
+std::mutex g_prof_mu;
 std::vector<ProfRec> g_prof_pending;
 std::vector<cudaEvent_t> g_event_pool;
 struct ProfAgg {
   const char* name;
-  int64_t launches;
+  int64_t calls, kernels;
   double ms;
 };
 std::vector<ProfAgg> g_prof_agg;
+std::atomic<long long> g_kernel_launches{0};
 
 cudaEvent_t take_event() {
   if (!g_event_pool.empty()) {
@@ -80,16 +99,24 @@ cudaEvent_t take_event() {
   return e;
 }
 
+// Runs `work` (which enqueues kernels on s); when profiling is on, brackets it
+// with events on s and records how many kernels it launched.
 template <class F>
-cudaError_t timed(const char* name, cudaStream_t s, F&& launch) {
-  if (!g_prof_on) return launch();
-  std::lock_guard<std::mutex> lk(g_mu);
-  ProfRec r{name, take_event(), take_event()};
-  cudaEventRecord(r.e0, s);
-  cudaError_t e = launch();
-  cudaEventRecord(r.e1, s);
-  g_prof_pending.push_back(r);
-  return e;
+auto timed(const char* name, cudaStream_t s, F&& work) -> decltype(work()) {
+  if (!g_prof_on) return work();
+  cudaEvent_t e0, e1;
+  {
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    e0 = take_event();
+    e1 = take_event();
+  }
+  const long long k0 = g_kernel_launches.load();
+  cudaEventRecord(e0, s);
+  auto r = work();
+  cudaEventRecord(e1, s);
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  g_prof_pending.push_back(ProfRec{name, e0, e1, g_kernel_launches.load() - k0});
+  return r;
 }
 
 void prof_flush_locked() {
@@ -101,16 +128,23 @@ void prof_flush_locked() {
     bool found = false;
     for (auto& a : g_prof_agg)
       if (strcmp(a.name, r.name) == 0) {
-        a.launches += 1;
+        a.calls += 1;
+        a.kernels += r.kernels;
         a.ms += ms;
         found = true;
       }
-    if (!found) g_prof_agg.push_back(ProfAgg{r.name, 1, ms});
+    if (!found) g_prof_agg.push_back(ProfAgg{r.name, 1, r.kernels, ms});
     g_event_pool.push_back(r.e0);
     g_event_pool.push_back(r.e1);
   }
   g_prof_pending.clear();
 }
+
+}  // namespace
+
+void tp::count_launches(int n) { g_kernel_launches.fetch_add(n); }
+
+namespace {
 
 // ---------------------------------------------------------------------------
 // TMA descriptor encoding (driver entry point fetched through the runtime)
@@ -152,18 +186,20 @@ bool encode_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols, int
 // GEMM planning
 // ---------------------------------------------------------------------------
 // A stored operand.  K-major: rows = M (or N), cols = K.  MN-major: rows = K,
-// cols = M (or N).
+// cols = M (or N).  `ones` marks the ones block of a column sum.
 struct Operand {
   const void* ptr;
   int mn;
   int64_t rows, cols, ld;
+  int ones;
 };
 inline Operand kmajor(const void* p, int64_t mn_extent, int64_t K, int64_t ld) {
-  return Operand{p, 0, mn_extent, K, ld};
+  return Operand{p, 0, mn_extent, K, ld, 0};
 }
 inline Operand mnmajor(const void* p, int64_t K, int64_t mn_extent, int64_t ld) {
-  return Operand{p, 1, K, mn_extent, ld};
+  return Operand{p, 1, K, mn_extent, ld, 0};
 }
+inline Operand ones_operand() { return Operand{nullptr, 0, 16, 64, 64, 1}; }
 
 struct Plan {
   struct Seg {
@@ -173,6 +209,8 @@ struct Plan {
   Seg seg[kMaxSegs];
   GemmGroup grp[kMaxGroups];
   int ns = 0, ng = 0;
+  int interleave = 0;   // leading groups enumerated by row block
+  int ncounters = 0;
   bool overflow = false;
 
   int add_seg(const Operand& A, const Operand& B, int64_t K) {
@@ -200,6 +238,23 @@ struct Plan {
     g.out_type = out_type;
     g.out = out;
     g.ldo = ldo;
+    g.prod_row = -1;
+    g.prod_col = -1;
+    return g;
+  }
+  // Counter block for row- or column-tile completion of producing groups.
+  int counters(int64_t n) {
+    const int b = ncounters;
+    ncounters += static_cast<int>(n);
+    if (ncounters > kMaxCounters) overflow = true;
+    return b;
+  }
+  // Column sums of a stored MN-major matrix src (rows = K tokens, cols = n)
+  // into fp32 out[n]: one GEMM against the ones block.
+  GemmGroup& add_colsum(const void* src, int64_t K, int64_t n, int64_t ld, void* out, int accumulate) {
+    const int si = add_seg(mnmajor(src, K, n, ld), ones_operand(), K);
+    GemmGroup& g = add_group(n, 1, si, si + 1, EPI_F32, OUT_F32, out, 1);
+    g.accumulate = accumulate;
     return g;
   }
 };
@@ -216,13 +271,160 @@ bool group_vec_ok(const GemmGroup& g, int in_esize) {
   return ok;
 }
 
-tp_status run_plan(Plan& pl, tp_dtype dt, const char* name, cudaStream_t s) {
+// Targets of the dependency counters: a consumer waits until every producer
+// tile feeding its counter has been stored by all epilogue warps.
+// A producer tile counts once per epilogue warp of each CTA that stores part of
+// it: per 128-row block for row counters, per CTA half (`halves` = 2 for the
+// two-SM kernel's 256-row tiles) for column counters.
+void set_dep_targets(GemmGroup* groups, int ng, int epi_parts, int halves) {
+  for (int i = 0; i < ng; ++i) {
+    GemmGroup& c = groups[i];
+    if (c.dep_kind == DEP_NONE) continue;
+    int tiles = 0;
+    for (int j = 0; j < ng; ++j) {
+      const GemmGroup& q = groups[j];
+      if (c.dep_kind == DEP_ROW && q.prod_row == c.dep_base) tiles += q.tiles_n;
+      if (c.dep_kind == DEP_COL && q.prod_col == c.dep_base) tiles += q.tiles_m * halves;
+    }
+    c.dep_target = tiles * epi_parts;
+  }
+}
+
+tp_status launch_simt_groups(const Plan& pl, const GemmGroup* groups, int ng, const DeviceState* dev,
+                             const char* name, cudaStream_t s) {
+  static SimtGemmParams p;
+  memset(&p, 0, sizeof(p));
+  for (int i = 0; i < pl.ns; ++i) {
+    const Plan::Seg& S = pl.seg[i];
+    SimtSeg& q = p.seg[i];
+    q.A = static_cast<const float*>(S.A.ptr);
+    q.sam = S.A.mn ? 1 : S.A.ld;
+    q.sak = S.A.mn ? S.A.ld : 1;
+    if (S.B.ones) {
+      q.B = static_cast<const float*>(dev->one_f32);
+      q.sbn = 0;
+      q.sbk = 0;
+    } else {
+      q.B = static_cast<const float*>(S.B.ptr);
+      q.sbn = S.B.mn ? 1 : S.B.ld;
+      q.sbk = S.B.mn ? S.B.ld : 1;
+    }
+    q.K = static_cast<int>(S.K);
+  }
+  int tiles = 0;
+  for (int i = 0; i < ng; ++i) {
+    GemmGroup g = groups[i];
+    g.tiles_m = (g.M + 63) / 64;
+    g.tiles_n = (g.N + 63) / 64;
+    g.tile_begin = tiles;
+    g.dep_kind = DEP_NONE;  // phases are ordered by separate launches instead
+    tiles += g.tiles_m * g.tiles_n;
+    p.grp[i] = g;
+  }
+  p.num_groups = ng;
+  p.num_segs = pl.ns;
+  p.total_tiles = tiles;
+  (void)name;
+  const cudaError_t e = launch_simt_gemm(p, s);
+  return e == cudaSuccess ? TP_OK : TP_ERR_CUDA;
+}
+
+// K of an output (the sum over its segments): the length of its tiles' main loop.
+int64_t group_k(const Plan& pl, const GemmGroup& g) {
+  int64_t k = 0;
+  for (int s = g.seg_begin; s < g.seg_end; ++s) k += pl.seg[s].K;
+  return k;
+}
+
+tp_status launch_tc_groups(const Plan& pl, const bool* used, GemmGroup* groups, int ng,
+                           int interleave, int ncounters, const DeviceState* dev, const char* name,
+                           cudaStream_t s, bool longest_first) {
+  if (ng == 0) return TP_OK;
+  const bool pair = g_use_pair != 0;
+  if (longest_first) {
+    // stable: longest contraction first
+    for (int i = 1; i < ng; ++i) {
+      GemmGroup g = groups[i];
+      const int64_t k = group_k(pl, g);
+      int j = i - 1;
+      while (j >= 0 && group_k(pl, groups[j]) < k) {
+        groups[j + 1] = groups[j];
+        --j;
+      }
+      groups[j + 1] = g;
+    }
+  }
+  static TcGemmParams p;
+  memset(&p, 0, sizeof(p));
+  for (int i = 0; i < pl.ns; ++i) {
+    const Plan::Seg& S = pl.seg[i];
+    p.seg[i].K = static_cast<int>(S.K);
+    p.seg[i].a_mn = S.A.mn;
+    p.seg[i].b_mn = S.B.mn;
+    p.seg[i].n_mma = S.B.ones ? 16 : 256;
+    p.seg[i].b_fixed = S.B.ones;
+    if (!used[i]) continue;
+    // K-major boxes are (64 K) x (128 or 256 rows); MN-major boxes (64 MN) x (64 K);
+    // the ones block is one (64 K) x (16 rows) box.
+    if (!encode_map(&p.mapA[i], S.A.ptr, S.A.rows, S.A.cols, S.A.ld, S.A.mn ? 64 : 128))
+      return TP_ERR_CUDA;
+    // the two-SM kernel stages half of a 256-wide B tile per CTA
+    const bool ok = S.B.ones ? encode_map(&p.mapB[i], dev->ones_bf16, 16, 64, 64, 16)
+                             : encode_map(&p.mapB[i], S.B.ptr, S.B.rows, S.B.cols, S.B.ld,
+                                          S.B.mn ? 64 : (pair ? 128 : 256));
+    if (!ok) return TP_ERR_CUDA;
+    if (pair && S.B.ones) p.seg[i].n_mma = 32;  // 16 rows of ones per CTA
+  }
+  int tiles = 0, inter_nt = 0;
+  double inter_b_bytes = 0;  // B operand bytes of the interleaved groups
+  const int rows_per_tile = pair ? 256 : 128;
+  for (int i = 0; i < ng; ++i) {
+    GemmGroup& g = groups[i];
+    g.tiles_m = (g.M + rows_per_tile - 1) / rows_per_tile;
+    g.tiles_n = (g.N + 255) / 256;
+    g.vec_ok = group_vec_ok(g, 2);
+    if (i < interleave) {
+      if (g.tiles_m != groups[0].tiles_m) return TP_ERR_INVALID;
+      inter_nt += g.tiles_n;
+      inter_b_bytes += 2.0 * static_cast<double>(g.N) * static_cast<double>(group_k(pl, g));
+    }
+  }
+  for (int i = 0; i < ng; ++i) {
+    GemmGroup& g = groups[i];
+    g.tile_begin = tiles;
+    tiles += g.tiles_m * g.tiles_n;
+  }
+  set_dep_targets(groups, ng, kEpiWarps, pair ? 2 : 1);
+  for (int i = 0; i < ng; ++i) p.grp[i] = groups[i];
+  p.pair = pair ? 1 : 0;
+  p.num_groups = ng;
+  p.num_segs = pl.ns;
+  p.total_tiles = tiles;
+  p.interleave_groups = interleave;
+  p.interleave_nt = inter_nt;
+  p.interleave_tiles = interleave > 0 ? groups[0].tiles_m * inter_nt : 0;
+  // Row-block order when the column operands are small enough to stay in L2
+  // across the whole sweep (their dependants then start early); otherwise the
+  // whole height per column tile, which streams each column operand once.
+  p.interleave_gm =
+      interleave > 0 ? (inter_b_bytes <= 32.0 * 1024 * 1024 ? 1 : groups[0].tiles_m) : 1;
+  p.num_counters = ncounters;
+  p.err = dev->err;
+  p.wait_limit_ns = g_wait_limit_ns;
+  p.fault_skip = g_fault_kind == 1;
+  g_fault_kind = 0;
+  (void)name;
+  const cudaError_t e = launch_tc_gemm(p, dev->num_sms, s);
+  return e == cudaSuccess ? TP_OK : TP_ERR_CUDA;
+}
+
+tp_status run_plan_impl(Plan& pl, tp_dtype dt, const char* name, cudaStream_t s) {
   if (pl.overflow) return TP_ERR_INVALID;
   // Drop empty outputs; mark outputs with no k-blocks and the segments that
   // kept outputs use.
   GemmGroup groups[kMaxGroups];
   bool used[kMaxSegs] = {};
-  int ng = 0;
+  int ng = 0, interleave = 0;
   for (int i = 0; i < pl.ng; ++i) {
     GemmGroup g = pl.grp[i];
     if (g.M <= 0 || g.N <= 0) continue;
@@ -232,6 +434,7 @@ tp_status run_plan(Plan& pl, tp_dtype dt, const char* name, cudaStream_t s) {
       used[sidx] = pl.seg[sidx].K > 0;
     }
     g.k_empty = ktot == 0;
+    if (i < pl.interleave) ++interleave;
     groups[ng++] = g;
   }
   if (ng == 0) return TP_OK;
@@ -243,6 +446,7 @@ tp_status run_plan(Plan& pl, tp_dtype dt, const char* name, cudaStream_t s) {
       const Operand* ops[2] = {&S.A, &S.B};
       for (int j = 0; j < 2; ++j) {
         const Operand& o = *ops[j];
+        if (o.ones) continue;
         if (!al16(o.ptr) || (o.ld % 8) != 0) return TP_ERR_ALIGN;
         if (o.rows <= 0 || o.cols <= 0) return TP_ERR_INVALID;
       }
@@ -253,69 +457,54 @@ tp_status run_plan(Plan& pl, tp_dtype dt, const char* name, cudaStream_t s) {
   if (st != TP_OK) return st;
 
   if (dt == TP_F32) {
-    static SimtGemmParams p;
-    memset(&p, 0, sizeof(p));
-    for (int i = 0; i < pl.ns; ++i) {
-      const Plan::Seg& S = pl.seg[i];
-      SimtSeg& q = p.seg[i];
-      q.A = static_cast<const float*>(S.A.ptr);
-      q.B = static_cast<const float*>(S.B.ptr);
-      q.sam = S.A.mn ? 1 : S.A.ld;
-      q.sak = S.A.mn ? S.A.ld : 1;
-      q.sbn = S.B.mn ? 1 : S.B.ld;
-      q.sbk = S.B.mn ? S.B.ld : 1;
-      q.K = static_cast<int>(S.K);
-    }
-    int tiles = 0;
+    // The fp32 engine is not persistent: dependent outputs go in a second launch.
+    GemmGroup first[kMaxGroups], second[kMaxGroups];
+    int n1 = 0, n2 = 0;
     for (int i = 0; i < ng; ++i) {
-      GemmGroup& g = groups[i];
-      g.tiles_m = (g.M + 63) / 64;
-      g.tiles_n = (g.N + 63) / 64;
-      g.tile_begin = tiles;
-      tiles += g.tiles_m * g.tiles_n;
-      p.grp[i] = g;
+      if (groups[i].dep_kind == DEP_NONE) first[n1++] = groups[i];
+      else second[n2++] = groups[i];
     }
-    p.num_groups = ng;
-    p.num_segs = pl.ns;
-    p.total_tiles = tiles;
-    cudaError_t e = timed(name, s, [&] { return launch_simt_gemm(p, s); });
-    return e == cudaSuccess ? TP_OK : TP_ERR_CUDA;
+    if (n1 > 0) {
+      st = launch_simt_groups(pl, first, n1, dev, name, s);
+      if (st != TP_OK) return st;
+    }
+    if (n2 > 0) st = launch_simt_groups(pl, second, n2, dev, name, s);
+    return st;
   }
 
   if (!get_encode()) return TP_ERR_CUDA;
-  static TcGemmParams p;
-  memset(&p, 0, sizeof(p));
-  for (int i = 0; i < pl.ns; ++i) {
-    const Plan::Seg& S = pl.seg[i];
-    p.seg[i].K = static_cast<int>(S.K);
-    p.seg[i].a_mn = S.A.mn;
-    p.seg[i].b_mn = S.B.mn;
-    if (!used[i]) continue;
-    // K-major boxes are (64 K) x (128 or 256 rows); MN-major boxes (64 MN) x (64 K).
-    if (!encode_map(&p.mapA[i], S.A.ptr, S.A.rows, S.A.cols, S.A.ld, S.A.mn ? 64 : 128))
-      return TP_ERR_CUDA;
-    if (!encode_map(&p.mapB[i], S.B.ptr, S.B.rows, S.B.cols, S.B.ld, S.B.mn ? 64 : 256))
-      return TP_ERR_CUDA;
-  }
-  int tiles = 0;
+  // Small plans run as one launch in which dependent tiles wait for the tiles
+  // they read (no launch boundary, no tail between the phases).  Large plans
+  // have enough tiles per SM that the boundary costs little; there the
+  // independent and the dependent outputs run as two launches, each ordered
+  // longest contraction first, which keeps the long tiles out of the tail.
+  int total = 0;
+  bool has_dep = false;
   for (int i = 0; i < ng; ++i) {
-    GemmGroup& g = groups[i];
-    g.tiles_m = (g.M + 127) / 128;
-    g.tiles_n = (g.N + 255) / 256;
-    g.tile_begin = tiles;
-    g.vec_ok = group_vec_ok(g, 2);
-    tiles += g.tiles_m * g.tiles_n;
-    p.grp[i] = g;
+    total += ((groups[i].M + 127) / 128) * ((groups[i].N + 255) / 256);
+    has_dep = has_dep || groups[i].dep_kind != DEP_NONE;
   }
-  p.num_groups = ng;
-  p.num_segs = pl.ns;
-  p.total_tiles = tiles;
-  p.err = dev->err;
-  p.wait_limit_ns = g_wait_limit_ns;
-  p.fault_skip = g_fault_kind == 1;
-  g_fault_kind = 0;
-  cudaError_t e = timed(name, s, [&] { return launch_tc_gemm(p, dev->num_sms, s); });
-  return e == cudaSuccess ? TP_OK : TP_ERR_CUDA;
+  if (has_dep && total > 8 * dev->num_sms) {
+    GemmGroup first[kMaxGroups], second[kMaxGroups];
+    int n1 = 0, n2 = 0;
+    for (int i = 0; i < ng; ++i) {
+      GemmGroup g = groups[i];
+      const bool dependent = g.dep_kind != DEP_NONE;
+      g.dep_kind = DEP_NONE;
+      g.prod_row = -1;
+      g.prod_col = -1;
+      if (dependent) second[n2++] = g;
+      else first[n1++] = g;
+    }
+    st = launch_tc_groups(pl, used, first, n1, 0, 0, dev, name, s, true);
+    if (st != TP_OK) return st;
+    return launch_tc_groups(pl, used, second, n2, 0, 0, dev, name, s, true);
+  }
+  return launch_tc_groups(pl, used, groups, ng, interleave, pl.ncounters, dev, name, s, false);
+}
+
+tp_status run_plan(Plan& pl, tp_dtype dt, const char* name, cudaStream_t s) {
+  return timed(name, s, [&] { return run_plan_impl(pl, dt, name, s); });
 }
 
 inline size_t esize(tp_dtype dt) { return dt == TP_F32 ? 4 : 2; }
@@ -353,37 +542,35 @@ extern "C" tp_status tp_mlp_fwd(tp_dtype dt, int64_t M, int64_t h, int64_t hp, i
   const size_t es = esize(dt);
   const int ot = dt == TP_F32 ? OUT_F32 : OUT_BF16;
 
-  // Column-parallel linear + bias + GELU: one output block per shard.
-  Plan p1;
+  Plan p;
+  const int rows = p.counters((M + 255) / 256 * 2);  // 128-row blocks, pair tiles rounded up
+  // Column-parallel linear + bias + GELU: one output block per shard, tiles
+  // enumerated row block by row block across the shards.
   for (int i = 0; i < N; ++i) {
-    const int si = p1.add_seg(kmajor(X, M, h, h), kmajor(W[i], ns, h, h), h);
-    GemmGroup& g = p1.add_group(M, ns, si, si + 1, EPI_BIAS_GELU, ot, bb(Z) + i * ns * es, hp);
+    const int si = p.add_seg(kmajor(X, M, h, h), kmajor(W[i], ns, h, h), h);
+    GemmGroup& g = p.add_group(M, ns, si, si + 1, EPI_BIAS_GELU, ot, bb(Z) + i * ns * es, hp);
     g.out2 = bb(Y) + i * ns * es;
     g.bias = a ? a[i] : nullptr;
+    g.prod_row = rows;
   }
-  tp_status st = run_plan(p1, dt, "gemm_column_gelu", s);
-  if (st != TP_OK) return st;
-
-  // Row-parallel linear: the shards are the segments of one output (g = sum).
-  Plan p2;
+  p.interleave = N;
+  // Row-parallel linear: the shards are the segments of one output (g = sum);
+  // a row block starts once all shards of its Y rows are stored.
+  const int s0 = p.ns;
   for (int i = 0; i < N; ++i)
-    p2.add_seg(kmajor(cb(Y) + i * ns * es, M, ns, hp), kmajor(U[i], h, ns, ns), ns);
-  GemmGroup& g = p2.add_group(M, h, 0, N, EPI_STORE, ot, Out, h);
+    p.add_seg(kmajor(cb(Y) + i * ns * es, M, ns, hp), kmajor(U[i], h, ns, ns), ns);
+  GemmGroup& g = p.add_group(M, h, s0, s0 + N, EPI_STORE, ot, Out, h);
   g.bias = b;
-  return run_plan(p2, dt, "gemm_row_shardsum", s);
-}
-
-extern "C" size_t tp_mlp_bwd_workspace_size(int64_t M, int64_t h, int64_t hp) {
-  if (M < 0 || h <= 0 || hp <= 0) return 0;
-  return colsum_workspace_bytes(M, hp) + colsum_workspace_bytes(M, h);
+  g.dep_kind = DEP_ROW;
+  g.dep_base = rows;
+  return run_plan(p, dt, "gemm_mlp_fwd", s);
 }
 
 extern "C" tp_status tp_mlp_bwd(tp_dtype dt, int64_t M, int64_t h, int64_t hp, int N,
                                 const void* dOut, const void* X, const void* const* W,
                                 const void* const* U, const void* Z, const void* Y, void* dZ,
                                 void* dX, void* const* dW, void* const* da, void* const* dU,
-                                void* db, int accumulate, void* workspace, size_t ws_bytes,
-                                void* stream) {
+                                void* db, int accumulate, void* stream) {
   if (!dtype_ok(dt)) return TP_ERR_UNSUPPORTED;
   if (M < 0 || h <= 0 || hp <= 0 || N < 1 || N > 8 || hp % N != 0) return TP_ERR_INVALID;
   if (M > INT32_MAX || h > INT32_MAX || hp > INT32_MAX) return TP_ERR_INVALID;
@@ -391,72 +578,56 @@ extern "C" tp_status tp_mlp_bwd(tp_dtype dt, int64_t M, int64_t h, int64_t hp, i
       !opt_shards_ok(da, N))
     return TP_ERR_INVALID;
   if (M > 0 && (!dOut || !X || !Z || !Y || !dZ || !dX)) return TP_ERR_INVALID;
-  const bool bias_grads = da != nullptr || db != nullptr;
-  if (bias_grads && (workspace == nullptr || ws_bytes < tp_mlp_bwd_workspace_size(M, h, hp)))
-    return TP_ERR_WORKSPACE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int64_t ns = hp / N;
   const size_t es = esize(dt);
   const int ot = dt == TP_F32 ? OUT_F32 : OUT_BF16;
 
-  // Launch 1: dU_i = dOut^T Y_i (contraction over tokens) and
-  //           dZ_i = (dOut U_i) * GELU'(Z_i)  (g backward is the identity).
-  Plan p1;
+  Plan p;
+  const int rows = p.counters((M + 255) / 256 * 2);  // 128-row blocks, pair tiles rounded up
+  int cols[8];
+  for (int i = 0; i < N; ++i) cols[i] = p.counters((ns + 255) / 256);
+  // dZ_i = (dOut U_i) * GELU'(Z_i): g backward is the identity, every shard
+  // sees dOut.  Counted per row block (for dX) and per column block (for dW, da).
   for (int i = 0; i < N; ++i) {
-    const int si = p1.add_seg(mnmajor(dOut, M, h, h), mnmajor(cb(Y) + i * ns * es, M, ns, hp), M);
-    GemmGroup& g = p1.add_group(h, ns, si, si + 1, EPI_F32, OUT_F32, dU[i], ns);
-    g.accumulate = accumulate;
-  }
-  for (int i = 0; i < N; ++i) {
-    const int si = p1.add_seg(kmajor(dOut, M, h, h), mnmajor(U[i], h, ns, ns), h);
-    GemmGroup& g = p1.add_group(M, ns, si, si + 1, EPI_DGELU, ot, bb(dZ) + i * ns * es, hp);
+    const int si = p.add_seg(kmajor(dOut, M, h, h), mnmajor(U[i], h, ns, ns), h);
+    GemmGroup& g = p.add_group(M, ns, si, si + 1, EPI_DGELU, ot, bb(dZ) + i * ns * es, hp);
     g.aux = cb(Z) + i * ns * es;
     g.ld_aux = hp;
+    g.prod_row = rows;
+    g.prod_col = cols[i];
   }
-  tp_status st = run_plan(p1, dt, "gemm_dU_dgelu", s);
-  if (st != TP_OK) return st;
-
-  // Launch 2: dX = sum_i dZ_i W_i (f backward = sum over shards, fused) and
-  //           dW_i = dZ_i^T X.
-  Plan p2;
-  for (int i = 0; i < N; ++i)
-    p2.add_seg(kmajor(cb(dZ) + i * ns * es, M, ns, hp), mnmajor(W[i], ns, h, h), ns);
-  p2.add_group(M, h, 0, N, EPI_STORE, ot, dX, h);
+  p.interleave = N;
+  // Independent of dZ: dU_i = dOut^T Y_i and db = colsum(dOut).
   for (int i = 0; i < N; ++i) {
-    const int si = p2.add_seg(mnmajor(cb(dZ) + i * ns * es, M, ns, hp), mnmajor(X, M, h, h), M);
-    GemmGroup& g = p2.add_group(ns, h, si, si + 1, EPI_F32, OUT_F32, dW[i], h);
+    const int si = p.add_seg(mnmajor(dOut, M, h, h), mnmajor(cb(Y) + i * ns * es, M, ns, hp), M);
+    GemmGroup& g = p.add_group(h, ns, si, si + 1, EPI_F32, OUT_F32, dU[i], ns);
     g.accumulate = accumulate;
   }
-  st = run_plan(p2, dt, "gemm_dX_shardsum_dW", s);
-  if (st != TP_OK) return st;
-
-  // Bias gradients: deterministic column sums.
-  if (bias_grads) {
-    uint8_t* ws = static_cast<uint8_t*>(workspace);
-    const int in_f32 = dt == TP_F32;
-    if (da) {
-      ShardOut o{};
-      for (int i = 0; i < N; ++i) o.p[i] = static_cast<float*>(da[i]);
-      o.cols_per_shard = ns;
-      o.n = N;
-      cudaError_t e = timed("colsum_da", s, [&] {
-        return launch_colsum(dZ, in_f32, M, hp, hp, o, accumulate, ws, s);
-      });
-      if (e != cudaSuccess) return TP_ERR_CUDA;
-    }
-    if (db) {
-      ShardOut o{};
-      o.p[0] = static_cast<float*>(db);
-      o.cols_per_shard = h;
-      o.n = 1;
-      cudaError_t e = timed("colsum_db", s, [&] {
-        return launch_colsum(dOut, in_f32, M, h, h, o, accumulate,
-                             ws + colsum_workspace_bytes(M, hp), s);
-      });
-      if (e != cudaSuccess) return TP_ERR_CUDA;
+  if (db) p.add_colsum(dOut, M, h, h, db, accumulate);
+  // dX = sum_i dZ_i W_i (f backward = sum over shards, fused), per row block.
+  const int s0 = p.ns;
+  for (int i = 0; i < N; ++i)
+    p.add_seg(kmajor(cb(dZ) + i * ns * es, M, ns, hp), mnmajor(W[i], ns, h, h), ns);
+  GemmGroup& gx = p.add_group(M, h, s0, s0 + N, EPI_STORE, ot, dX, h);
+  gx.dep_kind = DEP_ROW;
+  gx.dep_base = rows;
+  // dW_i = dZ_i^T X and da_i = colsum(dZ_i), per column block of dZ_i.
+  for (int i = 0; i < N; ++i) {
+    const int si = p.add_seg(mnmajor(cb(dZ) + i * ns * es, M, ns, hp), mnmajor(X, M, h, h), M);
+    GemmGroup& g = p.add_group(ns, h, si, si + 1, EPI_F32, OUT_F32, dW[i], h);
+    g.accumulate = accumulate;
+    g.dep_kind = DEP_COL;
+    g.dep_base = cols[i];
+  }
+  if (da) {
+    for (int i = 0; i < N; ++i) {
+      GemmGroup& g = p.add_colsum(cb(dZ) + i * ns * es, M, ns, hp, da[i], accumulate);
+      g.dep_kind = DEP_COL;
+      g.dep_base = cols[i];
     }
   }
-  return TP_OK;
+  return run_plan(p, dt, "gemm_mlp_bwd", s);
 }
 
 // ===========================================================================
@@ -480,7 +651,7 @@ extern "C" tp_status tp_attn_proj_fwd(tp_dtype dt, int64_t M, int64_t h, int n_h
   const int ot = dt == TP_F32 ? OUT_F32 : OUT_BF16;
 
   Plan p;
-  // Output projection first: O = sum_i C_i Wo_i^T + bo.
+  // Output projection: O = sum_i C_i Wo_i^T + bo (the shards are segments).
   for (int i = 0; i < N; ++i) p.add_seg(kmajor(cb(C) + i * d * es, M, d, h), kmajor(Wo[i], h, d, d), d);
   GemmGroup& go = p.add_group(M, h, 0, N, EPI_STORE, ot, O, h);
   go.bias = bo;
@@ -493,18 +664,12 @@ extern "C" tp_status tp_attn_proj_fwd(tp_dtype dt, int64_t M, int64_t h, int n_h
   return run_plan(p, dt, "gemm_attn_fwd", s);
 }
 
-extern "C" size_t tp_attn_proj_bwd_workspace_size(int64_t M, int64_t h) {
-  if (M < 0 || h <= 0) return 0;
-  return colsum_workspace_bytes(M, 3 * h) + colsum_workspace_bytes(M, h);
-}
-
 extern "C" tp_status tp_attn_proj_bwd(tp_dtype dt, int64_t M, int64_t h, int n_heads, int N,
                                       const void* dQKV, const void* dO, const void* X,
                                       const void* C, const void* const* Wqkv,
                                       const void* const* Wo, void* dX, void* dC,
                                       void* const* dWqkv, void* const* dbqkv, void* const* dWo,
-                                      void* dbo, int accumulate, void* workspace, size_t ws_bytes,
-                                      void* stream) {
+                                      void* dbo, int accumulate, void* stream) {
   if (!dtype_ok(dt)) return TP_ERR_UNSUPPORTED;
   if (M < 0 || h <= 0 || N < 1 || N > 8 || n_heads < 1 || n_heads % N != 0 || h % n_heads != 0)
     return TP_ERR_INVALID;
@@ -513,68 +678,39 @@ extern "C" tp_status tp_attn_proj_bwd(tp_dtype dt, int64_t M, int64_t h, int n_h
       !opt_shards_ok(dbqkv, N))
     return TP_ERR_INVALID;
   if (M > 0 && (!dQKV || !dO || !X || !C || !dX || !dC)) return TP_ERR_INVALID;
-  const bool bias_grads = dbqkv != nullptr || dbo != nullptr;
-  if (bias_grads && (workspace == nullptr || ws_bytes < tp_attn_proj_bwd_workspace_size(M, h)))
-    return TP_ERR_WORKSPACE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int64_t d = h / N;
   const int64_t w = 3 * d;
   const size_t es = esize(dt);
   const int ot = dt == TP_F32 ? OUT_F32 : OUT_BF16;
 
-  // Weight gradients (contractions over tokens), one launch.
-  Plan p1;
-  for (int i = 0; i < N; ++i) {
-    const int si = p1.add_seg(mnmajor(cb(dQKV) + i * w * es, M, w, 3 * h), mnmajor(X, M, h, h), M);
-    GemmGroup& g = p1.add_group(w, h, si, si + 1, EPI_F32, OUT_F32, dWqkv[i], h);
-    g.accumulate = accumulate;
-  }
-  for (int i = 0; i < N; ++i) {
-    const int si = p1.add_seg(mnmajor(dO, M, h, h), mnmajor(cb(C) + i * d * es, M, d, h), M);
-    GemmGroup& g = p1.add_group(h, d, si, si + 1, EPI_F32, OUT_F32, dWo[i], d);
-    g.accumulate = accumulate;
-  }
-  tp_status st = run_plan(p1, dt, "gemm_attn_dW", s);
-  if (st != TP_OK) return st;
-
-  // Activation gradients: dX = sum_i dQKV_i Wqkv_i (shard sum), dC_i = dO Wo_i.
-  Plan p2;
+  // One launch, longest contractions first; every input is given, so no tile waits.
+  Plan p;
+  // dX = sum_i dQKV_i Wqkv_i (f backward: sum over shards, fused).
   for (int i = 0; i < N; ++i)
-    p2.add_seg(kmajor(cb(dQKV) + i * w * es, M, w, 3 * h), mnmajor(Wqkv[i], w, h, h), w);
-  p2.add_group(M, h, 0, N, EPI_STORE, ot, dX, h);
+    p.add_seg(kmajor(cb(dQKV) + i * w * es, M, w, 3 * h), mnmajor(Wqkv[i], w, h, h), w);
+  p.add_group(M, h, 0, N, EPI_STORE, ot, dX, h);
+  // dC_i = dO Wo_i (g backward: identity).
   for (int i = 0; i < N; ++i) {
-    const int si = p2.add_seg(kmajor(dO, M, h, h), mnmajor(Wo[i], h, d, d), h);
-    p2.add_group(M, d, si, si + 1, EPI_STORE, ot, bb(dC) + i * d * es, h);
+    const int si = p.add_seg(kmajor(dO, M, h, h), mnmajor(Wo[i], h, d, d), h);
+    p.add_group(M, d, si, si + 1, EPI_STORE, ot, bb(dC) + i * d * es, h);
   }
-  st = run_plan(p2, dt, "gemm_attn_dX_dC", s);
-  if (st != TP_OK) return st;
-
-  if (bias_grads) {
-    uint8_t* ws = static_cast<uint8_t*>(workspace);
-    const int in_f32 = dt == TP_F32;
-    if (dbqkv) {
-      ShardOut o{};
-      for (int i = 0; i < N; ++i) o.p[i] = static_cast<float*>(dbqkv[i]);
-      o.cols_per_shard = w;
-      o.n = N;
-      cudaError_t e = timed("colsum_dbqkv", s, [&] {
-        return launch_colsum(dQKV, in_f32, M, 3 * h, 3 * h, o, accumulate, ws, s);
-      });
-      if (e != cudaSuccess) return TP_ERR_CUDA;
-    }
-    if (dbo) {
-      ShardOut o{};
-      o.p[0] = static_cast<float*>(dbo);
-      o.cols_per_shard = h;
-      o.n = 1;
-      cudaError_t e = timed("colsum_dbo", s, [&] {
-        return launch_colsum(dO, in_f32, M, h, h, o, accumulate,
-                             ws + colsum_workspace_bytes(M, 3 * h), s);
-      });
-      if (e != cudaSuccess) return TP_ERR_CUDA;
-    }
+  // Weight gradients: contractions over tokens.
+  for (int i = 0; i < N; ++i) {
+    const int si = p.add_seg(mnmajor(cb(dQKV) + i * w * es, M, w, 3 * h), mnmajor(X, M, h, h), M);
+    GemmGroup& g = p.add_group(w, h, si, si + 1, EPI_F32, OUT_F32, dWqkv[i], h);
+    g.accumulate = accumulate;
   }
-  return TP_OK;
+  for (int i = 0; i < N; ++i) {
+    const int si = p.add_seg(mnmajor(dO, M, h, h), mnmajor(cb(C) + i * d * es, M, d, h), M);
+    GemmGroup& g = p.add_group(h, d, si, si + 1, EPI_F32, OUT_F32, dWo[i], d);
+    g.accumulate = accumulate;
+  }
+  // Bias gradients: column sums as GEMMs against the ones block.
+  if (dbqkv)
+    for (int i = 0; i < N; ++i) p.add_colsum(cb(dQKV) + i * w * es, M, w, 3 * h, dbqkv[i], accumulate);
+  if (dbo) p.add_colsum(dO, M, h, h, dbo, accumulate);
+  return run_plan(p, dt, "gemm_attn_bwd", s);
 }
 
 // ===========================================================================
@@ -730,24 +866,34 @@ extern "C" int tp_num_sms(void) {
 extern "C" void tp_profile_enable(int on) { g_prof_on = on != 0; }
 
 extern "C" void tp_profile_reset(void) {
-  std::lock_guard<std::mutex> lk(g_mu);
+  std::lock_guard<std::mutex> lk(g_prof_mu);
   prof_flush_locked();
   g_prof_agg.clear();
 }
 
-extern "C" int tp_profile_read(const char** names, int64_t* launches, double* total_ms, int cap) {
-  std::lock_guard<std::mutex> lk(g_mu);
+extern "C" int tp_profile_read(const char** names, int64_t* calls, int64_t* kernel_launches,
+                               double* total_ms, int cap) {
+  std::lock_guard<std::mutex> lk(g_prof_mu);
   prof_flush_locked();
   const int n = static_cast<int>(g_prof_agg.size());
   for (int i = 0; i < n && i < cap; ++i) {
     if (names) names[i] = g_prof_agg[i].name;
-    if (launches) launches[i] = g_prof_agg[i].launches;
+    if (calls) calls[i] = g_prof_agg[i].calls;
+    if (kernel_launches) kernel_launches[i] = g_prof_agg[i].kernels;
     if (total_ms) total_ms[i] = g_prof_agg[i].ms;
   }
   return n;
 }
 
+extern "C" tp_status tp_gelu_eval(const float* z, float* y, float* dy, int64_t n, void* stream) {
+  if (n < 0 || (n > 0 && (z == nullptr || (y == nullptr && dy == nullptr)))) return TP_ERR_INVALID;
+  const cudaError_t e = launch_gelu_eval(z, y, dy, n, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? TP_OK : TP_ERR_CUDA;
+}
+
 extern "C" void tp_debug_inject_fault(int kind) { g_fault_kind = kind; }
+
+extern "C" void tp_debug_set_gemm_kernel(int pair) { g_use_pair = pair != 0; }
 
 extern "C" void tp_debug_set_wait_limit_ms(int ms) {
   g_wait_limit_ns = static_cast<unsigned long long>(ms > 0 ? ms : 1000) * 1000000ull;

@@ -9,18 +9,36 @@
 
 namespace tp {
 
+// erf(x) by Abramowitz & Stegun, Handbook of Mathematical Functions, formula
+// 7.1.26: erf(x) = 1 - (a1 t + a2 t^2 + a3 t^3 + a4 t^4 + a5 t^5) e^{-x^2},
+// t = 1 / (1 + p x) for x >= 0, odd in x, |error| <= 1.5e-7.  The factor
+// e^{-x^2} is returned too: with x = z / sqrt 2 it is the e^{-z^2/2} of the
+// normal density, so GELU' reuses it.
+__device__ __forceinline__ float erf_as7126(float x, float& e_mx2) {
+  const float ax = fabsf(x);
+  const float t = __fdividef(1.0f, fmaf(0.3275911f, ax, 1.0f));
+  float q = fmaf(1.061405429f, t, -1.453152027f);
+  q = fmaf(q, t, 1.421413741f);
+  q = fmaf(q, t, -0.284496736f);
+  q = fmaf(q, t, 0.254829592f);
+  e_mx2 = __expf(-ax * ax);
+  return copysignf(fmaf(-q * t, e_mx2, 1.0f), x);
+}
+
 // GELU(z) = z * Phi(z), Phi(z) = (1 + erf(z / sqrt 2)) / 2 (exact erf form; the
 // activation between the column- and row-parallel linears of the MLP block,
 // "Megatron tensor / model parallelism" notes, section MLP层).
 __device__ __forceinline__ float gelu_f(float z) {
-  return 0.5f * z * (1.0f + erff(z * 0.70710678118654752f));
+  float e;
+  const float r = erf_as7126(z * 0.70710678118654752f, e);
+  return 0.5f * z * (1.0f + r);
 }
 
 // d GELU / dz = Phi(z) + z * phi(z), phi(z) = exp(-z^2 / 2) / sqrt(2 pi).
 __device__ __forceinline__ float gelu_grad_f(float z) {
-  const float cdf = 0.5f * (1.0f + erff(z * 0.70710678118654752f));
-  const float pdf = expf(-0.5f * z * z) * 0.39894228040143268f;
-  return fmaf(z, pdf, cdf);
+  float e;
+  const float r = erf_as7126(z * 0.70710678118654752f, e);
+  return fmaf(z * 0.39894228040143268f, e, 0.5f * (1.0f + r));
 }
 
 __device__ __forceinline__ float bf2f(__nv_bfloat16 x) { return __bfloat162float(x); }

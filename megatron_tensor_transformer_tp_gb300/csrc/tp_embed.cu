@@ -1,7 +1,6 @@
 // HBM-bound kernels of the block: the vocab-parallel embedding gather, the
 // deterministic grouping of tokens by id (counting sort, stable in token
-// order), the input-side embedding gradient as ordered segment sums, and
-// deterministic column sums for bias gradients.
+// order) and the input-side embedding gradient as ordered segment sums.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -180,100 +179,6 @@ __global__ void segment_sum_rows(const int* __restrict__ offsets, const int* __r
   }
 }
 
-// ---------------------------------------------------------------------------
-// Deterministic column sums: partial sums over 128-row chunks in a fixed
-// order, then the chunks summed in order.  The vector kernel gives each lane
-// 8 adjacent columns (one 16-byte load per row for bf16, two for fp32) and
-// each of the 8 warps 16 rows of the chunk; warps combine in fixed order.
-// ---------------------------------------------------------------------------
-constexpr int CS_ROWS = 128;
-constexpr int CS_VCOLS = 256;  // columns per CTA of the vector kernel
-constexpr int CS_COLS = 64;    // columns per CTA of the scalar kernel
-
-__global__ void __launch_bounds__(256) colsum_partial_vec(const void* __restrict__ src, int in_f32,
-                                                          int64_t M, int64_t ncols, int64_t ld,
-                                                          float* __restrict__ partial) {
-  __shared__ float red[8][CS_VCOLS + 4];
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  const int64_t c0 = static_cast<int64_t>(blockIdx.x) * CS_VCOLS + lane * 8;
-  const int64_t r0 = static_cast<int64_t>(blockIdx.y) * CS_ROWS;
-  float acc[8];
-#pragma unroll
-  for (int j = 0; j < 8; ++j) acc[j] = 0.f;
-  if (c0 < ncols) {
-    const int64_t rend = r0 + CS_ROWS < M ? r0 + CS_ROWS : M;
-#pragma unroll 4
-    for (int64_t r = r0 + w; r < rend; r += 8) {
-      if (in_f32) {
-        const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(src) + r * ld + c0);
-        const float4 a = __ldg(p), b = __ldg(p + 1);
-        acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
-        acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
-      } else {
-        const uint4 u = __ldg(reinterpret_cast<const uint4*>(
-            static_cast<const __nv_bfloat16*>(src) + r * ld + c0));
-        float x0, x1;
-        unpack_bf16x2(u.x, x0, x1); acc[0] += x0; acc[1] += x1;
-        unpack_bf16x2(u.y, x0, x1); acc[2] += x0; acc[3] += x1;
-        unpack_bf16x2(u.z, x0, x1); acc[4] += x0; acc[5] += x1;
-        unpack_bf16x2(u.w, x0, x1); acc[6] += x0; acc[7] += x1;
-      }
-    }
-  }
-#pragma unroll
-  for (int j = 0; j < 8; ++j) red[w][lane * 8 + j] = acc[j];
-  __syncthreads();
-  const int64_t col = static_cast<int64_t>(blockIdx.x) * CS_VCOLS + threadIdx.x;
-  if (col < ncols) {
-    float t = 0.f;
-#pragma unroll
-    for (int k = 0; k < 8; ++k) t += red[k][threadIdx.x];
-    partial[static_cast<int64_t>(blockIdx.y) * ncols + col] = t;
-  }
-}
-
-__global__ void __launch_bounds__(256) colsum_partial(const void* __restrict__ src, int in_f32,
-                                                      int64_t M, int64_t ncols, int64_t ld,
-                                                      float* __restrict__ partial) {
-  __shared__ float red[4][CS_COLS];
-  const int tx = threadIdx.x & 63, ty = threadIdx.x >> 6;
-  const int64_t col = static_cast<int64_t>(blockIdx.x) * CS_COLS + tx;
-  const int64_t r0 = static_cast<int64_t>(blockIdx.y) * CS_ROWS;
-  float s = 0.f;
-  if (col < ncols) {
-    for (int64_t r = r0 + ty; r < r0 + CS_ROWS && r < M; r += 4) {
-      const int64_t idx = r * ld + col;
-      s += in_f32 ? static_cast<const float*>(src)[idx]
-                  : bf2f(static_cast<const __nv_bfloat16*>(src)[idx]);
-    }
-  }
-  red[ty][tx] = s;
-  __syncthreads();
-  if (ty == 0 && col < ncols)
-    partial[static_cast<int64_t>(blockIdx.y) * ncols + col] =
-        ((red[0][tx] + red[1][tx]) + red[2][tx]) + red[3][tx];
-}
-
-__global__ void colsum_final(const float* __restrict__ partial, int64_t chunks, int64_t ncols,
-                             const __grid_constant__ ShardOut out, int accumulate) {
-  for (int64_t c = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; c < ncols;
-       c += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    float s = 0.f;
-    for (int64_t k = 0; k < chunks; ++k) s += partial[k * ncols + c];
-    const int64_t sh = c / out.cols_per_shard;
-    float* o = out.p[sh] + (c - sh * out.cols_per_shard);
-    *o = accumulate ? *o + s : s;
-  }
-}
-
-__global__ void colsum_zero_rows(int64_t ncols, const __grid_constant__ ShardOut out) {
-  for (int64_t c = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; c < ncols;
-       c += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int64_t sh = c / out.cols_per_shard;
-    out.p[sh][c - sh * out.cols_per_shard] = 0.f;
-  }
-}
-
 inline int blocks_for(int64_t n, int threads, int cap = 65535 * 8) {
   int64_t b = (n + threads - 1) / threads;
   if (b < 1) b = 1;
@@ -295,6 +200,7 @@ cudaError_t launch_embed_gather(const int64_t* ids, int64_t T, int64_t row_bytes
     embed_gather_vec16<<<blocks, 256, 0, s>>>(ids, T, row_bytes, rt, static_cast<uint8_t*>(out));
   else
     embed_gather_bytes<<<blocks, 256, 0, s>>>(ids, T, row_bytes, rt, static_cast<uint8_t*>(out));
+  count_launches(1);
   return cudaGetLastError();
 }
 
@@ -324,6 +230,7 @@ cudaError_t launch_embed_sort(const int64_t* ids, int64_t T, int64_t V, void* ws
     sort_scatter<<<blocks_for(T, 256), 256, 0, s>>>(ids, T, V, offsets, counts, perm);
     sort_segments<<<blocks_for(V, 256), 256, 0, s>>>(offsets, V, perm);
   }
+  count_launches(T > 0 ? 4 : 1);
   return cudaGetLastError();
 }
 
@@ -334,34 +241,7 @@ cudaError_t launch_segment_sum(const void* ws, int64_t V, int64_t T, const void*
   const int* perm = sort_perm(const_cast<void*>(ws), V);
   segment_sum_rows<<<blocks_for(V * 32, 256), 256, 0, s>>>(offsets, perm, V, dEmb, in_f32, h, dE,
                                                            accumulate);
-  return cudaGetLastError();
-}
-
-size_t colsum_workspace_bytes(int64_t M, int64_t ncols) {
-  const int64_t chunks = (M + CS_ROWS - 1) / CS_ROWS;
-  return align256(static_cast<size_t>(chunks > 0 ? chunks : 1) * ncols * 4);
-}
-
-cudaError_t launch_colsum(const void* src, int in_f32, int64_t M, int64_t ncols, int64_t ld,
-                          const ShardOut& out, int accumulate, void* ws, cudaStream_t s) {
-  if (ncols <= 0) return cudaSuccess;
-  if (M <= 0) {
-    if (!accumulate) colsum_zero_rows<<<blocks_for(ncols, 256), 256, 0, s>>>(ncols, out);
-    return cudaGetLastError();
-  }
-  const int64_t chunks = (M + CS_ROWS - 1) / CS_ROWS;
-  float* partial = static_cast<float*>(ws);
-  const int es = in_f32 ? 4 : 2;
-  const bool vec = (reinterpret_cast<uintptr_t>(src) % 16) == 0 && (ld * es) % 16 == 0 &&
-                   (ncols % 8) == 0;
-  if (vec) {
-    dim3 grid(static_cast<unsigned>((ncols + CS_VCOLS - 1) / CS_VCOLS), static_cast<unsigned>(chunks));
-    colsum_partial_vec<<<grid, 256, 0, s>>>(src, in_f32, M, ncols, ld, partial);
-  } else {
-    dim3 grid(static_cast<unsigned>((ncols + CS_COLS - 1) / CS_COLS), static_cast<unsigned>(chunks));
-    colsum_partial<<<grid, 256, 0, s>>>(src, in_f32, M, ncols, ld, partial);
-  }
-  colsum_final<<<blocks_for(ncols, 256), 256, 0, s>>>(partial, chunks, ncols, out, accumulate);
+  count_launches(1);
   return cudaGetLastError();
 }
 

@@ -101,11 +101,33 @@ __global__ void __launch_bounds__(STHREADS) simt_gemm_kernel(const __grid_consta
     for (int j = 0; j < 4; ++j) epilogue_elem(G, m0 + ty * 4 + i, n0 + tx * 4 + j, acc[i][j]);
 }
 
+// Evaluates the epilogues' GELU and GELU' on an array (test hook for the
+// device math).
+__global__ void gelu_eval_kernel(const float* __restrict__ z, float* __restrict__ y,
+                                 float* __restrict__ dy, int64_t n) {
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const float v = z[i];
+    if (y) y[i] = gelu_f(v);
+    if (dy) dy[i] = gelu_grad_f(v);
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_gelu_eval(const float* z, float* y, float* dy, int64_t n, cudaStream_t s) {
+  if (n <= 0) return cudaSuccess;
+  int64_t blocks = (n + 255) / 256;
+  if (blocks > 4096) blocks = 4096;
+  gelu_eval_kernel<<<static_cast<int>(blocks), 256, 0, s>>>(z, y, dy, n);
+  count_launches(1);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_simt_gemm(const SimtGemmParams& p, cudaStream_t s) {
   if (p.total_tiles <= 0) return cudaSuccess;
   simt_gemm_kernel<<<p.total_tiles, STHREADS, 0, s>>>(p);
+  count_launches(1);
   return cudaGetLastError();
 }
 

@@ -46,7 +46,7 @@ constexpr int A_TILE_BYTES = BM * BK * 2;  // 16 KB
 constexpr int B_TILE_BYTES = BN * BK * 2;  // 32 KB
 constexpr int STAGE_BYTES = A_TILE_BYTES + B_TILE_BYTES;
 constexpr int TMEM_COLS = 2 * BN;  // two fp32 accumulators
-constexpr int NUM_EPI_WARPS = 8;  // two per SM sub-partition, each half the columns
+constexpr int NUM_EPI_WARPS = kEpiWarps;  // two per SM sub-partition, each half the columns
 constexpr int NUM_THREADS = 64 + 32 * NUM_EPI_WARPS;
 constexpr int TILE_RING = 4;      // tile ids handed from the producer to the other roles
 constexpr int MN_BOX_BYTES = 64 * BK * 2;  // one 64(MN) x 64(K) box: 8 KB
@@ -148,10 +148,16 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t
 
 // Instruction descriptor of tcgen05.mma kind::f16: D f32, A and B bf16,
 // transpose bits select MN-major operands, N >> 3 at bit 17, M >> 4 at bit 24.
-__device__ __forceinline__ uint32_t idesc_bf16(int a_mn, int b_mn) {
+__device__ __forceinline__ uint32_t idesc_bf16(int a_mn, int b_mn, int n) {
   return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(a_mn) << 15) |
-         (static_cast<uint32_t>(b_mn) << 16) | (static_cast<uint32_t>(BN >> 3) << 17) |
+         (static_cast<uint32_t>(b_mn) << 16) | (static_cast<uint32_t>(n >> 3) << 17) |
          (static_cast<uint32_t>(BM >> 4) << 24);
+}
+
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
 }
 
 __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
@@ -191,16 +197,46 @@ struct TileCoord {
   int g, m0, n0;
 };
 
-__device__ __forceinline__ TileCoord decode_tile(const TcGemmParams& p, int tile) {
-  int g = 0;
+template <int ROWS>
+__device__ __forceinline__ TileCoord decode_tile_rows(const TcGemmParams& p, int tile) {
+  if (tile < p.interleave_tiles) {
+    // Leading groups share the row tiling.  They are enumerated in super-rows
+    // of GM row blocks; inside a super-row, column tile by column tile (across
+    // the groups) and row block fastest.  GM = 1 finishes row blocks one after
+    // the other (their dependants can start early); GM = all rows streams each
+    // column tile's operand once (large operands stay L2-friendly).
+    const int GM = p.interleave_gm;
+    const int per_super = GM * p.interleave_nt;
+    const int sr = tile / per_super;
+    const int m_lo = sr * GM;
+    const int gm = min(GM, p.grp[0].tiles_m - m_lo);
+    const int r = tile - sr * per_super;
+    int nt = r / gm;
+    const int mt = m_lo + (r - nt * gm);
+    int g = 0;
+    while (nt >= p.grp[g].tiles_n) {
+      nt -= p.grp[g].tiles_n;
+      ++g;
+    }
+    TileCoord c;
+    c.g = g;
+    c.m0 = mt * ROWS;
+    c.n0 = nt * BN;
+    return c;
+  }
+  int g = p.interleave_groups;
   while (g + 1 < p.num_groups && tile >= p.grp[g + 1].tile_begin) ++g;
   const GemmGroup& G = p.grp[g];
   const int local = tile - G.tile_begin;
   TileCoord c;
   c.g = g;
-  c.m0 = (local % G.tiles_m) * BM;
+  c.m0 = (local % G.tiles_m) * ROWS;
   c.n0 = (local / G.tiles_m) * BN;
   return c;
+}
+
+__device__ __forceinline__ TileCoord decode_tile(const TcGemmParams& p, int tile) {
+  return decode_tile_rows<BM>(p, tile);
 }
 
 // ---------------------------------------------------------------------------
@@ -450,6 +486,7 @@ __device__ __forceinline__ void epilogue_chunk(const GemmGroup& G, uint4* st, in
 // ---------------------------------------------------------------------------
 constexpr int kSchedSlots = 64;
 __device__ int g_sched[2 * kSchedSlots];
+__device__ int g_dep[kSchedSlots * kMaxCounters];
 
 // ---------------------------------------------------------------------------
 // The kernel
@@ -508,6 +545,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
   const WaitCtx wctx{abort_flag, p.err, p.wait_limit_ns};
   const uint32_t tiles_base = smem_addr(smem);
   int* sched = g_sched + 2 * p.sched_slot;
+  int* dep = g_dep + kMaxCounters * p.sched_slot;
 
   if (warp == 0 && lane == 0) {
     // ---------------------- tile scheduler + TMA producer ----------------------
@@ -532,9 +570,33 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
       if (t < 0) break;
       const TileCoord tc = decode_tile(p, t);
       const GemmGroup& G = p.grp[tc.g];
+      if (G.dep_kind != DEP_NONE) {
+        // wait (bounded) until the tiles this one reads have been stored
+        const int* ctr = dep + G.dep_base + (G.dep_kind == DEP_ROW ? tc.m0 / BM : tc.m0 / BN);
+        if (ld_acquire_gpu(ctr) < G.dep_target) {
+          const unsigned long long t0 = global_ns();
+          while (ld_acquire_gpu(ctr) < G.dep_target) {
+            if (*abort_flag) {
+              ok = false;
+              break;
+            }
+            if (global_ns() - t0 > p.wait_limit_ns) {
+              *abort_flag = 1;
+              atomicOr(p.err, kErrTimeout);
+              ok = false;
+              break;
+            }
+            __nanosleep(128);
+          }
+        }
+        // order the TMA (async proxy) reads after the acquire
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+      }
       for (int s = G.seg_begin; ok && s < G.seg_end; ++s) {
         const TcSeg& S = p.seg[s];
         const int nk = (S.K + BK - 1) / BK;
+        const uint32_t stage_bytes =
+            A_TILE_BYTES + (S.n_mma == BN ? B_TILE_BYTES : static_cast<uint32_t>(S.n_mma) * BK * 2);
         for (int kb = 0; kb < nk; ++kb) {
           if (!wait_bounded(empty_bar(stage), phase ^ 1u, wctx)) {
             ok = false;
@@ -546,7 +608,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
             // Injected fault: this stage is never filled, so the consumer's
             // bounded wait on it expires.
           } else {
-            mbar_arrive_expect_tx(full_bar(stage), STAGE_BYTES);
+            mbar_arrive_expect_tx(full_bar(stage), stage_bytes);
             pending_phase[stage] = static_cast<int>(phase);
             const int k0 = kb * BK;
             if (S.a_mn) {
@@ -555,7 +617,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
             } else {
               tma_load_2d(a_dst, &p.mapA[s], full_bar(stage), k0, tc.m0);
             }
-            if (S.b_mn) {
+            if (S.b_fixed) {
+              tma_load_2d(b_dst, &p.mapB[s], full_bar(stage), 0, 0);
+            } else if (S.b_mn) {
 #pragma unroll
               for (int j = 0; j < BN / 64; ++j)
                 tma_load_2d(b_dst + j * MN_BOX_BYTES, &p.mapB[s], full_bar(stage), tc.n0 + 64 * j,
@@ -607,7 +671,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
       for (int s = G.seg_begin; ok && s < G.seg_end; ++s) {
         const TcSeg& S = p.seg[s];
         const int nk = (S.K + BK - 1) / BK;
-        const uint32_t idesc = idesc_bf16(S.a_mn, S.b_mn);
+        const uint32_t idesc = idesc_bf16(S.a_mn, S.b_mn, S.n_mma);
         for (int kb = 0; kb < nk; ++kb) {
           if (!wait_bounded(full_bar(stage), phase, wctx)) {
             ok = false;
@@ -684,6 +748,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
         epilogue_chunk(G, epi_stage, lane, row0, n, v);
       }
       tc_fence_before();
+      if (G.prod_row >= 0 || G.prod_col >= 0) {
+        // make this warp's stores visible GPU-wide, then count the tile part
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) {
+          if (G.prod_row >= 0) atomicAdd(dep + G.prod_row + tc.m0 / BM, 1);
+          if (G.prod_col >= 0) atomicAdd(dep + G.prod_col + tc.n0 / BN, 1);
+        }
+      }
       __syncwarp();
       if (lane == 0) mbar_arrive(tempty_bar(buf));
     }
@@ -702,6 +775,461 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
     // The last CTA to finish resets this launch slot's counters.
     __threadfence();
     if (atomicAdd(sched + 1, 1) == static_cast<int>(gridDim.x) - 1) {
+      for (int c = 0; c < p.num_counters; ++c) atomicExch(dep + c, 0);
+      atomicExch(sched, 0);
+      atomicExch(sched + 1, 0);
+    }
+  }
+}
+
+// ===========================================================================
+// Two-SM variant: a cluster of two CTAs computes a 256 x 256 tile with
+// tcgen05.mma.cta_group::2.  Each CTA stages its own 128 rows of A and its own
+// 128 columns of B, so a stage is 32 KB instead of 48 KB and six stages fit;
+// the two SMs' tensor cores share one instruction issued by the leader
+// (cluster rank 0).  Each CTA's TMEM holds the accumulator of its 128 rows,
+// and each CTA runs the same epilogue as the one-SM kernel on its rows.
+//
+// Coordination (all waits bounded):
+//   leader producer   claims tiles, writes each tile id into both CTAs' rings,
+//                     expects both halves' bytes on its full[s]
+//   both producers    TMA their halves into their own smem; the copies of
+//                     both CTAs complete on the leader's full[s]
+//   leader MMA        waits full[s], issues the pair MMA, commits (multicast
+//                     to both CTAs) to empty[s] and to tfull[b]
+//   both epilogues    read their TMEM rows, then arrive on the leader's tempty[b]
+// A cluster barrier at the end keeps both CTAs' shared memory alive until
+// neither touches the other's any more.
+// ===========================================================================
+constexpr int BM2 = 256;                           // rows per pair tile
+constexpr int STAGES2 = 6;
+constexpr int B_HALF_BYTES = 128 * BK * 2;          // 16 KB
+constexpr int STAGE2_BYTES = A_TILE_BYTES + B_HALF_BYTES;
+constexpr int SMEM2_BYTES =
+    STAGES2 * STAGE2_BYTES + BAR_BYTES + NUM_EPI_WARPS * EPI_STAGE_BYTES + 1024;
+
+// TMA load into this CTA's shared memory whose completion is signalled on an
+// mbarrier that may live in the peer CTA of the pair (cluster address).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map,
+                                                 uint32_t bar_cluster, int c0, int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(c0), "r"(c1)
+      : "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// Shared-memory address of the same object in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ void st_cluster_u32(uint32_t cluster_addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+
+struct WaitCtx2 {
+  volatile int* abort_flag;
+  uint32_t peer_abort;  // cluster address of the peer's abort flag
+  unsigned* err;
+  unsigned long long limit_ns;
+};
+
+__device__ __forceinline__ void raise_abort2(const WaitCtx2& w, bool timed_out) {
+  *w.abort_flag = 1;
+  st_cluster_u32(w.peer_abort, 1u);
+  if (timed_out) atomicOr(w.err, kErrTimeout);
+}
+
+// Bounded wait with cluster-scope acquire (the phase may be completed by the
+// peer CTA).  Returns false on abort or timeout.
+__device__ __forceinline__ bool wait2(uint32_t bar, uint32_t parity, const WaitCtx2& w) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const unsigned long long t0 = global_ns();
+  while (true) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if (*w.abort_flag) return false;
+    if (global_ns() - t0 > w.limit_ns) {
+      raise_abort2(w, true);
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ void mma_bf16_pair(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                              uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrives on the mbarrier at `bar` in both CTAs of the pair once all prior
+// MMAs of this thread have completed.
+__device__ __forceinline__ void mma_commit_pair(uint32_t bar, uint16_t mask = 0x3) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(bar),
+      "h"(mask)
+      : "memory");
+}
+
+__device__ __forceinline__ uint32_t idesc_bf16_m256(int a_mn, int b_mn, int n) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(a_mn) << 15) |
+         (static_cast<uint32_t>(b_mn) << 16) | (static_cast<uint32_t>(n >> 3) << 17) |
+         (static_cast<uint32_t>(BM2 >> 4) << 24);
+}
+
+__global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_pair_kernel(const __grid_constant__ TcGemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES2 * STAGE2_BYTES);
+  // bars: full[S], empty[S], tfull[2], tempty[2], drain, tile_full[R], tile_empty[R]
+  constexpr int kBarCount = 2 * STAGES2 + 5 + 2 * TILE_RING;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kBarCount);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + kBarCount + 1);
+  volatile int* tile_ids = reinterpret_cast<volatile int*>(bars + kBarCount + 2);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_rank();
+  const uint32_t peer = rank ^ 1u;
+  const bool leader = rank == 0;
+  const uint32_t bar0 = smem_addr(bars);
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES2 + s); };
+  auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * STAGES2 + b); };
+  auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * STAGES2 + 2 + b); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * STAGES2 + 4);
+  auto tile_full_bar = [&](int r) { return bar0 + 8u * (2 * STAGES2 + 5 + r); };
+  auto tile_empty_bar = [&](int r) { return bar0 + 8u * (2 * STAGES2 + 5 + TILE_RING + r); };
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES2; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(tfull_bar(b), 1);
+      mbar_init(tempty_bar(b), 2 * NUM_EPI_WARPS);
+    }
+    mbar_init(drain_bar, 1);
+    for (int r = 0; r < TILE_RING; ++r) {
+      mbar_init(tile_full_bar(r), 1);
+      // leader: its MMA thread and epilogue warps; peer: its producer and epilogue warps
+      mbar_init(tile_empty_bar(r), 2 * (1 + NUM_EPI_WARPS));
+    }
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_addr(tmem_slot)),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();  // both CTAs' barriers are initialised before any remote arrive
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const WaitCtx2 wctx{abort_flag, map_to_rank(smem_addr(const_cast<int*>(abort_flag)), peer), p.err,
+                      p.wait_limit_ns};
+  const uint32_t tiles_base = smem_addr(smem);
+  int* sched = g_sched + 2 * p.sched_slot;
+  int* dep = g_dep + kMaxCounters * p.sched_slot;
+  const uint32_t tile_ids_addr = smem_addr(const_cast<int*>(tile_ids));
+
+  // Every role reads the i-th tile id from its CTA's ring, then releases the
+  // slot on the leader's tile_empty barrier.
+  auto take_tile = [&](int i, int& t) -> bool {
+    const int r = i % TILE_RING;
+    if (!wait2(tile_full_bar(r), static_cast<uint32_t>((i / TILE_RING) & 1), wctx)) return false;
+    t = tile_ids[r];
+    return true;
+  };
+  auto release_tile = [&](int i) {
+    const int r = i % TILE_RING;
+    if (leader) mbar_arrive(tile_empty_bar(r));
+    else mbar_arrive_remote(map_to_rank(tile_empty_bar(r), 0));
+  };
+
+  if (warp == 0 && lane == 0) {
+    // --------------- tile scheduler (leader) + TMA producer (both) ---------------
+    for (int s = 0; s < p.num_segs; ++s) {
+      prefetch_tmap(&p.mapA[s]);
+      prefetch_tmap(&p.mapB[s]);
+    }
+    int stage = 0;
+    uint32_t phase = 0;
+    int pending_phase[STAGES2];
+    for (int s = 0; s < STAGES2; ++s) pending_phase[s] = -1;
+    bool first = true;
+    bool ok = true;
+    int claim = blockIdx.x >> 1;  // the cluster's first tile
+    for (int i = 0; ok; ++i) {
+      int t;
+      if (leader) {
+        const int r = i % TILE_RING;
+        if (!wait2(tile_empty_bar(r), static_cast<uint32_t>((i / TILE_RING) & 1) ^ 1u, wctx)) break;
+        t = claim < p.total_tiles ? claim : -1;
+        tile_ids[r] = t;
+        st_cluster_u32(map_to_rank(tile_ids_addr + 4u * r, peer), static_cast<uint32_t>(t));
+        mbar_arrive(tile_full_bar(r));
+        mbar_arrive_remote(map_to_rank(tile_full_bar(r), peer));
+      } else {
+        if (!take_tile(i, t)) break;
+        release_tile(i);
+      }
+      if (t < 0) break;
+      const TileCoord tc = decode_tile_rows<BM2>(p, t);
+      const GemmGroup& G = p.grp[tc.g];
+      const int row0 = tc.m0 + 128 * static_cast<int>(rank);  // this CTA's rows
+      if (G.dep_kind != DEP_NONE) {
+        const int* ctr = dep + G.dep_base + (G.dep_kind == DEP_ROW ? row0 / BM : tc.m0 / BN);
+        if (ld_acquire_gpu(ctr) < G.dep_target) {
+          const unsigned long long t0 = global_ns();
+          while (ld_acquire_gpu(ctr) < G.dep_target) {
+            if (*abort_flag) {
+              ok = false;
+              break;
+            }
+            if (global_ns() - t0 > p.wait_limit_ns) {
+              raise_abort2(wctx, true);
+              ok = false;
+              break;
+            }
+            __nanosleep(128);
+          }
+        }
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+      }
+      for (int s = G.seg_begin; ok && s < G.seg_end; ++s) {
+        const TcSeg& S = p.seg[s];
+        const int nk = (S.K + BK - 1) / BK;
+        const uint32_t b_bytes = S.b_fixed ? static_cast<uint32_t>(S.n_mma / 2) * BK * 2 : B_HALF_BYTES;
+        const int ncol0 = tc.n0 + 128 * static_cast<int>(rank);  // this CTA's half of B
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!wait2(empty_bar(stage), phase ^ 1u, wctx)) {
+            ok = false;
+            break;
+          }
+          const uint32_t a_dst = tiles_base + stage * STAGE2_BYTES;
+          const uint32_t b_dst = a_dst + A_TILE_BYTES;
+          if (first && p.fault_skip) {
+            // Injected fault: this stage is never filled.
+          } else {
+            // both halves complete on the leader's full barrier
+            const uint32_t fb = map_to_rank(full_bar(stage), 0);
+            if (leader) {
+              mbar_arrive_expect_tx(full_bar(stage), 2 * (A_TILE_BYTES + b_bytes));
+              pending_phase[stage] = static_cast<int>(phase);
+            }
+            const int k0 = kb * BK;
+            if (S.a_mn) {
+              tma_load_2d_pair(a_dst, &p.mapA[s], fb, row0, k0);
+              tma_load_2d_pair(a_dst + MN_BOX_BYTES, &p.mapA[s], fb, row0 + 64, k0);
+            } else {
+              tma_load_2d_pair(a_dst, &p.mapA[s], fb, k0, row0);
+            }
+            if (S.b_fixed) {
+              tma_load_2d_pair(b_dst, &p.mapB[s], fb, 0, 0);
+            } else if (S.b_mn) {
+              tma_load_2d_pair(b_dst, &p.mapB[s], fb, ncol0, k0);
+              tma_load_2d_pair(b_dst + MN_BOX_BYTES, &p.mapB[s], fb, ncol0 + 64, k0);
+            } else {
+              tma_load_2d_pair(b_dst, &p.mapB[s], fb, k0, ncol0);
+            }
+          }
+          first = false;
+          if (++stage == STAGES2) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (leader) claim = static_cast<int>(gridDim.x >> 1) + atomicAdd(sched, 1);
+    }
+    if (*abort_flag) {
+      // Drain: the leader waits (bounded) until every stage it expected has
+      // landed, which covers both CTAs' copies of those stages; the peer,
+      // which cannot wait on the leader's barriers, lets a short fixed
+      // interval pass for its own copies in flight.
+      if (leader) {
+        for (int s = 0; s < STAGES2; ++s) {
+          if (pending_phase[s] < 0) continue;
+          const unsigned long long t0 = global_ns();
+          while (!mbar_try_wait(full_bar(s), static_cast<uint32_t>(pending_phase[s]))) {
+            if (global_ns() - t0 > p.wait_limit_ns) break;
+          }
+        }
+      } else {
+        const unsigned long long t0 = global_ns();
+        while (global_ns() - t0 < 200000ull) __nanosleep(1000);
+      }
+    }
+  } else if (warp == 1 && lane == 0 && leader) {
+    // ------------------------- leader: pair MMA issuer -------------------------
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    bool issued_any = false;
+    for (int lt = 0; ok; ++lt) {
+      int tile;
+      if (!take_tile(lt, tile)) break;
+      release_tile(lt);
+      if (tile < 0) break;
+      const TileCoord tc = decode_tile_rows<BM2>(p, tile);
+      const GemmGroup& G = p.grp[tc.g];
+      const int buf = lt & 1;
+      const uint32_t tphase = static_cast<uint32_t>(lt >> 1) & 1u;
+      if (!wait2(tempty_bar(buf), tphase ^ 1u, wctx)) break;
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
+      uint32_t acc = 0;
+      for (int s = G.seg_begin; ok && s < G.seg_end; ++s) {
+        const TcSeg& S = p.seg[s];
+        const int nk = (S.K + BK - 1) / BK;
+        const uint32_t idesc = idesc_bf16_m256(S.a_mn, S.b_mn, S.n_mma);
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!wait2(full_bar(stage), phase, wctx)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_base = tiles_base + stage * STAGE2_BYTES;
+          const uint32_t b_base = a_base + A_TILE_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            const uint64_t ad = S.a_mn ? sdesc(a_base + kk * 2048, MN_BOX_BYTES, 1024)
+                                       : sdesc(a_base + kk * 32, 16, 1024);
+            const uint64_t bd = S.b_mn ? sdesc(b_base + kk * 2048, MN_BOX_BYTES, 1024)
+                                       : sdesc(b_base + kk * 32, 16, 1024);
+            mma_bf16_pair(d_tmem, ad, bd, idesc, acc);
+            acc = 1;
+          }
+          issued_any = true;
+          mma_commit_pair(empty_bar(stage));
+          if (++stage == STAGES2) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) break;
+      mma_commit_pair(tfull_bar(buf));
+    }
+    if (*abort_flag && issued_any) {
+      mma_commit_pair(drain_bar, 0x1);  // this CTA only
+      const unsigned long long t0 = global_ns();
+      while (!mbar_try_wait(drain_bar, 0)) {
+        if (global_ns() - t0 > p.wait_limit_ns) break;
+      }
+    }
+  } else if (warp >= 2) {
+    // ---------------------------- epilogue (both CTAs) ----------------------------
+    const int quarter = warp & 3;
+    const int c_begin = ((warp - 2) >> 2) * (BN / 64);
+    uint4* epi_stage = reinterpret_cast<uint4*>(smem + STAGES2 * STAGE2_BYTES + BAR_BYTES +
+                                                (warp - 2) * EPI_STAGE_BYTES);
+    const uint32_t tempty_leader0 = map_to_rank(tempty_bar(0), 0);
+    const uint32_t tempty_leader1 = map_to_rank(tempty_bar(1), 0);
+    for (int lt = 0;; ++lt) {
+      int tile;
+      if (!take_tile(lt, tile)) break;
+      __syncwarp();
+      if (lane == 0) release_tile(lt);
+      if (tile < 0) break;
+      const TileCoord tc = decode_tile_rows<BM2>(p, tile);
+      const GemmGroup& G = p.grp[tc.g];
+      const int buf = lt & 1;
+      const uint32_t tphase = static_cast<uint32_t>(lt >> 1) & 1u;
+      if (!wait2(tfull_bar(buf), tphase, wctx)) break;
+      tc_fence_after();
+      const int row0 = tc.m0 + 128 * static_cast<int>(rank) + quarter * 32;
+      const uint32_t taddr =
+          tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(buf * BN);
+      for (int c = c_begin; c < c_begin + BN / 64; ++c) {
+        const int n = tc.n0 + c * 32;
+        if (n >= G.N) break;  // warp-uniform
+        uint32_t rr[32];
+        float v[32];
+        if (G.k_empty) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] = 0.f;
+        } else {
+          tmem_ld32(taddr + static_cast<uint32_t>(c * 32), rr);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(rr[j]);
+        }
+        epilogue_chunk(G, epi_stage, lane, row0, n, v);
+      }
+      tc_fence_before();
+      if (G.prod_row >= 0 || G.prod_col >= 0) {
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) {
+          if (G.prod_row >= 0) atomicAdd(dep + G.prod_row + (tc.m0 + 128 * static_cast<int>(rank)) / BM, 1);
+          if (G.prod_col >= 0) atomicAdd(dep + G.prod_col + tc.n0 / BN, 1);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) {
+        if (leader) mbar_arrive(tempty_bar(buf));
+        else mbar_arrive_remote(buf ? tempty_leader1 : tempty_leader0);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();  // no CTA touches the other's shared memory after this
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                 "r"(TMEM_COLS)
+                 : "memory");
+  }
+  if (threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(sched + 1, 1) == static_cast<int>(gridDim.x) - 1) {
+      for (int c = 0; c < p.num_counters; ++c) atomicExch(dep + c, 0);
       atomicExch(sched, 0);
       atomicExch(sched + 1, 0);
     }
@@ -712,18 +1240,58 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
 
 cudaError_t launch_tc_gemm(const TcGemmParams& p_in, int num_sms, cudaStream_t s) {
   static bool attr_set = false;
+  static int max_clusters = 0;
   static unsigned slot_seq = 0;
   if (!attr_set) {
     cudaError_t e =
         cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(tc_gemm_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             SMEM2_BYTES);
+    if (e != cudaSuccess) return e;
+    // Every cluster of the persistent grid must be resident at once (tiles
+    // may wait on tiles other clusters hold), so size the grid by occupancy.
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(2 * (num_sms / 2), 1, 1);
+    cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = SMEM2_BYTES;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaOccupancyMaxActiveClusters(&max_clusters, tc_gemm_pair_kernel, &cfg);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
   if (p_in.total_tiles <= 0) return cudaSuccess;
   TcGemmParams& p = const_cast<TcGemmParams&>(p_in);
   p.sched_slot = static_cast<int>(slot_seq++ % kSchedSlots);
+  if (p.pair) {
+    int clusters = max_clusters < num_sms / 2 ? max_clusters : num_sms / 2;
+    if (clusters > p.total_tiles) clusters = p.total_tiles;
+    if (clusters < 1) return cudaErrorInvalidConfiguration;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(2 * clusters, 1, 1);
+    cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = SMEM2_BYTES;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, tc_gemm_pair_kernel, p);
+    count_launches(1);
+    return e != cudaSuccess ? e : cudaGetLastError();
+  }
   const int grid = p.total_tiles < num_sms ? p.total_tiles : num_sms;
   tc_gemm_kernel<<<grid, NUM_THREADS, SMEM_BYTES, s>>>(p);
+  count_launches(1);
   return cudaGetLastError();
 }
 

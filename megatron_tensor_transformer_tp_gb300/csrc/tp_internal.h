@@ -7,8 +7,10 @@
 
 namespace tp {
 
-constexpr int kMaxGroups = 32;    // independent output matrices in one GEMM launch
-constexpr int kMaxSegs = 32;      // (A, B) operand pairs summed into the outputs
+constexpr int kMaxGroups = 40;    // output matrices in one GEMM launch
+constexpr int kMaxSegs = 48;      // (A, B) operand pairs summed into the outputs
+constexpr int kEpiWarps = 8;      // epilogue warps of the tensor-core engine
+constexpr int kMaxCounters = 512; // tile-completion counters of one launch
 constexpr int kMaxRanges = 64;    // vocabulary ranges
 
 // Error bits of the device error word.
@@ -25,12 +27,22 @@ enum Epi : int {
 
 enum OutType : int { OUT_BF16 = 0, OUT_F32 = 1 };
 
+// Tile dependencies inside one launch.  A producing group counts finished
+// tiles per row block (prod_row + m-tile) and/or per column block (prod_col +
+// n-tile); a consuming group's tile waits until its counter reaches
+// dep_target: DEP_ROW uses counter dep_base + m-tile (same row tiling as the
+// producer), DEP_COL uses dep_base + m0 / 256 (its rows are the producer's
+// columns, as for a contraction over tokens of the producer's output).
+enum Dep : int { DEP_NONE = 0, DEP_ROW = 1, DEP_COL = 2 };
+
 // One output matrix D (M x N) = sum over its segments of A_s B_s^T.
 struct GemmGroup {
   int M, N;
   int seg_begin, seg_end;
   int epi, out_type, accumulate, vec_ok;
   int tiles_m, tiles_n, tile_begin, k_empty;  // k_empty: no k-blocks, D = 0
+  int dep_kind, dep_base, dep_target;
+  int prod_row, prod_col;                     // counter bases, -1 = none
   void* out;            // D, row pitch ldo (elements)
   void* out2;           // second output (GELU: Y), same pitch as out
   const void* aux;      // DGELU: Z, row pitch ld_aux
@@ -51,7 +63,9 @@ struct GemmGroup {
 struct TcSeg {
   int K;
   int a_mn, b_mn;
-  int pad;
+  int n_mma;    // MMA N: 256, or 16 for a column sum against the ones block
+  int b_fixed;  // B is the ones block: every k-block loads the same box
+  int pad[3];
 };
 
 struct TcGemmParams {
@@ -62,6 +76,12 @@ struct TcGemmParams {
   int num_groups, num_segs, total_tiles;
   int fault_skip;        // fault injection: producer skips its first stage
   int sched_slot;        // dynamic tile counter slot (set by the launcher)
+  int interleave_groups; // leading groups sharing one row tiling, enumerated in
+  int interleave_tiles;  // super-rows of interleave_gm row blocks: (super-row,
+  int interleave_nt;     // column tile across the groups, row block)
+  int interleave_gm;
+  int num_counters;
+  int pair;              // 1: two-SM kernel (256-row pair tiles), 0: one-SM kernel
   unsigned* err;         // device error word
   unsigned long long wait_limit_ns;
 };
@@ -88,16 +108,13 @@ struct RangeTable {
   int n;
 };
 
-// Shard pointer table for per-shard fp32 outputs of column sums.
-struct ShardOut {
-  float* p[kMaxGroups];
-  int64_t cols_per_shard;
-  int n;
-};
+// Every kernel launch the library makes is counted (reported by the profiler).
+void count_launches(int n);
 
 // Launchers (each returns the launch error).
 cudaError_t launch_tc_gemm(const TcGemmParams& p, int num_sms, cudaStream_t s);
 cudaError_t launch_simt_gemm(const SimtGemmParams& p, cudaStream_t s);
+cudaError_t launch_gelu_eval(const float* z, float* y, float* dy, int64_t n, cudaStream_t s);
 cudaError_t launch_embed_gather(const int64_t* ids, int64_t T, int64_t row_bytes,
                                 const RangeTable& rt, void* out, cudaStream_t s);
 // Grouping of tokens by id.  ws holds offsets[V+1], perm[T], counts[V].
@@ -108,9 +125,5 @@ int* sort_perm(void* ws, int64_t V);
 // Input-side embedding gradient alone: dE_r rows = segment sums (+ old).
 cudaError_t launch_segment_sum(const void* ws, int64_t V, int64_t T, const void* dEmb, int in_f32,
                                int64_t h, const RangeTable& dE, int accumulate, cudaStream_t s);
-// Deterministic column sums of src (M x ncols, pitch ld) into per-shard fp32 outputs.
-size_t colsum_workspace_bytes(int64_t M, int64_t ncols);
-cudaError_t launch_colsum(const void* src, int in_f32, int64_t M, int64_t ncols, int64_t ld,
-                          const ShardOut& out, int accumulate, void* ws, cudaStream_t s);
 
 }  // namespace tp

@@ -30,8 +30,7 @@ def run_attn(inp, bias=True):
     dWo = [torch.full((h, d), float("nan"), dtype=f, device="cuda") for _ in range(N)]
     dbq = [torch.full((3 * d,), float("nan"), dtype=f, device="cuda") for _ in range(N)] if bias else None
     dbo = torch.full((h,), float("nan"), dtype=f, device="cuda") if bias else None
-    ws = torch.empty(tp.tp_attn_proj_bwd_workspace_size(M, h), dtype=torch.uint8, device="cuda")
-    tp.tp_attn_proj_bwd(dQKV, dO, X, C, Wq, Wo, dX, dC, dWq, dbq, dWo, dbo, nh, workspace=ws)
+    tp.tp_attn_proj_bwd(dQKV, dO, X, C, Wq, Wo, dX, dC, dWq, dbq, dWo, dbo, nh)
     assert tp.tp_get_status() == tp.TP_OK
     return dict(QKV=QKV, O=Oo, dX=dX, dC=dC, dWqkv=dWq, dbqkv=dbq, dWo=dWo, dbo=dbo)
 

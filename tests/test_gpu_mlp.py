@@ -38,8 +38,7 @@ def run_mlp(inp, bias=True, accumulate=False, grads_init=None):
         db = torch.full((h,), float("nan"), dtype=f, device="cuda") if bias else None
     else:
         dW, dU, da, db = grads_init
-    ws = torch.empty(tp.tp_mlp_bwd_workspace_size(M, h, hp), dtype=torch.uint8, device="cuda")
-    tp.tp_mlp_bwd(dOut, X, W, U, Z, Y, dZ, dX, dW, da, dU, db, accumulate=accumulate, workspace=ws)
+    tp.tp_mlp_bwd(dOut, X, W, U, Z, Y, dZ, dX, dW, da, dU, db, accumulate=accumulate)
     assert tp.tp_get_status() == tp.TP_OK
     return dict(Z=Z, Y=Y, Out=Out, dZ=dZ, dX=dX, dW=dW, dU=dU, da=da, db=db)
 
