@@ -289,11 +289,12 @@ TP_API tp_status tp_gelu_eval(const float* z, float* y, float* dy, int64_t n, vo
  * the kernel returns early with TP_ERR_TIMEOUT recorded.  kind 0: off.
  * wait_limit_ms sets the bounded-wait limit (default 1000 ms). */
 TP_API void tp_debug_inject_fault(int kind);
-/* Selects the tensor-core GEMM kernel for bf16 work: 1 (default) the two-SM
- * kernel (CTA pairs computing 256 x 256 tiles with tcgen05 cta_group::2),
- * 0 the one-SM kernel (128 x 256 tiles).  Both give the same results up to
- * fp32 summation order; tests run both. */
-TP_API void tp_debug_set_gemm_kernel(int pair);
+/* Selects the tensor-core GEMM kernel for bf16 work: 0 the one-SM kernel
+ * (128 x 256 tiles), 1 the two-SM kernel (CTA pairs computing 256 x 256 tiles
+ * with tcgen05 cta_group::2), 2 (default) per launch: the two-SM kernel for
+ * large launches with MN-major operands, the one-SM kernel otherwise.  All
+ * give the same results up to fp32 summation order; tests run each. */
+TP_API void tp_debug_set_gemm_kernel(int mode);
 TP_API void tp_debug_set_wait_limit_ms(int ms);
 
 #ifdef __cplusplus

@@ -333,9 +333,9 @@ def tp_debug_inject_fault(kind: int):
     lib().tp_debug_inject_fault(int(kind))
 
 
-def tp_debug_set_gemm_kernel(pair: int):
-    """1: two-SM tensor-core kernel (default), 0: one-SM kernel."""
-    lib().tp_debug_set_gemm_kernel(int(pair))
+def tp_debug_set_gemm_kernel(mode: int):
+    """0: one-SM tensor-core kernel, 1: two-SM kernel, 2: per launch (default)."""
+    lib().tp_debug_set_gemm_kernel(int(mode))
 
 
 def tp_debug_set_wait_limit_ms(ms: int):

@@ -43,7 +43,7 @@ DeviceState g_dev[kMaxDevices];
 std::mutex g_mu;
 
 int g_fault_kind = 0;
-int g_use_pair = 1;  // 1: two-SM GEMM kernel for bf16, 0: one-SM kernel
+int g_gemm_mode = 2;  // 0: one-SM kernel, 1: two-SM kernel, 2: choose per launch
 unsigned long long g_wait_limit_ns = 1000ull * 1000ull * 1000ull;
 
 tp_status device_state(DeviceState** out) {
@@ -177,6 +177,23 @@ bool encode_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols, int
   cuuint32_t box[2] = {64, box_rows};
   cuuint32_t estr[2] = {1, 1};
   return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), gdim, gstride, box,
+                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// An MN-major bf16 matrix (rows = K, cols = MN, MN a multiple of 64) as a 3D
+// map (64 MN, K rows, MN / 64 blocks) whose (64, 64, nblocks) box lands in
+// shared memory as nblocks consecutive (64 x 64) blocks, the layout of the
+// per-block 2D boxes.  Returns false if the driver rejects the map.
+bool encode_map_mn3d(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols, int64_t ld,
+                     uint32_t nblocks) {
+  if (cols % 64 != 0) return false;
+  cuuint64_t gdim[3] = {64, static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(cols / 64)};
+  cuuint64_t gstride[2] = {static_cast<cuuint64_t>(ld) * 2, 128};
+  cuuint32_t box[3] = {64, 64, nblocks};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), gdim, gstride, box,
                   estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
@@ -340,7 +357,22 @@ tp_status launch_tc_groups(const Plan& pl, const bool* used, GemmGroup* groups, 
                            int interleave, int ncounters, const DeviceState* dev, const char* name,
                            cudaStream_t s, bool longest_first) {
   if (ng == 0) return TP_OK;
-  const bool pair = g_use_pair != 0;
+  // Kernel choice (measured on GB300): the two-SM kernel (256 x 256 pair tiles,
+  // 6-stage ring) is faster on large launches whose operands include MN-major
+  // (transposed) matrices, the backward and weight-gradient contractions; the
+  // one-SM kernel (128 x 256 tiles) on K-major launches and on small ones,
+  // where its finer tiles balance better.
+  bool pair = g_gemm_mode == 1;
+  if (g_gemm_mode == 2) {
+    bool has_mn = false;
+    int64_t tiles128 = 0;
+    for (int i = 0; i < ng; ++i) {
+      tiles128 += static_cast<int64_t>((groups[i].M + 127) / 128) * ((groups[i].N + 255) / 256);
+      for (int sidx = groups[i].seg_begin; sidx < groups[i].seg_end; ++sidx)
+        has_mn = has_mn || pl.seg[sidx].A.mn || pl.seg[sidx].B.mn;
+    }
+    pair = has_mn && tiles128 > 8 * static_cast<int64_t>(dev->num_sms);
+  }
   if (longest_first) {
     // stable: longest contraction first
     for (int i = 1; i < ng; ++i) {
@@ -364,15 +396,23 @@ tp_status launch_tc_groups(const Plan& pl, const bool* used, GemmGroup* groups, 
     p.seg[i].n_mma = S.B.ones ? 16 : 256;
     p.seg[i].b_fixed = S.B.ones;
     if (!used[i]) continue;
-    // K-major boxes are (64 K) x (128 or 256 rows); MN-major boxes (64 MN) x (64 K);
-    // the ones block is one (64 K) x (16 rows) box.
-    if (!encode_map(&p.mapA[i], S.A.ptr, S.A.rows, S.A.cols, S.A.ld, S.A.mn ? 64 : 128))
+    // K-major boxes are (64 K) x (128 or 256 rows); MN-major operands use one 3D
+    // box per stage when their width is a multiple of 64, else (64 MN) x (64 K)
+    // 2D boxes; the ones block is one (64 K) x (16 rows) box.  The two-SM
+    // kernel stages half of a 256-wide B tile per CTA.
+    const uint32_t b_rows = pair ? 128 : 256;
+    if (S.A.mn && encode_map_mn3d(&p.mapA[i], S.A.ptr, S.A.rows, S.A.cols, S.A.ld, 2)) {
+      p.seg[i].a_3d = 1;
+    } else if (!encode_map(&p.mapA[i], S.A.ptr, S.A.rows, S.A.cols, S.A.ld, S.A.mn ? 64 : 128)) {
       return TP_ERR_CUDA;
-    // the two-SM kernel stages half of a 256-wide B tile per CTA
-    const bool ok = S.B.ones ? encode_map(&p.mapB[i], dev->ones_bf16, 16, 64, 64, 16)
-                             : encode_map(&p.mapB[i], S.B.ptr, S.B.rows, S.B.cols, S.B.ld,
-                                          S.B.mn ? 64 : (pair ? 128 : 256));
-    if (!ok) return TP_ERR_CUDA;
+    }
+    if (S.B.ones) {
+      if (!encode_map(&p.mapB[i], dev->ones_bf16, 16, 64, 64, 16)) return TP_ERR_CUDA;
+    } else if (S.B.mn && encode_map_mn3d(&p.mapB[i], S.B.ptr, S.B.rows, S.B.cols, S.B.ld, b_rows / 64)) {
+      p.seg[i].b_3d = 1;
+    } else if (!encode_map(&p.mapB[i], S.B.ptr, S.B.rows, S.B.cols, S.B.ld, S.B.mn ? 64 : b_rows)) {
+      return TP_ERR_CUDA;
+    }
     if (pair && S.B.ones) p.seg[i].n_mma = 32;  // 16 rows of ones per CTA
   }
   int tiles = 0, inter_nt = 0;
@@ -893,7 +933,7 @@ extern "C" tp_status tp_gelu_eval(const float* z, float* y, float* dy, int64_t n
 
 extern "C" void tp_debug_inject_fault(int kind) { g_fault_kind = kind; }
 
-extern "C" void tp_debug_set_gemm_kernel(int pair) { g_use_pair = pair != 0; }
+extern "C" void tp_debug_set_gemm_kernel(int mode) { g_gemm_mode = (mode >= 0 && mode <= 2) ? mode : 2; }
 
 extern "C" void tp_debug_set_wait_limit_ms(int ms) {
   g_wait_limit_ns = static_cast<unsigned long long>(ms > 0 ? ms : 1000) * 1000000ull;

@@ -123,6 +123,26 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// 3D tile load: an MN-major operand viewed as (64 MN, K rows, MN / 64 blocks);
+// one box brings all of a tile's 64-wide blocks, stacked 8 KB apart.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int c0, int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap* map,
+                                                 uint32_t bar_cluster, int c0, int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -611,7 +631,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
             mbar_arrive_expect_tx(full_bar(stage), stage_bytes);
             pending_phase[stage] = static_cast<int>(phase);
             const int k0 = kb * BK;
-            if (S.a_mn) {
+            if (S.a_3d) {
+              tma_load_3d(a_dst, &p.mapA[s], full_bar(stage), 0, k0, tc.m0 / 64);
+            } else if (S.a_mn) {
               tma_load_2d(a_dst, &p.mapA[s], full_bar(stage), tc.m0, k0);
               tma_load_2d(a_dst + MN_BOX_BYTES, &p.mapA[s], full_bar(stage), tc.m0 + 64, k0);
             } else {
@@ -619,6 +641,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
             }
             if (S.b_fixed) {
               tma_load_2d(b_dst, &p.mapB[s], full_bar(stage), 0, 0);
+            } else if (S.b_3d) {
+              tma_load_3d(b_dst, &p.mapB[s], full_bar(stage), 0, k0, tc.n0 / 64);
             } else if (S.b_mn) {
 #pragma unroll
               for (int j = 0; j < BN / 64; ++j)
@@ -1061,7 +1085,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_pair_kernel(const __gr
               pending_phase[stage] = static_cast<int>(phase);
             }
             const int k0 = kb * BK;
-            if (S.a_mn) {
+            if (S.a_3d) {
+              tma_load_3d_pair(a_dst, &p.mapA[s], fb, 0, k0, row0 / 64);
+            } else if (S.a_mn) {
               tma_load_2d_pair(a_dst, &p.mapA[s], fb, row0, k0);
               tma_load_2d_pair(a_dst + MN_BOX_BYTES, &p.mapA[s], fb, row0 + 64, k0);
             } else {
@@ -1069,6 +1095,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_pair_kernel(const __gr
             }
             if (S.b_fixed) {
               tma_load_2d_pair(b_dst, &p.mapB[s], fb, 0, 0);
+            } else if (S.b_3d) {
+              tma_load_3d_pair(b_dst, &p.mapB[s], fb, 0, k0, ncol0 / 64);
             } else if (S.b_mn) {
               tma_load_2d_pair(b_dst, &p.mapB[s], fb, ncol0, k0);
               tma_load_2d_pair(b_dst + MN_BOX_BYTES, &p.mapB[s], fb, ncol0 + 64, k0);

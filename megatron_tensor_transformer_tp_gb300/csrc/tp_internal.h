@@ -65,7 +65,8 @@ struct TcSeg {
   int a_mn, b_mn;
   int n_mma;    // MMA N: 256, or 16 for a column sum against the ones block
   int b_fixed;  // B is the ones block: every k-block loads the same box
-  int pad[3];
+  int a_3d, b_3d;  // MN-major operand mapped in 3D: one box covers all its 64-wide blocks
+  int pad;
 };
 
 struct TcGemmParams {
