@@ -373,6 +373,12 @@ tp_status launch_tc_groups(const Plan& pl, const bool* used, GemmGroup* groups, 
     }
     pair = has_mn && tiles128 > 8 * static_cast<int64_t>(dev->num_sms);
   }
+  // Tile width: 256 for every output.  (128-wide tiles for the long dependent
+  // contractions of small fused launches were measured slower on GB300: a
+  // 128-wide MMA is bound by shared-memory bandwidth and doubles A traffic.)
+  int seg_bn[kMaxSegs];
+  for (int i = 0; i < pl.ns; ++i) seg_bn[i] = 256;
+  for (int i = 0; i < ng; ++i) groups[i].bn = 256;
   if (longest_first) {
     // stable: longest contraction first
     for (int i = 1; i < ng; ++i) {
@@ -393,14 +399,14 @@ tp_status launch_tc_groups(const Plan& pl, const bool* used, GemmGroup* groups, 
     p.seg[i].K = static_cast<int>(S.K);
     p.seg[i].a_mn = S.A.mn;
     p.seg[i].b_mn = S.B.mn;
-    p.seg[i].n_mma = S.B.ones ? 16 : 256;
+    p.seg[i].n_mma = S.B.ones ? 16 : seg_bn[i];
     p.seg[i].b_fixed = S.B.ones;
     if (!used[i]) continue;
     // K-major boxes are (64 K) x (128 or 256 rows); MN-major operands use one 3D
     // box per stage when their width is a multiple of 64, else (64 MN) x (64 K)
     // 2D boxes; the ones block is one (64 K) x (16 rows) box.  The two-SM
     // kernel stages half of a 256-wide B tile per CTA.
-    const uint32_t b_rows = pair ? 128 : 256;
+    const uint32_t b_rows = pair ? 128 : static_cast<uint32_t>(seg_bn[i]);
     if (S.A.mn && encode_map_mn3d(&p.mapA[i], S.A.ptr, S.A.rows, S.A.cols, S.A.ld, 2)) {
       p.seg[i].a_3d = 1;
     } else if (!encode_map(&p.mapA[i], S.A.ptr, S.A.rows, S.A.cols, S.A.ld, S.A.mn ? 64 : 128)) {
@@ -421,7 +427,7 @@ tp_status launch_tc_groups(const Plan& pl, const bool* used, GemmGroup* groups, 
   for (int i = 0; i < ng; ++i) {
     GemmGroup& g = groups[i];
     g.tiles_m = (g.M + rows_per_tile - 1) / rows_per_tile;
-    g.tiles_n = (g.N + 255) / 256;
+    g.tiles_n = (g.N + g.bn - 1) / g.bn;
     g.vec_ok = group_vec_ok(g, 2);
     if (i < interleave) {
       if (g.tiles_m != groups[0].tiles_m) return TP_ERR_INVALID;

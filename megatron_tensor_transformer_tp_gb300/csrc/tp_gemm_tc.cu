@@ -251,7 +251,7 @@ __device__ __forceinline__ TileCoord decode_tile_rows(const TcGemmParams& p, int
   TileCoord c;
   c.g = g;
   c.m0 = (local % G.tiles_m) * ROWS;
-  c.n0 = (local / G.tiles_m) * BN;
+  c.n0 = (local / G.tiles_m) * G.bn;
   return c;
 }
 
@@ -615,8 +615,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
       for (int s = G.seg_begin; ok && s < G.seg_end; ++s) {
         const TcSeg& S = p.seg[s];
         const int nk = (S.K + BK - 1) / BK;
-        const uint32_t stage_bytes =
-            A_TILE_BYTES + (S.n_mma == BN ? B_TILE_BYTES : static_cast<uint32_t>(S.n_mma) * BK * 2);
+        const uint32_t stage_bytes = A_TILE_BYTES + static_cast<uint32_t>(S.n_mma) * BK * 2;
         for (int kb = 0; kb < nk; ++kb) {
           if (!wait_bounded(empty_bar(stage), phase ^ 1u, wctx)) {
             ok = false;
@@ -644,8 +643,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
             } else if (S.b_3d) {
               tma_load_3d(b_dst, &p.mapB[s], full_bar(stage), 0, k0, tc.n0 / 64);
             } else if (S.b_mn) {
-#pragma unroll
-              for (int j = 0; j < BN / 64; ++j)
+              for (int j = 0; j < S.n_mma / 64; ++j)
                 tma_load_2d(b_dst + j * MN_BOX_BYTES, &p.mapB[s], full_bar(stage), tc.n0 + 64 * j,
                             k0);
             } else {
@@ -739,7 +737,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
     const int quarter = warp & 3;              // TMEM lanes this warp may access
     uint4* epi_stage = reinterpret_cast<uint4*>(smem + STAGES * STAGE_BYTES + BAR_BYTES +
                                                 (warp - 2) * EPI_STAGE_BYTES);
-    const int c_begin = ((warp - 2) >> 2) * (BN / 64);  // first of its 4 column chunks
+    const int half = (warp - 2) >> 2;  // which half of the tile's columns
     for (int lt = 0;; ++lt) {
       const int r = lt % TILE_RING;
       if (!wait_bounded(tile_full_bar(r), static_cast<uint32_t>((lt / TILE_RING) & 1), wctx)) break;
@@ -756,7 +754,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
       const int row0 = tc.m0 + quarter * 32;
       const uint32_t taddr =
           tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(buf * BN);
-      for (int c = c_begin; c < c_begin + BN / 64; ++c) {
+      const int cpw = G.bn / 64;  // 32-column chunks per warp
+      const int c_begin = half * cpw;
+      for (int c = c_begin; c < c_begin + cpw; ++c) {
         const int n = tc.n0 + c * 32;
         if (n >= G.N) break;  // warp-uniform
         uint32_t rr[32];

@@ -43,6 +43,7 @@ struct GemmGroup {
   int tiles_m, tiles_n, tile_begin, k_empty;  // k_empty: no k-blocks, D = 0
   int dep_kind, dep_base, dep_target;
   int prod_row, prod_col;                     // counter bases, -1 = none
+  int bn;                                     // tile width: 256, or 128 (one-SM kernel)
   void* out;            // D, row pitch ldo (elements)
   void* out2;           // second output (GELU: Y), same pitch as out
   const void* aux;      // DGELU: Z, row pitch ld_aux
