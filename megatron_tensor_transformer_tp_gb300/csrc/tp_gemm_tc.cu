@@ -12,11 +12,13 @@
 // ColumnParallelLinear and RowParallelLinear; "Megatron tensor / model
 // parallelism" notes, section MLP层的通讯量分析).
 //
-// CTA layout (320 threads):
-//   warp 0      tile scheduler + TMA producer (one lane)
-//   warp 1      TMEM allocator + MMA issuer (one lane)
-//   warps 2..9  epilogue: TMEM -> registers -> fused op -> global; two warps
-//               per TMEM lane quarter, each taking half of the tile's columns
+// CTA layout (576 threads):
+//   warp 0       tile scheduler + TMA producer (one lane)
+//   warp 1       TMEM allocator + MMA issuer (one lane)
+//   warps 2..17  epilogue: TMEM -> registers -> fused op -> global; four warps
+//                per TMEM lane quarter, each taking a quarter of the tile's
+//                columns (enough warps per SM sub-partition to hide the
+//                latency of the GELU / GELU' arithmetic and the stores)
 // Tile 128 x 256 x 64, 4-stage smem ring, two TMEM accumulators (2 x 256
 // columns) so the epilogue of one tile overlaps the main loop of the next.
 // Tiles are handed out dynamically: each CTA starts with tile blockIdx.x and
@@ -46,14 +48,16 @@ constexpr int A_TILE_BYTES = BM * BK * 2;  // 16 KB
 constexpr int B_TILE_BYTES = BN * BK * 2;  // 32 KB
 constexpr int STAGE_BYTES = A_TILE_BYTES + B_TILE_BYTES;
 constexpr int TMEM_COLS = 2 * BN;  // two fp32 accumulators
-constexpr int NUM_EPI_WARPS = kEpiWarps;  // two per SM sub-partition, each half the columns
+constexpr int NUM_EPI_WARPS = kEpiWarps;  // four per TMEM lane quarter, each a quarter of the columns
+constexpr int EPI_PARTS = NUM_EPI_WARPS / 4;  // column parts of a tile
 constexpr int NUM_THREADS = 64 + 32 * NUM_EPI_WARPS;
 constexpr int TILE_RING = 4;      // tile ids handed from the producer to the other roles
 constexpr int MN_BOX_BYTES = 64 * BK * 2;  // one 64(MN) x 64(K) box: 8 KB
 constexpr int BAR_BYTES = 512;
-constexpr int EPI_STAGE_BYTES = 32 * 32 * 4;  // per epilogue warp: one 32x32 fp32 chunk
+constexpr int EPI_STAGE_BYTES = 32 * 64;  // per epilogue warp: 32 rows x 64 bytes
+constexpr int EPI_WARP_BYTES = EPI_STAGE_BYTES;
 constexpr int SMEM_BYTES =
-    STAGES * STAGE_BYTES + BAR_BYTES + NUM_EPI_WARPS * EPI_STAGE_BYTES + 1024;  // + alignment slack
+    STAGES * STAGE_BYTES + BAR_BYTES + NUM_EPI_WARPS * EPI_WARP_BYTES + 1024;  // + alignment slack
 
 // ---------------------------------------------------------------------------
 // PTX wrappers
@@ -340,19 +344,24 @@ __device__ __forceinline__ void stage_store_rows(uint4* st, void* base, int out_
                                   static_cast<int64_t>(row0 + r) * ld + n + c * 8) = w;
     }
   } else {
+    // two 16-column halves, each 32 rows x 64 bytes
 #pragma unroll
-    for (int c = 0; c < 8; ++c)
-      st[lane * 8 + (c ^ (lane & 7))] =
-          make_uint4(__float_as_uint(v[4 * c + 0]), __float_as_uint(v[4 * c + 1]),
-                     __float_as_uint(v[4 * c + 2]), __float_as_uint(v[4 * c + 3]));
-    __syncwarp();
+    for (int hh = 0; hh < 2; ++hh) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int r = i * 4 + (lane >> 3), c = lane & 7;
-      const uint4 w = st[r * 8 + (c ^ (r & 7))];
-      if (row0 + r < M)
-        *reinterpret_cast<uint4*>(static_cast<float*>(base) + static_cast<int64_t>(row0 + r) * ld +
-                                  n + c * 4) = w;
+      for (int c = 0; c < 4; ++c)
+        st[lane * 4 + (c ^ ((lane >> 1) & 3))] =
+            make_uint4(__float_as_uint(v[16 * hh + 4 * c + 0]), __float_as_uint(v[16 * hh + 4 * c + 1]),
+                       __float_as_uint(v[16 * hh + 4 * c + 2]), __float_as_uint(v[16 * hh + 4 * c + 3]));
+      __syncwarp();
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int r = i * 8 + (lane >> 2), c = lane & 3;
+        const uint4 w = st[r * 4 + (c ^ ((r >> 1) & 3))];
+        if (row0 + r < M)
+          *reinterpret_cast<uint4*>(static_cast<float*>(base) + static_cast<int64_t>(row0 + r) * ld +
+                                    n + 16 * hh + c * 4) = w;
+      }
+      __syncwarp();
     }
   }
   __syncwarp();
@@ -384,24 +393,36 @@ __device__ __forceinline__ void stage_load_rows_bf16(uint4* st, const void* base
 __device__ __forceinline__ void stage_add_rows_f32(uint4* st, const void* base, int64_t ld, int row0,
                                                    int M, int n, float* v, int lane) {
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int r = i * 4 + (lane >> 3), c = lane & 7;
-    uint4 w = make_uint4(0, 0, 0, 0);
-    if (row0 + r < M)
-      w = *reinterpret_cast<const uint4*>(static_cast<const float*>(base) +
-                                          static_cast<int64_t>(row0 + r) * ld + n + c * 4);
-    st[r * 8 + (c ^ (r & 7))] = w;
-  }
-  __syncwarp();
+  for (int hh = 0; hh < 2; ++hh) {
 #pragma unroll
-  for (int c = 0; c < 8; ++c) {
-    const uint4 w = st[lane * 8 + (c ^ (lane & 7))];
-    v[4 * c + 0] += __uint_as_float(w.x);
-    v[4 * c + 1] += __uint_as_float(w.y);
-    v[4 * c + 2] += __uint_as_float(w.z);
-    v[4 * c + 3] += __uint_as_float(w.w);
+    for (int i = 0; i < 4; ++i) {
+      const int r = i * 8 + (lane >> 2), c = lane & 3;
+      uint4 w = make_uint4(0, 0, 0, 0);
+      if (row0 + r < M)
+        w = *reinterpret_cast<const uint4*>(static_cast<const float*>(base) +
+                                            static_cast<int64_t>(row0 + r) * ld + n + 16 * hh + c * 4);
+      st[r * 4 + (c ^ ((r >> 1) & 3))] = w;
+    }
+    __syncwarp();
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const uint4 w = st[lane * 4 + (c ^ ((lane >> 1) & 3))];
+      v[16 * hh + 4 * c + 0] += __uint_as_float(w.x);
+      v[16 * hh + 4 * c + 1] += __uint_as_float(w.y);
+      v[16 * hh + 4 * c + 2] += __uint_as_float(w.z);
+      v[16 * hh + 4 * c + 3] += __uint_as_float(w.w);
+    }
+    __syncwarp();
   }
-  __syncwarp();
+}
+
+// Pulls the bias of a warp's columns [n, n + 64) into L1 while the tile's
+// main loop runs, so the epilogue's per-chunk bias reads do not wait on L2.
+__device__ __forceinline__ void prefetch_bias(const GemmGroup& G, int n, int lane) {
+  if (G.bias != nullptr && lane < 2 && n < G.N) {
+    const int c = min(n + 63 * lane, G.N - 1);
+    asm volatile("prefetch.global.L1 [%0];" ::"l"(static_cast<const __nv_bfloat16*>(G.bias) + c));
+  }
 }
 
 // Epilogue of one 32 x 32 chunk: rows row0 .. row0+31 (lane l owns row0 + l),
@@ -417,6 +438,7 @@ __device__ __forceinline__ void epilogue_chunk(const GemmGroup& G, uint4* st, in
     case EPI_STORE:
     case EPI_BIAS_GELU: {
       if (G.bias != nullptr) {
+        // same address in every lane; the line was prefetched at tile start
         float b[32];
         load_bf16_chunk(static_cast<const __nv_bfloat16*>(G.bias) + n, b, ncols, coal);
 #pragma unroll
@@ -464,20 +486,26 @@ __device__ __forceinline__ void epilogue_chunk(const GemmGroup& G, uint4* st, in
       if (G.epi == EPI_SEGSUM && row_ok) {
         const int64_t id = G.seg_row0 + row;
         const int b = G.seg_offsets[id], e = G.seg_offsets[id + 1];
-        if (b < e) {
-          float s[32];
+        // the segment's rows added in position order, 16 columns at a time
+        for (int t = b; t < e; ++t) {
+          const __nv_bfloat16* src = static_cast<const __nv_bfloat16*>(G.seg_src) +
+                                     static_cast<int64_t>(G.seg_perm[t]) * G.ld_seg + n;
+          if (coal) {
+            const uint4* s4 = reinterpret_cast<const uint4*>(src);
 #pragma unroll
-          for (int j = 0; j < 32; ++j) s[j] = 0.f;
-          for (int t = b; t < e; ++t) {
-            float x[32];
-            const __nv_bfloat16* src = static_cast<const __nv_bfloat16*>(G.seg_src) +
-                                       static_cast<int64_t>(G.seg_perm[t]) * G.ld_seg + n;
-            load_bf16_chunk(src, x, ncols, coal);
+            for (int q = 0; q < 4; ++q) {
+              const uint4 w = __ldg(s4 + q);
+              float x0, x1;
+              unpack_bf16x2(w.x, x0, x1); v[8 * q + 0] += x0; v[8 * q + 1] += x1;
+              unpack_bf16x2(w.y, x0, x1); v[8 * q + 2] += x0; v[8 * q + 3] += x1;
+              unpack_bf16x2(w.z, x0, x1); v[8 * q + 4] += x0; v[8 * q + 5] += x1;
+              unpack_bf16x2(w.w, x0, x1); v[8 * q + 6] += x0; v[8 * q + 7] += x1;
+            }
+          } else {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) s[j] += x[j];
+            for (int j = 0; j < 32; ++j)
+              if (j < ncols) v[j] += bf2f(src[j]);
           }
-#pragma unroll
-          for (int j = 0; j < 32; ++j) v[j] += s[j];
         }
       }
       if (coal) {
@@ -575,21 +603,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
     }
     int stage = 0;
     uint32_t phase = 0;
-    int pending_phase[STAGES];
-    for (int s = 0; s < STAGES; ++s) pending_phase[s] = -1;
-    bool first = true;
+    // stages with a copy issued (bit s) and the phase it completes (bit s)
+    uint32_t pend_valid = 0, pend_phase = 0;
+    // Hot-loop values live in registers: reading the kernel parameters
+    // through references re-loads them after every asm statement.
+    const int total_tiles = p.total_tiles;
+    bool skip_first = p.fault_skip != 0;
     bool ok = true;
     int tile = blockIdx.x;
     for (int i = 0; ok; ++i) {
       // publish the tile id (or -1 = done) to the other roles
       const int r = i % TILE_RING;
       if (!wait_bounded(tile_empty_bar(r), static_cast<uint32_t>((i / TILE_RING) & 1) ^ 1u, wctx)) break;
-      const int t = tile < p.total_tiles ? tile : -1;
+      const int t = tile < total_tiles ? tile : -1;
       tile_ids[r] = t;
       mbar_arrive(tile_full_bar(r));
       if (t < 0) break;
       const TileCoord tc = decode_tile(p, t);
       const GemmGroup& G = p.grp[tc.g];
+      const int seg_begin = G.seg_begin, seg_end = G.seg_end;
       if (G.dep_kind != DEP_NONE) {
         // wait (bounded) until the tiles this one reads have been stored
         const int* ctr = dep + G.dep_base + (G.dep_kind == DEP_ROW ? tc.m0 / BM : tc.m0 / BN);
@@ -612,8 +644,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
         // order the TMA (async proxy) reads after the acquire
         asm volatile("fence.proxy.async.global;" ::: "memory");
       }
-      for (int s = G.seg_begin; ok && s < G.seg_end; ++s) {
-        const TcSeg& S = p.seg[s];
+      for (int s = seg_begin; ok && s < seg_end; ++s) {
+        const TcSeg S = p.seg[s];
+        const CUtensorMap* mapA = &p.mapA[s];
+        const CUtensorMap* mapB = &p.mapB[s];
         const int nk = (S.K + BK - 1) / BK;
         const uint32_t stage_bytes = A_TILE_BYTES + static_cast<uint32_t>(S.n_mma) * BK * 2;
         for (int kb = 0; kb < nk; ++kb) {
@@ -623,34 +657,35 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
           }
           const uint32_t a_dst = tiles_base + stage * STAGE_BYTES;
           const uint32_t b_dst = a_dst + A_TILE_BYTES;
-          if (first && p.fault_skip) {
+          const uint32_t fb = full_bar(stage);
+          if (skip_first) {
             // Injected fault: this stage is never filled, so the consumer's
             // bounded wait on it expires.
+            skip_first = false;
           } else {
-            mbar_arrive_expect_tx(full_bar(stage), stage_bytes);
-            pending_phase[stage] = static_cast<int>(phase);
+            mbar_arrive_expect_tx(fb, stage_bytes);
+            pend_valid |= 1u << stage;
+            pend_phase = (pend_phase & ~(1u << stage)) | (phase << stage);
             const int k0 = kb * BK;
             if (S.a_3d) {
-              tma_load_3d(a_dst, &p.mapA[s], full_bar(stage), 0, k0, tc.m0 / 64);
+              tma_load_3d(a_dst, mapA, fb, 0, k0, tc.m0 / 64);
             } else if (S.a_mn) {
-              tma_load_2d(a_dst, &p.mapA[s], full_bar(stage), tc.m0, k0);
-              tma_load_2d(a_dst + MN_BOX_BYTES, &p.mapA[s], full_bar(stage), tc.m0 + 64, k0);
+              tma_load_2d(a_dst, mapA, fb, tc.m0, k0);
+              tma_load_2d(a_dst + MN_BOX_BYTES, mapA, fb, tc.m0 + 64, k0);
             } else {
-              tma_load_2d(a_dst, &p.mapA[s], full_bar(stage), k0, tc.m0);
+              tma_load_2d(a_dst, mapA, fb, k0, tc.m0);
             }
             if (S.b_fixed) {
-              tma_load_2d(b_dst, &p.mapB[s], full_bar(stage), 0, 0);
+              tma_load_2d(b_dst, mapB, fb, 0, 0);
             } else if (S.b_3d) {
-              tma_load_3d(b_dst, &p.mapB[s], full_bar(stage), 0, k0, tc.n0 / 64);
+              tma_load_3d(b_dst, mapB, fb, 0, k0, tc.n0 / 64);
             } else if (S.b_mn) {
               for (int j = 0; j < S.n_mma / 64; ++j)
-                tma_load_2d(b_dst + j * MN_BOX_BYTES, &p.mapB[s], full_bar(stage), tc.n0 + 64 * j,
-                            k0);
+                tma_load_2d(b_dst + j * MN_BOX_BYTES, mapB, fb, tc.n0 + 64 * j, k0);
             } else {
-              tma_load_2d(b_dst, &p.mapB[s], full_bar(stage), k0, tc.n0);
+              tma_load_2d(b_dst, mapB, fb, k0, tc.n0);
             }
           }
-          first = false;
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
@@ -663,9 +698,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
     if (*abort_flag) {
       // Drain: wait (bounded) until every copy this thread issued has landed.
       for (int s = 0; s < STAGES; ++s) {
-        if (pending_phase[s] < 0) continue;
+        if (!((pend_valid >> s) & 1u)) continue;
         const unsigned long long t0 = global_ns();
-        while (!mbar_try_wait(full_bar(s), static_cast<uint32_t>(pending_phase[s]))) {
+        while (!mbar_try_wait(full_bar(s), (pend_phase >> s) & 1u)) {
           if (global_ns() - t0 > p.wait_limit_ns) break;
         }
       }
@@ -689,28 +724,30 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
       if (!wait_bounded(tempty_bar(buf), tphase ^ 1u, wctx)) break;
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
+      const int seg_begin = G.seg_begin, seg_end = G.seg_end;
       uint32_t acc = 0;
-      for (int s = G.seg_begin; ok && s < G.seg_end; ++s) {
-        const TcSeg& S = p.seg[s];
+      for (int s = seg_begin; ok && s < seg_end; ++s) {
+        const TcSeg S = p.seg[s];
         const int nk = (S.K + BK - 1) / BK;
         const uint32_t idesc = idesc_bf16(S.a_mn, S.b_mn, S.n_mma);
+        // Descriptors of stage 0; a stage / k-step offset is added to the
+        // 14-bit start-address field (shared addresses stay below 256 KB).
+        // K-major: 16 K elements = 32 bytes along the swizzled row.
+        // MN-major: 16 K rows = 2 swizzle atoms of 8 rows x 128 bytes.
+        const uint64_t a_desc0 = sdesc(tiles_base, S.a_mn ? MN_BOX_BYTES : 16, 1024);
+        const uint64_t b_desc0 = sdesc(tiles_base + A_TILE_BYTES, S.b_mn ? MN_BOX_BYTES : 16, 1024);
+        const uint32_t a_step = S.a_mn ? (2048 >> 4) : (32 >> 4);
+        const uint32_t b_step = S.b_mn ? (2048 >> 4) : (32 >> 4);
         for (int kb = 0; kb < nk; ++kb) {
           if (!wait_bounded(full_bar(stage), phase, wctx)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t a_base = tiles_base + stage * STAGE_BYTES;
-          const uint32_t b_base = a_base + A_TILE_BYTES;
+          const uint32_t off = static_cast<uint32_t>(stage * STAGE_BYTES) >> 4;
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
-            // K-major: 16 K elements = 32 bytes along the swizzled row.
-            // MN-major: 16 K rows = 2 swizzle atoms of 8 rows x 128 bytes.
-            const uint64_t ad = S.a_mn ? sdesc(a_base + kk * 2048, MN_BOX_BYTES, 1024)
-                                       : sdesc(a_base + kk * 32, 16, 1024);
-            const uint64_t bd = S.b_mn ? sdesc(b_base + kk * 2048, MN_BOX_BYTES, 1024)
-                                       : sdesc(b_base + kk * 32, 16, 1024);
-            mma_bf16(d_tmem, ad, bd, idesc, acc);
+            mma_bf16(d_tmem, a_desc0 + off + kk * a_step, b_desc0 + off + kk * b_step, idesc, acc);
             acc = 1;
           }
           issued_any = true;
@@ -736,8 +773,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
     // -------------------------------- Epilogue --------------------------------
     const int quarter = warp & 3;              // TMEM lanes this warp may access
     uint4* epi_stage = reinterpret_cast<uint4*>(smem + STAGES * STAGE_BYTES + BAR_BYTES +
-                                                (warp - 2) * EPI_STAGE_BYTES);
-    const int half = (warp - 2) >> 2;  // which half of the tile's columns
+                                                (warp - 2) * EPI_WARP_BYTES);
+    const int part = (warp - 2) >> 2;  // which quarter of the tile's columns
     for (int lt = 0;; ++lt) {
       const int r = lt % TILE_RING;
       if (!wait_bounded(tile_full_bar(r), static_cast<uint32_t>((lt / TILE_RING) & 1), wctx)) break;
@@ -749,13 +786,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
       const GemmGroup& G = p.grp[tc.g];
       const int buf = lt & 1;
       const uint32_t tphase = static_cast<uint32_t>(lt >> 1) & 1u;
+      const int cpw = G.bn / (32 * EPI_PARTS);  // 32-column chunks per warp
+      const int c_begin = part * cpw;
+      prefetch_bias(G, tc.n0 + c_begin * 32, lane);
       if (!wait_bounded(tfull_bar(buf), tphase, wctx)) break;
       tc_fence_after();
       const int row0 = tc.m0 + quarter * 32;
       const uint32_t taddr =
           tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(buf * BN);
-      const int cpw = G.bn / 64;  // 32-column chunks per warp
-      const int c_begin = half * cpw;
       for (int c = c_begin; c < c_begin + cpw; ++c) {
         const int n = tc.n0 + c * 32;
         if (n >= G.N) break;  // warp-uniform
@@ -830,7 +868,9 @@ constexpr int STAGES2 = 6;
 constexpr int B_HALF_BYTES = 128 * BK * 2;          // 16 KB
 constexpr int STAGE2_BYTES = A_TILE_BYTES + B_HALF_BYTES;
 constexpr int SMEM2_BYTES =
-    STAGES2 * STAGE2_BYTES + BAR_BYTES + NUM_EPI_WARPS * EPI_STAGE_BYTES + 1024;
+    STAGES2 * STAGE2_BYTES + BAR_BYTES + NUM_EPI_WARPS * EPI_WARP_BYTES + 1024;
+static_assert(SMEM_BYTES <= 227 * 1024 && SMEM2_BYTES <= 227 * 1024,
+              "dynamic shared memory above the 227 KB a CTA may use");
 
 // TMA load into this CTA's shared memory whose completion is signalled on an
 // mbarrier that may live in the peer CTA of the pair (cluster address).
@@ -1021,9 +1061,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_pair_kernel(const __gr
     }
     int stage = 0;
     uint32_t phase = 0;
-    int pending_phase[STAGES2];
-    for (int s = 0; s < STAGES2; ++s) pending_phase[s] = -1;
-    bool first = true;
+    uint32_t pend_valid = 0, pend_phase = 0;  // stages the leader expects, and their phase
+    const int total_tiles = p.total_tiles;
+    bool skip_first = p.fault_skip != 0;
     bool ok = true;
     int claim = blockIdx.x >> 1;  // the cluster's first tile
     for (int i = 0; ok; ++i) {
@@ -1031,7 +1071,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_pair_kernel(const __gr
       if (leader) {
         const int r = i % TILE_RING;
         if (!wait2(tile_empty_bar(r), static_cast<uint32_t>((i / TILE_RING) & 1) ^ 1u, wctx)) break;
-        t = claim < p.total_tiles ? claim : -1;
+        t = claim < total_tiles ? claim : -1;
         tile_ids[r] = t;
         st_cluster_u32(map_to_rank(tile_ids_addr + 4u * r, peer), static_cast<uint32_t>(t));
         mbar_arrive(tile_full_bar(r));
@@ -1043,6 +1083,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_pair_kernel(const __gr
       if (t < 0) break;
       const TileCoord tc = decode_tile_rows<BM2>(p, t);
       const GemmGroup& G = p.grp[tc.g];
+      const int seg_begin = G.seg_begin, seg_end = G.seg_end;
       const int row0 = tc.m0 + 128 * static_cast<int>(rank);  // this CTA's rows
       if (G.dep_kind != DEP_NONE) {
         const int* ctr = dep + G.dep_base + (G.dep_kind == DEP_ROW ? row0 / BM : tc.m0 / BN);
@@ -1063,8 +1104,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_pair_kernel(const __gr
         }
         asm volatile("fence.proxy.async.global;" ::: "memory");
       }
-      for (int s = G.seg_begin; ok && s < G.seg_end; ++s) {
-        const TcSeg& S = p.seg[s];
+      for (int s = seg_begin; ok && s < seg_end; ++s) {
+        const TcSeg S = p.seg[s];
+        const CUtensorMap* mapA = &p.mapA[s];
+        const CUtensorMap* mapB = &p.mapB[s];
         const int nk = (S.K + BK - 1) / BK;
         const uint32_t b_bytes = S.b_fixed ? static_cast<uint32_t>(S.n_mma / 2) * BK * 2 : B_HALF_BYTES;
         const int ncol0 = tc.n0 + 128 * static_cast<int>(rank);  // this CTA's half of B
@@ -1075,36 +1118,37 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_pair_kernel(const __gr
           }
           const uint32_t a_dst = tiles_base + stage * STAGE2_BYTES;
           const uint32_t b_dst = a_dst + A_TILE_BYTES;
-          if (first && p.fault_skip) {
+          if (skip_first) {
             // Injected fault: this stage is never filled.
+            skip_first = false;
           } else {
             // both halves complete on the leader's full barrier
             const uint32_t fb = map_to_rank(full_bar(stage), 0);
             if (leader) {
               mbar_arrive_expect_tx(full_bar(stage), 2 * (A_TILE_BYTES + b_bytes));
-              pending_phase[stage] = static_cast<int>(phase);
+              pend_valid |= 1u << stage;
+              pend_phase = (pend_phase & ~(1u << stage)) | (phase << stage);
             }
             const int k0 = kb * BK;
             if (S.a_3d) {
-              tma_load_3d_pair(a_dst, &p.mapA[s], fb, 0, k0, row0 / 64);
+              tma_load_3d_pair(a_dst, mapA, fb, 0, k0, row0 / 64);
             } else if (S.a_mn) {
-              tma_load_2d_pair(a_dst, &p.mapA[s], fb, row0, k0);
-              tma_load_2d_pair(a_dst + MN_BOX_BYTES, &p.mapA[s], fb, row0 + 64, k0);
+              tma_load_2d_pair(a_dst, mapA, fb, row0, k0);
+              tma_load_2d_pair(a_dst + MN_BOX_BYTES, mapA, fb, row0 + 64, k0);
             } else {
-              tma_load_2d_pair(a_dst, &p.mapA[s], fb, k0, row0);
+              tma_load_2d_pair(a_dst, mapA, fb, k0, row0);
             }
             if (S.b_fixed) {
-              tma_load_2d_pair(b_dst, &p.mapB[s], fb, 0, 0);
+              tma_load_2d_pair(b_dst, mapB, fb, 0, 0);
             } else if (S.b_3d) {
-              tma_load_3d_pair(b_dst, &p.mapB[s], fb, 0, k0, ncol0 / 64);
+              tma_load_3d_pair(b_dst, mapB, fb, 0, k0, ncol0 / 64);
             } else if (S.b_mn) {
-              tma_load_2d_pair(b_dst, &p.mapB[s], fb, ncol0, k0);
-              tma_load_2d_pair(b_dst + MN_BOX_BYTES, &p.mapB[s], fb, ncol0 + 64, k0);
+              tma_load_2d_pair(b_dst, mapB, fb, ncol0, k0);
+              tma_load_2d_pair(b_dst + MN_BOX_BYTES, mapB, fb, ncol0 + 64, k0);
             } else {
-              tma_load_2d_pair(b_dst, &p.mapB[s], fb, k0, ncol0);
+              tma_load_2d_pair(b_dst, mapB, fb, k0, ncol0);
             }
           }
-          first = false;
           if (++stage == STAGES2) {
             stage = 0;
             phase ^= 1u;
@@ -1120,9 +1164,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_pair_kernel(const __gr
       // interval pass for its own copies in flight.
       if (leader) {
         for (int s = 0; s < STAGES2; ++s) {
-          if (pending_phase[s] < 0) continue;
+          if (!((pend_valid >> s) & 1u)) continue;
           const unsigned long long t0 = global_ns();
-          while (!mbar_try_wait(full_bar(s), static_cast<uint32_t>(pending_phase[s]))) {
+          while (!mbar_try_wait(full_bar(s), (pend_phase >> s) & 1u)) {
             if (global_ns() - t0 > p.wait_limit_ns) break;
           }
         }
@@ -1149,26 +1193,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_pair_kernel(const __gr
       if (!wait2(tempty_bar(buf), tphase ^ 1u, wctx)) break;
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
+      const int seg_begin = G.seg_begin, seg_end = G.seg_end;
       uint32_t acc = 0;
-      for (int s = G.seg_begin; ok && s < G.seg_end; ++s) {
-        const TcSeg& S = p.seg[s];
+      for (int s = seg_begin; ok && s < seg_end; ++s) {
+        const TcSeg S = p.seg[s];
         const int nk = (S.K + BK - 1) / BK;
         const uint32_t idesc = idesc_bf16_m256(S.a_mn, S.b_mn, S.n_mma);
+        const uint64_t a_desc0 = sdesc(tiles_base, S.a_mn ? MN_BOX_BYTES : 16, 1024);
+        const uint64_t b_desc0 = sdesc(tiles_base + A_TILE_BYTES, S.b_mn ? MN_BOX_BYTES : 16, 1024);
+        const uint32_t a_step = S.a_mn ? (2048 >> 4) : (32 >> 4);
+        const uint32_t b_step = S.b_mn ? (2048 >> 4) : (32 >> 4);
         for (int kb = 0; kb < nk; ++kb) {
           if (!wait2(full_bar(stage), phase, wctx)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t a_base = tiles_base + stage * STAGE2_BYTES;
-          const uint32_t b_base = a_base + A_TILE_BYTES;
+          const uint32_t off = static_cast<uint32_t>(stage * STAGE2_BYTES) >> 4;
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
-            const uint64_t ad = S.a_mn ? sdesc(a_base + kk * 2048, MN_BOX_BYTES, 1024)
-                                       : sdesc(a_base + kk * 32, 16, 1024);
-            const uint64_t bd = S.b_mn ? sdesc(b_base + kk * 2048, MN_BOX_BYTES, 1024)
-                                       : sdesc(b_base + kk * 32, 16, 1024);
-            mma_bf16_pair(d_tmem, ad, bd, idesc, acc);
+            mma_bf16_pair(d_tmem, a_desc0 + off + kk * a_step, b_desc0 + off + kk * b_step, idesc, acc);
             acc = 1;
           }
           issued_any = true;
@@ -1192,9 +1236,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_pair_kernel(const __gr
   } else if (warp >= 2) {
     // ---------------------------- epilogue (both CTAs) ----------------------------
     const int quarter = warp & 3;
-    const int c_begin = ((warp - 2) >> 2) * (BN / 64);
+    constexpr int cpw = BN / (32 * EPI_PARTS);  // 32-column chunks per warp
+    const int c_begin = ((warp - 2) >> 2) * cpw;
     uint4* epi_stage = reinterpret_cast<uint4*>(smem + STAGES2 * STAGE2_BYTES + BAR_BYTES +
-                                                (warp - 2) * EPI_STAGE_BYTES);
+                                                (warp - 2) * EPI_WARP_BYTES);
     const uint32_t tempty_leader0 = map_to_rank(tempty_bar(0), 0);
     const uint32_t tempty_leader1 = map_to_rank(tempty_bar(1), 0);
     for (int lt = 0;; ++lt) {
@@ -1207,12 +1252,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_pair_kernel(const __gr
       const GemmGroup& G = p.grp[tc.g];
       const int buf = lt & 1;
       const uint32_t tphase = static_cast<uint32_t>(lt >> 1) & 1u;
+      prefetch_bias(G, tc.n0 + c_begin * 32, lane);
       if (!wait2(tfull_bar(buf), tphase, wctx)) break;
       tc_fence_after();
       const int row0 = tc.m0 + 128 * static_cast<int>(rank) + quarter * 32;
       const uint32_t taddr =
           tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(buf * BN);
-      for (int c = c_begin; c < c_begin + BN / 64; ++c) {
+      for (int c = c_begin; c < c_begin + cpw; ++c) {
         const int n = tc.n0 + c * 32;
         if (n >= G.N) break;  // warp-uniform
         uint32_t rr[32];

@@ -9,7 +9,7 @@ namespace tp {
 
 constexpr int kMaxGroups = 40;    // output matrices in one GEMM launch
 constexpr int kMaxSegs = 48;      // (A, B) operand pairs summed into the outputs
-constexpr int kEpiWarps = 8;      // epilogue warps of the tensor-core engine
+constexpr int kEpiWarps = 16;     // epilogue warps of the tensor-core engine
 constexpr int kMaxCounters = 512; // tile-completion counters of one launch
 constexpr int kMaxRanges = 64;    // vocabulary ranges
 
