@@ -357,21 +357,16 @@ tp_status launch_tc_groups(const Plan& pl, const bool* used, GemmGroup* groups, 
                            int interleave, int ncounters, const DeviceState* dev, const char* name,
                            cudaStream_t s, bool longest_first) {
   if (ng == 0) return TP_OK;
-  // Kernel choice (measured on GB300): the two-SM kernel (256 x 256 pair tiles,
-  // 6-stage ring) is faster on large launches whose operands include MN-major
-  // (transposed) matrices, the backward and weight-gradient contractions; the
-  // one-SM kernel (128 x 256 tiles) on K-major launches and on small ones,
-  // where its finer tiles balance better.
+  // Kernel choice (measured on GB300): the two-SM kernel (256 x 256 pair
+  // tiles, 6-stage ring, 32 KB loaded per SM per k-block instead of 48 KB) is
+  // faster on large launches, K-major or MN-major; the one-SM kernel (128 x 256
+  // tiles) on small ones, where its finer tiles balance better across SMs.
   bool pair = g_gemm_mode == 1;
   if (g_gemm_mode == 2) {
-    bool has_mn = false;
     int64_t tiles128 = 0;
-    for (int i = 0; i < ng; ++i) {
+    for (int i = 0; i < ng; ++i)
       tiles128 += static_cast<int64_t>((groups[i].M + 127) / 128) * ((groups[i].N + 255) / 256);
-      for (int sidx = groups[i].seg_begin; sidx < groups[i].seg_end; ++sidx)
-        has_mn = has_mn || pl.seg[sidx].A.mn || pl.seg[sidx].B.mn;
-    }
-    pair = has_mn && tiles128 > 8 * static_cast<int64_t>(dev->num_sms);
+    pair = tiles128 > 8 * static_cast<int64_t>(dev->num_sms);
   }
   // Tile width: 256 for every output.  (128-wide tiles for the long dependent
   // contractions of small fused launches were measured slower on GB300: a

@@ -118,33 +118,30 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, cons
   }
 }
 
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
-                                            int c0, int c1) {
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, uint64_t map, uint32_t bar, int c0,
+                                            int c1) {
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1)
-      : "memory");
+      "l"(map), "r"(bar), "r"(c0), "r"(c1));
 }
 
 // 3D tile load: an MN-major operand viewed as (64 MN, K rows, MN / 64 blocks);
 // one box brings all of a tile's 64-wide blocks, stacked 8 KB apart.
-__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
-                                            int c0, int c1, int c2) {
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, uint64_t map, uint32_t bar, int c0,
+                                            int c1, int c2) {
   asm volatile(
       "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
-      : "memory");
+      "l"(map), "r"(bar), "r"(c0), "r"(c1), "r"(c2));
 }
 
-__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap* map,
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, uint64_t map,
                                                  uint32_t bar_cluster, int c0, int c1, int c2) {
   asm volatile(
       "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(c0), "r"(c1), "r"(c2)
-      : "memory");
+      "l"(map), "r"(bar_cluster), "r"(c0), "r"(c1), "r"(c2));
 }
 
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
@@ -190,8 +187,7 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
-      : "memory");
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
 }
 
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
@@ -528,6 +524,91 @@ __device__ __forceinline__ void epilogue_chunk(const GemmGroup& G, uint4* st, in
 }
 
 // ---------------------------------------------------------------------------
+// Producer main loop of one segment, specialised on the operand forms:
+// A_MODE 0 = K-major box, 1 = MN-major (two 64-wide boxes), 2 = MN-major 3D box;
+// B_MODE 0 = K-major box, 1 = MN-major (N / 64 boxes), 2 = MN-major 3D box,
+// 3 = the fixed ones block.  Keeping the form out of the loop leaves the loop
+// body a straight line of TMA issues, which measured markedly faster than
+// branching on the form every k-block.
+// ---------------------------------------------------------------------------
+struct ProdRing {
+  uint32_t tiles_base, full0, empty0;  // smem addresses: stage 0 data, full[0], empty[0]
+  int stage;
+  uint32_t phase;
+  uint32_t pend_valid, pend_phase;     // stages with a copy issued, and its phase
+  bool skip_first;                     // fault injection: leave the first stage unfilled
+};
+
+template <int STAGES_, int STAGE_BYTES_, int A_MODE, int B_MODE>
+__device__ __forceinline__ bool produce_kblocks(ProdRing& R, const WaitCtx& wctx, uint64_t mapA,
+                                                uint64_t mapB, int nk, int m0, int n0, int n_mma) {
+  const uint32_t stage_bytes = A_TILE_BYTES + static_cast<uint32_t>(n_mma) * BK * 2;
+  for (int kb = 0; kb < nk; ++kb) {
+    if (!wait_bounded(R.empty0 + 8u * R.stage, R.phase ^ 1u, wctx)) return false;
+    const uint32_t a_dst = R.tiles_base + R.stage * STAGE_BYTES_;
+    const uint32_t b_dst = a_dst + A_TILE_BYTES;
+    const uint32_t fb = R.full0 + 8u * R.stage;
+    if (R.skip_first) {
+      R.skip_first = false;  // this stage is never filled; the consumer's wait expires
+    } else {
+      mbar_arrive_expect_tx(fb, stage_bytes);
+      R.pend_valid |= 1u << R.stage;
+      R.pend_phase = (R.pend_phase & ~(1u << R.stage)) | (R.phase << R.stage);
+      const int k0 = kb * BK;
+      if (A_MODE == 0) {
+        tma_load_2d(a_dst, mapA, fb, k0, m0);
+      } else if (A_MODE == 2) {
+        tma_load_3d(a_dst, mapA, fb, 0, k0, m0 / 64);
+      } else {
+        tma_load_2d(a_dst, mapA, fb, m0, k0);
+        tma_load_2d(a_dst + MN_BOX_BYTES, mapA, fb, m0 + 64, k0);
+      }
+      if (B_MODE == 0) {
+        tma_load_2d(b_dst, mapB, fb, k0, n0);
+      } else if (B_MODE == 2) {
+        tma_load_3d(b_dst, mapB, fb, 0, k0, n0 / 64);
+      } else if (B_MODE == 3) {
+        tma_load_2d(b_dst, mapB, fb, 0, 0);
+      } else {
+        for (int j = 0; j < n_mma / 64; ++j)
+          tma_load_2d(b_dst + j * MN_BOX_BYTES, mapB, fb, n0 + 64 * j, k0);
+      }
+    }
+    if (++R.stage == STAGES_) {
+      R.stage = 0;
+      R.phase ^= 1u;
+    }
+  }
+  return true;
+}
+
+template <int STAGES_, int STAGE_BYTES_>
+__device__ __forceinline__ bool produce_segment(ProdRing& R, const WaitCtx& wctx, const TcSeg& S,
+                                                uint64_t mapA, uint64_t mapB, int m0, int n0) {
+  const int a_mode = S.a_3d ? 2 : (S.a_mn ? 1 : 0);
+  const int b_mode = S.b_fixed ? 3 : (S.b_3d ? 2 : (S.b_mn ? 1 : 0));
+  const int nk = (S.K + BK - 1) / BK;
+  const int n_mma = S.n_mma;
+#define TP_PRODUCE(am, bm) \
+  produce_kblocks<STAGES_, STAGE_BYTES_, am, bm>(R, wctx, mapA, mapB, nk, m0, n0, n_mma)
+  switch (a_mode * 4 + b_mode) {
+    case 0: return TP_PRODUCE(0, 0);
+    case 1: return TP_PRODUCE(0, 1);
+    case 2: return TP_PRODUCE(0, 2);
+    case 3: return TP_PRODUCE(0, 3);
+    case 4: return TP_PRODUCE(1, 0);
+    case 5: return TP_PRODUCE(1, 1);
+    case 6: return TP_PRODUCE(1, 2);
+    case 7: return TP_PRODUCE(1, 3);
+    case 8: return TP_PRODUCE(2, 0);
+    case 9: return TP_PRODUCE(2, 1);
+    case 10: return TP_PRODUCE(2, 2);
+    default: return TP_PRODUCE(2, 3);
+  }
+#undef TP_PRODUCE
+}
+
+// ---------------------------------------------------------------------------
 // Dynamic tile scheduling: one (next, done) counter pair per launch slot.  The
 // last CTA to finish resets its pair, so the next launch using the slot starts
 // from zero.  Launches rotate over the slots.
@@ -601,14 +682,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
       prefetch_tmap(&p.mapA[s]);
       prefetch_tmap(&p.mapB[s]);
     }
-    int stage = 0;
-    uint32_t phase = 0;
-    // stages with a copy issued (bit s) and the phase it completes (bit s)
-    uint32_t pend_valid = 0, pend_phase = 0;
+    ProdRing R{tiles_base, full_bar(0), empty_bar(0), 0, 0u, 0u, 0u, p.fault_skip != 0};
     // Hot-loop values live in registers: reading the kernel parameters
     // through references re-loads them after every asm statement.
     const int total_tiles = p.total_tiles;
-    bool skip_first = p.fault_skip != 0;
     bool ok = true;
     int tile = blockIdx.x;
     for (int i = 0; ok; ++i) {
@@ -646,51 +723,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
       }
       for (int s = seg_begin; ok && s < seg_end; ++s) {
         const TcSeg S = p.seg[s];
-        const CUtensorMap* mapA = &p.mapA[s];
-        const CUtensorMap* mapB = &p.mapB[s];
-        const int nk = (S.K + BK - 1) / BK;
-        const uint32_t stage_bytes = A_TILE_BYTES + static_cast<uint32_t>(S.n_mma) * BK * 2;
-        for (int kb = 0; kb < nk; ++kb) {
-          if (!wait_bounded(empty_bar(stage), phase ^ 1u, wctx)) {
-            ok = false;
-            break;
-          }
-          const uint32_t a_dst = tiles_base + stage * STAGE_BYTES;
-          const uint32_t b_dst = a_dst + A_TILE_BYTES;
-          const uint32_t fb = full_bar(stage);
-          if (skip_first) {
-            // Injected fault: this stage is never filled, so the consumer's
-            // bounded wait on it expires.
-            skip_first = false;
-          } else {
-            mbar_arrive_expect_tx(fb, stage_bytes);
-            pend_valid |= 1u << stage;
-            pend_phase = (pend_phase & ~(1u << stage)) | (phase << stage);
-            const int k0 = kb * BK;
-            if (S.a_3d) {
-              tma_load_3d(a_dst, mapA, fb, 0, k0, tc.m0 / 64);
-            } else if (S.a_mn) {
-              tma_load_2d(a_dst, mapA, fb, tc.m0, k0);
-              tma_load_2d(a_dst + MN_BOX_BYTES, mapA, fb, tc.m0 + 64, k0);
-            } else {
-              tma_load_2d(a_dst, mapA, fb, k0, tc.m0);
-            }
-            if (S.b_fixed) {
-              tma_load_2d(b_dst, mapB, fb, 0, 0);
-            } else if (S.b_3d) {
-              tma_load_3d(b_dst, mapB, fb, 0, k0, tc.n0 / 64);
-            } else if (S.b_mn) {
-              for (int j = 0; j < S.n_mma / 64; ++j)
-                tma_load_2d(b_dst + j * MN_BOX_BYTES, mapB, fb, tc.n0 + 64 * j, k0);
-            } else {
-              tma_load_2d(b_dst, mapB, fb, k0, tc.n0);
-            }
-          }
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1u;
-          }
-        }
+        ok = produce_segment<STAGES, STAGE_BYTES>(R, wctx, S, reinterpret_cast<uint64_t>(&p.mapA[s]),
+                                                  reinterpret_cast<uint64_t>(&p.mapB[s]), tc.m0, tc.n0);
       }
       // next tile: the first gridDim tiles are static, the rest claimed in order
       tile = static_cast<int>(gridDim.x) + atomicAdd(sched, 1);
@@ -698,9 +732,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
     if (*abort_flag) {
       // Drain: wait (bounded) until every copy this thread issued has landed.
       for (int s = 0; s < STAGES; ++s) {
-        if (!((pend_valid >> s) & 1u)) continue;
+        if (!((R.pend_valid >> s) & 1u)) continue;
         const unsigned long long t0 = global_ns();
-        while (!mbar_try_wait(full_bar(s), (pend_phase >> s) & 1u)) {
+        while (!mbar_try_wait(full_bar(s), (R.pend_phase >> s) & 1u)) {
           if (global_ns() - t0 > p.wait_limit_ns) break;
         }
       }
@@ -874,13 +908,12 @@ static_assert(SMEM_BYTES <= 227 * 1024 && SMEM2_BYTES <= 227 * 1024,
 
 // TMA load into this CTA's shared memory whose completion is signalled on an
 // mbarrier that may live in the peer CTA of the pair (cluster address).
-__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map,
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, uint64_t map,
                                                  uint32_t bar_cluster, int c0, int c1) {
   asm volatile(
       "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(c0), "r"(c1)
-      : "memory");
+      "l"(map), "r"(bar_cluster), "r"(c0), "r"(c1));
 }
 
 __device__ __forceinline__ uint32_t cluster_rank() {
@@ -956,8 +989,7 @@ __device__ __forceinline__ void mma_bf16_pair(uint32_t d_tmem, uint64_t a, uint6
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
-      : "memory");
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
 }
 
 // Arrives on the mbarrier at `bar` in both CTAs of the pair once all prior
@@ -974,6 +1006,81 @@ __device__ __forceinline__ uint32_t idesc_bf16_m256(int a_mn, int b_mn, int n) {
   return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(a_mn) << 15) |
          (static_cast<uint32_t>(b_mn) << 16) | (static_cast<uint32_t>(n >> 3) << 17) |
          (static_cast<uint32_t>(BM2 >> 4) << 24);
+}
+
+// Producer main loop of one segment for the two-SM kernel (same operand
+// forms as produce_kblocks; each CTA loads its 128 rows of A and its half of
+// B, and both CTAs' copies complete on the leader's full barrier).
+template <int A_MODE, int B_MODE>
+__device__ __forceinline__ bool produce_kblocks_pair(ProdRing& R, const WaitCtx2& wctx, bool leader,
+                                                     uint64_t mapA, uint64_t mapB, int nk, int row0,
+                                                     int ncol0, uint32_t b_bytes) {
+  for (int kb = 0; kb < nk; ++kb) {
+    if (!wait2(R.empty0 + 8u * R.stage, R.phase ^ 1u, wctx)) return false;
+    const uint32_t a_dst = R.tiles_base + R.stage * STAGE2_BYTES;
+    const uint32_t b_dst = a_dst + A_TILE_BYTES;
+    if (R.skip_first) {
+      R.skip_first = false;  // this stage is never filled; the consumer's wait expires
+    } else {
+      const uint32_t own_full = R.full0 + 8u * R.stage;
+      const uint32_t fb = map_to_rank(own_full, 0);
+      if (leader) {
+        mbar_arrive_expect_tx(own_full, 2 * (A_TILE_BYTES + b_bytes));
+        R.pend_valid |= 1u << R.stage;
+        R.pend_phase = (R.pend_phase & ~(1u << R.stage)) | (R.phase << R.stage);
+      }
+      const int k0 = kb * BK;
+      if (A_MODE == 0) {
+        tma_load_2d_pair(a_dst, mapA, fb, k0, row0);
+      } else if (A_MODE == 2) {
+        tma_load_3d_pair(a_dst, mapA, fb, 0, k0, row0 / 64);
+      } else {
+        tma_load_2d_pair(a_dst, mapA, fb, row0, k0);
+        tma_load_2d_pair(a_dst + MN_BOX_BYTES, mapA, fb, row0 + 64, k0);
+      }
+      if (B_MODE == 0) {
+        tma_load_2d_pair(b_dst, mapB, fb, k0, ncol0);
+      } else if (B_MODE == 2) {
+        tma_load_3d_pair(b_dst, mapB, fb, 0, k0, ncol0 / 64);
+      } else if (B_MODE == 3) {
+        tma_load_2d_pair(b_dst, mapB, fb, 0, 0);
+      } else {
+        tma_load_2d_pair(b_dst, mapB, fb, ncol0, k0);
+        tma_load_2d_pair(b_dst + MN_BOX_BYTES, mapB, fb, ncol0 + 64, k0);
+      }
+    }
+    if (++R.stage == STAGES2) {
+      R.stage = 0;
+      R.phase ^= 1u;
+    }
+  }
+  return true;
+}
+
+__device__ __forceinline__ bool produce_segment_pair(ProdRing& R, const WaitCtx2& wctx, bool leader,
+                                                     const TcSeg& S, uint64_t mapA, uint64_t mapB,
+                                                     int row0, int ncol0) {
+  const int a_mode = S.a_3d ? 2 : (S.a_mn ? 1 : 0);
+  const int b_mode = S.b_fixed ? 3 : (S.b_3d ? 2 : (S.b_mn ? 1 : 0));
+  const int nk = (S.K + BK - 1) / BK;
+  const uint32_t b_bytes = S.b_fixed ? static_cast<uint32_t>(S.n_mma / 2) * BK * 2 : B_HALF_BYTES;
+#define TP_PRODUCE2(am, bm) \
+  produce_kblocks_pair<am, bm>(R, wctx, leader, mapA, mapB, nk, row0, ncol0, b_bytes)
+  switch (a_mode * 4 + b_mode) {
+    case 0: return TP_PRODUCE2(0, 0);
+    case 1: return TP_PRODUCE2(0, 1);
+    case 2: return TP_PRODUCE2(0, 2);
+    case 3: return TP_PRODUCE2(0, 3);
+    case 4: return TP_PRODUCE2(1, 0);
+    case 5: return TP_PRODUCE2(1, 1);
+    case 6: return TP_PRODUCE2(1, 2);
+    case 7: return TP_PRODUCE2(1, 3);
+    case 8: return TP_PRODUCE2(2, 0);
+    case 9: return TP_PRODUCE2(2, 1);
+    case 10: return TP_PRODUCE2(2, 2);
+    default: return TP_PRODUCE2(2, 3);
+  }
+#undef TP_PRODUCE2
 }
 
 __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_pair_kernel(const __grid_constant__ TcGemmParams p) {
@@ -1059,11 +1166,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_pair_kernel(const __gr
       prefetch_tmap(&p.mapA[s]);
       prefetch_tmap(&p.mapB[s]);
     }
-    int stage = 0;
-    uint32_t phase = 0;
-    uint32_t pend_valid = 0, pend_phase = 0;  // stages the leader expects, and their phase
+    ProdRing R{tiles_base, full_bar(0), empty_bar(0), 0, 0u, 0u, 0u, p.fault_skip != 0};
     const int total_tiles = p.total_tiles;
-    bool skip_first = p.fault_skip != 0;
     bool ok = true;
     int claim = blockIdx.x >> 1;  // the cluster's first tile
     for (int i = 0; ok; ++i) {
@@ -1104,56 +1208,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_pair_kernel(const __gr
         }
         asm volatile("fence.proxy.async.global;" ::: "memory");
       }
+      const int ncol0 = tc.n0 + 128 * static_cast<int>(rank);  // this CTA's half of B
       for (int s = seg_begin; ok && s < seg_end; ++s) {
         const TcSeg S = p.seg[s];
-        const CUtensorMap* mapA = &p.mapA[s];
-        const CUtensorMap* mapB = &p.mapB[s];
-        const int nk = (S.K + BK - 1) / BK;
-        const uint32_t b_bytes = S.b_fixed ? static_cast<uint32_t>(S.n_mma / 2) * BK * 2 : B_HALF_BYTES;
-        const int ncol0 = tc.n0 + 128 * static_cast<int>(rank);  // this CTA's half of B
-        for (int kb = 0; kb < nk; ++kb) {
-          if (!wait2(empty_bar(stage), phase ^ 1u, wctx)) {
-            ok = false;
-            break;
-          }
-          const uint32_t a_dst = tiles_base + stage * STAGE2_BYTES;
-          const uint32_t b_dst = a_dst + A_TILE_BYTES;
-          if (skip_first) {
-            // Injected fault: this stage is never filled.
-            skip_first = false;
-          } else {
-            // both halves complete on the leader's full barrier
-            const uint32_t fb = map_to_rank(full_bar(stage), 0);
-            if (leader) {
-              mbar_arrive_expect_tx(full_bar(stage), 2 * (A_TILE_BYTES + b_bytes));
-              pend_valid |= 1u << stage;
-              pend_phase = (pend_phase & ~(1u << stage)) | (phase << stage);
-            }
-            const int k0 = kb * BK;
-            if (S.a_3d) {
-              tma_load_3d_pair(a_dst, mapA, fb, 0, k0, row0 / 64);
-            } else if (S.a_mn) {
-              tma_load_2d_pair(a_dst, mapA, fb, row0, k0);
-              tma_load_2d_pair(a_dst + MN_BOX_BYTES, mapA, fb, row0 + 64, k0);
-            } else {
-              tma_load_2d_pair(a_dst, mapA, fb, k0, row0);
-            }
-            if (S.b_fixed) {
-              tma_load_2d_pair(b_dst, mapB, fb, 0, 0);
-            } else if (S.b_3d) {
-              tma_load_3d_pair(b_dst, mapB, fb, 0, k0, ncol0 / 64);
-            } else if (S.b_mn) {
-              tma_load_2d_pair(b_dst, mapB, fb, ncol0, k0);
-              tma_load_2d_pair(b_dst + MN_BOX_BYTES, mapB, fb, ncol0 + 64, k0);
-            } else {
-              tma_load_2d_pair(b_dst, mapB, fb, k0, ncol0);
-            }
-          }
-          if (++stage == STAGES2) {
-            stage = 0;
-            phase ^= 1u;
-          }
-        }
+        ok = produce_segment_pair(R, wctx, leader, S, reinterpret_cast<uint64_t>(&p.mapA[s]),
+                                  reinterpret_cast<uint64_t>(&p.mapB[s]), row0, ncol0);
       }
       if (leader) claim = static_cast<int>(gridDim.x >> 1) + atomicAdd(sched, 1);
     }
@@ -1164,9 +1223,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_pair_kernel(const __gr
       // interval pass for its own copies in flight.
       if (leader) {
         for (int s = 0; s < STAGES2; ++s) {
-          if (!((pend_valid >> s) & 1u)) continue;
+          if (!((R.pend_valid >> s) & 1u)) continue;
           const unsigned long long t0 = global_ns();
-          while (!mbar_try_wait(full_bar(s), (pend_phase >> s) & 1u)) {
+          while (!mbar_try_wait(full_bar(s), (R.pend_phase >> s) & 1u)) {
             if (global_ns() - t0 > p.wait_limit_ns) break;
           }
         }
