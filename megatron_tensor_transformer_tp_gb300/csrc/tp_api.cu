@@ -290,9 +290,10 @@ bool group_vec_ok(const GemmGroup& g, int in_esize) {
 
 // Targets of the dependency counters: a consumer waits until every producer
 // tile feeding its counter has been stored by all epilogue warps.
-// A producer tile counts once per epilogue warp of each CTA that stores part of
-// it: per 128-row block for row counters, per CTA half (`halves` = 2 for the
-// two-SM kernel's 256-row tiles) for column counters.
+// A producer tile counts epi_parts times per CTA that stores part of it (once
+// in the one-SM kernel, once per epilogue warp in the two-SM kernel): per
+// 128-row block for row counters, per CTA half (`halves` = 2 for the two-SM
+// kernel's 256-row tiles) for column counters.
 void set_dep_targets(GemmGroup* groups, int ng, int epi_parts, int halves) {
   for (int i = 0; i < ng; ++i) {
     GemmGroup& c = groups[i];
@@ -435,7 +436,8 @@ tp_status launch_tc_groups(const Plan& pl, const bool* used, GemmGroup* groups, 
     g.tile_begin = tiles;
     tiles += g.tiles_m * g.tiles_n;
   }
-  set_dep_targets(groups, ng, kEpiWarps, pair ? 2 : 1);
+  // one count per producer tile (one-SM kernel), one per epilogue warp and CTA (two-SM kernel)
+  set_dep_targets(groups, ng, pair ? kEpiWarps : 1, pair ? 2 : 1);
   for (int i = 0; i < ng; ++i) p.grp[i] = groups[i];
   p.pair = pair ? 1 : 0;
   p.num_groups = ng;

@@ -844,17 +844,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
         epilogue_chunk(G, epi_stage, lane, row0, n, v);
       }
       tc_fence_before();
-      if (G.prod_row >= 0 || G.prod_col >= 0) {
-        // make this warp's stores visible GPU-wide, then count the tile part
-        __threadfence();
-        __syncwarp();
-        if (lane == 0) {
-          if (G.prod_row >= 0) atomicAdd(dep + G.prod_row + tc.m0 / BM, 1);
-          if (G.prod_col >= 0) atomicAdd(dep + G.prod_col + tc.n0 / BN, 1);
-        }
-      }
       __syncwarp();
       if (lane == 0) mbar_arrive(tempty_bar(buf));
+      if ((G.prod_row >= 0 || G.prod_col >= 0) && warp == 2 + lt % NUM_EPI_WARPS) {
+        // One warp per tile (rotating) counts the tile for its dependants:
+        // once every epilogue warp has arrived on tempty (release.cta after
+        // its stores; this wait acquires), a GPU-scope fence and the counter
+        // add publish all of the tile's stores.  The other warps move on
+        // without a fence.
+        if (lane == 0) {
+          if (wait_bounded(tempty_bar(buf), tphase, wctx)) {
+            __threadfence();
+            if (G.prod_row >= 0) atomicAdd(dep + G.prod_row + tc.m0 / BM, 1);
+            if (G.prod_col >= 0) atomicAdd(dep + G.prod_col + tc.n0 / BN, 1);
+          }
+        }
+        __syncwarp();
+      }
     }
   }
 
