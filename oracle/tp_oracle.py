@@ -367,6 +367,91 @@ def tied_embed_grad_rows(ids, dEmb, X, dLogits_full, vocab_rows):
 
 
 # --------------------------------------------------------------------------
+# Vocab-parallel cross-entropy
+# --------------------------------------------------------------------------
+def vocab_parallel_cross_entropy(X, E_shards, range_starts, targets):
+    """Per-token loss of the vocab-parallel cross-entropy, and its log-sum-exp.
+
+    Follows the forward of [Walkthrough] §_VocabParallelCrossEntropy and the
+    four stages of [Study notes] §交叉熵张量并行 ([TP notes] §Cross-entropy层
+    states why: no all-gather of the (b, s, v) logits):
+      1. each range's logits L_r = X E_r^T;
+      2. the row maximum over all ranges (all-reduce MAX) is subtracted;
+      3a. predicted logit: each range picks its shifted logit at the target
+          when the target lies in its range and 0 otherwise; the ranges' values
+          are summed (all-reduce SUM);
+      3b. the sum of exp of the shifted logits, per range then over ranges;
+      4. loss = log(sum) - predicted.
+    A target in no range gets predicted = 0 (every range masks it), so its loss
+    is log(sum) of the shifted logits, as the pages' masking gives.
+    Returns (loss, lse) with lse = max + log(sum) per token.
+    Pinned by: torch cross_entropy on the unsharded logits (valid targets),
+    invariance to the vocabulary split, the all-zero-logits closed form
+    log V, and stability at logits of order 1e3.
+    """
+    targets = np.asarray(targets, dtype=np.int64)
+    logits = [np.asarray(X, dtype=np.float64) @ np.asarray(Er, dtype=np.float64).T for Er in E_shards]
+    T = logits[0].shape[0]
+    logits_max = np.max(np.stack([L.max(axis=1) for L in logits]), axis=0)  # all-reduce MAX
+    shifted = [L - logits_max[:, None] for L in logits]
+    predicted = np.zeros(T)
+    rows = np.arange(T)
+    for r, L in enumerate(shifted):
+        start, end = range_starts[r], range_starts[r + 1]
+        target_mask = (targets < start) | (targets >= end)
+        masked_target = np.where(target_mask, 0, targets - start)
+        pred_r = L[rows, masked_target]
+        pred_r[target_mask] = 0.0
+        predicted += pred_r  # all-reduce SUM
+    sum_exp = np.zeros(T)
+    for L in shifted:
+        sum_exp += np.exp(L).sum(axis=1)  # all-reduce SUM
+    loss = np.log(sum_exp) - predicted
+    return loss, logits_max + np.log(sum_exp)
+
+
+def vocab_parallel_cross_entropy_grad(X, E_shards, range_starts, targets, dloss):
+    """Gradient of the per-token losses w.r.t. each range's logits.
+
+    [Walkthrough] §_VocabParallelCrossEntropy backward: every logit gets its
+    softmax probability; the target position in the range that owns it gets
+    1 subtracted (a target in no range subtracts nothing); the result is
+    scaled by the upstream gradient of its token.  Returns the per-range
+    (T, |r|) blocks.
+    Pinned by: torch autograd of cross_entropy on the unsharded logits, and
+    the all-zero-logits closed form 1/V - onehot.
+    """
+    targets = np.asarray(targets, dtype=np.int64)
+    dloss = np.asarray(dloss, dtype=np.float64)
+    logits = [np.asarray(X, dtype=np.float64) @ np.asarray(Er, dtype=np.float64).T for Er in E_shards]
+    T = logits[0].shape[0]
+    logits_max = np.max(np.stack([L.max(axis=1) for L in logits]), axis=0)
+    exp_logits = [np.exp(L - logits_max[:, None]) for L in logits]
+    sum_exp = sum(e.sum(axis=1) for e in exp_logits)
+    rows = np.arange(T)
+    grads = []
+    for r, e in enumerate(exp_logits):
+        start, end = range_starts[r], range_starts[r + 1]
+        target_mask = (targets < start) | (targets >= end)
+        masked_target = np.where(target_mask, 0, targets - start)
+        g = e / sum_exp[:, None]  # softmax
+        g[rows, masked_target] -= 1.0 - target_mask.astype(np.float64)
+        grads.append(g * dloss[:, None])
+    return grads
+
+
+def logits_side_dx(dLogits_shards, E_shards):
+    """Input gradient of the tied output layer: dX = sum_r dLogits_r E_r.
+    The logits are a column-parallel linear over the vocabulary ([Study
+    notes] §交叉熵张量并行 stage 1, parallel_lm_logits), so its input gradient
+    is the sum over ranges of the per-range products (the f operator's
+    backward all-reduce, [Walkthrough] §ColumnParallelLinear).
+    Pinned by: equality with the unsharded dLogits E."""
+    return sum(np.asarray(dL, dtype=np.float64) @ np.asarray(Er, dtype=np.float64)
+               for dL, Er in zip(dLogits_shards, E_shards))
+
+
+# --------------------------------------------------------------------------
 # Closed forms the pages state
 # --------------------------------------------------------------------------
 def param_count(H, L, V):

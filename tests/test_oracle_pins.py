@@ -490,3 +490,128 @@ def test_planted_scatter_off_by_one_is_caught(monkeypatch):
         return out
     monkeypatch.setattr(O, "embed_scatter_grad", broken)
     assert check_scatter(O) > 1e-3
+
+
+# ----------------------------------------------------------------------------
+# Vocab-parallel cross-entropy
+# ----------------------------------------------------------------------------
+def tiny_ce(seed=0, T=6, h=5, V=13, ranges=(0, 4, 9, 13), scale=1.0):
+    g = rng(seed)
+    X = g.standard_normal((T, h))
+    E = g.standard_normal((V, h)) * scale
+    t = g.integers(0, V, T)
+    dl = g.standard_normal(T)
+    Es = [E[ranges[r]:ranges[r + 1]] for r in range(len(ranges) - 1)]
+    return X, E, Es, list(ranges), t, dl
+
+
+def check_ce_torch(mod, scale=1.0):
+    """Max |oracle - torch| of the loss and of its gradient (valid targets)."""
+    X, E, Es, r, t, dl = tiny_ce(scale=scale)
+    loss, lse = mod.vocab_parallel_cross_entropy(X, Es, r, t)
+    L = torch.tensor(X @ E.T, dtype=torch.float64, requires_grad=True)
+    ref = F.cross_entropy(L, torch.tensor(t), reduction="none")
+    (ref * torch.tensor(dl)).sum().backward()
+    g = np.concatenate(mod.vocab_parallel_cross_entropy_grad(X, Es, r, t, dl), axis=1)
+    e_lse = np.abs(lse - torch.logsumexp(L.detach(), dim=1).numpy()).max()
+    return max(np.abs(loss - ref.detach().numpy()).max(), np.abs(g - L.grad.numpy()).max(), e_lse)
+
+
+def test_ce_matches_torch_cross_entropy():
+    assert check_ce_torch(O) < 1e-12
+
+
+def test_ce_stable_at_large_logits():
+    # logits of order 1e3: exp without the max shift would overflow
+    assert check_ce_torch(O, scale=300.0) < 1e-9
+
+
+def test_ce_invariant_to_vocab_split():
+    X, E, _, _, t, dl = tiny_ce(1)
+    outs = []
+    for r in ([0, 13], [0, 6, 13], [0, 1, 2, 12, 13]):
+        Es = [E[r[i]:r[i + 1]] for i in range(len(r) - 1)]
+        loss, lse = O.vocab_parallel_cross_entropy(X, Es, r, t)
+        g = np.concatenate(O.vocab_parallel_cross_entropy_grad(X, Es, r, t, dl), axis=1)
+        outs.append((loss, lse, g))
+    for o in outs[1:]:
+        for a, b in zip(o, outs[0]):
+            assert np.abs(a - b).max() < 1e-12
+
+
+def test_ce_zero_logits_closed_form():
+    # all logits 0: loss = log V for every token, grad = (1/V - onehot) * dloss;
+    # a target in no range (the pages' masking): loss = log V, grad = dloss / V
+    T, h, V = 5, 3, 11
+    X = rng(2).standard_normal((T, h))
+    E = np.zeros((V, h))
+    t = np.array([0, 10, 5, -1, 11])
+    dl = np.arange(1.0, T + 1)
+    r = [0, 5, 11]
+    Es = [E[0:5], E[5:11]]
+    loss, lse = O.vocab_parallel_cross_entropy(X, Es, r, t)
+    assert np.allclose(loss, math.log(V), atol=1e-15) and np.allclose(lse, math.log(V), atol=1e-15)
+    g = np.concatenate(O.vocab_parallel_cross_entropy_grad(X, Es, r, t, dl), axis=1)
+    want = np.full((T, V), 1.0 / V)
+    for i, ti in enumerate(t):
+        if 0 <= ti < V:
+            want[i, ti] -= 1.0
+    want *= dl[:, None]
+    assert np.abs(g - want).max() < 1e-15
+
+
+def test_logits_side_dx_equals_unsharded():
+    X, E, Es, r, t, dl = tiny_ce(3)
+    g = O.vocab_parallel_cross_entropy_grad(X, Es, r, t, dl)
+    full = np.concatenate(g, axis=1) @ E
+    assert np.abs(O.logits_side_dx(g, Es) - full).max() < 1e-12
+
+
+def test_planted_unmasked_predicted_logit_is_caught(monkeypatch):
+    real = O.vocab_parallel_cross_entropy
+
+    def broken(X, E_shards, range_starts, targets):
+        # every range contributes its logit at the clamped index (mask dropped)
+        loss, lse = real(X, E_shards, range_starts, targets)
+        targets = np.asarray(targets)
+        extra = np.zeros(len(targets))
+        for r, Er in enumerate(E_shards):
+            s, e = range_starts[r], range_starts[r + 1]
+            out = (targets < s) | (targets >= e)
+            idx = np.clip(targets - s, 0, e - s - 1)
+            L = X @ Er.T - (lse - 0)[:, None]
+            extra += np.where(out, L[np.arange(len(targets)), idx], 0.0)
+        return loss - extra, lse
+    monkeypatch.setattr(O, "vocab_parallel_cross_entropy", broken)
+    assert check_ce_torch(O) > 1e-3
+
+
+def test_planted_missing_target_term_in_grad_is_caught(monkeypatch):
+    def broken(X, E_shards, range_starts, targets, dloss):
+        L = [X @ Er.T for Er in E_shards]
+        m = np.max(np.stack([l.max(axis=1) for l in L]), axis=0)
+        e = [np.exp(l - m[:, None]) for l in L]
+        s = sum(x.sum(axis=1) for x in e)
+        return [x / s[:, None] * np.asarray(dloss)[:, None] for x in e]  # softmax only
+    monkeypatch.setattr(O, "vocab_parallel_cross_entropy_grad", broken)
+    assert check_ce_torch(O) > 1e-3
+
+
+def test_planted_per_range_max_is_caught(monkeypatch):
+    def broken(X, E_shards, range_starts, targets):
+        # each range shifts by its own maximum, then the sums are added as if shared
+        targets = np.asarray(targets)
+        T = X.shape[0]
+        pred = np.zeros(T)
+        sum_exp = np.zeros(T)
+        for r, Er in enumerate(E_shards):
+            L = X @ Er.T
+            L = L - L.max(axis=1)[:, None]
+            s, e = range_starts[r], range_starts[r + 1]
+            inside = (targets >= s) & (targets < e)
+            idx = np.where(inside, targets - s, 0)
+            pred += np.where(inside, L[np.arange(T), idx], 0.0)
+            sum_exp += np.exp(L).sum(axis=1)
+        return np.log(sum_exp) - pred, np.log(sum_exp)
+    monkeypatch.setattr(O, "vocab_parallel_cross_entropy", broken)
+    assert check_ce_torch(O) > 1e-3
