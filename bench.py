@@ -340,7 +340,47 @@ class EmbedBench:
                 "embed_sort": ("hbm", self.T * 8.0 + self.T * 4.0 + (self.V + 1) * 4.0)}
 
 
-BENCHES = {"mlp": MLPBench, "attn": AttnBench, "embed": EmbedBench}
+class CEBench:
+    """Vocab-parallel cross-entropy: forward (loss without stored logits) and
+    backward (dLogits per range and the logits-side dX)."""
+    kind = "ce"
+
+    def __init__(self, name, tp, torch):
+        self.name, self.tp, self.torch = name, tp, torch
+        inp = SI.ce_inputs(SI.WORKLOADS[name])
+        d = lambda t: t.cuda().contiguous()
+        bf = torch.bfloat16
+        self.T, self.V, self.h, self.N, self.rs = inp["T"], inp["V"], inp["h"], inp["N"], inp["ranges"]
+        self.X, self.E = d(inp["X"]), [d(t) for t in inp["E_shards"]]
+        self.targets, self.dloss = d(inp["targets"]), d(inp["dloss"])
+        self.loss = torch.empty(self.T, device="cuda")
+        self.lse = torch.empty(self.T, device="cuda")
+        self.ws = torch.empty(tp.tp_vocab_cross_entropy_workspace_size(self.T, self.V, self.rs),
+                              dtype=torch.uint8, device="cuda")
+        widths = [self.rs[r + 1] - self.rs[r] for r in range(self.N)]
+        self.dL = [torch.empty(self.T, tp.logits_pitch(w, bf), dtype=bf, device="cuda") for w in widths]
+        self.dX = torch.empty(self.T, self.h, dtype=bf, device="cuda")
+        self.parts = sum((w + 63) // 64 for w in widths)
+
+    def step(self):
+        tp = self.tp
+        tp.tp_vocab_cross_entropy_fwd(self.X, self.E, self.rs, self.targets, self.loss, self.lse, self.ws)
+        tp.tp_vocab_cross_entropy_bwd(self.X, self.E, self.rs, self.targets, self.lse, self.dloss,
+                                      self.dL, self.dX)
+
+    def units(self):
+        # forward logits, recomputed logits, dX = sum_r dLogits_r E_r
+        return 6.0 * self.T * self.V * self.h, "TFLOP/s", 1e12
+
+    def kernel_work(self):
+        f = 2.0 * self.T * self.V * self.h
+        # the reduction reads every (max, sum) pair and the target logit, reads
+        # the targets and writes loss and lse
+        red = self.parts * self.T * 8.0 + self.T * (4.0 + 8.0 + 4.0 + 4.0)
+        return {"gemm_ce_fwd": ("tensor", f), "gemm_ce_bwd": ("tensor", 2 * f), "ce_reduce": ("hbm", red)}
+
+
+BENCHES = {"mlp": MLPBench, "attn": AttnBench, "embed": EmbedBench, "ce": CEBench}
 
 
 def time_steps(torch, fn, steps, warmup, flush):
@@ -645,8 +685,8 @@ def gather_row(tp, torch, b, name, peaks, peak_src, sets=4, per_graph=16, replay
 def secondary_rows(tp, torch, flush, peaks, peak_src, main_workload):
     """The other rows of the block, each on its own workload, a few timed steps."""
     rows = {}
-    for name in ("embed_tied_V50257_h4096_T8192", "attn_b1_s2048_h4096_heads8_N8",
-                 "mlp_b2_s2048_h4096_hp16384_N2"):
+    for name in ("embed_tied_V50257_h4096_T8192", "ce_V50257_h4096_T8192",
+                 "attn_b1_s2048_h4096_heads8_N8", "mlp_b2_s2048_h4096_hp16384_N2"):
         if name == main_workload:
             continue
         cfg = SI.WORKLOADS[name]

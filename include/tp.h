@@ -198,6 +198,61 @@ TP_API tp_status tp_vocab_logits(tp_dtype dt, int64_t T, int64_t h, int64_t V, i
                           void* const* logits, const int64_t* ld_logits, void* stream);
 
 /*
+ * tp_vocab_cross_entropy_fwd -- per-token loss of the vocab-parallel
+ * cross-entropy without storing the logits.
+ * [Walkthrough] §_VocabParallelCrossEntropy forward; [Study notes]
+ * §交叉熵张量并行 stages 1-4; [TP notes] §Cross-entropy层 (no all-gather of
+ * the (b, s, v) logits).  The logits GEMM per range runs with an epilogue that
+ * keeps each 64-column part of a row on chip and writes only its (max, sum of
+ * exp(logit - max)) and, where the row's target falls in it, the target logit;
+ * a reduction kernel then merges the parts in fixed order (the all-reduce MAX
+ * and SUM of the pages) and computes
+ *   lse[t]  = max_t + log(sum_t)
+ *   loss[t] = log(sum_t) - (logit[t, target_t] - max_t)   (0 <= target_t < V)
+ *   loss[t] = log(sum_t)                                  (target in no range,
+ *                                                          the pages' masking)
+ * Logits are fp32 accumulations of bf16 inputs and never rounded to bf16.
+ * Arguments: X (T, h) bf16; E shard array (|r|, h) bf16; range_starts host
+ *   int64[N+1]; targets (T) int64 device; loss, lse (T) fp32 device out;
+ *   workspace of tp_vocab_cross_entropy_workspace_size bytes, 256-byte aligned
+ *   (TP_ERR_WORKSPACE if smaller or NULL, TP_ERR_ALIGN if misaligned).
+ * bf16 only (TP_ERR_UNSUPPORTED for fp32).  Deterministic.
+ */
+TP_API tp_status tp_vocab_cross_entropy_fwd(tp_dtype dt, int64_t T, int64_t h, int64_t V, int N,
+                                     const void* X, const void* const* E,
+                                     const int64_t* range_starts, const int64_t* targets,
+                                     float* loss, float* lse, void* workspace,
+                                     size_t workspace_bytes, void* stream);
+
+/* Bytes of the forward's workspace: (max, sum) fp32 pairs for every row and
+ * 64-column part of every range, plus one fp32 target logit per row, each
+ * block rounded up to 256 bytes.  0 for invalid sizes or ranges. */
+TP_API size_t tp_vocab_cross_entropy_workspace_size(int64_t T, int64_t V, int N,
+                                                    const int64_t* range_starts);
+
+/*
+ * tp_vocab_cross_entropy_bwd -- gradient of the per-token losses.
+ * [Walkthrough] §_VocabParallelCrossEntropy backward (softmax, minus 1 at the
+ * target in the range that owns it, times the upstream gradient); the
+ * logits-side input gradient sums the ranges' products ([Walkthrough]
+ * §ColumnParallelLinear backward all-reduce).  One launch (two for large
+ * sizes): the logits are recomputed per range with the epilogue
+ *   dLogits_r[t, v] = (exp(logit - lse[t]) - [s_r + v == target_t]) * dloss[t]
+ * and, if dX is given, dX = sum_r dLogits_r E_r with each row block starting
+ * once its dLogits rows are stored.  dLogits feed tied_embed_grad for dE.
+ * Arguments: X, E, range_starts, targets as in the forward; lse (T) fp32 from
+ *   the forward; dloss (T) fp32; dLogits shard array, block r (T, |r|) bf16
+ *   out with pitch ld_dlogits[r] (host int64[N], >= |r|, a multiple of 8);
+ *   dX (T, h) bf16 out or NULL.  bf16 only.
+ */
+TP_API tp_status tp_vocab_cross_entropy_bwd(tp_dtype dt, int64_t T, int64_t h, int64_t V, int N,
+                                     const void* X, const void* const* E,
+                                     const int64_t* range_starts, const int64_t* targets,
+                                     const float* lse, const float* dloss,
+                                     void* const* dLogits, const int64_t* ld_dlogits, void* dX,
+                                     void* stream);
+
+/*
  * tied_embed_grad -- gradient of the word embedding shared by the input and
  * output layers: the sum of both contributions ([TP notes] §输出层Embedding).
  *   dE[v] = sum_{t : id_t = v} dEmb[t]  +  sum_t dLogits[t, v] X[t, :]

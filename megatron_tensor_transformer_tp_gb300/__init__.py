@@ -20,6 +20,8 @@ __all__ = [
     "TP_ERR_TIMEOUT", "TP_ERR_WORKSPACE", "TP_ERR_ALIGN", "TP_F32", "TP_BF16",
     "tp_mlp_fwd", "tp_mlp_bwd", "tp_attn_proj_fwd", "tp_attn_proj_bwd", "vocab_parallel_embed",
     "tp_vocab_logits", "tied_embed_grad", "tied_embed_grad_workspace_size",
+    "tp_vocab_cross_entropy_fwd", "tp_vocab_cross_entropy_bwd",
+    "tp_vocab_cross_entropy_workspace_size",
     "tied_embed_grad_noalloc", "tp_get_status",
     "tp_status_string", "tp_num_sms", "tp_profile_enable", "tp_profile_reset", "tp_profile_read",
     "tp_debug_inject_fault", "tp_debug_set_wait_limit_ms", "tp_debug_set_gemm_kernel",
@@ -53,6 +55,13 @@ _SIGNATURES = {
     "tied_embed_grad": (_int, [_int, _i64, _i64, _i64, _int, _c_void_p, _c_void_p, _c_void_p, _PP,
                                _PI64, _PI64, _PP, _int, _c_void_p, _size_t, _c_void_p]),
     "tied_embed_grad_workspace_size": (_size_t, [_i64, _i64]),
+    "tp_vocab_cross_entropy_fwd": (_int, [_int, _i64, _i64, _i64, _int, _c_void_p, _PP, _PI64,
+                                          _c_void_p, _c_void_p, _c_void_p, _c_void_p, _size_t,
+                                          _c_void_p]),
+    "tp_vocab_cross_entropy_workspace_size": (_size_t, [_i64, _i64, _int, _PI64]),
+    "tp_vocab_cross_entropy_bwd": (_int, [_int, _i64, _i64, _i64, _int, _c_void_p, _PP, _PI64,
+                                          _c_void_p, _c_void_p, _c_void_p, _PP, _PI64, _c_void_p,
+                                          _c_void_p]),
     "tied_embed_grad_noalloc": (_int, [_int, _i64, _i64, _i64, _int, _c_void_p, _c_void_p,
                                        _c_void_p, _PP, _PI64, _PI64, _PP, _int, _c_void_p]),
     "tp_get_status": (_int, [_c_void_p]),
@@ -241,6 +250,50 @@ def tp_vocab_logits(X, E, range_starts, logits, stream=None):
     _check(lib().tp_vocab_logits(_dtype(X), T, h, V, N, _dev(X, "X"), e[0], rs, lg[0], ld,
                                  _stream(stream)),
            "tp_vocab_logits")
+
+
+def tp_vocab_cross_entropy_workspace_size(T: int, V: int, range_starts) -> int:
+    rs = _i64s(range_starts)
+    return int(lib().tp_vocab_cross_entropy_workspace_size(T, V, len(range_starts) - 1, rs))
+
+
+def tp_vocab_cross_entropy_fwd(X, E, range_starts, targets, loss, lse, workspace, stream=None):
+    """loss, lse (T,) fp32 <- vocab-parallel cross-entropy of the logits X E_r^T
+    (never stored); workspace: CUDA uint8 tensor of
+    tp_vocab_cross_entropy_workspace_size bytes."""
+    T, h = X.shape
+    N = len(E)
+    V = int(range_starts[-1])
+    if targets.dtype != torch.int64:
+        raise TypeError("targets must be int64")
+    if workspace.dtype != torch.uint8:
+        raise TypeError("workspace must be a uint8 tensor")
+    e = _ptrs(E, "E")
+    rs = _i64s(range_starts)
+    _check(lib().tp_vocab_cross_entropy_fwd(_dtype(X), T, h, V, N, _dev(X, "X"), e[0], rs,
+                                            _dev(targets, "targets"), _dev(loss, "loss"),
+                                            _dev(lse, "lse"), _dev(workspace, "workspace"),
+                                            workspace.numel(), _stream(stream)),
+           "tp_vocab_cross_entropy_fwd")
+
+
+def tp_vocab_cross_entropy_bwd(X, E, range_starts, targets, lse, dloss, dLogits, dX=None,
+                               stream=None):
+    """dLogits (per-range (T, pitch_r) bf16; columns [0, |r|) written) and, if
+    given, dX (T, h) <- gradient of the per-token losses scaled by dloss."""
+    T, h = X.shape
+    N = len(E)
+    V = int(range_starts[-1])
+    if targets.dtype != torch.int64:
+        raise TypeError("targets must be int64")
+    e, dl = _ptrs(E, "E"), _ptrs(dLogits, "dLogits")
+    rs = _i64s(range_starts)
+    ld = _i64s([t.shape[1] for t in dLogits])
+    _check(lib().tp_vocab_cross_entropy_bwd(_dtype(X), T, h, V, N, _dev(X, "X"), e[0], rs,
+                                            _dev(targets, "targets"), _dev(lse, "lse"),
+                                            _dev(dloss, "dloss"), dl[0], ld, _dev(dX, "dX"),
+                                            _stream(stream)),
+           "tp_vocab_cross_entropy_bwd")
 
 
 def tied_embed_grad_workspace_size(T, V) -> int:

@@ -277,6 +277,7 @@ struct Plan {
 };
 
 inline bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline bool al256(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 255u) == 0; }
 
 bool group_vec_ok(const GemmGroup& g, int in_esize) {
   const int oes = g.out_type == OUT_F32 ? 4 : 2;
@@ -809,6 +810,118 @@ extern "C" tp_status tp_vocab_logits(tp_dtype dt, int64_t T, int64_t h, int64_t 
     p.add_group(T, nr, si, si + 1, EPI_STORE, ot, logits[r], ld_logits[r]);
   }
   return run_plan(p, dt, "gemm_logits", s);
+}
+
+// ===========================================================================
+// Vocab-parallel cross-entropy
+// ===========================================================================
+namespace {
+int64_t ce_parts(const int64_t* rs, int N) {
+  int64_t P = 0;
+  for (int r = 0; r < N; ++r) P += (rs[r + 1] - rs[r] + 63) / 64;
+  return P;
+}
+size_t round256(size_t b) { return (b + 255) / 256 * 256; }
+
+bool ce_args_ok(int64_t T, int64_t h, int64_t V, int N, const void* X, const void* const* E,
+                const int64_t* rs, const int64_t* targets) {
+  if (T < 0 || h <= 0 || V <= 0 || N > kMaxGroups || !ranges_ok(rs, N, V) || !shards_ok(E, N))
+    return false;
+  if (T > INT32_MAX || V > INT32_MAX || h > INT32_MAX) return false;
+  return T == 0 || (X != nullptr && targets != nullptr);
+}
+}  // namespace
+
+extern "C" size_t tp_vocab_cross_entropy_workspace_size(int64_t T, int64_t V, int N,
+                                                        const int64_t* range_starts) {
+  if (T <= 0 || V <= 0 || N < 1 || N > kMaxGroups || !ranges_ok(range_starts, N, V)) return 0;
+  return round256(static_cast<size_t>(ce_parts(range_starts, N)) * static_cast<size_t>(T) * 8) +
+         round256(static_cast<size_t>(T) * 4);
+}
+
+extern "C" tp_status tp_vocab_cross_entropy_fwd(tp_dtype dt, int64_t T, int64_t h, int64_t V, int N,
+                                                const void* X, const void* const* E,
+                                                const int64_t* range_starts, const int64_t* targets,
+                                                float* loss, float* lse, void* workspace,
+                                                size_t workspace_bytes, void* stream) {
+  if (!dtype_ok(dt)) return TP_ERR_UNSUPPORTED;
+  if (!ce_args_ok(T, h, V, N, X, E, range_starts, targets)) return TP_ERR_INVALID;
+  if (T > 0 && (loss == nullptr || lse == nullptr)) return TP_ERR_INVALID;
+  if (T == 0) return TP_OK;
+  if (dt != TP_BF16) return TP_ERR_UNSUPPORTED;  // the fused epilogue lives in the tensor-core engine
+  const size_t need = tp_vocab_cross_entropy_workspace_size(T, V, N, range_starts);
+  if (workspace == nullptr || workspace_bytes < need) return TP_ERR_WORKSPACE;
+  if (!al256(workspace)) return TP_ERR_ALIGN;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int64_t P = ce_parts(range_starts, N);
+  float* part = static_cast<float*>(workspace);
+  float* tlogit = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
+                                           round256(static_cast<size_t>(P) * T * 8));
+  // Logits per range with the cross-entropy epilogue: no logits are stored.
+  Plan p;
+  int64_t part0 = 0;
+  for (int r = 0; r < N; ++r) {
+    const int64_t nr = range_starts[r + 1] - range_starts[r];
+    const int si = p.add_seg(kmajor(X, T, h, h), kmajor(E[r], nr, h, h), h);
+    GemmGroup& g = p.add_group(T, nr, si, si + 1, EPI_CE_FWD, OUT_F32, nullptr, 0);
+    g.col0 = range_starts[r];
+    g.row_target = targets;
+    g.ce_part = part;
+    g.ce_target = tlogit;
+    g.ce_part0 = static_cast<int>(part0);
+    g.ce_rows = static_cast<int>(T);
+    part0 += (nr + 63) / 64;
+  }
+  tp_status st = run_plan(p, dt, "gemm_ce_fwd", s);
+  if (st != TP_OK) return st;
+  const cudaError_t e = timed("ce_reduce", s, [&] {
+    return launch_ce_reduce(part, static_cast<int>(P), T, targets, V, tlogit, loss, lse, s);
+  });
+  return e == cudaSuccess ? TP_OK : TP_ERR_CUDA;
+}
+
+extern "C" tp_status tp_vocab_cross_entropy_bwd(tp_dtype dt, int64_t T, int64_t h, int64_t V, int N,
+                                                const void* X, const void* const* E,
+                                                const int64_t* range_starts, const int64_t* targets,
+                                                const float* lse, const float* dloss,
+                                                void* const* dLogits, const int64_t* ld_dlogits,
+                                                void* dX, void* stream) {
+  if (!dtype_ok(dt)) return TP_ERR_UNSUPPORTED;
+  if (!ce_args_ok(T, h, V, N, X, E, range_starts, targets) || ld_dlogits == nullptr)
+    return TP_ERR_INVALID;
+  if (T > 0 && (lse == nullptr || dloss == nullptr || !shards_ok(dLogits, N))) return TP_ERR_INVALID;
+  for (int r = 0; r < N; ++r)
+    if (ld_dlogits[r] < range_starts[r + 1] - range_starts[r]) return TP_ERR_INVALID;
+  if (T == 0) return TP_OK;
+  if (dt != TP_BF16) return TP_ERR_UNSUPPORTED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  Plan p;
+  const int rows = p.counters((T + 255) / 256 * 2);  // 128-row blocks, pair tiles rounded up
+  // dLogits_r = (softmax - onehot) * dloss, the logits recomputed per range.
+  for (int r = 0; r < N; ++r) {
+    const int64_t nr = range_starts[r + 1] - range_starts[r];
+    const int si = p.add_seg(kmajor(X, T, h, h), kmajor(E[r], nr, h, h), h);
+    GemmGroup& g = p.add_group(T, nr, si, si + 1, EPI_CE_BWD, OUT_BF16, dLogits[r], ld_dlogits[r]);
+    g.col0 = range_starts[r];
+    g.row_target = targets;
+    g.row_lse = lse;
+    g.row_dloss = dloss;
+    g.prod_row = dX ? rows : -1;
+  }
+  p.interleave = N;
+  // dX = sum_r dLogits_r E_r: the output layer's input gradient, summed over
+  // ranges; a row block starts once its dLogits rows are stored.
+  if (dX) {
+    const int s0 = p.ns;
+    for (int r = 0; r < N; ++r) {
+      const int64_t nr = range_starts[r + 1] - range_starts[r];
+      p.add_seg(kmajor(dLogits[r], T, nr, ld_dlogits[r]), mnmajor(E[r], nr, h, h), nr);
+    }
+    GemmGroup& gx = p.add_group(T, h, s0, s0 + N, EPI_STORE, OUT_BF16, dX, h);
+    gx.dep_kind = DEP_ROW;
+    gx.dep_base = rows;
+  }
+  return run_plan(p, dt, "gemm_ce_bwd", s);
 }
 
 extern "C" size_t tied_embed_grad_workspace_size(int64_t T, int64_t V) {

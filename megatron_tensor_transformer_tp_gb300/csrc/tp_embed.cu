@@ -245,4 +245,66 @@ cudaError_t launch_segment_sum(const void* ws, int64_t V, int64_t T, const void*
   return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------------------
+// Vocab-parallel cross-entropy: combine the per-part (max, sum exp) pairs of
+// each row in fixed part order (the on-chip form of the all-reduce MAX and the
+// all-reduce SUM of [Walkthrough] §_VocabParallelCrossEntropy), then
+// loss = log(sum) - (target logit - max) and lse = max + log(sum).  A block
+// covers 32 rows with 32 slices of the parts each; slices merge in order.
+// ---------------------------------------------------------------------------
+namespace {
+
+__device__ __forceinline__ void lse_merge(float& m, float& s, float mj, float sj) {
+  if (mj == -INFINITY) return;  // an empty slice (no parts)
+  if (mj > m) {
+    s = s * expf(m - mj) + sj;
+    m = mj;
+  } else {
+    s += sj * expf(mj - m);
+  }
+}
+
+constexpr int CE_SLICES = 32;
+
+__global__ void __launch_bounds__(32 * CE_SLICES) ce_reduce_kernel(const float2* __restrict__ part, int P, int64_t T,
+                                                        const int64_t* __restrict__ targets, int64_t V,
+                                                        const float* __restrict__ target_logit,
+                                                        float* __restrict__ loss, float* __restrict__ lse) {
+  __shared__ float sm[CE_SLICES][32], ss[CE_SLICES][32];
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * 32 + tx;
+  float m = -INFINITY, s = 0.f;
+  if (row < T) {
+    const int p0 = static_cast<int>(static_cast<int64_t>(P) * ty / CE_SLICES);
+    const int p1 = static_cast<int>(static_cast<int64_t>(P) * (ty + 1) / CE_SLICES);
+    for (int p = p0; p < p1; ++p) {
+      const float2 v = part[static_cast<int64_t>(p) * T + row];
+      lse_merge(m, s, v.x, v.y);
+    }
+  }
+  sm[ty][tx] = m;
+  ss[ty][tx] = s;
+  __syncthreads();
+  if (ty == 0 && row < T) {
+    float M = sm[0][tx], S = ss[0][tx];
+    for (int k = 1; k < CE_SLICES; ++k) lse_merge(M, S, sm[k][tx], ss[k][tx]);
+    const float log_s = logf(S);
+    const int64_t t = targets[row];
+    // a target in no range: predicted (shifted) logit 0, so loss = log(sum)
+    loss[row] = (t >= 0 && t < V) ? log_s - (target_logit[row] - M) : log_s;
+    lse[row] = M + log_s;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_ce_reduce(const void* part, int P, int64_t T, const int64_t* targets, int64_t V,
+                             const float* target_logit, float* loss, float* lse, cudaStream_t s) {
+  if (T <= 0) return cudaSuccess;
+  ce_reduce_kernel<<<static_cast<unsigned>((T + 31) / 32), 32 * CE_SLICES, 0, s>>>(
+      static_cast<const float2*>(part), P, T, targets, V, target_logit, loss, lse);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
 }  // namespace tp

@@ -477,6 +477,31 @@ __device__ __forceinline__ void epilogue_chunk(const GemmGroup& G, uint4* st, in
       }
       break;
     }
+    case EPI_CE_BWD: {
+      // dlogit = (softmax - onehot(target)) * dloss, softmax = 2^((acc - lse) log2 e)
+      float lse = 0.f, dl = 0.f;
+      int64_t tgt = -1;
+      if (row_ok) {
+        lse = G.row_lse[row];
+        dl = G.row_dloss[row];
+        tgt = G.row_target[row] - G.col0;
+        tgt = tgt < G.N ? tgt - n : -1;  // a target in a later range is no column here
+      }
+      const float l2e = 1.4426950408889634f;
+      const float base = -lse * l2e;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        float pj = ex2_ftz(fmaf(v[j], l2e, base));
+        if (tgt == j) pj -= 1.f;
+        v[j] = pj * dl;
+      }
+      if (coal) {
+        stage_store_rows(st, G.out, OUT_BF16, G.ldo, row0, G.M, n, v, lane);
+      } else if (row_ok) {
+        store_chunk(G.out, OUT_BF16, G.ldo, row, n, v, ncols, false);
+      }
+      break;
+    }
     case EPI_F32:
     case EPI_SEGSUM: {
       if (G.epi == EPI_SEGSUM && row_ok) {
@@ -606,6 +631,52 @@ __device__ __forceinline__ bool produce_segment(ProdRing& R, const WaitCtx& wctx
     default: return TP_PRODUCE(2, 3);
   }
 #undef TP_PRODUCE
+}
+
+// ---------------------------------------------------------------------------
+// Cross-entropy forward epilogue of one warp's region: its 32 rows (lane =
+// row) and 64 columns [n0 + 32 c_begin, +64), one "part" of the row.  The
+// logits stay in TMEM and registers: the warp writes the part's (max, sum of
+// exp(logit - max)) per row, and the logit at the row's target column when
+// the target lies in the part.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void ce_fwd_epilogue_warp(const GemmGroup& G, int lane, int row0, int n0,
+                                                     int c_begin, int cpw, uint32_t taddr) {
+  const int nb = n0 + c_begin * 32;
+  if (nb >= G.N) return;  // warp-uniform: no part here
+  const int row = row0 + lane;
+  const bool row_ok = row < G.M;
+  int64_t tgt = row_ok ? G.row_target[row] - G.col0 : -1;
+  if (tgt >= G.N) tgt = -1;  // the target is in a later range (the tile's zero-filled columns)
+  const float l2e = 1.4426950408889634f;
+  float m = -INFINITY, s = 0.f;
+  for (int c = c_begin; c < c_begin + cpw; ++c) {
+    const int n = n0 + c * 32;
+    if (n >= G.N) break;  // warp-uniform
+    const int ncols = min(32, G.N - n);
+    uint32_t rr[32];
+    tmem_ld32(taddr + static_cast<uint32_t>(c * 32), rr);
+    float mx = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (j < ncols) mx = fmaxf(mx, __uint_as_float(rr[j]));
+    const int64_t tj = tgt - n;
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (tj == j && row_ok) G.ce_target[row] = __uint_as_float(rr[j]);
+    const float nm = fmaxf(m, mx);
+    float acc = s * ex2_ftz((m - nm) * l2e);
+    const float base = -nm * l2e;
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (j < ncols) acc += ex2_ftz(fmaf(__uint_as_float(rr[j]), l2e, base));
+    m = nm;
+    s = acc;
+  }
+  if (row_ok) {
+    const int64_t part = G.ce_part0 + nb / 64;
+    reinterpret_cast<float2*>(G.ce_part)[part * G.ce_rows + row] = make_float2(m, s);
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -828,7 +899,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
       const int row0 = tc.m0 + quarter * 32;
       const uint32_t taddr =
           tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(buf * BN);
-      for (int c = c_begin; c < c_begin + cpw; ++c) {
+      if (G.epi == EPI_CE_FWD) ce_fwd_epilogue_warp(G, lane, row0, tc.n0, c_begin, cpw, taddr);
+      for (int c = c_begin; G.epi != EPI_CE_FWD && c < c_begin + cpw; ++c) {
         const int n = tc.n0 + c * 32;
         if (n >= G.N) break;  // warp-uniform
         uint32_t rr[32];
@@ -1323,7 +1395,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_pair_kernel(const __gr
       const int row0 = tc.m0 + 128 * static_cast<int>(rank) + quarter * 32;
       const uint32_t taddr =
           tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(buf * BN);
-      for (int c = c_begin; c < c_begin + cpw; ++c) {
+      if (G.epi == EPI_CE_FWD) ce_fwd_epilogue_warp(G, lane, row0, tc.n0, c_begin, cpw, taddr);
+      for (int c = c_begin; G.epi != EPI_CE_FWD && c < c_begin + cpw; ++c) {
         const int n = tc.n0 + c * 32;
         if (n >= G.N) break;  // warp-uniform
         uint32_t rr[32];

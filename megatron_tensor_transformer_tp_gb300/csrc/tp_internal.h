@@ -22,7 +22,10 @@ enum Epi : int {
   EPI_BIAS_GELU = 1,  // z = acc + bias[n]; out = z, out2 = GELU(z)
   EPI_DGELU = 2,      // out = acc * GELU'(aux[m, n])
   EPI_F32 = 3,        // out (f32) = acc (+ out if accumulate)
-  EPI_SEGSUM = 4      // out (f32) = acc + sum_{j in seg(row)} seg_src[perm[j], n] (+ out)
+  EPI_SEGSUM = 4,     // out (f32) = acc + sum_{j in seg(row)} seg_src[perm[j], n] (+ out)
+  EPI_CE_FWD = 5,     // cross-entropy partials: per row and 64-column part, (max, sum exp(acc - max))
+                      // to ce_part; the logit at the row's target column to ce_target; no output
+  EPI_CE_BWD = 6      // out (bf16) = (exp(acc - row_lse[m]) - [col0 + n == row_target[m]]) * row_dloss[m]
 };
 
 enum OutType : int { OUT_BF16 = 0, OUT_F32 = 1 };
@@ -56,6 +59,17 @@ struct GemmGroup {
   const void* seg_src;
   int64_t ld_seg;
   int64_t seg_row0;
+  // EPI_CE_FWD / EPI_CE_BWD: global column of the group's column 0 (its
+  // vocabulary range start), per-row target ids; the forward writes part
+  // (ce_part0 + n / 64) of row m at ce_part[2 * (part * ce_rows + m)] (max,
+  // sum); the backward reads row_lse and row_dloss.
+  int64_t col0;
+  const int64_t* row_target;
+  const float* row_lse;
+  const float* row_dloss;
+  float* ce_part;
+  float* ce_target;
+  int ce_part0, ce_rows;
 };
 
 // One operand pair of the tensor-core engine.  Operands are bf16.
@@ -122,6 +136,8 @@ cudaError_t launch_embed_gather(const int64_t* ids, int64_t T, int64_t row_bytes
 // Grouping of tokens by id.  ws holds offsets[V+1], perm[T], counts[V].
 size_t sort_workspace_bytes(int64_t T, int64_t V);
 cudaError_t launch_embed_sort(const int64_t* ids, int64_t T, int64_t V, void* ws, cudaStream_t s);
+cudaError_t launch_ce_reduce(const void* part, int P, int64_t T, const int64_t* targets, int64_t V,
+                             const float* target_logit, float* loss, float* lse, cudaStream_t s);
 int* sort_offsets(void* ws);
 int* sort_perm(void* ws, int64_t V);
 // Input-side embedding gradient alone: dE_r rows = segment sums (+ old).

@@ -45,6 +45,9 @@ WORKLOADS = {
     # bf16 vocab-parallel tied embedding: V=50257, h=4096, b=4, s=2048, two ranges
     "embed_tied_V50257_h4096_T8192": dict(kind="embed", dtype="bf16", V=50257, h=4096, b=4,
                                           s=2048, ranges=[0, 25129, 50257], seed=1004),
+    # bf16 vocab-parallel cross-entropy on the same output layer: T=8192 tokens, two ranges
+    "ce_V50257_h4096_T8192": dict(kind="ce", dtype="bf16", V=50257, h=4096, b=4, s=2048,
+                                  ranges=[0, 25129, 50257], seed=1005),
 }
 
 _TORCH_DTYPE = {"f32": torch.float32, "bf16": torch.bfloat16}
@@ -168,3 +171,19 @@ def embed_inputs(cfg: dict, T: int | None = None) -> dict:
     dL_shards = [dLogits[:, ranges[r]:ranges[r + 1]].contiguous() for r in range(len(ranges) - 1)]
     return dict(T=T, V=V, h=h, N=len(ranges) - 1, dtype=dt, ranges=ranges, ids=ids, E=E,
                 E_shards=E_shards, X=X, dEmb=dEmb, dLogits=dLogits, dLogits_shards=dL_shards)
+
+
+def ce_inputs(cfg: dict) -> dict:
+    """Inputs of the vocab-parallel cross-entropy: the last hidden state X
+    (T, h) ~ N(0, 1), the tied embedding E (V, h) ~ N(0, 0.02) split into its
+    vocabulary ranges, targets uniform in [0, V), and the upstream gradient of
+    the mean loss, dloss = 1/T per token (fp32)."""
+    dt, seed = cfg["dtype"], cfg["seed"]
+    T, h, V, ranges = cfg["b"] * cfg["s"], cfg["h"], cfg["V"], list(cfg["ranges"])
+    X = normal(seed, 31, (T, h), 1.0, dt)
+    E = normal(seed, 32, (V, h), 0.02, dt)
+    targets = uniform_ids(seed, 33, T, V)
+    dloss = torch.full((T,), 1.0 / T, dtype=torch.float32)
+    E_shards = [E[ranges[r]:ranges[r + 1]].contiguous() for r in range(len(ranges) - 1)]
+    return dict(T=T, h=h, V=V, N=len(ranges) - 1, ranges=ranges, X=X, E=E, E_shards=E_shards,
+                targets=targets, dloss=dloss)

@@ -122,3 +122,29 @@ def test_logits_pitch_rule():
     assert tp.logits_pitch(25129, torch.bfloat16) == 25136
     assert tp.logits_pitch(25128, torch.bfloat16) == 25128
     assert tp.logits_pitch(150, torch.float32) == 152
+
+
+def test_cross_entropy_validation_and_workspace_size():
+    e = ptrs(2)
+    rs = rs_arr([0, 100, 250])
+    T, V = 64, 250
+    need = tp.tp_vocab_cross_entropy_workspace_size(T, V, [0, 100, 250])
+    # (max, sum) pairs for ceil(100/64) + ceil(150/64) = 5 parts per row, plus a
+    # target logit per row, each block rounded up to 256 bytes
+    assert need == (5 * T * 8 + 255) // 256 * 256 + (T * 4 + 255) // 256 * 256
+    assert tp.tp_vocab_cross_entropy_workspace_size(T, V, [0, 100, 251]) == 0  # bad ranges
+
+    def fwd(dt=tp.TP_BF16, ws=FAKE, nbytes=need, V=V, rs=rs):
+        return L.tp_vocab_cross_entropy_fwd(dt, T, 64, V, 2, FAKE, e[0], rs, FAKE, FAKE, FAKE,
+                                            ws, nbytes, None)
+    assert fwd(dt=tp.TP_F32) == tp.TP_ERR_UNSUPPORTED
+    assert fwd(ws=None) == tp.TP_ERR_WORKSPACE
+    assert fwd(nbytes=need - 1) == tp.TP_ERR_WORKSPACE
+    assert fwd(ws=FAKE + 16) == tp.TP_ERR_ALIGN
+    assert fwd(V=251) == tp.TP_ERR_INVALID
+    ld = rs_arr([104, 152])
+    assert L.tp_vocab_cross_entropy_bwd(tp.TP_F32, T, 64, V, 2, FAKE, e[0], rs, FAKE, FAKE, FAKE,
+                                        e[0], ld, None, None) == tp.TP_ERR_UNSUPPORTED
+    short = rs_arr([104, 144])  # pitch below the second range's width
+    assert L.tp_vocab_cross_entropy_bwd(tp.TP_BF16, T, 64, V, 2, FAKE, e[0], rs, FAKE, FAKE, FAKE,
+                                        e[0], short, None, None) == tp.TP_ERR_INVALID
