@@ -452,6 +452,107 @@ def logits_side_dx(dLogits_shards, E_shards):
 
 
 # --------------------------------------------------------------------------
+# Mixed-precision optimizer step
+# --------------------------------------------------------------------------
+def grad_scaler_update(state, found_inf, cfg):
+    """Dynamic loss-scale update ([Walkthrough] §DynamicGradScaler.update).
+
+    On an overflow the growth tracker resets and the hysteresis tracker counts
+    down; once it is <= 0 the scale backs off (times backoff_factor, not below
+    min_scale), and keeps backing off on further overflows until a growth
+    resets the tracker.  growth_interval overflow-free steps in a row multiply
+    the scale by growth_factor and reset both trackers.  Returns a new dict.
+    Pinned by: the growth, hysteresis, back-off and floor behaviours the page
+    states, step by step.
+    """
+    s = dict(state)
+    if found_inf:
+        s["growth_tracker"] = 0
+        s["hysteresis_tracker"] -= 1
+        if s["hysteresis_tracker"] <= 0:
+            s["scale"] = max(s["scale"] * cfg["backoff_factor"], cfg["min_scale"])
+    else:
+        s["growth_tracker"] += 1
+        if s["growth_tracker"] == cfg["growth_interval"]:
+            s["growth_tracker"] = 0
+            s["hysteresis_tracker"] = cfg["hysteresis"]
+            s["scale"] = s["scale"] * cfg["growth_factor"]
+    return s
+
+
+def unscale_and_check(grads, scale):
+    """Main gradients divided by the loss scale, and whether any is inf/nan
+    across all groups ([Walkthrough] §MixedPrecisionOptimizer.step, step 2)."""
+    out = [np.asarray(g, dtype=np.float64) / scale for g in grads]
+    found_inf = any(not np.all(np.isfinite(g)) for g in out)
+    return out, found_inf
+
+
+def clip_by_global_norm(grads, max_norm):
+    """Gradient clipping by the L2 norm of all gradients as one vector
+    ([Study notes] §梯度裁剪: if ||g|| > max_norm, g <- g * max_norm / ||g||;
+    otherwise unchanged; max_norm <= 0 disables).  Returns (grads, ||g||).
+    Pinned by: a closed form (||g|| = 5 scaled to 1) and torch
+    clip_grad_norm_ (which adds 1e-6 to the norm: 2e-7 relative here)."""
+    total = math.sqrt(sum(float(np.sum(np.asarray(g, dtype=np.float64) ** 2)) for g in grads))
+    if max_norm > 0 and total > max_norm:
+        grads = [np.asarray(g, dtype=np.float64) * (max_norm / total) for g in grads]
+    return grads, total
+
+
+def adam_update(param, grad, m, v, step, cfg, weight_decay):
+    """One Adam update of one tensor ([Study notes] §Adam优化器中的Momentum和
+    Variance: m_t = b1 m + (1-b1) g, v_t = b2 v + (1-b2) g^2, theta -= lr *
+    m_hat / (sqrt(v_hat) + eps), with the hats the usual bias corrections
+    1 - b^t; weight decay as torch Adam's, added to the gradient, since
+    [Walkthrough] builds Adam(param_groups, lr, weight_decay, betas, eps)).
+    step is the 1-based count of applied updates.  Returns (param, m, v).
+    Pinned by: torch.optim.Adam in float64 over several steps."""
+    g = np.asarray(grad, dtype=np.float64) + weight_decay * np.asarray(param, dtype=np.float64)
+    m = cfg["beta1"] * np.asarray(m, dtype=np.float64) + (1 - cfg["beta1"]) * g
+    v = cfg["beta2"] * np.asarray(v, dtype=np.float64) + (1 - cfg["beta2"]) * g * g
+    m_hat = m / (1 - cfg["beta1"] ** step)
+    v_hat = v / (1 - cfg["beta2"] ** step)
+    param = np.asarray(param, dtype=np.float64) - cfg["lr"] * m_hat / (np.sqrt(v_hat) + cfg["eps"])
+    return param, m, v
+
+
+def mixed_precision_adam_step(groups, state, cfg):
+    """One step of the mixed-precision optimizer ([Walkthrough]
+    §MixedPrecisionOptimizer.step, in its order):
+      1. the gradients are the fp32 main gradients (copy to main: identity);
+      2. unscale by the loss scale and check for inf/nan (if the scaler is on);
+      3. update the loss scale;
+      4. on inf/nan skip the update (parameters, moments and the step count
+         stay; the scale has already changed);
+      5. clip by the global L2 norm;
+      6. Adam on the fp32 main parameters;
+      7. copy the main parameters to the bf16 model parameters.
+    groups: list of dicts param, grad, m, v, weight_decay (fp64 arrays).
+    state: scale, growth_tracker, hysteresis_tracker, step.
+    Returns (updated, grad_norm, new groups with param/m/v/model, new state);
+    grad_norm is the norm of the unscaled gradients (inf/nan on overflow).
+    Pinned through its parts and by the skip test."""
+    scale = state["scale"] if cfg["use_scaler"] else 1.0
+    grads, found_inf = unscale_and_check([g["grad"] for g in groups], scale)
+    new_state = dict(state)
+    if cfg["use_scaler"]:
+        new_state = grad_scaler_update(state, found_inf, cfg)
+    norm_sq = sum(float(np.sum(g * g)) for g in grads)
+    grad_norm = math.sqrt(norm_sq) if math.isfinite(norm_sq) else norm_sq
+    if found_inf:
+        return False, grad_norm, [dict(g) for g in groups], new_state
+    grads, _ = clip_by_global_norm(grads, cfg["max_norm"])
+    step = state["step"] + 1
+    new_state["step"] = step
+    out = []
+    for grp, g in zip(groups, grads):
+        p, m, v = adam_update(grp["param"], g, grp["m"], grp["v"], step, cfg, grp["weight_decay"])
+        out.append(dict(grp, param=p, m=m, v=v))
+    return True, grad_norm, out, new_state
+
+
+# --------------------------------------------------------------------------
 # Closed forms the pages state
 # --------------------------------------------------------------------------
 def param_count(H, L, V):

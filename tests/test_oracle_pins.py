@@ -615,3 +615,119 @@ def test_planted_per_range_max_is_caught(monkeypatch):
         return np.log(sum_exp) - pred, np.log(sum_exp)
     monkeypatch.setattr(O, "vocab_parallel_cross_entropy", broken)
     assert check_ce_torch(O) > 1e-3
+
+
+# ----------------------------------------------------------------------------
+# Mixed-precision optimizer step
+# ----------------------------------------------------------------------------
+ADAM_CFG = dict(lr=1e-3, beta1=0.9, beta2=0.95, eps=1e-8, max_norm=0.0, use_scaler=False,
+                min_scale=1.0, growth_factor=2.0, backoff_factor=0.5, growth_interval=3, hysteresis=2)
+
+
+def check_adam_torch(mod, steps=4):
+    g = rng(11)
+    shapes = [(7, 5), (9,)]
+    wds = [0.1, 0.0]
+    params = [g.standard_normal(s) for s in shapes]
+    grads = [[g.standard_normal(s) for s in shapes] for _ in range(steps)]
+    tparams = [torch.tensor(p, dtype=torch.float64, requires_grad=True) for p in params]
+    opt = torch.optim.Adam([{"params": [tp], "weight_decay": wd} for tp, wd in zip(tparams, wds)],
+                           lr=ADAM_CFG["lr"], betas=(ADAM_CFG["beta1"], ADAM_CFG["beta2"]),
+                           eps=ADAM_CFG["eps"])
+    groups = [dict(param=p.copy(), grad=None, m=np.zeros_like(p), v=np.zeros_like(p), weight_decay=wd)
+              for p, wd in zip(params, wds)]
+    state = dict(scale=1.0, growth_tracker=0, hysteresis_tracker=2, step=0)
+    for k in range(steps):
+        for tp, gr in zip(tparams, grads[k]):
+            tp.grad = torch.tensor(gr, dtype=torch.float64)
+        opt.step()
+        for grp, gr in zip(groups, grads[k]):
+            grp["grad"] = gr
+        ok, _, groups, state = mod.mixed_precision_adam_step(groups, state, ADAM_CFG)
+        assert ok
+    return max(np.abs(grp["param"] - tp.detach().numpy()).max() for grp, tp in zip(groups, tparams))
+
+
+def test_adam_matches_torch():
+    assert check_adam_torch(O) < 1e-12
+
+
+def check_clip(mod):
+    """Error of the clip against the closed form: two groups whose joint norm is 5."""
+    g = [np.array([3.0, 0.0]), np.array([[4.0]])]
+    out, norm = mod.clip_by_global_norm(g, 1.0)
+    return max(abs(norm - 5.0), abs(out[0][0] - 0.6), abs(out[0][1]), abs(out[1][0, 0] - 0.8))
+
+
+def test_clip_closed_form_and_torch():
+    assert check_clip(O) == 0.0
+    g = [np.array([3.0, 0.0]), np.array([[4.0]])]
+    same, n2 = O.clip_by_global_norm(g, 10.0)
+    assert n2 == 5.0 and same[0] is g[0]
+    h = [rng(12).standard_normal((6, 4)) * 3, rng(13).standard_normal(5)]
+    t = [torch.tensor(x, requires_grad=True) for x in h]
+    for x, tt in zip(h, t):
+        tt.grad = torch.tensor(x)
+    torch.nn.utils.clip_grad_norm_(t, 2.0)
+    out, _ = O.clip_by_global_norm(h, 2.0)
+    for a, tt in zip(out, t):
+        assert np.abs(a - tt.grad.numpy()).max() < 1e-6 * np.abs(a).max()
+
+
+def test_grad_scaler_behaviour():
+    cfg = dict(ADAM_CFG, use_scaler=True, min_scale=0.25)
+    s = dict(scale=4.0, growth_tracker=0, hysteresis_tracker=2, step=0)
+    # growth_interval (3) overflow-free steps grow the scale and reset the trackers
+    for k in range(3):
+        s = O.grad_scaler_update(s, False, cfg)
+    assert s["scale"] == 8.0 and s["growth_tracker"] == 0 and s["hysteresis_tracker"] == 2
+    # the first overflow only spends hysteresis; the second backs off
+    s = O.grad_scaler_update(s, True, cfg)
+    assert s["scale"] == 8.0 and s["hysteresis_tracker"] == 1
+    s = O.grad_scaler_update(s, True, cfg)
+    assert s["scale"] == 4.0
+    # further overflows keep backing off (hysteresis is cumulative), down to min_scale
+    for _ in range(6):
+        s = O.grad_scaler_update(s, True, cfg)
+    assert s["scale"] == 0.25
+    # an overflow resets the run of clean steps
+    s = O.grad_scaler_update(s, False, cfg)
+    s = O.grad_scaler_update(s, True, cfg)
+    assert s["growth_tracker"] == 0
+
+
+def test_step_skipped_on_overflow_and_unscale_before_clip():
+    cfg = dict(ADAM_CFG, use_scaler=True, max_norm=1.0)
+    p = np.ones(4)
+    grp = dict(param=p.copy(), grad=np.array([1.0, np.inf, 0.0, 0.0]), m=np.zeros(4), v=np.zeros(4),
+               weight_decay=0.0)
+    st = dict(scale=8.0, growth_tracker=1, hysteresis_tracker=1, step=5)
+    ok, _, out, st2 = O.mixed_precision_adam_step([grp], st, cfg)
+    assert not ok and np.array_equal(out[0]["param"], p) and st2["step"] == 5 and st2["scale"] == 4.0
+    # scale 8 and grads (0, 0, 24, 32): unscaled norm 5 is clipped to 1, so the
+    # clipped grads are (0, 0, 0.6, 0.8) and m = (1 - b1) * g after one step
+    grp = dict(param=p.copy(), grad=np.array([0.0, 0.0, 24.0, 32.0]), m=np.zeros(4), v=np.zeros(4),
+               weight_decay=0.0)
+    ok, norm, out, st3 = O.mixed_precision_adam_step([grp], dict(st, hysteresis_tracker=2), cfg)
+    assert ok and norm == 5.0 and st3["step"] == 6
+    assert np.allclose(out[0]["m"], (1 - cfg["beta1"]) * np.array([0, 0, 0.6, 0.8]), atol=1e-15)
+
+
+def test_planted_missing_bias_correction_is_caught(monkeypatch):
+    def broken(param, grad, m, v, step, cfg, weight_decay):
+        g = grad + weight_decay * param
+        m = cfg["beta1"] * m + (1 - cfg["beta1"]) * g
+        v = cfg["beta2"] * v + (1 - cfg["beta2"]) * g * g
+        return param - cfg["lr"] * m / (np.sqrt(v) + cfg["eps"]), m, v
+    monkeypatch.setattr(O, "adam_update", broken)
+    assert check_adam_torch(O) > 1e-6
+
+
+def test_planted_per_group_clip_is_caught(monkeypatch):
+    real = O.clip_by_global_norm
+
+    def broken(grads, max_norm):
+        outs = [real([g], max_norm)[0][0] for g in grads]
+        return outs, real(grads, max_norm)[1]
+    monkeypatch.setattr(O, "clip_by_global_norm", broken)
+    assert check_clip(O) > 1e-3
