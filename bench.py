@@ -380,7 +380,38 @@ class CEBench:
         return {"gemm_ce_fwd": ("tensor", f), "gemm_ce_bwd": ("tensor", 2 * f), "ce_reduce": ("hbm", red)}
 
 
-BENCHES = {"mlp": MLPBench, "attn": AttnBench, "embed": EmbedBench, "ce": CEBench}
+class AdamBench:
+    """Mixed-precision Adam step over fp32 flat groups: the norm pass reads the
+    gradients (4 B per value); the update reads parameter, gradient and both
+    moments and writes parameter, moments and the bf16 model copy (30 B)."""
+    kind = "adam"
+
+    def __init__(self, name, tp, torch):
+        self.name, self.tp, self.torch = name, tp, torch
+        inp = SI.adam_inputs(SI.WORKLOADS[name])
+        self.hyper = inp["hyper"]
+        self.groups = []
+        for g in inp["groups"]:
+            d = {k: g[k].cuda() for k in ("param", "grad", "m", "v")}
+            d["model"] = torch.empty(g["param"].numel(), dtype=torch.bfloat16, device="cuda")
+            d["weight_decay"] = g["weight_decay"]
+            self.groups.append(d)
+        self.n = sum(g["param"].numel() for g in self.groups)
+        self.state = tp.make_optimizer_state(**inp["state"])
+        self.ws = torch.empty(tp.tp_adam_step_workspace_size(), dtype=torch.uint8, device="cuda")
+
+    def step(self):
+        self.tp.tp_adam_step(self.groups, self.hyper, self.state, self.ws)
+
+    def units(self):
+        return 34.0 * self.n, "GB/s", 1e9
+
+    def kernel_work(self):
+        return {"adam_update": ("hbm", 30.0 * self.n), "adam_norm": ("hbm", 4.0 * self.n)}
+
+
+BENCHES = {"mlp": MLPBench, "attn": AttnBench, "embed": EmbedBench, "ce": CEBench,
+           "adam": AdamBench}
 
 
 def time_steps(torch, fn, steps, warmup, flush):
@@ -614,7 +645,7 @@ def main(argv=None):
     line = {
         "metric": METRIC, "value": value, "unit": unit, "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "scaling": "weak", "vs_baseline": None, "dtype": cfg.get("dtype", "bf16"),
         "data": "synthetic (seeded normals; no dataset)",
         "config": {"workload": args.workload, **{k: v for k, v in cfg.items() if k not in ("kind", "seed")},
                    "parallelism": f"replicas{ws}" if ws > 1 else "single-gpu, N logical shards",
@@ -686,7 +717,8 @@ def secondary_rows(tp, torch, flush, peaks, peak_src, main_workload):
     """The other rows of the block, each on its own workload, a few timed steps."""
     rows = {}
     for name in ("embed_tied_V50257_h4096_T8192", "ce_V50257_h4096_T8192",
-                 "attn_b1_s2048_h4096_heads8_N8", "mlp_b2_s2048_h4096_hp16384_N2"):
+                 "attn_b1_s2048_h4096_heads8_N8", "mlp_b2_s2048_h4096_hp16384_N2",
+                 "adam_layer_H4096"):
         if name == main_workload:
             continue
         cfg = SI.WORKLOADS[name]

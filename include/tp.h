@@ -13,6 +13,7 @@
  *   [TP notes]    "Megatron tensor / model parallelism" notes
  *                 (amentiraz.github.io, posts/Megtron张量/模型并行)
  *   [Core DDP]    megatron.core.distributed overview (zwxr.cn news 246059)
+ *   [Study notes] Megatron / ZeRO study notes (baty7811.com blog)
  *
  * Conventions shared by every entry point
  * ---------------------------------------
@@ -303,6 +304,92 @@ TP_API tp_status tied_embed_grad_noalloc(tp_dtype dt, int64_t T, int64_t h, int6
                                          const void* const* dLogits, const int64_t* ld_dlogits,
                                          const int64_t* range_starts, void* const* dE,
                                          int accumulate, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Mixed-precision Adam step                                                 */
+/* ------------------------------------------------------------------------ */
+
+/* Optimizer state that lives on the device between steps (24 bytes, 4-byte
+ * aligned, caller-owned device memory).  scale, growth_tracker,
+ * hysteresis_tracker and step are read and updated by every tp_adam_step;
+ * found_inf and grad_norm are outputs of the last step. */
+typedef struct {
+  float scale;                /* loss scale the gradients carry (unused without the scaler) */
+  int32_t growth_tracker;     /* overflow-free steps since the last growth or overflow */
+  int32_t hysteresis_tracker; /* overflows left before the scale backs off */
+  int32_t step;               /* number of updates applied so far (Adam's t) */
+  int32_t found_inf;          /* out: 1 if the last step saw inf/nan and was skipped */
+  float grad_norm;            /* out: L2 norm of all unscaled gradients of the last step
+                                 (inf or nan when found_inf) */
+} tp_optimizer_state;
+
+/* Hyper-parameters of the step (host struct, read during the call). */
+typedef struct {
+  double lr, beta1, beta2, eps; /* Adam; 0 <= beta1, beta2 < 1 */
+  double max_norm;              /* global-norm clip threshold; <= 0 disables clipping */
+  int32_t use_scaler;           /* 1: dynamic loss scaling, 0: gradients are unscaled */
+  float min_scale;              /* the scale never backs off below this */
+  float growth_factor;          /* scale *= growth_factor after growth_interval clean steps */
+  float backoff_factor;         /* scale *= backoff_factor once hysteresis overflows are used up */
+  int32_t growth_interval;      /* >= 1 */
+  int32_t hysteresis;           /* value the hysteresis tracker is reset to on growth */
+} tp_adam_config;
+
+/* One parameter group: n elements in flat fp32 device buffers (host struct). */
+typedef struct {
+  float* param;        /* fp32 main parameters, updated in place */
+  const float* grad;   /* fp32 main gradients (times the loss scale when the scaler is on) */
+  float* exp_avg;      /* Adam first moment m, updated in place */
+  float* exp_avg_sq;   /* Adam second moment v, updated in place */
+  void* model_param;   /* bf16 model parameters written from the updated main ones, or NULL */
+  int64_t n;           /* >= 0 */
+  double weight_decay; /* L2 term added to the gradient: g + weight_decay * param */
+} tp_param_group;
+
+/*
+ * tp_adam_step -- one step of the mixed-precision optimizer over all groups
+ * ([Walkthrough] §MixedPrecisionOptimizer.step and §DynamicGradScaler;
+ * [Study notes] §梯度裁剪 and §Adam优化器中的Momentum和Variance), in the
+ * pages' order:
+ *   1. g = grad / scale (scale = state->scale with the scaler, else 1) and a
+ *      check of every g for inf/nan, across all groups;
+ *   2. with the scaler, the scale update: an overflow resets growth_tracker,
+ *      decrements hysteresis_tracker and, once that is <= 0, sets scale =
+ *      max(scale * backoff_factor, min_scale); a clean step increments
+ *      growth_tracker and, when it reaches growth_interval, resets it, resets
+ *      hysteresis_tracker to hysteresis and multiplies scale by growth_factor;
+ *   3. on overflow nothing else changes (params, moments and step stay);
+ *   4. ||g|| over all groups; if max_norm > 0 and ||g|| > max_norm,
+ *      g *= max_norm / ||g||;
+ *   5. t = step + 1; per element g += weight_decay * p; m = b1 m + (1-b1) g;
+ *      v = b2 v + (1-b2) g^2; p -= lr / (1 - b1^t) * m / (sqrt(v / (1 - b2^t)) + eps);
+ *   6. model_param = bf16(p) (round to nearest even) where given.
+ * The fp32 main gradients are the DDP buffer's main_grad ([Core DDP] §3.2),
+ * so "copy gradients to the main parameters" is the identity here.
+ * Arguments:
+ *   groups      HOST array of ngroups descriptors (NULL allowed when ngroups is 0);
+ *               0 <= ngroups <= 64.  param, grad, exp_avg and exp_avg_sq of a
+ *               group with n > 0 are non-NULL and 16-byte aligned; model_param
+ *               is NULL or 8-byte aligned.  No two buffers overlap.
+ *   cfg         HOST pointer.
+ *   state       DEVICE pointer to the tp_optimizer_state, 4-byte aligned.
+ *   workspace   device scratch of tp_adam_step_workspace_size() bytes, 16-byte
+ *               aligned (TP_ERR_WORKSPACE if smaller or NULL, TP_ERR_ALIGN if
+ *               misaligned).
+ * Precision: per-element arithmetic in fp32; the norm sums fp32 squares of up
+ * to 32 elements and adds those partial sums in fp64, in an order fixed for a
+ * given GPU model (bit-identical results run to run).  An unscaled gradient
+ * whose fp32 square overflows (|g| > ~1.8e19) counts as an overflow.
+ * Errors: TP_ERR_INVALID for NULL cfg/state, ngroups out of range, n < 0, a
+ * NULL buffer, betas outside [0, 1) or growth_interval < 1 with the scaler;
+ * TP_ERR_ALIGN for misaligned buffers; all before anything is launched.
+ * Launches three kernels (norm partials, a one-block finalize, the update).
+ */
+TP_API tp_status tp_adam_step(const tp_param_group* groups, int ngroups, const tp_adam_config* cfg,
+                              tp_optimizer_state* state, void* workspace, size_t ws_bytes,
+                              void* stream);
+
+TP_API size_t tp_adam_step_workspace_size(void);
 
 /* ------------------------------------------------------------------------ */
 /* Status, profiling and debugging                                           */

@@ -25,7 +25,9 @@ __all__ = [
     "tied_embed_grad_noalloc", "tp_get_status",
     "tp_status_string", "tp_num_sms", "tp_profile_enable", "tp_profile_reset", "tp_profile_read",
     "tp_debug_inject_fault", "tp_debug_set_wait_limit_ms", "tp_debug_set_gemm_kernel",
-    "tp_gelu_eval", "logits_pitch",
+    "tp_gelu_eval", "logits_pitch", "tp_adam_step", "tp_adam_step_workspace_size",
+    "tp_optimizer_state", "tp_adam_config", "tp_param_group", "make_optimizer_state",
+    "read_optimizer_state",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libtp.so")
@@ -36,6 +38,30 @@ TP_F32, TP_BF16 = 0, 1
 _c_void_p, _i64, _int, _size_t = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
 _PP = ctypes.POINTER(ctypes.c_void_p)
 _PI64 = ctypes.POINTER(ctypes.c_int64)
+
+
+
+class tp_optimizer_state(ctypes.Structure):
+    """Device-resident optimizer state (layout of the C struct)."""
+    _fields_ = [("scale", ctypes.c_float), ("growth_tracker", ctypes.c_int32),
+                ("hysteresis_tracker", ctypes.c_int32), ("step", ctypes.c_int32),
+                ("found_inf", ctypes.c_int32), ("grad_norm", ctypes.c_float)]
+
+
+class tp_adam_config(ctypes.Structure):
+    _fields_ = [("lr", ctypes.c_double), ("beta1", ctypes.c_double), ("beta2", ctypes.c_double),
+                ("eps", ctypes.c_double), ("max_norm", ctypes.c_double),
+                ("use_scaler", ctypes.c_int32), ("min_scale", ctypes.c_float),
+                ("growth_factor", ctypes.c_float), ("backoff_factor", ctypes.c_float),
+                ("growth_interval", ctypes.c_int32), ("hysteresis", ctypes.c_int32)]
+
+
+class tp_param_group(ctypes.Structure):
+    _fields_ = [("param", ctypes.c_void_p), ("grad", ctypes.c_void_p),
+                ("exp_avg", ctypes.c_void_p), ("exp_avg_sq", ctypes.c_void_p),
+                ("model_param", ctypes.c_void_p), ("n", ctypes.c_int64),
+                ("weight_decay", ctypes.c_double)]
+
 
 _SIGNATURES = {
     "tp_mlp_fwd": (_int, [_int, _i64, _i64, _i64, _int, _c_void_p, _PP, _PP, _PP, _c_void_p,
@@ -75,6 +101,9 @@ _SIGNATURES = {
     "tp_debug_set_gemm_kernel": (None, [_int]),
     "tp_gelu_eval": (_int, [_c_void_p, _c_void_p, _c_void_p, _i64, _c_void_p]),
     "tp_debug_set_wait_limit_ms": (None, [_int]),
+    "tp_adam_step": (_int, [ctypes.POINTER(tp_param_group), _int, ctypes.POINTER(tp_adam_config),
+                            _c_void_p, _c_void_p, _size_t, _c_void_p]),
+    "tp_adam_step_workspace_size": (_size_t, []),
 }
 
 _LIB: Optional[ctypes.CDLL] = None
@@ -345,6 +374,53 @@ def tied_embed_grad_noalloc(ids, dEmb, X, dLogits, range_starts, dE, accumulate=
 # ----------------------------------------------------------------------------
 # status, profiling, debugging
 # ----------------------------------------------------------------------------
+def tp_adam_step_workspace_size() -> int:
+    return int(lib().tp_adam_step_workspace_size())
+
+
+def make_optimizer_state(scale=1.0, growth_tracker=0, hysteresis_tracker=0, step=0,
+                         device="cuda") -> torch.Tensor:
+    """The 24-byte tp_optimizer_state packed into a uint8 device tensor."""
+    st = tp_optimizer_state(scale, growth_tracker, hysteresis_tracker, step, 0, 0.0)
+    raw = torch.frombuffer(bytearray(bytes(st)), dtype=torch.uint8)
+    return raw.to(device)
+
+
+def read_optimizer_state(state: torch.Tensor) -> dict:
+    """Copies the device state back and unpacks it (synchronous)."""
+    st = tp_optimizer_state.from_buffer_copy(bytes(state.cpu().numpy().tobytes()))
+    return {name: getattr(st, name) for name, _ in tp_optimizer_state._fields_}
+
+
+_ADAM_KEYS = ("lr", "beta1", "beta2", "eps", "max_norm", "use_scaler", "min_scale",
+              "growth_factor", "backoff_factor", "growth_interval", "hysteresis")
+
+
+def tp_adam_step(groups, cfg: dict, state: torch.Tensor, workspace: torch.Tensor, stream=None):
+    """groups: sequence of dicts with fp32 tensors param, grad, m, v, optional
+    bf16 tensor model (or None) and float weight_decay; cfg: dict with the keys
+    of tp_adam_config; state: the device tensor from make_optimizer_state."""
+    arr = (tp_param_group * max(1, len(groups)))()
+    for i, g in enumerate(groups):
+        n = g["param"].numel()
+        for k in ("param", "grad", "m", "v"):
+            if g[k].dtype != torch.float32 or g[k].numel() != n:
+                raise TypeError(f"groups[{i}][{k!r}] must be float32 with {n} elements")
+        model = g.get("model")
+        if model is not None and (model.dtype != torch.bfloat16 or model.numel() != n):
+            raise TypeError(f"groups[{i}]['model'] must be bfloat16 with {n} elements")
+        arr[i] = tp_param_group(_dev(g["param"], "param"), _dev(g["grad"], "grad"),
+                                _dev(g["m"], "m"), _dev(g["v"], "v"), _dev(model, "model"),
+                                n, float(g.get("weight_decay", 0.0)))
+    c = tp_adam_config(*[cfg[k] for k in _ADAM_KEYS])
+    if state.numel() * state.element_size() != ctypes.sizeof(tp_optimizer_state):
+        raise ValueError("state must be the 24-byte tensor from make_optimizer_state")
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(lib().tp_adam_step(arr, len(groups), ctypes.byref(c), _dev(state, "state"),
+                              _dev(workspace, "workspace"), ws_bytes, _stream(stream)),
+           "tp_adam_step")
+
+
 def tp_get_status(stream=None) -> int:
     return int(lib().tp_get_status(_stream(stream)))
 

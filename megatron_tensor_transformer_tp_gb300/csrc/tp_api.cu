@@ -983,6 +983,75 @@ extern "C" tp_status tied_embed_grad(tp_dtype dt, int64_t T, int64_t h, int64_t 
 }
 
 // ===========================================================================
+// Mixed-precision Adam step
+// ===========================================================================
+extern "C" size_t tp_adam_step_workspace_size(void) { return opt_workspace_bytes(); }
+
+extern "C" tp_status tp_adam_step(const tp_param_group* groups, int ngroups, const tp_adam_config* cfg,
+                                  tp_optimizer_state* state, void* workspace, size_t ws_bytes,
+                                  void* stream) {
+  if (cfg == nullptr || state == nullptr || ngroups < 0 || ngroups > kMaxOptGroups) return TP_ERR_INVALID;
+  if (ngroups > 0 && groups == nullptr) return TP_ERR_INVALID;
+  if (!(cfg->beta1 >= 0.0 && cfg->beta1 < 1.0 && cfg->beta2 >= 0.0 && cfg->beta2 < 1.0))
+    return TP_ERR_INVALID;
+  if (cfg->use_scaler && cfg->growth_interval < 1) return TP_ERR_INVALID;
+  auto al = [](const void* q, uintptr_t a) { return (reinterpret_cast<uintptr_t>(q) & (a - 1)) == 0; };
+  OptParams P;
+  memset(&P, 0, sizeof(P));
+  const int64_t chunk = opt_chunk_elems();
+  int64_t c = 0;
+  for (int i = 0; i < ngroups; ++i) {
+    const tp_param_group& g = groups[i];
+    if (g.n < 0) return TP_ERR_INVALID;
+    if (g.n > 0) {
+      if (!g.param || !g.grad || !g.exp_avg || !g.exp_avg_sq) return TP_ERR_INVALID;
+      if (!al(g.param, 16) || !al(g.grad, 16) || !al(g.exp_avg, 16) || !al(g.exp_avg_sq, 16) ||
+          !al(g.model_param, 8))
+        return TP_ERR_ALIGN;
+    }
+    OptGroup& o = P.group[i];
+    o.param = g.param;
+    o.grad = g.grad;
+    o.exp_avg = g.exp_avg;
+    o.exp_avg_sq = g.exp_avg_sq;
+    o.model_param = g.model_param;
+    o.n = g.n;
+    o.chunk_begin = c;
+    o.weight_decay = static_cast<float>(g.weight_decay);
+    c += (g.n + chunk - 1) / chunk;
+  }
+  if (!al(state, 4)) return TP_ERR_ALIGN;
+  if (workspace == nullptr || ws_bytes < opt_workspace_bytes()) return TP_ERR_WORKSPACE;
+  if (!al(workspace, 16)) return TP_ERR_ALIGN;
+  P.state = state;
+  P.nchunks = c;
+  P.ngroups = ngroups;
+  P.use_scaler = cfg->use_scaler != 0;
+  P.growth_interval = cfg->growth_interval;
+  P.hysteresis = cfg->hysteresis;
+  P.beta1 = static_cast<float>(cfg->beta1);
+  P.one_minus_beta1 = static_cast<float>(1.0 - cfg->beta1);
+  P.beta2 = static_cast<float>(cfg->beta2);
+  P.one_minus_beta2 = static_cast<float>(1.0 - cfg->beta2);
+  P.eps = static_cast<float>(cfg->eps);
+  P.min_scale = cfg->min_scale;
+  P.growth_factor = cfg->growth_factor;
+  P.backoff_factor = cfg->backoff_factor;
+  P.lr = cfg->lr;
+  P.beta1_d = cfg->beta1;
+  P.beta2_d = cfg->beta2;
+  P.max_norm = cfg->max_norm;
+  DeviceState* dev = nullptr;
+  if (device_state(&dev) != TP_OK) return TP_ERR_CUDA;
+  const int sms = dev->num_sms;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = timed("adam_norm", s, [&] { return launch_adam_norm(P, sms, workspace, s); });
+  if (e != cudaSuccess) return TP_ERR_CUDA;
+  e = timed("adam_update", s, [&] { return launch_adam_update(P, sms, workspace, s); });
+  return e == cudaSuccess ? TP_OK : TP_ERR_CUDA;
+}
+
+// ===========================================================================
 // Status, profiling, debugging
 // ===========================================================================
 extern "C" tp_status tp_get_status(void* stream) {

@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "tp.h"
+
 namespace tp {
 
 constexpr int kMaxGroups = 40;    // output matrices in one GEMM launch
@@ -123,6 +125,41 @@ struct RangeTable {
   const void* ptr[kMaxRanges];
   int n;
 };
+
+// Mixed-precision Adam step.  Parameter groups are cut into chunks of
+// opt_chunk_elems() elements; chunk c belongs to the last group whose
+// chunk_begin <= c.
+constexpr int kMaxOptGroups = 64;
+constexpr int kMaxOptGrid = 4096;
+
+struct OptGroup {
+  float* param;
+  const float* grad;
+  float* exp_avg;
+  float* exp_avg_sq;
+  void* model_param;  // bf16 or null
+  int64_t n, chunk_begin;
+  float weight_decay;
+  int pad;
+};
+
+struct OptParams {
+  OptGroup group[kMaxOptGroups];
+  tp_optimizer_state* state;
+  int64_t nchunks;
+  int ngroups;
+  int use_scaler, growth_interval, hysteresis;
+  float beta1, one_minus_beta1, beta2, one_minus_beta2, eps;
+  float min_scale, growth_factor, backoff_factor;
+  double lr, beta1_d, beta2_d, max_norm;
+};
+
+int64_t opt_chunk_elems();
+size_t opt_workspace_bytes();
+// Norm partials, then the one-block finalize (scaler, clip, bias corrections).
+cudaError_t launch_adam_norm(const OptParams& p, int num_sms, void* ws, cudaStream_t s);
+// The per-element update (skips itself when the finalize found an overflow).
+cudaError_t launch_adam_update(const OptParams& p, int num_sms, void* ws, cudaStream_t s);
 
 // Every kernel launch the library makes is counted (reported by the profiler).
 void count_launches(int n);

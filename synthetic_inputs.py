@@ -24,7 +24,7 @@ import numpy as np
 import torch
 
 __all__ = ["WORKLOADS", "normal", "uniform_ids", "mlp_inputs", "attn_inputs",
-           "embed_inputs", "split_rows", "split_cols"]
+           "embed_inputs", "ce_inputs", "adam_inputs", "split_rows", "split_cols"]
 
 # Workloads: shapes and seeds only.  Names state the sizes.
 WORKLOADS = {
@@ -48,6 +48,18 @@ WORKLOADS = {
     # bf16 vocab-parallel cross-entropy on the same output layer: T=8192 tokens, two ranges
     "ce_V50257_h4096_T8192": dict(kind="ce", dtype="bf16", V=50257, h=4096, b=4, s=2048,
                                   ranges=[0, 25129, 50257], seed=1005),
+    # fp32 mixed-precision Adam step over one transformer layer of the H=4096 model:
+    # QKV (3H, H), attention output (H, H), MLP up (4H, H), MLP down (H, 4H) with
+    # weight decay; two LayerNorms' gain and bias (H each) without; 201,342,976 values
+    "adam_layer_H4096": dict(kind="adam", dtype="f32", H=4096, seed=1006,
+                             sizes=[3 * 4096 * 4096, 4096 * 4096, 4 * 4096 * 4096,
+                                    4 * 4096 * 4096, 4096, 4096, 4096, 4096],
+                             weight_decay=[0.1, 0.1, 0.1, 0.1, 0.0, 0.0, 0.0, 0.0],
+                             state=dict(scale=4096.0, growth_tracker=0, hysteresis_tracker=2,
+                                        step=100),
+                             hyper=dict(lr=1e-4, beta1=0.9, beta2=0.95, eps=1e-8, max_norm=1.0,
+                                        use_scaler=1, min_scale=1.0, growth_factor=2.0,
+                                        backoff_factor=0.5, growth_interval=1000, hysteresis=2)),
 }
 
 _TORCH_DTYPE = {"f32": torch.float32, "bf16": torch.bfloat16}
@@ -187,3 +199,26 @@ def ce_inputs(cfg: dict) -> dict:
     E_shards = [E[ranges[r]:ranges[r + 1]].contiguous() for r in range(len(ranges) - 1)]
     return dict(T=T, h=h, V=V, N=len(ranges) - 1, ranges=ranges, X=X, E=E, E_shards=E_shards,
                 targets=targets, dloss=dloss)
+
+
+def adam_inputs(cfg: dict, sizes=None) -> dict:
+    """Inputs of one mixed-precision Adam step (fp32, flat groups): main
+    parameters ~ N(0, 0.02), unscaled gradients ~ N(0, 1e-3) stored times the
+    loss scale (what a scaled backward leaves in the fp32 main gradients),
+    first moments ~ N(0, 1e-4), second moments the square of an N(0, 1e-3)
+    draw, all mid-training (state step 100).  ``sizes`` overrides the group
+    sizes (weight decay then alternates 0.1, 0.0)."""
+    seed = cfg["seed"]
+    sizes = list(cfg["sizes"]) if sizes is None else list(sizes)
+    wds = list(cfg["weight_decay"]) if len(sizes) == len(cfg["sizes"]) else \
+        [0.1 if i % 2 == 0 else 0.0 for i in range(len(sizes))]
+    scale = float(cfg["state"]["scale"])
+    groups = []
+    for i, n in enumerate(sizes):
+        groups.append(dict(
+            param=normal(seed, 100 + 4 * i, (n,), 0.02, "f32"),
+            grad=normal(seed, 101 + 4 * i, (n,), 1e-3 * scale, "f32"),
+            m=normal(seed, 102 + 4 * i, (n,), 1e-4, "f32"),
+            v=normal(seed, 103 + 4 * i, (n,), 1e-3, "f32").square_(),
+            weight_decay=wds[i]))
+    return dict(groups=groups, state=dict(cfg["state"]), hyper=dict(cfg["hyper"]))

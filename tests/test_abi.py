@@ -148,3 +148,67 @@ def test_cross_entropy_validation_and_workspace_size():
     short = rs_arr([104, 144])  # pitch below the second range's width
     assert L.tp_vocab_cross_entropy_bwd(tp.TP_BF16, T, 64, V, 2, FAKE, e[0], rs, FAKE, FAKE, FAKE,
                                         e[0], short, None, None) == tp.TP_ERR_INVALID
+
+
+ADAM_CFG = dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, max_norm=1.0, use_scaler=1,
+                min_scale=1.0, growth_factor=2.0, backoff_factor=0.5, growth_interval=1000,
+                hysteresis=2)
+
+
+def adam(groups, n, cfg=None, state=FAKE, ws=FAKE, ws_bytes=None):
+    c = tp.tp_adam_config(*[(cfg or ADAM_CFG)[k] for k in tp._ADAM_KEYS])
+    arr = (tp.tp_param_group * max(1, n))(*groups) if groups is not None else None
+    if ws_bytes is None:
+        ws_bytes = tp.tp_adam_step_workspace_size()
+    return L.tp_adam_step(arr, n, ctypes.byref(c), state, ws, ws_bytes, None)
+
+
+def group(n=1000, base=FAKE, model=None, **kw):
+    g = dict(param=base, grad=base + 16 * 4096, exp_avg=base + 32 * 4096,
+             exp_avg_sq=base + 48 * 4096, model_param=model, n=n, weight_decay=0.1)
+    g.update(kw)
+    return tp.tp_param_group(**g)
+
+
+def test_adam_step_validation():
+    assert tp.tp_adam_step_workspace_size() >= 256
+    assert adam(None, 1) == tp.TP_ERR_INVALID                     # groups NULL
+    assert adam([group()], -1) == tp.TP_ERR_INVALID
+    assert adam([group()] * 65, 65) == tp.TP_ERR_INVALID          # more than 64 groups
+    assert adam([group(n=-1)], 1) == tp.TP_ERR_INVALID
+    assert adam([group(grad=None)], 1) == tp.TP_ERR_INVALID
+    assert adam([group()], 1, state=None) == tp.TP_ERR_INVALID
+    assert adam([group()], 1, cfg=dict(ADAM_CFG, beta2=1.0)) == tp.TP_ERR_INVALID
+    assert adam([group()], 1, cfg=dict(ADAM_CFG, beta1=-0.1)) == tp.TP_ERR_INVALID
+    assert adam([group()], 1, cfg=dict(ADAM_CFG, growth_interval=0)) == tp.TP_ERR_INVALID
+    assert adam([group(base=FAKE + 4)], 1) == tp.TP_ERR_ALIGN     # fp32 buffers 16-byte aligned
+    assert adam([group(model=FAKE + 2)], 1) == tp.TP_ERR_ALIGN    # bf16 copy 8-byte aligned
+    assert adam([group()], 1, state=FAKE + 2) == tp.TP_ERR_ALIGN
+    assert adam([group()], 1, ws=None) == tp.TP_ERR_WORKSPACE
+    assert adam([group()], 1, ws_bytes=100) == tp.TP_ERR_WORKSPACE
+    assert adam([group()], 1, ws=FAKE + 8) == tp.TP_ERR_ALIGN
+    # an empty group needs no buffers
+    assert adam([group(n=0, param=None, grad=None)], 1, ws=None) == tp.TP_ERR_WORKSPACE
+
+
+def test_optimizer_struct_layout_matches_header(tmp_path):
+    """The binding's ctypes structures have the C header's sizes and offsets."""
+    src = tmp_path / "layout.c"
+    fields = {"tp_optimizer_state": tp.tp_optimizer_state, "tp_adam_config": tp.tp_adam_config,
+              "tp_param_group": tp.tp_param_group}
+    lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "tp.h"', 'int main(void) {']
+    for name, cls in fields.items():
+        lines.append(f'printf("{name} %zu\\n", sizeof({name}));')
+        for f, _ in cls._fields_:
+            lines.append(f'printf("{name}.{f} %zu\\n", offsetof({name}, {f}));')
+    lines.append("return 0; }")
+    src.write_text("\n".join(lines))
+    exe = tmp_path / "layout"
+    import subprocess
+    subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
+    out = dict(l.split() for l in subprocess.run([str(exe)], capture_output=True, text=True,
+                                                  check=True).stdout.splitlines())
+    for name, cls in fields.items():
+        assert int(out[name]) == ctypes.sizeof(cls), name
+        for f, _ in cls._fields_:
+            assert int(out[f"{name}.{f}"]) == getattr(cls, f).offset, f"{name}.{f}"
