@@ -21,7 +21,8 @@ namespace tp {
 namespace {
 
 constexpr int kOptThreads = 256;
-constexpr int64_t kOptChunk = 8192;  // elements per chunk (a multiple of 4)
+constexpr int64_t kOptChunk = 8192;  // elements per chunk (a multiple of 4 x kOptThreads)
+static_assert(kOptChunk % (4 * kOptThreads) == 0, "chunk = whole float4 rows of the block");
 
 // Scalars the finalize kernel hands to the update kernel (workspace head).
 struct OptControl {
@@ -63,14 +64,27 @@ __global__ void __launch_bounds__(kOptThreads) opt_norm_kernel(const __grid_cons
     const float* src = P.group[g].grad + off;
     float part = 0.f;
     const int64_t nv = len >> 2;
-    for (int64_t i = threadIdx.x; i < nv; i += kOptThreads) {
-      const float4 q = __ldcs(reinterpret_cast<const float4*>(src) + i);
+    auto add4 = [&](const float4 q) {
       const float a = q.x * inv_scale, b = q.y * inv_scale, d = q.z * inv_scale, e = q.w * inv_scale;
       bad |= !(isfinite(a) && isfinite(b) && isfinite(d) && isfinite(e));
       part = fmaf(a, a, part);
       part = fmaf(b, b, part);
       part = fmaf(d, d, part);
       part = fmaf(e, e, part);
+    };
+    if (len == kOptChunk) {
+      // full chunk: all of the thread's loads in flight at once, then the
+      // same summation order as the general loop
+      constexpr int kPer = static_cast<int>(kOptChunk / 4 / kOptThreads);
+      const float4* s4 = reinterpret_cast<const float4*>(src) + threadIdx.x;
+      float4 q[kPer];
+#pragma unroll
+      for (int j = 0; j < kPer; ++j) q[j] = __ldcs(s4 + j * kOptThreads);
+#pragma unroll
+      for (int j = 0; j < kPer; ++j) add4(q[j]);
+    } else {
+      for (int64_t i = threadIdx.x; i < nv; i += kOptThreads)
+        add4(__ldcs(reinterpret_cast<const float4*>(src) + i));
     }
     for (int64_t i = (nv << 2) + threadIdx.x; i < len; i += kOptThreads) {
       const float a = src[i] * inv_scale;

@@ -20,7 +20,7 @@ from tests.gpu_util import TOL, assert_close, rel_err
 
 pytestmark = pytest.mark.gpu
 
-HYPER = dict(lr=1e-3, beta1=0.9, beta2=0.95, eps=1e-8, max_norm=1.0, use_scaler=1, min_scale=1.0,
+HYPER = dict(lr=1e-3, beta1=0.9, beta2=0.95, eps=1e-8, max_norm=0.1, use_scaler=1, min_scale=1.0,
              growth_factor=2.0, backoff_factor=0.5, growth_interval=1000, hysteresis=2)
 STATE = dict(scale=1024.0, growth_tracker=0, hysteresis_tracker=2, step=7)
 SEED = 1006
