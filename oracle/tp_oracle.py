@@ -19,13 +19,15 @@ Notation: M = b*s tokens, h hidden size, h' = FFN width, N shards.  Column
 shard i holds W_i (h'/N, h) (torch ``weight`` layout, so A_i = W_i^T); row
 shard i holds U_i (h, h'/N) (B_i = U_i^T).  Every matrix is row-major.
 
-Readings where the pages are silent or garbled (each also listed in the design doc):
+Readings where the pages are silent or garbled:
   * GELU is the exact erf form (the pages' formula is an image).
   * The row-parallel bias is added once, after the shard sum.
   * The second vocabulary range of the 300-word example is [150, 300).
   * An id that falls in no range yields a zero row (masked sum), not an error.
   * The oracle keeps every intermediate in fp64; it does not mimic bf16
     rounding of saved activations (the tolerance absorbs it).
+  * Attention per head is softmax(Q K^T / sqrt(d)) V (the pages draw it as a
+    figure), with GPT's causal mask when asked; no attention dropout.
 
 Parity status per function is stated in its docstring: "pinned by ..." names
 the tests that tie it to something other than itself.
@@ -254,6 +256,95 @@ def attn_proj_bwd_weight_rows(dQKV, dO, X, C, N, qkv_rows, o_rows):
 # --------------------------------------------------------------------------
 # Vocab-parallel embedding
 # --------------------------------------------------------------------------
+def attention_head_columns(h, n_heads, N, j):
+    """Column offsets of global head j in the shard-major QKV (T, 3h) and in
+    the context C (T, h).  Shard i owns heads [i n_heads/N, (i+1) n_heads/N)
+    and its QKV columns [i 3h/N, (i+1) 3h/N) = [Q_i K_i V_i], each h/N wide,
+    its heads in order inside each ([TP notes] §Self-Attention层: Q, K, V
+    split by columns with whole heads per shard).  Returns (q, k, v, c)."""
+    d = h // n_heads
+    per = n_heads // N
+    i, jl = divmod(j, per)
+    base = i * 3 * (h // N)
+    return base + jl * d, base + h // N + jl * d, base + 2 * (h // N) + jl * d, j * d
+
+
+def attention_head(q, k, v, causal):
+    """One head of one sequence: S = q k^T / sqrt(d), keys after the query
+    masked to -inf when causal, P = softmax over keys with the row max
+    subtracted ([Walkthrough] §_VocabParallelCrossEntropy's stable softmax),
+    out = P v.  The pages draw the single-head formula as a figure; the scaled
+    dot product with the 1/sqrt(d) factor is the plain reading, and the causal
+    mask is GPT's.  Returns (P (s, s), out (s, d))."""
+    s, d = q.shape
+    S = (q @ k.T) / math.sqrt(d)
+    if causal:
+        S = np.where(np.tril(np.ones((s, s), dtype=bool)), S, -np.inf)
+    E = np.exp(S - S.max(axis=1, keepdims=True))
+    P = E / E.sum(axis=1, keepdims=True)
+    return P, P @ v
+
+
+def attention_head_grad(q, k, v, P, g):
+    """Gradient of ``attention_head`` given its P and the output gradient g
+    (the chain rule through out = P v, the softmax and S = q k^T / sqrt(d)):
+        dv = P^T g,  dP = g v^T,  dS = P * (dP - sum_keys(P * dP)) / sqrt(d),
+        dq = dS k,  dk = dS^T q.
+    Masked entries have P = 0 and carry no gradient.  Returns (dq, dk, dv)."""
+    d = q.shape[1]
+    dP = g @ v.T
+    dS = P * (dP - np.sum(P * dP, axis=1, keepdims=True)) / math.sqrt(d)
+    return dS @ k, dS.T @ q, P.T @ g
+
+
+def attention_core(QKV, s, n_heads, N, causal):
+    """Per-head attention between the QKV projection and the output
+    projection for b = T / s sequences of s tokens: every (sequence, head)
+    pair runs ``attention_head`` on its columns of the shard-major QKV and
+    writes head j's output to context columns [j d, (j+1) d).  Heads are
+    independent ([TP notes] §Self-Attention层; [Walkthrough]
+    §ParallelSelfAttention: every rank computes its own heads).
+    Returns (C (T, h), P (b, n_heads, s, s)).
+    Pinned by: torch scaled_dot_product_attention in float64 per head, torch
+    multi_head_attention_forward through the sharded projections, a closed
+    form (q = 0: the running or full mean of v) and brute force on a tiny
+    case."""
+    T, h3 = QKV.shape
+    h = h3 // 3
+    d = h // n_heads
+    b = T // s
+    C = np.zeros((T, h))
+    P = np.zeros((b, n_heads, s, s))
+    for bi in range(b):
+        rows = slice(bi * s, (bi + 1) * s)
+        for j in range(n_heads):
+            qc, kc, vc, cc = attention_head_columns(h, n_heads, N, j)
+            P[bi, j], C[rows, cc:cc + d] = attention_head(
+                QKV[rows, qc:qc + d], QKV[rows, kc:kc + d], QKV[rows, vc:vc + d], causal)
+    return C, P
+
+
+def attention_core_grad(QKV, P, dC, s, n_heads, N):
+    """Gradient of ``attention_core`` with respect to QKV, given its
+    probabilities P and the context gradient dC: ``attention_head_grad`` per
+    (sequence, head), written back in the QKV layout.
+    Pinned by: torch autograd through scaled_dot_product_attention in
+    float64, and through multi_head_attention_forward."""
+    T, h3 = QKV.shape
+    h = h3 // 3
+    d = h // n_heads
+    b = T // s
+    dQKV = np.zeros((T, h3))
+    for bi in range(b):
+        rows = slice(bi * s, (bi + 1) * s)
+        for j in range(n_heads):
+            qc, kc, vc, cc = attention_head_columns(h, n_heads, N, j)
+            dq, dk, dv = attention_head_grad(QKV[rows, qc:qc + d], QKV[rows, kc:kc + d],
+                                             QKV[rows, vc:vc + d], P[bi, j], dC[rows, cc:cc + d])
+            dQKV[rows, qc:qc + d], dQKV[rows, kc:kc + d], dQKV[rows, vc:vc + d] = dq, dk, dv
+    return dQKV
+
+
 def vocab_mask(ids, start, end):
     """Mask and shift of one vocabulary range.
 

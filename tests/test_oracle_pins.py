@@ -290,6 +290,170 @@ def test_attn_bwd_finite_differences():
 
 
 # ----------------------------------------------------------------------------
+# Attention core (per head, between the projections)
+# ----------------------------------------------------------------------------
+def tiny_core(seed=3, b=2, s=5, n_heads=4, N=2, d=3, scale=1.0):
+    """Per-head q, k, v (b, heads, s, d) and their shard-major QKV layout,
+    assembled here by the layout's definition (shard i = [Q_i K_i V_i], its
+    heads in order inside each)."""
+    g = rng(seed)
+    q, k, v = (g.standard_normal((b, n_heads, s, d)) * scale for _ in range(3))
+    dC = g.standard_normal((b * s, n_heads * d))
+    per = n_heads // N
+    cols = []
+    for i in range(N):
+        for t in (q, k, v):
+            for jl in range(per):
+                cols.append(t[:, i * per + jl].reshape(b * s, d))
+    QKV = np.concatenate(cols, axis=1)
+    return dict(q=q, k=k, v=v, QKV=QKV, dC=dC, b=b, s=s, n_heads=n_heads, N=N, d=d)
+
+
+def check_core_sdpa(mod, causal):
+    """Largest difference to torch's scaled_dot_product_attention (float64)
+    in the context and in dQKV (autograd)."""
+    c = tiny_core()
+    b, s, H, d = c["b"], c["s"], c["n_heads"], c["d"]
+    C, P = mod.attention_core(c["QKV"], s, H, c["N"], causal)
+    dQKV = mod.attention_core_grad(c["QKV"], P, c["dC"], s, H, c["N"])
+    tq, tk, tv = (torch.tensor(c[x], requires_grad=True) for x in ("q", "k", "v"))
+    out = F.scaled_dot_product_attention(tq, tk, tv, is_causal=causal)  # (b, H, s, d)
+    ref_C = out.permute(0, 2, 1, 3).reshape(b * s, H * d)
+    ref_C.backward(torch.tensor(c["dC"]))
+    err = np.abs(C - ref_C.detach().numpy()).max()
+    # dQKV in the layout, compared through the same assembly as the inputs
+    per = H // c["N"]
+    k0 = 0
+    for i in range(c["N"]):
+        for t in (tq, tk, tv):
+            for jl in range(per):
+                ref = t.grad[:, i * per + jl].reshape(b * s, d).numpy()
+                err = max(err, np.abs(dQKV[:, k0:k0 + d] - ref).max())
+                k0 += d
+    return err
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_attention_core_matches_torch_sdpa(causal):
+    assert check_core_sdpa(O, causal) < 1e-12
+
+
+def check_core_mha(mod):
+    """X -> sharded QKV projection -> attention core -> sharded output
+    projection equals torch multi_head_attention_forward on the unsharded
+    weights (causal), forward and input gradient."""
+    a = tiny_attn(seed=9, M=12, h=16, N=2)
+    s, H = 6, 4  # two sequences of 6 tokens, 2 heads per shard
+    X = a["X"]
+    QKV, _ = mod.attn_proj_fwd(X, a["Ws"], a["Bs"], a["C"], a["Wos"], a["bo"])
+    C, P = mod.attention_core(QKV, s, H, a["N"], True)
+    _, out = mod.attn_proj_fwd(X, a["Ws"], a["Bs"], C, a["Wos"], a["bo"])
+    tX = torch.tensor(X.reshape(2, s, 16).transpose(1, 0, 2).copy())  # (s, b, h)
+    mask = torch.triu(torch.ones(s, s, dtype=torch.bool), 1)
+    ref, _ = F.multi_head_attention_forward(
+        tX, tX, tX, 16, H, torch.tensor(a["Wqkv"]), torch.tensor(a["bqkv"]), None, None, False, 0.0,
+        torch.tensor(a["Wo"]), torch.tensor(a["bo"]), training=False, need_weights=False,
+        attn_mask=mask)
+    ref = ref.numpy().transpose(1, 0, 2).reshape(12, 16)
+    return np.abs(out - ref).max()
+
+
+def test_attention_core_through_projections_matches_torch_mha():
+    assert check_core_mha(O) < 1e-12
+
+
+def check_core_uniform(mod):
+    """q = 0 makes every allowed key equally likely: the causal context is the
+    running mean of v, the full one the mean of all v."""
+    c = tiny_core()
+    QKV = c["QKV"].copy()
+    b, s, H, N, d = c["b"], c["s"], c["n_heads"], c["N"], c["d"]
+    per = H // N
+    for i in range(N):  # zero the Q block of every shard
+        QKV[:, i * 3 * per * d: i * 3 * per * d + per * d] = 0.0
+    err = 0.0
+    for causal in (True, False):
+        C, _ = mod.attention_core(QKV, s, H, N, causal)
+        for bi in range(b):
+            for j in range(H):
+                v = c["v"][bi, j]
+                want = np.cumsum(v, axis=0) / np.arange(1, s + 1)[:, None] if causal else \
+                    np.broadcast_to(v.mean(axis=0), (s, d))
+                err = max(err, np.abs(C[bi * s:(bi + 1) * s, j * d:(j + 1) * d] - want).max())
+    return err
+
+
+def test_attention_core_uniform_closed_form():
+    assert check_core_uniform(O) < 1e-14
+
+
+def test_attention_head_brute_force():
+    g = rng(4)
+    q, k, v = (g.standard_normal((3, 2)) for _ in range(3))
+    P, out = O.attention_head(q, k, v, True)
+    for i in range(3):
+        w = [math.exp(sum(q[i, c] * k[j, c] for c in range(2)) / math.sqrt(2)) for j in range(i + 1)]
+        tot = sum(w)
+        for c in range(2):
+            assert abs(out[i, c] - sum(w[j] * v[j, c] for j in range(i + 1)) / tot) < 1e-14
+        for j in range(3):
+            assert abs(P[i, j] - (w[j] / tot if j <= i else 0.0)) < 1e-15
+
+
+def test_planted_missing_attention_scale_is_caught(monkeypatch):
+    real = O.attention_head
+
+    def broken(q, k, v, causal):
+        return real(q * math.sqrt(q.shape[1]), k, v, causal)  # the 1/sqrt(d) undone
+    monkeypatch.setattr(O, "attention_head", broken)
+    assert check_core_sdpa(O, True) > 1e-3
+
+
+def test_planted_causal_mask_off_by_one_is_caught(monkeypatch):
+    def broken(q, k, v, causal):
+        s, d = q.shape
+        S = (q @ k.T) / math.sqrt(d)
+        if causal:  # the diagonal masked as well (a finite fill keeps row 0 defined)
+            S = np.where(np.tril(np.ones((s, s), dtype=bool), -1), S, -1e300)
+        E = np.exp(S - S.max(axis=1, keepdims=True))
+        P = E / E.sum(axis=1, keepdims=True)
+        return P, P @ v
+    monkeypatch.setattr(O, "attention_head", broken)
+    assert check_core_uniform(O) > 1e-3
+
+
+def test_planted_softmax_over_queries_is_caught(monkeypatch):
+    def broken(q, k, v, causal):
+        s, d = q.shape
+        S = (q @ k.T) / math.sqrt(d)
+        if causal:
+            S = np.where(np.tril(np.ones((s, s), dtype=bool)), S, -np.inf)
+        E = np.exp(S - S.max(axis=0, keepdims=True))
+        P = E / E.sum(axis=0, keepdims=True)
+        return P, P @ v
+    monkeypatch.setattr(O, "attention_head", broken)
+    assert check_core_sdpa(O, False) > 1e-3
+
+
+def test_planted_missing_softmax_correction_in_grad_is_caught(monkeypatch):
+    def broken(q, k, v, P, g):
+        dS = P * (g @ v.T) / math.sqrt(q.shape[1])  # the row-sum term dropped
+        return dS @ k, dS.T @ q, P.T @ g
+    monkeypatch.setattr(O, "attention_head_grad", broken)
+    assert check_core_sdpa(O, True) > 1e-3
+
+
+def test_planted_head_layout_swap_is_caught(monkeypatch):
+    real = O.attention_head_columns
+
+    def broken(h, n_heads, N, j):
+        q, k, v, c = real(h, n_heads, N, j)
+        return k, q, v, c  # Q and K blocks swapped
+    monkeypatch.setattr(O, "attention_head_columns", broken)
+    assert check_core_mha(O) > 1e-3
+
+
+# ----------------------------------------------------------------------------
 # Vocab-parallel embedding
 # ----------------------------------------------------------------------------
 def test_vocab_mask_page_example():
