@@ -164,6 +164,56 @@ TP_API tp_status tp_attn_proj_bwd(tp_dtype dt, int64_t M, int64_t h, int n_heads
                            void* const* dWo, void* dbo, int accumulate, void* stream);
 
 /* ------------------------------------------------------------------------ */
+/* Attention core (per head, between the QKV and output projections)        */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * tp_attn_core_fwd -- softmax attention of every head of every sequence
+ * ([TP notes] §Self-Attention层: each head computed on its own, heads split
+ * across shards by columns; [Walkthrough] §ParallelSelfAttention).  The
+ * pages draw the per-head formula as a figure; it is read as
+ *   S = Q_j K_j^T / sqrt(d),  P = softmax over keys (row max subtracted),
+ *   C[:, j d:(j+1) d] = P V_j,
+ * with GPT's causal mask (key position > query position excluded) when
+ * causal != 0.  No attention dropout.
+ * Layout (bf16 only; TP_ERR_UNSUPPORTED for TP_F32):
+ *   T = b s tokens, b sequences of s tokens each in consecutive rows;
+ *   d = h / n_heads; N shards, n_heads % N == 0, heads per shard in order.
+ *   QKV (T, 3h)   the shard-major output of tp_attn_proj_fwd: shard i holds
+ *                 columns [i 3h/N, (i+1) 3h/N) = [Q_i K_i V_i], each h/N wide
+ *                 and holding its heads in order.
+ *   P   out (b, n_heads, s, s) bf16 probabilities (row = query, col = key;
+ *                 zero where masked), saved for the backward.
+ *   C   out (T, h) context, head j in columns [j d, (j+1) d) (the C input of
+ *                 tp_attn_proj_fwd).
+ *   lse out (b, n_heads, s) fp32 log-sum-exp of every score row, or NULL.
+ *   workspace of tp_attn_core_workspace_size bytes, 256-byte aligned.
+ * Constraints: T % s == 0 (TP_ERR_INVALID); d and s multiples of 8
+ * (TP_ERR_ALIGN, TMA's 16-byte rule for head offsets and P's rows).
+ * The scores are computed twice (once for the row statistics, once for P):
+ * no (s x s) fp32 score matrix is stored.
+ */
+TP_API tp_status tp_attn_core_fwd(tp_dtype dt, int64_t T, int64_t s, int64_t h, int n_heads, int N,
+                                  int causal, const void* QKV, void* P, void* C, float* lse,
+                                  void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * tp_attn_core_bwd -- gradient of tp_attn_core_fwd with respect to QKV,
+ * given its P and C and the context gradient dC (T, h):
+ *   D = rowsum(dC_j * C_j),  dS = P * (dC_j V_j^T - D) / sqrt(d),
+ *   dQ_j = dS K_j,  dK_j = dS^T Q_j,  dV_j = P^T dC_j,
+ * written to dQKV (T, 3h) in the QKV layout (every column written).
+ * workspace as for the forward (it holds dS, (b, n_heads, s, s) bf16).
+ */
+TP_API tp_status tp_attn_core_bwd(tp_dtype dt, int64_t T, int64_t s, int64_t h, int n_heads, int N,
+                                  int causal, const void* QKV, const void* P, const void* C,
+                                  const void* dC, void* dQKV, void* workspace, size_t ws_bytes,
+                                  void* stream);
+
+/* Workspace bytes of tp_attn_core_fwd and _bwd (0 for invalid sizes or T = 0). */
+TP_API size_t tp_attn_core_workspace_size(int64_t T, int64_t s, int64_t h, int n_heads);
+
+/* ------------------------------------------------------------------------ */
 /* Vocab-parallel word embedding and tied output layer                       */
 /* ------------------------------------------------------------------------ */
 

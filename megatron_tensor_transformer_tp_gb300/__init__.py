@@ -27,7 +27,7 @@ __all__ = [
     "tp_debug_inject_fault", "tp_debug_set_wait_limit_ms", "tp_debug_set_gemm_kernel",
     "tp_gelu_eval", "logits_pitch", "tp_adam_step", "tp_adam_step_workspace_size",
     "tp_optimizer_state", "tp_adam_config", "tp_param_group", "make_optimizer_state",
-    "read_optimizer_state",
+    "read_optimizer_state", "tp_attn_core_fwd", "tp_attn_core_bwd", "tp_attn_core_workspace_size",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libtp.so")
@@ -104,6 +104,11 @@ _SIGNATURES = {
     "tp_adam_step": (_int, [ctypes.POINTER(tp_param_group), _int, ctypes.POINTER(tp_adam_config),
                             _c_void_p, _c_void_p, _size_t, _c_void_p]),
     "tp_adam_step_workspace_size": (_size_t, []),
+    "tp_attn_core_fwd": (_int, [_int, _i64, _i64, _i64, _int, _int, _int, _c_void_p, _c_void_p,
+                                _c_void_p, _c_void_p, _c_void_p, _size_t, _c_void_p]),
+    "tp_attn_core_bwd": (_int, [_int, _i64, _i64, _i64, _int, _int, _int, _c_void_p, _c_void_p,
+                                _c_void_p, _c_void_p, _c_void_p, _c_void_p, _size_t, _c_void_p]),
+    "tp_attn_core_workspace_size": (_size_t, [_i64, _i64, _i64, _int]),
 }
 
 _LIB: Optional[ctypes.CDLL] = None
@@ -374,6 +379,35 @@ def tied_embed_grad_noalloc(ids, dEmb, X, dLogits, range_starts, dE, accumulate=
 # ----------------------------------------------------------------------------
 # status, profiling, debugging
 # ----------------------------------------------------------------------------
+def tp_attn_core_workspace_size(T, s, h, n_heads) -> int:
+    return int(lib().tp_attn_core_workspace_size(T, s, h, n_heads))
+
+
+def _ws_bytes(workspace):
+    return workspace.numel() * workspace.element_size() if workspace is not None else 0
+
+
+def tp_attn_core_fwd(QKV, s, n_heads, N, causal, P, C, lse=None, workspace=None, stream=None):
+    """P (b, n_heads, s, s) bf16 and C (T, h) <- per-head softmax attention of
+    the shard-major QKV (T, 3h); lse (b, n_heads, s) fp32 or None."""
+    T, h3 = QKV.shape
+    _check(lib().tp_attn_core_fwd(_dtype(QKV), T, s, h3 // 3, n_heads, N, int(bool(causal)),
+                                  _dev(QKV, "QKV"), _dev(P, "P"), _dev(C, "C"), _dev(lse, "lse"),
+                                  _dev(workspace, "workspace"), _ws_bytes(workspace),
+                                  _stream(stream)),
+           "tp_attn_core_fwd")
+
+
+def tp_attn_core_bwd(QKV, P, C, dC, s, n_heads, N, causal, dQKV, workspace=None, stream=None):
+    """dQKV (T, 3h) <- gradient of tp_attn_core_fwd given P, C and dC."""
+    T, h3 = QKV.shape
+    _check(lib().tp_attn_core_bwd(_dtype(QKV), T, s, h3 // 3, n_heads, N, int(bool(causal)),
+                                  _dev(QKV, "QKV"), _dev(P, "P"), _dev(C, "C"), _dev(dC, "dC"),
+                                  _dev(dQKV, "dQKV"), _dev(workspace, "workspace"),
+                                  _ws_bytes(workspace), _stream(stream)),
+           "tp_attn_core_bwd")
+
+
 def tp_adam_step_workspace_size() -> int:
     return int(lib().tp_adam_step_workspace_size())
 

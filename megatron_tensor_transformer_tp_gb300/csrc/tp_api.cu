@@ -6,7 +6,9 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <algorithm>
 #include <atomic>
+#include <math.h>
 #include <mutex>
 #include <vector>
 
@@ -257,6 +259,7 @@ struct Plan {
     g.ldo = ldo;
     g.prod_row = -1;
     g.prod_col = -1;
+    g.alpha = 1.f;
     return g;
   }
   // Counter block for row- or column-tile completion of producing groups.
@@ -278,6 +281,7 @@ struct Plan {
 
 inline bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline bool al256(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 255u) == 0; }
+inline size_t round256(size_t b) { return (b + 255) / 256 * 256; }
 
 bool group_vec_ok(const GemmGroup& g, int in_esize) {
   const int oes = g.out_type == OUT_F32 ? 4 : 2;
@@ -758,6 +762,237 @@ extern "C" tp_status tp_attn_proj_bwd(tp_dtype dt, int64_t M, int64_t h, int n_h
 }
 
 // ===========================================================================
+// Attention core
+// ===========================================================================
+namespace {
+
+// Pointers of (sequence bi, global head j) in the shard-major QKV layout:
+// shard i = j / (heads per shard) holds [Q_i K_i V_i], each h/N columns, its
+// heads in order inside each.
+struct HeadPtrs {
+  const uint8_t *q, *k, *v;
+  size_t qc, kc, vc, cc;  // element columns of Q, K, V in QKV and of the head in C
+};
+HeadPtrs head_ptrs(const void* QKV, int64_t bi, int64_t s, int64_t h, int n_heads, int N, int j) {
+  const int64_t d = h / n_heads, per = n_heads / N, i = j / per, jl = j % per;
+  const int64_t base = i * 3 * (h / N);
+  HeadPtrs r;
+  r.qc = static_cast<size_t>(base + jl * d);
+  r.kc = static_cast<size_t>(base + h / N + jl * d);
+  r.vc = static_cast<size_t>(base + 2 * (h / N) + jl * d);
+  r.cc = static_cast<size_t>(j * d);
+  const uint8_t* row0 = cb(QKV) + static_cast<size_t>(bi * s) * static_cast<size_t>(3 * h) * 2;
+  r.q = row0 + r.qc * 2;
+  r.k = row0 + r.kc * 2;
+  r.v = row0 + r.vc * 2;
+  return r;
+}
+
+struct AttnDims {
+  int64_t b, d, P;  // sequences, head width, 64-key parts per score row
+  int64_t pairs;    // b * n_heads
+};
+
+tp_status attn_args(tp_dtype dt, int64_t T, int64_t s, int64_t h, int n_heads, int N, AttnDims* out) {
+  if (!dtype_ok(dt)) return TP_ERR_UNSUPPORTED;
+  if (T < 0 || s <= 0 || h <= 0 || n_heads < 1 || N < 1 || N > 8 || n_heads % N != 0 ||
+      h % n_heads != 0 || T % s != 0)
+    return TP_ERR_INVALID;
+  if (T > INT32_MAX || s > INT32_MAX || 3 * h > INT32_MAX) return TP_ERR_INVALID;
+  if (dt != TP_BF16) return TP_ERR_UNSUPPORTED;  // the fused epilogues live in the tensor-core engine
+  const int64_t d = h / n_heads;
+  // TMA: every head's column offset and the probabilities' row pitch s are
+  // whole 16-byte units
+  if (d % 8 != 0 || s % 8 != 0) return TP_ERR_ALIGN;
+  out->b = T / s;
+  out->d = d;
+  out->P = (s + 63) / 64;
+  out->pairs = out->b * n_heads;
+  return TP_OK;
+}
+
+size_t attn_fwd_ws(const AttnDims& a, int64_t s) {
+  return round256(static_cast<size_t>(a.pairs * a.P * s) * 8) + round256(static_cast<size_t>(a.pairs * s) * 4);
+}
+size_t attn_bwd_ws(const AttnDims& a, int64_t s) {
+  return round256(static_cast<size_t>(a.pairs * s) * 4) + round256(static_cast<size_t>(a.pairs * s * s) * 2);
+}
+
+// (sequence, head) pairs per GEMM launch: within the engine's group and
+// counter limits (groups_per_pair outputs and counters_per_pair counters each).
+int64_t pairs_per_launch(int groups_per_pair, int64_t counters_per_pair) {
+  int64_t n = kMaxGroups / groups_per_pair;
+  if (counters_per_pair > 0) n = std::min<int64_t>(n, kMaxCounters / counters_per_pair);
+  return n;
+}
+
+}  // namespace
+
+extern "C" size_t tp_attn_core_workspace_size(int64_t T, int64_t s, int64_t h, int n_heads) {
+  AttnDims a;
+  if (attn_args(TP_BF16, T, s, h, n_heads, 1, &a) != TP_OK || T == 0) return 0;
+  return std::max(attn_fwd_ws(a, s), attn_bwd_ws(a, s));
+}
+
+extern "C" tp_status tp_attn_core_fwd(tp_dtype dt, int64_t T, int64_t s, int64_t h, int n_heads, int N,
+                                      int causal, const void* QKV, void* P, void* C, float* lse,
+                                      void* workspace, size_t ws_bytes, void* stream) {
+  AttnDims a;
+  tp_status st = attn_args(dt, T, s, h, n_heads, N, &a);
+  if (st != TP_OK) return st;
+  if (T == 0) return TP_OK;
+  if (!QKV || !P || !C) return TP_ERR_INVALID;
+  if (workspace == nullptr || ws_bytes < attn_fwd_ws(a, s)) return TP_ERR_WORKSPACE;
+  if (!al256(workspace)) return TP_ERR_ALIGN;
+  cudaStream_t strm = static_cast<cudaStream_t>(stream);
+  float* parts = static_cast<float*>(workspace);
+  float* row_lse = lse ? lse
+                       : reinterpret_cast<float*>(bb(workspace) +
+                                                  round256(static_cast<size_t>(a.pairs * a.P * s) * 8));
+  const float alpha = static_cast<float>(1.0 / sqrt(static_cast<double>(a.d)));
+  const int kr_s = causal ? KR_TRI : KR_NONE;
+  // 1. per row and 64-key part: (max, sum exp) of alpha q k^T, no scores stored
+  const int64_t per1 = pairs_per_launch(1, 0);
+  for (int64_t g0 = 0; g0 < a.pairs; g0 += per1) {
+    Plan p;
+    for (int64_t g = g0; g < std::min(a.pairs, g0 + per1); ++g) {
+      const HeadPtrs hp = head_ptrs(QKV, g / n_heads, s, h, n_heads, N, static_cast<int>(g % n_heads));
+      const int si = p.add_seg(kmajor(hp.q, s, a.d, 3 * h), kmajor(hp.k, s, a.d, 3 * h), a.d);
+      GemmGroup& gr = p.add_group(s, s, si, si + 1, EPI_CE_FWD, OUT_F32, nullptr, 0);
+      gr.alpha = alpha;
+      gr.causal = causal != 0;
+      gr.kr_mode = kr_s;
+      gr.ce_part = parts;
+      gr.ce_part0 = static_cast<int>(g * a.P);
+      gr.ce_rows = static_cast<int>(s);
+    }
+    st = run_plan(p, dt, "gemm_attn_scores", strm);
+    if (st != TP_OK) return st;
+  }
+  // 2. log-sum-exp per row, parts merged in order
+  cudaError_t e = timed("attn_lse", strm, [&] {
+    return launch_attn_lse(parts, static_cast<int>(a.P), s, a.pairs * s, row_lse, strm);
+  });
+  if (e != cudaSuccess) return TP_ERR_CUDA;
+  // 3. P = exp(alpha q k^T - lse) (scores recomputed, stored in bf16), and in
+  //    the same launch C_j = P V_j, a row block once its P rows are stored
+  const int64_t rows_per_pair = (s + 255) / 256 * 2;  // 128-row blocks, pair tiles rounded up
+  const int64_t per3 = pairs_per_launch(2, rows_per_pair);
+  if (per3 < 1) return TP_ERR_INVALID;
+  for (int64_t g0 = 0; g0 < a.pairs; g0 += per3) {
+    Plan p;
+    const int64_t g1 = std::min(a.pairs, g0 + per3);
+    int rows[kMaxGroups];
+    for (int64_t g = g0; g < g1; ++g) {
+      const HeadPtrs hp = head_ptrs(QKV, g / n_heads, s, h, n_heads, N, static_cast<int>(g % n_heads));
+      rows[g - g0] = p.counters(rows_per_pair);
+      const int si = p.add_seg(kmajor(hp.q, s, a.d, 3 * h), kmajor(hp.k, s, a.d, 3 * h), a.d);
+      GemmGroup& gr = p.add_group(s, s, si, si + 1, EPI_SOFTMAX, OUT_BF16,
+                                  bb(P) + static_cast<size_t>(g * s * s) * 2, s);
+      gr.alpha = alpha;
+      gr.causal = causal != 0;
+      gr.kr_mode = kr_s;
+      gr.row_lse = row_lse + g * s;
+      gr.prod_row = rows[g - g0];
+    }
+    for (int64_t g = g0; g < g1; ++g) {
+      const int64_t bi = g / n_heads;
+      const HeadPtrs hp = head_ptrs(QKV, bi, s, h, n_heads, N, static_cast<int>(g % n_heads));
+      const void* Pg = bb(P) + static_cast<size_t>(g * s * s) * 2;
+      const int si = p.add_seg(kmajor(Pg, s, s, s), mnmajor(hp.v, s, a.d, 3 * h), s);
+      GemmGroup& gr = p.add_group(s, a.d, si, si + 1, EPI_STORE, OUT_BF16,
+                                  bb(C) + (static_cast<size_t>(bi * s) * h + hp.cc) * 2, h);
+      gr.kr_mode = causal ? KR_END : KR_NONE;
+      gr.dep_kind = DEP_ROW;
+      gr.dep_base = rows[g - g0];
+    }
+    st = run_plan(p, dt, "gemm_attn_pv", strm);
+    if (st != TP_OK) return st;
+  }
+  return TP_OK;
+}
+
+extern "C" tp_status tp_attn_core_bwd(tp_dtype dt, int64_t T, int64_t s, int64_t h, int n_heads, int N,
+                                      int causal, const void* QKV, const void* P, const void* C,
+                                      const void* dC, void* dQKV, void* workspace, size_t ws_bytes,
+                                      void* stream) {
+  AttnDims a;
+  tp_status st = attn_args(dt, T, s, h, n_heads, N, &a);
+  if (st != TP_OK) return st;
+  if (T == 0) return TP_OK;
+  if (!QKV || !P || !C || !dC || !dQKV) return TP_ERR_INVALID;
+  if (workspace == nullptr || ws_bytes < attn_bwd_ws(a, s)) return TP_ERR_WORKSPACE;
+  if (!al256(workspace)) return TP_ERR_ALIGN;
+  cudaStream_t strm = static_cast<cudaStream_t>(stream);
+  float* D = static_cast<float*>(workspace);
+  uint8_t* dS = bb(workspace) + round256(static_cast<size_t>(a.pairs * s) * 4);
+  const float alpha = static_cast<float>(1.0 / sqrt(static_cast<double>(a.d)));
+  // 1. D = rowsum(dC * C) per head and token (= sum over keys of P dP)
+  cudaError_t e = timed("attn_rowdot", strm, [&] {
+    return launch_attn_rowdot(C, dC, h, s, n_heads, static_cast<int>(a.d), a.pairs, D, strm);
+  });
+  if (e != cudaSuccess) return TP_ERR_CUDA;
+  // 2. per pair: dS = P (dC V^T - D) alpha and dV = P^T dC; then dQ = dS K per
+  //    row block of dS, dK = dS^T Q per column block of dS
+  const int64_t rows_per_pair = (s + 255) / 256 * 2;
+  const int64_t cols_per_pair = (s + 255) / 256;
+  const int64_t per = pairs_per_launch(4, rows_per_pair + cols_per_pair);
+  if (per < 1) return TP_ERR_INVALID;
+  for (int64_t g0 = 0; g0 < a.pairs; g0 += per) {
+    Plan p;
+    const int64_t g1 = std::min(a.pairs, g0 + per);
+    int rows[kMaxGroups], cols[kMaxGroups];
+    auto dS_of = [&](int64_t g) { return dS + static_cast<size_t>(g * s * s) * 2; };
+    auto dC_of = [&](int64_t g, const HeadPtrs& hp) {
+      return cb(dC) + (static_cast<size_t>((g / n_heads) * s) * h + hp.cc) * 2;
+    };
+    auto dqkv_of = [&](int64_t g, size_t col) {
+      return bb(dQKV) + (static_cast<size_t>((g / n_heads) * s) * 3 * h + col) * 2;
+    };
+    for (int64_t g = g0; g < g1; ++g) {
+      const HeadPtrs hp = head_ptrs(QKV, g / n_heads, s, h, n_heads, N, static_cast<int>(g % n_heads));
+      rows[g - g0] = p.counters(rows_per_pair);
+      cols[g - g0] = p.counters(cols_per_pair);
+      const int si = p.add_seg(kmajor(dC_of(g, hp), s, a.d, h), kmajor(hp.v, s, a.d, 3 * h), a.d);
+      GemmGroup& gr = p.add_group(s, s, si, si + 1, EPI_SMAX_BWD, OUT_BF16, dS_of(g), s);
+      gr.aux = cb(P) + static_cast<size_t>(g * s * s) * 2;
+      gr.ld_aux = s;
+      gr.row_lse = D + g * s;
+      gr.alpha = alpha;
+      gr.kr_mode = causal ? KR_TRI : KR_NONE;
+      gr.prod_row = rows[g - g0];
+      gr.prod_col = cols[g - g0];
+    }
+    for (int64_t g = g0; g < g1; ++g) {
+      const HeadPtrs hp = head_ptrs(QKV, g / n_heads, s, h, n_heads, N, static_cast<int>(g % n_heads));
+      const void* Pg = cb(P) + static_cast<size_t>(g * s * s) * 2;
+      const int si = p.add_seg(mnmajor(Pg, s, s, s), mnmajor(dC_of(g, hp), s, a.d, h), s);
+      GemmGroup& gr = p.add_group(s, a.d, si, si + 1, EPI_STORE, OUT_BF16, dqkv_of(g, hp.vc), 3 * h);
+      gr.kr_mode = causal ? KR_BEGIN : KR_NONE;
+    }
+    for (int64_t g = g0; g < g1; ++g) {
+      const HeadPtrs hp = head_ptrs(QKV, g / n_heads, s, h, n_heads, N, static_cast<int>(g % n_heads));
+      const int si = p.add_seg(kmajor(dS_of(g), s, s, s), mnmajor(hp.k, s, a.d, 3 * h), s);
+      GemmGroup& gr = p.add_group(s, a.d, si, si + 1, EPI_STORE, OUT_BF16, dqkv_of(g, hp.qc), 3 * h);
+      gr.kr_mode = causal ? KR_END : KR_NONE;
+      gr.dep_kind = DEP_ROW;
+      gr.dep_base = rows[g - g0];
+    }
+    for (int64_t g = g0; g < g1; ++g) {
+      const HeadPtrs hp = head_ptrs(QKV, g / n_heads, s, h, n_heads, N, static_cast<int>(g % n_heads));
+      const int si = p.add_seg(mnmajor(dS_of(g), s, s, s), mnmajor(hp.q, s, a.d, 3 * h), s);
+      GemmGroup& gr = p.add_group(s, a.d, si, si + 1, EPI_STORE, OUT_BF16, dqkv_of(g, hp.kc), 3 * h);
+      gr.kr_mode = causal ? KR_BEGIN : KR_NONE;
+      gr.dep_kind = DEP_COL;
+      gr.dep_base = cols[g - g0];
+    }
+    st = run_plan(p, dt, "gemm_attn_bwd", strm);
+    if (st != TP_OK) return st;
+  }
+  return TP_OK;
+}
+
+// ===========================================================================
 // Vocab-parallel embedding, logits, tied gradient
 // ===========================================================================
 namespace {
@@ -821,7 +1056,6 @@ int64_t ce_parts(const int64_t* rs, int N) {
   for (int r = 0; r < N; ++r) P += (rs[r + 1] - rs[r] + 63) / 64;
   return P;
 }
-size_t round256(size_t b) { return (b + 255) / 256 * 256; }
 
 bool ce_args_ok(int64_t T, int64_t h, int64_t V, int N, const void* X, const void* const* E,
                 const int64_t* rs, const int64_t* targets) {

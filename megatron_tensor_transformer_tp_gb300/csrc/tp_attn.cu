@@ -1,0 +1,93 @@
+// Row kernels of the attention core (the GEMMs run on the tensor-core engine):
+//   attn_lse_kernel     merges the per-64-key (max, sum exp) parts of every
+//                       score row into its log-sum-exp, parts in order;
+//   attn_rowdot_kernel  D = sum over a head's columns of dC * C per token,
+//                       the softmax backward's row term (sum_keys P dP).
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "tp_internal.h"
+
+namespace tp {
+namespace {
+
+// rows = pairs * s; part p of row r of pair g at part[(g * P + p) * s + r]
+__global__ void __launch_bounds__(256) attn_lse_kernel(const float2* __restrict__ part, int P, int64_t s,
+                                                        int64_t rows, float* __restrict__ lse) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= rows) return;
+  const int64_t g = i / s, r = i - g * s;
+  const float2* q = part + g * P * s + r;
+  float m = -INFINITY, sum = 0.f;
+  for (int p = 0; p < P; ++p) {
+    const float2 x = q[static_cast<int64_t>(p) * s];
+    if (x.x == -INFINITY) continue;  // a part with no key counted
+    const float nm = fmaxf(m, x.x);
+    sum = sum * expf(m - nm) + x.y * expf(x.x - nm);
+    m = nm;
+  }
+  lse[i] = m + logf(sum);
+}
+
+// One warp per (pair, token): D[g * s + t] = sum_c dC[row, c0 + c] C[row, c0 + c]
+// over the head's d columns (16-byte loads when d and the offsets allow).
+__global__ void __launch_bounds__(256) attn_rowdot_kernel(const __nv_bfloat16* __restrict__ C,
+                                                           const __nv_bfloat16* __restrict__ dC,
+                                                           int64_t h, int64_t s, int n_heads, int d,
+                                                           int64_t rows, int vec,
+                                                           float* __restrict__ D) {
+  const int64_t w = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (w >= rows) return;
+  const int64_t g = w / s, t = w - g * s;
+  const int64_t b = g / n_heads, j = g - b * n_heads;
+  const int64_t off = (b * s + t) * h + j * d;
+  float acc = 0.f;
+  if (vec) {
+    const uint4* c4 = reinterpret_cast<const uint4*>(C + off);
+    const uint4* g4 = reinterpret_cast<const uint4*>(dC + off);
+    for (int k = lane; k < d / 8; k += 32) {
+      const uint4 a = __ldg(c4 + k), e = __ldg(g4 + k);
+      const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
+      const __nv_bfloat162* e2 = reinterpret_cast<const __nv_bfloat162*>(&e);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float2 x = __bfloat1622float2(a2[q]), y = __bfloat1622float2(e2[q]);
+        acc = fmaf(x.x, y.x, acc);
+        acc = fmaf(x.y, y.y, acc);
+      }
+    }
+  } else {
+    for (int k = lane; k < d; k += 32) acc = fmaf(__bfloat162float(C[off + k]), __bfloat162float(dC[off + k]), acc);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  if (lane == 0) D[w] = acc;
+}
+
+}  // namespace
+
+cudaError_t launch_attn_lse(const void* part, int P, int64_t s, int64_t rows, float* lse, cudaStream_t st) {
+  const int64_t blocks = (rows + 255) / 256;
+  attn_lse_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(static_cast<const float2*>(part), P, s,
+                                                                  rows, lse);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_attn_rowdot(const void* C, const void* dC, int64_t h, int64_t s, int n_heads, int d,
+                               int64_t pairs, float* D, cudaStream_t st) {
+  const int64_t rows = pairs * s;
+  const int vec = (d % 8 == 0) && (h % 8 == 0) && ((reinterpret_cast<uintptr_t>(C) & 15u) == 0) &&
+                  ((reinterpret_cast<uintptr_t>(dC) & 15u) == 0);
+  const int64_t blocks = (rows * 32 + 255) / 256;
+  attn_rowdot_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(
+      static_cast<const __nv_bfloat16*>(C), static_cast<const __nv_bfloat16*>(dC), h, s, n_heads, d,
+      rows, vec, D);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+}  // namespace tp

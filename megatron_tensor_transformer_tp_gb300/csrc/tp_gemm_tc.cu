@@ -259,6 +259,34 @@ __device__ __forceinline__ TileCoord decode_tile(const TcGemmParams& p, int tile
   return decode_tile_rows<BM>(p, tile);
 }
 
+// k-block range [kb0, kb1) of a tile (ROWS rows from m0, columns from n0) of
+// group G for a contraction of length K: everything, or the causal part.
+template <int ROWS>
+__device__ __forceinline__ void tile_kb_range(const GemmGroup& G, int K, int m0, int n0, int& kb0,
+                                              int& kb1) {
+  const int nk = (K + BK - 1) / BK;
+  kb0 = 0;
+  kb1 = nk;
+  if (G.kr_mode == KR_TRI) {
+    if (n0 > m0 + ROWS - 1) kb1 = 0;
+  } else if (G.kr_mode == KR_END) {
+    kb1 = min(nk, (m0 + ROWS + BK - 1) / BK);
+  } else if (G.kr_mode == KR_BEGIN) {
+    kb0 = min(nk, m0 / BK);
+  }
+}
+
+// A tile with no k-blocks: its accumulator is never written, the epilogue
+// works on zeros.
+template <int ROWS>
+__device__ __forceinline__ bool tile_empty(const TcGemmParams& p, const GemmGroup& G, int m0, int n0) {
+  if (G.k_empty) return true;
+  if (G.kr_mode == KR_NONE) return false;
+  int kb0, kb1;
+  tile_kb_range<ROWS>(G, p.seg[G.seg_begin].K, m0, n0, kb0, kb1);
+  return kb1 <= kb0;
+}
+
 // ---------------------------------------------------------------------------
 // Epilogue of one 32-column chunk of one row
 // ---------------------------------------------------------------------------
@@ -502,6 +530,44 @@ __device__ __forceinline__ void epilogue_chunk(const GemmGroup& G, uint4* st, in
       }
       break;
     }
+    case EPI_SOFTMAX: {
+      // p = exp(alpha acc - lse) = 2^(acc alpha log2 e - lse log2 e); 0 for keys after the query
+      const float l2e = 1.4426950408889634f;
+      const float lse = row_ok ? G.row_lse[row] : 0.f;
+      const float a = G.alpha * l2e, base = -lse * l2e;
+      const int jmax = G.causal ? row - n : 31;  // columns j <= jmax are kept
+#pragma unroll
+      for (int j = 0; j < 32; ++j) v[j] = j <= jmax ? ex2_ftz(fmaf(v[j], a, base)) : 0.f;
+      if (coal) {
+        stage_store_rows(st, G.out, OUT_BF16, G.ldo, row0, G.M, n, v, lane);
+      } else if (row_ok) {
+        store_chunk(G.out, OUT_BF16, G.ldo, row, n, v, ncols, false);
+      }
+      break;
+    }
+    case EPI_SMAX_BWD: {
+      // dS = P * (dP - D) * alpha with P = aux, D = row_lse (the row's sum of P dP)
+      float z[32];
+      if (coal) {
+        stage_load_rows_bf16(st, G.aux, G.ld_aux, row0, G.M, n, z, lane);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) z[j] = 0.f;
+        if (row_ok)
+          load_bf16_chunk(static_cast<const __nv_bfloat16*>(G.aux) +
+                              static_cast<int64_t>(row) * G.ld_aux + n,
+                          z, ncols, false);
+      }
+      const float dd = row_ok ? G.row_lse[row] : 0.f;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) v[j] = z[j] * (v[j] - dd) * G.alpha;
+      if (coal) {
+        stage_store_rows(st, G.out, OUT_BF16, G.ldo, row0, G.M, n, v, lane);
+      } else if (row_ok) {
+        store_chunk(G.out, OUT_BF16, G.ldo, row, n, v, ncols, false);
+      }
+      break;
+    }
     case EPI_F32:
     case EPI_SEGSUM: {
       if (G.epi == EPI_SEGSUM && row_ok) {
@@ -566,9 +632,10 @@ struct ProdRing {
 
 template <int STAGES_, int STAGE_BYTES_, int A_MODE, int B_MODE>
 __device__ __forceinline__ bool produce_kblocks(ProdRing& R, const WaitCtx& wctx, uint64_t mapA,
-                                                uint64_t mapB, int nk, int m0, int n0, int n_mma) {
+                                                uint64_t mapB, int kb0, int kb1, int m0, int n0,
+                                                int n_mma) {
   const uint32_t stage_bytes = A_TILE_BYTES + static_cast<uint32_t>(n_mma) * BK * 2;
-  for (int kb = 0; kb < nk; ++kb) {
+  for (int kb = kb0; kb < kb1; ++kb) {
     if (!wait_bounded(R.empty0 + 8u * R.stage, R.phase ^ 1u, wctx)) return false;
     const uint32_t a_dst = R.tiles_base + R.stage * STAGE_BYTES_;
     const uint32_t b_dst = a_dst + A_TILE_BYTES;
@@ -609,13 +676,13 @@ __device__ __forceinline__ bool produce_kblocks(ProdRing& R, const WaitCtx& wctx
 
 template <int STAGES_, int STAGE_BYTES_>
 __device__ __forceinline__ bool produce_segment(ProdRing& R, const WaitCtx& wctx, const TcSeg& S,
-                                                uint64_t mapA, uint64_t mapB, int m0, int n0) {
+                                                uint64_t mapA, uint64_t mapB, int kb0, int kb1,
+                                                int m0, int n0) {
   const int a_mode = S.a_3d ? 2 : (S.a_mn ? 1 : 0);
   const int b_mode = S.b_fixed ? 3 : (S.b_3d ? 2 : (S.b_mn ? 1 : 0));
-  const int nk = (S.K + BK - 1) / BK;
   const int n_mma = S.n_mma;
 #define TP_PRODUCE(am, bm) \
-  produce_kblocks<STAGES_, STAGE_BYTES_, am, bm>(R, wctx, mapA, mapB, nk, m0, n0, n_mma)
+  produce_kblocks<STAGES_, STAGE_BYTES_, am, bm>(R, wctx, mapA, mapB, kb0, kb1, m0, n0, n_mma)
   switch (a_mode * 4 + b_mode) {
     case 0: return TP_PRODUCE(0, 0);
     case 1: return TP_PRODUCE(0, 1);
@@ -646,30 +713,36 @@ __device__ __forceinline__ void ce_fwd_epilogue_warp(const GemmGroup& G, int lan
   if (nb >= G.N) return;  // warp-uniform: no part here
   const int row = row0 + lane;
   const bool row_ok = row < G.M;
-  int64_t tgt = row_ok ? G.row_target[row] - G.col0 : -1;
+  int64_t tgt = (row_ok && G.row_target) ? G.row_target[row] - G.col0 : -1;
   if (tgt >= G.N) tgt = -1;  // the target is in a later range (the tile's zero-filled columns)
   const float l2e = 1.4426950408889634f;
+  const float alpha = G.alpha;
   float m = -INFINITY, s = 0.f;
   for (int c = c_begin; c < c_begin + cpw; ++c) {
     const int n = n0 + c * 32;
     if (n >= G.N) break;  // warp-uniform
-    const int ncols = min(32, G.N - n);
+    // columns j < jn of this chunk count (causal: key n + j <= query row)
+    const int jn = G.causal ? min(min(32, G.N - n), row - n + 1) : min(32, G.N - n);
     uint32_t rr[32];
     tmem_ld32(taddr + static_cast<uint32_t>(c * 32), rr);
+    float x[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(rr[j]) * alpha;
     float mx = -INFINITY;
 #pragma unroll
     for (int j = 0; j < 32; ++j)
-      if (j < ncols) mx = fmaxf(mx, __uint_as_float(rr[j]));
+      if (j < jn) mx = fmaxf(mx, x[j]);
     const int64_t tj = tgt - n;
 #pragma unroll
     for (int j = 0; j < 32; ++j)
-      if (tj == j && row_ok) G.ce_target[row] = __uint_as_float(rr[j]);
+      if (tj == j && row_ok) G.ce_target[row] = x[j];
     const float nm = fmaxf(m, mx);
+    if (nm == -INFINITY) continue;  // nothing counted yet in this row
     float acc = s * ex2_ftz((m - nm) * l2e);
     const float base = -nm * l2e;
 #pragma unroll
     for (int j = 0; j < 32; ++j)
-      if (j < ncols) acc += ex2_ftz(fmaf(__uint_as_float(rr[j]), l2e, base));
+      if (j < jn) acc += ex2_ftz(fmaf(x[j], l2e, base));
     m = nm;
     s = acc;
   }
@@ -794,8 +867,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
       }
       for (int s = seg_begin; ok && s < seg_end; ++s) {
         const TcSeg S = p.seg[s];
+        int kb0, kb1;
+        tile_kb_range<BM>(G, S.K, tc.m0, tc.n0, kb0, kb1);
         ok = produce_segment<STAGES, STAGE_BYTES>(R, wctx, S, reinterpret_cast<uint64_t>(&p.mapA[s]),
-                                                  reinterpret_cast<uint64_t>(&p.mapB[s]), tc.m0, tc.n0);
+                                                  reinterpret_cast<uint64_t>(&p.mapB[s]), kb0, kb1,
+                                                  tc.m0, tc.n0);
       }
       // next tile: the first gridDim tiles are static, the rest claimed in order
       tile = static_cast<int>(gridDim.x) + atomicAdd(sched, 1);
@@ -833,7 +909,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
       uint32_t acc = 0;
       for (int s = seg_begin; ok && s < seg_end; ++s) {
         const TcSeg S = p.seg[s];
-        const int nk = (S.K + BK - 1) / BK;
+        int kb0, kb1;
+        tile_kb_range<BM>(G, S.K, tc.m0, tc.n0, kb0, kb1);
         const uint32_t idesc = idesc_bf16(S.a_mn, S.b_mn, S.n_mma);
         // Descriptors of stage 0; a stage / k-step offset is added to the
         // 14-bit start-address field (shared addresses stay below 256 KB).
@@ -843,7 +920,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
         const uint64_t b_desc0 = sdesc(tiles_base + A_TILE_BYTES, S.b_mn ? MN_BOX_BYTES : 16, 1024);
         const uint32_t a_step = S.a_mn ? (2048 >> 4) : (32 >> 4);
         const uint32_t b_step = S.b_mn ? (2048 >> 4) : (32 >> 4);
-        for (int kb = 0; kb < nk; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!wait_bounded(full_bar(stage), phase, wctx)) {
             ok = false;
             break;
@@ -899,13 +976,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
       const int row0 = tc.m0 + quarter * 32;
       const uint32_t taddr =
           tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(buf * BN);
+      const bool empty = tile_empty<BM>(p, G, tc.m0, tc.n0);
       if (G.epi == EPI_CE_FWD) ce_fwd_epilogue_warp(G, lane, row0, tc.n0, c_begin, cpw, taddr);
       for (int c = c_begin; G.epi != EPI_CE_FWD && c < c_begin + cpw; ++c) {
         const int n = tc.n0 + c * 32;
         if (n >= G.N) break;  // warp-uniform
         uint32_t rr[32];
         float v[32];
-        if (G.k_empty) {
+        if (empty) {
 #pragma unroll
           for (int j = 0; j < 32; ++j) v[j] = 0.f;
         } else {
@@ -1091,9 +1169,9 @@ __device__ __forceinline__ uint32_t idesc_bf16_m256(int a_mn, int b_mn, int n) {
 // B, and both CTAs' copies complete on the leader's full barrier).
 template <int A_MODE, int B_MODE>
 __device__ __forceinline__ bool produce_kblocks_pair(ProdRing& R, const WaitCtx2& wctx, bool leader,
-                                                     uint64_t mapA, uint64_t mapB, int nk, int row0,
-                                                     int ncol0, uint32_t b_bytes) {
-  for (int kb = 0; kb < nk; ++kb) {
+                                                     uint64_t mapA, uint64_t mapB, int kb0, int kb1,
+                                                     int row0, int ncol0, uint32_t b_bytes) {
+  for (int kb = kb0; kb < kb1; ++kb) {
     if (!wait2(R.empty0 + 8u * R.stage, R.phase ^ 1u, wctx)) return false;
     const uint32_t a_dst = R.tiles_base + R.stage * STAGE2_BYTES;
     const uint32_t b_dst = a_dst + A_TILE_BYTES;
@@ -1137,13 +1215,12 @@ __device__ __forceinline__ bool produce_kblocks_pair(ProdRing& R, const WaitCtx2
 
 __device__ __forceinline__ bool produce_segment_pair(ProdRing& R, const WaitCtx2& wctx, bool leader,
                                                      const TcSeg& S, uint64_t mapA, uint64_t mapB,
-                                                     int row0, int ncol0) {
+                                                     int kb0, int kb1, int row0, int ncol0) {
   const int a_mode = S.a_3d ? 2 : (S.a_mn ? 1 : 0);
   const int b_mode = S.b_fixed ? 3 : (S.b_3d ? 2 : (S.b_mn ? 1 : 0));
-  const int nk = (S.K + BK - 1) / BK;
   const uint32_t b_bytes = S.b_fixed ? static_cast<uint32_t>(S.n_mma / 2) * BK * 2 : B_HALF_BYTES;
 #define TP_PRODUCE2(am, bm) \
-  produce_kblocks_pair<am, bm>(R, wctx, leader, mapA, mapB, nk, row0, ncol0, b_bytes)
+  produce_kblocks_pair<am, bm>(R, wctx, leader, mapA, mapB, kb0, kb1, row0, ncol0, b_bytes)
   switch (a_mode * 4 + b_mode) {
     case 0: return TP_PRODUCE2(0, 0);
     case 1: return TP_PRODUCE2(0, 1);
@@ -1289,8 +1366,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_pair_kernel(const __gr
       const int ncol0 = tc.n0 + 128 * static_cast<int>(rank);  // this CTA's half of B
       for (int s = seg_begin; ok && s < seg_end; ++s) {
         const TcSeg S = p.seg[s];
+        int kb0, kb1;
+        tile_kb_range<BM2>(G, S.K, tc.m0, tc.n0, kb0, kb1);
         ok = produce_segment_pair(R, wctx, leader, S, reinterpret_cast<uint64_t>(&p.mapA[s]),
-                                  reinterpret_cast<uint64_t>(&p.mapB[s]), row0, ncol0);
+                                  reinterpret_cast<uint64_t>(&p.mapB[s]), kb0, kb1, row0, ncol0);
       }
       if (leader) claim = static_cast<int>(gridDim.x >> 1) + atomicAdd(sched, 1);
     }
@@ -1334,13 +1413,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_pair_kernel(const __gr
       uint32_t acc = 0;
       for (int s = seg_begin; ok && s < seg_end; ++s) {
         const TcSeg S = p.seg[s];
-        const int nk = (S.K + BK - 1) / BK;
+        int kb0, kb1;
+        tile_kb_range<BM2>(G, S.K, tc.m0, tc.n0, kb0, kb1);
         const uint32_t idesc = idesc_bf16_m256(S.a_mn, S.b_mn, S.n_mma);
         const uint64_t a_desc0 = sdesc(tiles_base, S.a_mn ? MN_BOX_BYTES : 16, 1024);
         const uint64_t b_desc0 = sdesc(tiles_base + A_TILE_BYTES, S.b_mn ? MN_BOX_BYTES : 16, 1024);
         const uint32_t a_step = S.a_mn ? (2048 >> 4) : (32 >> 4);
         const uint32_t b_step = S.b_mn ? (2048 >> 4) : (32 >> 4);
-        for (int kb = 0; kb < nk; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!wait2(full_bar(stage), phase, wctx)) {
             ok = false;
             break;
@@ -1395,13 +1475,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_pair_kernel(const __gr
       const int row0 = tc.m0 + 128 * static_cast<int>(rank) + quarter * 32;
       const uint32_t taddr =
           tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(buf * BN);
+      const bool empty = tile_empty<BM2>(p, G, tc.m0, tc.n0);
       if (G.epi == EPI_CE_FWD) ce_fwd_epilogue_warp(G, lane, row0, tc.n0, c_begin, cpw, taddr);
       for (int c = c_begin; G.epi != EPI_CE_FWD && c < c_begin + cpw; ++c) {
         const int n = tc.n0 + c * 32;
         if (n >= G.N) break;  // warp-uniform
         uint32_t rr[32];
         float v[32];
-        if (G.k_empty) {
+        if (empty) {
 #pragma unroll
           for (int j = 0; j < 32; ++j) v[j] = 0.f;
         } else {

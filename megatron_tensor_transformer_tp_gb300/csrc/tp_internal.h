@@ -27,8 +27,18 @@ enum Epi : int {
   EPI_SEGSUM = 4,     // out (f32) = acc + sum_{j in seg(row)} seg_src[perm[j], n] (+ out)
   EPI_CE_FWD = 5,     // cross-entropy partials: per row and 64-column part, (max, sum exp(acc - max))
                       // to ce_part; the logit at the row's target column to ce_target; no output
-  EPI_CE_BWD = 6      // out (bf16) = (exp(acc - row_lse[m]) - [col0 + n == row_target[m]]) * row_dloss[m]
+  EPI_CE_BWD = 6,     // out (bf16) = (exp(acc - row_lse[m]) - [col0 + n == row_target[m]]) * row_dloss[m]
+  EPI_SOFTMAX = 7,    // out (bf16) = exp(alpha acc - row_lse[m]), 0 where causal masks (n > m)
+  EPI_SMAX_BWD = 8    // out (bf16) = aux[m, n] * (acc - row_lse[m]) * alpha  (softmax backward)
 };
+
+// Per-tile k-block ranges of causal attention (rows and columns of the output
+// are query / key positions of one sequence, or the contraction runs over them):
+//   KR_TRI    a tile whose every column lies after its every row has no
+//             k-blocks (its epilogue still runs, on zeros);
+//   KR_END    the contraction runs over keys <= the tile's last row;
+//   KR_BEGIN  the contraction runs over queries >= the tile's first row.
+enum KRange : int { KR_NONE = 0, KR_TRI = 1, KR_END = 2, KR_BEGIN = 3 };
 
 enum OutType : int { OUT_BF16 = 0, OUT_F32 = 1 };
 
@@ -72,6 +82,11 @@ struct GemmGroup {
   float* ce_part;
   float* ce_target;
   int ce_part0, ce_rows;
+  // Attention: the accumulator is scaled by alpha in the CE_FWD, SOFTMAX and
+  // SMAX_BWD epilogues (CE_FWD: 1); causal masks columns n > m in CE_FWD and
+  // SOFTMAX; kr_mode selects the tile's k-block range (KRange).
+  float alpha;
+  int causal, kr_mode, pad_attn;
 };
 
 // One operand pair of the tensor-core engine.  Operands are bf16.
@@ -125,6 +140,12 @@ struct RangeTable {
   const void* ptr[kMaxRanges];
   int n;
 };
+
+// Attention core row kernels: per-part (max, sum) merge into log-sum-exp, and
+// the per-(pair, token) dot product of dC and C over a head's columns.
+cudaError_t launch_attn_lse(const void* part, int P, int64_t s, int64_t rows, float* lse, cudaStream_t st);
+cudaError_t launch_attn_rowdot(const void* C, const void* dC, int64_t h, int64_t s, int n_heads, int d,
+                               int64_t pairs, float* D, cudaStream_t st);
 
 // Mixed-precision Adam step.  Parameter groups are cut into chunks of
 // opt_chunk_elems() elements; chunk c belongs to the last group whose

@@ -24,7 +24,7 @@ import numpy as np
 import torch
 
 __all__ = ["WORKLOADS", "normal", "uniform_ids", "mlp_inputs", "attn_inputs",
-           "embed_inputs", "ce_inputs", "adam_inputs", "split_rows", "split_cols"]
+           "embed_inputs", "ce_inputs", "adam_inputs", "attn_core_inputs", "split_rows", "split_cols"]
 
 # Workloads: shapes and seeds only.  Names state the sizes.
 WORKLOADS = {
@@ -222,3 +222,14 @@ def adam_inputs(cfg: dict, sizes=None) -> dict:
             v=normal(seed, 103 + 4 * i, (n,), 1e-3, "f32").square_(),
             weight_decay=wds[i]))
     return dict(groups=groups, state=dict(cfg["state"]), hyper=dict(cfg["hyper"]))
+
+
+def attn_core_inputs(cfg: dict) -> dict:
+    """Inputs of the attention core on an attention workload: the shard-major
+    QKV (T, 3h) and the context gradient dC (T, h), both ~ N(0, 1) bf16, for
+    b sequences of s tokens."""
+    seed, b, s, h = cfg["seed"], cfg["b"], cfg["s"], cfg["h"]
+    T = b * s
+    return dict(T=T, s=s, h=h, n_heads=cfg["n_heads"], N=cfg["N"],
+                QKV=normal(seed, 41, (T, 3 * h), 1.0, "bf16"),
+                dC=normal(seed, 42, (T, h), 1.0, "bf16"))

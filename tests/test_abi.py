@@ -212,3 +212,29 @@ def test_optimizer_struct_layout_matches_header(tmp_path):
         assert int(out[name]) == ctypes.sizeof(cls), name
         for f, _ in cls._fields_:
             assert int(out[f"{name}.{f}"]) == getattr(cls, f).offset, f"{name}.{f}"
+
+
+def core(fn="fwd", dt=tp.TP_BF16, T=512, s=256, h=512, heads=4, N=2, ws_bytes=1 << 30, ws=FAKE * 256):
+    if fn == "fwd":
+        return L.tp_attn_core_fwd(dt, T, s, h, heads, N, 1, FAKE, FAKE, FAKE, None, ws, ws_bytes, None)
+    return L.tp_attn_core_bwd(dt, T, s, h, heads, N, 1, FAKE, FAKE, FAKE, FAKE, FAKE, ws, ws_bytes, None)
+
+
+def test_attn_core_validation_and_workspace_size():
+    for fn in ("fwd", "bwd"):
+        assert core(fn, dt=tp.TP_F32) == tp.TP_ERR_UNSUPPORTED
+        assert core(fn, T=500) == tp.TP_ERR_INVALID             # T not a multiple of s
+        assert core(fn, heads=3) == tp.TP_ERR_INVALID           # h % heads
+        assert core(fn, heads=2, N=4) == tp.TP_ERR_INVALID      # heads % N
+        assert core(fn, N=9, heads=9, h=576) == tp.TP_ERR_INVALID
+        assert core(fn, s=252, T=504) == tp.TP_ERR_ALIGN        # s % 8
+        assert core(fn, h=40, heads=8, N=2) == tp.TP_ERR_ALIGN  # d = 5
+        assert core(fn, ws=None) == tp.TP_ERR_WORKSPACE
+        assert core(fn, ws_bytes=1024) == tp.TP_ERR_WORKSPACE
+        assert core(fn, ws=FAKE * 256 + 16) == tp.TP_ERR_ALIGN
+        assert core(fn, T=0) == tp.TP_OK
+    b, H, s = 2, 4, 256
+    fwd = b * H * (s // 64) * s * 8 + b * H * s * 4
+    bwd = b * H * s * 4 + b * H * s * s * 2
+    assert tp.tp_attn_core_workspace_size(512, 256, 512, 4) == max(fwd, bwd)
+    assert tp.tp_attn_core_workspace_size(500, 256, 512, 4) == 0
