@@ -380,6 +380,48 @@ class CEBench:
         return {"gemm_ce_fwd": ("tensor", f), "gemm_ce_bwd": ("tensor", 2 * f), "ce_reduce": ("hbm", red)}
 
 
+class AttnCoreBench:
+    """Causal attention core per head: forward (row statistics, P and C = P V)
+    and backward (dS with dV, then dQ and dK).  The step's FLOPs are the
+    method's: 4 b H s^2 d forward and 8 b H s^2 d backward, times the causal
+    fraction (s + 1) / 2s; the forward's second score GEMM (P is recomputed
+    rather than storing fp32 scores) is not counted in the step."""
+    kind = "attn_core"
+
+    def __init__(self, name, tp, torch):
+        self.name, self.tp, self.torch = name, tp, torch
+        cfg = SI.WORKLOADS[name]
+        a = SI.attn_core_inputs(cfg)
+        self.s, self.H, self.N, self.causal = a["s"], a["n_heads"], a["N"], cfg["causal"]
+        self.T, self.h = a["T"], a["h"]
+        self.b, self.d = self.T // self.s, self.h // self.H
+        self.QKV, self.dC = a["QKV"].cuda(), a["dC"].cuda()
+        bf = torch.bfloat16
+        self.P = torch.empty(self.b, self.H, self.s, self.s, dtype=bf, device="cuda")
+        self.C = torch.empty(self.T, self.h, dtype=bf, device="cuda")
+        self.dQKV = torch.empty(self.T, 3 * self.h, dtype=bf, device="cuda")
+        self.ws = torch.empty(tp.tp_attn_core_workspace_size(self.T, self.s, self.h, self.H),
+                              dtype=torch.uint8, device="cuda")
+        self.frac = (self.s + 1) / (2.0 * self.s) if self.causal else 1.0
+
+    def step(self):
+        tp = self.tp
+        tp.tp_attn_core_fwd(self.QKV, self.s, self.H, self.N, self.causal, self.P, self.C, None, self.ws)
+        tp.tp_attn_core_bwd(self.QKV, self.P, self.C, self.dC, self.s, self.H, self.N, self.causal,
+                            self.dQKV, self.ws)
+
+    def units(self):
+        return 12.0 * self.b * self.H * self.s * self.s * self.d * self.frac, "TFLOP/s", 1e12
+
+    def kernel_work(self):
+        u = 2.0 * self.b * self.H * self.s * self.s * self.d * self.frac  # one s x s x d contraction
+        rows = self.b * self.H * self.s
+        return {"gemm_attn_scores": ("tensor", u), "gemm_attn_pv": ("tensor", 2 * u),
+                "gemm_attn_bwd": ("tensor", 4 * u),
+                "attn_lse": ("hbm", rows * (self.s + 63) // 64 * 8.0 + rows * 4.0),
+                "attn_rowdot": ("hbm", 2.0 * self.T * self.h * 2 + rows * 4.0)}
+
+
 class AdamBench:
     """Mixed-precision Adam step over fp32 flat groups: the norm pass reads the
     gradients (4 B per value); the update reads parameter, gradient and both
@@ -411,7 +453,7 @@ class AdamBench:
 
 
 BENCHES = {"mlp": MLPBench, "attn": AttnBench, "embed": EmbedBench, "ce": CEBench,
-           "adam": AdamBench}
+           "adam": AdamBench, "attn_core": AttnCoreBench}
 
 
 def time_steps(torch, fn, steps, warmup, flush):
@@ -718,7 +760,7 @@ def secondary_rows(tp, torch, flush, peaks, peak_src, main_workload):
     rows = {}
     for name in ("embed_tied_V50257_h4096_T8192", "ce_V50257_h4096_T8192",
                  "attn_b1_s2048_h4096_heads8_N8", "mlp_b2_s2048_h4096_hp16384_N2",
-                 "adam_layer_H4096"):
+                 "attn_core_b1_s2048_heads8_d512_causal", "adam_layer_H4096"):
         if name == main_workload:
             continue
         cfg = SI.WORKLOADS[name]

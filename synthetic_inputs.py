@@ -48,6 +48,9 @@ WORKLOADS = {
     # bf16 vocab-parallel cross-entropy on the same output layer: T=8192 tokens, two ranges
     "ce_V50257_h4096_T8192": dict(kind="ce", dtype="bf16", V=50257, h=4096, b=4, s=2048,
                                   ranges=[0, 25129, 50257], seed=1005),
+    # bf16 causal attention core between the projections: b=1, s=2048, 8 heads of 512, N=8
+    "attn_core_b1_s2048_heads8_d512_causal": dict(kind="attn_core", dtype="bf16", b=1, s=2048,
+                                                  h=4096, n_heads=8, N=8, causal=True, seed=1007),
     # fp32 mixed-precision Adam step over one transformer layer of the H=4096 model:
     # QKV (3H, H), attention output (H, H), MLP up (4H, H), MLP down (H, 4H) with
     # weight decay; two LayerNorms' gain and bias (H each) without; 201,342,976 values

@@ -101,10 +101,10 @@ def test_attn_core_masked_probabilities_are_zero_and_deterministic():
     assert torch.allclose(P.sum(-1), torch.ones_like(P.sum(-1)), atol=2e-2)
 
 
-def test_attn_core_b1_s2048_h4096_heads8_N8_causal_full():
-    """The workload of the attention block (one sequence of 2048 tokens, 8
-    heads of 512, one per shard), every output against the oracle."""
-    cfg = SI.WORKLOADS["attn_b1_s2048_h4096_heads8_N8"]
+def test_attn_core_b1_s2048_heads8_d512_causal_full():
+    """The attention block's shapes (one sequence of 2048 tokens, 8 heads of
+    512, one per shard), causal, every output against the oracle."""
+    cfg = SI.WORKLOADS["attn_core_b1_s2048_heads8_d512_causal"]
     a = SI.attn_core_inputs(cfg)
     s, H, N = a["s"], a["n_heads"], a["N"]
     check(a["QKV"], a["dC"], s, H, N, True, run_core(a["QKV"], a["dC"], s, H, N, True))
