@@ -439,12 +439,25 @@ tp_status launch_tc_groups(const Plan& pl, const bool* used, GemmGroup* groups, 
   for (int i = 0; i < ng; ++i) {
     GemmGroup& g = groups[i];
     g.tile_begin = tiles;
-    tiles += g.tiles_m * g.tiles_n;
+    // causal groups whose empty tiles need not run (and that count no tiles
+    // for dependants) enumerate only their causal tiles
+    g.tri = g.kr_mode == KR_TRI && g.tri_ok && g.prod_row < 0 && g.prod_col < 0 && i >= interleave;
+    if (g.tri) {
+      for (int mt = 0; mt < g.tiles_m; ++mt)
+        tiles += std::min(g.tiles_n, (mt * rows_per_tile + rows_per_tile - 1) / g.bn + 1);
+    } else {
+      tiles += g.tiles_m * g.tiles_n;
+    }
   }
   // one count per producer tile (one-SM kernel), one per epilogue warp and CTA (two-SM kernel)
   set_dep_targets(groups, ng, pair ? kEpiWarps : 1, pair ? 2 : 1);
   for (int i = 0; i < ng; ++i) p.grp[i] = groups[i];
   p.pair = pair ? 1 : 0;
+  p.attn = 0;
+  for (int i = 0; i < ng; ++i)
+    if (groups[i].kr_mode != KR_NONE || groups[i].causal || groups[i].alpha != 1.f ||
+        groups[i].epi == EPI_SOFTMAX || groups[i].epi == EPI_SMAX_BWD)
+      p.attn = 1;
   p.num_groups = ng;
   p.num_segs = pl.ns;
   p.total_tiles = tiles;
@@ -865,13 +878,14 @@ extern "C" tp_status tp_attn_core_fwd(tp_dtype dt, int64_t T, int64_t s, int64_t
       gr.ce_part = parts;
       gr.ce_part0 = static_cast<int>(g * a.P);
       gr.ce_rows = static_cast<int>(s);
+      gr.tri_ok = 1;  // parts after a row's last key are never read
     }
     st = run_plan(p, dt, "gemm_attn_scores", strm);
     if (st != TP_OK) return st;
   }
   // 2. log-sum-exp per row, parts merged in order
   cudaError_t e = timed("attn_lse", strm, [&] {
-    return launch_attn_lse(parts, static_cast<int>(a.P), s, a.pairs * s, row_lse, strm);
+    return launch_attn_lse(parts, static_cast<int>(a.P), s, a.pairs * s, causal != 0, row_lse, strm);
   });
   if (e != cudaSuccess) return TP_ERR_CUDA;
   // 3. P = exp(alpha q k^T - lse) (scores recomputed, stored in bf16), and in
@@ -960,6 +974,7 @@ extern "C" tp_status tp_attn_core_bwd(tp_dtype dt, int64_t T, int64_t s, int64_t
       gr.row_lse = D + g * s;
       gr.alpha = alpha;
       gr.kr_mode = causal ? KR_TRI : KR_NONE;
+      gr.tri_ok = 1;  // dQ and dK read only the causal tiles of dS
       gr.prod_row = rows[g - g0];
       gr.prod_col = cols[g - g0];
     }

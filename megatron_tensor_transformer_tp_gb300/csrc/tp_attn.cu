@@ -1,6 +1,6 @@
 // Row kernels of the attention core (the GEMMs run on the tensor-core engine):
 //   attn_lse_kernel     merges the per-64-key (max, sum exp) parts of every
-//                       score row into its log-sum-exp, parts in order;
+//                       score row into its log-sum-exp, in a fixed order;
 //   attn_rowdot_kernel  D = sum over a head's columns of dC * C per token,
 //                       the softmax backward's row term (sum_keys P dP).
 #include <cuda_bf16.h>
@@ -13,22 +13,43 @@
 namespace tp {
 namespace {
 
-// rows = pairs * s; part p of row r of pair g at part[(g * P + p) * s + r]
-__global__ void __launch_bounds__(256) attn_lse_kernel(const float2* __restrict__ part, int P, int64_t s,
-                                                        int64_t rows, float* __restrict__ lse) {
-  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (i >= rows) return;
-  const int64_t g = i / s, r = i - g * s;
-  const float2* q = part + g * P * s + r;
+// rows = pairs * s; part p of row r of pair g at part[(g * P + p) * s + r].
+// A block takes 32 rows (lane = row) and 8 slices (warp = slice): slice w
+// merges parts w, w + 8, ... of its row, then slice 0 merges the 8 slices in
+// order.  Causal rows stop at the part of their own position.
+constexpr int kLseSlices = 8;
+
+__device__ __forceinline__ void lse_merge(float& m, float& sum, float xm, float xs) {
+  if (xm == -INFINITY) return;  // nothing counted there
+  const float nm = fmaxf(m, xm);
+  sum = sum * expf(m - nm) + xs * expf(xm - nm);
+  m = nm;
+}
+
+__global__ void __launch_bounds__(32 * kLseSlices) attn_lse_kernel(const float2* __restrict__ part, int P,
+                                                                    int64_t s, int64_t rows, int causal,
+                                                                    float* __restrict__ lse) {
+  __shared__ float sm[kLseSlices][32], ss[kLseSlices][32];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * 32 + lane;
   float m = -INFINITY, sum = 0.f;
-  for (int p = 0; p < P; ++p) {
-    const float2 x = q[static_cast<int64_t>(p) * s];
-    if (x.x == -INFINITY) continue;  // a part with no key counted
-    const float nm = fmaxf(m, x.x);
-    sum = sum * expf(m - nm) + x.y * expf(x.x - nm);
-    m = nm;
+  if (i < rows) {
+    const int64_t g = i / s, r = i - g * s;
+    const int plim = causal ? static_cast<int>(r / 64) + 1 : P;
+    const float2* q = part + g * P * s + r;
+    for (int p = w; p < plim; p += kLseSlices) {
+      const float2 x = q[static_cast<int64_t>(p) * s];
+      lse_merge(m, sum, x.x, x.y);
+    }
   }
-  lse[i] = m + logf(sum);
+  sm[w][lane] = m;
+  ss[w][lane] = sum;
+  __syncthreads();
+  if (w == 0 && i < rows) {
+    float M = sm[0][lane], S = ss[0][lane];
+    for (int k = 1; k < kLseSlices; ++k) lse_merge(M, S, sm[k][lane], ss[k][lane]);
+    lse[i] = M + logf(S);
+  }
 }
 
 // One warp per (pair, token): D[g * s + t] = sum_c dC[row, c0 + c] C[row, c0 + c]
@@ -69,10 +90,11 @@ __global__ void __launch_bounds__(256) attn_rowdot_kernel(const __nv_bfloat16* _
 
 }  // namespace
 
-cudaError_t launch_attn_lse(const void* part, int P, int64_t s, int64_t rows, float* lse, cudaStream_t st) {
-  const int64_t blocks = (rows + 255) / 256;
-  attn_lse_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(static_cast<const float2*>(part), P, s,
-                                                                  rows, lse);
+cudaError_t launch_attn_lse(const void* part, int P, int64_t s, int64_t rows, int causal, float* lse,
+                            cudaStream_t st) {
+  const int64_t blocks = (rows + 31) / 32;
+  attn_lse_kernel<<<static_cast<unsigned>(blocks), 32 * kLseSlices, 0, st>>>(
+      static_cast<const float2*>(part), P, s, rows, causal, lse);
   count_launches(1);
   return cudaGetLastError();
 }

@@ -217,7 +217,7 @@ struct TileCoord {
   int g, m0, n0;
 };
 
-template <int ROWS>
+template <int ROWS, bool ATTN>
 __device__ __forceinline__ TileCoord decode_tile_rows(const TcGemmParams& p, int tile) {
   if (tile < p.interleave_tiles) {
     // Leading groups share the row tiling.  They are enumerated in super-rows
@@ -250,23 +250,41 @@ __device__ __forceinline__ TileCoord decode_tile_rows(const TcGemmParams& p, int
   const int local = tile - G.tile_begin;
   TileCoord c;
   c.g = g;
-  c.m0 = (local % G.tiles_m) * ROWS;
+  if (ATTN && G.tri) {
+    // causal: only the tiles with a column at or before their last row, row
+    // block by row block (row block mt has min(tiles_n, (mt+1) ROWS / bn
+    // rounded up) of them)
+    int mt = 0, acc = 0;
+    for (; mt < G.tiles_m - 1; ++mt) {
+      const int cnt = min(G.tiles_n, (mt * ROWS + ROWS - 1) / G.bn + 1);
+      if (local < acc + cnt) break;
+      acc += cnt;
+    }
+    c.m0 = mt * ROWS;
+    c.n0 = (local - acc) * G.bn;
+    return c;
+  }
+  int mt = local % G.tiles_m;
+  if (ATTN && G.kr_mode == KR_END) mt = G.tiles_m - 1 - mt;  // longest contraction first
+  c.m0 = mt * ROWS;
   c.n0 = (local / G.tiles_m) * G.bn;
   return c;
 }
 
+template <bool ATTN>
 __device__ __forceinline__ TileCoord decode_tile(const TcGemmParams& p, int tile) {
-  return decode_tile_rows<BM>(p, tile);
+  return decode_tile_rows<BM, ATTN>(p, tile);
 }
 
 // k-block range [kb0, kb1) of a tile (ROWS rows from m0, columns from n0) of
 // group G for a contraction of length K: everything, or the causal part.
-template <int ROWS>
+template <int ROWS, bool ATTN>
 __device__ __forceinline__ void tile_kb_range(const GemmGroup& G, int K, int m0, int n0, int& kb0,
                                               int& kb1) {
   const int nk = (K + BK - 1) / BK;
   kb0 = 0;
   kb1 = nk;
+  if (!ATTN) return;
   if (G.kr_mode == KR_TRI) {
     if (n0 > m0 + ROWS - 1) kb1 = 0;
   } else if (G.kr_mode == KR_END) {
@@ -278,12 +296,12 @@ __device__ __forceinline__ void tile_kb_range(const GemmGroup& G, int K, int m0,
 
 // A tile with no k-blocks: its accumulator is never written, the epilogue
 // works on zeros.
-template <int ROWS>
+template <int ROWS, bool ATTN>
 __device__ __forceinline__ bool tile_empty(const TcGemmParams& p, const GemmGroup& G, int m0, int n0) {
   if (G.k_empty) return true;
-  if (G.kr_mode == KR_NONE) return false;
+  if (!ATTN || G.kr_mode == KR_NONE) return false;
   int kb0, kb1;
-  tile_kb_range<ROWS>(G, p.seg[G.seg_begin].K, m0, n0, kb0, kb1);
+  tile_kb_range<ROWS, ATTN>(G, p.seg[G.seg_begin].K, m0, n0, kb0, kb1);
   return kb1 <= kb0;
 }
 
@@ -452,12 +470,53 @@ __device__ __forceinline__ void prefetch_bias(const GemmGroup& G, int n, int lan
 // Epilogue of one 32 x 32 chunk: rows row0 .. row0+31 (lane l owns row0 + l),
 // columns n .. n+31.  Called by all 32 lanes of the warp (the staged paths
 // are warp-collective); rows >= M are computed but never stored.
+template <bool ATTN>
 __device__ __forceinline__ void epilogue_chunk(const GemmGroup& G, uint4* st, int lane, int row0,
                                                int n, float* v) {
   const int row = row0 + lane;
   const bool row_ok = row < G.M;
   const int ncols = min(32, G.N - n);
   const bool coal = (ncols == 32) && G.vec_ok;  // warp-uniform
+  if constexpr (ATTN) {
+    if (G.epi == EPI_SOFTMAX) {
+      // p = exp(alpha acc - lse) = 2^(acc alpha log2 e - lse log2 e); 0 for keys after the query
+      const float l2e = 1.4426950408889634f;
+      const float lse = row_ok ? G.row_lse[row] : 0.f;
+      const float a = G.alpha * l2e, base = -lse * l2e;
+      const int jmax = G.causal ? row - n : 31;  // columns j <= jmax are kept
+#pragma unroll
+      for (int j = 0; j < 32; ++j) v[j] = j <= jmax ? ex2_ftz(fmaf(v[j], a, base)) : 0.f;
+      if (coal) {
+        stage_store_rows(st, G.out, OUT_BF16, G.ldo, row0, G.M, n, v, lane);
+      } else if (row_ok) {
+        store_chunk(G.out, OUT_BF16, G.ldo, row, n, v, ncols, false);
+      }
+      return;
+    }
+    if (G.epi == EPI_SMAX_BWD) {
+      // dS = P * (dP - D) * alpha with P = aux, D = row_lse (the row's sum of P dP)
+      float z[32];
+      if (coal) {
+        stage_load_rows_bf16(st, G.aux, G.ld_aux, row0, G.M, n, z, lane);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) z[j] = 0.f;
+        if (row_ok)
+          load_bf16_chunk(static_cast<const __nv_bfloat16*>(G.aux) +
+                              static_cast<int64_t>(row) * G.ld_aux + n,
+                          z, ncols, false);
+      }
+      const float dd = row_ok ? G.row_lse[row] : 0.f;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) v[j] = z[j] * (v[j] - dd) * G.alpha;
+      if (coal) {
+        stage_store_rows(st, G.out, OUT_BF16, G.ldo, row0, G.M, n, v, lane);
+      } else if (row_ok) {
+        store_chunk(G.out, OUT_BF16, G.ldo, row, n, v, ncols, false);
+      }
+      return;
+    }
+  }
   switch (G.epi) {
     case EPI_STORE:
     case EPI_BIAS_GELU: {
@@ -523,44 +582,6 @@ __device__ __forceinline__ void epilogue_chunk(const GemmGroup& G, uint4* st, in
         if (tgt == j) pj -= 1.f;
         v[j] = pj * dl;
       }
-      if (coal) {
-        stage_store_rows(st, G.out, OUT_BF16, G.ldo, row0, G.M, n, v, lane);
-      } else if (row_ok) {
-        store_chunk(G.out, OUT_BF16, G.ldo, row, n, v, ncols, false);
-      }
-      break;
-    }
-    case EPI_SOFTMAX: {
-      // p = exp(alpha acc - lse) = 2^(acc alpha log2 e - lse log2 e); 0 for keys after the query
-      const float l2e = 1.4426950408889634f;
-      const float lse = row_ok ? G.row_lse[row] : 0.f;
-      const float a = G.alpha * l2e, base = -lse * l2e;
-      const int jmax = G.causal ? row - n : 31;  // columns j <= jmax are kept
-#pragma unroll
-      for (int j = 0; j < 32; ++j) v[j] = j <= jmax ? ex2_ftz(fmaf(v[j], a, base)) : 0.f;
-      if (coal) {
-        stage_store_rows(st, G.out, OUT_BF16, G.ldo, row0, G.M, n, v, lane);
-      } else if (row_ok) {
-        store_chunk(G.out, OUT_BF16, G.ldo, row, n, v, ncols, false);
-      }
-      break;
-    }
-    case EPI_SMAX_BWD: {
-      // dS = P * (dP - D) * alpha with P = aux, D = row_lse (the row's sum of P dP)
-      float z[32];
-      if (coal) {
-        stage_load_rows_bf16(st, G.aux, G.ld_aux, row0, G.M, n, z, lane);
-      } else {
-#pragma unroll
-        for (int j = 0; j < 32; ++j) z[j] = 0.f;
-        if (row_ok)
-          load_bf16_chunk(static_cast<const __nv_bfloat16*>(G.aux) +
-                              static_cast<int64_t>(row) * G.ld_aux + n,
-                          z, ncols, false);
-      }
-      const float dd = row_ok ? G.row_lse[row] : 0.f;
-#pragma unroll
-      for (int j = 0; j < 32; ++j) v[j] = z[j] * (v[j] - dd) * G.alpha;
       if (coal) {
         stage_store_rows(st, G.out, OUT_BF16, G.ldo, row0, G.M, n, v, lane);
       } else if (row_ok) {
@@ -707,6 +728,7 @@ __device__ __forceinline__ bool produce_segment(ProdRing& R, const WaitCtx& wctx
 // exp(logit - max)) per row, and the logit at the row's target column when
 // the target lies in the part.
 // ---------------------------------------------------------------------------
+template <bool ATTN>
 __device__ __forceinline__ void ce_fwd_epilogue_warp(const GemmGroup& G, int lane, int row0, int n0,
                                                      int c_begin, int cpw, uint32_t taddr) {
   const int nb = n0 + c_begin * 32;
@@ -716,18 +738,18 @@ __device__ __forceinline__ void ce_fwd_epilogue_warp(const GemmGroup& G, int lan
   int64_t tgt = (row_ok && G.row_target) ? G.row_target[row] - G.col0 : -1;
   if (tgt >= G.N) tgt = -1;  // the target is in a later range (the tile's zero-filled columns)
   const float l2e = 1.4426950408889634f;
-  const float alpha = G.alpha;
+  const float alpha = ATTN ? G.alpha : 1.f;
   float m = -INFINITY, s = 0.f;
   for (int c = c_begin; c < c_begin + cpw; ++c) {
     const int n = n0 + c * 32;
     if (n >= G.N) break;  // warp-uniform
     // columns j < jn of this chunk count (causal: key n + j <= query row)
-    const int jn = G.causal ? min(min(32, G.N - n), row - n + 1) : min(32, G.N - n);
+    const int jn = (ATTN && G.causal) ? min(min(32, G.N - n), row - n + 1) : min(32, G.N - n);
     uint32_t rr[32];
     tmem_ld32(taddr + static_cast<uint32_t>(c * 32), rr);
     float x[32];
 #pragma unroll
-    for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(rr[j]) * alpha;
+    for (int j = 0; j < 32; ++j) x[j] = ATTN ? __uint_as_float(rr[j]) * alpha : __uint_as_float(rr[j]);
     float mx = -INFINITY;
 #pragma unroll
     for (int j = 0; j < 32; ++j)
@@ -737,7 +759,7 @@ __device__ __forceinline__ void ce_fwd_epilogue_warp(const GemmGroup& G, int lan
     for (int j = 0; j < 32; ++j)
       if (tj == j && row_ok) G.ce_target[row] = x[j];
     const float nm = fmaxf(m, mx);
-    if (nm == -INFINITY) continue;  // nothing counted yet in this row
+    if (ATTN && nm == -INFINITY) continue;  // nothing counted yet in this row
     float acc = s * ex2_ftz((m - nm) * l2e);
     const float base = -nm * l2e;
 #pragma unroll
@@ -764,6 +786,7 @@ __device__ int g_dep[kSchedSlots * kMaxCounters];
 // ---------------------------------------------------------------------------
 // The kernel
 // ---------------------------------------------------------------------------
+template <bool ATTN>
 __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_constant__ TcGemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -840,7 +863,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
       tile_ids[r] = t;
       mbar_arrive(tile_full_bar(r));
       if (t < 0) break;
-      const TileCoord tc = decode_tile(p, t);
+      const TileCoord tc = decode_tile<ATTN>(p, t);
       const GemmGroup& G = p.grp[tc.g];
       const int seg_begin = G.seg_begin, seg_end = G.seg_end;
       if (G.dep_kind != DEP_NONE) {
@@ -868,7 +891,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
       for (int s = seg_begin; ok && s < seg_end; ++s) {
         const TcSeg S = p.seg[s];
         int kb0, kb1;
-        tile_kb_range<BM>(G, S.K, tc.m0, tc.n0, kb0, kb1);
+        tile_kb_range<BM, ATTN>(G, S.K, tc.m0, tc.n0, kb0, kb1);
         ok = produce_segment<STAGES, STAGE_BYTES>(R, wctx, S, reinterpret_cast<uint64_t>(&p.mapA[s]),
                                                   reinterpret_cast<uint64_t>(&p.mapB[s]), kb0, kb1,
                                                   tc.m0, tc.n0);
@@ -898,7 +921,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
       const int tile = tile_ids[r];
       mbar_arrive(tile_empty_bar(r));
       if (tile < 0) break;
-      const TileCoord tc = decode_tile(p, tile);
+      const TileCoord tc = decode_tile<ATTN>(p, tile);
       const GemmGroup& G = p.grp[tc.g];
       const int buf = lt & 1;
       const uint32_t tphase = static_cast<uint32_t>(lt >> 1) & 1u;
@@ -910,7 +933,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
       for (int s = seg_begin; ok && s < seg_end; ++s) {
         const TcSeg S = p.seg[s];
         int kb0, kb1;
-        tile_kb_range<BM>(G, S.K, tc.m0, tc.n0, kb0, kb1);
+        tile_kb_range<BM, ATTN>(G, S.K, tc.m0, tc.n0, kb0, kb1);
         const uint32_t idesc = idesc_bf16(S.a_mn, S.b_mn, S.n_mma);
         // Descriptors of stage 0; a stage / k-step offset is added to the
         // 14-bit start-address field (shared addresses stay below 256 KB).
@@ -964,7 +987,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
       __syncwarp();
       if (lane == 0) mbar_arrive(tile_empty_bar(r));
       if (tile < 0) break;
-      const TileCoord tc = decode_tile(p, tile);
+      const TileCoord tc = decode_tile<ATTN>(p, tile);
       const GemmGroup& G = p.grp[tc.g];
       const int buf = lt & 1;
       const uint32_t tphase = static_cast<uint32_t>(lt >> 1) & 1u;
@@ -976,8 +999,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
       const int row0 = tc.m0 + quarter * 32;
       const uint32_t taddr =
           tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(buf * BN);
-      const bool empty = tile_empty<BM>(p, G, tc.m0, tc.n0);
-      if (G.epi == EPI_CE_FWD) ce_fwd_epilogue_warp(G, lane, row0, tc.n0, c_begin, cpw, taddr);
+      const bool empty = tile_empty<BM, ATTN>(p, G, tc.m0, tc.n0);
+      if (G.epi == EPI_CE_FWD) ce_fwd_epilogue_warp<ATTN>(G, lane, row0, tc.n0, c_begin, cpw, taddr);
       for (int c = c_begin; G.epi != EPI_CE_FWD && c < c_begin + cpw; ++c) {
         const int n = tc.n0 + c * 32;
         if (n >= G.N) break;  // warp-uniform
@@ -991,7 +1014,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
 #pragma unroll
           for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(rr[j]);
         }
-        epilogue_chunk(G, epi_stage, lane, row0, n, v);
+        epilogue_chunk<ATTN>(G, epi_stage, lane, row0, n, v);
       }
       tc_fence_before();
       __syncwarp();
@@ -1238,6 +1261,7 @@ __device__ __forceinline__ bool produce_segment_pair(ProdRing& R, const WaitCtx2
 #undef TP_PRODUCE2
 }
 
+template <bool ATTN>
 __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_pair_kernel(const __grid_constant__ TcGemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -1340,7 +1364,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_pair_kernel(const __gr
         release_tile(i);
       }
       if (t < 0) break;
-      const TileCoord tc = decode_tile_rows<BM2>(p, t);
+      const TileCoord tc = decode_tile_rows<BM2, ATTN>(p, t);
       const GemmGroup& G = p.grp[tc.g];
       const int seg_begin = G.seg_begin, seg_end = G.seg_end;
       const int row0 = tc.m0 + 128 * static_cast<int>(rank);  // this CTA's rows
@@ -1367,7 +1391,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_pair_kernel(const __gr
       for (int s = seg_begin; ok && s < seg_end; ++s) {
         const TcSeg S = p.seg[s];
         int kb0, kb1;
-        tile_kb_range<BM2>(G, S.K, tc.m0, tc.n0, kb0, kb1);
+        tile_kb_range<BM2, ATTN>(G, S.K, tc.m0, tc.n0, kb0, kb1);
         ok = produce_segment_pair(R, wctx, leader, S, reinterpret_cast<uint64_t>(&p.mapA[s]),
                                   reinterpret_cast<uint64_t>(&p.mapB[s]), kb0, kb1, row0, ncol0);
       }
@@ -1402,7 +1426,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_pair_kernel(const __gr
       if (!take_tile(lt, tile)) break;
       release_tile(lt);
       if (tile < 0) break;
-      const TileCoord tc = decode_tile_rows<BM2>(p, tile);
+      const TileCoord tc = decode_tile_rows<BM2, ATTN>(p, tile);
       const GemmGroup& G = p.grp[tc.g];
       const int buf = lt & 1;
       const uint32_t tphase = static_cast<uint32_t>(lt >> 1) & 1u;
@@ -1414,7 +1438,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_pair_kernel(const __gr
       for (int s = seg_begin; ok && s < seg_end; ++s) {
         const TcSeg S = p.seg[s];
         int kb0, kb1;
-        tile_kb_range<BM2>(G, S.K, tc.m0, tc.n0, kb0, kb1);
+        tile_kb_range<BM2, ATTN>(G, S.K, tc.m0, tc.n0, kb0, kb1);
         const uint32_t idesc = idesc_bf16_m256(S.a_mn, S.b_mn, S.n_mma);
         const uint64_t a_desc0 = sdesc(tiles_base, S.a_mn ? MN_BOX_BYTES : 16, 1024);
         const uint64_t b_desc0 = sdesc(tiles_base + A_TILE_BYTES, S.b_mn ? MN_BOX_BYTES : 16, 1024);
@@ -1465,7 +1489,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_pair_kernel(const __gr
       __syncwarp();
       if (lane == 0) release_tile(lt);
       if (tile < 0) break;
-      const TileCoord tc = decode_tile_rows<BM2>(p, tile);
+      const TileCoord tc = decode_tile_rows<BM2, ATTN>(p, tile);
       const GemmGroup& G = p.grp[tc.g];
       const int buf = lt & 1;
       const uint32_t tphase = static_cast<uint32_t>(lt >> 1) & 1u;
@@ -1475,8 +1499,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_pair_kernel(const __gr
       const int row0 = tc.m0 + 128 * static_cast<int>(rank) + quarter * 32;
       const uint32_t taddr =
           tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(buf * BN);
-      const bool empty = tile_empty<BM2>(p, G, tc.m0, tc.n0);
-      if (G.epi == EPI_CE_FWD) ce_fwd_epilogue_warp(G, lane, row0, tc.n0, c_begin, cpw, taddr);
+      const bool empty = tile_empty<BM2, ATTN>(p, G, tc.m0, tc.n0);
+      if (G.epi == EPI_CE_FWD) ce_fwd_epilogue_warp<ATTN>(G, lane, row0, tc.n0, c_begin, cpw, taddr);
       for (int c = c_begin; G.epi != EPI_CE_FWD && c < c_begin + cpw; ++c) {
         const int n = tc.n0 + c * 32;
         if (n >= G.N) break;  // warp-uniform
@@ -1490,7 +1514,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_pair_kernel(const __gr
 #pragma unroll
           for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(rr[j]);
         }
-        epilogue_chunk(G, epi_stage, lane, row0, n, v);
+        epilogue_chunk<ATTN>(G, epi_stage, lane, row0, n, v);
       }
       tc_fence_before();
       if (G.prod_row >= 0 || G.prod_col >= 0) {
@@ -1536,11 +1560,17 @@ cudaError_t launch_tc_gemm(const TcGemmParams& p_in, int num_sms, cudaStream_t s
   static int max_clusters = 0;
   static unsigned slot_seq = 0;
   if (!attr_set) {
-    cudaError_t e =
-        cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(tc_gemm_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             SMEM2_BYTES);
+    cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<false>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(tc_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               SMEM_BYTES);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(tc_gemm_pair_kernel<false>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM2_BYTES);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(tc_gemm_pair_kernel<true>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM2_BYTES);
     if (e != cudaSuccess) return e;
     // Every cluster of the persistent grid must be resident at once (tiles
     // may wait on tiles other clusters hold), so size the grid by occupancy.
@@ -1555,7 +1585,7 @@ cudaError_t launch_tc_gemm(const TcGemmParams& p_in, int num_sms, cudaStream_t s
     cfg.dynamicSmemBytes = SMEM2_BYTES;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaOccupancyMaxActiveClusters(&max_clusters, tc_gemm_pair_kernel, &cfg);
+    e = cudaOccupancyMaxActiveClusters(&max_clusters, tc_gemm_pair_kernel<false>, &cfg);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
@@ -1578,12 +1608,14 @@ cudaError_t launch_tc_gemm(const TcGemmParams& p_in, int num_sms, cudaStream_t s
     cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, tc_gemm_pair_kernel, p);
+    cudaError_t e = p.attn ? cudaLaunchKernelEx(&cfg, tc_gemm_pair_kernel<true>, p)
+                           : cudaLaunchKernelEx(&cfg, tc_gemm_pair_kernel<false>, p);
     count_launches(1);
     return e != cudaSuccess ? e : cudaGetLastError();
   }
   const int grid = p.total_tiles < num_sms ? p.total_tiles : num_sms;
-  tc_gemm_kernel<<<grid, NUM_THREADS, SMEM_BYTES, s>>>(p);
+  if (p.attn) tc_gemm_kernel<true><<<grid, NUM_THREADS, SMEM_BYTES, s>>>(p);
+  else tc_gemm_kernel<false><<<grid, NUM_THREADS, SMEM_BYTES, s>>>(p);
   count_launches(1);
   return cudaGetLastError();
 }

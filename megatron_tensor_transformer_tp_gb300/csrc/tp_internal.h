@@ -86,7 +86,10 @@ struct GemmGroup {
   // SMAX_BWD epilogues (CE_FWD: 1); causal masks columns n > m in CE_FWD and
   // SOFTMAX; kr_mode selects the tile's k-block range (KRange).
   float alpha;
-  int causal, kr_mode, pad_attn;
+  int causal, kr_mode;
+  int tri_ok;  // KR_TRI tiles with no k-blocks need not run (their outputs are never read)
+  int tri;     // set by the launcher: only the causal tiles are enumerated
+  int pad_attn;
 };
 
 // One operand pair of the tensor-core engine.  Operands are bf16.
@@ -115,6 +118,7 @@ struct TcGemmParams {
   int interleave_gm;
   int num_counters;
   int pair;              // 1: two-SM kernel (256-row pair tiles), 0: one-SM kernel
+  int attn;              // 1: the kernels' attention instance (causal ranges, softmax epilogues)
   unsigned* err;         // device error word
   unsigned long long wait_limit_ns;
 };
@@ -143,7 +147,8 @@ struct RangeTable {
 
 // Attention core row kernels: per-part (max, sum) merge into log-sum-exp, and
 // the per-(pair, token) dot product of dC and C over a head's columns.
-cudaError_t launch_attn_lse(const void* part, int P, int64_t s, int64_t rows, float* lse, cudaStream_t st);
+cudaError_t launch_attn_lse(const void* part, int P, int64_t s, int64_t rows, int causal, float* lse,
+                            cudaStream_t st);
 cudaError_t launch_attn_rowdot(const void* C, const void* dC, int64_t h, int64_t s, int n_heads, int d,
                                int64_t pairs, float* D, cudaStream_t st);
 
