@@ -453,6 +453,9 @@ tp_status launch_tc_groups(const Plan& pl, const bool* used, GemmGroup* groups, 
   set_dep_targets(groups, ng, pair ? kEpiWarps : 1, pair ? 2 : 1);
   for (int i = 0; i < ng; ++i) p.grp[i] = groups[i];
   p.pair = pair ? 1 : 0;
+  p.has_dep = 0;
+  for (int i = 0; i < ng; ++i)
+    if (groups[i].dep_kind != DEP_NONE) p.has_dep = 1;
   p.attn = 0;
   for (int i = 0; i < ng; ++i)
     if (groups[i].kr_mode != KR_NONE || groups[i].causal || groups[i].alpha != 1.f ||

@@ -56,8 +56,17 @@ constexpr int MN_BOX_BYTES = 64 * BK * 2;  // one 64(MN) x 64(K) box: 8 KB
 constexpr int BAR_BYTES = 512;
 constexpr int EPI_STAGE_BYTES = 32 * 64;  // per epilogue warp: 32 rows x 64 bytes
 constexpr int EPI_WARP_BYTES = EPI_STAGE_BYTES;
-constexpr int SMEM_BYTES =
-    STAGES * STAGE_BYTES + BAR_BYTES + NUM_EPI_WARPS * EPI_WARP_BYTES + 1024;  // + alignment slack
+// Per-group tile table in shared memory (the producer's decode reads it
+// instead of the kernel parameters, whose dynamically indexed loads miss the
+// constant cache).
+struct GrpLite {
+  int tile_begin, tiles_m, tiles_n;
+  int flags;  // bit 0: causal tiles only (tri); bits 8..15: kr_mode
+};
+constexpr int TBL_BYTES = 1024;
+static_assert(kMaxGroups * sizeof(GrpLite) <= TBL_BYTES, "group table does not fit");
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + BAR_BYTES + NUM_EPI_WARPS * EPI_WARP_BYTES +
+                           TBL_BYTES + 1024;  // + alignment slack
 
 // ---------------------------------------------------------------------------
 // PTX wrappers
@@ -218,7 +227,7 @@ struct TileCoord {
 };
 
 template <int ROWS, bool ATTN>
-__device__ __forceinline__ TileCoord decode_tile_rows(const TcGemmParams& p, int tile) {
+__device__ __forceinline__ TileCoord decode_tile_rows(const TcGemmParams& p, const GrpLite* L, int tile) {
   if (tile < p.interleave_tiles) {
     // Leading groups share the row tiling.  They are enumerated in super-rows
     // of GM row blocks; inside a super-row, column tile by column tile (across
@@ -229,13 +238,13 @@ __device__ __forceinline__ TileCoord decode_tile_rows(const TcGemmParams& p, int
     const int per_super = GM * p.interleave_nt;
     const int sr = tile / per_super;
     const int m_lo = sr * GM;
-    const int gm = min(GM, p.grp[0].tiles_m - m_lo);
+    const int gm = min(GM, L[0].tiles_m - m_lo);
     const int r = tile - sr * per_super;
     int nt = r / gm;
     const int mt = m_lo + (r - nt * gm);
     int g = 0;
-    while (nt >= p.grp[g].tiles_n) {
-      nt -= p.grp[g].tiles_n;
+    while (nt >= L[g].tiles_n) {
+      nt -= L[g].tiles_n;
       ++g;
     }
     TileCoord c;
@@ -245,35 +254,39 @@ __device__ __forceinline__ TileCoord decode_tile_rows(const TcGemmParams& p, int
     return c;
   }
   int g = p.interleave_groups;
-  while (g + 1 < p.num_groups && tile >= p.grp[g + 1].tile_begin) ++g;
-  const GemmGroup& G = p.grp[g];
+  const int ng = p.num_groups;
+  while (g + 1 < ng && tile >= L[g + 1].tile_begin) ++g;
+  const GrpLite G = L[g];
   const int local = tile - G.tile_begin;
   TileCoord c;
   c.g = g;
-  if (ATTN && G.tri) {
+  if (ATTN && (G.flags & 1)) {
     // causal: only the tiles with a column at or before their last row, row
     // block by row block (row block mt has min(tiles_n, (mt+1) ROWS / bn
     // rounded up) of them)
     int mt = 0, acc = 0;
     for (; mt < G.tiles_m - 1; ++mt) {
-      const int cnt = min(G.tiles_n, (mt * ROWS + ROWS - 1) / G.bn + 1);
+      const int cnt = min(G.tiles_n, (mt * ROWS + ROWS - 1) / BN + 1);
       if (local < acc + cnt) break;
       acc += cnt;
     }
     c.m0 = mt * ROWS;
-    c.n0 = (local - acc) * G.bn;
+    c.n0 = (local - acc) * BN;
     return c;
   }
   int mt = local % G.tiles_m;
-  if (ATTN && G.kr_mode == KR_END) mt = G.tiles_m - 1 - mt;  // longest contraction first
+  if (ATTN && ((G.flags >> 8) & 0xff) == KR_END) mt = G.tiles_m - 1 - mt;  // longest contraction first
   c.m0 = mt * ROWS;
-  c.n0 = (local / G.tiles_m) * G.bn;
+  c.n0 = (local / G.tiles_m) * BN;
   return c;
 }
 
-template <bool ATTN>
-__device__ __forceinline__ TileCoord decode_tile(const TcGemmParams& p, int tile) {
-  return decode_tile_rows<BM, ATTN>(p, tile);
+// Fills the shared group table (all threads of the CTA may take part).
+__device__ __forceinline__ void fill_group_table(const TcGemmParams& p, GrpLite* L, int tid, int nthreads) {
+  for (int i = tid; i < p.num_groups; i += nthreads) {
+    const GemmGroup& G = p.grp[i];
+    L[i] = GrpLite{G.tile_begin, G.tiles_m, G.tiles_n, (G.tri ? 1 : 0) | (G.kr_mode << 8)};
+  }
 }
 
 // k-block range [kb0, kb1) of a tile (ROWS rows from m0, columns from n0) of
@@ -796,7 +809,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
   constexpr int kBarCount = 2 * STAGES + 5 + 2 * TILE_RING;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kBarCount);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + kBarCount + 1);
+  // tile ring: (tile id or -1, group, m0, n0) per slot, decoded once by the producer
   volatile int* tile_ids = reinterpret_cast<volatile int*>(bars + kBarCount + 2);
+  static_assert((kBarCount + 2) * 8 + 16 * TILE_RING <= BAR_BYTES, "barrier area");
+  GrpLite* gtab = reinterpret_cast<GrpLite*>(smem + STAGES * STAGE_BYTES + BAR_BYTES +
+                                             NUM_EPI_WARPS * EPI_WARP_BYTES);
+  fill_group_table(p, gtab, threadIdx.x, NUM_THREADS);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -853,6 +871,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
     // Hot-loop values live in registers: reading the kernel parameters
     // through references re-loads them after every asm statement.
     const int total_tiles = p.total_tiles;
+    const bool claim_ahead = !p.has_dep;
     bool ok = true;
     int tile = blockIdx.x;
     for (int i = 0; ok; ++i) {
@@ -860,10 +879,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
       const int r = i % TILE_RING;
       if (!wait_bounded(tile_empty_bar(r), static_cast<uint32_t>((i / TILE_RING) & 1) ^ 1u, wctx)) break;
       const int t = tile < total_tiles ? tile : -1;
-      tile_ids[r] = t;
+      TileCoord tc{0, 0, 0};
+      if (t >= 0) tc = decode_tile_rows<BM, ATTN>(p, gtab, t);
+      tile_ids[4 * r] = t;
+      tile_ids[4 * r + 1] = tc.g;
+      tile_ids[4 * r + 2] = tc.m0;
+      tile_ids[4 * r + 3] = tc.n0;
       mbar_arrive(tile_full_bar(r));
       if (t < 0) break;
-      const TileCoord tc = decode_tile<ATTN>(p, t);
+      // Next tile: the first gridDim tiles are static, the rest claimed in
+      // order.  Without dependent tiles the claim is made now, so its atomic
+      // round trip overlaps this tile's loads; with them it waits until this
+      // tile's loads are issued (a held tile would sit behind a dependency wait).
+      int next = -1;
+      if (claim_ahead) next = static_cast<int>(gridDim.x) + atomicAdd(sched, 1);
       const GemmGroup& G = p.grp[tc.g];
       const int seg_begin = G.seg_begin, seg_end = G.seg_end;
       if (G.dep_kind != DEP_NONE) {
@@ -897,7 +926,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
                                                   tc.m0, tc.n0);
       }
       // next tile: the first gridDim tiles are static, the rest claimed in order
-      tile = static_cast<int>(gridDim.x) + atomicAdd(sched, 1);
+      tile = claim_ahead ? next : static_cast<int>(gridDim.x) + atomicAdd(sched, 1);
     }
     if (*abort_flag) {
       // Drain: wait (bounded) until every copy this thread issued has landed.
@@ -918,10 +947,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
     for (int lt = 0; ok; ++lt) {
       const int r = lt % TILE_RING;
       if (!wait_bounded(tile_full_bar(r), static_cast<uint32_t>((lt / TILE_RING) & 1), wctx)) break;
-      const int tile = tile_ids[r];
+      const int tile = tile_ids[4 * r];
+      const TileCoord tc{tile_ids[4 * r + 1], tile_ids[4 * r + 2], tile_ids[4 * r + 3]};
       mbar_arrive(tile_empty_bar(r));
       if (tile < 0) break;
-      const TileCoord tc = decode_tile<ATTN>(p, tile);
       const GemmGroup& G = p.grp[tc.g];
       const int buf = lt & 1;
       const uint32_t tphase = static_cast<uint32_t>(lt >> 1) & 1u;
@@ -983,11 +1012,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
     for (int lt = 0;; ++lt) {
       const int r = lt % TILE_RING;
       if (!wait_bounded(tile_full_bar(r), static_cast<uint32_t>((lt / TILE_RING) & 1), wctx)) break;
-      const int tile = tile_ids[r];
+      const int tile = tile_ids[4 * r];
+      const TileCoord tc{tile_ids[4 * r + 1], tile_ids[4 * r + 2], tile_ids[4 * r + 3]};
       __syncwarp();
       if (lane == 0) mbar_arrive(tile_empty_bar(r));
       if (tile < 0) break;
-      const TileCoord tc = decode_tile<ATTN>(p, tile);
       const GemmGroup& G = p.grp[tc.g];
       const int buf = lt & 1;
       const uint32_t tphase = static_cast<uint32_t>(lt >> 1) & 1u;
@@ -1081,7 +1110,7 @@ constexpr int STAGES2 = 6;
 constexpr int B_HALF_BYTES = 128 * BK * 2;          // 16 KB
 constexpr int STAGE2_BYTES = A_TILE_BYTES + B_HALF_BYTES;
 constexpr int SMEM2_BYTES =
-    STAGES2 * STAGE2_BYTES + BAR_BYTES + NUM_EPI_WARPS * EPI_WARP_BYTES + 1024;
+    STAGES2 * STAGE2_BYTES + BAR_BYTES + NUM_EPI_WARPS * EPI_WARP_BYTES + TBL_BYTES + 1024;
 static_assert(SMEM_BYTES <= 227 * 1024 && SMEM2_BYTES <= 227 * 1024,
               "dynamic shared memory above the 227 KB a CTA may use");
 
@@ -1271,7 +1300,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_pair_kernel(const __gr
   constexpr int kBarCount = 2 * STAGES2 + 5 + 2 * TILE_RING;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kBarCount);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + kBarCount + 1);
+  // tile ring: (tile id or -1, group, m0, n0) per slot, decoded once by the leader's producer
   volatile int* tile_ids = reinterpret_cast<volatile int*>(bars + kBarCount + 2);
+  static_assert((kBarCount + 2) * 8 + 16 * TILE_RING <= BAR_BYTES, "barrier area");
+  GrpLite* gtab = reinterpret_cast<GrpLite*>(smem + STAGES2 * STAGE2_BYTES + BAR_BYTES +
+                                             NUM_EPI_WARPS * EPI_WARP_BYTES);
+  fill_group_table(p, gtab, threadIdx.x, NUM_THREADS);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -1327,10 +1361,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_pair_kernel(const __gr
 
   // Every role reads the i-th tile id from its CTA's ring, then releases the
   // slot on the leader's tile_empty barrier.
-  auto take_tile = [&](int i, int& t) -> bool {
+  auto take_tile = [&](int i, int& t, TileCoord& tc) -> bool {
     const int r = i % TILE_RING;
     if (!wait2(tile_full_bar(r), static_cast<uint32_t>((i / TILE_RING) & 1), wctx)) return false;
-    t = tile_ids[r];
+    t = tile_ids[4 * r];
+    tc = TileCoord{tile_ids[4 * r + 1], tile_ids[4 * r + 2], tile_ids[4 * r + 3]};
     return true;
   };
   auto release_tile = [&](int i) {
@@ -1349,22 +1384,30 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_pair_kernel(const __gr
     const int total_tiles = p.total_tiles;
     bool ok = true;
     int claim = blockIdx.x >> 1;  // the cluster's first tile
+    const bool claim_ahead = !p.has_dep;
     for (int i = 0; ok; ++i) {
       int t;
+      TileCoord tc{0, 0, 0};
       if (leader) {
         const int r = i % TILE_RING;
         if (!wait2(tile_empty_bar(r), static_cast<uint32_t>((i / TILE_RING) & 1) ^ 1u, wctx)) break;
         t = claim < total_tiles ? claim : -1;
-        tile_ids[r] = t;
-        st_cluster_u32(map_to_rank(tile_ids_addr + 4u * r, peer), static_cast<uint32_t>(t));
+        if (t >= 0) tc = decode_tile_rows<BM2, ATTN>(p, gtab, t);
+        const int vals[4] = {t, tc.g, tc.m0, tc.n0};
+        for (int q = 0; q < 4; ++q) {
+          tile_ids[4 * r + q] = vals[q];
+          st_cluster_u32(map_to_rank(tile_ids_addr + 4u * (4 * r + q), peer), static_cast<uint32_t>(vals[q]));
+        }
         mbar_arrive(tile_full_bar(r));
         mbar_arrive_remote(map_to_rank(tile_full_bar(r), peer));
       } else {
-        if (!take_tile(i, t)) break;
+        if (!take_tile(i, t, tc)) break;
         release_tile(i);
       }
       if (t < 0) break;
-      const TileCoord tc = decode_tile_rows<BM2, ATTN>(p, t);
+      // the leader claims the cluster's next tile (ahead when nothing waits; see the one-SM kernel)
+      int next = -1;
+      if (leader && claim_ahead) next = static_cast<int>(gridDim.x >> 1) + atomicAdd(sched, 1);
       const GemmGroup& G = p.grp[tc.g];
       const int seg_begin = G.seg_begin, seg_end = G.seg_end;
       const int row0 = tc.m0 + 128 * static_cast<int>(rank);  // this CTA's rows
@@ -1395,7 +1438,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_pair_kernel(const __gr
         ok = produce_segment_pair(R, wctx, leader, S, reinterpret_cast<uint64_t>(&p.mapA[s]),
                                   reinterpret_cast<uint64_t>(&p.mapB[s]), kb0, kb1, row0, ncol0);
       }
-      if (leader) claim = static_cast<int>(gridDim.x >> 1) + atomicAdd(sched, 1);
+      if (leader) claim = claim_ahead ? next : static_cast<int>(gridDim.x >> 1) + atomicAdd(sched, 1);
     }
     if (*abort_flag) {
       // Drain: the leader waits (bounded) until every stage it expected has
@@ -1423,10 +1466,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_pair_kernel(const __gr
     bool issued_any = false;
     for (int lt = 0; ok; ++lt) {
       int tile;
-      if (!take_tile(lt, tile)) break;
+      TileCoord tc;
+      if (!take_tile(lt, tile, tc)) break;
       release_tile(lt);
       if (tile < 0) break;
-      const TileCoord tc = decode_tile_rows<BM2, ATTN>(p, tile);
       const GemmGroup& G = p.grp[tc.g];
       const int buf = lt & 1;
       const uint32_t tphase = static_cast<uint32_t>(lt >> 1) & 1u;
@@ -1485,11 +1528,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_pair_kernel(const __gr
     const uint32_t tempty_leader1 = map_to_rank(tempty_bar(1), 0);
     for (int lt = 0;; ++lt) {
       int tile;
-      if (!take_tile(lt, tile)) break;
+      TileCoord tc;
+      if (!take_tile(lt, tile, tc)) break;
       __syncwarp();
       if (lane == 0) release_tile(lt);
       if (tile < 0) break;
-      const TileCoord tc = decode_tile_rows<BM2, ATTN>(p, tile);
       const GemmGroup& G = p.grp[tc.g];
       const int buf = lt & 1;
       const uint32_t tphase = static_cast<uint32_t>(lt >> 1) & 1u;

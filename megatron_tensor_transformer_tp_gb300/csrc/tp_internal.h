@@ -119,6 +119,7 @@ struct TcGemmParams {
   int num_counters;
   int pair;              // 1: two-SM kernel (256-row pair tiles), 0: one-SM kernel
   int attn;              // 1: the kernels' attention instance (causal ranges, softmax epilogues)
+  int has_dep;           // 1: some tile waits on others (tile claims are not made ahead)
   unsigned* err;         // device error word
   unsigned long long wait_limit_ns;
 };
