@@ -269,46 +269,63 @@ def attention_head_columns(h, n_heads, N, j):
     return base + jl * d, base + h // N + jl * d, base + 2 * (h // N) + jl * d, j * d
 
 
-def attention_head(q, k, v, causal):
+def attention_head(q, k, v, causal, keep=None, p=0.0):
     """One head of one sequence: S = q k^T / sqrt(d), keys after the query
     masked to -inf when causal, P = softmax over keys with the row max
     subtracted ([Walkthrough] §_VocabParallelCrossEntropy's stable softmax),
-    out = P v.  The pages draw the single-head formula as a figure; the scaled
-    dot product with the 1/sqrt(d) factor is the plain reading, and the causal
-    mask is GPT's.  Returns (P (s, s), out (s, d))."""
+    out = P v; with attention dropout, out = (P * keep / (1 - p)) v.  The
+    pages draw the single-head formula as a figure; the scaled dot product
+    with the 1/sqrt(d) factor is the plain reading, and the causal mask is
+    GPT's.  Returns (P (s, s), out (s, d)), P before dropout."""
     s, d = q.shape
     S = (q @ k.T) / math.sqrt(d)
     if causal:
         S = np.where(np.tril(np.ones((s, s), dtype=bool)), S, -np.inf)
     E = np.exp(S - S.max(axis=1, keepdims=True))
     P = E / E.sum(axis=1, keepdims=True)
-    return P, P @ v
+    Pd = P if keep is None else P * keep / (1.0 - p)
+    return P, Pd @ v
 
 
-def attention_head_grad(q, k, v, P, g):
+def attention_head_grad(q, k, v, P, g, keep=None, p=0.0):
     """Gradient of ``attention_head`` given its P and the output gradient g
-    (the chain rule through out = P v, the softmax and S = q k^T / sqrt(d)):
-        dv = P^T g,  dP = g v^T,  dS = P * (dP - sum_keys(P * dP)) / sqrt(d),
-        dq = dS k,  dk = dS^T q.
+    (the chain rule through out = Pd v, the dropout, the softmax and
+    S = q k^T / sqrt(d)):
+        dv = Pd^T g,  dP = (g v^T) * keep / (1 - p),
+        dS = P * (dP - sum_keys(P * dP)) / sqrt(d),  dq = dS k,  dk = dS^T q.
     Masked entries have P = 0 and carry no gradient.  Returns (dq, dk, dv)."""
     d = q.shape[1]
+    Pd = P if keep is None else P * keep / (1.0 - p)
     dP = g @ v.T
+    if keep is not None:
+        dP = dP * keep / (1.0 - p)
     dS = P * (dP - np.sum(P * dP, axis=1, keepdims=True)) / math.sqrt(d)
-    return dS @ k, dS.T @ q, P.T @ g
+    return dS @ k, dS.T @ q, Pd.T @ g
 
 
-def attention_core(QKV, s, n_heads, N, causal):
+def attention_keep(bi, j, s, n_heads, N, p, seed, layer):
+    """Attention-dropout keep flags (s, s) of sequence bi, head j: elements
+    ((bi n_heads + j) s + query) s + key of the stream of head j's shard."""
+    if p <= 0.0:
+        return None
+    shard = j // (n_heads // N)
+    e0 = ((bi * n_heads + j) * s) * s
+    return dropout_keep(seed, dropout_stream(layer, 0, shard), e0, s * s, p).reshape(s, s)
+
+
+def attention_core(QKV, s, n_heads, N, causal, p_attn=0.0, seed=0, layer=0):
     """Per-head attention between the QKV projection and the output
     projection for b = T / s sequences of s tokens: every (sequence, head)
     pair runs ``attention_head`` on its columns of the shard-major QKV and
     writes head j's output to context columns [j d, (j+1) d).  Heads are
     independent ([TP notes] §Self-Attention层; [Walkthrough]
-    §ParallelSelfAttention: every rank computes its own heads).
-    Returns (C (T, h), P (b, n_heads, s, s)).
+    §ParallelSelfAttention: every rank computes its own heads, and its
+    attention dropout draws from its own stream).
+    Returns (C (T, h), P (b, n_heads, s, s)), P before dropout.
     Pinned by: torch scaled_dot_product_attention in float64 per head, torch
     multi_head_attention_forward through the sharded projections, a closed
-    form (q = 0: the running or full mean of v) and brute force on a tiny
-    case."""
+    form (q = 0: the running or full mean of v), brute force on a tiny case,
+    and torch autograd of a whole layer with dropout."""
     T, h3 = QKV.shape
     h = h3 // 3
     d = h // n_heads
@@ -319,17 +336,19 @@ def attention_core(QKV, s, n_heads, N, causal):
         rows = slice(bi * s, (bi + 1) * s)
         for j in range(n_heads):
             qc, kc, vc, cc = attention_head_columns(h, n_heads, N, j)
+            keep = attention_keep(bi, j, s, n_heads, N, p_attn, seed, layer)
             P[bi, j], C[rows, cc:cc + d] = attention_head(
-                QKV[rows, qc:qc + d], QKV[rows, kc:kc + d], QKV[rows, vc:vc + d], causal)
+                QKV[rows, qc:qc + d], QKV[rows, kc:kc + d], QKV[rows, vc:vc + d], causal,
+                keep=keep, p=p_attn)
     return C, P
 
 
-def attention_core_grad(QKV, P, dC, s, n_heads, N):
+def attention_core_grad(QKV, P, dC, s, n_heads, N, p_attn=0.0, seed=0, layer=0):
     """Gradient of ``attention_core`` with respect to QKV, given its
     probabilities P and the context gradient dC: ``attention_head_grad`` per
     (sequence, head), written back in the QKV layout.
     Pinned by: torch autograd through scaled_dot_product_attention in
-    float64, and through multi_head_attention_forward."""
+    float64, through multi_head_attention_forward, and through a whole layer."""
     T, h3 = QKV.shape
     h = h3 // 3
     d = h // n_heads
@@ -339,8 +358,10 @@ def attention_core_grad(QKV, P, dC, s, n_heads, N):
         rows = slice(bi * s, (bi + 1) * s)
         for j in range(n_heads):
             qc, kc, vc, cc = attention_head_columns(h, n_heads, N, j)
+            keep = attention_keep(bi, j, s, n_heads, N, p_attn, seed, layer)
             dq, dk, dv = attention_head_grad(QKV[rows, qc:qc + d], QKV[rows, kc:kc + d],
-                                             QKV[rows, vc:vc + d], P[bi, j], dC[rows, cc:cc + d])
+                                             QKV[rows, vc:vc + d], P[bi, j], dC[rows, cc:cc + d],
+                                             keep=keep, p=p_attn)
             dQKV[rows, qc:qc + d], dQKV[rows, kc:kc + d], dQKV[rows, vc:vc + d] = dq, dk, dv
     return dQKV
 
@@ -641,6 +662,175 @@ def mixed_precision_adam_step(groups, state, cfg):
         p, m, v = adam_update(grp["param"], g, grp["m"], grp["v"], step, cfg, grp["weight_decay"])
         out.append(dict(grp, param=p, m=m, v=v))
     return True, grad_norm, out, new_state
+
+
+# --------------------------------------------------------------------------
+# Transformer layer: counter-based dropout, LayerNorm, residuals
+# --------------------------------------------------------------------------
+# Philox4x64-10 (Salmon, Moraes, Dror and Shaw, "Parallel random numbers: as
+# easy as 1, 2, 3", SC 2011): ten rounds of two 64 x 64 -> 128-bit products
+# with a Weyl-sequence key schedule.  The pages fix only where the random
+# streams differ (dropout inside the tensor-parallel region draws per shard,
+# outside it all shards draw the same numbers: [Walkthrough] §模型并行, the
+# dropout figure); the generator and the mask layout below are this build's.
+_PH_M0, _PH_M1 = 0xD2E7470EE14C6C93, 0xCA5A826395121157
+_PH_W0, _PH_W1 = 0x9E3779B97F4A7C15, 0xBB67AE8584CAA73B
+_U32 = np.uint64(0xFFFFFFFF)
+
+
+def _mulhilo64(a, b):
+    """Full 128-bit product of uint64 arrays as (hi, lo), from 32-bit halves."""
+    a = np.asarray(a, dtype=np.uint64)
+    b = np.asarray(b, dtype=np.uint64)
+    s32 = np.uint64(32)
+    al, ah = a & _U32, a >> s32
+    bl, bh = b & _U32, b >> s32
+    ll, lh, hl, hh = al * bl, al * bh, ah * bl, ah * bh
+    mid = (ll >> s32) + (lh & _U32) + (hl & _U32)
+    hi = hh + (lh >> s32) + (hl >> s32) + (mid >> s32)
+    return hi, a * b
+
+
+def philox4x64(c0, k0, k1, c1=0, c2=0, c3=0):
+    """Philox4x64-10 of counters (c0, c1, c2, c3) under key (k0, k1); c0 may
+    be an array.  Returns the four uint64 output words.
+    Pinned by: numpy.random.Philox (the same generator; its first block is
+    counter 1)."""
+    with np.errstate(over="ignore"):
+        x0 = np.asarray(c0, dtype=np.uint64)
+        x1 = np.full_like(x0, np.uint64(c1))
+        x2 = np.full_like(x0, np.uint64(c2))
+        x3 = np.full_like(x0, np.uint64(c3))
+        key0, key1 = np.uint64(k0), np.uint64(k1)
+        for _ in range(10):
+            hi0, lo0 = _mulhilo64(np.uint64(_PH_M0), x0)
+            hi1, lo1 = _mulhilo64(np.uint64(_PH_M1), x2)
+            x0, x1, x2, x3 = hi1 ^ x1 ^ key0, lo1, hi0 ^ x3 ^ key1, lo0
+            key0 = key0 + np.uint64(_PH_W0)
+            key1 = key1 + np.uint64(_PH_W1)
+    return x0, x1, x2, x3
+
+
+def dropout_keep(seed, stream, e0, n, p):
+    """Keep flags of elements e0 .. e0+n-1 of one dropout site: element e
+    takes the 16-bit field 16 (e mod 4) of output word (e mod 16) / 4 of
+    Philox4x64-10 at counter (e / 16, 0, 0, 0) under key (seed, stream), and is
+    kept iff that field is >= floor(p 2^16) (keep probability 1 - floor(p 2^16)
+    / 2^16).  Pinned by: numpy.random.Philox and the keep rate."""
+    e = np.arange(e0, e0 + n, dtype=np.uint64)
+    blocks = e // np.uint64(16)
+    words = philox4x64(blocks, seed, stream)
+    W = np.stack(words, axis=0)  # (4, n)
+    w = ((e % np.uint64(16)) // np.uint64(4)).astype(np.int64)
+    shift = np.uint64(16) * (e % np.uint64(4))
+    field = (W[w, np.arange(n)] >> shift) & np.uint64(0xFFFF)
+    return field >= np.uint64(int(math.floor(p * 65536.0)))
+
+
+def dropout_stream(layer, kind, shard=0):
+    """Stream id of a dropout site: kind 0 = attention probabilities (one
+    stream per shard: inside the tensor-parallel region), 1 = attention
+    output, 2 = MLP output (one stream shared by all shards: after the
+    shard sum).  Layers are 256 streams apart."""
+    return layer * 256 + kind * 64 + (shard if kind == 0 else 0)
+
+
+def layernorm(x, g, b, eps):
+    """LayerNorm over the last axis with biased variance, fp64 (the fp32
+    gain and bias of [Study notes]' mixed-precision notes):
+        y = (x - mean) / sqrt(var + eps) * g + b.
+    Returns (y, mean, rstd).  Pinned by: torch layer_norm in float64."""
+    x = np.asarray(x, dtype=np.float64)
+    mean = x.mean(axis=-1)
+    var = ((x - mean[..., None]) ** 2).mean(axis=-1)
+    rstd = 1.0 / np.sqrt(var + eps)
+    return (x - mean[..., None]) * rstd[..., None] * g + b, mean, rstd
+
+
+def layernorm_grad(dy, x, g, mean, rstd):
+    """Gradient of ``layernorm``: with xhat = (x - mean) rstd and n features,
+        dxhat = dy g,  dx = rstd (dxhat - mean(dxhat) - xhat mean(dxhat xhat)),
+        dg = sum over rows of dy xhat,  db = sum over rows of dy.
+    Pinned by: torch autograd through layer_norm in float64."""
+    xhat = (np.asarray(x, dtype=np.float64) - mean[..., None]) * rstd[..., None]
+    dxhat = dy * g
+    dx = rstd[..., None] * (dxhat - dxhat.mean(axis=-1, keepdims=True) -
+                            xhat * (dxhat * xhat).mean(axis=-1, keepdims=True))
+    return dx, (dy * xhat).sum(axis=0), dy.sum(axis=0)
+
+
+def dropout_residual(res, x, keep, p):
+    """out = res + x * keep / (1 - p): the dropout after a row-parallel
+    linear and the residual add of [Walkthrough] §ParallelTransformerLayer."""
+    return res + x * keep / (1.0 - p)
+
+
+def transformer_layer_fwd(x, P, cfg):
+    """One tensor-parallel transformer layer ([Walkthrough]
+    §ParallelTransformerLayer = attention + MLP, with the dropout after each
+    row-parallel linear defined in the layer; LayerNorm before each block, as
+    in Megatron's GPT):
+        ln1 = LN(x; g1, b1)
+        QKV = [ln1 Wqkv_i^T + bqkv_i]_i            (column-parallel, per shard)
+        C   = attention core of QKV (attention dropout per shard stream)
+        O   = sum_i C_i Wo_i^T + bo                 (row-parallel + shard sum)
+        h1  = x + dropout(O)                        (one stream for all shards)
+        ln2 = LN(h1; g2, b2)
+        Z, Y, M = MLP(ln2)                          (column -> GELU -> row)
+        out = h1 + dropout(M)
+    P: g1, b1, Wqkv, bqkv, Wo, bo, g2, b2, W, a, U, b (lists for shards).
+    cfg: s, n_heads, N, causal, eps, p_attn, p_hidden, seed, layer.
+    Returns (out, saved) with every intermediate the backward needs.
+    Pinned by: torch autograd of the same layer in float64."""
+    T, h = x.shape
+    ln1, m1, r1 = layernorm(x, P["g1"], P["b1"], cfg["eps"])
+    QKV, _ = attn_proj_fwd(ln1, P["Wqkv"], P["bqkv"], np.zeros((T, h)), P["Wo"], None)
+    C, Pr = attention_core(QKV, cfg["s"], cfg["n_heads"], cfg["N"], cfg["causal"],
+                           cfg["p_attn"], cfg["seed"], cfg["layer"])
+    _, O = attn_proj_fwd(ln1, P["Wqkv"], P["bqkv"], C, P["Wo"], P["bo"])
+    keep1 = dropout_keep(cfg["seed"], dropout_stream(cfg["layer"], 1), 0, T * h,
+                         cfg["p_hidden"]).reshape(T, h)
+    h1 = dropout_residual(x, O, keep1, cfg["p_hidden"])
+    ln2, m2, r2 = layernorm(h1, P["g2"], P["b2"], cfg["eps"])
+    Z, Y, M = mlp_fwd(ln2, P["W"], P["a"], P["U"], P["b"])
+    keep2 = dropout_keep(cfg["seed"], dropout_stream(cfg["layer"], 2), 0, T * h,
+                         cfg["p_hidden"]).reshape(T, h)
+    out = dropout_residual(h1, M, keep2, cfg["p_hidden"])
+    saved = dict(x=x, ln1=ln1, m1=m1, r1=r1, QKV=QKV, C=C, P=Pr, O=O, keep1=keep1, h1=h1,
+                 ln2=ln2, m2=m2, r2=r2, Z=Z, Y=Y, M=M, keep2=keep2)
+    return out, saved
+
+
+def transformer_layer_bwd(dout, saved, P, cfg):
+    """Backward of ``transformer_layer_fwd`` by the chain rule through its
+    steps in reverse: the residual passes dout to h1 unchanged, the dropout
+    scales by keep / (1 - p), then MLP, LayerNorm 2, attention output
+    projection, attention core, QKV projection, LayerNorm 1.
+    Returns dx and the parameter gradients (same keys as P, prefixed d)."""
+    p = cfg["p_hidden"]
+    dM = dout * saved["keep2"] / (1.0 - p)
+    g = mlp_bwd(dM, saved["ln2"], P["W"], P["a"], P["U"])
+    dln2 = g["dX"]
+    dh1_ln, dg2, db2 = layernorm_grad(dln2, saved["h1"], P["g2"], saved["m2"], saved["r2"])
+    dh1 = dout + dh1_ln
+    dO = dh1 * saved["keep1"] / (1.0 - p)
+    T, h = dO.shape
+    zero_qkv = np.zeros_like(saved["QKV"])
+    dC = attn_proj_bwd(zero_qkv, dO, saved["ln1"], saved["C"], P["Wqkv"], P["Wo"])["dC"]
+    dQKV = attention_core_grad(saved["QKV"], saved["P"], dC, cfg["s"], cfg["n_heads"], cfg["N"],
+                               cfg["p_attn"], cfg["seed"], cfg["layer"])
+    ga = attn_proj_bwd(dQKV, dO, saved["ln1"], saved["C"], P["Wqkv"], P["Wo"])
+    dx_ln, dg1, db1 = layernorm_grad(ga["dX"], saved["x"], P["g1"], saved["m1"], saved["r1"])
+    return dict(dx=dh1 + dx_ln, dg1=dg1, db1=db1, dWqkv=ga["dWqkv"], dbqkv=ga["dbqkv"],
+                dWo=ga["dWo"], dbo=ga["dbo"], dg2=dg2, db2=db2, dW=g["dW"], da=g["da"],
+                dU=g["dU"], db=g["db"], dQKV=dQKV, dC=dC, dO=dO)
+
+
+def embed_position_dropout(words, pos_table, positions, keep, p):
+    """Input of the first layer ([Walkthrough] §Embedding.forward): word
+    embeddings (the vocab-parallel lookup, summed over ranges) plus position
+    embeddings, then dropout: (words + pos_table[positions]) * keep / (1 - p)."""
+    return (np.asarray(words, dtype=np.float64) + pos_table[np.asarray(positions)]) * keep / (1.0 - p)
 
 
 # --------------------------------------------------------------------------

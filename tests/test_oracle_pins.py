@@ -403,14 +403,14 @@ def test_attention_head_brute_force():
 def test_planted_missing_attention_scale_is_caught(monkeypatch):
     real = O.attention_head
 
-    def broken(q, k, v, causal):
-        return real(q * math.sqrt(q.shape[1]), k, v, causal)  # the 1/sqrt(d) undone
+    def broken(q, k, v, causal, **kw):
+        return real(q * math.sqrt(q.shape[1]), k, v, causal, **kw)  # the 1/sqrt(d) undone
     monkeypatch.setattr(O, "attention_head", broken)
     assert check_core_sdpa(O, True) > 1e-3
 
 
 def test_planted_causal_mask_off_by_one_is_caught(monkeypatch):
-    def broken(q, k, v, causal):
+    def broken(q, k, v, causal, **kw):
         s, d = q.shape
         S = (q @ k.T) / math.sqrt(d)
         if causal:  # the diagonal masked as well (a finite fill keeps row 0 defined)
@@ -423,7 +423,7 @@ def test_planted_causal_mask_off_by_one_is_caught(monkeypatch):
 
 
 def test_planted_softmax_over_queries_is_caught(monkeypatch):
-    def broken(q, k, v, causal):
+    def broken(q, k, v, causal, **kw):
         s, d = q.shape
         S = (q @ k.T) / math.sqrt(d)
         if causal:
@@ -436,7 +436,7 @@ def test_planted_softmax_over_queries_is_caught(monkeypatch):
 
 
 def test_planted_missing_softmax_correction_in_grad_is_caught(monkeypatch):
-    def broken(q, k, v, P, g):
+    def broken(q, k, v, P, g, **kw):
         dS = P * (g @ v.T) / math.sqrt(q.shape[1])  # the row-sum term dropped
         return dS @ k, dS.T @ q, P.T @ g
     monkeypatch.setattr(O, "attention_head_grad", broken)
@@ -895,3 +895,191 @@ def test_planted_per_group_clip_is_caught(monkeypatch):
         return outs, real(grads, max_norm)[1]
     monkeypatch.setattr(O, "clip_by_global_norm", broken)
     assert check_clip(O) > 1e-3
+
+
+# ----------------------------------------------------------------------------
+# Transformer layer: Philox dropout, LayerNorm, the whole layer
+# ----------------------------------------------------------------------------
+@pytest.mark.parametrize("key", [(0, 0), (1, 2), (2**64 - 1, 12345), (0xDEADBEEF, 2**63)])
+def test_philox_matches_numpy(key):
+    c = np.arange(1, 9, dtype=np.uint64)
+    words = O.philox4x64(c, key[0], key[1])
+    bg = np.random.Philox(key=np.array(key, dtype=np.uint64), counter=np.zeros(4, dtype=np.uint64))
+    raw = bg.random_raw(4 * len(c))  # numpy's first block is counter 1
+    for i in range(len(c)):
+        for j in range(4):
+            assert int(words[j][i]) == int(raw[4 * i + j])
+
+
+def test_philox_high_counter_words_match_numpy():
+    # counters with the upper words set: numpy's counter is 256-bit, ours (c0, c1, c2, c3)
+    bg = np.random.Philox(key=np.array([7, 9], dtype=np.uint64),
+                          counter=np.array([2**64 - 1, 5, 0, 0], dtype=np.uint64))
+    raw = bg.random_raw(4)  # counter + 1 = (0, 6, 0, 0)
+    words = O.philox4x64(np.array([0], dtype=np.uint64), 7, 9, c1=6)
+    assert [int(w[0]) for w in words] == [int(r) for r in raw]
+
+
+def test_dropout_keep_rate_and_streams():
+    n, p = 200000, 0.1
+    k = O.dropout_keep(11, 3, 0, n, p)
+    keep = 1 - math.floor(p * 65536) / 65536
+    assert abs(k.mean() - keep) < 5 * math.sqrt(keep * (1 - keep) / n)
+    assert not np.array_equal(k, O.dropout_keep(11, 4, 0, n, p))      # another stream
+    assert np.array_equal(k[1000:2000], O.dropout_keep(11, 3, 1000, 1000, p))  # offsets
+    assert O.dropout_keep(11, 3, 0, 1000, 0.0).all()
+    # the attention streams differ per shard, the hidden ones do not
+    assert O.dropout_stream(2, 0, 0) != O.dropout_stream(2, 0, 1)
+    assert O.dropout_stream(2, 1, 0) == O.dropout_stream(2, 1, 1)
+
+
+def check_layernorm(mod):
+    g = rng(21)
+    x = g.standard_normal((7, 12)) * 3 + 1
+    gam, bet = g.standard_normal(12), g.standard_normal(12)
+    dy = g.standard_normal((7, 12))
+    y, mean, rstd = mod.layernorm(x, gam, bet, 1e-5)
+    tx = torch.tensor(x, requires_grad=True)
+    tg, tb = torch.tensor(gam, requires_grad=True), torch.tensor(bet, requires_grad=True)
+    ty = F.layer_norm(tx, (12,), tg, tb, 1e-5)
+    ty.backward(torch.tensor(dy))
+    dx, dg, db = mod.layernorm_grad(dy, x, gam, mean, rstd)
+    return max(np.abs(y - ty.detach().numpy()).max(), np.abs(dx - tx.grad.numpy()).max(),
+               np.abs(dg - tg.grad.numpy()).max(), np.abs(db - tb.grad.numpy()).max())
+
+
+def test_layernorm_matches_torch():
+    assert check_layernorm(O) < 1e-12
+
+
+def tiny_layer(seed=31, s=6, b=2, h=16, H=4, N=2, hp=32, p_attn=0.2, p_hidden=0.25):
+    g = rng(seed)
+    T = b * s
+    d = h // N
+    Wqkv = g.standard_normal((3 * h, h)) * 0.3
+    Wo = g.standard_normal((h, h)) * 0.3
+    W = g.standard_normal((hp, h)) * 0.3
+    U = g.standard_normal((h, hp)) * 0.3
+    P = dict(g1=1 + 0.1 * g.standard_normal(h), b1=0.1 * g.standard_normal(h),
+             bqkv_full=0.1 * g.standard_normal(3 * h), bo=0.1 * g.standard_normal(h),
+             g2=1 + 0.1 * g.standard_normal(h), b2=0.1 * g.standard_normal(h),
+             a_full=0.1 * g.standard_normal(hp), b=0.1 * g.standard_normal(h),
+             Wqkv_full=Wqkv, Wo_full=Wo, W_full=W, U_full=U)
+    P["Wqkv"] = [np.concatenate([Wqkv[j * h + i * d: j * h + (i + 1) * d] for j in range(3)]) for i in range(N)]
+    P["bqkv"] = [np.concatenate([P["bqkv_full"][j * h + i * d: j * h + (i + 1) * d] for j in range(3)])
+                 for i in range(N)]
+    P["Wo"] = [Wo[:, i * d:(i + 1) * d] for i in range(N)]
+    n = hp // N
+    P["W"] = [W[i * n:(i + 1) * n] for i in range(N)]
+    P["a"] = [P["a_full"][i * n:(i + 1) * n] for i in range(N)]
+    P["U"] = [U[:, i * n:(i + 1) * n] for i in range(N)]
+    cfg = dict(s=s, n_heads=H, N=N, causal=True, eps=1e-5, p_attn=p_attn, p_hidden=p_hidden,
+               seed=77, layer=3)
+    x = g.standard_normal((T, h))
+    dout = g.standard_normal((T, h))
+    return x, dout, P, cfg
+
+
+def torch_layer(x, P, cfg, mod):
+    """The same layer written with torch ops on the unsharded weights."""
+    s, H, N = cfg["s"], cfg["n_heads"], cfg["N"]
+    T, h = x.shape
+    d = h // H
+    b = T // s
+    t = {k: torch.tensor(v, requires_grad=True) for k, v in P.items() if not isinstance(v, list)}
+    tx = torch.tensor(x, requires_grad=True)
+    ln1 = F.layer_norm(tx, (h,), t["g1"], t["b1"], cfg["eps"])
+    qkv = F.linear(ln1, t["Wqkv_full"], t["bqkv_full"])
+    q, k, v = qkv[:, :h], qkv[:, h:2 * h], qkv[:, 2 * h:]
+    ctx = []
+    for bi in range(b):
+        heads = []
+        for j in range(H):
+            r, c = slice(bi * s, (bi + 1) * s), slice(j * d, (j + 1) * d)
+            S = q[r, c] @ k[r, c].T / math.sqrt(d)
+            S = S.masked_fill(torch.triu(torch.ones(s, s, dtype=torch.bool), 1), float("-inf"))
+            Pj = torch.softmax(S, dim=1)
+            keep = mod.attention_keep(bi, j, s, H, N, cfg["p_attn"], cfg["seed"], cfg["layer"])
+            Pj = Pj * torch.tensor(keep) / (1 - cfg["p_attn"])
+            heads.append(Pj @ v[r, c])
+        ctx.append(torch.cat(heads, dim=1))
+    C = torch.cat(ctx, dim=0)
+    p = cfg["p_hidden"]
+    k1 = torch.tensor(mod.dropout_keep(cfg["seed"], mod.dropout_stream(cfg["layer"], 1), 0, T * h, p).reshape(T, h))
+    k2 = torch.tensor(mod.dropout_keep(cfg["seed"], mod.dropout_stream(cfg["layer"], 2), 0, T * h, p).reshape(T, h))
+    h1 = tx + F.linear(C, t["Wo_full"], t["bo"]) * k1 / (1 - p)
+    ln2 = F.layer_norm(h1, (h,), t["g2"], t["b2"], cfg["eps"])
+    M = F.linear(F.gelu(F.linear(ln2, t["W_full"], t["a_full"])), t["U_full"], t["b"])
+    return tx, t, h1 + M * k2 / (1 - p)
+
+
+def check_layer(mod):
+    x, dout, P, cfg = tiny_layer()
+    out, saved = mod.transformer_layer_fwd(x, P, cfg)
+    grads = mod.transformer_layer_bwd(dout, saved, P, cfg)
+    tx, t, tout = torch_layer(x, P, cfg, mod)
+    tout.backward(torch.tensor(dout))
+    h = x.shape[1]
+    N = cfg["N"]
+    d = h // N
+    err = np.abs(out - tout.detach().numpy()).max()
+    err = max(err, np.abs(grads["dx"] - tx.grad.numpy()).max())
+    for k in ("g1", "b1", "bo", "g2", "b2", "b"):
+        err = max(err, np.abs(grads["d" + k] - t[k].grad.numpy()).max())
+    gW, gU, gWqkv, gWo = t["W_full"].grad.numpy(), t["U_full"].grad.numpy(), t["Wqkv_full"].grad.numpy(), t["Wo_full"].grad.numpy()
+    n = gW.shape[0] // N
+    for i in range(N):
+        err = max(err, np.abs(grads["dW"][i] - gW[i * n:(i + 1) * n]).max(),
+                  np.abs(grads["dU"][i] - gU[:, i * n:(i + 1) * n]).max(),
+                  np.abs(grads["da"][i] - t["a_full"].grad.numpy()[i * n:(i + 1) * n]).max(),
+                  np.abs(grads["dWo"][i] - gWo[:, i * d:(i + 1) * d]).max())
+        ref_qkv = np.concatenate([gWqkv[j * h + i * d: j * h + (i + 1) * d] for j in range(3)])
+        ref_b = np.concatenate([t["bqkv_full"].grad.numpy()[j * h + i * d: j * h + (i + 1) * d] for j in range(3)])
+        err = max(err, np.abs(grads["dWqkv"][i] - ref_qkv).max(), np.abs(grads["dbqkv"][i] - ref_b).max())
+    return err
+
+
+def test_transformer_layer_matches_torch_autograd():
+    assert check_layer(O) < 1e-10
+
+
+def test_planted_unbiased_layernorm_variance_is_caught(monkeypatch):
+    def broken(x, g, b, eps):
+        x = np.asarray(x, dtype=np.float64)
+        mean = x.mean(axis=-1)
+        var = x.var(axis=-1, ddof=1)
+        rstd = 1.0 / np.sqrt(var + eps)
+        return (x - mean[..., None]) * rstd[..., None] * g + b, mean, rstd
+    monkeypatch.setattr(O, "layernorm", broken)
+    assert check_layernorm(O) > 1e-3
+
+
+def test_planted_unscaled_dropout_is_caught(monkeypatch):
+    monkeypatch.setattr(O, "dropout_residual", lambda res, x, keep, p: res + x * keep)
+    assert check_layer(O) > 1e-3
+
+
+def test_planted_dropped_residual_gradient_is_caught(monkeypatch):
+    real = O.layernorm_grad
+    calls = []
+
+    def broken(dy, x, g, mean, rstd):
+        dx, dg, db = real(dy, x, g, mean, rstd)
+        calls.append(1)
+        return (dx - dy * 0.5 if len(calls) == 1 else dx), dg, db  # a wrong term in LN2's dx
+    monkeypatch.setattr(O, "layernorm_grad", broken)
+    assert check_layer(O) > 1e-3
+
+
+def test_planted_shared_attention_dropout_stream_is_caught(monkeypatch):
+    # every shard drawing from shard 0's stream is a plausible mistake: the
+    # stream layout makes the shards' masks differ, which this detects
+    real = O.dropout_stream
+    monkeypatch.setattr(O, "dropout_stream", lambda layer, kind, shard=0: real(layer, kind, 0))
+    x, dout, P, cfg = tiny_layer()
+    k0 = O.attention_keep(0, 0, cfg["s"], cfg["n_heads"], cfg["N"], 0.5, 1, 0)
+    k_other_shard = O.attention_keep(0, cfg["n_heads"] - 1, cfg["s"], cfg["n_heads"], cfg["N"], 0.5, 1, 0)
+    monkeypatch.undo()
+    r0 = O.attention_keep(0, 0, cfg["s"], cfg["n_heads"], cfg["N"], 0.5, 1, 0)
+    r1 = O.attention_keep(0, cfg["n_heads"] - 1, cfg["s"], cfg["n_heads"], cfg["N"], 0.5, 1, 0)
+    assert np.array_equal(k0, r0) and not np.array_equal(k_other_shard, r1)
