@@ -213,6 +213,141 @@ TP_API tp_status tp_attn_core_bwd(tp_dtype dt, int64_t T, int64_t s, int64_t h, 
 /* Workspace bytes of tp_attn_core_fwd and _bwd (0 for invalid sizes or T = 0). */
 TP_API size_t tp_attn_core_workspace_size(int64_t T, int64_t s, int64_t h, int n_heads);
 
+/*
+ * tp_attn_core_dropout_fwd / _bwd -- the attention core with attention
+ * dropout on the probabilities (rate p_attn, 0 <= p_attn < 1), the dropout
+ * that sits inside the tensor-parallel region and therefore draws from one
+ * random stream per shard ([Walkthrough] §模型并行, the dropout figure:
+ * different seeds inside the parallel region, the same seed after the shard
+ * sum; §ParallelSelfAttention: attention dropout through the model-parallel
+ * RNG tracker).
+ *   C = (P * keep / (1 - p_attn)) V per head; P is stored before dropout, and
+ *   Pd (same layout as P, bf16) receives P * keep / (1 - p_attn).
+ * keep: element ((sequence * n_heads + head) * s + query) * s + key of the
+ * stream stream0 + shard(head) under key seed, drawn from Philox4x64-10
+ * (Salmon et al., SC 2011): the 16-bit field 16 (e mod 4) of output word
+ * (e mod 16) / 4 at counter (e / 16, 0, 0, 0), kept iff it is >=
+ * floor(p_attn * 65536) computed from the fp32 p_attn.  The backward draws the
+ * same bits again.  p_attn > 0 needs s % 16 == 0 (TP_ERR_INVALID otherwise)
+ * and a non-NULL Pd.  Other arguments as tp_attn_core_fwd / _bwd; the
+ * backward's dV is Pd^T dC and its dP is (dC V^T) * keep / (1 - p_attn).
+ */
+TP_API tp_status tp_attn_core_dropout_fwd(tp_dtype dt, int64_t T, int64_t s, int64_t h, int n_heads,
+                                          int N, int causal, float p_attn, uint64_t seed,
+                                          uint64_t stream0, const void* QKV, void* P, void* Pd, void* C,
+                                          float* lse, void* workspace, size_t ws_bytes, void* stream);
+TP_API tp_status tp_attn_core_dropout_bwd(tp_dtype dt, int64_t T, int64_t s, int64_t h, int n_heads,
+                                          int N, int causal, float p_attn, uint64_t seed,
+                                          uint64_t stream0, const void* QKV, const void* P,
+                                          const void* Pd, const void* C, const void* dC, void* dQKV,
+                                          void* workspace, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* One tensor-parallel transformer layer                                     */
+/* ------------------------------------------------------------------------ */
+
+/* Sizes and rates of a layer (host struct). */
+typedef struct {
+  int64_t T, s, h, hp; /* tokens (b sequences of s), hidden size, FFN width */
+  int32_t n_heads, N;  /* heads, shards (heads % N == 0, hp % N == 0, 1 <= N <= 8) */
+  int32_t causal;      /* GPT causal attention mask */
+  float eps;           /* LayerNorm epsilon */
+  float p_attn;        /* attention-probability dropout rate */
+  float p_hidden;      /* dropout rate after each row-parallel linear */
+  uint64_t seed;       /* dropout key */
+  uint64_t layer;      /* layer index: the layer's streams are 256 * layer + {0..63 attention
+                          (one per shard), 64 attention output, 128 MLP output} */
+} tp_layer_config;
+
+/* Weights (host struct of device pointers; shard arrays are host arrays of N
+ * device pointers as elsewhere).  LayerNorm parameters fp32, the rest bf16. */
+typedef struct {
+  const float* g1;
+  const float* b1;          /* LayerNorm 1 (h) */
+  const void* const* Wqkv;  /* (3h/N, h) per shard, rows [Q_i; K_i; V_i] */
+  const void* const* bqkv;  /* (3h/N) per shard or NULL */
+  const void* const* Wo;    /* (h, h/N) per shard */
+  const void* bo;           /* (h) or NULL */
+  const float* g2;
+  const float* b2;          /* LayerNorm 2 (h) */
+  const void* const* W;     /* MLP column-parallel (hp/N, h) per shard */
+  const void* const* a;     /* (hp/N) per shard or NULL */
+  const void* const* U;     /* MLP row-parallel (h, hp/N) per shard */
+  const void* b;            /* (h) or NULL */
+} tp_layer_params;
+
+/* Activations the forward writes and the backward reads (caller-owned device
+ * buffers, bf16 unless marked). */
+typedef struct {
+  void* ln1;    /* (T, h) LayerNorm 1 output */
+  float* mean1;
+  float* rstd1; /* (T) fp32 */
+  void* QKV;    /* (T, 3h) shard-major */
+  void* P;      /* (b, n_heads, s, s) probabilities before dropout */
+  void* Pd;     /* same shape after dropout; may be NULL when p_attn == 0 */
+  void* C;      /* (T, h) attention context */
+  void* h1;     /* (T, h) residual stream after the attention block */
+  void* ln2;    /* (T, h) LayerNorm 2 output */
+  float* mean2;
+  float* rstd2; /* (T) fp32 */
+  void* Z;
+  void* Y;      /* (T, hp) MLP pre-activation and activation */
+} tp_layer_saved;
+
+/* Parameter gradients (fp32 device buffers; shard arrays as the weights). */
+typedef struct {
+  float* dg1;
+  float* db1;
+  void* const* dWqkv;
+  void* const* dbqkv; /* or NULL */
+  void* const* dWo;
+  float* dbo;         /* or NULL */
+  float* dg2;
+  float* db2;
+  void* const* dW;
+  void* const* da;    /* or NULL */
+  void* const* dU;
+  float* db;          /* or NULL */
+} tp_layer_grads;
+
+/*
+ * tp_transformer_layer_fwd -- [Walkthrough] §ParallelTransformerLayer
+ * (attention + MLP, with the dropout after each row-parallel linear defined in
+ * the layer), LayerNorm before each block as in GPT:
+ *   ln1 = LN(x; g1, b1);  QKV_i = ln1 Wqkv_i^T + bqkv_i;  C = attention core
+ *   (causal, attention dropout per shard);  O = sum_i C_i Wo_i^T + bo;
+ *   h1 = x + dropout(O);  ln2 = LN(h1; g2, b2);  Z, Y, M = MLP(ln2);
+ *   out = h1 + dropout(M).
+ * LayerNorm: biased variance, fp32 statistics and parameters, bf16 output.
+ * x, out (T, h) bf16; saved as above.  Needs h % 16 == 0, h <= 8192, and the
+ * constraints of the attention core and MLP entry points.
+ * tp_transformer_layer_bwd -- the gradient: dx (T, h) bf16 and the parameter
+ * gradients (accumulate: add into them).  Both draw the dropout bits from the
+ * config's streams; the backward draws them again.
+ */
+/*
+ * tp_position_embed_dropout -- the first layer's input ([Walkthrough]
+ * §Embedding.forward: word embeddings plus position embeddings, then the
+ * embedding dropout):  out = (words + pos_table[positions]) * keep / (1 - p).
+ *   words (T, h) bf16 (the vocab-parallel lookup), pos_table (max_pos, h)
+ *   bf16, positions (T) int64 (a position outside [0, max_pos) adds a zero
+ *   row), out (T, h) bf16.
+ *   keep: element row * h + col of stream stream_id under key seed, drawn as
+ *   for tp_attn_core_dropout_fwd.  h % 16 == 0; 16-byte aligned rows.
+ */
+TP_API tp_status tp_position_embed_dropout(int64_t T, int64_t h, int64_t max_pos, const void* words,
+                                           const void* pos_table, const int64_t* positions, float p,
+                                           uint64_t seed, uint64_t stream_id, void* out, void* stream);
+
+TP_API size_t tp_transformer_layer_workspace_size(const tp_layer_config* cfg);
+TP_API tp_status tp_transformer_layer_fwd(const tp_layer_config* cfg, const tp_layer_params* w,
+                                          const void* x, void* out, const tp_layer_saved* sv,
+                                          void* workspace, size_t ws_bytes, void* stream);
+TP_API tp_status tp_transformer_layer_bwd(const tp_layer_config* cfg, const tp_layer_params* w,
+                                          const void* x, const tp_layer_saved* sv, const void* dout,
+                                          void* dx, const tp_layer_grads* g, int accumulate,
+                                          void* workspace, size_t ws_bytes, void* stream);
+
 /* ------------------------------------------------------------------------ */
 /* Vocab-parallel word embedding and tied output layer                       */
 /* ------------------------------------------------------------------------ */

@@ -28,6 +28,9 @@ __all__ = [
     "tp_gelu_eval", "logits_pitch", "tp_adam_step", "tp_adam_step_workspace_size",
     "tp_optimizer_state", "tp_adam_config", "tp_param_group", "make_optimizer_state",
     "read_optimizer_state", "tp_attn_core_fwd", "tp_attn_core_bwd", "tp_attn_core_workspace_size",
+    "tp_attn_core_dropout_fwd", "tp_attn_core_dropout_bwd", "tp_position_embed_dropout",
+    "tp_transformer_layer_workspace_size", "tp_transformer_layer_fwd", "tp_transformer_layer_bwd",
+    "tp_layer_config", "layer_stream",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libtp.so")
@@ -61,6 +64,28 @@ class tp_param_group(ctypes.Structure):
                 ("exp_avg", ctypes.c_void_p), ("exp_avg_sq", ctypes.c_void_p),
                 ("model_param", ctypes.c_void_p), ("n", ctypes.c_int64),
                 ("weight_decay", ctypes.c_double)]
+
+
+class tp_layer_config(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int64), ("s", ctypes.c_int64), ("h", ctypes.c_int64),
+                ("hp", ctypes.c_int64), ("n_heads", ctypes.c_int32), ("N", ctypes.c_int32),
+                ("causal", ctypes.c_int32), ("eps", ctypes.c_float), ("p_attn", ctypes.c_float),
+                ("p_hidden", ctypes.c_float), ("seed", ctypes.c_uint64), ("layer", ctypes.c_uint64)]
+
+
+class tp_layer_params(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in ("g1", "b1", "Wqkv", "bqkv", "Wo", "bo", "g2", "b2",
+                                                "W", "a", "U", "b")]
+
+
+class tp_layer_saved(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in ("ln1", "mean1", "rstd1", "QKV", "P", "Pd", "C", "h1",
+                                                "ln2", "mean2", "rstd2", "Z", "Y")]
+
+
+class tp_layer_grads(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in ("dg1", "db1", "dWqkv", "dbqkv", "dWo", "dbo", "dg2",
+                                                "db2", "dW", "da", "dU", "db")]
 
 
 _SIGNATURES = {
@@ -109,6 +134,24 @@ _SIGNATURES = {
     "tp_attn_core_bwd": (_int, [_int, _i64, _i64, _i64, _int, _int, _int, _c_void_p, _c_void_p,
                                 _c_void_p, _c_void_p, _c_void_p, _c_void_p, _size_t, _c_void_p]),
     "tp_attn_core_workspace_size": (_size_t, [_i64, _i64, _i64, _int]),
+    "tp_attn_core_dropout_fwd": (_int, [_int, _i64, _i64, _i64, _int, _int, _int, ctypes.c_float,
+                                        ctypes.c_uint64, ctypes.c_uint64, _c_void_p, _c_void_p,
+                                        _c_void_p, _c_void_p, _c_void_p, _c_void_p, _size_t, _c_void_p]),
+    "tp_attn_core_dropout_bwd": (_int, [_int, _i64, _i64, _i64, _int, _int, _int, ctypes.c_float,
+                                        ctypes.c_uint64, ctypes.c_uint64, _c_void_p, _c_void_p,
+                                        _c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p, _size_t,
+                                        _c_void_p]),
+    "tp_position_embed_dropout": (_int, [_i64, _i64, _i64, _c_void_p, _c_void_p, _c_void_p,
+                                         ctypes.c_float, ctypes.c_uint64, ctypes.c_uint64, _c_void_p,
+                                         _c_void_p]),
+    "tp_transformer_layer_workspace_size": (_size_t, [ctypes.POINTER(tp_layer_config)]),
+    "tp_transformer_layer_fwd": (_int, [ctypes.POINTER(tp_layer_config), ctypes.POINTER(tp_layer_params),
+                                        _c_void_p, _c_void_p, ctypes.POINTER(tp_layer_saved), _c_void_p,
+                                        _size_t, _c_void_p]),
+    "tp_transformer_layer_bwd": (_int, [ctypes.POINTER(tp_layer_config), ctypes.POINTER(tp_layer_params),
+                                        _c_void_p, ctypes.POINTER(tp_layer_saved), _c_void_p, _c_void_p,
+                                        ctypes.POINTER(tp_layer_grads), _int, _c_void_p, _size_t,
+                                        _c_void_p]),
 }
 
 _LIB: Optional[ctypes.CDLL] = None
@@ -406,6 +449,95 @@ def tp_attn_core_bwd(QKV, P, C, dC, s, n_heads, N, causal, dQKV, workspace=None,
                                   _dev(dQKV, "dQKV"), _dev(workspace, "workspace"),
                                   _ws_bytes(workspace), _stream(stream)),
            "tp_attn_core_bwd")
+
+
+def layer_stream(layer: int, kind: int, shard: int = 0) -> int:
+    """Dropout stream of a layer's site (the library's numbering): kind 0 =
+    attention probabilities (per shard), 1 = attention output, 2 = MLP output."""
+    return layer * 256 + kind * 64 + (shard if kind == 0 else 0)
+
+
+def tp_attn_core_dropout_fwd(QKV, s, n_heads, N, causal, p_attn, seed, stream0, P, Pd, C, lse=None,
+                             workspace=None, stream=None):
+    T, h3 = QKV.shape
+    _check(lib().tp_attn_core_dropout_fwd(_dtype(QKV), T, s, h3 // 3, n_heads, N, int(bool(causal)),
+                                          float(p_attn), int(seed), int(stream0), _dev(QKV, "QKV"),
+                                          _dev(P, "P"), _dev(Pd, "Pd"), _dev(C, "C"), _dev(lse, "lse"),
+                                          _dev(workspace, "workspace"), _ws_bytes(workspace),
+                                          _stream(stream)),
+           "tp_attn_core_dropout_fwd")
+
+
+def tp_attn_core_dropout_bwd(QKV, P, Pd, C, dC, s, n_heads, N, causal, p_attn, seed, stream0, dQKV,
+                             workspace=None, stream=None):
+    T, h3 = QKV.shape
+    _check(lib().tp_attn_core_dropout_bwd(_dtype(QKV), T, s, h3 // 3, n_heads, N, int(bool(causal)),
+                                          float(p_attn), int(seed), int(stream0), _dev(QKV, "QKV"),
+                                          _dev(P, "P"), _dev(Pd, "Pd"), _dev(C, "C"), _dev(dC, "dC"),
+                                          _dev(dQKV, "dQKV"), _dev(workspace, "workspace"),
+                                          _ws_bytes(workspace), _stream(stream)),
+           "tp_attn_core_dropout_bwd")
+
+
+def tp_position_embed_dropout(words, pos_table, positions, p, seed, stream_id, out, stream=None):
+    T, h = words.shape
+    if positions.dtype != torch.int64:
+        raise TypeError("positions must be int64")
+    _check(lib().tp_position_embed_dropout(T, h, pos_table.shape[0], _dev(words, "words"),
+                                           _dev(pos_table, "pos_table"), _dev(positions, "positions"),
+                                           float(p), int(seed), int(stream_id), _dev(out, "out"),
+                                           _stream(stream)),
+           "tp_position_embed_dropout")
+
+
+def _layer_cfg(cfg: dict) -> tp_layer_config:
+    return tp_layer_config(cfg["T"], cfg["s"], cfg["h"], cfg["hp"], cfg["n_heads"], cfg["N"],
+                           int(bool(cfg["causal"])), cfg["eps"], cfg["p_attn"], cfg["p_hidden"],
+                           cfg["seed"], cfg["layer"])
+
+
+def tp_transformer_layer_workspace_size(cfg: dict) -> int:
+    c = _layer_cfg(cfg)
+    return int(lib().tp_transformer_layer_workspace_size(ctypes.byref(c)))
+
+
+def _ptr_or_shards(v, name, keep):
+    if v is None:
+        return None
+    if isinstance(v, (list, tuple)):
+        arr = _ptrs(v, name)
+        keep.append(arr)
+        return ctypes.cast(arr[0], ctypes.c_void_p).value
+    return _dev(v, name)
+
+
+def _struct(cls, d, keep):
+    return cls(*[_ptr_or_shards(d.get(n), n, keep) for n, _ in cls._fields_])
+
+
+def tp_transformer_layer_fwd(cfg, params, x, out, saved, workspace, stream=None):
+    """params / saved: dicts keyed by the C structs' field names (tensors, or
+    lists of shard tensors for the shard arrays)."""
+    keep = []
+    c = _layer_cfg(cfg)
+    w, sv = _struct(tp_layer_params, params, keep), _struct(tp_layer_saved, saved, keep)
+    _check(lib().tp_transformer_layer_fwd(ctypes.byref(c), ctypes.byref(w), _dev(x, "x"), _dev(out, "out"),
+                                          ctypes.byref(sv), _dev(workspace, "workspace"),
+                                          _ws_bytes(workspace), _stream(stream)),
+           "tp_transformer_layer_fwd")
+
+
+def tp_transformer_layer_bwd(cfg, params, x, saved, dout, dx, grads, workspace, accumulate=False,
+                             stream=None):
+    keep = []
+    c = _layer_cfg(cfg)
+    w, sv = _struct(tp_layer_params, params, keep), _struct(tp_layer_saved, saved, keep)
+    g = _struct(tp_layer_grads, grads, keep)
+    _check(lib().tp_transformer_layer_bwd(ctypes.byref(c), ctypes.byref(w), _dev(x, "x"), ctypes.byref(sv),
+                                          _dev(dout, "dout"), _dev(dx, "dx"), ctypes.byref(g),
+                                          int(bool(accumulate)), _dev(workspace, "workspace"),
+                                          _ws_bytes(workspace), _stream(stream)),
+           "tp_transformer_layer_bwd")
 
 
 def tp_adam_step_workspace_size() -> int:

@@ -18,7 +18,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libtp.so")
-SOURCES = ["tp_api.cu", "tp_gemm_tc.cu", "tp_gemm_simt.cu", "tp_embed.cu", "tp_noalloc.cu", "tp_opt.cu", "tp_attn.cu"]
+SOURCES = ["tp_api.cu", "tp_gemm_tc.cu", "tp_gemm_simt.cu", "tp_embed.cu", "tp_noalloc.cu", "tp_opt.cu", "tp_attn.cu", "tp_layer.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

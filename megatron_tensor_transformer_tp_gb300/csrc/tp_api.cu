@@ -827,12 +827,20 @@ tp_status attn_args(tp_dtype dt, int64_t T, int64_t s, int64_t h, int n_heads, i
   return TP_OK;
 }
 
+// Attention-dropout keep words: 32 keys per uint32, per (pair, query row).
+size_t attn_keep_bytes(const AttnDims& a, int64_t s) {
+  return round256(static_cast<size_t>(a.pairs * s * ((s + 31) / 32)) * 4);
+}
 size_t attn_fwd_ws(const AttnDims& a, int64_t s) {
-  return round256(static_cast<size_t>(a.pairs * a.P * s) * 8) + round256(static_cast<size_t>(a.pairs * s) * 4);
+  return round256(static_cast<size_t>(a.pairs * a.P * s) * 8) + round256(static_cast<size_t>(a.pairs * s) * 4) +
+         attn_keep_bytes(a, s);
 }
 size_t attn_bwd_ws(const AttnDims& a, int64_t s) {
-  return round256(static_cast<size_t>(a.pairs * s) * 4) + round256(static_cast<size_t>(a.pairs * s * s) * 2);
+  return round256(static_cast<size_t>(a.pairs * s) * 4) + round256(static_cast<size_t>(a.pairs * s * s) * 2) +
+         attn_keep_bytes(a, s);
 }
+
+bool drop_ok(float p, int64_t s) { return p >= 0.f && p < 1.f && (p == 0.f || s % 16 == 0); }
 
 // (sequence, head) pairs per GEMM launch: within the engine's group and
 // counter limits (groups_per_pair outputs and counters_per_pair counters each).
@@ -850,14 +858,17 @@ extern "C" size_t tp_attn_core_workspace_size(int64_t T, int64_t s, int64_t h, i
   return std::max(attn_fwd_ws(a, s), attn_bwd_ws(a, s));
 }
 
-extern "C" tp_status tp_attn_core_fwd(tp_dtype dt, int64_t T, int64_t s, int64_t h, int n_heads, int N,
-                                      int causal, const void* QKV, void* P, void* C, float* lse,
-                                      void* workspace, size_t ws_bytes, void* stream) {
+namespace {
+tp_status attn_core_fwd_impl(tp_dtype dt, int64_t T, int64_t s, int64_t h, int n_heads, int N, int causal,
+                             float p_drop, uint64_t seed, uint64_t stream0, const void* QKV, void* P,
+                             void* Pd, void* C, float* lse, void* workspace, size_t ws_bytes,
+                             void* stream) {
   AttnDims a;
   tp_status st = attn_args(dt, T, s, h, n_heads, N, &a);
   if (st != TP_OK) return st;
+  if (!drop_ok(p_drop, s)) return TP_ERR_INVALID;
   if (T == 0) return TP_OK;
-  if (!QKV || !P || !C) return TP_ERR_INVALID;
+  if (!QKV || !P || !C || (p_drop > 0.f && !Pd)) return TP_ERR_INVALID;
   if (workspace == nullptr || ws_bytes < attn_fwd_ws(a, s)) return TP_ERR_WORKSPACE;
   if (!al256(workspace)) return TP_ERR_ALIGN;
   cudaStream_t strm = static_cast<cudaStream_t>(stream);
@@ -865,6 +876,9 @@ extern "C" tp_status tp_attn_core_fwd(tp_dtype dt, int64_t T, int64_t s, int64_t
   float* row_lse = lse ? lse
                        : reinterpret_cast<float*>(bb(workspace) +
                                                   round256(static_cast<size_t>(a.pairs * a.P * s) * 8));
+  uint32_t* keep = reinterpret_cast<uint32_t*>(bb(workspace) + round256(static_cast<size_t>(a.pairs * a.P * s) * 8) +
+                                               round256(static_cast<size_t>(a.pairs * s) * 4));
+  const int wpr = static_cast<int>((s + 31) / 32);
   const float alpha = static_cast<float>(1.0 / sqrt(static_cast<double>(a.d)));
   const int kr_s = causal ? KR_TRI : KR_NONE;
   // 1. per row and 64-key part: (max, sum exp) of alpha q k^T, no scores stored
@@ -891,6 +905,12 @@ extern "C" tp_status tp_attn_core_fwd(tp_dtype dt, int64_t T, int64_t s, int64_t
     return launch_attn_lse(parts, static_cast<int>(a.P), s, a.pairs * s, causal != 0, row_lse, strm);
   });
   if (e != cudaSuccess) return TP_ERR_CUDA;
+  if (p_drop > 0.f) {
+    e = timed("attn_keep", strm, [&] {
+      return launch_attn_keep(a.pairs, s, n_heads, n_heads / N, seed, stream0, p_drop, keep, strm);
+    });
+    if (e != cudaSuccess) return TP_ERR_CUDA;
+  }
   // 3. P = exp(alpha q k^T - lse) (scores recomputed, stored in bf16), and in
   //    the same launch C_j = P V_j, a row block once its P rows are stored
   const int64_t rows_per_pair = (s + 255) / 256 * 2;  // 128-row blocks, pair tiles rounded up
@@ -911,11 +931,17 @@ extern "C" tp_status tp_attn_core_fwd(tp_dtype dt, int64_t T, int64_t s, int64_t
       gr.kr_mode = kr_s;
       gr.row_lse = row_lse + g * s;
       gr.prod_row = rows[g - g0];
+      if (p_drop > 0.f) {
+        gr.out2 = bb(Pd) + static_cast<size_t>(g * s * s) * 2;
+        gr.drop_mask = keep + g * s * wpr;
+        gr.drop_wpr = wpr;
+        gr.drop_scale = 1.f / (1.f - p_drop);
+      }
     }
     for (int64_t g = g0; g < g1; ++g) {
       const int64_t bi = g / n_heads;
       const HeadPtrs hp = head_ptrs(QKV, bi, s, h, n_heads, N, static_cast<int>(g % n_heads));
-      const void* Pg = bb(P) + static_cast<size_t>(g * s * s) * 2;
+      const void* Pg = bb(p_drop > 0.f ? Pd : P) + static_cast<size_t>(g * s * s) * 2;
       const int si = p.add_seg(kmajor(Pg, s, s, s), mnmajor(hp.v, s, a.d, 3 * h), s);
       GemmGroup& gr = p.add_group(s, a.d, si, si + 1, EPI_STORE, OUT_BF16,
                                   bb(C) + (static_cast<size_t>(bi * s) * h + hp.cc) * 2, h);
@@ -929,26 +955,35 @@ extern "C" tp_status tp_attn_core_fwd(tp_dtype dt, int64_t T, int64_t s, int64_t
   return TP_OK;
 }
 
-extern "C" tp_status tp_attn_core_bwd(tp_dtype dt, int64_t T, int64_t s, int64_t h, int n_heads, int N,
-                                      int causal, const void* QKV, const void* P, const void* C,
-                                      const void* dC, void* dQKV, void* workspace, size_t ws_bytes,
-                                      void* stream) {
+tp_status attn_core_bwd_impl(tp_dtype dt, int64_t T, int64_t s, int64_t h, int n_heads, int N, int causal,
+                             float p_drop, uint64_t seed, uint64_t stream0, const void* QKV, const void* P,
+                             const void* Pd, const void* C, const void* dC, void* dQKV, void* workspace,
+                             size_t ws_bytes, void* stream) {
   AttnDims a;
   tp_status st = attn_args(dt, T, s, h, n_heads, N, &a);
   if (st != TP_OK) return st;
+  if (!drop_ok(p_drop, s)) return TP_ERR_INVALID;
   if (T == 0) return TP_OK;
-  if (!QKV || !P || !C || !dC || !dQKV) return TP_ERR_INVALID;
+  if (!QKV || !P || !C || !dC || !dQKV || (p_drop > 0.f && !Pd)) return TP_ERR_INVALID;
   if (workspace == nullptr || ws_bytes < attn_bwd_ws(a, s)) return TP_ERR_WORKSPACE;
   if (!al256(workspace)) return TP_ERR_ALIGN;
   cudaStream_t strm = static_cast<cudaStream_t>(stream);
   float* D = static_cast<float*>(workspace);
   uint8_t* dS = bb(workspace) + round256(static_cast<size_t>(a.pairs * s) * 4);
+  uint32_t* keep = reinterpret_cast<uint32_t*>(dS + round256(static_cast<size_t>(a.pairs * s * s) * 2));
+  const int wpr = static_cast<int>((s + 31) / 32);
   const float alpha = static_cast<float>(1.0 / sqrt(static_cast<double>(a.d)));
   // 1. D = rowsum(dC * C) per head and token (= sum over keys of P dP)
   cudaError_t e = timed("attn_rowdot", strm, [&] {
     return launch_attn_rowdot(C, dC, h, s, n_heads, static_cast<int>(a.d), a.pairs, D, strm);
   });
   if (e != cudaSuccess) return TP_ERR_CUDA;
+  if (p_drop > 0.f) {  // the forward's keep bits, drawn again
+    e = timed("attn_keep", strm, [&] {
+      return launch_attn_keep(a.pairs, s, n_heads, n_heads / N, seed, stream0, p_drop, keep, strm);
+    });
+    if (e != cudaSuccess) return TP_ERR_CUDA;
+  }
   // 2. per pair: dS = P (dC V^T - D) alpha and dV = P^T dC; then dQ = dS K per
   //    row block of dS, dK = dS^T Q per column block of dS
   const int64_t rows_per_pair = (s + 255) / 256 * 2;
@@ -980,10 +1015,15 @@ extern "C" tp_status tp_attn_core_bwd(tp_dtype dt, int64_t T, int64_t s, int64_t
       gr.tri_ok = 1;  // dQ and dK read only the causal tiles of dS
       gr.prod_row = rows[g - g0];
       gr.prod_col = cols[g - g0];
+      if (p_drop > 0.f) {
+        gr.drop_mask = keep + g * s * wpr;
+        gr.drop_wpr = wpr;
+        gr.drop_scale = 1.f / (1.f - p_drop);
+      }
     }
     for (int64_t g = g0; g < g1; ++g) {
       const HeadPtrs hp = head_ptrs(QKV, g / n_heads, s, h, n_heads, N, static_cast<int>(g % n_heads));
-      const void* Pg = cb(P) + static_cast<size_t>(g * s * s) * 2;
+      const void* Pg = cb(p_drop > 0.f ? Pd : P) + static_cast<size_t>(g * s * s) * 2;
       const int si = p.add_seg(mnmajor(Pg, s, s, s), mnmajor(dC_of(g, hp), s, a.d, h), s);
       GemmGroup& gr = p.add_group(s, a.d, si, si + 1, EPI_STORE, OUT_BF16, dqkv_of(g, hp.vc), 3 * h);
       gr.kr_mode = causal ? KR_BEGIN : KR_NONE;
@@ -1008,6 +1048,39 @@ extern "C" tp_status tp_attn_core_bwd(tp_dtype dt, int64_t T, int64_t s, int64_t
     if (st != TP_OK) return st;
   }
   return TP_OK;
+}
+}  // namespace
+
+extern "C" tp_status tp_attn_core_fwd(tp_dtype dt, int64_t T, int64_t s, int64_t h, int n_heads, int N,
+                                      int causal, const void* QKV, void* P, void* C, float* lse,
+                                      void* workspace, size_t ws_bytes, void* stream) {
+  return attn_core_fwd_impl(dt, T, s, h, n_heads, N, causal, 0.f, 0, 0, QKV, P, nullptr, C, lse, workspace,
+                            ws_bytes, stream);
+}
+
+extern "C" tp_status tp_attn_core_bwd(tp_dtype dt, int64_t T, int64_t s, int64_t h, int n_heads, int N,
+                                      int causal, const void* QKV, const void* P, const void* C,
+                                      const void* dC, void* dQKV, void* workspace, size_t ws_bytes,
+                                      void* stream) {
+  return attn_core_bwd_impl(dt, T, s, h, n_heads, N, causal, 0.f, 0, 0, QKV, P, nullptr, C, dC, dQKV,
+                            workspace, ws_bytes, stream);
+}
+
+extern "C" tp_status tp_attn_core_dropout_fwd(tp_dtype dt, int64_t T, int64_t s, int64_t h, int n_heads,
+                                              int N, int causal, float p_attn, uint64_t seed,
+                                              uint64_t stream0, const void* QKV, void* P, void* Pd, void* C,
+                                              float* lse, void* workspace, size_t ws_bytes, void* stream) {
+  return attn_core_fwd_impl(dt, T, s, h, n_heads, N, causal, p_attn, seed, stream0, QKV, P, Pd, C, lse,
+                            workspace, ws_bytes, stream);
+}
+
+extern "C" tp_status tp_attn_core_dropout_bwd(tp_dtype dt, int64_t T, int64_t s, int64_t h, int n_heads,
+                                              int N, int causal, float p_attn, uint64_t seed,
+                                              uint64_t stream0, const void* QKV, const void* P,
+                                              const void* Pd, const void* C, const void* dC, void* dQKV,
+                                              void* workspace, size_t ws_bytes, void* stream) {
+  return attn_core_bwd_impl(dt, T, s, h, n_heads, N, causal, p_attn, seed, stream0, QKV, P, Pd, C, dC, dQKV,
+                            workspace, ws_bytes, stream);
 }
 
 // ===========================================================================
@@ -1232,6 +1305,251 @@ extern "C" tp_status tied_embed_grad(tp_dtype dt, int64_t T, int64_t h, int64_t 
     g.seg_row0 = range_starts[r];
   }
   return run_plan(p, dt, "gemm_tied_grad_segsum", s);
+}
+
+// ===========================================================================
+// Transformer layer
+// ===========================================================================
+namespace {
+
+// Workspace carve-up of the layer (each piece 256-byte aligned).
+struct LayerWs {
+  uint8_t* base;
+  size_t off;
+  template <class T>
+  T* take(size_t bytes) {
+    T* p = reinterpret_cast<T*>(base + off);
+    off += round256(bytes);
+    return p;
+  }
+};
+
+size_t layer_ws_bytes(const tp_layer_config& c) {
+  const size_t th = static_cast<size_t>(c.T * c.h) * 2;
+  size_t b = 0;
+  b += 8 * round256(th);                                          // O, M, dM, dln2, dh1, dO, dC, dln1
+  b += round256(static_cast<size_t>(c.T * c.hp) * 2);             // dZ
+  b += round256(static_cast<size_t>(c.T * 3 * c.h) * 2);          // dQKV
+  b += round256(static_cast<size_t>(ln_bwd_blocks(c.T)) * 2 * c.h * 4);  // LayerNorm partials
+  b += tp_attn_core_workspace_size(c.T, c.s, c.h, c.n_heads);     // core
+  return b;
+}
+
+tp_status layer_check(const tp_layer_config* c, const tp_layer_params* w) {
+  if (!c || !w) return TP_ERR_INVALID;
+  if (c->T < 0 || c->s <= 0 || c->h <= 0 || c->hp <= 0 || c->N < 1 || c->N > 8 || c->n_heads < 1 ||
+      c->n_heads % c->N != 0 || c->h % c->n_heads != 0 || c->hp % c->N != 0 || c->T % c->s != 0)
+    return TP_ERR_INVALID;
+  if (c->h % 16 != 0 || c->h > 8192) return TP_ERR_INVALID;
+  if (!(c->p_hidden >= 0.f && c->p_hidden < 1.f) || !drop_ok(c->p_attn, c->s) || !(c->eps > 0.f))
+    return TP_ERR_INVALID;
+  if (!w->g1 || !w->b1 || !w->g2 || !w->b2 || !shards_ok(w->Wqkv, c->N) || !shards_ok(w->Wo, c->N) ||
+      !shards_ok(w->W, c->N) || !shards_ok(w->U, c->N) || !opt_shards_ok(w->bqkv, c->N) ||
+      !opt_shards_ok(w->a, c->N))
+    return TP_ERR_INVALID;
+  return TP_OK;
+}
+
+// QKV_i = X Wqkv_i^T + bqkv_i and, separately, O = sum_i C_i Wo_i^T + bo.
+tp_status qkv_proj(int64_t M, int64_t h, int N, const void* X, const void* const* Wqkv,
+                   const void* const* bqkv, void* QKV, cudaStream_t s) {
+  const int64_t d = h / N;
+  Plan p;
+  for (int i = 0; i < N; ++i) {
+    const int si = p.add_seg(kmajor(X, M, h, h), kmajor(Wqkv[i], 3 * d, h, h), h);
+    GemmGroup& g = p.add_group(M, 3 * d, si, si + 1, EPI_STORE, OUT_BF16, bb(QKV) + i * 3 * d * 2, 3 * h);
+    g.bias = bqkv ? bqkv[i] : nullptr;
+  }
+  return run_plan(p, TP_BF16, "gemm_layer_qkv", s);
+}
+tp_status out_proj(int64_t M, int64_t h, int N, const void* C, const void* const* Wo, const void* bo,
+                   void* O, cudaStream_t s) {
+  const int64_t d = h / N;
+  Plan p;
+  for (int i = 0; i < N; ++i) p.add_seg(kmajor(cb(C) + i * d * 2, M, d, h), kmajor(Wo[i], h, d, d), d);
+  GemmGroup& go = p.add_group(M, h, 0, N, EPI_STORE, OUT_BF16, O, h);
+  go.bias = bo;
+  return run_plan(p, TP_BF16, "gemm_layer_oproj", s);
+}
+// dC_i = dO Wo_i, dWo_i = dO^T C_i, dbo = colsum(dO).
+tp_status out_proj_bwd(int64_t M, int64_t h, int N, const void* dO, const void* C, const void* const* Wo,
+                       void* dC, void* const* dWo, void* dbo, int accumulate, cudaStream_t s) {
+  const int64_t d = h / N;
+  Plan p;
+  for (int i = 0; i < N; ++i) {
+    const int si = p.add_seg(kmajor(dO, M, h, h), mnmajor(Wo[i], h, d, d), h);
+    p.add_group(M, d, si, si + 1, EPI_STORE, OUT_BF16, bb(dC) + i * d * 2, h);
+  }
+  for (int i = 0; i < N; ++i) {
+    const int si = p.add_seg(mnmajor(dO, M, h, h), mnmajor(cb(C) + i * d * 2, M, d, h), M);
+    GemmGroup& g = p.add_group(h, d, si, si + 1, EPI_F32, OUT_F32, dWo[i], d);
+    g.accumulate = accumulate;
+  }
+  if (dbo) p.add_colsum(dO, M, h, h, dbo, accumulate);
+  return run_plan(p, TP_BF16, "gemm_layer_oproj_bwd", s);
+}
+// dX = sum_i dQKV_i Wqkv_i, dWqkv_i = dQKV_i^T X, dbqkv_i = colsum(dQKV_i).
+tp_status qkv_proj_bwd(int64_t M, int64_t h, int N, const void* dQKV, const void* X,
+                       const void* const* Wqkv, void* dX, void* const* dWqkv, void* const* dbqkv,
+                       int accumulate, cudaStream_t s) {
+  const int64_t w = 3 * (h / N);
+  Plan p;
+  for (int i = 0; i < N; ++i) p.add_seg(kmajor(cb(dQKV) + i * w * 2, M, w, 3 * h), mnmajor(Wqkv[i], w, h, h), w);
+  p.add_group(M, h, 0, N, EPI_STORE, OUT_BF16, dX, h);
+  for (int i = 0; i < N; ++i) {
+    const int si = p.add_seg(mnmajor(cb(dQKV) + i * w * 2, M, w, 3 * h), mnmajor(X, M, h, h), M);
+    GemmGroup& g = p.add_group(w, h, si, si + 1, EPI_F32, OUT_F32, dWqkv[i], h);
+    g.accumulate = accumulate;
+  }
+  if (dbqkv)
+    for (int i = 0; i < N; ++i) p.add_colsum(cb(dQKV) + i * w * 2, M, w, 3 * h, dbqkv[i], accumulate);
+  return run_plan(p, TP_BF16, "gemm_layer_qkv_bwd", s);
+}
+
+uint64_t layer_stream(uint64_t layer, int kind) { return layer * 256 + static_cast<uint64_t>(kind) * 64; }
+
+}  // namespace
+
+extern "C" tp_status tp_position_embed_dropout(int64_t T, int64_t h, int64_t max_pos, const void* words,
+                                               const void* pos_table, const int64_t* positions, float p,
+                                               uint64_t seed, uint64_t stream_id, void* out, void* stream) {
+  if (T < 0 || h <= 0 || max_pos <= 0 || h % 16 != 0 || !(p >= 0.f && p < 1.f)) return TP_ERR_INVALID;
+  if (T == 0) return TP_OK;
+  if (!words || !pos_table || !positions || !out) return TP_ERR_INVALID;
+  if (!al16(words) || !al16(pos_table) || !al16(out)) return TP_ERR_ALIGN;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const cudaError_t e = timed("pos_embed_dropout", s, [&] {
+    return launch_pos_embed_dropout(words, pos_table, positions, T, h, max_pos, seed, stream_id, p, out, s);
+  });
+  return e == cudaSuccess ? TP_OK : TP_ERR_CUDA;
+}
+
+extern "C" size_t tp_transformer_layer_workspace_size(const tp_layer_config* cfg) {
+  if (!cfg || cfg->T <= 0 || cfg->s <= 0 || cfg->T % cfg->s != 0 || cfg->n_heads < 1 || cfg->h <= 0 ||
+      cfg->hp <= 0)
+    return 0;
+  return layer_ws_bytes(*cfg);
+}
+
+extern "C" tp_status tp_transformer_layer_fwd(const tp_layer_config* cfg, const tp_layer_params* w,
+                                              const void* x, void* out, const tp_layer_saved* sv,
+                                              void* workspace, size_t ws_bytes, void* stream) {
+  tp_status st = layer_check(cfg, w);
+  if (st != TP_OK) return st;
+  const tp_layer_config& c = *cfg;
+  if (c.T == 0) return TP_OK;
+  if (!x || !out || !sv || !sv->ln1 || !sv->mean1 || !sv->rstd1 || !sv->QKV || !sv->P || !sv->C ||
+      !sv->h1 || !sv->ln2 || !sv->mean2 || !sv->rstd2 || !sv->Z || !sv->Y || (c.p_attn > 0.f && !sv->Pd))
+    return TP_ERR_INVALID;
+  if (!workspace || ws_bytes < layer_ws_bytes(c)) return TP_ERR_WORKSPACE;
+  if (!al256(workspace)) return TP_ERR_ALIGN;
+  if (!al16(x) || !al16(out) || !al16(sv->h1)) return TP_ERR_ALIGN;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  LayerWs ws{bb(workspace), 0};
+  const size_t th = static_cast<size_t>(c.T * c.h) * 2;
+  void* O = ws.take<uint8_t>(th);
+  void* M = ws.take<uint8_t>(th);
+  ws.off += 6 * round256(th) + round256(static_cast<size_t>(c.T * c.hp) * 2) +
+            round256(static_cast<size_t>(c.T * 3 * c.h) * 2) +
+            round256(static_cast<size_t>(ln_bwd_blocks(c.T)) * 2 * c.h * 4);
+  void* core_ws = ws.take<uint8_t>(0);
+  const size_t core_bytes = tp_attn_core_workspace_size(c.T, c.s, c.h, c.n_heads);
+
+  cudaError_t e = timed("layer_ln", s, [&] {
+    return launch_ln_fwd(x, w->g1, w->b1, c.T, c.h, c.eps, sv->ln1, sv->mean1, sv->rstd1, s);
+  });
+  if (e != cudaSuccess) return TP_ERR_CUDA;
+  if ((st = qkv_proj(c.T, c.h, c.N, sv->ln1, w->Wqkv, w->bqkv, sv->QKV, s)) != TP_OK) return st;
+  st = attn_core_fwd_impl(TP_BF16, c.T, c.s, c.h, c.n_heads, c.N, c.causal, c.p_attn, c.seed,
+                          layer_stream(c.layer, 0), sv->QKV, sv->P, sv->Pd, sv->C, nullptr, core_ws,
+                          core_bytes, stream);
+  if (st != TP_OK) return st;
+  if ((st = out_proj(c.T, c.h, c.N, sv->C, w->Wo, w->bo, O, s)) != TP_OK) return st;
+  e = timed("layer_dropout_add", s, [&] {
+    return launch_dropout_add(O, x, c.T * c.h, c.seed, layer_stream(c.layer, 1), c.p_hidden, sv->h1, s);
+  });
+  if (e != cudaSuccess) return TP_ERR_CUDA;
+  e = timed("layer_ln", s, [&] {
+    return launch_ln_fwd(sv->h1, w->g2, w->b2, c.T, c.h, c.eps, sv->ln2, sv->mean2, sv->rstd2, s);
+  });
+  if (e != cudaSuccess) return TP_ERR_CUDA;
+  st = tp_mlp_fwd(TP_BF16, c.T, c.h, c.hp, c.N, sv->ln2, w->W, w->a, w->U, w->b, sv->Z, sv->Y, M, stream);
+  if (st != TP_OK) return st;
+  e = timed("layer_dropout_add", s, [&] {
+    return launch_dropout_add(M, sv->h1, c.T * c.h, c.seed, layer_stream(c.layer, 2), c.p_hidden, out, s);
+  });
+  return e == cudaSuccess ? TP_OK : TP_ERR_CUDA;
+}
+
+extern "C" tp_status tp_transformer_layer_bwd(const tp_layer_config* cfg, const tp_layer_params* w,
+                                              const void* x, const tp_layer_saved* sv, const void* dout,
+                                              void* dx, const tp_layer_grads* g, int accumulate,
+                                              void* workspace, size_t ws_bytes, void* stream) {
+  tp_status st = layer_check(cfg, w);
+  if (st != TP_OK) return st;
+  const tp_layer_config& c = *cfg;
+  if (c.T == 0) return TP_OK;
+  if (!x || !dout || !dx || !sv || !g || !g->dg1 || !g->db1 || !g->dg2 || !g->db2 ||
+      !shards_ok(g->dWqkv, c.N) || !shards_ok(g->dWo, c.N) || !shards_ok(g->dW, c.N) ||
+      !shards_ok(g->dU, c.N) || !opt_shards_ok(g->dbqkv, c.N) || !opt_shards_ok(g->da, c.N))
+    return TP_ERR_INVALID;
+  if (!sv->ln1 || !sv->QKV || !sv->P || !sv->C || !sv->h1 || !sv->ln2 || !sv->Z || !sv->Y ||
+      (c.p_attn > 0.f && !sv->Pd))
+    return TP_ERR_INVALID;
+  if (!workspace || ws_bytes < layer_ws_bytes(c)) return TP_ERR_WORKSPACE;
+  if (!al256(workspace)) return TP_ERR_ALIGN;
+  if (!al16(dout) || !al16(dx)) return TP_ERR_ALIGN;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  LayerWs ws{bb(workspace), 0};
+  const size_t th = static_cast<size_t>(c.T * c.h) * 2;
+  ws.take<uint8_t>(th);  // O (forward)
+  ws.take<uint8_t>(th);  // M (forward)
+  void* dM = ws.take<uint8_t>(th);
+  void* dln2 = ws.take<uint8_t>(th);
+  void* dh1 = ws.take<uint8_t>(th);
+  void* dO = ws.take<uint8_t>(th);
+  void* dC = ws.take<uint8_t>(th);
+  void* dln1 = ws.take<uint8_t>(th);
+  void* dZ = ws.take<uint8_t>(static_cast<size_t>(c.T * c.hp) * 2);
+  void* dQKV = ws.take<uint8_t>(static_cast<size_t>(c.T * 3 * c.h) * 2);
+  float* partial = ws.take<float>(static_cast<size_t>(ln_bwd_blocks(c.T)) * 2 * c.h * 4);
+  void* core_ws = ws.take<uint8_t>(0);
+  const size_t core_bytes = tp_attn_core_workspace_size(c.T, c.s, c.h, c.n_heads);
+
+  // MLP output dropout, then the MLP
+  cudaError_t e = timed("layer_dropout_add", s, [&] {
+    return launch_dropout_add(dout, nullptr, c.T * c.h, c.seed, layer_stream(c.layer, 2), c.p_hidden, dM, s);
+  });
+  if (e != cudaSuccess) return TP_ERR_CUDA;
+  st = tp_mlp_bwd(TP_BF16, c.T, c.h, c.hp, c.N, dM, sv->ln2, w->W, w->U, sv->Z, sv->Y, dZ, dln2, g->dW,
+                  g->da, g->dU, g->db, accumulate, stream);
+  if (st != TP_OK) return st;
+  // LayerNorm 2, plus the residual path: dh1 = dout + LN2'(dln2)
+  e = timed("layer_ln_bwd", s, [&] {
+    return launch_ln_bwd(dln2, sv->h1, w->g2, sv->mean2, sv->rstd2, dout, c.T, c.h, dh1, g->dg2, g->db2,
+                         accumulate, partial, s);
+  });
+  if (e != cudaSuccess) return TP_ERR_CUDA;
+  // attention output dropout, output projection, attention core, QKV projection
+  e = timed("layer_dropout_add", s, [&] {
+    return launch_dropout_add(dh1, nullptr, c.T * c.h, c.seed, layer_stream(c.layer, 1), c.p_hidden, dO, s);
+  });
+  if (e != cudaSuccess) return TP_ERR_CUDA;
+  if ((st = out_proj_bwd(c.T, c.h, c.N, dO, sv->C, w->Wo, dC, g->dWo, g->dbo, accumulate, s)) != TP_OK)
+    return st;
+  st = attn_core_bwd_impl(TP_BF16, c.T, c.s, c.h, c.n_heads, c.N, c.causal, c.p_attn, c.seed,
+                          layer_stream(c.layer, 0), sv->QKV, sv->P, sv->Pd, sv->C, dC, dQKV, core_ws,
+                          core_bytes, stream);
+  if (st != TP_OK) return st;
+  if ((st = qkv_proj_bwd(c.T, c.h, c.N, dQKV, sv->ln1, w->Wqkv, dln1, g->dWqkv, g->dbqkv, accumulate, s)) !=
+      TP_OK)
+    return st;
+  // LayerNorm 1, plus the residual path: dx = dh1 + LN1'(dln1)
+  e = timed("layer_ln_bwd", s, [&] {
+    return launch_ln_bwd(dln1, x, w->g1, sv->mean1, sv->rstd1, dh1, c.T, c.h, dx, g->dg1, g->db1, accumulate,
+                         partial, s);
+  });
+  return e == cudaSuccess ? TP_OK : TP_ERR_CUDA;
 }
 
 // ===========================================================================

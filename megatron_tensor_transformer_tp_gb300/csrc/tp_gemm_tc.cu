@@ -504,6 +504,17 @@ __device__ __forceinline__ void epilogue_chunk(const GemmGroup& G, uint4* st, in
       } else if (row_ok) {
         store_chunk(G.out, OUT_BF16, G.ldo, row, n, v, ncols, false);
       }
+      if (G.drop_mask != nullptr) {
+        // attention dropout: the kept probabilities, scaled, for the P V product
+        const uint32_t keep = row_ok ? G.drop_mask[static_cast<int64_t>(row) * G.drop_wpr + (n >> 5)] : 0u;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = (keep >> j) & 1u ? v[j] * G.drop_scale : 0.f;
+        if (coal) {
+          stage_store_rows(st, G.out2, OUT_BF16, G.ldo, row0, G.M, n, v, lane);
+        } else if (row_ok) {
+          store_chunk(G.out2, OUT_BF16, G.ldo, row, n, v, ncols, false);
+        }
+      }
       return;
     }
     if (G.epi == EPI_SMAX_BWD) {
@@ -520,6 +531,12 @@ __device__ __forceinline__ void epilogue_chunk(const GemmGroup& G, uint4* st, in
                           z, ncols, false);
       }
       const float dd = row_ok ? G.row_lse[row] : 0.f;
+      if (G.drop_mask != nullptr) {
+        // attention dropout: dP = (dC V^T) * keep * scale
+        const uint32_t keep = row_ok ? G.drop_mask[static_cast<int64_t>(row) * G.drop_wpr + (n >> 5)] : 0u;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = (keep >> j) & 1u ? v[j] * G.drop_scale : 0.f;
+      }
 #pragma unroll
       for (int j = 0; j < 32; ++j) v[j] = z[j] * (v[j] - dd) * G.alpha;
       if (coal) {

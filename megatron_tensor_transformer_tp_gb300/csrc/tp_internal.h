@@ -89,7 +89,13 @@ struct GemmGroup {
   int causal, kr_mode;
   int tri_ok;  // KR_TRI tiles with no k-blocks need not run (their outputs are never read)
   int tri;     // set by the launcher: only the causal tiles are enumerated
-  int pad_attn;
+  // Attention dropout: keep bits of row m, keys 32 w .. 32 w + 31, at
+  // drop_mask[m * drop_wpr + w]; kept values are scaled by drop_scale.
+  // SOFTMAX then also stores the dropped probabilities to out2; SMAX_BWD
+  // scales its accumulator (dP) by the mask.
+  const uint32_t* drop_mask;
+  int drop_wpr;
+  float drop_scale;
 };
 
 // One operand pair of the tensor-core engine.  Operands are bf16.
@@ -152,6 +158,24 @@ cudaError_t launch_attn_lse(const void* part, int P, int64_t s, int64_t rows, in
                             cudaStream_t st);
 cudaError_t launch_attn_rowdot(const void* C, const void* dC, int64_t h, int64_t s, int n_heads, int d,
                                int64_t pairs, float* D, cudaStream_t st);
+
+// Transformer-layer row kernels (LayerNorm, dropout + residual, attention
+// dropout bits).  Dropout keeps element e iff its 16-bit Philox field is >=
+// dropout_threshold(p).
+uint32_t dropout_threshold(float p);
+cudaError_t launch_ln_fwd(const void* x, const float* g, const float* b, int64_t T, int64_t h, float eps,
+                          void* y, float* mean, float* rstd, cudaStream_t st);
+int ln_bwd_blocks(int64_t T);
+cudaError_t launch_ln_bwd(const void* dy, const void* x, const float* g, const float* mean,
+                          const float* rstd, const void* dres, int64_t T, int64_t h, void* dx,
+                          float* dg, float* db, int accumulate, float* partial, cudaStream_t st);
+cudaError_t launch_dropout_add(const void* x, const void* res, int64_t n, uint64_t seed, uint64_t stream,
+                               float p, void* out, cudaStream_t st);
+cudaError_t launch_pos_embed_dropout(const void* words, const void* pos_table, const int64_t* positions,
+                                     int64_t T, int64_t h, int64_t max_pos, uint64_t seed, uint64_t stream,
+                                     float p, void* out, cudaStream_t st);
+cudaError_t launch_attn_keep(int64_t pairs, int64_t s, int n_heads, int heads_per_shard, uint64_t seed,
+                             uint64_t stream0, float p, uint32_t* words, cudaStream_t st);
 
 // Mixed-precision Adam step.  Parameter groups are cut into chunks of
 // opt_chunk_elems() elements; chunk c belongs to the last group whose

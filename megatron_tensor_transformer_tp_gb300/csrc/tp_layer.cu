@@ -1,0 +1,367 @@
+// Row kernels of the transformer layer ("Megatron" walkthrough,
+// §ParallelTransformerLayer; "Megatron / ZeRO" study notes on fp32 LayerNorm
+// parameters):
+//   ln_fwd_kernel        LayerNorm of bf16 rows with fp32 gain and bias,
+//                        saving the row mean and 1/std;
+//   ln_bwd_kernel        its input gradient (plus an optional residual
+//                        gradient) and per-block partial gain/bias gradients;
+//   colsum_partials      the partials summed in block order (deterministic);
+//   dropout_add_kernel   out = res + x * keep / (1 - p) and its backward;
+//   pos_embed_dropout    (word + position embedding) with dropout;
+//   attn_keep_kernel     attention-dropout keep bits, 32 keys per word.
+// Dropout draws from Philox4x64-10 (Salmon et al., "Parallel random numbers:
+// as easy as 1, 2, 3", SC 2011): element e of a site with key (seed, stream)
+// takes the 16-bit field 16 (e mod 4) of word (e mod 16) / 4 at counter e / 16
+// and is kept iff the field is >= the threshold floor(p 2^16).
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "tp_internal.h"
+
+namespace tp {
+namespace {
+
+constexpr int kLnThreads = 256;  // rows up to 256 x 32 = 8192 wide
+
+__device__ __forceinline__ void philox4x64_10(uint64_t c0, uint64_t k0, uint64_t k1, uint64_t out[4]) {
+  const uint64_t M0 = 0xD2E7470EE14C6C93ull, M1 = 0xCA5A826395121157ull;
+  const uint64_t W0 = 0x9E3779B97F4A7C15ull, W1 = 0xBB67AE8584CAA73Bull;
+  uint64_t x0 = c0, x1 = 0, x2 = 0, x3 = 0;
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    const uint64_t hi0 = __umul64hi(M0, x0), lo0 = M0 * x0;
+    const uint64_t hi1 = __umul64hi(M1, x2), lo1 = M1 * x2;
+    x0 = hi1 ^ x1 ^ k0;
+    x1 = lo1;
+    x2 = hi0 ^ x3 ^ k1;
+    x3 = lo0;
+    k0 += W0;
+    k1 += W1;
+  }
+  out[0] = x0;
+  out[1] = x1;
+  out[2] = x2;
+  out[3] = x3;
+}
+
+// Keep bits of the 16 elements of Philox block `blk` (bit f = element 16 blk + f).
+__device__ __forceinline__ uint32_t keep16(uint64_t blk, uint64_t seed, uint64_t stream, uint32_t thr) {
+  uint64_t w[4];
+  philox4x64_10(blk, seed, stream, w);
+  uint32_t bits = 0;
+#pragma unroll
+  for (int f = 0; f < 16; ++f) {
+    const uint32_t field = static_cast<uint32_t>((w[f >> 2] >> (16 * (f & 3))) & 0xFFFFull);
+    bits |= (field >= thr ? 1u : 0u) << f;
+  }
+  return bits;
+}
+
+// Fixed-order block sum of one float (all threads receive it).
+__device__ __forceinline__ float block_sum(float v, float* red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __syncthreads();  // red is reused between calls
+  if (lane == 0) red[w] = v;
+  __syncthreads();
+  float t = 0.f;
+  for (int i = 0; i < kLnThreads / 32; ++i) t += red[i];
+  return t;
+}
+
+template <int kLnMaxPer>
+__global__ void __launch_bounds__(kLnThreads) ln_fwd_kernel(const __nv_bfloat16* __restrict__ x,
+                                                            const float* __restrict__ g,
+                                                            const float* __restrict__ b, int64_t h,
+                                                            float eps, __nv_bfloat16* __restrict__ y,
+                                                            float* __restrict__ mean_out,
+                                                            float* __restrict__ rstd_out) {
+  __shared__ float red[kLnThreads / 32];
+  const int64_t row = blockIdx.x;
+  const __nv_bfloat16* xr = x + row * h;
+  float v[kLnMaxPer];
+  float s = 0.f;
+#pragma unroll
+  for (int i = 0; i < kLnMaxPer; ++i) {
+    const int64_t c = threadIdx.x + static_cast<int64_t>(i) * kLnThreads;
+    v[i] = c < h ? __bfloat162float(xr[c]) : 0.f;
+    s += v[i];
+  }
+  const float mean = block_sum(s, red) / static_cast<float>(h);
+  float q = 0.f;
+#pragma unroll
+  for (int i = 0; i < kLnMaxPer; ++i) {
+    const int64_t c = threadIdx.x + static_cast<int64_t>(i) * kLnThreads;
+    const float dlt = c < h ? v[i] - mean : 0.f;
+    q += dlt * dlt;
+  }
+  const float rstd = rsqrtf(block_sum(q, red) / static_cast<float>(h) + eps);
+#pragma unroll
+  for (int i = 0; i < kLnMaxPer; ++i) {
+    const int64_t c = threadIdx.x + static_cast<int64_t>(i) * kLnThreads;
+    if (c < h) y[row * h + c] = __float2bfloat16_rn((v[i] - mean) * rstd * g[c] + b[c]);
+  }
+  if (threadIdx.x == 0) {
+    mean_out[row] = mean;
+    rstd_out[row] = rstd;
+  }
+}
+
+// Rows [blockIdx.x * rows_per, ...): dx = rstd (dxhat - mean(dxhat) - xhat
+// mean(dxhat xhat)) (+ dres), dxhat = dy g; the block's rows' dy xhat and dy
+// summed per column into partial[blockIdx.x][0..h) and [h..2h).
+template <int kLnMaxPer>
+__global__ void __launch_bounds__(kLnThreads) ln_bwd_kernel(
+    const __nv_bfloat16* __restrict__ dy, const __nv_bfloat16* __restrict__ x,
+    const float* __restrict__ g, const float* __restrict__ mean_in, const float* __restrict__ rstd_in,
+    const __nv_bfloat16* __restrict__ dres, int64_t T, int64_t h, int rows_per,
+    __nv_bfloat16* __restrict__ dx, float* __restrict__ partial) {
+  __shared__ float red[kLnThreads / 32];
+  float pg[kLnMaxPer], pb[kLnMaxPer];
+#pragma unroll
+  for (int i = 0; i < kLnMaxPer; ++i) pg[i] = pb[i] = 0.f;
+  const int64_t r0 = static_cast<int64_t>(blockIdx.x) * rows_per;
+  const int64_t r1 = min(T, r0 + rows_per);
+  for (int64_t row = r0; row < r1; ++row) {
+    const float mean = mean_in[row], rstd = rstd_in[row];
+    float xh[kLnMaxPer], dxh[kLnMaxPer];
+    float s1 = 0.f, s2 = 0.f;
+#pragma unroll
+    for (int i = 0; i < kLnMaxPer; ++i) {
+      const int64_t c = threadIdx.x + static_cast<int64_t>(i) * kLnThreads;
+      float d = 0.f, xv = 0.f, gv = 0.f;
+      if (c < h) {
+        d = __bfloat162float(dy[row * h + c]);
+        xv = (__bfloat162float(x[row * h + c]) - mean) * rstd;
+        gv = g[c];
+      }
+      xh[i] = xv;
+      dxh[i] = d * gv;
+      pg[i] += d * xv;
+      pb[i] += d;
+      s1 += dxh[i];
+      s2 += dxh[i] * xv;
+    }
+    const float m1 = block_sum(s1, red) / static_cast<float>(h);
+    const float m2 = block_sum(s2, red) / static_cast<float>(h);
+#pragma unroll
+    for (int i = 0; i < kLnMaxPer; ++i) {
+      const int64_t c = threadIdx.x + static_cast<int64_t>(i) * kLnThreads;
+      if (c < h) {
+        float o = rstd * (dxh[i] - m1 - xh[i] * m2);
+        if (dres) o += __bfloat162float(dres[row * h + c]);
+        dx[row * h + c] = __float2bfloat16_rn(o);
+      }
+    }
+  }
+  float* pp = partial + static_cast<int64_t>(blockIdx.x) * 2 * h;
+#pragma unroll
+  for (int i = 0; i < kLnMaxPer; ++i) {
+    const int64_t c = threadIdx.x + static_cast<int64_t>(i) * kLnThreads;
+    if (c < h) {
+      pp[c] = pg[i];
+      pp[h + c] = pb[i];
+    }
+  }
+}
+
+// out[c] (+)= sum over blocks k in order of partial[k][c], c < n.
+__global__ void colsum_partials_kernel(const float* __restrict__ partial, int nblocks, int64_t n,
+                                       int64_t pitch, float* __restrict__ out, int accumulate) {
+  const int64_t c = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (c >= n) return;
+  float s = 0.f;
+  for (int k = 0; k < nblocks; ++k) s += partial[static_cast<int64_t>(k) * pitch + c];
+  out[c] = accumulate ? out[c] + s : s;
+}
+
+// 16 elements per thread (one Philox block): out = res + x * keep * scale, or
+// (res == null) out = x * keep * scale.  n is a multiple of 16.
+__global__ void __launch_bounds__(256) dropout_add_kernel(const __nv_bfloat16* __restrict__ x,
+                                                          const __nv_bfloat16* __restrict__ res,
+                                                          int64_t nblk, uint64_t seed, uint64_t stream,
+                                                          uint32_t thr, float scale,
+                                                          __nv_bfloat16* __restrict__ out) {
+  const int64_t blk = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (blk >= nblk) return;
+  const uint32_t bits = keep16(static_cast<uint64_t>(blk), seed, stream, thr);
+  const uint4* x4 = reinterpret_cast<const uint4*>(x) + blk * 2;
+  uint4 xv[2] = {x4[0], x4[1]};
+  uint4 rv[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
+  if (res) {
+    const uint4* r4 = reinterpret_cast<const uint4*>(res) + blk * 2;
+    rv[0] = r4[0];
+    rv[1] = r4[1];
+  }
+  uint4 ov[2];
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {
+    const __nv_bfloat162* xa = reinterpret_cast<const __nv_bfloat162*>(&xv[q]);
+    const __nv_bfloat162* ra = reinterpret_cast<const __nv_bfloat162*>(&rv[q]);
+    __nv_bfloat162* oa = reinterpret_cast<__nv_bfloat162*>(&ov[q]);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int f = q * 8 + 2 * k;
+      const float2 a = __bfloat1622float2(xa[k]), r = __bfloat1622float2(ra[k]);
+      const float k0 = (bits >> f) & 1u ? scale : 0.f, k1 = (bits >> (f + 1)) & 1u ? scale : 0.f;
+      oa[k] = __floats2bfloat162_rn(r.x + a.x * k0, r.y + a.y * k1);
+    }
+  }
+  uint4* o4 = reinterpret_cast<uint4*>(out) + blk * 2;
+  o4[0] = ov[0];
+  o4[1] = ov[1];
+}
+
+// Input of the first layer: out = (words + pos_table[positions[row]]) * keep *
+// scale, 16 elements of one row per thread (h % 16 == 0).
+__global__ void __launch_bounds__(256) pos_embed_dropout_kernel(
+    const __nv_bfloat16* __restrict__ words, const __nv_bfloat16* __restrict__ pos_table,
+    const int64_t* __restrict__ positions, int64_t h, int64_t max_pos, int64_t nblk, uint64_t seed,
+    uint64_t stream, uint32_t thr, float scale, __nv_bfloat16* __restrict__ out) {
+  const int64_t blk = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (blk >= nblk) return;
+  const int64_t e = blk * 16, row = e / h, col = e - row * h;
+  const uint32_t bits = keep16(static_cast<uint64_t>(blk), seed, stream, thr);
+  const uint4* w4 = reinterpret_cast<const uint4*>(words + e);
+  const int64_t pos = positions[row];
+  const bool pos_ok = pos >= 0 && pos < max_pos;  // a position outside the table adds zeros
+  const uint4* p4 = reinterpret_cast<const uint4*>(pos_table + (pos_ok ? pos : 0) * h + col);
+  uint4 ov[2];
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {
+    const uint4 wv = w4[q], pv = pos_ok ? p4[q] : make_uint4(0, 0, 0, 0);
+    const __nv_bfloat162* wa = reinterpret_cast<const __nv_bfloat162*>(&wv);
+    const __nv_bfloat162* pa = reinterpret_cast<const __nv_bfloat162*>(&pv);
+    __nv_bfloat162* oa = reinterpret_cast<__nv_bfloat162*>(&ov[q]);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int f = q * 8 + 2 * k;
+      const float2 a = __bfloat1622float2(wa[k]), b = __bfloat1622float2(pa[k]);
+      const float k0 = (bits >> f) & 1u ? scale : 0.f, k1 = (bits >> (f + 1)) & 1u ? scale : 0.f;
+      oa[k] = __floats2bfloat162_rn((a.x + b.x) * k0, (a.y + b.y) * k1);
+    }
+  }
+  uint4* o4 = reinterpret_cast<uint4*>(out + e);
+  o4[0] = ov[0];
+  o4[1] = ov[1];
+}
+
+// Keep bits of attention dropout: word w of row q of pair g covers keys
+// 32 w .. 32 w + 31 of element block ((g s + q) s + 32 w) / 16 (s % 16 == 0);
+// pair g = sequence * heads + head draws from stream stream0 + shard(head).
+__global__ void __launch_bounds__(256) attn_keep_kernel(int64_t pairs, int64_t s, int wpr, int n_heads,
+                                                        int heads_per_shard, uint64_t seed,
+                                                        uint64_t stream0, uint32_t thr,
+                                                        uint32_t* __restrict__ words) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t total = pairs * s * wpr;
+  if (i >= total) return;
+  const int64_t w = i % wpr, gq = i / wpr;  // gq = g * s + q
+  const int64_t g = gq / s;
+  const int j = static_cast<int>(g % n_heads);
+  const uint64_t stream = stream0 + static_cast<uint64_t>(j / heads_per_shard);
+  const int64_t e = gq * s + 32 * w;
+  uint32_t bits = keep16(static_cast<uint64_t>(e / 16), seed, stream, thr);
+  if (32 * w + 16 < s) bits |= keep16(static_cast<uint64_t>(e / 16 + 1), seed, stream, thr) << 16;
+  words[i] = bits;
+}
+
+}  // namespace
+
+uint32_t dropout_threshold(float p) {
+  const double t = floor(static_cast<double>(p) * 65536.0);
+  return t < 0 ? 0u : (t > 65536.0 ? 65536u : static_cast<uint32_t>(t));
+}
+
+// Values per thread for a row of h: the smallest of 4, 8, 16, 32 that covers it.
+static int ln_per(int64_t h) {
+  for (int p = 4; p <= 32; p *= 2)
+    if (h <= static_cast<int64_t>(p) * kLnThreads) return p;
+  return 0;
+}
+
+cudaError_t launch_ln_fwd(const void* x, const float* g, const float* b, int64_t T, int64_t h, float eps,
+                          void* y, float* mean, float* rstd, cudaStream_t st) {
+  if (T == 0) return cudaSuccess;
+  const auto* xb = static_cast<const __nv_bfloat16*>(x);
+  auto* yb = static_cast<__nv_bfloat16*>(y);
+  const unsigned grid = static_cast<unsigned>(T);
+  switch (ln_per(h)) {
+    case 4: ln_fwd_kernel<4><<<grid, kLnThreads, 0, st>>>(xb, g, b, h, eps, yb, mean, rstd); break;
+    case 8: ln_fwd_kernel<8><<<grid, kLnThreads, 0, st>>>(xb, g, b, h, eps, yb, mean, rstd); break;
+    case 16: ln_fwd_kernel<16><<<grid, kLnThreads, 0, st>>>(xb, g, b, h, eps, yb, mean, rstd); break;
+    case 32: ln_fwd_kernel<32><<<grid, kLnThreads, 0, st>>>(xb, g, b, h, eps, yb, mean, rstd); break;
+    default: return cudaErrorInvalidValue;
+  }
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+int ln_bwd_blocks(int64_t T) {
+  const int64_t rows_per = 16;
+  return static_cast<int>((T + rows_per - 1) / rows_per);
+}
+
+cudaError_t launch_ln_bwd(const void* dy, const void* x, const float* g, const float* mean,
+                          const float* rstd, const void* dres, int64_t T, int64_t h, void* dx,
+                          float* dg, float* db, int accumulate, float* partial, cudaStream_t st) {
+  if (T == 0) return cudaSuccess;
+  const int nb = ln_bwd_blocks(T);
+  const auto* dyb = static_cast<const __nv_bfloat16*>(dy);
+  const auto* xb = static_cast<const __nv_bfloat16*>(x);
+  const auto* rb = static_cast<const __nv_bfloat16*>(dres);
+  auto* dxb = static_cast<__nv_bfloat16*>(dx);
+#define TP_LNB(P) ln_bwd_kernel<P><<<nb, kLnThreads, 0, st>>>(dyb, xb, g, mean, rstd, rb, T, h, 16, dxb, partial)
+  switch (ln_per(h)) {
+    case 4: TP_LNB(4); break;
+    case 8: TP_LNB(8); break;
+    case 16: TP_LNB(16); break;
+    case 32: TP_LNB(32); break;
+    default: return cudaErrorInvalidValue;
+  }
+#undef TP_LNB
+  const unsigned cb = static_cast<unsigned>((h + 255) / 256);
+  colsum_partials_kernel<<<cb, 256, 0, st>>>(partial, nb, h, 2 * h, dg, accumulate);
+  colsum_partials_kernel<<<cb, 256, 0, st>>>(partial + h, nb, h, 2 * h, db, accumulate);
+  count_launches(3);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dropout_add(const void* x, const void* res, int64_t n, uint64_t seed, uint64_t stream,
+                               float p, void* out, cudaStream_t st) {
+  const int64_t nblk = n / 16;
+  if (nblk == 0) return cudaSuccess;
+  dropout_add_kernel<<<static_cast<unsigned>((nblk + 255) / 256), 256, 0, st>>>(
+      static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(res), nblk, seed, stream,
+      dropout_threshold(p), 1.0f / (1.0f - p), static_cast<__nv_bfloat16*>(out));
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_pos_embed_dropout(const void* words, const void* pos_table, const int64_t* positions,
+                                     int64_t T, int64_t h, int64_t max_pos, uint64_t seed, uint64_t stream,
+                                     float p, void* out, cudaStream_t st) {
+  const int64_t nblk = T * h / 16;
+  if (nblk == 0) return cudaSuccess;
+  pos_embed_dropout_kernel<<<static_cast<unsigned>((nblk + 255) / 256), 256, 0, st>>>(
+      static_cast<const __nv_bfloat16*>(words), static_cast<const __nv_bfloat16*>(pos_table), positions, h,
+      max_pos, nblk, seed, stream, dropout_threshold(p), 1.0f / (1.0f - p), static_cast<__nv_bfloat16*>(out));
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_attn_keep(int64_t pairs, int64_t s, int n_heads, int heads_per_shard, uint64_t seed,
+                             uint64_t stream0, float p, uint32_t* words, cudaStream_t st) {
+  const int wpr = static_cast<int>((s + 31) / 32);
+  const int64_t total = pairs * s * wpr;
+  if (total == 0) return cudaSuccess;
+  attn_keep_kernel<<<static_cast<unsigned>((total + 255) / 256), 256, 0, st>>>(
+      pairs, s, wpr, n_heads, heads_per_shard, seed, stream0, dropout_threshold(p), words);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+}  // namespace tp

@@ -829,8 +829,13 @@ def transformer_layer_bwd(dout, saved, P, cfg):
 def embed_position_dropout(words, pos_table, positions, keep, p):
     """Input of the first layer ([Walkthrough] §Embedding.forward): word
     embeddings (the vocab-parallel lookup, summed over ranges) plus position
-    embeddings, then dropout: (words + pos_table[positions]) * keep / (1 - p)."""
-    return (np.asarray(words, dtype=np.float64) + pos_table[np.asarray(positions)]) * keep / (1.0 - p)
+    embeddings, then dropout: (words + pos_table[positions]) * keep / (1 - p).
+    A position outside the table adds a zero row (this build's reading: the
+    pages index in range only)."""
+    pos = np.asarray(positions)
+    ok = (pos >= 0) & (pos < len(pos_table))
+    pe = np.where(ok[:, None], np.asarray(pos_table, dtype=np.float64)[np.where(ok, pos, 0)], 0.0)
+    return (np.asarray(words, dtype=np.float64) + pe) * keep / (1.0 - p)
 
 
 # --------------------------------------------------------------------------

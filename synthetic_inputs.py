@@ -24,7 +24,7 @@ import numpy as np
 import torch
 
 __all__ = ["WORKLOADS", "normal", "uniform_ids", "mlp_inputs", "attn_inputs",
-           "embed_inputs", "ce_inputs", "adam_inputs", "attn_core_inputs", "split_rows", "split_cols"]
+           "embed_inputs", "ce_inputs", "adam_inputs", "attn_core_inputs", "layer_inputs", "split_rows", "split_cols"]
 
 # Workloads: shapes and seeds only.  Names state the sizes.
 WORKLOADS = {
@@ -51,6 +51,11 @@ WORKLOADS = {
     # bf16 causal attention core between the projections: b=1, s=2048, 8 heads of 512, N=8
     "attn_core_b1_s2048_heads8_d512_causal": dict(kind="attn_core", dtype="bf16", b=1, s=2048,
                                                   h=4096, n_heads=8, N=8, causal=True, seed=1007),
+    # bf16 transformer layer of the H=4096 model: b=1, s=2048, 8 heads of 512, h'=16384, N=8,
+    # causal, attention and hidden dropout 0.1
+    "layer_b1_s2048_h4096_heads8_hp16384_N8": dict(kind="layer", dtype="bf16", b=1, s=2048, h=4096,
+                                                   hp=16384, n_heads=8, N=8, causal=True, eps=1e-5,
+                                                   p_attn=0.1, p_hidden=0.1, layer=0, seed=1008),
     # fp32 mixed-precision Adam step over one transformer layer of the H=4096 model:
     # QKV (3H, H), attention output (H, H), MLP up (4H, H), MLP down (H, 4H) with
     # weight decay; two LayerNorms' gain and bias (H each) without; 201,342,976 values
@@ -236,3 +241,32 @@ def attn_core_inputs(cfg: dict) -> dict:
     return dict(T=T, s=s, h=h, n_heads=cfg["n_heads"], N=cfg["N"],
                 QKV=normal(seed, 41, (T, 3 * h), 1.0, "bf16"),
                 dC=normal(seed, 42, (T, h), 1.0, "bf16"))
+
+
+def layer_inputs(cfg: dict, T: int | None = None) -> dict:
+    """Inputs of one transformer layer: x and dout ~ N(0, 1) bf16 (T, h);
+    unsharded weights ~ N(0, 0.02) bf16 split into shards as the layer uses
+    them (Wqkv rows [Q; K; V] with shard i taking its h/N rows of each,
+    Wo / U by columns, W by rows), biases ~ N(0, 0.02), LayerNorm gains
+    1 + N(0, 0.1) and biases N(0, 0.1) in fp32.  T defaults to b s."""
+    seed, h, hp, N = cfg["seed"], cfg["h"], cfg["hp"], cfg["N"]
+    T = cfg["b"] * cfg["s"] if T is None else T
+    d = h // N
+    Wqkv = normal(seed, 51, (3 * h, h), 0.02, "bf16")
+    bqkv = normal(seed, 52, (3 * h,), 0.02, "bf16")
+    Wo = normal(seed, 53, (h, h), 0.02, "bf16")
+    W = normal(seed, 54, (hp, h), 0.02, "bf16")
+    U = normal(seed, 55, (h, hp), 0.02, "bf16")
+    n = hp // N
+    return dict(
+        T=T, x=normal(seed, 56, (T, h), 1.0, "bf16"), dout=normal(seed, 57, (T, h), 1.0, "bf16"),
+        g1=1.0 + normal(seed, 58, (h,), 0.1, "f32"), b1=normal(seed, 59, (h,), 0.1, "f32"),
+        g2=1.0 + normal(seed, 60, (h,), 0.1, "f32"), b2=normal(seed, 61, (h,), 0.1, "f32"),
+        Wqkv=[torch.cat([Wqkv[j * h + i * d: j * h + (i + 1) * d] for j in range(3)]).contiguous()
+              for i in range(N)],
+        bqkv=[torch.cat([bqkv[j * h + i * d: j * h + (i + 1) * d] for j in range(3)]).contiguous()
+              for i in range(N)],
+        Wo=split_cols(Wo, N), bo=normal(seed, 62, (h,), 0.02, "bf16"),
+        W=[W[i * n:(i + 1) * n].contiguous() for i in range(N)],
+        a=[t.contiguous() for t in normal(seed, 63, (hp,), 0.02, "bf16").split(n)],
+        U=split_cols(U, N), b=normal(seed, 64, (h,), 0.02, "bf16"))

@@ -234,7 +234,49 @@ def test_attn_core_validation_and_workspace_size():
         assert core(fn, ws=FAKE * 256 + 16) == tp.TP_ERR_ALIGN
         assert core(fn, T=0) == tp.TP_OK
     b, H, s = 2, 4, 256
-    fwd = b * H * (s // 64) * s * 8 + b * H * s * 4
-    bwd = b * H * s * 4 + b * H * s * s * 2
+    keep = b * H * s * (s // 32) * 4  # attention-dropout keep words
+    fwd = b * H * (s // 64) * s * 8 + b * H * s * 4 + keep
+    bwd = b * H * s * 4 + b * H * s * s * 2 + keep
     assert tp.tp_attn_core_workspace_size(512, 256, 512, 4) == max(fwd, bwd)
     assert tp.tp_attn_core_workspace_size(500, 256, 512, 4) == 0
+
+
+def layer_cfg(**kw):
+    c = dict(T=512, s=256, h=512, hp=2048, n_heads=4, N=2, causal=1, eps=1e-5, p_attn=0.1,
+             p_hidden=0.1, seed=1, layer=0)
+    c.update(kw)
+    return tp._layer_cfg(c)
+
+
+def layer_fwd(cfg, params=None, ws_bytes=None):
+    import ctypes as C
+    sh = ptrs(2)
+    w = params or tp.tp_layer_params(FAKE, FAKE, C.cast(sh[0], C.c_void_p).value, None,
+                                     C.cast(sh[0], C.c_void_p).value, None, FAKE, FAKE,
+                                     C.cast(sh[0], C.c_void_p).value, None,
+                                     C.cast(sh[0], C.c_void_p).value, None)
+    sv = tp.tp_layer_saved(*([FAKE] * 13))
+    if ws_bytes is None:
+        ws_bytes = 1 << 34
+    return L.tp_transformer_layer_fwd(C.byref(cfg), C.byref(w), FAKE, FAKE, C.byref(sv), FAKE * 256,
+                                      ws_bytes, None), sh
+
+
+def test_layer_validation():
+    assert layer_fwd(layer_cfg(T=500))[0] == tp.TP_ERR_INVALID         # T % s
+    assert layer_fwd(layer_cfg(h=520, n_heads=4))[0] == tp.TP_ERR_INVALID  # h % 16
+    assert layer_fwd(layer_cfg(p_hidden=1.0))[0] == tp.TP_ERR_INVALID
+    assert layer_fwd(layer_cfg(p_attn=0.1, s=200, T=400))[0] == tp.TP_ERR_INVALID  # s % 16 with dropout
+    assert layer_fwd(layer_cfg(hp=2047))[0] == tp.TP_ERR_INVALID
+    assert layer_fwd(layer_cfg(), ws_bytes=16)[0] == tp.TP_ERR_WORKSPACE
+    assert layer_fwd(layer_cfg(T=0))[0] == tp.TP_OK
+    c = layer_cfg()
+    assert L.tp_transformer_layer_workspace_size(ctypes.byref(c)) > 0
+
+
+def test_position_embed_dropout_validation():
+    f = L.tp_position_embed_dropout
+    assert f(8, 40, 16, FAKE, FAKE, FAKE, 0.1, 1, 2, FAKE, None) == tp.TP_ERR_INVALID   # h % 16
+    assert f(8, 64, 16, FAKE, FAKE, FAKE, 1.5, 1, 2, FAKE, None) == tp.TP_ERR_INVALID
+    assert f(8, 64, 16, FAKE + 2, FAKE, FAKE, 0.1, 1, 2, FAKE, None) == tp.TP_ERR_ALIGN
+    assert f(0, 64, 16, None, None, None, 0.1, 1, 2, None, None) == tp.TP_OK
