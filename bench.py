@@ -422,6 +422,79 @@ class AttnCoreBench:
                 "attn_rowdot": ("hbm", 2.0 * self.T * self.h * 2 + rows * 4.0)}
 
 
+class LayerBench:
+    """One transformer layer, forward and backward (LayerNorm, QKV projection,
+    causal attention core with attention dropout, output projection, dropout +
+    residual, LayerNorm, MLP, dropout + residual).  The step's FLOPs: three
+    times the forward's linear layers (8 T h^2 + 4 T h h') plus the attention
+    core's 12 b H s^2 d times the causal fraction; the row kernels' work is
+    counted in bytes per kernel."""
+    kind = "layer"
+
+    def __init__(self, name, tp, torch):
+        self.name, self.tp, self.torch = name, tp, torch
+        cfg = dict(SI.WORKLOADS[name])
+        inp = SI.layer_inputs(cfg)
+        self.T, self.h, self.hp, self.s = inp["T"], cfg["h"], cfg["hp"], cfg["s"]
+        self.H, self.N = cfg["n_heads"], cfg["N"]
+        self.b, self.d = self.T // self.s, self.h // self.H
+        self.cfg = dict(cfg, T=self.T)
+        d = lambda t: t.cuda().contiguous()
+        self.params = dict(g1=d(inp["g1"]), b1=d(inp["b1"]), g2=d(inp["g2"]), b2=d(inp["b2"]),
+                           Wqkv=[d(t) for t in inp["Wqkv"]], bqkv=[d(t) for t in inp["bqkv"]],
+                           Wo=[d(t) for t in inp["Wo"]], bo=d(inp["bo"]), W=[d(t) for t in inp["W"]],
+                           a=[d(t) for t in inp["a"]], U=[d(t) for t in inp["U"]], b=d(inp["b"]))
+        bf, f32 = torch.bfloat16, torch.float32
+        e = lambda *shape, dt=bf: torch.empty(*shape, dtype=dt, device="cuda")
+        T, h, hp, H, s = self.T, self.h, self.hp, self.H, self.s
+        self.saved = dict(ln1=e(T, h), mean1=e(T, dt=f32), rstd1=e(T, dt=f32), QKV=e(T, 3 * h),
+                          P=e(self.b, H, s, s), Pd=e(self.b, H, s, s), C=e(T, h), h1=e(T, h),
+                          ln2=e(T, h), mean2=e(T, dt=f32), rstd2=e(T, dt=f32), Z=e(T, hp), Y=e(T, hp))
+        N, d3, n = self.N, h // self.N, hp // self.N
+        self.grads = dict(dg1=e(h, dt=f32), db1=e(h, dt=f32), dg2=e(h, dt=f32), db2=e(h, dt=f32),
+                          dbo=e(h, dt=f32), db=e(h, dt=f32),
+                          dWqkv=[e(3 * d3, h, dt=f32) for _ in range(N)],
+                          dbqkv=[e(3 * d3, dt=f32) for _ in range(N)],
+                          dWo=[e(h, d3, dt=f32) for _ in range(N)], dW=[e(n, h, dt=f32) for _ in range(N)],
+                          da=[e(n, dt=f32) for _ in range(N)], dU=[e(h, n, dt=f32) for _ in range(N)])
+        self.x, self.dout = d(inp["x"]), d(inp["dout"])
+        self.out, self.dx = torch.empty_like(self.x), torch.empty_like(self.x)
+        self.ws = torch.empty(tp.tp_transformer_layer_workspace_size(self.cfg), dtype=torch.uint8,
+                              device="cuda")
+        self.frac = (s + 1) / (2.0 * s) if cfg["causal"] else 1.0
+
+    def step(self):
+        tp = self.tp
+        tp.tp_transformer_layer_fwd(self.cfg, self.params, self.x, self.out, self.saved, self.ws)
+        tp.tp_transformer_layer_bwd(self.cfg, self.params, self.x, self.saved, self.dout, self.dx,
+                                    self.grads, self.ws)
+
+    def units(self):
+        T, h, hp = self.T, self.h, self.hp
+        core = 12.0 * self.b * self.H * self.s * self.s * self.d * self.frac
+        return 3.0 * (8.0 * T * h * h + 4.0 * T * h * hp) + core, "TFLOP/s", 1e12
+
+    def kernel_work(self):
+        T, h, hp = self.T, self.h, self.hp
+        u = 2.0 * self.b * self.H * self.s * self.s * self.d * self.frac
+        rows = self.b * self.H * self.s
+        th = T * h * 2.0
+        return {"gemm_layer_qkv": ("tensor", 6.0 * T * h * h), "gemm_layer_oproj": ("tensor", 2.0 * T * h * h),
+                "gemm_layer_oproj_bwd": ("tensor", 4.0 * T * h * h),
+                "gemm_layer_qkv_bwd": ("tensor", 12.0 * T * h * h),
+                "gemm_mlp_fwd": ("tensor", 4.0 * T * h * hp), "gemm_mlp_bwd": ("tensor", 8.0 * T * h * hp),
+                "gemm_attn_scores": ("tensor", u), "gemm_attn_pv": ("tensor", 2 * u),
+                "gemm_attn_bwd": ("tensor", 4 * u),
+                "attn_lse": ("hbm", rows * (self.s + 63) // 64 * 8.0 + rows * 4.0),
+                "attn_rowdot": ("hbm", 2.0 * th + rows * 4.0),
+                "attn_keep": ("hbm", rows * ((self.s + 31) // 32) * 4.0),
+                # per call: read x, write y (bf16) plus the row statistics
+                "layer_ln": ("hbm", 2.0 * th + 8.0 * T),
+                "layer_ln_bwd": ("hbm", 4.0 * th + 8.0 * T),
+                # forward: read x and res, write out; backward: read dout, write dx (mean of both)
+                "layer_dropout_add": ("hbm", 2.5 * th)}
+
+
 class AdamBench:
     """Mixed-precision Adam step over fp32 flat groups: the norm pass reads the
     gradients (4 B per value); the update reads parameter, gradient and both
@@ -453,7 +526,7 @@ class AdamBench:
 
 
 BENCHES = {"mlp": MLPBench, "attn": AttnBench, "embed": EmbedBench, "ce": CEBench,
-           "adam": AdamBench, "attn_core": AttnCoreBench}
+           "adam": AdamBench, "attn_core": AttnCoreBench, "layer": LayerBench}
 
 
 def time_steps(torch, fn, steps, warmup, flush):
@@ -760,7 +833,8 @@ def secondary_rows(tp, torch, flush, peaks, peak_src, main_workload):
     rows = {}
     for name in ("embed_tied_V50257_h4096_T8192", "ce_V50257_h4096_T8192",
                  "attn_b1_s2048_h4096_heads8_N8", "mlp_b2_s2048_h4096_hp16384_N2",
-                 "attn_core_b1_s2048_heads8_d512_causal", "adam_layer_H4096"):
+                 "attn_core_b1_s2048_heads8_d512_causal", "layer_b1_s2048_h4096_heads8_hp16384_N8",
+                 "adam_layer_H4096"):
         if name == main_workload:
             continue
         cfg = SI.WORKLOADS[name]
