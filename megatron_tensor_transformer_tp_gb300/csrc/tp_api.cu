@@ -907,7 +907,7 @@ tp_status attn_core_fwd_impl(tp_dtype dt, int64_t T, int64_t s, int64_t h, int n
   if (e != cudaSuccess) return TP_ERR_CUDA;
   if (p_drop > 0.f) {
     e = timed("attn_keep", strm, [&] {
-      return launch_attn_keep(a.pairs, s, n_heads, n_heads / N, seed, stream0, p_drop, keep, strm);
+      return launch_attn_keep(a.pairs, s, n_heads, n_heads / N, causal != 0, seed, stream0, p_drop, keep, strm);
     });
     if (e != cudaSuccess) return TP_ERR_CUDA;
   }
@@ -980,7 +980,7 @@ tp_status attn_core_bwd_impl(tp_dtype dt, int64_t T, int64_t s, int64_t h, int n
   if (e != cudaSuccess) return TP_ERR_CUDA;
   if (p_drop > 0.f) {  // the forward's keep bits, drawn again
     e = timed("attn_keep", strm, [&] {
-      return launch_attn_keep(a.pairs, s, n_heads, n_heads / N, seed, stream0, p_drop, keep, strm);
+      return launch_attn_keep(a.pairs, s, n_heads, n_heads / N, causal != 0, seed, stream0, p_drop, keep, strm);
     });
     if (e != cudaSuccess) return TP_ERR_CUDA;
   }
@@ -1330,7 +1330,7 @@ size_t layer_ws_bytes(const tp_layer_config& c) {
   b += 8 * round256(th);                                          // O, M, dM, dln2, dh1, dO, dC, dln1
   b += round256(static_cast<size_t>(c.T * c.hp) * 2);             // dZ
   b += round256(static_cast<size_t>(c.T * 3 * c.h) * 2);          // dQKV
-  b += round256(static_cast<size_t>(ln_bwd_blocks(c.T)) * 2 * c.h * 4);  // LayerNorm partials
+  b += round256(ln_bwd_scratch_floats(c.T, c.h) * 4);             // LayerNorm partials
   b += tp_attn_core_workspace_size(c.T, c.s, c.h, c.n_heads);     // core
   return b;
 }
@@ -1451,7 +1451,7 @@ extern "C" tp_status tp_transformer_layer_fwd(const tp_layer_config* cfg, const 
   void* M = ws.take<uint8_t>(th);
   ws.off += 6 * round256(th) + round256(static_cast<size_t>(c.T * c.hp) * 2) +
             round256(static_cast<size_t>(c.T * 3 * c.h) * 2) +
-            round256(static_cast<size_t>(ln_bwd_blocks(c.T)) * 2 * c.h * 4);
+            round256(ln_bwd_scratch_floats(c.T, c.h) * 4);
   void* core_ws = ws.take<uint8_t>(0);
   const size_t core_bytes = tp_attn_core_workspace_size(c.T, c.s, c.h, c.n_heads);
 
@@ -1512,7 +1512,7 @@ extern "C" tp_status tp_transformer_layer_bwd(const tp_layer_config* cfg, const 
   void* dln1 = ws.take<uint8_t>(th);
   void* dZ = ws.take<uint8_t>(static_cast<size_t>(c.T * c.hp) * 2);
   void* dQKV = ws.take<uint8_t>(static_cast<size_t>(c.T * 3 * c.h) * 2);
-  float* partial = ws.take<float>(static_cast<size_t>(ln_bwd_blocks(c.T)) * 2 * c.h * 4);
+  float* partial = ws.take<float>(ln_bwd_scratch_floats(c.T, c.h) * 4);
   void* core_ws = ws.take<uint8_t>(0);
   const size_t core_bytes = tp_attn_core_workspace_size(c.T, c.s, c.h, c.n_heads);
 

@@ -166,6 +166,7 @@ uint32_t dropout_threshold(float p);
 cudaError_t launch_ln_fwd(const void* x, const float* g, const float* b, int64_t T, int64_t h, float eps,
                           void* y, float* mean, float* rstd, cudaStream_t st);
 int ln_bwd_blocks(int64_t T);
+size_t ln_bwd_scratch_floats(int64_t T, int64_t h);  // the backward's partial sums
 cudaError_t launch_ln_bwd(const void* dy, const void* x, const float* g, const float* mean,
                           const float* rstd, const void* dres, int64_t T, int64_t h, void* dx,
                           float* dg, float* db, int accumulate, float* partial, cudaStream_t st);
@@ -174,8 +175,8 @@ cudaError_t launch_dropout_add(const void* x, const void* res, int64_t n, uint64
 cudaError_t launch_pos_embed_dropout(const void* words, const void* pos_table, const int64_t* positions,
                                      int64_t T, int64_t h, int64_t max_pos, uint64_t seed, uint64_t stream,
                                      float p, void* out, cudaStream_t st);
-cudaError_t launch_attn_keep(int64_t pairs, int64_t s, int n_heads, int heads_per_shard, uint64_t seed,
-                             uint64_t stream0, float p, uint32_t* words, cudaStream_t st);
+cudaError_t launch_attn_keep(int64_t pairs, int64_t s, int n_heads, int heads_per_shard, int causal,
+                             uint64_t seed, uint64_t stream0, float p, uint32_t* words, cudaStream_t st);
 
 // Mixed-precision Adam step.  Parameter groups are cut into chunks of
 // opt_chunk_elems() elements; chunk c belongs to the last group whose

@@ -5,7 +5,7 @@
 //                        saving the row mean and 1/std;
 //   ln_bwd_kernel        its input gradient (plus an optional residual
 //                        gradient) and per-block partial gain/bias gradients;
-//   colsum_partials      the partials summed in block order (deterministic);
+//   colsum_level1/2      the partials summed in a fixed two-level order;
 //   dropout_add_kernel   out = res + x * keep / (1 - p) and its backward;
 //   pos_embed_dropout    (word + position embedding) with dropout;
 //   attn_keep_kernel     attention-dropout keep bits, 32 keys per word.
@@ -72,7 +72,33 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
   return t;
 }
 
-template <int kLnMaxPer>
+// Eight consecutive bf16 of a row as floats (one 16-byte load), and back.
+__device__ __forceinline__ void load8(const __nv_bfloat16* p, float* v) {
+  const uint4 q = *reinterpret_cast<const uint4*>(p);
+  const __nv_bfloat162* a = reinterpret_cast<const __nv_bfloat162*>(&q);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float2 f = __bfloat1622float2(a[k]);
+    v[2 * k] = f.x;
+    v[2 * k + 1] = f.y;
+  }
+}
+__device__ __forceinline__ void store8(__nv_bfloat16* p, const float* v) {
+  uint4 q;
+  __nv_bfloat162* a = reinterpret_cast<__nv_bfloat162*>(&q);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) a[k] = __floats2bfloat162_rn(v[2 * k], v[2 * k + 1]);
+  *reinterpret_cast<uint4*>(p) = q;
+}
+__device__ __forceinline__ void load8f(const float* p, float* v) {
+  const float4 a = *reinterpret_cast<const float4*>(p), b = *reinterpret_cast<const float4*>(p + 4);
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+  v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+
+// A thread owns PER values of a row in groups of eight consecutive columns:
+// group k covers columns 8 (k kLnThreads + tid) .. + 7 (h % 8 == 0).
+template <int PER>
 __global__ void __launch_bounds__(kLnThreads) ln_fwd_kernel(const __nv_bfloat16* __restrict__ x,
                                                             const float* __restrict__ g,
                                                             const float* __restrict__ b, int64_t h,
@@ -82,27 +108,43 @@ __global__ void __launch_bounds__(kLnThreads) ln_fwd_kernel(const __nv_bfloat16*
   __shared__ float red[kLnThreads / 32];
   const int64_t row = blockIdx.x;
   const __nv_bfloat16* xr = x + row * h;
-  float v[kLnMaxPer];
+  float v[PER];
   float s = 0.f;
 #pragma unroll
-  for (int i = 0; i < kLnMaxPer; ++i) {
-    const int64_t c = threadIdx.x + static_cast<int64_t>(i) * kLnThreads;
-    v[i] = c < h ? __bfloat162float(xr[c]) : 0.f;
-    s += v[i];
+  for (int k = 0; k < PER / 8; ++k) {
+    const int64_t c = (static_cast<int64_t>(k) * kLnThreads + threadIdx.x) * 8;
+    if (c < h) {
+      load8(xr + c, v + 8 * k);
+    } else {
+#pragma unroll
+      for (int t = 0; t < 8; ++t) v[8 * k + t] = 0.f;
+    }
+#pragma unroll
+    for (int t = 0; t < 8; ++t) s += v[8 * k + t];
   }
   const float mean = block_sum(s, red) / static_cast<float>(h);
   float q = 0.f;
 #pragma unroll
-  for (int i = 0; i < kLnMaxPer; ++i) {
-    const int64_t c = threadIdx.x + static_cast<int64_t>(i) * kLnThreads;
-    const float dlt = c < h ? v[i] - mean : 0.f;
-    q += dlt * dlt;
+  for (int k = 0; k < PER / 8; ++k) {
+    const int64_t c = (static_cast<int64_t>(k) * kLnThreads + threadIdx.x) * 8;
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+      const float dlt = c < h ? v[8 * k + t] - mean : 0.f;
+      q += dlt * dlt;
+    }
   }
   const float rstd = rsqrtf(block_sum(q, red) / static_cast<float>(h) + eps);
 #pragma unroll
-  for (int i = 0; i < kLnMaxPer; ++i) {
-    const int64_t c = threadIdx.x + static_cast<int64_t>(i) * kLnThreads;
-    if (c < h) y[row * h + c] = __float2bfloat16_rn((v[i] - mean) * rstd * g[c] + b[c]);
+  for (int k = 0; k < PER / 8; ++k) {
+    const int64_t c = (static_cast<int64_t>(k) * kLnThreads + threadIdx.x) * 8;
+    if (c < h) {
+      float gg[8], bb[8], o[8];
+      load8f(g + c, gg);
+      load8f(b + c, bb);
+#pragma unroll
+      for (int t = 0; t < 8; ++t) o[t] = (v[8 * k + t] - mean) * rstd * gg[t] + bb[t];
+      store8(y + row * h + c, o);
+    }
   }
   if (threadIdx.x == 0) {
     mean_out[row] = mean;
@@ -113,69 +155,109 @@ __global__ void __launch_bounds__(kLnThreads) ln_fwd_kernel(const __nv_bfloat16*
 // Rows [blockIdx.x * rows_per, ...): dx = rstd (dxhat - mean(dxhat) - xhat
 // mean(dxhat xhat)) (+ dres), dxhat = dy g; the block's rows' dy xhat and dy
 // summed per column into partial[blockIdx.x][0..h) and [h..2h).
-template <int kLnMaxPer>
+template <int PER>
 __global__ void __launch_bounds__(kLnThreads) ln_bwd_kernel(
     const __nv_bfloat16* __restrict__ dy, const __nv_bfloat16* __restrict__ x,
     const float* __restrict__ g, const float* __restrict__ mean_in, const float* __restrict__ rstd_in,
     const __nv_bfloat16* __restrict__ dres, int64_t T, int64_t h, int rows_per,
     __nv_bfloat16* __restrict__ dx, float* __restrict__ partial) {
   __shared__ float red[kLnThreads / 32];
-  float pg[kLnMaxPer], pb[kLnMaxPer];
+  float pg[PER], pb[PER], gg[PER];
 #pragma unroll
-  for (int i = 0; i < kLnMaxPer; ++i) pg[i] = pb[i] = 0.f;
+  for (int k = 0; k < PER / 8; ++k) {
+    const int64_t c = (static_cast<int64_t>(k) * kLnThreads + threadIdx.x) * 8;
+    if (c < h) {
+      load8f(g + c, gg + 8 * k);
+    } else {
+#pragma unroll
+      for (int t = 0; t < 8; ++t) gg[8 * k + t] = 0.f;
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < PER; ++i) pg[i] = pb[i] = 0.f;
   const int64_t r0 = static_cast<int64_t>(blockIdx.x) * rows_per;
   const int64_t r1 = min(T, r0 + rows_per);
   for (int64_t row = r0; row < r1; ++row) {
     const float mean = mean_in[row], rstd = rstd_in[row];
-    float xh[kLnMaxPer], dxh[kLnMaxPer];
+    float xh[PER], dxh[PER];
     float s1 = 0.f, s2 = 0.f;
 #pragma unroll
-    for (int i = 0; i < kLnMaxPer; ++i) {
-      const int64_t c = threadIdx.x + static_cast<int64_t>(i) * kLnThreads;
-      float d = 0.f, xv = 0.f, gv = 0.f;
+    for (int k = 0; k < PER / 8; ++k) {
+      const int64_t c = (static_cast<int64_t>(k) * kLnThreads + threadIdx.x) * 8;
+      float d[8], xv[8];
       if (c < h) {
-        d = __bfloat162float(dy[row * h + c]);
-        xv = (__bfloat162float(x[row * h + c]) - mean) * rstd;
-        gv = g[c];
+        load8(dy + row * h + c, d);
+        load8(x + row * h + c, xv);
+      } else {
+#pragma unroll
+        for (int t = 0; t < 8; ++t) d[t] = xv[t] = mean;
       }
-      xh[i] = xv;
-      dxh[i] = d * gv;
-      pg[i] += d * xv;
-      pb[i] += d;
-      s1 += dxh[i];
-      s2 += dxh[i] * xv;
+#pragma unroll
+      for (int t = 0; t < 8; ++t) {
+        const float xn = c < h ? (xv[t] - mean) * rstd : 0.f;
+        const float dd = c < h ? d[t] : 0.f;
+        xh[8 * k + t] = xn;
+        dxh[8 * k + t] = dd * gg[8 * k + t];
+        pg[8 * k + t] += dd * xn;
+        pb[8 * k + t] += dd;
+        s1 += dxh[8 * k + t];
+        s2 += dxh[8 * k + t] * xn;
+      }
     }
     const float m1 = block_sum(s1, red) / static_cast<float>(h);
     const float m2 = block_sum(s2, red) / static_cast<float>(h);
 #pragma unroll
-    for (int i = 0; i < kLnMaxPer; ++i) {
-      const int64_t c = threadIdx.x + static_cast<int64_t>(i) * kLnThreads;
+    for (int k = 0; k < PER / 8; ++k) {
+      const int64_t c = (static_cast<int64_t>(k) * kLnThreads + threadIdx.x) * 8;
       if (c < h) {
-        float o = rstd * (dxh[i] - m1 - xh[i] * m2);
-        if (dres) o += __bfloat162float(dres[row * h + c]);
-        dx[row * h + c] = __float2bfloat16_rn(o);
+        float o[8], r[8];
+        if (dres) {
+          load8(dres + row * h + c, r);
+        } else {
+#pragma unroll
+          for (int t = 0; t < 8; ++t) r[t] = 0.f;
+        }
+#pragma unroll
+        for (int t = 0; t < 8; ++t) o[t] = rstd * (dxh[8 * k + t] - m1 - xh[8 * k + t] * m2) + r[t];
+        store8(dx + row * h + c, o);
       }
     }
   }
   float* pp = partial + static_cast<int64_t>(blockIdx.x) * 2 * h;
 #pragma unroll
-  for (int i = 0; i < kLnMaxPer; ++i) {
-    const int64_t c = threadIdx.x + static_cast<int64_t>(i) * kLnThreads;
+  for (int k = 0; k < PER / 8; ++k) {
+    const int64_t c = (static_cast<int64_t>(k) * kLnThreads + threadIdx.x) * 8;
     if (c < h) {
-      pp[c] = pg[i];
-      pp[h + c] = pb[i];
+#pragma unroll
+      for (int t = 0; t < 8; ++t) {
+        pp[c + t] = pg[8 * k + t];
+        pp[h + c + t] = pb[8 * k + t];
+      }
     }
   }
 }
 
-// out[c] (+)= sum over blocks k in order of partial[k][c], c < n.
-__global__ void colsum_partials_kernel(const float* __restrict__ partial, int nblocks, int64_t n,
-                                       int64_t pitch, float* __restrict__ out, int accumulate) {
+// Column sums of partial rows in two fixed-order levels: block (x, y) sums
+// rows [32 y, 32 y + 32) of columns 256 x .. into part2[y]; the final kernel
+// sums the groups in order into out (+ out when accumulating).  n columns.
+constexpr int kColGroup = 32;
+__global__ void colsum_level1_kernel(const float* __restrict__ partial, int nrows, int64_t n,
+                                     float* __restrict__ part2) {
   const int64_t c = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (c >= n) return;
+  const int k0 = blockIdx.y * kColGroup, k1 = min(nrows, k0 + kColGroup);
   float s = 0.f;
-  for (int k = 0; k < nblocks; ++k) s += partial[static_cast<int64_t>(k) * pitch + c];
-  out[c] = accumulate ? out[c] + s : s;
+  for (int k = k0; k < k1; ++k) s += partial[static_cast<int64_t>(k) * n + c];
+  part2[static_cast<int64_t>(blockIdx.y) * n + c] = s;
+}
+__global__ void colsum_level2_kernel(const float* __restrict__ part2, int ngroups, int64_t h,
+                                     float* __restrict__ dg, float* __restrict__ db, int accumulate) {
+  const int64_t c = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (c >= 2 * h) return;
+  float s = 0.f;
+  for (int k = 0; k < ngroups; ++k) s += part2[static_cast<int64_t>(k) * 2 * h + c];
+  float* out = c < h ? dg + c : db + (c - h);
+  *out = accumulate ? *out + s : s;
 }
 
 // 16 elements per thread (one Philox block): out = res + x * keep * scale, or
@@ -187,7 +269,7 @@ __global__ void __launch_bounds__(256) dropout_add_kernel(const __nv_bfloat16* _
                                                           __nv_bfloat16* __restrict__ out) {
   const int64_t blk = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (blk >= nblk) return;
-  const uint32_t bits = keep16(static_cast<uint64_t>(blk), seed, stream, thr);
+  // the loads go out first; the Philox rounds run while they are in flight
   const uint4* x4 = reinterpret_cast<const uint4*>(x) + blk * 2;
   uint4 xv[2] = {x4[0], x4[1]};
   uint4 rv[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
@@ -196,6 +278,7 @@ __global__ void __launch_bounds__(256) dropout_add_kernel(const __nv_bfloat16* _
     rv[0] = r4[0];
     rv[1] = r4[1];
   }
+  const uint32_t bits = keep16(static_cast<uint64_t>(blk), seed, stream, thr);
   uint4 ov[2];
 #pragma unroll
   for (int q = 0; q < 2; ++q) {
@@ -224,15 +307,17 @@ __global__ void __launch_bounds__(256) pos_embed_dropout_kernel(
   const int64_t blk = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (blk >= nblk) return;
   const int64_t e = blk * 16, row = e / h, col = e - row * h;
-  const uint32_t bits = keep16(static_cast<uint64_t>(blk), seed, stream, thr);
   const uint4* w4 = reinterpret_cast<const uint4*>(words + e);
   const int64_t pos = positions[row];
   const bool pos_ok = pos >= 0 && pos < max_pos;  // a position outside the table adds zeros
   const uint4* p4 = reinterpret_cast<const uint4*>(pos_table + (pos_ok ? pos : 0) * h + col);
+  const uint4 wv2[2] = {w4[0], w4[1]};
+  const uint4 pv2[2] = {pos_ok ? p4[0] : make_uint4(0, 0, 0, 0), pos_ok ? p4[1] : make_uint4(0, 0, 0, 0)};
+  const uint32_t bits = keep16(static_cast<uint64_t>(blk), seed, stream, thr);
   uint4 ov[2];
 #pragma unroll
   for (int q = 0; q < 2; ++q) {
-    const uint4 wv = w4[q], pv = pos_ok ? p4[q] : make_uint4(0, 0, 0, 0);
+    const uint4 wv = wv2[q], pv = pv2[q];
     const __nv_bfloat162* wa = reinterpret_cast<const __nv_bfloat162*>(&wv);
     const __nv_bfloat162* pa = reinterpret_cast<const __nv_bfloat162*>(&pv);
     __nv_bfloat162* oa = reinterpret_cast<__nv_bfloat162*>(&ov[q]);
@@ -253,13 +338,17 @@ __global__ void __launch_bounds__(256) pos_embed_dropout_kernel(
 // 32 w .. 32 w + 31 of element block ((g s + q) s + 32 w) / 16 (s % 16 == 0);
 // pair g = sequence * heads + head draws from stream stream0 + shard(head).
 __global__ void __launch_bounds__(256) attn_keep_kernel(int64_t pairs, int64_t s, int wpr, int n_heads,
-                                                        int heads_per_shard, uint64_t seed,
+                                                        int heads_per_shard, int causal, uint64_t seed,
                                                         uint64_t stream0, uint32_t thr,
                                                         uint32_t* __restrict__ words) {
   const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t total = pairs * s * wpr;
   if (i >= total) return;
   const int64_t w = i % wpr, gq = i / wpr;  // gq = g * s + q
+  if (causal && 32 * w > gq % s) {  // every key of the word lies after the query: never read
+    words[i] = 0u;
+    return;
+  }
   const int64_t g = gq / s;
   const int j = static_cast<int>(g % n_heads);
   const uint64_t stream = stream0 + static_cast<uint64_t>(j / heads_per_shard);
@@ -276,9 +365,9 @@ uint32_t dropout_threshold(float p) {
   return t < 0 ? 0u : (t > 65536.0 ? 65536u : static_cast<uint32_t>(t));
 }
 
-// Values per thread for a row of h: the smallest of 4, 8, 16, 32 that covers it.
+// Values per thread for a row of h: the smallest of 8, 16, 32 that covers it.
 static int ln_per(int64_t h) {
-  for (int p = 4; p <= 32; p *= 2)
+  for (int p = 8; p <= 32; p *= 2)
     if (h <= static_cast<int64_t>(p) * kLnThreads) return p;
   return 0;
 }
@@ -290,7 +379,6 @@ cudaError_t launch_ln_fwd(const void* x, const float* g, const float* b, int64_t
   auto* yb = static_cast<__nv_bfloat16*>(y);
   const unsigned grid = static_cast<unsigned>(T);
   switch (ln_per(h)) {
-    case 4: ln_fwd_kernel<4><<<grid, kLnThreads, 0, st>>>(xb, g, b, h, eps, yb, mean, rstd); break;
     case 8: ln_fwd_kernel<8><<<grid, kLnThreads, 0, st>>>(xb, g, b, h, eps, yb, mean, rstd); break;
     case 16: ln_fwd_kernel<16><<<grid, kLnThreads, 0, st>>>(xb, g, b, h, eps, yb, mean, rstd); break;
     case 32: ln_fwd_kernel<32><<<grid, kLnThreads, 0, st>>>(xb, g, b, h, eps, yb, mean, rstd); break;
@@ -300,9 +388,13 @@ cudaError_t launch_ln_fwd(const void* x, const float* g, const float* b, int64_t
   return cudaGetLastError();
 }
 
-int ln_bwd_blocks(int64_t T) {
-  const int64_t rows_per = 16;
-  return static_cast<int>((T + rows_per - 1) / rows_per);
+constexpr int kLnBwdRows = 4;  // rows per block of the backward
+
+int ln_bwd_blocks(int64_t T) { return static_cast<int>((T + kLnBwdRows - 1) / kLnBwdRows); }
+
+size_t ln_bwd_scratch_floats(int64_t T, int64_t h) {
+  const int64_t nb = ln_bwd_blocks(T);
+  return static_cast<size_t>((nb + (nb + kColGroup - 1) / kColGroup) * 2 * h);
 }
 
 cudaError_t launch_ln_bwd(const void* dy, const void* x, const float* g, const float* mean,
@@ -314,18 +406,21 @@ cudaError_t launch_ln_bwd(const void* dy, const void* x, const float* g, const f
   const auto* xb = static_cast<const __nv_bfloat16*>(x);
   const auto* rb = static_cast<const __nv_bfloat16*>(dres);
   auto* dxb = static_cast<__nv_bfloat16*>(dx);
-#define TP_LNB(P) ln_bwd_kernel<P><<<nb, kLnThreads, 0, st>>>(dyb, xb, g, mean, rstd, rb, T, h, 16, dxb, partial)
+#define TP_LNB(P) \
+  ln_bwd_kernel<P><<<nb, kLnThreads, 0, st>>>(dyb, xb, g, mean, rstd, rb, T, h, kLnBwdRows, dxb, partial)
   switch (ln_per(h)) {
-    case 4: TP_LNB(4); break;
     case 8: TP_LNB(8); break;
     case 16: TP_LNB(16); break;
     case 32: TP_LNB(32); break;
     default: return cudaErrorInvalidValue;
   }
 #undef TP_LNB
-  const unsigned cb = static_cast<unsigned>((h + 255) / 256);
-  colsum_partials_kernel<<<cb, 256, 0, st>>>(partial, nb, h, 2 * h, dg, accumulate);
-  colsum_partials_kernel<<<cb, 256, 0, st>>>(partial + h, nb, h, 2 * h, db, accumulate);
+  const int ngroups = (nb + kColGroup - 1) / kColGroup;
+  float* part2 = partial + static_cast<int64_t>(nb) * 2 * h;
+  const dim3 g1(static_cast<unsigned>((2 * h + 255) / 256), static_cast<unsigned>(ngroups));
+  colsum_level1_kernel<<<g1, 256, 0, st>>>(partial, nb, 2 * h, part2);
+  colsum_level2_kernel<<<static_cast<unsigned>((2 * h + 255) / 256), 256, 0, st>>>(part2, ngroups, h, dg, db,
+                                                                                      accumulate);
   count_launches(3);
   return cudaGetLastError();
 }
@@ -353,13 +448,13 @@ cudaError_t launch_pos_embed_dropout(const void* words, const void* pos_table, c
   return cudaGetLastError();
 }
 
-cudaError_t launch_attn_keep(int64_t pairs, int64_t s, int n_heads, int heads_per_shard, uint64_t seed,
-                             uint64_t stream0, float p, uint32_t* words, cudaStream_t st) {
+cudaError_t launch_attn_keep(int64_t pairs, int64_t s, int n_heads, int heads_per_shard, int causal,
+                             uint64_t seed, uint64_t stream0, float p, uint32_t* words, cudaStream_t st) {
   const int wpr = static_cast<int>((s + 31) / 32);
   const int64_t total = pairs * s * wpr;
   if (total == 0) return cudaSuccess;
   attn_keep_kernel<<<static_cast<unsigned>((total + 255) / 256), 256, 0, st>>>(
-      pairs, s, wpr, n_heads, heads_per_shard, seed, stream0, dropout_threshold(p), words);
+      pairs, s, wpr, n_heads, heads_per_shard, causal, seed, stream0, dropout_threshold(p), words);
   count_launches(1);
   return cudaGetLastError();
 }
