@@ -3,9 +3,9 @@
 // parameters):
 //   ln_fwd_kernel        LayerNorm of bf16 rows with fp32 gain and bias,
 //                        saving the row mean and 1/std;
-//   ln_bwd_kernel        its input gradient (plus an optional residual
-//                        gradient) and per-block partial gain/bias gradients;
-//   colsum_level1/2      the partials summed in a fixed two-level order;
+//   ln_bwd_kernel        its input gradient (plus an optional residual gradient);
+//   ln_param_grad        gain and bias gradients over 16-row groups, then
+//   colsum_level2        the groups summed in order (deterministic);
 //   dropout_add_kernel   out = res + x * keep / (1 - p) and its backward;
 //   pos_embed_dropout    (word + position embedding) with dropout;
 //   attn_keep_kernel     attention-dropout keep bits, 32 keys per word.
@@ -152,109 +152,103 @@ __global__ void __launch_bounds__(kLnThreads) ln_fwd_kernel(const __nv_bfloat16*
   }
 }
 
-// Rows [blockIdx.x * rows_per, ...): dx = rstd (dxhat - mean(dxhat) - xhat
-// mean(dxhat xhat)) (+ dres), dxhat = dy g; the block's rows' dy xhat and dy
-// summed per column into partial[blockIdx.x][0..h) and [h..2h).
+// One row per block: dx = rstd (dxhat - mean(dxhat) - xhat mean(dxhat xhat))
+// (+ dres), dxhat = dy g.
 template <int PER>
 __global__ void __launch_bounds__(kLnThreads) ln_bwd_kernel(
     const __nv_bfloat16* __restrict__ dy, const __nv_bfloat16* __restrict__ x,
     const float* __restrict__ g, const float* __restrict__ mean_in, const float* __restrict__ rstd_in,
-    const __nv_bfloat16* __restrict__ dres, int64_t T, int64_t h, int rows_per,
-    __nv_bfloat16* __restrict__ dx, float* __restrict__ partial) {
+    const __nv_bfloat16* __restrict__ dres, int64_t h, __nv_bfloat16* __restrict__ dx) {
   __shared__ float red[kLnThreads / 32];
-  float pg[PER], pb[PER], gg[PER];
+  const int64_t row = blockIdx.x;
+  const float mean = mean_in[row], rstd = rstd_in[row];
+  float xh[PER], dxh[PER];
+  float s1 = 0.f, s2 = 0.f;
 #pragma unroll
   for (int k = 0; k < PER / 8; ++k) {
     const int64_t c = (static_cast<int64_t>(k) * kLnThreads + threadIdx.x) * 8;
+    float d[8], xv[8], gg[8];
     if (c < h) {
-      load8f(g + c, gg + 8 * k);
+      load8(dy + row * h + c, d);
+      load8(x + row * h + c, xv);
+      load8f(g + c, gg);
     } else {
 #pragma unroll
-      for (int t = 0; t < 8; ++t) gg[8 * k + t] = 0.f;
+      for (int t = 0; t < 8; ++t) d[t] = xv[t] = gg[t] = 0.f;
+    }
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+      const float xn = c < h ? (xv[t] - mean) * rstd : 0.f;
+      xh[8 * k + t] = xn;
+      dxh[8 * k + t] = d[t] * gg[t];
+      s1 += dxh[8 * k + t];
+      s2 += dxh[8 * k + t] * xn;
     }
   }
-#pragma unroll
-  for (int i = 0; i < PER; ++i) pg[i] = pb[i] = 0.f;
-  const int64_t r0 = static_cast<int64_t>(blockIdx.x) * rows_per;
-  const int64_t r1 = min(T, r0 + rows_per);
-  for (int64_t row = r0; row < r1; ++row) {
-    const float mean = mean_in[row], rstd = rstd_in[row];
-    float xh[PER], dxh[PER];
-    float s1 = 0.f, s2 = 0.f;
-#pragma unroll
-    for (int k = 0; k < PER / 8; ++k) {
-      const int64_t c = (static_cast<int64_t>(k) * kLnThreads + threadIdx.x) * 8;
-      float d[8], xv[8];
-      if (c < h) {
-        load8(dy + row * h + c, d);
-        load8(x + row * h + c, xv);
-      } else {
-#pragma unroll
-        for (int t = 0; t < 8; ++t) d[t] = xv[t] = mean;
-      }
-#pragma unroll
-      for (int t = 0; t < 8; ++t) {
-        const float xn = c < h ? (xv[t] - mean) * rstd : 0.f;
-        const float dd = c < h ? d[t] : 0.f;
-        xh[8 * k + t] = xn;
-        dxh[8 * k + t] = dd * gg[8 * k + t];
-        pg[8 * k + t] += dd * xn;
-        pb[8 * k + t] += dd;
-        s1 += dxh[8 * k + t];
-        s2 += dxh[8 * k + t] * xn;
-      }
-    }
-    const float m1 = block_sum(s1, red) / static_cast<float>(h);
-    const float m2 = block_sum(s2, red) / static_cast<float>(h);
-#pragma unroll
-    for (int k = 0; k < PER / 8; ++k) {
-      const int64_t c = (static_cast<int64_t>(k) * kLnThreads + threadIdx.x) * 8;
-      if (c < h) {
-        float o[8], r[8];
-        if (dres) {
-          load8(dres + row * h + c, r);
-        } else {
-#pragma unroll
-          for (int t = 0; t < 8; ++t) r[t] = 0.f;
-        }
-#pragma unroll
-        for (int t = 0; t < 8; ++t) o[t] = rstd * (dxh[8 * k + t] - m1 - xh[8 * k + t] * m2) + r[t];
-        store8(dx + row * h + c, o);
-      }
-    }
-  }
-  float* pp = partial + static_cast<int64_t>(blockIdx.x) * 2 * h;
+  const float m1 = block_sum(s1, red) / static_cast<float>(h);
+  const float m2 = block_sum(s2, red) / static_cast<float>(h);
 #pragma unroll
   for (int k = 0; k < PER / 8; ++k) {
     const int64_t c = (static_cast<int64_t>(k) * kLnThreads + threadIdx.x) * 8;
     if (c < h) {
+      float o[8], r[8];
+      if (dres) {
+        load8(dres + row * h + c, r);
+      } else {
 #pragma unroll
-      for (int t = 0; t < 8; ++t) {
-        pp[c + t] = pg[8 * k + t];
-        pp[h + c + t] = pb[8 * k + t];
+        for (int t = 0; t < 8; ++t) r[t] = 0.f;
       }
+#pragma unroll
+      for (int t = 0; t < 8; ++t) o[t] = rstd * (dxh[8 * k + t] - m1 - xh[8 * k + t] * m2) + r[t];
+      store8(dx + row * h + c, o);
     }
   }
 }
 
-// Column sums of partial rows in two fixed-order levels: block (x, y) sums
-// rows [32 y, 32 y + 32) of columns 256 x .. into part2[y]; the final kernel
-// sums the groups in order into out (+ out when accumulating).  n columns.
-constexpr int kColGroup = 32;
-__global__ void colsum_level1_kernel(const float* __restrict__ partial, int nrows, int64_t n,
-                                     float* __restrict__ part2) {
-  const int64_t c = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (c >= n) return;
-  const int k0 = blockIdx.y * kColGroup, k1 = min(nrows, k0 + kColGroup);
-  float s = 0.f;
-  for (int k = k0; k < k1; ++k) s += partial[static_cast<int64_t>(k) * n + c];
-  part2[static_cast<int64_t>(blockIdx.y) * n + c] = s;
+// Gain and bias gradients, first level: block (x, y) sums dy xhat and dy over
+// rows [16 y, 16 (y + 1)) for eight columns per thread,
+// columns 8 (256 x + tid) ..; rows in order.  partial[y][0..h) = dg part,
+// partial[y][h..2h) = db part.
+constexpr int kLnColRows = 16;
+__global__ void __launch_bounds__(256) ln_param_grad_kernel(
+    const __nv_bfloat16* __restrict__ dy, const __nv_bfloat16* __restrict__ x,
+    const float* __restrict__ mean_in, const float* __restrict__ rstd_in, int64_t T, int64_t h,
+    float* __restrict__ partial) {
+  const int64_t c = (static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x) * 8;
+  if (c >= h) return;
+  const int64_t r0 = static_cast<int64_t>(blockIdx.y) * kLnColRows;
+  const int64_t r1 = min(T, r0 + kLnColRows);
+  float ag[8], ab[8];
+#pragma unroll
+  for (int t = 0; t < 8; ++t) ag[t] = ab[t] = 0.f;
+#pragma unroll 4
+  for (int64_t r = r0; r < r1; ++r) {
+    float d[8], xv[8];
+    load8(dy + r * h + c, d);
+    load8(x + r * h + c, xv);
+    const float mean = mean_in[r], rstd = rstd_in[r];
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+      ag[t] += d[t] * ((xv[t] - mean) * rstd);
+      ab[t] += d[t];
+    }
+  }
+  float* pp = partial + static_cast<int64_t>(blockIdx.y) * 2 * h;
+#pragma unroll
+  for (int t = 0; t < 8; ++t) {
+    pp[c + t] = ag[t];
+    pp[h + c + t] = ab[t];
+  }
 }
+
+// Second level: the groups' partials summed in order into dg and db (+ the
+// existing values when accumulating); 2h columns.
 __global__ void colsum_level2_kernel(const float* __restrict__ part2, int ngroups, int64_t h,
                                      float* __restrict__ dg, float* __restrict__ db, int accumulate) {
   const int64_t c = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (c >= 2 * h) return;
   float s = 0.f;
+#pragma unroll 8
   for (int k = 0; k < ngroups; ++k) s += part2[static_cast<int64_t>(k) * 2 * h + c];
   float* out = c < h ? dg + c : db + (c - h);
   *out = accumulate ? *out + s : s;
@@ -388,26 +382,22 @@ cudaError_t launch_ln_fwd(const void* x, const float* g, const float* b, int64_t
   return cudaGetLastError();
 }
 
-constexpr int kLnBwdRows = 4;  // rows per block of the backward
-
-int ln_bwd_blocks(int64_t T) { return static_cast<int>((T + kLnBwdRows - 1) / kLnBwdRows); }
+int ln_bwd_blocks(int64_t T) { return static_cast<int>((T + kLnColRows - 1) / kLnColRows); }
 
 size_t ln_bwd_scratch_floats(int64_t T, int64_t h) {
-  const int64_t nb = ln_bwd_blocks(T);
-  return static_cast<size_t>((nb + (nb + kColGroup - 1) / kColGroup) * 2 * h);
+  return static_cast<size_t>(ln_bwd_blocks(T)) * 2 * static_cast<size_t>(h);
 }
 
 cudaError_t launch_ln_bwd(const void* dy, const void* x, const float* g, const float* mean,
                           const float* rstd, const void* dres, int64_t T, int64_t h, void* dx,
                           float* dg, float* db, int accumulate, float* partial, cudaStream_t st) {
   if (T == 0) return cudaSuccess;
-  const int nb = ln_bwd_blocks(T);
   const auto* dyb = static_cast<const __nv_bfloat16*>(dy);
   const auto* xb = static_cast<const __nv_bfloat16*>(x);
   const auto* rb = static_cast<const __nv_bfloat16*>(dres);
   auto* dxb = static_cast<__nv_bfloat16*>(dx);
-#define TP_LNB(P) \
-  ln_bwd_kernel<P><<<nb, kLnThreads, 0, st>>>(dyb, xb, g, mean, rstd, rb, T, h, kLnBwdRows, dxb, partial)
+  const unsigned grid = static_cast<unsigned>(T);
+#define TP_LNB(P) ln_bwd_kernel<P><<<grid, kLnThreads, 0, st>>>(dyb, xb, g, mean, rstd, rb, h, dxb)
   switch (ln_per(h)) {
     case 8: TP_LNB(8); break;
     case 16: TP_LNB(16); break;
@@ -415,11 +405,10 @@ cudaError_t launch_ln_bwd(const void* dy, const void* x, const float* g, const f
     default: return cudaErrorInvalidValue;
   }
 #undef TP_LNB
-  const int ngroups = (nb + kColGroup - 1) / kColGroup;
-  float* part2 = partial + static_cast<int64_t>(nb) * 2 * h;
-  const dim3 g1(static_cast<unsigned>((2 * h + 255) / 256), static_cast<unsigned>(ngroups));
-  colsum_level1_kernel<<<g1, 256, 0, st>>>(partial, nb, 2 * h, part2);
-  colsum_level2_kernel<<<static_cast<unsigned>((2 * h + 255) / 256), 256, 0, st>>>(part2, ngroups, h, dg, db,
+  const int ngroups = ln_bwd_blocks(T);
+  const dim3 g1(static_cast<unsigned>((h / 8 + 255) / 256), static_cast<unsigned>(ngroups));
+  ln_param_grad_kernel<<<g1, 256, 0, st>>>(dyb, xb, mean, rstd, T, h, partial);
+  colsum_level2_kernel<<<static_cast<unsigned>((2 * h + 255) / 256), 256, 0, st>>>(partial, ngroups, h, dg, db,
                                                                                       accumulate);
   count_launches(3);
   return cudaGetLastError();
