@@ -183,3 +183,62 @@ def test_layer_b1_s2048_h4096_heads8_hp16384_N8_full():
     every output and gradient against the oracle."""
     cfg = SI.WORKLOADS["layer_b1_s2048_h4096_heads8_hp16384_N8"]
     check_layer(cfg, SI.layer_inputs(cfg))
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_attn_core_dropout_non_causal_both_kernels(mode):
+    tp = _tp()
+    b, s, h, H, N, p, seed, layer = 1, 512, 512, 4, 4, 0.3, 5, 1
+    T = b * s
+    QKV = SI.normal(23, 1, (T, 3 * h), 1.0, "bf16")
+    dC = SI.normal(23, 2, (T, h), 1.0, "bf16")
+    P = torch.empty(b, H, s, s, dtype=torch.bfloat16, device="cuda")
+    Pd, C = torch.empty_like(P), torch.empty(T, h, dtype=torch.bfloat16, device="cuda")
+    dQKV = torch.empty(T, 3 * h, dtype=torch.bfloat16, device="cuda")
+    ws = torch.empty(tp.tp_attn_core_workspace_size(T, s, h, H), dtype=torch.uint8, device="cuda")
+    tp.tp_debug_set_gemm_kernel(mode)
+    try:
+        tp.tp_attn_core_dropout_fwd(QKV.cuda(), s, H, N, False, p, seed, tp.layer_stream(layer, 0), P, Pd, C,
+                                    None, ws)
+        tp.tp_attn_core_dropout_bwd(QKV.cuda(), P, Pd, C, dC.cuda(), s, H, N, False, p, seed,
+                                    tp.layer_stream(layer, 0), dQKV, ws)
+        assert tp.tp_get_status() == tp.TP_OK
+    finally:
+        tp.tp_debug_set_gemm_kernel(2)
+    Qn = f64(QKV)
+    rC, rP = O.attention_core(Qn, s, H, N, False, f32p(p), seed, layer)
+    assert_close(C, rC, "bf16", "C")
+    rd = O.attention_core_grad(Qn, rP, f64(dC), s, H, N, f32p(p), seed, layer)
+    assert_close(dQKV, rd, "bf16", "dQKV")
+    Pdn = Pd.float().cpu().numpy()
+    for j in range(H):
+        assert np.array_equal(Pdn[0, j] != 0, O.attention_keep(0, j, s, H, N, f32p(p), seed, layer))
+
+
+def test_layer_one_head_per_shard_three_sequences():
+    cfg = dict(SMALL, n_heads=8, N=8, s=64, h=512, hp=1024, layer=5)
+    check_layer(cfg, SI.layer_inputs(dict(cfg, b=3)))
+
+
+def test_layer_gradients_accumulate():
+    tp = _tp()
+    cfg = dict(SMALL, s=64)
+    inp = SI.layer_inputs(dict(cfg, b=1))
+    out, saved, dx, grads = run_layer(cfg, inp)
+    # run the backward again adding into the same gradient buffers: every gradient doubles
+    c = dict(cfg, T=inp["T"])
+    d = lambda t: t.cuda().contiguous()
+    params = dict(g1=d(inp["g1"]), b1=d(inp["b1"]), g2=d(inp["g2"]), b2=d(inp["b2"]),
+                  Wqkv=[d(t) for t in inp["Wqkv"]], bqkv=[d(t) for t in inp["bqkv"]],
+                  Wo=[d(t) for t in inp["Wo"]], bo=d(inp["bo"]), W=[d(t) for t in inp["W"]],
+                  a=[d(t) for t in inp["a"]], U=[d(t) for t in inp["U"]], b=d(inp["b"]))
+    before = {k: ([t.clone() for t in v] if isinstance(v, list) else v.clone()) for k, v in grads.items()}
+    ws = torch.empty(tp.tp_transformer_layer_workspace_size(c), dtype=torch.uint8, device="cuda")
+    dx2 = torch.empty_like(dx)
+    tp.tp_transformer_layer_bwd(c, params, d(inp["x"]), saved, d(inp["dout"]), dx2, grads, ws, accumulate=True)
+    assert tp.tp_get_status() == tp.TP_OK
+    assert torch.equal(dx, dx2)
+    for k, v in grads.items():
+        pairs = zip(v, before[k]) if isinstance(v, list) else [(v, before[k])]
+        for a, b in pairs:
+            assert torch.allclose(a, 2 * b, rtol=1e-5, atol=1e-6), k

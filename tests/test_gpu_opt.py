@@ -228,3 +228,9 @@ def test_adam_layer_H4096_full():
     updated, norm, ref, ref_state = O.mixed_precision_adam_step(oracle_groups(groups), state, hyper)
     assert updated and st["grad_norm"] > hyper["max_norm"]
     check_against(dev, groups, ref, ref_state, norm, st, updated)
+
+
+def test_adam_sixty_four_groups():
+    sizes = [(i * 997) % 5000 + 1 for i in range(64)]
+    groups = make_groups(sizes)
+    run_and_check(groups, STATE, HYPER, with_model=[i % 2 == 0 for i in range(64)])
