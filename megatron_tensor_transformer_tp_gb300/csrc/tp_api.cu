@@ -201,6 +201,21 @@ bool encode_map_mn3d(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// An output (rows x cols, row pitch ld elements, bf16 or fp32) as a 2D map for
+// the epilogue's bulk tensor stores: one box is a 32-row chunk of 64-byte
+// rows (32 bf16 or 16 fp32 columns) in the 64-byte swizzle of the stage.
+bool encode_store_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols, int64_t ld, bool f32) {
+  const int es = f32 ? 4 : 2;
+  cuuint64_t gdim[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t gstride[1] = {static_cast<cuuint64_t>(ld) * es};
+  cuuint32_t box[2] = {f32 ? 16u : 32u, 32u};
+  cuuint32_t estr[2] = {1, 1};
+  return g_encode(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                  const_cast<void*>(ptr), gdim, gstride, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // ---------------------------------------------------------------------------
 // GEMM planning
 // ---------------------------------------------------------------------------
@@ -260,6 +275,8 @@ struct Plan {
     g.prod_row = -1;
     g.prod_col = -1;
     g.alpha = 1.f;
+    g.out_map = -1;
+    g.out2_map = -1;
     return g;
   }
   // Counter block for row- or column-tile completion of producing groups.
@@ -447,6 +464,40 @@ tp_status launch_tc_groups(const Plan& pl, const bool* used, GemmGroup* groups, 
         tiles += std::min(g.tiles_n, (mt * rows_per_tile + rows_per_tile - 1) / g.bn + 1);
     } else {
       tiles += g.tiles_m * g.tiles_n;
+    }
+  }
+  // Bulk tensor-store maps for the bf16 outputs the epilogue stores whole
+  // (16-byte aligned rows), as long as map slots last.
+  int nmaps = 0;
+  for (int i = 0; i < ng; ++i) {
+    GemmGroup& g = groups[i];
+    g.out_map = g.out2_map = -1;
+    if (!g.vec_ok || g.out == nullptr || g.k_empty) continue;
+    const bool f32 = g.out_type == OUT_F32;
+    bool ok = false;
+    switch (g.epi) {
+      case EPI_STORE: case EPI_BIAS_GELU: case EPI_DGELU: case EPI_CE_BWD: case EPI_SOFTMAX:
+      case EPI_SMAX_BWD:
+        ok = true;
+        break;
+      case EPI_F32: case EPI_SEGSUM:
+        ok = !g.accumulate;
+        break;
+      default:
+        break;
+    }
+    // the stores of these epilogues are bf16 whatever out_type says
+    const bool out_f32 = f32 && !(g.epi == EPI_CE_BWD || g.epi == EPI_SOFTMAX || g.epi == EPI_SMAX_BWD);
+    // fp32 outputs keep the lanes' stores: their two 64-byte halves per chunk
+    // would wait on each other's bulk read (measured slower on the backward)
+    if (!ok || out_f32) continue;
+    const bool two = g.out2 != nullptr && (g.epi == EPI_BIAS_GELU || g.epi == EPI_SOFTMAX);
+    if (nmaps + (two ? 2 : 1) > kMaxStoreMaps) break;
+    if (!encode_store_map(&p.mapO[nmaps], g.out, g.M, g.N, g.ldo, out_f32)) continue;
+    g.out_map = nmaps++;
+    if (two) {
+      if (encode_store_map(&p.mapO[nmaps], g.out2, g.M, g.N, g.ldo, out_f32)) g.out2_map = nmaps++;
+      else g.out_map = -1, --nmaps;
     }
   }
   // one count per producer tile (one-SM kernel), one per epilogue warp and CTA (two-SM kernel)

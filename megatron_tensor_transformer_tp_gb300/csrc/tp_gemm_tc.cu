@@ -377,8 +377,63 @@ __device__ __forceinline__ void load_bf16_chunk(const __nv_bfloat16* src, float*
 // so each global access instruction of the warp covers whole 64-byte (bf16)
 // or 128-byte (fp32) row segments instead of 32 half-filled sectors.
 // ---------------------------------------------------------------------------
+// The warp's stage may still be read by its last bulk tensor store: lane 0
+// waits for those reads, then the warp may write it again.
+__device__ __forceinline__ void stage_acquire(int lane) {
+  if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+  __syncwarp();
+}
+__device__ __forceinline__ void tma_store_2d(uint64_t map, uint32_t src, int c0, int c1) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(map),
+               "r"(src), "r"(c0), "r"(c1)
+               : "memory");
+}
+// Stores a 32 x 32 chunk (rows row0.., columns n..).  With a store map the
+// chunk goes out as bulk tensor stores from the stage (its 64-byte rows in
+// the 64-byte swizzle the map expects; rows and columns past the matrix are
+// clipped by the copy); otherwise the lanes store the stage's rows.
 __device__ __forceinline__ void stage_store_rows(uint4* st, void* base, int out_type, int64_t ld,
-                                                 int row0, int M, int n, const float* v, int lane) {
+                                                 int row0, int M, int n, const float* v, int lane,
+                                                 uint64_t map) {
+  stage_acquire(lane);
+  if (map != 0) {
+    const uint32_t sbase = smem_addr(st);
+    if (out_type == OUT_BF16) {
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint4 w;
+        w.x = pack_bf16x2(v[8 * c + 0], v[8 * c + 1]);
+        w.y = pack_bf16x2(v[8 * c + 2], v[8 * c + 3]);
+        w.z = pack_bf16x2(v[8 * c + 4], v[8 * c + 5]);
+        w.w = pack_bf16x2(v[8 * c + 6], v[8 * c + 7]);
+        st[lane * 4 + (c ^ ((lane >> 1) & 3))] = w;
+      }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_2d(map, sbase, n, row0);
+        asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+      }
+    } else {
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        if (hh == 1) stage_acquire(lane);
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          st[lane * 4 + (c ^ ((lane >> 1) & 3))] =
+              make_uint4(__float_as_uint(v[16 * hh + 4 * c + 0]), __float_as_uint(v[16 * hh + 4 * c + 1]),
+                         __float_as_uint(v[16 * hh + 4 * c + 2]), __float_as_uint(v[16 * hh + 4 * c + 3]));
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_2d(map, sbase, n + 16 * hh, row0);
+          asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+        }
+      }
+    }
+    __syncwarp();
+    return;
+  }
   if (out_type == OUT_BF16) {
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
@@ -424,6 +479,7 @@ __device__ __forceinline__ void stage_store_rows(uint4* st, void* base, int out_
 
 __device__ __forceinline__ void stage_load_rows_bf16(uint4* st, const void* base, int64_t ld,
                                                      int row0, int M, int n, float* z, int lane) {
+  stage_acquire(lane);
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const int r = i * 8 + (lane >> 2), c = lane & 3;
@@ -447,6 +503,7 @@ __device__ __forceinline__ void stage_load_rows_bf16(uint4* st, const void* base
 
 __device__ __forceinline__ void stage_add_rows_f32(uint4* st, const void* base, int64_t ld, int row0,
                                                    int M, int n, float* v, int lane) {
+  stage_acquire(lane);
 #pragma unroll
   for (int hh = 0; hh < 2; ++hh) {
 #pragma unroll
@@ -484,8 +541,11 @@ __device__ __forceinline__ void prefetch_bias(const GemmGroup& G, int n, int lan
 // columns n .. n+31.  Called by all 32 lanes of the warp (the staged paths
 // are warp-collective); rows >= M are computed but never stored.
 template <bool ATTN>
-__device__ __forceinline__ void epilogue_chunk(const GemmGroup& G, uint4* st, int lane, int row0,
-                                               int n, float* v) {
+__device__ __forceinline__ void epilogue_chunk(const GemmGroup& G, const CUtensorMap* mapO, uint4* st,
+                                               int lane, int row0, int n, float* v) {
+  // bulk-store maps of the group's outputs (0: the lanes store)
+  const uint64_t map1 = G.out_map >= 0 ? reinterpret_cast<uint64_t>(mapO + G.out_map) : 0ull;
+  const uint64_t map2 = G.out2_map >= 0 ? reinterpret_cast<uint64_t>(mapO + G.out2_map) : 0ull;
   const int row = row0 + lane;
   const bool row_ok = row < G.M;
   const int ncols = min(32, G.N - n);
@@ -500,7 +560,7 @@ __device__ __forceinline__ void epilogue_chunk(const GemmGroup& G, uint4* st, in
 #pragma unroll
       for (int j = 0; j < 32; ++j) v[j] = j <= jmax ? ex2_ftz(fmaf(v[j], a, base)) : 0.f;
       if (coal) {
-        stage_store_rows(st, G.out, OUT_BF16, G.ldo, row0, G.M, n, v, lane);
+        stage_store_rows(st, G.out, OUT_BF16, G.ldo, row0, G.M, n, v, lane, map1);
       } else if (row_ok) {
         store_chunk(G.out, OUT_BF16, G.ldo, row, n, v, ncols, false);
       }
@@ -510,7 +570,7 @@ __device__ __forceinline__ void epilogue_chunk(const GemmGroup& G, uint4* st, in
 #pragma unroll
         for (int j = 0; j < 32; ++j) v[j] = (keep >> j) & 1u ? v[j] * G.drop_scale : 0.f;
         if (coal) {
-          stage_store_rows(st, G.out2, OUT_BF16, G.ldo, row0, G.M, n, v, lane);
+          stage_store_rows(st, G.out2, OUT_BF16, G.ldo, row0, G.M, n, v, lane, map2);
         } else if (row_ok) {
           store_chunk(G.out2, OUT_BF16, G.ldo, row, n, v, ncols, false);
         }
@@ -540,7 +600,7 @@ __device__ __forceinline__ void epilogue_chunk(const GemmGroup& G, uint4* st, in
 #pragma unroll
       for (int j = 0; j < 32; ++j) v[j] = z[j] * (v[j] - dd) * G.alpha;
       if (coal) {
-        stage_store_rows(st, G.out, OUT_BF16, G.ldo, row0, G.M, n, v, lane);
+        stage_store_rows(st, G.out, OUT_BF16, G.ldo, row0, G.M, n, v, lane, map1);
       } else if (row_ok) {
         store_chunk(G.out, OUT_BF16, G.ldo, row, n, v, ncols, false);
       }
@@ -558,7 +618,7 @@ __device__ __forceinline__ void epilogue_chunk(const GemmGroup& G, uint4* st, in
         for (int j = 0; j < 32; ++j) v[j] += b[j];
       }
       if (coal) {
-        stage_store_rows(st, G.out, G.out_type, G.ldo, row0, G.M, n, v, lane);
+        stage_store_rows(st, G.out, G.out_type, G.ldo, row0, G.M, n, v, lane, map1);
       } else if (row_ok) {
         store_chunk(G.out, G.out_type, G.ldo, row, n, v, ncols, false);
       }
@@ -566,7 +626,7 @@ __device__ __forceinline__ void epilogue_chunk(const GemmGroup& G, uint4* st, in
 #pragma unroll
         for (int j = 0; j < 32; ++j) v[j] = gelu_f(v[j]);
         if (coal) {
-          stage_store_rows(st, G.out2, G.out_type, G.ldo, row0, G.M, n, v, lane);
+          stage_store_rows(st, G.out2, G.out_type, G.ldo, row0, G.M, n, v, lane, map2);
         } else if (row_ok) {
           store_chunk(G.out2, G.out_type, G.ldo, row, n, v, ncols, false);
         }
@@ -588,7 +648,7 @@ __device__ __forceinline__ void epilogue_chunk(const GemmGroup& G, uint4* st, in
 #pragma unroll
       for (int j = 0; j < 32; ++j) v[j] *= gelu_grad_f(z[j]);
       if (coal) {
-        stage_store_rows(st, G.out, G.out_type, G.ldo, row0, G.M, n, v, lane);
+        stage_store_rows(st, G.out, G.out_type, G.ldo, row0, G.M, n, v, lane, map1);
       } else if (row_ok) {
         store_chunk(G.out, G.out_type, G.ldo, row, n, v, ncols, false);
       }
@@ -613,7 +673,7 @@ __device__ __forceinline__ void epilogue_chunk(const GemmGroup& G, uint4* st, in
         v[j] = pj * dl;
       }
       if (coal) {
-        stage_store_rows(st, G.out, OUT_BF16, G.ldo, row0, G.M, n, v, lane);
+        stage_store_rows(st, G.out, OUT_BF16, G.ldo, row0, G.M, n, v, lane, map1);
       } else if (row_ok) {
         store_chunk(G.out, OUT_BF16, G.ldo, row, n, v, ncols, false);
       }
@@ -648,7 +708,7 @@ __device__ __forceinline__ void epilogue_chunk(const GemmGroup& G, uint4* st, in
       }
       if (coal) {
         if (G.accumulate) stage_add_rows_f32(st, G.out, G.ldo, row0, G.M, n, v, lane);
-        stage_store_rows(st, G.out, OUT_F32, G.ldo, row0, G.M, n, v, lane);
+        stage_store_rows(st, G.out, OUT_F32, G.ldo, row0, G.M, n, v, lane, map1);
       } else if (row_ok) {
         float* o = static_cast<float*>(G.out) + static_cast<int64_t>(row) * G.ldo + n;
         if (G.accumulate) {
@@ -1060,9 +1120,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
 #pragma unroll
           for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(rr[j]);
         }
-        epilogue_chunk<ATTN>(G, epi_stage, lane, row0, n, v);
+        epilogue_chunk<ATTN>(G, p.mapO, epi_stage, lane, row0, n, v);
       }
       tc_fence_before();
+      if (G.prod_row >= 0 || G.prod_col >= 0) {
+        // dependants read this tile: its bulk stores complete before the warp arrives
+        if (lane == 0) {
+          asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+          asm volatile("fence.proxy.async.global;" ::: "memory");
+        }
+      }
       __syncwarp();
       if (lane == 0) mbar_arrive(tempty_bar(buf));
       if ((G.prod_row >= 0 || G.prod_col >= 0) && warp == 2 + lt % NUM_EPI_WARPS) {
@@ -1083,6 +1150,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
     }
   }
 
+  // every bulk tensor store of the epilogue has finished before the CTA exits
+  if (warp >= 2 && lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -1574,10 +1643,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_pair_kernel(const __gr
 #pragma unroll
           for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(rr[j]);
         }
-        epilogue_chunk<ATTN>(G, epi_stage, lane, row0, n, v);
+        epilogue_chunk<ATTN>(G, p.mapO, epi_stage, lane, row0, n, v);
       }
       tc_fence_before();
       if (G.prod_row >= 0 || G.prod_col >= 0) {
+        if (lane == 0) {
+          asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+          asm volatile("fence.proxy.async.global;" ::: "memory");
+        }
         __threadfence();
         __syncwarp();
         if (lane == 0) {
@@ -1593,6 +1666,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_pair_kernel(const __gr
     }
   }
 
+  // every bulk tensor store of the epilogue has finished before the CTA exits
+  if (warp >= 2 && lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
   tc_fence_before();
   __syncthreads();
   cluster_sync_all();  // no CTA touches the other's shared memory after this

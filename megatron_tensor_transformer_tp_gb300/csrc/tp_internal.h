@@ -96,6 +96,9 @@ struct GemmGroup {
   const uint32_t* drop_mask;
   int drop_wpr;
   float drop_scale;
+  // Bulk tensor-store maps of out / out2 in TcGemmParams::mapO, or -1 (set by
+  // the launcher; the epilogue then stores through the TMA).
+  int out_map, out2_map;
 };
 
 // One operand pair of the tensor-core engine.  Operands are bf16.
@@ -110,9 +113,12 @@ struct TcSeg {
   int pad;
 };
 
+constexpr int kMaxStoreMaps = 48;  // output maps of one launch (more outputs store without the TMA)
+
 struct TcGemmParams {
   CUtensorMap mapA[kMaxSegs];
   CUtensorMap mapB[kMaxSegs];
+  CUtensorMap mapO[kMaxStoreMaps];
   TcSeg seg[kMaxSegs];
   GemmGroup grp[kMaxGroups];
   int num_groups, num_segs, total_tiles;
