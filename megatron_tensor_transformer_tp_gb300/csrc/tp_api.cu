@@ -332,7 +332,7 @@ void set_dep_targets(GemmGroup* groups, int ng, int epi_parts, int halves) {
 
 tp_status launch_simt_groups(const Plan& pl, const GemmGroup* groups, int ng, const DeviceState* dev,
                              const char* name, cudaStream_t s) {
-  static SimtGemmParams p;
+  static thread_local SimtGemmParams p;
   memset(&p, 0, sizeof(p));
   for (int i = 0; i < pl.ns; ++i) {
     const Plan::Seg& S = pl.seg[i];
@@ -410,7 +410,7 @@ tp_status launch_tc_groups(const Plan& pl, const bool* used, GemmGroup* groups, 
       groups[j + 1] = g;
     }
   }
-  static TcGemmParams p;
+  static thread_local TcGemmParams p;  // per host thread: calls from several threads do not share it
   memset(&p, 0, sizeof(p));
   for (int i = 0; i < pl.ns; ++i) {
     const Plan::Seg& S = pl.seg[i];
