@@ -34,6 +34,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "tp_device.cuh"
 #include "tp_internal.h"
 
@@ -1693,7 +1695,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_pair_kernel(const __gr
 cudaError_t launch_tc_gemm(const TcGemmParams& p_in, int num_sms, cudaStream_t s) {
   static bool attr_set = false;
   static int max_clusters = 0;
-  static unsigned slot_seq = 0;
+  static std::atomic<unsigned> slot_seq{0};  // launch slots rotate across all host threads
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<false>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
@@ -1726,7 +1728,7 @@ cudaError_t launch_tc_gemm(const TcGemmParams& p_in, int num_sms, cudaStream_t s
   }
   if (p_in.total_tiles <= 0) return cudaSuccess;
   TcGemmParams& p = const_cast<TcGemmParams&>(p_in);
-  p.sched_slot = static_cast<int>(slot_seq++ % kSchedSlots);
+  p.sched_slot = static_cast<int>(slot_seq.fetch_add(1) % kSchedSlots);
   if (p.pair) {
     int clusters = max_clusters < num_sms / 2 ? max_clusters : num_sms / 2;
     if (clusters > p.total_tiles) clusters = p.total_tiles;
