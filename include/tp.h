@@ -622,6 +622,11 @@ TP_API void tp_debug_inject_fault(int kind);
  * large launches with MN-major operands, the one-SM kernel otherwise.  All
  * give the same results up to fp32 summation order; tests run each. */
 TP_API void tp_debug_set_gemm_kernel(int mode);
+/* Plans whose outputs depend on each other run as one launch (dependent tiles
+ * wait for the tiles they read) unless they have more than `tiles_per_sm`
+ * 128 x 256 tiles per SM; larger plans run as two launches, independent
+ * outputs first.  Default 8; values <= 0 restore it. */
+TP_API void tp_debug_set_split_threshold(int tiles_per_sm);
 TP_API void tp_debug_set_wait_limit_ms(int ms);
 
 #ifdef __cplusplus

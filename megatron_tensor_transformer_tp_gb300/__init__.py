@@ -25,6 +25,7 @@ __all__ = [
     "tied_embed_grad_noalloc", "tp_get_status",
     "tp_status_string", "tp_num_sms", "tp_profile_enable", "tp_profile_reset", "tp_profile_read",
     "tp_debug_inject_fault", "tp_debug_set_wait_limit_ms", "tp_debug_set_gemm_kernel",
+    "tp_debug_set_split_threshold",
     "tp_gelu_eval", "logits_pitch", "tp_adam_step", "tp_adam_step_workspace_size",
     "tp_optimizer_state", "tp_adam_config", "tp_param_group", "make_optimizer_state",
     "read_optimizer_state", "tp_attn_core_fwd", "tp_attn_core_bwd", "tp_attn_core_workspace_size",
@@ -124,6 +125,7 @@ _SIGNATURES = {
                                ctypes.POINTER(ctypes.c_double), _int]),
     "tp_debug_inject_fault": (None, [_int]),
     "tp_debug_set_gemm_kernel": (None, [_int]),
+    "tp_debug_set_split_threshold": (None, [_int]),
     "tp_gelu_eval": (_int, [_c_void_p, _c_void_p, _c_void_p, _i64, _c_void_p]),
     "tp_debug_set_wait_limit_ms": (None, [_int]),
     "tp_adam_step": (_int, [ctypes.POINTER(tp_param_group), _int, ctypes.POINTER(tp_adam_config),
@@ -631,6 +633,11 @@ def tp_debug_inject_fault(kind: int):
 def tp_debug_set_gemm_kernel(mode: int):
     """0: one-SM tensor-core kernel, 1: two-SM kernel, 2: per launch (default)."""
     lib().tp_debug_set_gemm_kernel(int(mode))
+
+
+def tp_debug_set_split_threshold(tiles_per_sm: int):
+    """Tiles per SM above which a plan with dependent outputs runs as two launches."""
+    lib().tp_debug_set_split_threshold(int(tiles_per_sm))
 
 
 def tp_debug_set_wait_limit_ms(ms: int):

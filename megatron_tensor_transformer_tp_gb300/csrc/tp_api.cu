@@ -46,6 +46,7 @@ std::mutex g_mu;
 
 int g_fault_kind = 0;
 int g_gemm_mode = 2;  // 0: one-SM kernel, 1: two-SM kernel, 2: choose per launch
+int g_split_tiles_per_sm = 8;  // plans with dependent tiles and more tiles per SM run as two launches
 unsigned long long g_wait_limit_ns = 1000ull * 1000ull * 1000ull;
 
 tp_status device_state(DeviceState** out) {
@@ -599,7 +600,7 @@ tp_status run_plan_impl(Plan& pl, tp_dtype dt, const char* name, cudaStream_t s)
     total += ((groups[i].M + 127) / 128) * ((groups[i].N + 255) / 256);
     has_dep = has_dep || groups[i].dep_kind != DEP_NONE;
   }
-  if (has_dep && total > 8 * dev->num_sms) {
+  if (has_dep && total > g_split_tiles_per_sm * dev->num_sms) {
     GemmGroup first[kMaxGroups], second[kMaxGroups];
     int n1 = 0, n2 = 0;
     for (int i = 0; i < ng; ++i) {
@@ -1740,6 +1741,10 @@ extern "C" tp_status tp_gelu_eval(const float* z, float* y, float* dy, int64_t n
 extern "C" void tp_debug_inject_fault(int kind) { g_fault_kind = kind; }
 
 extern "C" void tp_debug_set_gemm_kernel(int mode) { g_gemm_mode = (mode >= 0 && mode <= 2) ? mode : 2; }
+
+extern "C" void tp_debug_set_split_threshold(int tiles_per_sm) {
+  g_split_tiles_per_sm = tiles_per_sm > 0 ? tiles_per_sm : 8;
+}
 
 extern "C" void tp_debug_set_wait_limit_ms(int ms) {
   g_wait_limit_ns = static_cast<unsigned long long>(ms > 0 ? ms : 1000) * 1000000ull;
