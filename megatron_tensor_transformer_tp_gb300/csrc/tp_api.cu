@@ -278,6 +278,7 @@ struct Plan {
     g.alpha = 1.f;
     g.out_map = -1;
     g.out2_map = -1;
+    g.aux_map = -1;
     return g;
   }
   // Counter block for row- or column-tile completion of producing groups.
@@ -468,12 +469,17 @@ tp_status launch_tc_groups(const Plan& pl, const bool* used, GemmGroup* groups, 
     }
   }
   // Bulk tensor-store maps for the bf16 outputs the epilogue stores whole
-  // (16-byte aligned rows), as long as map slots last.
+  // (16-byte aligned rows) and bulk-load maps for its bf16 operands, as long
+  // as map slots last.
   int nmaps = 0;
   for (int i = 0; i < ng; ++i) {
     GemmGroup& g = groups[i];
-    g.out_map = g.out2_map = -1;
+    g.out_map = g.out2_map = g.aux_map = -1;
     if (!g.vec_ok || g.out == nullptr || g.k_empty) continue;
+    // the dGELU / softmax-backward operand comes in through one bulk load per chunk
+    if ((g.epi == EPI_DGELU || g.epi == EPI_SMAX_BWD) && g.aux != nullptr && nmaps < kMaxStoreMaps &&
+        encode_store_map(&p.mapO[nmaps], g.aux, g.M, g.N, g.ld_aux, false))
+      g.aux_map = nmaps++;
     const bool f32 = g.out_type == OUT_F32;
     bool ok = false;
     switch (g.epi) {

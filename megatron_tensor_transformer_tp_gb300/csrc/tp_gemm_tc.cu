@@ -385,6 +385,28 @@ __device__ __forceinline__ void stage_acquire(int lane) {
   if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
   __syncwarp();
 }
+// A warp's bulk tensor load of one auxiliary chunk (the dGELU / softmax
+// backward operand) into its stage: the warp's own mbarrier and its phase.
+struct AuxLoad {
+  uint32_t bar;
+  uint32_t phase;
+  volatile int* abort_flag;
+  unsigned* err;
+  unsigned long long limit_ns;
+};
+__device__ __forceinline__ bool aux_wait(const AuxLoad& a) {
+  if (mbar_try_wait(a.bar, a.phase)) return true;
+  const unsigned long long t0 = global_ns();
+  while (!mbar_try_wait(a.bar, a.phase)) {
+    if (*a.abort_flag) return false;
+    if (global_ns() - t0 > a.limit_ns) {
+      *a.abort_flag = 1;
+      atomicOr(a.err, kErrTimeout);
+      return false;
+    }
+  }
+  return true;
+}
 __device__ __forceinline__ void tma_store_2d(uint64_t map, uint32_t src, int c0, int c1) {
   asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(map),
                "r"(src), "r"(c0), "r"(c1)
@@ -479,6 +501,28 @@ __device__ __forceinline__ void stage_store_rows(uint4* st, void* base, int out_
   __syncwarp();
 }
 
+// 32 x 32 bf16 chunk of the auxiliary operand through one bulk tensor load
+// (rows past the matrix read as zeros); lane l then holds row row0 + l.
+__device__ __forceinline__ void stage_load_aux_tma(uint4* st, uint64_t map, AuxLoad& a, int row0, int n,
+                                                   float* z, int lane) {
+  stage_acquire(lane);
+  if (lane == 0) {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    mbar_arrive_expect_tx(a.bar, 32 * 64);
+    tma_load_2d(smem_addr(st), map, a.bar, n, row0);
+  }
+  aux_wait(a);
+  a.phase ^= 1u;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const uint4 w = st[lane * 4 + (c ^ ((lane >> 1) & 3))];
+    unpack_bf16x2(w.x, z[8 * c + 0], z[8 * c + 1]);
+    unpack_bf16x2(w.y, z[8 * c + 2], z[8 * c + 3]);
+    unpack_bf16x2(w.z, z[8 * c + 4], z[8 * c + 5]);
+    unpack_bf16x2(w.w, z[8 * c + 6], z[8 * c + 7]);
+  }
+  __syncwarp();
+}
 __device__ __forceinline__ void stage_load_rows_bf16(uint4* st, const void* base, int64_t ld,
                                                      int row0, int M, int n, float* z, int lane) {
   stage_acquire(lane);
@@ -544,10 +588,11 @@ __device__ __forceinline__ void prefetch_bias(const GemmGroup& G, int n, int lan
 // are warp-collective); rows >= M are computed but never stored.
 template <bool ATTN>
 __device__ __forceinline__ void epilogue_chunk(const GemmGroup& G, const CUtensorMap* mapO, uint4* st,
-                                               int lane, int row0, int n, float* v) {
-  // bulk-store maps of the group's outputs (0: the lanes store)
+                                               AuxLoad& ax, int lane, int row0, int n, float* v) {
+  // bulk-store maps of the group's outputs (0: the lanes store), bulk-load map of its operand
   const uint64_t map1 = G.out_map >= 0 ? reinterpret_cast<uint64_t>(mapO + G.out_map) : 0ull;
   const uint64_t map2 = G.out2_map >= 0 ? reinterpret_cast<uint64_t>(mapO + G.out2_map) : 0ull;
+  const uint64_t mapx = G.aux_map >= 0 ? reinterpret_cast<uint64_t>(mapO + G.aux_map) : 0ull;
   const int row = row0 + lane;
   const bool row_ok = row < G.M;
   const int ncols = min(32, G.N - n);
@@ -583,7 +628,8 @@ __device__ __forceinline__ void epilogue_chunk(const GemmGroup& G, const CUtenso
       // dS = P * (dP - D) * alpha with P = aux, D = row_lse (the row's sum of P dP)
       float z[32];
       if (coal) {
-        stage_load_rows_bf16(st, G.aux, G.ld_aux, row0, G.M, n, z, lane);
+        if (mapx != 0) stage_load_aux_tma(st, mapx, ax, row0, n, z, lane);
+        else stage_load_rows_bf16(st, G.aux, G.ld_aux, row0, G.M, n, z, lane);
       } else {
 #pragma unroll
         for (int j = 0; j < 32; ++j) z[j] = 0.f;
@@ -638,7 +684,8 @@ __device__ __forceinline__ void epilogue_chunk(const GemmGroup& G, const CUtenso
     case EPI_DGELU: {
       float z[32];
       if (coal) {
-        stage_load_rows_bf16(st, G.aux, G.ld_aux, row0, G.M, n, z, lane);
+        if (mapx != 0) stage_load_aux_tma(st, mapx, ax, row0, n, z, lane);
+        else stage_load_rows_bf16(st, G.aux, G.ld_aux, row0, G.M, n, z, lane);
       } else {
 #pragma unroll
         for (int j = 0; j < 32; ++j) z[j] = 0.f;
@@ -890,7 +937,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + kBarCount + 1);
   // tile ring: (tile id or -1, group, m0, n0) per slot, decoded once by the producer
   volatile int* tile_ids = reinterpret_cast<volatile int*>(bars + kBarCount + 2);
-  static_assert((kBarCount + 2) * 8 + 16 * TILE_RING <= BAR_BYTES, "barrier area");
+  // one mbarrier per epilogue warp for its auxiliary-operand loads
+  uint64_t* aux_bars = bars + kBarCount + 2 + 2 * TILE_RING;
+  static_assert((kBarCount + 2 + 2 * TILE_RING + NUM_EPI_WARPS) * 8 <= BAR_BYTES, "barrier area");
   GrpLite* gtab = reinterpret_cast<GrpLite*>(smem + STAGES * STAGE_BYTES + BAR_BYTES +
                                              NUM_EPI_WARPS * EPI_WARP_BYTES);
   fill_group_table(p, gtab, threadIdx.x, NUM_THREADS);
@@ -920,6 +969,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
       mbar_init(tile_full_bar(r), 1);
       mbar_init(tile_empty_bar(r), 1 + NUM_EPI_WARPS);
     }
+    for (int w = 0; w < NUM_EPI_WARPS; ++w) mbar_init(smem_addr(aux_bars + w), 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -1088,6 +1138,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
     uint4* epi_stage = reinterpret_cast<uint4*>(smem + STAGES * STAGE_BYTES + BAR_BYTES +
                                                 (warp - 2) * EPI_WARP_BYTES);
     const int part = (warp - 2) >> 2;  // which quarter of the tile's columns
+    AuxLoad ax{smem_addr(aux_bars + (warp - 2)), 0u, abort_flag, p.err, p.wait_limit_ns};
     for (int lt = 0;; ++lt) {
       const int r = lt % TILE_RING;
       if (!wait_bounded(tile_full_bar(r), static_cast<uint32_t>((lt / TILE_RING) & 1), wctx)) break;
@@ -1122,7 +1173,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
 #pragma unroll
           for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(rr[j]);
         }
-        epilogue_chunk<ATTN>(G, p.mapO, epi_stage, lane, row0, n, v);
+        epilogue_chunk<ATTN>(G, p.mapO, epi_stage, ax, lane, row0, n, v);
       }
       tc_fence_before();
       if (G.prod_row >= 0 || G.prod_col >= 0) {
@@ -1390,7 +1441,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_pair_kernel(const __gr
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + kBarCount + 1);
   // tile ring: (tile id or -1, group, m0, n0) per slot, decoded once by the leader's producer
   volatile int* tile_ids = reinterpret_cast<volatile int*>(bars + kBarCount + 2);
-  static_assert((kBarCount + 2) * 8 + 16 * TILE_RING <= BAR_BYTES, "barrier area");
+  // one mbarrier per epilogue warp for its auxiliary-operand loads
+  uint64_t* aux_bars = bars + kBarCount + 2 + 2 * TILE_RING;
+  static_assert((kBarCount + 2 + 2 * TILE_RING + NUM_EPI_WARPS) * 8 <= BAR_BYTES, "barrier area");
   GrpLite* gtab = reinterpret_cast<GrpLite*>(smem + STAGES2 * STAGE2_BYTES + BAR_BYTES +
                                              NUM_EPI_WARPS * EPI_WARP_BYTES);
   fill_group_table(p, gtab, threadIdx.x, NUM_THREADS);
@@ -1424,6 +1477,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_pair_kernel(const __gr
       // leader: its MMA thread and epilogue warps; peer: its producer and epilogue warps
       mbar_init(tile_empty_bar(r), 2 * (1 + NUM_EPI_WARPS));
     }
+    for (int w = 0; w < NUM_EPI_WARPS; ++w) mbar_init(smem_addr(aux_bars + w), 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -1614,6 +1668,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_pair_kernel(const __gr
                                                 (warp - 2) * EPI_WARP_BYTES);
     const uint32_t tempty_leader0 = map_to_rank(tempty_bar(0), 0);
     const uint32_t tempty_leader1 = map_to_rank(tempty_bar(1), 0);
+    AuxLoad ax{smem_addr(aux_bars + (warp - 2)), 0u, abort_flag, p.err, p.wait_limit_ns};
     for (int lt = 0;; ++lt) {
       int tile;
       TileCoord tc;
@@ -1645,7 +1700,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_pair_kernel(const __gr
 #pragma unroll
           for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(rr[j]);
         }
-        epilogue_chunk<ATTN>(G, p.mapO, epi_stage, lane, row0, n, v);
+        epilogue_chunk<ATTN>(G, p.mapO, epi_stage, ax, lane, row0, n, v);
       }
       tc_fence_before();
       if (G.prod_row >= 0 || G.prod_col >= 0) {

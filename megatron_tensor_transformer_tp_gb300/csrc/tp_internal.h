@@ -96,9 +96,9 @@ struct GemmGroup {
   const uint32_t* drop_mask;
   int drop_wpr;
   float drop_scale;
-  // Bulk tensor-store maps of out / out2 in TcGemmParams::mapO, or -1 (set by
-  // the launcher; the epilogue then stores through the TMA).
-  int out_map, out2_map;
+  // Bulk tensor-store maps of out / out2 and the bulk-load map of aux in
+  // TcGemmParams::mapO, or -1 (set by the launcher).
+  int out_map, out2_map, aux_map, pad_maps;
 };
 
 // One operand pair of the tensor-core engine.  Operands are bf16.
