@@ -5,7 +5,7 @@
 //                        saving the row mean and 1/std;
 //   ln_bwd_kernel        its input gradient (plus an optional residual gradient);
 //   ln_param_grad        gain and bias gradients over 16-row groups, then
-//   colsum_level2        the groups summed in order (deterministic);
+//   ln_param_grad_sum    the groups summed in order (deterministic);
 //   dropout_add_kernel   out = res + x * keep / (1 - p) and its backward;
 //   pos_embed_dropout    (word + position embedding) with dropout;
 //   attn_keep_kernel     attention-dropout keep bits, 32 keys per word.
@@ -241,9 +241,9 @@ __global__ void __launch_bounds__(256) ln_param_grad_kernel(
   }
 }
 
-// Second level: the groups' partials summed in order into dg and db (+ the
+// The groups' partials summed in order into dg and db (+ the
 // existing values when accumulating); 2h columns.
-__global__ void colsum_level2_kernel(const float* __restrict__ part2, int ngroups, int64_t h,
+__global__ void ln_param_grad_sum_kernel(const float* __restrict__ part2, int ngroups, int64_t h,
                                      float* __restrict__ dg, float* __restrict__ db, int accumulate) {
   const int64_t c = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (c >= 2 * h) return;
@@ -408,7 +408,7 @@ cudaError_t launch_ln_bwd(const void* dy, const void* x, const float* g, const f
   const int ngroups = ln_bwd_blocks(T);
   const dim3 g1(static_cast<unsigned>((h / 8 + 255) / 256), static_cast<unsigned>(ngroups));
   ln_param_grad_kernel<<<g1, 256, 0, st>>>(dyb, xb, mean, rstd, T, h, partial);
-  colsum_level2_kernel<<<static_cast<unsigned>((2 * h + 255) / 256), 256, 0, st>>>(partial, ngroups, h, dg, db,
+  ln_param_grad_sum_kernel<<<static_cast<unsigned>((2 * h + 255) / 256), 256, 0, st>>>(partial, ngroups, h, dg, db,
                                                                                       accumulate);
   count_launches(3);
   return cudaGetLastError();
