@@ -489,7 +489,8 @@ class LayerBench:
         T, h, hp, H, s = self.T, self.h, self.hp, self.H, self.s
         self.saved = dict(ln1=e(T, h), mean1=e(T, dt=f32), rstd1=e(T, dt=f32), QKV=e(T, 3 * h),
                           P=e(self.b, H, s, s), Pd=e(self.b, H, s, s), C=e(T, h), h1=e(T, h),
-                          ln2=e(T, h), mean2=e(T, dt=f32), rstd2=e(T, dt=f32), Z=e(T, hp), Y=e(T, hp))
+                          ln2=e(T, h), mean2=e(T, dt=f32), rstd2=e(T, dt=f32), Z=e(T, hp), Y=e(T, hp),
+                          attn_keep=e(self.b * H * s * ((s + 31) // 32), dt=torch.int32))
         N, d3, n = self.N, h // self.N, hp // self.N
         self.grads = dict(dg1=e(h, dt=f32), db1=e(h, dt=f32), dg2=e(h, dt=f32), db2=e(h, dt=f32),
                           dbo=e(h, dt=f32), db=e(h, dt=f32),

@@ -81,7 +81,7 @@ class tp_layer_params(ctypes.Structure):
 
 class tp_layer_saved(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in ("ln1", "mean1", "rstd1", "QKV", "P", "Pd", "C", "h1",
-                                                "ln2", "mean2", "rstd2", "Z", "Y")]
+                                                "ln2", "mean2", "rstd2", "Z", "Y", "attn_keep")]
 
 
 class tp_layer_grads(ctypes.Structure):

@@ -898,7 +898,11 @@ size_t attn_bwd_ws(const AttnDims& a, int64_t s) {
          attn_keep_bytes(a, s);
 }
 
-bool drop_ok(float p, int64_t s) { return p >= 0.f && p < 1.f && (p == 0.f || s % 16 == 0); }
+// Attention dropout needs whole 16-key Philox blocks per row and fits its keep
+// kernel's grid (s and the (sequence, head) pairs below 65536).
+bool drop_ok(float p, int64_t s) {
+  return p >= 0.f && p < 1.f && (p == 0.f || (s % 16 == 0 && s <= 65535));
+}
 
 // (sequence, head) pairs per GEMM launch: within the engine's group and
 // counter limits (groups_per_pair outputs and counters_per_pair counters each).
@@ -917,14 +921,17 @@ extern "C" size_t tp_attn_core_workspace_size(int64_t T, int64_t s, int64_t h, i
 }
 
 namespace {
+// keep_out (optional): where the forward leaves the attention-dropout keep
+// words (else the workspace); keep_in (optional): the backward reads them
+// there instead of drawing them again.
 tp_status attn_core_fwd_impl(tp_dtype dt, int64_t T, int64_t s, int64_t h, int n_heads, int N, int causal,
                              float p_drop, uint64_t seed, uint64_t stream0, const void* QKV, void* P,
                              void* Pd, void* C, float* lse, void* workspace, size_t ws_bytes,
-                             void* stream) {
+                             void* stream, uint32_t* keep_out = nullptr) {
   AttnDims a;
   tp_status st = attn_args(dt, T, s, h, n_heads, N, &a);
   if (st != TP_OK) return st;
-  if (!drop_ok(p_drop, s)) return TP_ERR_INVALID;
+  if (!drop_ok(p_drop, s) || (p_drop > 0.f && a.pairs > 65535)) return TP_ERR_INVALID;
   if (T == 0) return TP_OK;
   if (!QKV || !P || !C || (p_drop > 0.f && !Pd)) return TP_ERR_INVALID;
   if (workspace == nullptr || ws_bytes < attn_fwd_ws(a, s)) return TP_ERR_WORKSPACE;
@@ -934,8 +941,10 @@ tp_status attn_core_fwd_impl(tp_dtype dt, int64_t T, int64_t s, int64_t h, int n
   float* row_lse = lse ? lse
                        : reinterpret_cast<float*>(bb(workspace) +
                                                   round256(static_cast<size_t>(a.pairs * a.P * s) * 8));
-  uint32_t* keep = reinterpret_cast<uint32_t*>(bb(workspace) + round256(static_cast<size_t>(a.pairs * a.P * s) * 8) +
-                                               round256(static_cast<size_t>(a.pairs * s) * 4));
+  uint32_t* keep = keep_out ? keep_out
+                            : reinterpret_cast<uint32_t*>(bb(workspace) +
+                                                          round256(static_cast<size_t>(a.pairs * a.P * s) * 8) +
+                                                          round256(static_cast<size_t>(a.pairs * s) * 4));
   const int wpr = static_cast<int>((s + 31) / 32);
   const float alpha = static_cast<float>(1.0 / sqrt(static_cast<double>(a.d)));
   const int kr_s = causal ? KR_TRI : KR_NONE;
@@ -1016,11 +1025,11 @@ tp_status attn_core_fwd_impl(tp_dtype dt, int64_t T, int64_t s, int64_t h, int n
 tp_status attn_core_bwd_impl(tp_dtype dt, int64_t T, int64_t s, int64_t h, int n_heads, int N, int causal,
                              float p_drop, uint64_t seed, uint64_t stream0, const void* QKV, const void* P,
                              const void* Pd, const void* C, const void* dC, void* dQKV, void* workspace,
-                             size_t ws_bytes, void* stream) {
+                             size_t ws_bytes, void* stream, const uint32_t* keep_in = nullptr) {
   AttnDims a;
   tp_status st = attn_args(dt, T, s, h, n_heads, N, &a);
   if (st != TP_OK) return st;
-  if (!drop_ok(p_drop, s)) return TP_ERR_INVALID;
+  if (!drop_ok(p_drop, s) || (p_drop > 0.f && a.pairs > 65535)) return TP_ERR_INVALID;
   if (T == 0) return TP_OK;
   if (!QKV || !P || !C || !dC || !dQKV || (p_drop > 0.f && !Pd)) return TP_ERR_INVALID;
   if (workspace == nullptr || ws_bytes < attn_bwd_ws(a, s)) return TP_ERR_WORKSPACE;
@@ -1028,7 +1037,8 @@ tp_status attn_core_bwd_impl(tp_dtype dt, int64_t T, int64_t s, int64_t h, int n
   cudaStream_t strm = static_cast<cudaStream_t>(stream);
   float* D = static_cast<float*>(workspace);
   uint8_t* dS = bb(workspace) + round256(static_cast<size_t>(a.pairs * s) * 4);
-  uint32_t* keep = reinterpret_cast<uint32_t*>(dS + round256(static_cast<size_t>(a.pairs * s * s) * 2));
+  uint32_t* keep_ws = reinterpret_cast<uint32_t*>(dS + round256(static_cast<size_t>(a.pairs * s * s) * 2));
+  const uint32_t* keep = keep_in ? keep_in : keep_ws;
   const int wpr = static_cast<int>((s + 31) / 32);
   const float alpha = static_cast<float>(1.0 / sqrt(static_cast<double>(a.d)));
   // 1. D = rowsum(dC * C) per head and token (= sum over keys of P dP)
@@ -1036,9 +1046,10 @@ tp_status attn_core_bwd_impl(tp_dtype dt, int64_t T, int64_t s, int64_t h, int n
     return launch_attn_rowdot(C, dC, h, s, n_heads, static_cast<int>(a.d), a.pairs, D, strm);
   });
   if (e != cudaSuccess) return TP_ERR_CUDA;
-  if (p_drop > 0.f) {  // the forward's keep bits, drawn again
+  if (p_drop > 0.f && keep_in == nullptr) {  // the forward's keep bits, drawn again
     e = timed("attn_keep", strm, [&] {
-      return launch_attn_keep(a.pairs, s, n_heads, n_heads / N, causal != 0, seed, stream0, p_drop, keep, strm);
+      return launch_attn_keep(a.pairs, s, n_heads, n_heads / N, causal != 0, seed, stream0, p_drop, keep_ws,
+                              strm);
     });
     if (e != cudaSuccess) return TP_ERR_CUDA;
   }
@@ -1520,7 +1531,7 @@ extern "C" tp_status tp_transformer_layer_fwd(const tp_layer_config* cfg, const 
   if ((st = qkv_proj(c.T, c.h, c.N, sv->ln1, w->Wqkv, w->bqkv, sv->QKV, s)) != TP_OK) return st;
   st = attn_core_fwd_impl(TP_BF16, c.T, c.s, c.h, c.n_heads, c.N, c.causal, c.p_attn, c.seed,
                           layer_stream(c.layer, 0), sv->QKV, sv->P, sv->Pd, sv->C, nullptr, core_ws,
-                          core_bytes, stream);
+                          core_bytes, stream, sv->attn_keep);
   if (st != TP_OK) return st;
   if ((st = out_proj(c.T, c.h, c.N, sv->C, w->Wo, w->bo, O, s)) != TP_OK) return st;
   e = timed("layer_dropout_add", s, [&] {
@@ -1597,7 +1608,7 @@ extern "C" tp_status tp_transformer_layer_bwd(const tp_layer_config* cfg, const 
     return st;
   st = attn_core_bwd_impl(TP_BF16, c.T, c.s, c.h, c.n_heads, c.N, c.causal, c.p_attn, c.seed,
                           layer_stream(c.layer, 0), sv->QKV, sv->P, sv->Pd, sv->C, dC, dQKV, core_ws,
-                          core_bytes, stream);
+                          core_bytes, stream, sv->attn_keep);
   if (st != TP_OK) return st;
   if ((st = qkv_proj_bwd(c.T, c.h, c.N, dQKV, sv->ln1, w->Wqkv, dln1, g->dWqkv, g->dbqkv, accumulate, s)) !=
       TP_OK)

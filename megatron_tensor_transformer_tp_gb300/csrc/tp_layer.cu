@@ -331,25 +331,24 @@ __global__ void __launch_bounds__(256) pos_embed_dropout_kernel(
 // Keep bits of attention dropout: word w of row q of pair g covers keys
 // 32 w .. 32 w + 31 of element block ((g s + q) s + 32 w) / 16 (s % 16 == 0);
 // pair g = sequence * heads + head draws from stream stream0 + shard(head).
-__global__ void __launch_bounds__(256) attn_keep_kernel(int64_t pairs, int64_t s, int wpr, int n_heads,
-                                                        int heads_per_shard, int causal, uint64_t seed,
-                                                        uint64_t stream0, uint32_t thr,
-                                                        uint32_t* __restrict__ words) {
-  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  const int64_t total = pairs * s * wpr;
-  if (i >= total) return;
-  const int64_t w = i % wpr, gq = i / wpr;  // gq = g * s + q
-  if (causal && 32 * w > gq % s) {  // every key of the word lies after the query: never read
-    words[i] = 0u;
+// Grid: x over the words of a row, y = q, z = g (no integer divisions).
+__global__ void __launch_bounds__(256) attn_keep_kernel(int64_t s, int wpr, int n_heads, int heads_per_shard,
+                                                        int causal, uint64_t seed, uint64_t stream0,
+                                                        uint32_t thr, uint32_t* __restrict__ words) {
+  const int w = blockIdx.x * blockDim.x + threadIdx.x;
+  if (w >= wpr) return;
+  const int64_t q = blockIdx.y, g = blockIdx.z;
+  uint32_t* out = words + (g * s + q) * wpr + w;
+  if (causal && 32 * static_cast<int64_t>(w) > q) {  // every key of the word lies after the query: never read
+    *out = 0u;
     return;
   }
-  const int64_t g = gq / s;
-  const int j = static_cast<int>(g % n_heads);
+  const int j = static_cast<int>(blockIdx.z % static_cast<unsigned>(n_heads));
   const uint64_t stream = stream0 + static_cast<uint64_t>(j / heads_per_shard);
-  const int64_t e = gq * s + 32 * w;
-  uint32_t bits = keep16(static_cast<uint64_t>(e / 16), seed, stream, thr);
-  if (32 * w + 16 < s) bits |= keep16(static_cast<uint64_t>(e / 16 + 1), seed, stream, thr) << 16;
-  words[i] = bits;
+  const uint64_t blk = static_cast<uint64_t>(((g * s + q) * s) / 16) + 2 * static_cast<uint64_t>(w);
+  uint32_t bits = keep16(blk, seed, stream, thr);
+  if (32 * static_cast<int64_t>(w) + 16 < s) bits |= keep16(blk + 1, seed, stream, thr) << 16;
+  *out = bits;
 }
 
 }  // namespace
@@ -440,10 +439,13 @@ cudaError_t launch_pos_embed_dropout(const void* words, const void* pos_table, c
 cudaError_t launch_attn_keep(int64_t pairs, int64_t s, int n_heads, int heads_per_shard, int causal,
                              uint64_t seed, uint64_t stream0, float p, uint32_t* words, cudaStream_t st) {
   const int wpr = static_cast<int>((s + 31) / 32);
-  const int64_t total = pairs * s * wpr;
-  if (total == 0) return cudaSuccess;
-  attn_keep_kernel<<<static_cast<unsigned>((total + 255) / 256), 256, 0, st>>>(
-      pairs, s, wpr, n_heads, heads_per_shard, causal, seed, stream0, dropout_threshold(p), words);
+  if (pairs == 0 || s == 0) return cudaSuccess;
+  if (s > 65535 || pairs > 65535) return cudaErrorInvalidValue;  // grid y / z limits
+  const int bx = wpr < 256 ? wpr : 256;
+  const dim3 grid(static_cast<unsigned>((wpr + bx - 1) / bx), static_cast<unsigned>(s),
+                  static_cast<unsigned>(pairs));
+  attn_keep_kernel<<<grid, bx, 0, st>>>(s, wpr, n_heads, heads_per_shard, causal, seed, stream0,
+                                        dropout_threshold(p), words);
   count_launches(1);
   return cudaGetLastError();
 }

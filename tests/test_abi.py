@@ -255,7 +255,7 @@ def layer_fwd(cfg, params=None, ws_bytes=None):
                                      C.cast(sh[0], C.c_void_p).value, None, FAKE, FAKE,
                                      C.cast(sh[0], C.c_void_p).value, None,
                                      C.cast(sh[0], C.c_void_p).value, None)
-    sv = tp.tp_layer_saved(*([FAKE] * 13))
+    sv = tp.tp_layer_saved(*([FAKE] * 14))
     if ws_bytes is None:
         ws_bytes = 1 << 34
     return L.tp_transformer_layer_fwd(C.byref(cfg), C.byref(w), FAKE, FAKE, C.byref(sv), FAKE * 256,

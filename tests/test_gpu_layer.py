@@ -98,7 +98,7 @@ def alloc_layer(cfg, T):
     return saved
 
 
-def run_layer(cfg, inp):
+def run_layer(cfg, inp, keep_buffer=False):
     tp = _tp()
     T, h, hp, N = inp["T"], cfg["h"], cfg["hp"], cfg["N"]
     c = dict(cfg, T=T)
@@ -108,6 +108,10 @@ def run_layer(cfg, inp):
                   Wo=[d(t) for t in inp["Wo"]], bo=d(inp["bo"]), W=[d(t) for t in inp["W"]],
                   a=[d(t) for t in inp["a"]], U=[d(t) for t in inp["U"]], b=d(inp["b"]))
     saved = alloc_layer(cfg, T)
+    if keep_buffer:
+        s = cfg["s"]
+        saved["attn_keep"] = torch.empty((T // s) * cfg["n_heads"] * s * ((s + 31) // 32),
+                                         dtype=torch.int32, device="cuda")
     x, dout = d(inp["x"]), d(inp["dout"])
     out = torch.empty_like(x)
     ws = torch.empty(tp.tp_transformer_layer_workspace_size(c), dtype=torch.uint8, device="cuda")
@@ -242,3 +246,18 @@ def test_layer_gradients_accumulate():
         pairs = zip(v, before[k]) if isinstance(v, list) else [(v, before[k])]
         for a, b in pairs:
             assert torch.allclose(a, 2 * b, rtol=1e-5, atol=1e-6), k
+
+
+def test_layer_saved_keep_words_match_redrawn():
+    """Keeping the attention-dropout bits from the forward gives the same
+    results as drawing them again in the backward."""
+    cfg = dict(SMALL)
+    inp = SI.layer_inputs(dict(cfg, b=2))
+    a, b = run_layer(cfg, inp), run_layer(cfg, inp, keep_buffer=True)
+    assert torch.equal(a[0], b[0]) and torch.equal(a[2], b[2])
+    for k in a[3]:
+        x, y = a[3][k], b[3][k]
+        if isinstance(x, list):
+            assert all(torch.equal(u, v) for u, v in zip(x, y))
+        else:
+            assert torch.equal(x, y)
