@@ -4,7 +4,7 @@
 //   ln_fwd_kernel        LayerNorm of bf16 rows with fp32 gain and bias,
 //                        saving the row mean and 1/std;
 //   ln_bwd_kernel        its input gradient (plus an optional residual gradient);
-//   ln_param_grad        gain and bias gradients over 16-row groups, then
+//   ln_param_grad        gain and bias gradients over 8-row groups, then
 //   ln_param_grad_sum    the groups summed in order (deterministic);
 //   dropout_add_kernel   out = res + x * keep / (1 - p) and its backward;
 //   pos_embed_dropout    (word + position embedding) with dropout;
@@ -206,10 +206,10 @@ __global__ void __launch_bounds__(kLnThreads) ln_bwd_kernel(
 }
 
 // Gain and bias gradients, first level: block (x, y) sums dy xhat and dy over
-// rows [16 y, 16 (y + 1)) for eight columns per thread,
+// rows [8 y, 8 (y + 1)) for eight columns per thread,
 // columns 8 (256 x + tid) ..; rows in order.  partial[y][0..h) = dg part,
 // partial[y][h..2h) = db part.
-constexpr int kLnColRows = 16;
+constexpr int kLnColRows = 8;
 __global__ void __launch_bounds__(256) ln_param_grad_kernel(
     const __nv_bfloat16* __restrict__ dy, const __nv_bfloat16* __restrict__ x,
     const float* __restrict__ mean_in, const float* __restrict__ rstd_in, int64_t T, int64_t h,
@@ -241,17 +241,28 @@ __global__ void __launch_bounds__(256) ln_param_grad_kernel(
   }
 }
 
-// The groups' partials summed in order into dg and db (+ the
-// existing values when accumulating); 2h columns.
-__global__ void ln_param_grad_sum_kernel(const float* __restrict__ part2, int ngroups, int64_t h,
-                                     float* __restrict__ dg, float* __restrict__ db, int accumulate) {
-  const int64_t c = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (c >= 2 * h) return;
+// The groups' partials summed into dg and db (+ the existing values when
+// accumulating); 2h columns.  A block takes 32 columns (lane = column) and 8
+// slices (warp = slice): slice w sums groups w, w + 8, ... in order, then
+// slice 0 adds the slices in order (fixed order, deterministic).
+__global__ void __launch_bounds__(256) ln_param_grad_sum_kernel(const float* __restrict__ part2, int ngroups,
+                                                                int64_t h, float* __restrict__ dg,
+                                                                float* __restrict__ db, int accumulate) {
+  __shared__ float red[8][32];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int64_t c = static_cast<int64_t>(blockIdx.x) * 32 + lane;
   float s = 0.f;
-#pragma unroll 8
-  for (int k = 0; k < ngroups; ++k) s += part2[static_cast<int64_t>(k) * 2 * h + c];
+  if (c < 2 * h) {
+#pragma unroll 4
+    for (int k = w; k < ngroups; k += 8) s += part2[static_cast<int64_t>(k) * 2 * h + c];
+  }
+  red[w][lane] = s;
+  __syncthreads();
+  if (w != 0 || c >= 2 * h) return;
+  float t = red[0][lane];
+  for (int k = 1; k < 8; ++k) t += red[k][lane];
   float* out = c < h ? dg + c : db + (c - h);
-  *out = accumulate ? *out + s : s;
+  *out = accumulate ? *out + t : t;
 }
 
 // 16 elements per thread (one Philox block): out = res + x * keep * scale, or
@@ -407,8 +418,8 @@ cudaError_t launch_ln_bwd(const void* dy, const void* x, const float* g, const f
   const int ngroups = ln_bwd_blocks(T);
   const dim3 g1(static_cast<unsigned>((h / 8 + 255) / 256), static_cast<unsigned>(ngroups));
   ln_param_grad_kernel<<<g1, 256, 0, st>>>(dyb, xb, mean, rstd, T, h, partial);
-  ln_param_grad_sum_kernel<<<static_cast<unsigned>((2 * h + 255) / 256), 256, 0, st>>>(partial, ngroups, h, dg, db,
-                                                                                      accumulate);
+  ln_param_grad_sum_kernel<<<static_cast<unsigned>((2 * h + 31) / 32), 256, 0, st>>>(partial, ngroups, h, dg,
+                                                                                      db, accumulate);
   count_launches(3);
   return cudaGetLastError();
 }
