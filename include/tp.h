@@ -322,8 +322,8 @@ typedef struct {
  *   h1 = x + dropout(O);  ln2 = LN(h1; g2, b2);  Z, Y, M = MLP(ln2);
  *   out = h1 + dropout(M).
  * LayerNorm: biased variance, fp32 statistics and parameters, bf16 output.
- * x, out (T, h) bf16; saved as above.  Needs h % 16 == 0, h <= 8192,
- * T <= 524280, and the constraints of the attention core and MLP entry points.
+ * x, out (T, h) bf16; saved as above.  Needs h % 16 == 0, h <= 8192, and the
+ * constraints of the attention core and MLP entry points.
  * tp_transformer_layer_bwd -- the gradient: dx (T, h) bf16 and the parameter
  * gradients (accumulate: add into them).  Both draw the dropout bits from the
  * config's streams; the backward draws them again.

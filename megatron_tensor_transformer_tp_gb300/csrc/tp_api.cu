@@ -1410,7 +1410,6 @@ tp_status layer_check(const tp_layer_config* c, const tp_layer_params* w) {
       c->n_heads % c->N != 0 || c->h % c->n_heads != 0 || c->hp % c->N != 0 || c->T % c->s != 0)
     return TP_ERR_INVALID;
   if (c->h % 16 != 0 || c->h > 8192) return TP_ERR_INVALID;
-  if (ln_bwd_blocks(c->T) > 65535) return TP_ERR_INVALID;  // the LayerNorm gradient grid
   if (!(c->p_hidden >= 0.f && c->p_hidden < 1.f) || !drop_ok(c->p_attn, c->s) || !(c->eps > 0.f))
     return TP_ERR_INVALID;
   if (!w->g1 || !w->b1 || !w->g2 || !w->b2 || !shards_ok(w->Wqkv, c->N) || !shards_ok(w->Wo, c->N) ||

@@ -3,9 +3,10 @@
 // parameters):
 //   ln_fwd_kernel        LayerNorm of bf16 rows with fp32 gain and bias,
 //                        saving the row mean and 1/std;
-//   ln_bwd_kernel        its input gradient (plus an optional residual gradient);
-//   ln_param_grad        gain and bias gradients over 8-row groups, then
-//   ln_param_grad_sum    the groups summed in order (deterministic);
+//   ln_bwd_kernel        its input gradient (plus an optional residual gradient)
+//                        and the gain and bias gradient parts of 8-row groups,
+//                        in one pass over dy and x;
+//   ln_param_grad_sum    the groups' parts summed in order (deterministic);
 //   dropout_add_kernel   out = res + x * keep / (1 - p) and its backward;
 //   pos_embed_dropout    (word + position embedding) with dropout;
 //   attn_keep_kernel     attention-dropout keep bits, 32 keys per word.
@@ -72,17 +73,7 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
   return t;
 }
 
-// Eight consecutive bf16 of a row as floats (one 16-byte load), and back.
-__device__ __forceinline__ void load8(const __nv_bfloat16* p, float* v) {
-  const uint4 q = *reinterpret_cast<const uint4*>(p);
-  const __nv_bfloat162* a = reinterpret_cast<const __nv_bfloat162*>(&q);
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const float2 f = __bfloat1622float2(a[k]);
-    v[2 * k] = f.x;
-    v[2 * k + 1] = f.y;
-  }
-}
+// Eight floats to eight consecutive bf16 of a row (one 16-byte store).
 __device__ __forceinline__ void store8(__nv_bfloat16* p, const float* v) {
   uint4 q;
   __nv_bfloat162* a = reinterpret_cast<__nv_bfloat162*>(&q);
@@ -95,149 +86,214 @@ __device__ __forceinline__ void load8f(const float* p, float* v) {
   v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
   v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
 }
-
-// A thread owns PER values of a row in groups of eight consecutive columns:
-// group k covers columns 8 (k kLnThreads + tid) .. + 7 (h % 8 == 0).
-template <int PER>
-__global__ void __launch_bounds__(kLnThreads) ln_fwd_kernel(const __nv_bfloat16* __restrict__ x,
-                                                            const float* __restrict__ g,
-                                                            const float* __restrict__ b, int64_t h,
-                                                            float eps, __nv_bfloat16* __restrict__ y,
-                                                            float* __restrict__ mean_out,
-                                                            float* __restrict__ rstd_out) {
-  __shared__ float red[kLnThreads / 32];
-  const int64_t row = blockIdx.x;
-  const __nv_bfloat16* xr = x + row * h;
-  float v[PER];
-  float s = 0.f;
+// The eight bf16 of one 16-byte load as floats.
+__device__ __forceinline__ void unpack8(const uint4& q, float* v) {
+  const __nv_bfloat162* a = reinterpret_cast<const __nv_bfloat162*>(&q);
 #pragma unroll
-  for (int k = 0; k < PER / 8; ++k) {
-    const int64_t c = (static_cast<int64_t>(k) * kLnThreads + threadIdx.x) * 8;
-    if (c < h) {
-      load8(xr + c, v + 8 * k);
-    } else {
-#pragma unroll
-      for (int t = 0; t < 8; ++t) v[8 * k + t] = 0.f;
-    }
-#pragma unroll
-    for (int t = 0; t < 8; ++t) s += v[8 * k + t];
-  }
-  const float mean = block_sum(s, red) / static_cast<float>(h);
-  float q = 0.f;
-#pragma unroll
-  for (int k = 0; k < PER / 8; ++k) {
-    const int64_t c = (static_cast<int64_t>(k) * kLnThreads + threadIdx.x) * 8;
-#pragma unroll
-    for (int t = 0; t < 8; ++t) {
-      const float dlt = c < h ? v[8 * k + t] - mean : 0.f;
-      q += dlt * dlt;
-    }
-  }
-  const float rstd = rsqrtf(block_sum(q, red) / static_cast<float>(h) + eps);
-#pragma unroll
-  for (int k = 0; k < PER / 8; ++k) {
-    const int64_t c = (static_cast<int64_t>(k) * kLnThreads + threadIdx.x) * 8;
-    if (c < h) {
-      float gg[8], bb[8], o[8];
-      load8f(g + c, gg);
-      load8f(b + c, bb);
-#pragma unroll
-      for (int t = 0; t < 8; ++t) o[t] = (v[8 * k + t] - mean) * rstd * gg[t] + bb[t];
-      store8(y + row * h + c, o);
-    }
-  }
-  if (threadIdx.x == 0) {
-    mean_out[row] = mean;
-    rstd_out[row] = rstd;
+  for (int k = 0; k < 4; ++k) {
+    const float2 f = __bfloat1622float2(a[k]);
+    v[2 * k] = f.x;
+    v[2 * k + 1] = f.y;
   }
 }
 
-// One row per block: dx = rstd (dxhat - mean(dxhat) - xhat mean(dxhat xhat))
-// (+ dres), dxhat = dy g.
+// A thread owns PER values of a row in groups of eight consecutive columns:
+// group k covers columns 8 (k kLnThreads + tid) .. + 7 (h % 8 == 0).  A block
+// takes kLnFwdRows consecutive rows in order; the next row is loaded while
+// this row's sums run.
+constexpr int kLnFwdRows = 4;
+
+template <int PER>
+__global__ void __launch_bounds__(kLnThreads) ln_fwd_kernel(const __nv_bfloat16* __restrict__ x,
+                                                            const float* __restrict__ g,
+                                                            const float* __restrict__ b, int64_t T,
+                                                            int64_t h, float eps,
+                                                            __nv_bfloat16* __restrict__ y,
+                                                            float* __restrict__ mean_out,
+                                                            float* __restrict__ rstd_out) {
+  constexpr int NV = PER / 8;
+  __shared__ float red[kLnThreads / 32];
+  const int64_t r0 = static_cast<int64_t>(blockIdx.x) * kLnFwdRows;
+  const int64_t r1 = min(T, r0 + kLnFwdRows);
+  const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+  uint4 cur[NV];
+#pragma unroll
+  for (int k = 0; k < NV; ++k) {
+    const int64_t c = (static_cast<int64_t>(k) * kLnThreads + threadIdx.x) * 8;
+    cur[k] = c < h ? *reinterpret_cast<const uint4*>(x + r0 * h + c) : zero;
+  }
+  for (int64_t r = r0; r < r1; ++r) {
+    uint4 nxt[NV];
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+      const int64_t c = (static_cast<int64_t>(k) * kLnThreads + threadIdx.x) * 8;
+      nxt[k] = (c < h && r + 1 < r1) ? *reinterpret_cast<const uint4*>(x + (r + 1) * h + c) : zero;
+    }
+    float v[PER];  // zero past h
+    float s = 0.f;
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+      unpack8(cur[k], v + 8 * k);
+#pragma unroll
+      for (int t = 0; t < 8; ++t) s += v[8 * k + t];
+    }
+    const float mean = block_sum(s, red) / static_cast<float>(h);
+    float q = 0.f;
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+      const int64_t c = (static_cast<int64_t>(k) * kLnThreads + threadIdx.x) * 8;
+#pragma unroll
+      for (int t = 0; t < 8; ++t) {
+        const float dlt = c < h ? v[8 * k + t] - mean : 0.f;
+        q += dlt * dlt;
+      }
+    }
+    const float rstd = rsqrtf(block_sum(q, red) / static_cast<float>(h) + eps);
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+      const int64_t c = (static_cast<int64_t>(k) * kLnThreads + threadIdx.x) * 8;
+      if (c < h) {
+        float gg[8], bb[8], o[8];
+        load8f(g + c, gg);
+        load8f(b + c, bb);
+#pragma unroll
+        for (int t = 0; t < 8; ++t) o[t] = (v[8 * k + t] - mean) * rstd * gg[t] + bb[t];
+        store8(y + r * h + c, o);
+      }
+      cur[k] = nxt[k];
+    }
+    if (threadIdx.x == 0) {
+      mean_out[r] = mean;
+      rstd_out[r] = rstd;
+    }
+  }
+}
+
+// A block takes kLnRows consecutive rows, in order: for each,
+// dx = rstd (dxhat - mean(dxhat) - xhat mean(dxhat xhat)) (+ dres), dxhat = dy g,
+// while the gain and bias gradient parts of the block's rows (sums of dy xhat
+// and of dy, rows in order) gather in registers; they go to
+// partial[block][0..h) and partial[block][h..2h).  The next row's dy and x and
+// this row's dres are loaded before this row's sums, so one pass over dy and x
+// gives both gradients.
+constexpr int kLnRows = 8;
+
+// Fixed-order block sums of two floats at once (all threads receive them).
+__device__ __forceinline__ float2 block_sum2(float a, float b, float2* red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    a += __shfl_xor_sync(0xffffffffu, a, o);
+    b += __shfl_xor_sync(0xffffffffu, b, o);
+  }
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __syncthreads();  // red is reused between rows
+  if (lane == 0) red[w] = make_float2(a, b);
+  __syncthreads();
+  float2 t = make_float2(0.f, 0.f);
+  for (int i = 0; i < kLnThreads / 32; ++i) {
+    t.x += red[i].x;
+    t.y += red[i].y;
+  }
+  return t;
+}
+
 template <int PER>
 __global__ void __launch_bounds__(kLnThreads) ln_bwd_kernel(
     const __nv_bfloat16* __restrict__ dy, const __nv_bfloat16* __restrict__ x,
     const float* __restrict__ g, const float* __restrict__ mean_in, const float* __restrict__ rstd_in,
-    const __nv_bfloat16* __restrict__ dres, int64_t h, __nv_bfloat16* __restrict__ dx) {
-  __shared__ float red[kLnThreads / 32];
-  const int64_t row = blockIdx.x;
-  const float mean = mean_in[row], rstd = rstd_in[row];
-  float xh[PER], dxh[PER];
-  float s1 = 0.f, s2 = 0.f;
+    const __nv_bfloat16* __restrict__ dres, int64_t T, int64_t h, __nv_bfloat16* __restrict__ dx,
+    float* __restrict__ partial) {
+  constexpr int NV = PER / 8;
+  __shared__ float2 red[kLnThreads / 32];
+  const int64_t r0 = static_cast<int64_t>(blockIdx.x) * kLnRows;
+  const int64_t r1 = min(T, r0 + kLnRows);
+  const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+  float gg[PER], ag[PER], ab[PER];
+  uint4 cd[NV], cx[NV];
 #pragma unroll
-  for (int k = 0; k < PER / 8; ++k) {
+  for (int k = 0; k < NV; ++k) {
     const int64_t c = (static_cast<int64_t>(k) * kLnThreads + threadIdx.x) * 8;
-    float d[8], xv[8], gg[8];
+    cd[k] = cx[k] = zero;
     if (c < h) {
-      load8(dy + row * h + c, d);
-      load8(x + row * h + c, xv);
-      load8f(g + c, gg);
+      load8f(g + c, gg + 8 * k);
+      cd[k] = *reinterpret_cast<const uint4*>(dy + r0 * h + c);
+      cx[k] = *reinterpret_cast<const uint4*>(x + r0 * h + c);
     } else {
 #pragma unroll
-      for (int t = 0; t < 8; ++t) d[t] = xv[t] = gg[t] = 0.f;
+      for (int t = 0; t < 8; ++t) gg[8 * k + t] = 0.f;
     }
 #pragma unroll
-    for (int t = 0; t < 8; ++t) {
-      const float xn = c < h ? (xv[t] - mean) * rstd : 0.f;
-      xh[8 * k + t] = xn;
-      dxh[8 * k + t] = d[t] * gg[t];
-      s1 += dxh[8 * k + t];
-      s2 += dxh[8 * k + t] * xn;
-    }
+    for (int t = 0; t < 8; ++t) ag[8 * k + t] = ab[8 * k + t] = 0.f;
   }
-  const float m1 = block_sum(s1, red) / static_cast<float>(h);
-  const float m2 = block_sum(s2, red) / static_cast<float>(h);
+  float mean = mean_in[r0], rstd = rstd_in[r0];
+  for (int64_t r = r0; r < r1; ++r) {
+    const bool more = r + 1 < r1;
+    uint4 nd[NV], nx[NV], rr[NV];
 #pragma unroll
-  for (int k = 0; k < PER / 8; ++k) {
+    for (int k = 0; k < NV; ++k) {
+      const int64_t c = (static_cast<int64_t>(k) * kLnThreads + threadIdx.x) * 8;
+      nd[k] = nx[k] = rr[k] = zero;
+      if (c < h) {
+        if (more) {
+          nd[k] = *reinterpret_cast<const uint4*>(dy + (r + 1) * h + c);
+          nx[k] = *reinterpret_cast<const uint4*>(x + (r + 1) * h + c);
+        }
+        if (dres) rr[k] = *reinterpret_cast<const uint4*>(dres + r * h + c);
+      }
+    }
+    const float nmean = more ? mean_in[r + 1] : 0.f, nrstd = more ? rstd_in[r + 1] : 0.f;
+    // columns past h hold dy = 0 and g = 0, so they add nothing below
+    float s1 = 0.f, s2 = 0.f;
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+      float d[8], xv[8];
+      unpack8(cd[k], d);
+      unpack8(cx[k], xv);
+#pragma unroll
+      for (int t = 0; t < 8; ++t) {
+        const float xn = (xv[t] - mean) * rstd, e = d[t] * gg[8 * k + t];
+        s1 += e;
+        s2 += e * xn;
+        ag[8 * k + t] += d[t] * xn;
+        ab[8 * k + t] += d[t];
+      }
+    }
+    const float2 m = block_sum2(s1, s2, red);
+    const float m1 = m.x / static_cast<float>(h), m2 = m.y / static_cast<float>(h);
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+      const int64_t c = (static_cast<int64_t>(k) * kLnThreads + threadIdx.x) * 8;
+      if (c < h) {
+        float d[8], xv[8], res[8], o[8];
+        unpack8(cd[k], d);
+        unpack8(cx[k], xv);
+        unpack8(rr[k], res);
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+          const float xn = (xv[t] - mean) * rstd;
+          o[t] = rstd * (d[t] * gg[8 * k + t] - m1 - xn * m2) + res[t];
+        }
+        store8(dx + r * h + c, o);
+      }
+      cd[k] = nd[k];
+      cx[k] = nx[k];
+    }
+    mean = nmean;
+    rstd = nrstd;
+  }
+  float* pp = partial + static_cast<int64_t>(blockIdx.x) * 2 * h;
+#pragma unroll
+  for (int k = 0; k < NV; ++k) {
     const int64_t c = (static_cast<int64_t>(k) * kLnThreads + threadIdx.x) * 8;
     if (c < h) {
-      float o[8], r[8];
-      if (dres) {
-        load8(dres + row * h + c, r);
-      } else {
 #pragma unroll
-        for (int t = 0; t < 8; ++t) r[t] = 0.f;
+      for (int t = 0; t < 8; t += 4) {
+        *reinterpret_cast<float4*>(pp + c + t) =
+            make_float4(ag[8 * k + t], ag[8 * k + t + 1], ag[8 * k + t + 2], ag[8 * k + t + 3]);
+        *reinterpret_cast<float4*>(pp + h + c + t) =
+            make_float4(ab[8 * k + t], ab[8 * k + t + 1], ab[8 * k + t + 2], ab[8 * k + t + 3]);
       }
-#pragma unroll
-      for (int t = 0; t < 8; ++t) o[t] = rstd * (dxh[8 * k + t] - m1 - xh[8 * k + t] * m2) + r[t];
-      store8(dx + row * h + c, o);
     }
-  }
-}
-
-// Gain and bias gradients, first level: block (x, y) sums dy xhat and dy over
-// rows [8 y, 8 (y + 1)) for eight columns per thread,
-// columns 8 (256 x + tid) ..; rows in order.  partial[y][0..h) = dg part,
-// partial[y][h..2h) = db part.
-constexpr int kLnColRows = 8;
-__global__ void __launch_bounds__(256) ln_param_grad_kernel(
-    const __nv_bfloat16* __restrict__ dy, const __nv_bfloat16* __restrict__ x,
-    const float* __restrict__ mean_in, const float* __restrict__ rstd_in, int64_t T, int64_t h,
-    float* __restrict__ partial) {
-  const int64_t c = (static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x) * 8;
-  if (c >= h) return;
-  const int64_t r0 = static_cast<int64_t>(blockIdx.y) * kLnColRows;
-  const int64_t r1 = min(T, r0 + kLnColRows);
-  float ag[8], ab[8];
-#pragma unroll
-  for (int t = 0; t < 8; ++t) ag[t] = ab[t] = 0.f;
-#pragma unroll 4
-  for (int64_t r = r0; r < r1; ++r) {
-    float d[8], xv[8];
-    load8(dy + r * h + c, d);
-    load8(x + r * h + c, xv);
-    const float mean = mean_in[r], rstd = rstd_in[r];
-#pragma unroll
-    for (int t = 0; t < 8; ++t) {
-      ag[t] += d[t] * ((xv[t] - mean) * rstd);
-      ab[t] += d[t];
-    }
-  }
-  float* pp = partial + static_cast<int64_t>(blockIdx.y) * 2 * h;
-#pragma unroll
-  for (int t = 0; t < 8; ++t) {
-    pp[c + t] = ag[t];
-    pp[h + c + t] = ab[t];
   }
 }
 
@@ -381,18 +437,18 @@ cudaError_t launch_ln_fwd(const void* x, const float* g, const float* b, int64_t
   if (T == 0) return cudaSuccess;
   const auto* xb = static_cast<const __nv_bfloat16*>(x);
   auto* yb = static_cast<__nv_bfloat16*>(y);
-  const unsigned grid = static_cast<unsigned>(T);
+  const unsigned grid = static_cast<unsigned>((T + kLnFwdRows - 1) / kLnFwdRows);
   switch (ln_per(h)) {
-    case 8: ln_fwd_kernel<8><<<grid, kLnThreads, 0, st>>>(xb, g, b, h, eps, yb, mean, rstd); break;
-    case 16: ln_fwd_kernel<16><<<grid, kLnThreads, 0, st>>>(xb, g, b, h, eps, yb, mean, rstd); break;
-    case 32: ln_fwd_kernel<32><<<grid, kLnThreads, 0, st>>>(xb, g, b, h, eps, yb, mean, rstd); break;
+    case 8: ln_fwd_kernel<8><<<grid, kLnThreads, 0, st>>>(xb, g, b, T, h, eps, yb, mean, rstd); break;
+    case 16: ln_fwd_kernel<16><<<grid, kLnThreads, 0, st>>>(xb, g, b, T, h, eps, yb, mean, rstd); break;
+    case 32: ln_fwd_kernel<32><<<grid, kLnThreads, 0, st>>>(xb, g, b, T, h, eps, yb, mean, rstd); break;
     default: return cudaErrorInvalidValue;
   }
   count_launches(1);
   return cudaGetLastError();
 }
 
-int ln_bwd_blocks(int64_t T) { return static_cast<int>((T + kLnColRows - 1) / kLnColRows); }
+int ln_bwd_blocks(int64_t T) { return static_cast<int>((T + kLnRows - 1) / kLnRows); }
 
 size_t ln_bwd_scratch_floats(int64_t T, int64_t h) {
   return static_cast<size_t>(ln_bwd_blocks(T)) * 2 * static_cast<size_t>(h);
@@ -406,8 +462,9 @@ cudaError_t launch_ln_bwd(const void* dy, const void* x, const float* g, const f
   const auto* xb = static_cast<const __nv_bfloat16*>(x);
   const auto* rb = static_cast<const __nv_bfloat16*>(dres);
   auto* dxb = static_cast<__nv_bfloat16*>(dx);
-  const unsigned grid = static_cast<unsigned>(T);
-#define TP_LNB(P) ln_bwd_kernel<P><<<grid, kLnThreads, 0, st>>>(dyb, xb, g, mean, rstd, rb, h, dxb)
+  const int ngroups = ln_bwd_blocks(T);
+  const unsigned grid = static_cast<unsigned>(ngroups);
+#define TP_LNB(P) ln_bwd_kernel<P><<<grid, kLnThreads, 0, st>>>(dyb, xb, g, mean, rstd, rb, T, h, dxb, partial)
   switch (ln_per(h)) {
     case 8: TP_LNB(8); break;
     case 16: TP_LNB(16); break;
@@ -415,12 +472,9 @@ cudaError_t launch_ln_bwd(const void* dy, const void* x, const float* g, const f
     default: return cudaErrorInvalidValue;
   }
 #undef TP_LNB
-  const int ngroups = ln_bwd_blocks(T);
-  const dim3 g1(static_cast<unsigned>((h / 8 + 255) / 256), static_cast<unsigned>(ngroups));
-  ln_param_grad_kernel<<<g1, 256, 0, st>>>(dyb, xb, mean, rstd, T, h, partial);
   ln_param_grad_sum_kernel<<<static_cast<unsigned>((2 * h + 31) / 32), 256, 0, st>>>(partial, ngroups, h, dg,
                                                                                       db, accumulate);
-  count_launches(3);
+  count_launches(2);
   return cudaGetLastError();
 }
 
