@@ -298,25 +298,29 @@ __global__ void __launch_bounds__(kLnThreads) ln_bwd_kernel(
 }
 
 // The groups' partials summed into dg and db (+ the existing values when
-// accumulating); 2h columns.  A block takes 32 columns (lane = column) and 8
-// slices (warp = slice): slice w sums groups w, w + 8, ... in order, then
-// slice 0 adds the slices in order (fixed order, deterministic).
-__global__ void __launch_bounds__(256) ln_param_grad_sum_kernel(const float* __restrict__ part2, int ngroups,
-                                                                int64_t h, float* __restrict__ dg,
-                                                                float* __restrict__ db, int accumulate) {
-  __shared__ float red[8][32];
+// accumulating); 2h columns.  A block takes 32 columns (lane = column) and
+// kLnSumSlices slices (warp = slice): slice w sums groups w, w + kLnSumSlices,
+// ... in order, then warp 0 adds the slices in order (fixed order,
+// deterministic).
+constexpr int kLnSumSlices = 32;
+__global__ void __launch_bounds__(32 * kLnSumSlices) ln_param_grad_sum_kernel(const float* __restrict__ part2,
+                                                                             int ngroups, int64_t h,
+                                                                             float* __restrict__ dg,
+                                                                             float* __restrict__ db,
+                                                                             int accumulate) {
+  __shared__ float red[kLnSumSlices][33];
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const int64_t c = static_cast<int64_t>(blockIdx.x) * 32 + lane;
   float s = 0.f;
   if (c < 2 * h) {
 #pragma unroll 4
-    for (int k = w; k < ngroups; k += 8) s += part2[static_cast<int64_t>(k) * 2 * h + c];
+    for (int k = w; k < ngroups; k += kLnSumSlices) s += part2[static_cast<int64_t>(k) * 2 * h + c];
   }
   red[w][lane] = s;
   __syncthreads();
   if (w != 0 || c >= 2 * h) return;
   float t = red[0][lane];
-  for (int k = 1; k < 8; ++k) t += red[k][lane];
+  for (int k = 1; k < kLnSumSlices; ++k) t += red[k][lane];
   float* out = c < h ? dg + c : db + (c - h);
   *out = accumulate ? *out + t : t;
 }
@@ -472,8 +476,8 @@ cudaError_t launch_ln_bwd(const void* dy, const void* x, const float* g, const f
     default: return cudaErrorInvalidValue;
   }
 #undef TP_LNB
-  ln_param_grad_sum_kernel<<<static_cast<unsigned>((2 * h + 31) / 32), 256, 0, st>>>(partial, ngroups, h, dg,
-                                                                                      db, accumulate);
+  ln_param_grad_sum_kernel<<<static_cast<unsigned>((2 * h + 31) / 32), 32 * kLnSumSlices, 0, st>>>(
+      partial, ngroups, h, dg, db, accumulate);
   count_launches(2);
   return cudaGetLastError();
 }
