@@ -323,7 +323,9 @@ typedef struct {
  *   out = h1 + dropout(M).
  * LayerNorm: biased variance, fp32 statistics and parameters, bf16 output.
  * x, out (T, h) bf16; saved as above.  Needs h % 16 == 0, h <= 8192, and the
- * constraints of the attention core and MLP entry points.
+ * constraints of the attention core and MLP entry points; s, d = h / n_heads
+ * and h' / N multiples of 8 (16-byte units for the bulk tensor copies), else
+ * TP_ERR_ALIGN before anything is launched.
  * tp_transformer_layer_bwd -- the gradient: dx (T, h) bf16 and the parameter
  * gradients (accumulate: add into them).  Both draw the dropout bits from the
  * config's streams; the backward draws them again.

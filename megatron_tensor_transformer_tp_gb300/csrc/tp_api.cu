@@ -386,11 +386,15 @@ tp_status launch_tc_groups(const Plan& pl, const bool* used, GemmGroup* groups, 
   // tiles, 6-stage ring, 32 KB loaded per SM per k-block instead of 48 KB) is
   // faster on large launches, K-major or MN-major; the one-SM kernel (128 x 256
   // tiles) on small ones, where its finer tiles balance better across SMs.
+  // Causal attention outputs count the tiles that hold work: about half, plus
+  // the diagonal.
   bool pair = g_gemm_mode == 1;
   if (g_gemm_mode == 2) {
     int64_t tiles128 = 0;
-    for (int i = 0; i < ng; ++i)
-      tiles128 += static_cast<int64_t>((groups[i].M + 127) / 128) * ((groups[i].N + 255) / 256);
+    for (int i = 0; i < ng; ++i) {
+      const int64_t rb = (groups[i].M + 127) / 128, t = rb * ((groups[i].N + 255) / 256);
+      tiles128 += groups[i].kr_mode != KR_NONE ? (t + rb) / 2 : t;
+    }
     pair = tiles128 > 8 * static_cast<int64_t>(dev->num_sms);
   }
   // Tile width: 256 for every output.  (128-wide tiles for the long dependent
@@ -1412,6 +1416,11 @@ tp_status layer_check(const tp_layer_config* c, const tp_layer_params* w) {
   if (c->h % 16 != 0 || c->h > 8192) return TP_ERR_INVALID;
   if (!(c->p_hidden >= 0.f && c->p_hidden < 1.f) || !drop_ok(c->p_attn, c->s) || !(c->eps > 0.f))
     return TP_ERR_INVALID;
+  // Bulk tensor copies need whole 16-byte units: the probabilities' row pitch
+  // s, every head's column offset (d) and every MLP shard's column offset
+  // (h'/N).  Checked here so that nothing is launched before the attention
+  // core or the MLP would refuse them.
+  if (c->s % 8 != 0 || (c->h / c->n_heads) % 8 != 0 || (c->hp / c->N) % 8 != 0) return TP_ERR_ALIGN;
   if (!w->g1 || !w->b1 || !w->g2 || !w->b2 || !shards_ok(w->Wqkv, c->N) || !shards_ok(w->Wo, c->N) ||
       !shards_ok(w->W, c->N) || !shards_ok(w->U, c->N) || !opt_shards_ok(w->bqkv, c->N) ||
       !opt_shards_ok(w->a, c->N))

@@ -268,6 +268,10 @@ def test_layer_validation():
     assert layer_fwd(layer_cfg(p_hidden=1.0))[0] == tp.TP_ERR_INVALID
     assert layer_fwd(layer_cfg(p_attn=0.1, s=200, T=400))[0] == tp.TP_ERR_INVALID  # s % 16 with dropout
     assert layer_fwd(layer_cfg(hp=2047))[0] == tp.TP_ERR_INVALID
+    # 16-byte units for the bulk tensor copies, refused before any launch
+    assert layer_fwd(layer_cfg(p_attn=0.0, s=45, T=90))[0] == tp.TP_ERR_ALIGN     # P row pitch
+    assert layer_fwd(layer_cfg(h=192, n_heads=48, N=2))[0] == tp.TP_ERR_ALIGN    # head width 4
+    assert layer_fwd(layer_cfg(hp=2056, N=2))[0] == tp.TP_ERR_ALIGN              # shard width 1028
     assert layer_fwd(layer_cfg(), ws_bytes=16)[0] == tp.TP_ERR_WORKSPACE
     assert layer_fwd(layer_cfg(T=0))[0] == tp.TP_OK
     c = layer_cfg()

@@ -169,6 +169,13 @@ def test_layer_parity_no_dropout_one_shard():
     check_layer(cfg, SI.layer_inputs(dict(cfg, b=2)))
 
 
+def test_layer_parity_s40_hidden_dropout_only():
+    """Three sequences of 40 tokens: every sequence ends inside a tile;
+    attention dropout off (it needs s % 16 == 0), hidden dropout on."""
+    cfg = dict(SMALL, s=40, p_attn=0.0, p_hidden=0.1, layer=3)
+    check_layer(cfg, SI.layer_inputs(dict(cfg, b=3)))
+
+
 def test_layer_deterministic():
     cfg = dict(SMALL)
     inp = SI.layer_inputs(dict(cfg, b=1))
