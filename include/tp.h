@@ -229,8 +229,9 @@ TP_API size_t tp_attn_core_workspace_size(int64_t T, int64_t s, int64_t h, int n
  * (e mod 16) / 4 at counter (e / 16, 0, 0, 0), kept iff it is >=
  * floor(p_attn * 65536) computed from the fp32 p_attn.  The backward draws the
  * same bits again.  p_attn > 0 needs s % 16 == 0, s <= 65535 and at most 65535
- * (sequence, head) pairs (TP_ERR_INVALID otherwise) and a non-NULL Pd.  Other arguments as tp_attn_core_fwd / _bwd; the
- * backward's dV is Pd^T dC and its dP is (dC V^T) * keep / (1 - p_attn).
+ * (sequence, head) pairs (TP_ERR_INVALID otherwise) and a non-NULL Pd.
+ * Other arguments as tp_attn_core_fwd / _bwd; the backward's dV is Pd^T dC
+ * and its dP is (dC V^T) * keep / (1 - p_attn).
  */
 TP_API tp_status tp_attn_core_dropout_fwd(tp_dtype dt, int64_t T, int64_t s, int64_t h, int n_heads,
                                           int N, int causal, float p_attn, uint64_t seed,
