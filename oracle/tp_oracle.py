@@ -112,7 +112,8 @@ def mlp_fwd(X, W_shards, a_shards, U_shards, b):
 
     [TP notes] §MLP层 (A by columns, B by rows, one all-reduce in forward).
     Returns Z (M,h') and Y (M,h') with shard i in columns [i h'/N, (i+1) h'/N),
-    and Out (M,h).
+    and Out (M,h).  Pinned through its two halves (unsharded equality, torch
+    float64 at N = 1) and the whole-block torch autograd check.
     """
     Z, Y = column_parallel_fwd(X, W_shards, a_shards)
     Out = row_parallel_fwd(Y, U_shards, b)
@@ -241,7 +242,8 @@ def attn_proj_bwd_weight_rows(dQKV, dO, X, C, N, qkv_rows, o_rows):
     evaluated only where asked, for full-size workloads):
     dWqkv_i[j] = dQKV_i[:, j]^T X for j in qkv_rows[i];
     dWo_i[k]   = dO[:, k]^T C_i   for k in o_rows[i];
-    and the bias gradients in full (column sums of dQKV_i and of dO)."""
+    and the bias gradients in full (column sums of dQKV_i and of dO).
+    Pinned by: equality with the rows of ``attn_proj_bwd``."""
     w = dQKV.shape[1] // N
     d = C.shape[1] // N
     dWqkv, dWo, dbqkv = [], [], []
@@ -276,7 +278,8 @@ def attention_head(q, k, v, causal, keep=None, p=0.0):
     out = P v; with attention dropout, out = (P * keep / (1 - p)) v.  The
     pages draw the single-head formula as a figure; the scaled dot product
     with the 1/sqrt(d) factor is the plain reading, and the causal mask is
-    GPT's.  Returns (P (s, s), out (s, d)), P before dropout."""
+    GPT's.  Returns (P (s, s), out (s, d)), P before dropout.  Pinned through
+    ``attention_core``: torch scaled_dot_product_attention in float64."""
     s, d = q.shape
     S = (q @ k.T) / math.sqrt(d)
     if causal:
@@ -293,7 +296,8 @@ def attention_head_grad(q, k, v, P, g, keep=None, p=0.0):
     S = q k^T / sqrt(d)):
         dv = Pd^T g,  dP = (g v^T) * keep / (1 - p),
         dS = P * (dP - sum_keys(P * dP)) / sqrt(d),  dq = dS k,  dk = dS^T q.
-    Masked entries have P = 0 and carry no gradient.  Returns (dq, dk, dv)."""
+    Masked entries have P = 0 and carry no gradient.  Returns (dq, dk, dv).
+    Pinned through ``attention_core_grad``: torch autograd in float64."""
     d = q.shape[1]
     Pd = P if keep is None else P * keep / (1.0 - p)
     dP = g @ v.T
@@ -305,7 +309,9 @@ def attention_head_grad(q, k, v, P, g, keep=None, p=0.0):
 
 def attention_keep(bi, j, s, n_heads, N, p, seed, layer):
     """Attention-dropout keep flags (s, s) of sequence bi, head j: elements
-    ((bi n_heads + j) s + query) s + key of the stream of head j's shard."""
+    ((bi n_heads + j) s + query) s + key of the stream of head j's shard.
+    Pinned through ``dropout_keep`` (numpy.random.Philox) and the planted
+    shared-stream test (the shards' masks must differ)."""
     if p <= 0.0:
         return None
     shard = j // (n_heads // N)
@@ -384,7 +390,9 @@ def vocab_mask(ids, start, end):
 def vocab_parallel_embed_partials(ids, E_shards, range_starts):
     """Per-range partial lookups: each range looks up the ids it owns and
     writes zero rows elsewhere ([Walkthrough] §VocabParallelEmbedding;
-    [TP notes] §输入层Embedding).  Returns a list of (T,h) fp64 partials."""
+    [TP notes] §输入层Embedding).  Returns a list of (T,h) fp64 partials.
+    Pinned through ``vocab_parallel_embed`` (the page's example, brute force)
+    and the planted wrong-range partial test."""
     parts = []
     for r, Er in enumerate(E_shards):
         masked, mask = vocab_mask(ids, range_starts[r], range_starts[r + 1])
@@ -594,7 +602,9 @@ def grad_scaler_update(state, found_inf, cfg):
 
 def unscale_and_check(grads, scale):
     """Main gradients divided by the loss scale, and whether any is inf/nan
-    across all groups ([Walkthrough] §MixedPrecisionOptimizer.step, step 2)."""
+    across all groups ([Walkthrough] §MixedPrecisionOptimizer.step, step 2).
+    Pinned through the optimizer-step tests (overflow skip, unscale before
+    the norm clip)."""
     out = [np.asarray(g, dtype=np.float64) / scale for g in grads]
     found_inf = any(not np.all(np.isfinite(g)) for g in out)
     return out, found_inf
@@ -761,7 +771,9 @@ def layernorm_grad(dy, x, g, mean, rstd):
 
 def dropout_residual(res, x, keep, p):
     """out = res + x * keep / (1 - p): the dropout after a row-parallel
-    linear and the residual add of [Walkthrough] §ParallelTransformerLayer."""
+    linear and the residual add of [Walkthrough] §ParallelTransformerLayer.
+    Pinned through the layer's torch autograd check and its planted unscaled
+    dropout."""
     return res + x * keep / (1.0 - p)
 
 
@@ -806,7 +818,8 @@ def transformer_layer_bwd(dout, saved, P, cfg):
     steps in reverse: the residual passes dout to h1 unchanged, the dropout
     scales by keep / (1 - p), then MLP, LayerNorm 2, attention output
     projection, attention core, QKV projection, LayerNorm 1.
-    Returns dx and the parameter gradients (same keys as P, prefixed d)."""
+    Returns dx and the parameter gradients (same keys as P, prefixed d).
+    Pinned by: torch autograd through the same layer in float64."""
     p = cfg["p_hidden"]
     dM = dout * saved["keep2"] / (1.0 - p)
     g = mlp_bwd(dM, saved["ln2"], P["W"], P["a"], P["U"])
@@ -831,7 +844,8 @@ def embed_position_dropout(words, pos_table, positions, keep, p):
     embeddings (the vocab-parallel lookup, summed over ranges) plus position
     embeddings, then dropout: (words + pos_table[positions]) * keep / (1 - p).
     A position outside the table adds a zero row (this build's reading: the
-    pages index in range only)."""
+    pages index in range only).  Pinned by: torch's embedding lookup (no
+    dropout), zero dropped entries and 1/(1 - p) survivors."""
     pos = np.asarray(positions)
     ok = (pos >= 0) & (pos < len(pos_table))
     pe = np.where(ok[:, None], np.asarray(pos_table, dtype=np.float64)[np.where(ok, pos, 0)], 0.0)

@@ -289,6 +289,23 @@ def test_attn_bwd_finite_differences():
     assert check_attn_bwd_fd(O) < 1e-7
 
 
+def test_attn_proj_weight_rows_equal_the_full_gradients():
+    """The sampled weight-gradient rows (used at full size) are the rows of the
+    finite-difference-pinned full gradients, in the order asked for (up to the
+    summation order of the library's matrix products: 1e-12 relative)."""
+    a = tiny_attn(M=6, h=16, N=4)
+    g = O.attn_proj_bwd(a["dQKV"], a["dO"], a["X"], a["C"], a["Ws"], a["Wos"])
+    qkv_rows = [[0, 5, 11], [3], [11, 2], [7, 7]]
+    o_rows = [[15, 0], [4], [9, 1, 2], [8]]
+    dWqkv, dWo, dbqkv, dbo = O.attn_proj_bwd_weight_rows(a["dQKV"], a["dO"], a["X"], a["C"], a["N"],
+                                                         qkv_rows, o_rows)
+    for i in range(a["N"]):
+        np.testing.assert_allclose(dWqkv[i], g["dWqkv"][i][qkv_rows[i]], rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(dWo[i], g["dWo"][i][o_rows[i]], rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(dbqkv[i], g["dbqkv"][i], rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(dbo, g["dbo"], rtol=1e-12, atol=1e-12)
+
+
 # ----------------------------------------------------------------------------
 # Attention core (per head, between the projections)
 # ----------------------------------------------------------------------------
@@ -1041,6 +1058,30 @@ def check_layer(mod):
 
 def test_transformer_layer_matches_torch_autograd():
     assert check_layer(O) < 1e-10
+
+
+def test_position_embedding_input_against_torch_embedding():
+    """The first layer's input: without dropout it is torch's embedding lookup
+    of the positions plus the words; with a keep mask the dropped entries are
+    exactly zero and the kept ones that sum divided by 1 - p (inverted
+    dropout); a position outside the table adds nothing."""
+    g = rng(31)
+    T, h, P = 12, 8, 10
+    words = g.standard_normal((T, h))
+    table = g.standard_normal((P, h))
+    pos = g.integers(0, P, T)
+    ref = torch.nn.functional.embedding(torch.tensor(pos), torch.tensor(table)).numpy() + words
+    out = O.embed_position_dropout(words, table, pos, np.ones((T, h)), 0.0)
+    np.testing.assert_allclose(out, ref, rtol=0, atol=1e-15)
+    keep = g.random((T, h)) >= 0.25
+    out = O.embed_position_dropout(words, table, pos, keep, 0.25)
+    assert np.all(out[~keep] == 0.0)
+    np.testing.assert_allclose(out[keep] * 0.75, ref[keep], rtol=1e-15, atol=1e-15)
+    bad = pos.copy()
+    bad[[0, 5]] = [-1, P]
+    out = O.embed_position_dropout(words, table, bad, np.ones((T, h)), 0.0)
+    np.testing.assert_array_equal(out[[0, 5]], words[[0, 5]])
+    np.testing.assert_allclose(np.delete(out, [0, 5], 0), np.delete(ref, [0, 5], 0), rtol=0, atol=1e-15)
 
 
 def test_planted_unbiased_layernorm_variance_is_caught(monkeypatch):
