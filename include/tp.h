@@ -329,7 +329,8 @@ typedef struct {
  * TP_ERR_ALIGN before anything is launched.
  * tp_transformer_layer_bwd -- the gradient: dx (T, h) bf16 and the parameter
  * gradients (accumulate: add into them).  Both draw the dropout bits from the
- * config's streams; the backward draws them again.
+ * config's streams; the backward draws the hidden-dropout bits again, and the
+ * attention-dropout bits too unless saved->attn_keep holds the forward's.
  */
 /*
  * tp_position_embed_dropout -- the first layer's input ([Walkthrough]
