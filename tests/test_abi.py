@@ -191,11 +191,13 @@ def test_adam_step_validation():
     assert adam([group(n=0, param=None, grad=None)], 1, ws=None) == tp.TP_ERR_WORKSPACE
 
 
-def test_optimizer_struct_layout_matches_header(tmp_path):
+def test_struct_layouts_match_header(tmp_path):
     """The binding's ctypes structures have the C header's sizes and offsets."""
     src = tmp_path / "layout.c"
     fields = {"tp_optimizer_state": tp.tp_optimizer_state, "tp_adam_config": tp.tp_adam_config,
-              "tp_param_group": tp.tp_param_group}
+              "tp_param_group": tp.tp_param_group, "tp_layer_config": tp.tp_layer_config,
+              "tp_layer_params": tp.tp_layer_params, "tp_layer_saved": tp.tp_layer_saved,
+              "tp_layer_grads": tp.tp_layer_grads}
     lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "tp.h"', 'int main(void) {']
     for name, cls in fields.items():
         lines.append(f'printf("{name} %zu\\n", sizeof({name}));')
