@@ -85,43 +85,78 @@ __global__ void sort_histogram(const int64_t* __restrict__ ids, int64_t T, int64
 }
 
 // Single-CTA exclusive scan of counts[0..V) into offsets[0..V]; counts is
-// reset to zero for reuse as the scatter cursor.
+// reset to zero for reuse as the scatter cursor.  The counts go through in
+// chunks of 4 x SCAN_THREADS (four consecutive per thread, one 16-byte load),
+// SCAN_DEPTH chunks in flight ahead of the one being scanned; a running total
+// carries from chunk to chunk.
 constexpr int SCAN_THREADS = 1024;
+constexpr int SCAN_CHUNK = 4 * SCAN_THREADS;
+constexpr int SCAN_DEPTH = 4;
+
+__device__ __forceinline__ int4 scan_load4(const int* counts, int64_t V, int64_t v) {
+  if (v + 3 < V) return *reinterpret_cast<const int4*>(counts + v);  // v % 4 == 0, base 256-aligned
+  int4 q = make_int4(0, 0, 0, 0);
+  if (v < V) q.x = counts[v];
+  if (v + 1 < V) q.y = counts[v + 1];
+  if (v + 2 < V) q.z = counts[v + 2];
+  return q;
+}
+
 __global__ void __launch_bounds__(SCAN_THREADS) sort_scan(int* __restrict__ counts, int64_t V,
                                                           int* __restrict__ offsets) {
   __shared__ int warp_sums[SCAN_THREADS / 32];
-  const int64_t per = (V + SCAN_THREADS - 1) / SCAN_THREADS;
-  const int64_t b = threadIdx.x * per;
-  const int64_t e = b + per < V ? b + per : V;
-  int local = 0;
-  for (int64_t v = b; v < e; ++v) local += counts[v];
-  // block-wide exclusive scan of `local`
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  int incl = local;
+  const int64_t nch = (V + SCAN_CHUNK - 1) / SCAN_CHUNK;
+  int4 q[SCAN_DEPTH];
 #pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += y;
-  }
-  if (lane == 31) warp_sums[w] = incl;
-  __syncthreads();
-  if (w == 0) {
-    int x = warp_sums[lane];
+  for (int d = 0; d < SCAN_DEPTH; ++d)
+    q[d] = scan_load4(counts, V, static_cast<int64_t>(d) * SCAN_CHUNK + 4 * threadIdx.x);
+  int carry = 0;
+  for (int64_t c0 = 0; c0 < nch; c0 += SCAN_DEPTH) {
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, x, o);
-      if (lane >= o) x += y;
+    for (int d = 0; d < SCAN_DEPTH; ++d) {
+      const int64_t c = c0 + d;
+      if (c >= nch) break;  // the same for every thread
+      const int64_t v = c * SCAN_CHUNK + 4 * threadIdx.x;
+      const int4 x = q[d];
+      q[d] = scan_load4(counts, V, v + static_cast<int64_t>(SCAN_DEPTH) * SCAN_CHUNK);
+      const int s0 = x.x, s1 = s0 + x.y, s2 = s1 + x.z, tot = s2 + x.w;
+      int incl = tot;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      if (lane == 31) warp_sums[w] = incl;
+      __syncthreads();
+      if (w == 0) {
+        int y = warp_sums[lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int z = __shfl_up_sync(0xffffffffu, y, o);
+          if (lane >= o) y += z;
+        }
+        warp_sums[lane] = y;  // inclusive over warps
+      }
+      __syncthreads();
+      const int e = carry + incl - tot + (w > 0 ? warp_sums[w - 1] : 0);
+      const int chunk_total = warp_sums[SCAN_THREADS / 32 - 1];
+      if (v + 3 < V) {
+        *reinterpret_cast<int4*>(offsets + v) = make_int4(e, e + s0, e + s1, e + s2);
+        *reinterpret_cast<int4*>(counts + v) = make_int4(0, 0, 0, 0);
+      } else {
+        const int ev[3] = {e, e + s0, e + s1};
+        for (int j = 0; j < 3; ++j)
+          if (v + j < V) {
+            offsets[v + j] = ev[j];
+            counts[v + j] = 0;
+          }
+      }
+      carry += chunk_total;
+      __syncthreads();  // warp_sums is rewritten by the next chunk
     }
-    warp_sums[lane] = x;  // inclusive over warps
   }
-  __syncthreads();
-  int run = incl - local + (w > 0 ? warp_sums[w - 1] : 0);
-  for (int64_t v = b; v < e; ++v) {
-    offsets[v] = run;
-    run += counts[v];
-    counts[v] = 0;
-  }
-  if (threadIdx.x == SCAN_THREADS - 1) offsets[V] = warp_sums[SCAN_THREADS / 32 - 1];
+  if (threadIdx.x == 0) offsets[V] = carry;
 }
 
 __global__ void sort_scatter(const int64_t* __restrict__ ids, int64_t T, int64_t V,
