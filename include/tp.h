@@ -36,7 +36,10 @@
  *    memory (an error word, tile-scheduler and tile-completion counters, a
  *    16 x 64 block of ones) and it never frees caller memory.  Launches
  *    rotate over 64 counter slots, so at most 64 launches may be in flight
- *    at the same time across all streams of a device.
+ *    at the same time across all streams of a device.  A call captured into a
+ *    CUDA graph keeps the slot it was given at capture: replay such a graph
+ *    on one stream at a time (replays in sequence reuse the slot safely, since
+ *    every launch resets its counters as it ends).
  *  - Execution: work is enqueued asynchronously on `stream` (a cudaStream_t
  *    passed as void*; NULL = legacy default stream).  Argument errors return
  *    synchronously before any launch.  Device-side errors (a bounded wait that
