@@ -387,15 +387,23 @@ tp_status launch_tc_groups(const Plan& pl, const bool* used, GemmGroup* groups, 
   // faster on large launches, K-major or MN-major; the one-SM kernel (128 x 256
   // tiles) on small ones, where its finer tiles balance better across SMs.
   // Causal attention outputs count the tiles that hold work: about half, plus
-  // the diagonal.
+  // the diagonal.  Launches of very long contractions (over 1000 k-blocks of
+  // tiles per SM, e.g. a shard sum over a whole vocabulary range) also take
+  // the two-SM kernel once they hold two one-SM tiles per SM: there the lower
+  // operand traffic per SM pays and the tile count no longer sets the balance.
   bool pair = g_gemm_mode == 1;
   if (g_gemm_mode == 2) {
-    int64_t tiles128 = 0;
+    int64_t tiles128 = 0, kb_tiles = 0;
     for (int i = 0; i < ng; ++i) {
       const int64_t rb = (groups[i].M + 127) / 128, t = rb * ((groups[i].N + 255) / 256);
-      tiles128 += groups[i].kr_mode != KR_NONE ? (t + rb) / 2 : t;
+      const int64_t tw = groups[i].kr_mode != KR_NONE ? (t + rb) / 2 : t;
+      int64_t kb = 0;
+      for (int sidx = groups[i].seg_begin; sidx < groups[i].seg_end; ++sidx) kb += (pl.seg[sidx].K + 63) / 64;
+      tiles128 += tw;
+      kb_tiles += tw * kb;
     }
-    pair = tiles128 > 8 * static_cast<int64_t>(dev->num_sms);
+    const int64_t sms = dev->num_sms;
+    pair = tiles128 > 8 * sms || (tiles128 >= 2 * sms && kb_tiles > 1000 * sms);
   }
   // Tile width: 256 for every output.  (128-wide tiles for the long dependent
   // contractions of small fused launches were measured slower on GB300: a
