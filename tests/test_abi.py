@@ -286,3 +286,85 @@ def test_position_embed_dropout_validation():
     assert f(8, 64, 16, FAKE, FAKE, FAKE, 1.5, 1, 2, FAKE, None) == tp.TP_ERR_INVALID
     assert f(8, 64, 16, FAKE + 2, FAKE, FAKE, 0.1, 1, 2, FAKE, None) == tp.TP_ERR_ALIGN
     assert f(0, 64, 16, None, None, None, 0.1, 1, 2, None, None) == tp.TP_OK
+
+
+def layer_bwd(cfg, ws_bytes=1 << 34, grads_null_shard=False, dout=FAKE):
+    """tp_transformer_layer_bwd with fake device pointers and real host shard arrays."""
+    import ctypes as C
+    sh = ptrs(2)
+    vp = lambda a: C.cast(a[0], C.c_void_p).value
+    w = tp.tp_layer_params(FAKE, FAKE, vp(sh), None, vp(sh), None, FAKE, FAKE, vp(sh), None, vp(sh), None)
+    sv = tp.tp_layer_saved(*([FAKE] * 13 + [None]))
+    dsh = ptrs(2)
+    bad = (C.c_void_p * 2)(FAKE, None)
+    dW = C.cast(bad, C.c_void_p).value if grads_null_shard else vp(dsh)
+    g = tp.tp_layer_grads(FAKE, FAKE, vp(dsh), None, vp(dsh), FAKE, FAKE, FAKE, dW, None, vp(dsh), FAKE)
+    return L.tp_transformer_layer_bwd(C.byref(cfg), C.byref(w), FAKE, C.byref(sv), dout, FAKE, C.byref(g),
+                                      0, FAKE * 256, ws_bytes, None), (sh, dsh, bad)
+
+
+def test_layer_backward_validation():
+    assert layer_bwd(layer_cfg(T=500))[0] == tp.TP_ERR_INVALID                     # T % s
+    assert layer_bwd(layer_cfg(p_attn=0.0, s=45, T=90))[0] == tp.TP_ERR_ALIGN       # P row pitch
+    assert layer_bwd(layer_cfg(), grads_null_shard=True)[0] == tp.TP_ERR_INVALID    # a NULL dW shard
+    assert layer_bwd(layer_cfg(), ws_bytes=16)[0] == tp.TP_ERR_WORKSPACE
+    assert layer_bwd(layer_cfg(), dout=FAKE + 8)[0] == tp.TP_ERR_ALIGN
+    assert layer_bwd(layer_cfg(T=0))[0] == tp.TP_OK
+
+
+def test_attn_proj_backward_validation():
+    w, o, dw, dwo = ptrs(4), ptrs(4), ptrs(4), ptrs(4)
+    f = L.tp_attn_proj_bwd
+    # heads not divisible by shards
+    assert f(tp.TP_BF16, 64, 512, 6, 4, FAKE, FAKE, FAKE, FAKE, w[0], o[0], FAKE, FAKE, dw[0], None,
+             dwo[0], None, 0, None) == tp.TP_ERR_INVALID
+    # a NULL weight-gradient shard
+    bad = (ctypes.c_void_p * 4)(FAKE, FAKE, None, FAKE)
+    badp = ctypes.cast(bad, ctypes.POINTER(ctypes.c_void_p))
+    assert f(tp.TP_BF16, 64, 512, 8, 4, FAKE, FAKE, FAKE, FAKE, w[0], o[0], FAKE, FAKE, badp, None,
+             dwo[0], None, 0, None) == tp.TP_ERR_INVALID
+    # dQKV off its 16-byte boundary: refused on the host
+    assert f(tp.TP_BF16, 64, 512, 8, 4, FAKE + 2, FAKE, FAKE, FAKE, w[0], o[0], FAKE, FAKE, dw[0], None,
+             dwo[0], None, 0, None) == tp.TP_ERR_ALIGN
+    assert f(7, 64, 512, 8, 4, FAKE, FAKE, FAKE, FAKE, w[0], o[0], FAKE, FAKE, dw[0], None,
+             dwo[0], None, 0, None) == tp.TP_ERR_UNSUPPORTED
+
+
+def test_vocab_logits_validation():
+    e, lg = ptrs(2), ptrs(2)
+    rs = rs_arr([0, 100, 250])
+    f = L.tp_vocab_logits
+    assert f(tp.TP_BF16, 64, 64, 250, 2, FAKE, e[0], rs_arr([0, 100, 251]), lg[0], rs_arr([104, 152]),
+             None) == tp.TP_ERR_INVALID                                    # ranges do not end at V
+    assert f(tp.TP_BF16, 64, 64, 250, 2, FAKE, e[0], rs, lg[0], rs_arr([104, 144]),
+             None) == tp.TP_ERR_INVALID                                    # pitch below the range width
+    assert f(tp.TP_BF16, 64, 64, 250, 2, FAKE, e[0], rs, lg[0], None, None) == tp.TP_ERR_INVALID
+    assert f(tp.TP_BF16, 64, 64, 250, 2, FAKE + 2, e[0], rs, lg[0], rs_arr([104, 152]),
+             None) == tp.TP_ERR_ALIGN                                      # X off 16 bytes
+    assert f(tp.TP_BF16, 0, 64, 250, 2, None, e[0], rs, None, rs_arr([104, 152]), None) == tp.TP_OK
+
+
+def test_attn_core_dropout_validation():
+    def fwd(p, s=256, T=512, Pd=FAKE):
+        return L.tp_attn_core_dropout_fwd(tp.TP_BF16, T, s, 512, 4, 2, 1, p, 1, 0, FAKE, FAKE, Pd, FAKE,
+                                          None, FAKE * 256, 1 << 30, None)
+    assert fwd(1.0) == tp.TP_ERR_INVALID                  # p must be below 1
+    assert fwd(-0.1) == tp.TP_ERR_INVALID
+    assert fwd(0.1, s=200, T=400) == tp.TP_ERR_INVALID    # attention dropout needs s % 16 == 0
+    assert fwd(0.1, Pd=None) == tp.TP_ERR_INVALID         # the dropped probabilities need a buffer
+    bwd = L.tp_attn_core_dropout_bwd(tp.TP_BF16, 400, 200, 512, 4, 2, 1, 0.1, 1, 0, FAKE, FAKE, FAKE, FAKE,
+                                     FAKE, FAKE, FAKE * 256, 1 << 30, None)
+    assert bwd == tp.TP_ERR_INVALID
+
+
+def test_tied_grad_noalloc_refuses_sizes_beyond_its_scratch():
+    e, d = ptrs(2), ptrs(2)
+    V = 1 << 20
+    rs = rs_arr([0, V // 2, V])
+    ld = rs_arr([V // 2, V // 2])
+    assert tp.tied_embed_grad_workspace_size(1 << 16, V) > (3 << 19)     # beyond 1.5 MiB
+    assert L.tied_embed_grad_noalloc(tp.TP_BF16, 1 << 16, 64, V, 2, FAKE, FAKE, FAKE, d[0], ld, rs, e[0],
+                                     0, None) == tp.TP_ERR_WORKSPACE
+    assert L.tied_embed_grad_noalloc(tp.TP_BF16, -1, 64, V, 2, FAKE, FAKE, FAKE, d[0], ld, rs, e[0],
+                                     0, None) == tp.TP_ERR_INVALID
+    # (its other argument checks are tied_embed_grad's, made after it looks up its device scratch)
