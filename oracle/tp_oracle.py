@@ -131,38 +131,47 @@ def mlp_bwd(dOut, X, W_shards, a_shards, U_shards):
         da_i = column sums of dZ_i,  db = column sums of dOut
         dX   = sum_i dZ_i W_i
     Z_i, Y_i are recomputed here in fp64 from X (the oracle never takes values
-    from the device).  Returns a dict of fp64 arrays (dW, dU, da are lists).
-    Pinned by: central finite differences on tiny shapes, unsharded dX.
+    from the device).  Returns a dict of fp64 arrays (dW, dU, da are lists;
+    dZ is (M, h') with shard i in columns [i h'/N, (i+1) h'/N), the layout of
+    Z).
+    Pinned by: central finite differences on tiny shapes (of X, W, U, a, b
+    and of the saved pre-activation Z itself), torch float64 autograd of the
+    unsharded block (including the gradient at the first linear's output),
+    unsharded dX.
     """
     Z, Y = column_parallel_fwd(X, W_shards, a_shards)
-    dW, dU, da = [], [], []
+    dW, dU, da, dZ = [], [], [], []
     dX = None
     for i in range(len(W_shards)):
         dYi = dOut @ U_shards[i]
         dZi = dYi * gelu_prime(Z[i])
+        dZ.append(dZi)
         dU.append(dOut.T @ Y[i])
         dW.append(dZi.T @ X)
         da.append(dZi.sum(axis=0))
         part = dZi @ W_shards[i]
         dX = part if dX is None else dX + part
-    out = dict(dX=dX, dW=dW, dU=dU, da=da, db=dOut.sum(axis=0))
+    out = dict(dX=dX, dW=dW, dU=dU, da=da, db=dOut.sum(axis=0), dZ=np.concatenate(dZ, axis=1))
     return out
 
 
 def mlp_bwd_sampled(dOut, X, W_shards, a_shards, U_shards, rows, units):
     """The same definitions as ``mlp_bwd``, evaluated only where asked.
 
-    ``rows``: token indices r for which dX[r] is formed (dX is row-local).
+    ``rows``: token indices r for which dZ[r] and dX[r] are formed (both are
+    row-local).
     ``units``: per shard, the FFN units j for which column j of dZ_i is formed
     over all tokens, giving row j of dW_i, column j of dU_i and da_i[j].
     Used at full workload sizes where the whole fp64 backward is too slow.
     """
-    # dX rows: dZ_i[r] needs only X[r] and dOut[r]
+    # dZ and dX rows: dZ_i[r] needs only X[r] and dOut[r]
     Xr, dOr = X[rows], dOut[rows]
     Zr, _ = column_parallel_fwd(Xr, W_shards, a_shards)
     dXr = None
+    dZrows = []
     for i in range(len(W_shards)):
         dZr = (dOr @ U_shards[i]) * gelu_prime(Zr[i])
+        dZrows.append(dZr)
         part = dZr @ W_shards[i]
         dXr = part if dXr is None else dXr + part
     dW, dU, da = [], [], []
@@ -175,7 +184,8 @@ def mlp_bwd_sampled(dOut, X, W_shards, a_shards, U_shards, rows, units):
         dW.append(dZj.T @ X)
         dU.append(dOut.T @ gelu(Zj))
         da.append(dZj.sum(axis=0))
-    return dict(dX_rows=dXr, dW_rows=dW, dU_cols=dU, da=da, db=dOut.sum(axis=0))
+    return dict(dX_rows=dXr, dZ_rows=np.concatenate(dZrows, axis=1), dW_rows=dW, dU_cols=dU, da=da,
+                db=dOut.sum(axis=0))
 
 
 # --------------------------------------------------------------------------

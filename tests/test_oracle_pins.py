@@ -189,6 +189,15 @@ def check_mlp_bwd_fd(mod):
         worst = max(worst, np.max(np.abs(grads["da"][i] - fd_grad(lambda: mlp_loss(mod, d, As=As), As[i]))))
     b = d["b"].copy()
     worst = max(worst, np.max(np.abs(grads["db"] - fd_grad(lambda: mlp_loss(mod, d, b=b), b))))
+    # the saved pre-activation: Out as a function of Z alone (Y = GELU(Z), then
+    # the row-parallel sum), differentiated numerically at the forward's Z
+    Z, _, _ = mod.mlp_fwd(d["X"], d["Ws"], d["As"], d["Us"], d["b"])
+    n = Z.shape[1] // d["N"]
+
+    def loss_of_z():
+        Y = [mod.gelu(Z[:, i * n:(i + 1) * n]) for i in range(d["N"])]
+        return float(np.sum(mod.row_parallel_fwd(Y, d["Us"], d["b"]) * d["dOut"]))
+    worst = max(worst, np.max(np.abs(grads["dZ"] - fd_grad(loss_of_z, Z))))
     return worst
 
 
@@ -200,9 +209,12 @@ def test_mlp_bwd_matches_torch_autograd_unsharded():
     d = tiny_mlp(5, M=6, h=8, hp=32, N=4)
     t = lambda x: torch.tensor(x, dtype=torch.float64, requires_grad=True)
     X, W, a, U, b = t(d["X"]), t(d["W"]), t(d["a"]), t(d["U"]), t(d["b"])
-    out = F.linear(F.gelu(F.linear(X, W, a), approximate="none"), U, b)
+    z = F.linear(X, W, a)
+    z.retain_grad()
+    out = F.linear(F.gelu(z, approximate="none"), U, b)
     (out * torch.tensor(d["dOut"])).sum().backward()
     g = O.mlp_bwd(d["dOut"], d["X"], d["Ws"], d["As"], d["Us"])
+    assert np.max(np.abs(g["dZ"] - z.grad.numpy())) < 1e-12
     assert np.max(np.abs(g["dX"] - X.grad.numpy())) < 1e-12
     assert np.max(np.abs(np.concatenate(g["dW"], 0) - W.grad.numpy())) < 1e-12
     assert np.max(np.abs(np.concatenate(g["dU"], 1) - U.grad.numpy())) < 1e-12
@@ -217,6 +229,7 @@ def test_mlp_bwd_sampled_equals_full():
     units = [[0, 5], [1], [2, 3, 7], [6]]
     s = O.mlp_bwd_sampled(d["dOut"], d["X"], d["Ws"], d["As"], d["Us"], rows, units)
     assert np.max(np.abs(s["dX_rows"] - full["dX"][rows])) < 1e-12
+    assert np.max(np.abs(s["dZ_rows"] - full["dZ"][rows])) < 1e-12
     for i, J in enumerate(units):
         assert np.max(np.abs(s["dW_rows"][i] - full["dW"][i][J])) < 1e-12
         assert np.max(np.abs(s["dU_cols"][i] - full["dU"][i][:, J])) < 1e-12
@@ -619,6 +632,18 @@ def test_planted_tanh_gelu_is_caught(monkeypatch):
 def test_planted_gelu_prime_dropped_term_is_caught(monkeypatch):
     monkeypatch.setattr(O, "gelu_prime", lambda z: 0.5 * (1 + O._erf(np.asarray(z) / math.sqrt(2))))
     assert check_gelu_prime(O) > 1e-3
+    assert check_mlp_bwd_fd(O) > 1e-3
+
+
+def test_planted_dz_from_wrong_shard_is_caught(monkeypatch):
+    real = O.mlp_bwd
+
+    def broken(*args, **kw):
+        g = real(*args, **kw)
+        n = g["dZ"].shape[1] // 2
+        g["dZ"] = np.concatenate([g["dZ"][:, n:], g["dZ"][:, :n]], axis=1)  # shards swapped
+        return g
+    monkeypatch.setattr(O, "mlp_bwd", broken)
     assert check_mlp_bwd_fd(O) > 1e-3
 
 
