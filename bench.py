@@ -4,9 +4,10 @@
                     [--workload NAME] [--no-rows]
 
 Prints ONE JSON line (rank 0).  The headline step is one forward + backward of
-the tensor-parallel MLP block (tp_mlp_fwd + tp_mlp_bwd) on the workload
-b=4, s=1024, h=1024, h'=4096, N=4 shards, bf16 with fp32 accumulation; the
-metric is its throughput in TFLOP/s (12*M*h*h' algorithmic FLOPs per step).
+the tensor-parallel MLP block (tp_mlp_fwd + tp_mlp_bwd) at the pages' model
+width: b=2, s=2048, h=4096, h'=16384, N=2 shards, bf16 with fp32
+accumulation; the metric is its throughput in TFLOP/s (12*M*h*h' algorithmic
+FLOPs per step).
 Inputs are synthetic and seeded (synthetic_inputs.py) and resident in HBM when
 the timed region starts; L2 is flushed (a 256 MiB write) before every timed
 step and the flush is outside the per-step events.
@@ -16,9 +17,12 @@ events taken by the library on the launching stream during the timed region),
 the end-to-end number through the C ABI with host buffers (pinned host->device
 copies of the step's inputs and device->host reads of its outputs inside the
 timed region), the clocks sampled by nvidia-smi during the timed region, the
-other rows of the block (embedding gather GB/s, attention projections, the
-model-width MLP, logits, tied gradient), and the fp64 CPU oracle timed on a
-bounded sample as a reported baseline.
+embedding gather's GB/s (the metric's second half) at top level, one short
+entry per other row (the smaller MLP, attention projections, logits and tied
+gradient, cross-entropy, attention core, transformer layer, Adam step), and
+the fp64 CPU oracle timed on a bounded sample as a reported baseline.  The
+line is kept short; every row's full per-kernel list goes to the file named
+by --detail.
 
 Multi-GPU: the block runs on one GPU; under torchrun every rank runs an
 independent replica (no collective on the data path) and the line reports the
@@ -44,7 +48,8 @@ if ROOT not in sys.path:
 import synthetic_inputs as SI  # noqa: E402
 
 METRIC = "TP-MLP fwd+bwd TFLOP/s (% BF16 peak); embed gather GB/s (% HBM)"
-DEFAULT_WORKLOAD = "mlp_b4_s1024_h1024_hp4096_N4"
+DEFAULT_WORKLOAD = "mlp_b2_s2048_h4096_hp16384_N2"
+DEFAULT_DETAIL = os.path.join("gpurun_out", "bench_detail.json")
 L2_FLUSH_BYTES = 256 << 20
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
@@ -625,6 +630,44 @@ def roofline_for(tp, bench, prof, peaks, peak_src, sustained=True):
     return top, out
 
 
+def workload_config(name: str, n_ranks: int) -> dict:
+    """The `config` object of the JSON line: the workload's name and sizes
+    (shared by both arms, so the two lines name the same workload)."""
+    cfg = SI.WORKLOADS[name]
+    out = {"workload": name, **{k: v for k, v in cfg.items() if k not in ("kind", "seed")},
+           "parallelism": f"replicas{n_ranks}" if n_ranks > 1 else "single-gpu, N logical shards",
+           "l2": "flushed before every timed step (256 MiB write)"}
+    return out
+
+
+def r4(x):
+    """Four significant digits (keeps the printed line short)."""
+    return None if x is None else float(f"{x:.4g}")
+
+
+def compact_row(name, row):
+    """One secondary row in the printed line: value, unit, ms per step and the
+    fraction of peak of its two kernels with the most device time."""
+    top = sorted(row["kernels"], key=lambda k: -k["share"])[:2]
+    return {"value": r4(row["value"]), "unit": row["unit"], "ms": r4(row["ms_per_step"]),
+            "frac": {k["kernel"]: r4(k["frac"]) for k in top}}
+
+
+def write_detail(path, detail):
+    """Full per-kernel lists of every row, written next to the run's outputs."""
+    if not path:
+        return None
+    try:
+        d = os.path.dirname(path)
+        if d:
+            os.makedirs(d, exist_ok=True)
+        with open(path, "w") as f:
+            json.dump(detail, f, indent=1)
+        return path
+    except OSError:
+        return None
+
+
 # ----------------------------------------------------------------------------
 # the oracle as CPU baseline / reference arm
 # ----------------------------------------------------------------------------
@@ -705,8 +748,7 @@ def run_reference(args):
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded normals; no dataset)",
-            "config": {"workload": wl, "b": cfg["b"], "s": cfg["s"], "h": cfg["h"], "hp": cfg["hp"],
-                       "N": cfg["N"], "sample_tokens": tokens},
+            "config": workload_config(wl, args.gpus),
             "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
                              "sample": f"fp64 numpy oracle MLP fwd+bwd on {tokens} of "
                                        f"{orc.M_full} tokens per step, same weights"},
@@ -727,6 +769,8 @@ def main(argv=None):
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-rows", action="store_true", help="skip the secondary rows")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--detail", default=DEFAULT_DETAIL,
+                    help="file for every row's per-kernel list ('' to skip)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -783,8 +827,7 @@ def main(argv=None):
         e2e = {"value": aggregate_throughput(e_units, e_sec) / scale, "unit": unit,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": e_sec / n_e2e * 1e3,
-               "how": "pinned host inputs copied and results read back every step, on two streams "
-                      "overlapping the neighbouring steps' compute (two device buffer sets)"}
+               "how": "pinned host copies in and out every step"}
 
     # ---- secondary rows -----------------------------------------------------
     rows = {}
@@ -795,36 +838,39 @@ def main(argv=None):
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline and cfg["kind"] == "mlp":
         tf, el, reps, tokens = oracle_mlp_sample(args.workload, 256, 10.0, 30.0)
-        cpu = {"value": tf, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
-               "sample": f"fp64 numpy oracle MLP fwd+bwd on {tokens} of {bench.M} tokens "
-                         f"(same weights), {reps} repeats in {el:.1f} s"}
+        cpu = {"value": r4(tf), "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
+               "sample": f"fp64 oracle fwd+bwd, {tokens} of {bench.M} tokens, same weights, "
+                         f"{reps}x in {el:.1f} s"}
 
     if rank != 0:
         return 0
-    gather = rows.get("embed_gather") if rows else None
+    gather = rows.pop("embed_gather", None) if rows else None
+    detail = {"headline": {"workload": args.workload, "kernels": kernels},
+              "embed_gather": gather, "rows": rows}
+    detail_path = write_detail(args.detail, detail)
     line = {
-        "metric": METRIC, "value": value, "unit": unit, "n_gpus": ws, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "metric": METRIC, "value": r4(value), "unit": unit, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": r4(ms_per_step), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": cfg.get("dtype", "bf16"),
         "data": "synthetic (seeded normals; no dataset)",
-        "config": {"workload": args.workload, **{k: v for k, v in cfg.items() if k not in ("kind", "seed")},
-                   "parallelism": f"replicas{ws}" if ws > 1 else "single-gpu, N logical shards",
-                   "l2": "flushed before every timed step (256 MiB write, outside the step events)",
-                   "flops_per_step": units},
+        "config": dict(workload_config(args.workload, ws), flops_per_step=units),
         "roofline": None if top is None else {
-            "bound": top["bound"], "achieved": top["achieved"], "peak": top["peak"],
-            "unit": top["unit"], "frac": top["frac"], "traffic": top["traffic"],
+            "bound": top["bound"], "achieved": r4(top["achieved"]), "peak": top["peak"],
+            "unit": top["unit"], "frac": r4(top["frac"]), "traffic": top["traffic"],
             "kernel": top["kernel"], "peak_source": top["peak_source"],
-            "avg_launch_us": top["avg_us"]},
-        "kernels": kernels,
-        "peak_tensor_frac_step": (value / ws) / peaks["bf16_tflops_sustained"],
-        "embed_gather": gather,
-        "rows": {k: v for k, v in rows.items() if k != "embed_gather"},
+            "avg_launch_us": r4(top["avg_us"]), "launches": top["launches"]},
+        "kernels_frac": {k["kernel"]: r4(k["frac"]) for k in kernels},
+        "embed_gather": None if gather is None else {
+            "value": r4(gather["value"]), "unit": "GB/s", "frac": r4(gather["frac"]),
+            "peak": gather["peak"], "avg_launch_us": r4(gather["avg_launch_us"]),
+            "traffic": gather["traffic"], "workload": gather["workload"]},
+        "rows": {k: compact_row(k, v) for k, v in rows.items()},
         "cpu_baseline": cpu,
-        "e2e": e2e,
+        "e2e": None if e2e is None else dict(e2e, value=r4(e2e["value"]),
+                                             ms_per_step=r4(e2e["ms_per_step"])),
         "gpu_launches": launches,
         "clocks": clocks,
-        "wall_s_timed_loop": wall,
+        "detail": detail_path,
     }
     print(json.dumps(line))
     return 0
@@ -878,6 +924,7 @@ def secondary_rows(tp, torch, flush, peaks, peak_src, main_workload):
     rows = {}
     for name in ("embed_tied_V50257_h4096_T8192", "ce_V50257_h4096_T8192",
                  "attn_b1_s2048_h4096_heads8_N8", "mlp_b2_s2048_h4096_hp16384_N2",
+                 "mlp_b4_s1024_h1024_hp4096_N4",
                  "attn_core_b1_s2048_heads8_d512_causal", "layer_b1_s2048_h4096_heads8_hp16384_N8",
                  "adam_layer_H4096"):
         if name == main_workload:

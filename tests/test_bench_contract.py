@@ -28,7 +28,7 @@ def test_reference_arm_prints_one_complete_json_line():
     assert d["unit"] == "TFLOP/s" and d["value"] > 0 and d["ms_per_step"] > 0
     assert d["steps"] == 3 and d["warmup"] == 3 and d["n_gpus"] == 1
     assert d["higher_is_better"] is True and d["vs_baseline"] is None
-    assert d["config"]["workload"] == "mlp_b4_s1024_h1024_hp4096_N4"
+    assert d["config"]["workload"] == "mlp_b2_s2048_h4096_hp16384_N2"
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"] and cb["sample"]
     e = d["e2e"]
