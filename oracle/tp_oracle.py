@@ -320,8 +320,8 @@ def attention_head_grad(q, k, v, P, g, keep=None, p=0.0):
 def attention_keep(bi, j, s, n_heads, N, p, seed, layer):
     """Attention-dropout keep flags (s, s) of sequence bi, head j: elements
     ((bi n_heads + j) s + query) s + key of the stream of head j's shard.
-    Pinned through ``dropout_keep`` (numpy.random.Philox) and the planted
-    shared-stream test (the shards' masks must differ)."""
+    Pinned through ``dropout_keep`` (the generator's known-answer vectors)
+    and the planted shared-stream test (the shards' masks must differ)."""
     if p <= 0.0:
         return None
     shard = j // (n_heads // N)
@@ -687,62 +687,54 @@ def mixed_precision_adam_step(groups, state, cfg):
 # --------------------------------------------------------------------------
 # Transformer layer: counter-based dropout, LayerNorm, residuals
 # --------------------------------------------------------------------------
-# Philox4x64-10 (Salmon, Moraes, Dror and Shaw, "Parallel random numbers: as
-# easy as 1, 2, 3", SC 2011): ten rounds of two 64 x 64 -> 128-bit products
+# Philox4x32-10 (Salmon, Moraes, Dror and Shaw, "Parallel random numbers: as
+# easy as 1, 2, 3", SC 2011): ten rounds of two 32 x 32 -> 64-bit products
 # with a Weyl-sequence key schedule.  The pages fix only where the random
 # streams differ (dropout inside the tensor-parallel region draws per shard,
 # outside it all shards draw the same numbers: [Walkthrough] §模型并行, the
 # dropout figure); the generator and the mask layout below are this build's.
-_PH_M0, _PH_M1 = 0xD2E7470EE14C6C93, 0xCA5A826395121157
-_PH_W0, _PH_W1 = 0x9E3779B97F4A7C15, 0xBB67AE8584CAA73B
+_PH_M0, _PH_M1 = 0xD2511F53, 0xCD9E8D57
+_PH_W0, _PH_W1 = 0x9E3779B9, 0xBB67AE85
 _U32 = np.uint64(0xFFFFFFFF)
 
 
-def _mulhilo64(a, b):
-    """Full 128-bit product of uint64 arrays as (hi, lo), from 32-bit halves."""
-    a = np.asarray(a, dtype=np.uint64)
-    b = np.asarray(b, dtype=np.uint64)
+def philox4x32(c0, c1, c2, c3, k0, k1):
+    """Philox4x32-10 of counters (c0, c1, c2, c3) under key (k0, k1), 32-bit
+    words held in uint64 arrays (every product of two 32-bit words is exact
+    in 64 bits); c0 .. c3 may be arrays.  Returns the four output words.
+    Pinned by: the known-answer vectors published with the generator
+    (tests/golden/philox4x32_kat.json)."""
     s32 = np.uint64(32)
-    al, ah = a & _U32, a >> s32
-    bl, bh = b & _U32, b >> s32
-    ll, lh, hl, hh = al * bl, al * bh, ah * bl, ah * bh
-    mid = (ll >> s32) + (lh & _U32) + (hl & _U32)
-    hi = hh + (lh >> s32) + (hl >> s32) + (mid >> s32)
-    return hi, a * b
-
-
-def philox4x64(c0, k0, k1, c1=0, c2=0, c3=0):
-    """Philox4x64-10 of counters (c0, c1, c2, c3) under key (k0, k1); c0 may
-    be an array.  Returns the four uint64 output words.
-    Pinned by: numpy.random.Philox (the same generator; its first block is
-    counter 1)."""
-    with np.errstate(over="ignore"):
-        x0 = np.asarray(c0, dtype=np.uint64)
-        x1 = np.full_like(x0, np.uint64(c1))
-        x2 = np.full_like(x0, np.uint64(c2))
-        x3 = np.full_like(x0, np.uint64(c3))
-        key0, key1 = np.uint64(k0), np.uint64(k1)
-        for _ in range(10):
-            hi0, lo0 = _mulhilo64(np.uint64(_PH_M0), x0)
-            hi1, lo1 = _mulhilo64(np.uint64(_PH_M1), x2)
-            x0, x1, x2, x3 = hi1 ^ x1 ^ key0, lo1, hi0 ^ x3 ^ key1, lo0
-            key0 = key0 + np.uint64(_PH_W0)
-            key1 = key1 + np.uint64(_PH_W1)
+    x0, x1, x2, x3 = np.broadcast_arrays(*(np.asarray(c, dtype=np.uint64) & _U32 for c in (c0, c1, c2, c3)))
+    x0, x1, x2, x3 = x0.copy(), x1.copy(), x2.copy(), x3.copy()
+    key0, key1 = np.uint64(k0) & _U32, np.uint64(k1) & _U32
+    for r in range(10):
+        if r > 0:
+            key0 = (key0 + np.uint64(_PH_W0)) & _U32
+            key1 = (key1 + np.uint64(_PH_W1)) & _U32
+        p0 = np.uint64(_PH_M0) * x0
+        p1 = np.uint64(_PH_M1) * x2
+        x0, x1, x2, x3 = (p1 >> s32) ^ x1 ^ key0, p1 & _U32, (p0 >> s32) ^ x3 ^ key1, p0 & _U32
     return x0, x1, x2, x3
 
 
 def dropout_keep(seed, stream, e0, n, p):
-    """Keep flags of elements e0 .. e0+n-1 of one dropout site: element e
-    takes the 16-bit field 16 (e mod 4) of output word (e mod 16) / 4 of
-    Philox4x64-10 at counter (e / 16, 0, 0, 0) under key (seed, stream), and is
-    kept iff that field is >= floor(p 2^16) (keep probability 1 - floor(p 2^16)
-    / 2^16).  Pinned by: numpy.random.Philox and the keep rate."""
+    """Keep flags of elements e0 .. e0+n-1 of one dropout site.  Element e
+    takes the 16-bit field 16 (e mod 2) of output word (e mod 8) / 2 of
+    Philox4x32-10 at counter (b mod 2^32, b / 2^32, stream mod 2^32,
+    stream / 2^32), b = e / 8, under key (seed mod 2^32, seed / 2^32), and is
+    kept iff that field is >= floor(p 2^16) (keep probability
+    1 - floor(p 2^16) / 2^16).  Pinned by: the generator's known-answer
+    vectors, the keep rate, distinct streams and seeds."""
     e = np.arange(e0, e0 + n, dtype=np.uint64)
-    blocks = e // np.uint64(16)
-    words = philox4x64(blocks, seed, stream)
+    b = e // np.uint64(8)
+    st = np.uint64(stream)
+    sd = np.uint64(seed)
+    words = philox4x32(b & _U32, b >> np.uint64(32), st & _U32, st >> np.uint64(32),
+                       sd & _U32, sd >> np.uint64(32))
     W = np.stack(words, axis=0)  # (4, n)
-    w = ((e % np.uint64(16)) // np.uint64(4)).astype(np.int64)
-    shift = np.uint64(16) * (e % np.uint64(4))
+    w = ((e % np.uint64(8)) // np.uint64(2)).astype(np.int64)
+    shift = np.uint64(16) * (e % np.uint64(2))
     field = (W[w, np.arange(n)] >> shift) & np.uint64(0xFFFF)
     return field >= np.uint64(int(math.floor(p * 65536.0)))
 

@@ -942,24 +942,41 @@ def test_planted_per_group_clip_is_caught(monkeypatch):
 # ----------------------------------------------------------------------------
 # Transformer layer: Philox dropout, LayerNorm, the whole layer
 # ----------------------------------------------------------------------------
-@pytest.mark.parametrize("key", [(0, 0), (1, 2), (2**64 - 1, 12345), (0xDEADBEEF, 2**63)])
-def test_philox_matches_numpy(key):
-    c = np.arange(1, 9, dtype=np.uint64)
-    words = O.philox4x64(c, key[0], key[1])
-    bg = np.random.Philox(key=np.array(key, dtype=np.uint64), counter=np.zeros(4, dtype=np.uint64))
-    raw = bg.random_raw(4 * len(c))  # numpy's first block is counter 1
-    for i in range(len(c)):
-        for j in range(4):
-            assert int(words[j][i]) == int(raw[4 * i + j])
+def check_philox(mod):
+    """Largest number of mismatching output words over the published
+    known-answer vectors (each vector also evaluated inside a batch)."""
+    kat = golden("philox4x32_kat.json")["vectors"]
+    bad = 0
+    for v in kat:
+        c = [int(x, 16) for x in v["ctr"]]
+        k = [int(x, 16) for x in v["key"]]
+        out = mod.philox4x32(*c, *k)
+        bad += sum(int(out[j]) != int(v["out"][j], 16) for j in range(4))
+        # the same counter as the middle element of an array of counters
+        arr = mod.philox4x32(np.array([c[0] ^ 1, c[0], c[0] ^ 2], dtype=np.uint64), c[1], c[2], c[3], *k)
+        bad += sum(int(arr[j][1]) != int(v["out"][j], 16) for j in range(4))
+    return bad
 
 
-def test_philox_high_counter_words_match_numpy():
-    # counters with the upper words set: numpy's counter is 256-bit, ours (c0, c1, c2, c3)
-    bg = np.random.Philox(key=np.array([7, 9], dtype=np.uint64),
-                          counter=np.array([2**64 - 1, 5, 0, 0], dtype=np.uint64))
-    raw = bg.random_raw(4)  # counter + 1 = (0, 6, 0, 0)
-    words = O.philox4x64(np.array([0], dtype=np.uint64), 7, 9, c1=6)
-    assert [int(w[0]) for w in words] == [int(r) for r in raw]
+def test_philox4x32_known_answers():
+    assert check_philox(O) == 0
+
+
+def test_planted_philox_key_schedule_off_by_one_round_is_caught(monkeypatch):
+    real_w0 = O._PH_W0
+    monkeypatch.setattr(O, "_PH_W0", (real_w0 + 1) & 0xFFFFFFFF)
+    assert check_philox(O) > 0
+
+
+def test_dropout_keep_layout_against_the_generator_directly():
+    # element e: word (e mod 8) / 2, field 16 (e mod 2) at counter (e / 8, 0, stream, 0)
+    seed, stream, p = (7 << 32) | 5, 3, 0.25
+    k = O.dropout_keep(seed, stream, 40, 24, p)
+    thr = math.floor(p * 65536)
+    for i, e in enumerate(range(40, 64)):
+        w = O.philox4x32(e // 8, 0, stream, 0, 5, 7)
+        field = (int(w[(e % 8) // 2]) >> (16 * (e % 2))) & 0xFFFF
+        assert bool(k[i]) == (field >= thr)
 
 
 def test_dropout_keep_rate_and_streams():
@@ -968,6 +985,7 @@ def test_dropout_keep_rate_and_streams():
     keep = 1 - math.floor(p * 65536) / 65536
     assert abs(k.mean() - keep) < 5 * math.sqrt(keep * (1 - keep) / n)
     assert not np.array_equal(k, O.dropout_keep(11, 4, 0, n, p))      # another stream
+    assert not np.array_equal(k, O.dropout_keep(11 + (1 << 32), 3, 0, n, p))  # the seed's upper word counts
     assert np.array_equal(k[1000:2000], O.dropout_keep(11, 3, 1000, 1000, p))  # offsets
     assert O.dropout_keep(11, 3, 0, 1000, 0.0).all()
     # the attention streams differ per shard, the hidden ones do not
