@@ -44,6 +44,12 @@
  *    passed as void*; NULL = legacy default stream).  Argument errors return
  *    synchronously before any launch.  Device-side errors (a bounded wait that
  *    expired) are reported by tp_get_status().
+ *  - First call on a device: the first call of any entry point with a device
+ *    current does one-time set-up (looks up the library's static device
+ *    symbols, writes its block of ones, sets kernel attributes), which may
+ *    load the module and synchronise the device.  Make one call per device
+ *    during set-up, before any stream capture and before latency-sensitive
+ *    stream work.
  *  - accumulate: 0 = overwrite the gradient outputs, 1 = add into them.
  */
 #ifndef TP_H_
@@ -227,9 +233,10 @@ TP_API size_t tp_attn_core_workspace_size(int64_t T, int64_t s, int64_t h, int n
  *   C = (P * keep / (1 - p_attn)) V per head; P is stored before dropout, and
  *   Pd (same layout as P, bf16) receives P * keep / (1 - p_attn).
  * keep: element ((sequence * n_heads + head) * s + query) * s + key of the
- * stream stream0 + shard(head) under key seed, drawn from Philox4x64-10
- * (Salmon et al., SC 2011): the 16-bit field 16 (e mod 4) of output word
- * (e mod 16) / 4 at counter (e / 16, 0, 0, 0), kept iff it is >=
+ * stream stream0 + shard(head) under seed, drawn from Philox4x32-10
+ * (Salmon et al., SC 2011): the 16-bit field 16 (e mod 2) of output word
+ * (e mod 8) / 2 at counter (e / 8 as two 32-bit words, low first, then the
+ * stream as two words) under key (seed as two words), kept iff it is >=
  * floor(p_attn * 65536) computed from the fp32 p_attn.  The backward draws the
  * same bits again.  p_attn > 0 needs s % 16 == 0, s <= 65535 and at most 65535
  * (sequence, head) pairs (TP_ERR_INVALID otherwise) and a non-NULL Pd.
@@ -488,8 +495,11 @@ TP_API size_t tied_embed_grad_workspace_size(int64_t T, int64_t V);
  *  - tied_embed_grad_workspace_size(T, V) must not exceed 1.5 MiB (for
  *    example V <= 131072 with T <= 65536); larger sizes return
  *    TP_ERR_WORKSPACE before anything is launched.
- *  - The first call on a device looks up the array's device address with that
- *    device current; make that first call before any stream capture.
+ *  - The first call on a device also looks up the array's device address with
+ *    that device current, which may synchronise the device: make that first
+ *    call during set-up, before any stream capture.
+ *  - Argument errors are those of tied_embed_grad and come first, then the
+ *    size limit, and only then anything that touches the device.
  *  - All calls share the one array, which keeps the last call's contents: calls
  *    that overlap on the GPU (different streams, no ordering between them) race
  *    and give wrong results.  Order them on one stream or with events.
@@ -578,7 +588,8 @@ typedef struct {
  * Errors: TP_ERR_INVALID for NULL cfg/state, ngroups out of range, n < 0, a
  * NULL buffer, betas outside [0, 1) or growth_interval < 1 with the scaler;
  * TP_ERR_ALIGN for misaligned buffers; all before anything is launched.
- * Launches three kernels (norm partials, a one-block finalize, the update).
+ * Launches two kernels: the norm pass (whose last block sums the partials in
+ * a fixed order and makes the scaler, skip and clip decisions) and the update.
  */
 TP_API tp_status tp_adam_step(const tp_param_group* groups, int ngroups, const tp_adam_config* cfg,
                               tp_optimizer_state* state, void* workspace, size_t ws_bytes,

@@ -910,7 +910,7 @@ size_t attn_bwd_ws(const AttnDims& a, int64_t s) {
          attn_keep_bytes(a, s);
 }
 
-// Attention dropout needs whole 16-key Philox blocks per row and fits its keep
+// Attention dropout needs whole 16-key generator blocks per row and fits its keep
 // kernel's grid (s and the (sequence, head) pairs below 65536).
 bool drop_ok(float p, int64_t s) {
   return p >= 0.f && p < 1.f && (p == 0.f || (s % 16 == 0 && s <= 65535));
@@ -1335,11 +1335,10 @@ extern "C" size_t tied_embed_grad_workspace_size(int64_t T, int64_t V) {
   return sort_workspace_bytes(T, V);
 }
 
-extern "C" tp_status tied_embed_grad(tp_dtype dt, int64_t T, int64_t h, int64_t V, int N,
-                                     const int64_t* ids, const void* dEmb, const void* X,
-                                     const void* const* dLogits, const int64_t* ld_dlogits,
-                                     const int64_t* range_starts, void* const* dE, int accumulate,
-                                     void* workspace, size_t ws_bytes, void* stream) {
+tp_status tp::tied_embed_grad_check(tp_dtype dt, int64_t T, int64_t h, int64_t V, int N,
+                                    const int64_t* ids, const void* dEmb, const void* X,
+                                    const void* const* dLogits, const int64_t* ld_dlogits,
+                                    const int64_t* range_starts, void* const* dE) {
   if (!dtype_ok(dt)) return TP_ERR_UNSUPPORTED;
   if (T < 0 || h <= 0 || V <= 0 || N > kMaxGroups || !ranges_ok(range_starts, N, V) ||
       !shards_ok(dE, N))
@@ -1352,6 +1351,17 @@ extern "C" tp_status tied_embed_grad(tp_dtype dt, int64_t T, int64_t h, int64_t 
     if (T > 0 && !X) return TP_ERR_INVALID;
   }
   if (T > 0 && (!ids || !dEmb)) return TP_ERR_INVALID;
+  return TP_OK;
+}
+
+extern "C" tp_status tied_embed_grad(tp_dtype dt, int64_t T, int64_t h, int64_t V, int N,
+                                     const int64_t* ids, const void* dEmb, const void* X,
+                                     const void* const* dLogits, const int64_t* ld_dlogits,
+                                     const int64_t* range_starts, void* const* dE, int accumulate,
+                                     void* workspace, size_t ws_bytes, void* stream) {
+  const tp_status chk =
+      tied_embed_grad_check(dt, T, h, V, N, ids, dEmb, X, dLogits, ld_dlogits, range_starts, dE);
+  if (chk != TP_OK) return chk;
   if (workspace == nullptr || ws_bytes < tied_embed_grad_workspace_size(T, V)) return TP_ERR_WORKSPACE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
 

@@ -166,7 +166,7 @@ cudaError_t launch_attn_rowdot(const void* C, const void* dC, int64_t h, int64_t
                                int64_t pairs, float* D, cudaStream_t st);
 
 // Transformer-layer row kernels (LayerNorm, dropout + residual, attention
-// dropout bits).  Dropout keeps element e iff its 16-bit Philox field is >=
+// dropout bits).  Dropout keeps element e iff its 16-bit Philox4x32-10 field is >=
 // dropout_threshold(p).
 uint32_t dropout_threshold(float p);
 cudaError_t launch_ln_fwd(const void* x, const float* g, const float* b, int64_t T, int64_t h, float eps,
@@ -230,6 +230,12 @@ cudaError_t launch_embed_gather(const int64_t* ids, int64_t T, int64_t row_bytes
                                 const RangeTable& rt, void* out, cudaStream_t s);
 // Grouping of tokens by id.  ws holds offsets[V+1], perm[T], counts[V].
 size_t sort_workspace_bytes(int64_t T, int64_t V);
+// Every host-side argument check of tied_embed_grad except the workspace's,
+// in its order; TP_OK when the arguments are valid.
+tp_status tied_embed_grad_check(tp_dtype dt, int64_t T, int64_t h, int64_t V, int N,
+                                const int64_t* ids, const void* dEmb, const void* X,
+                                const void* const* dLogits, const int64_t* ld_dlogits,
+                                const int64_t* range_starts, void* const* dE);
 cudaError_t launch_embed_sort(const int64_t* ids, int64_t T, int64_t V, void* ws, cudaStream_t s);
 cudaError_t launch_ce_reduce(const void* part, int P, int64_t T, const int64_t* targets, int64_t V,
                              const float* target_logit, float* loss, float* lse, cudaStream_t s);

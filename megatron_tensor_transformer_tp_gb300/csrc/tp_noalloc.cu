@@ -14,6 +14,7 @@
 #include <mutex>
 
 #include "tp.h"
+#include "tp_internal.h"
 
 namespace {
 
@@ -50,7 +51,11 @@ extern "C" TP_API tp_status tied_embed_grad_noalloc(tp_dtype dt, int64_t T, int6
                                                     const int64_t* ld_dlogits,
                                                     const int64_t* range_starts, void* const* dE,
                                                     int accumulate, void* stream) {
-  if (T < 0 || V <= 0) return TP_ERR_INVALID;
+  // Argument errors first, then the size limit, and only then the device: an
+  // invalid call returns its argument error even without a usable GPU.
+  const tp_status chk =
+      tp::tied_embed_grad_check(dt, T, h, V, N, ids, dEmb, X, dLogits, ld_dlogits, range_starts, dE);
+  if (chk != TP_OK) return chk;
   if (tied_embed_grad_workspace_size(T, V) > kScratchBytes) return TP_ERR_WORKSPACE;
   void* scratch = nullptr;
   const tp_status st = scratch_for_current_device(&scratch);

@@ -367,4 +367,26 @@ def test_tied_grad_noalloc_refuses_sizes_beyond_its_scratch():
                                      0, None) == tp.TP_ERR_WORKSPACE
     assert L.tied_embed_grad_noalloc(tp.TP_BF16, -1, 64, V, 2, FAKE, FAKE, FAKE, d[0], ld, rs, e[0],
                                      0, None) == tp.TP_ERR_INVALID
-    # (its other argument checks are tied_embed_grad's, made after it looks up its device scratch)
+
+
+def test_tied_grad_noalloc_checks_arguments_before_size_and_device():
+    """tied_embed_grad's argument checks come first, then the scratch limit,
+    and only then the device (none here): each bad argument gives its own
+    error, even with a size beyond the scratch."""
+    e, d = ptrs(2), ptrs(2)
+    f = L.tied_embed_grad_noalloc
+    big_V = 1 << 20
+    big_rs, big_ld = rs_arr([0, big_V // 2, big_V]), rs_arr([big_V // 2, big_V // 2])
+    T = 1 << 16
+    assert f(7, T, 64, big_V, 2, FAKE, FAKE, FAKE, d[0], big_ld, big_rs, e[0], 0, None) == \
+        tp.TP_ERR_UNSUPPORTED                                              # dtype, oversized size
+    assert f(tp.TP_BF16, T, 64, big_V, 2, FAKE, FAKE, FAKE, d[0], big_ld, rs_arr([0, 5, big_V - 1]),
+             e[0], 0, None) == tp.TP_ERR_INVALID                           # ranges do not end at V
+    assert f(tp.TP_BF16, T, 0, big_V, 2, FAKE, FAKE, FAKE, d[0], big_ld, big_rs, e[0], 0, None) == \
+        tp.TP_ERR_INVALID                                                  # h = 0
+    assert f(tp.TP_BF16, T, 64, big_V, 2, FAKE, FAKE, FAKE, d[0], rs_arr([8, 8]), big_rs, e[0], 0,
+             None) == tp.TP_ERR_INVALID                                    # pitch below range width
+    assert f(tp.TP_BF16, T, 64, big_V, 2, None, FAKE, FAKE, d[0], big_ld, big_rs, e[0], 0, None) == \
+        tp.TP_ERR_INVALID                                                  # no ids
+    assert f(tp.TP_BF16, T, 64, big_V, 2, FAKE, FAKE, None, d[0], big_ld, big_rs, e[0], 0, None) == \
+        tp.TP_ERR_INVALID                                                  # dLogits without X

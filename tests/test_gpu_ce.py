@@ -69,8 +69,8 @@ def check_full(X, Es, ranges, targets, dloss, res):
     for r, (a, b) in enumerate(zip(dLog, g)):
         assert_close(a, b, "bf16", f"dLogits[{r}]")
     if dX is not None:
-        # against the oracle's dX from the GPU's own bf16 dLogits and from the exact ones
-        assert_close(dX, O.logits_side_dx(g, En), "bf16", "dX")
+        # dX sums products of the saved bf16 dLogits: element-wise measure reported
+        assert_close(dX, O.logits_side_dx(g, En), "bf16", "dX", elementwise=False)
 
 
 @pytest.mark.parametrize("T,h,ranges", [(200, 256, [0, 333, 1000]), (129, 128, [0, 64, 65, 300]),
@@ -120,5 +120,5 @@ def test_ce_embed_tied_V50257_h4096_T8192_sampled():
     gr = O.vocab_parallel_cross_entropy_grad(Xn, En, ranges, t, dl)
     for r in range(len(Es)):
         assert_close(dLog[r][rows], gr[r], "bf16", f"dLogits[{r}] rows")
-    assert_close(dX[rows], O.logits_side_dx(gr, En), "bf16", "dX rows")
+    assert_close(dX[rows], O.logits_side_dx(gr, En), "bf16", "dX rows", elementwise=False)
     assert torch.isfinite(loss).all() and torch.isfinite(dX.float()).all()

@@ -45,4 +45,4 @@ def test_bounded_wait_expires_reports_timeout_and_recovers():
     tp.tp_mlp_fwd(X, W, None, U, None, Z, Y, Out)
     assert tp.tp_get_status() == tp.TP_OK
     _, _, ref = O.mlp_fwd(f64(inp["X"]), f64_list(inp["W_shards"]), None, f64_list(inp["U_shards"]), None)
-    assert_close(Out, ref, "bf16", "Out after recovery")
+    assert_close(Out, ref, "bf16", "Out after recovery", elementwise=False)  # sums the bf16 Y

@@ -74,7 +74,7 @@ def test_attn_core_dropout_parity():
     assert tp.tp_get_status() == tp.TP_OK
     Qn = f64(QKV)
     rC, rP = O.attention_core(Qn, s, H, N, True, f32p(p), seed, layer)
-    assert_close(C, rC, "bf16", "C")
+    assert_close(C, rC, "bf16", "C", elementwise=False)  # sums products of the bf16 P
     assert_close(P, rP, "bf16", "P")
     lower = np.tril(np.ones((s, s), dtype=bool))
     Pdn = Pd.float().cpu().numpy()
@@ -83,7 +83,7 @@ def test_attn_core_dropout_parity():
             keep = O.attention_keep(bi, j, s, H, N, f32p(p), seed, layer)
             assert np.array_equal((Pdn[bi, j] != 0) & lower, keep & lower), (bi, j)
     rd = O.attention_core_grad(Qn, rP, f64(dC), s, H, N, f32p(p), seed, layer)
-    assert_close(dQKV, rd, "bf16", "dQKV")
+    assert_close(dQKV, rd, "bf16", "dQKV", elementwise=False)  # from the bf16 dS and P
 
 
 def alloc_layer(cfg, T):
@@ -142,17 +142,20 @@ def oracle_layer(cfg, inp):
 
 
 def check_layer(cfg, inp):
+    # Only ln1 is computed from the layer's input alone; every later tensor is
+    # computed from saved bf16 activations (ln1, QKV, P, C, h1, ln2, Z, Y, dZ),
+    # so for those the element-wise measure is reported, not asserted.
     out, saved, dx, grads = run_layer(cfg, inp)
     rout, rsv, rg = oracle_layer(cfg, inp)
     for k in ("ln1", "QKV", "C", "h1", "ln2"):
-        assert_close(saved[k], rsv[k], "bf16", k)
-    assert_close(out, rout, "bf16", "out")
-    assert_close(dx, rg["dx"], "bf16", "dx")
+        assert_close(saved[k], rsv[k], "bf16", k, elementwise=(k == "ln1"))
+    assert_close(out, rout, "bf16", "out", elementwise=False)
+    assert_close(dx, rg["dx"], "bf16", "dx", elementwise=False)
     for k in ("dg1", "db1", "dg2", "db2", "dbo", "db"):
-        assert_close(grads[k], rg[k], "bf16", k)
+        assert_close(grads[k], rg[k], "bf16", k, elementwise=False)
     for k in ("dWqkv", "dbqkv", "dWo", "dW", "da", "dU"):
         for i, (a, r) in enumerate(zip(grads[k], rg[k])):
-            assert_close(a, r, "bf16", f"{k}[{i}]")
+            assert_close(a, r, "bf16", f"{k}[{i}]", elementwise=False)
 
 
 SMALL = dict(s=128, h=256, hp=1024, n_heads=4, N=2, causal=True, eps=1e-5, p_attn=0.1, p_hidden=0.1,
@@ -218,9 +221,9 @@ def test_attn_core_dropout_non_causal_both_kernels(mode):
         tp.tp_debug_set_gemm_kernel(2)
     Qn = f64(QKV)
     rC, rP = O.attention_core(Qn, s, H, N, False, f32p(p), seed, layer)
-    assert_close(C, rC, "bf16", "C")
+    assert_close(C, rC, "bf16", "C", elementwise=False)  # sums products of the bf16 P
     rd = O.attention_core_grad(Qn, rP, f64(dC), s, H, N, f32p(p), seed, layer)
-    assert_close(dQKV, rd, "bf16", "dQKV")
+    assert_close(dQKV, rd, "bf16", "dQKV", elementwise=False)
     Pdn = Pd.float().cpu().numpy()
     for j in range(H):
         assert np.array_equal(Pdn[0, j] != 0, O.attention_keep(0, j, s, H, N, f32p(p), seed, layer))

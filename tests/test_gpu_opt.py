@@ -98,9 +98,11 @@ def check_against(dev, before, ref_groups, ref_state, ref_norm, st, updated):
                 assert torch.isnan(d["model"].float()).all()
             continue
         assert_close(p, r["param"], "f32", f"param[{i}]")
-        # the update itself, not only the parameter it is added to
+        # the update itself, not only the parameter it is added to (recovered as a
+        # difference of fp32 parameters, each element carries the parameter's 2^-24
+        # relative rounding: element-wise measure reported, not asserted)
         assert_close(p.double() - b["param"].double(), r["param"] - b["param"].double().numpy(),
-                     "f32", f"param update[{i}]")
+                     "f32", f"param update[{i}]", elementwise=False)
         assert_close(d["m"], r["m"], "f32", f"m[{i}]")
         assert_close(d["v"], r["v"], "f32", f"v[{i}]")
         if d["model"] is not None:
