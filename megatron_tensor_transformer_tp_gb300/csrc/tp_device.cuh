@@ -56,6 +56,16 @@ __device__ __forceinline__ float gelu_grad_f(float z) {
   return fmaf(z * 0.39894228040143268f, e, 0.5f * (1.0f + r));
 }
 
+// The same two functions through CUDA's erff / expf, for the fp32 engine:
+// its 1e-4 bar is also met element by element, which the approximation's
+// 1.5e-7 absolute error in erf does not allow near the zero of GELU'.
+__device__ __forceinline__ float gelu_exact_f(float z) {
+  return 0.5f * z * (1.0f + erff(z * 0.70710678118654752f));
+}
+__device__ __forceinline__ float gelu_grad_exact_f(float z) {
+  return fmaf(z * 0.39894228040143268f, expf(-0.5f * z * z), 0.5f * (1.0f + erff(z * 0.70710678118654752f)));
+}
+
 __device__ __forceinline__ float bf2f(__nv_bfloat16 x) { return __bfloat162float(x); }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {

@@ -24,12 +24,12 @@ __device__ __forceinline__ void epilogue_elem(const GemmGroup& G, int m, int n, 
       if (G.bias != nullptr) v += static_cast<const float*>(G.bias)[n];
       static_cast<float*>(G.out)[static_cast<int64_t>(m) * G.ldo + n] = v;
       if (G.epi == EPI_BIAS_GELU)
-        static_cast<float*>(G.out2)[static_cast<int64_t>(m) * G.ldo + n] = gelu_f(v);
+        static_cast<float*>(G.out2)[static_cast<int64_t>(m) * G.ldo + n] = gelu_exact_f(v);
       break;
     }
     case EPI_DGELU: {
       const float z = static_cast<const float*>(G.aux)[static_cast<int64_t>(m) * G.ld_aux + n];
-      static_cast<float*>(G.out)[static_cast<int64_t>(m) * G.ldo + n] = v * gelu_grad_f(z);
+      static_cast<float*>(G.out)[static_cast<int64_t>(m) * G.ldo + n] = v * gelu_grad_exact_f(z);
       break;
     }
     case EPI_F32:
