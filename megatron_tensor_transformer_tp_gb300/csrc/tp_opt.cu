@@ -1,12 +1,13 @@
 // Mixed-precision Adam step over flat fp32 parameter groups ("Megatron"
 // walkthrough, section MixedPrecisionOptimizer.step and DynamicGradScaler;
 // "Megatron / ZeRO" study notes, sections on gradient clipping and on Adam's
-// momentum and variance).  Three kernels, all HBM-bound streams:
+// momentum and variance).  Two kernels, both HBM-bound streams:
 //   opt_norm_kernel      unscaled gradients' sum of squares and overflow flag,
 //                        one fp64 partial per block (fixed chunk assignment);
-//   opt_finalize_kernel  one block: partials summed in fixed order, the loss
-//                        scale updated, the clip coefficient and the bias
-//                        corrections prepared, the step skipped on overflow;
+//                        the last block to finish (a completion counter) then
+//                        sums the partials in fixed order, updates the loss
+//                        scale, prepares the clip coefficient and the bias
+//                        corrections, and marks the step skipped on overflow;
 //   opt_adam_kernel      unscale + clip + weight decay + Adam + bf16 copy of
 //                        every element, in one pass.
 // Deterministic: every sum has a fixed order for a given device.
@@ -15,10 +16,18 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "tp_internal.h"
 
 namespace tp {
 namespace {
+
+// Completion counters of the norm launches, one per launch slot; launches
+// rotate over the slots and the last block of a launch resets its counter.
+constexpr int kOptSlots = 64;
+__device__ int g_opt_done[kOptSlots];
+std::atomic<unsigned> g_opt_slot_seq{0};
 
 constexpr int kOptThreads = 256;
 constexpr int64_t kOptChunk = 8192;  // elements per chunk (a multiple of 4 x kOptThreads)
@@ -51,9 +60,66 @@ __device__ __forceinline__ float inv_scale_of(const OptParams& P) {
   return P.use_scaler ? 1.0f / P.state->scale : 1.0f;
 }
 
+// The finalize step, run by the last block of the norm launch: partials
+// summed in a fixed order (thread i takes i, i + 256, ..., then a fixed tree),
+// then the scaler update, the skip decision, the clip coefficient and the bias
+// corrections.
+__device__ void opt_finalize_block(const OptParams& P, const double* partial, const int* flag,
+                                   int nparts, OptControl* ctl, double* red, int* bred) {
+  double acc = 0.0;
+  int bad = 0;
+  for (int i = threadIdx.x; i < nparts; i += kOptThreads) {
+    acc += __ldcg(partial + i);
+    bad |= __ldcg(flag + i);
+  }
+  red[threadIdx.x] = acc;
+  bred[threadIdx.x] = bad;
+  __syncthreads();
+  for (int w = kOptThreads / 2; w > 0; w >>= 1) {
+    if (threadIdx.x < w) {
+      red[threadIdx.x] += red[threadIdx.x + w];
+      bred[threadIdx.x] |= bred[threadIdx.x + w];
+    }
+    __syncthreads();
+  }
+  if (threadIdx.x != 0) return;
+  tp_optimizer_state* st = P.state;
+  const double norm_sq = red[0];
+  const int found_inf = bred[0] != 0 || !isfinite(norm_sq);
+  const float grad_mul0 = inv_scale_of(P);
+  // dynamic loss scale ("Megatron" walkthrough, DynamicGradScaler.update)
+  if (P.use_scaler) {
+    if (found_inf) {
+      st->growth_tracker = 0;
+      st->hysteresis_tracker -= 1;
+      if (st->hysteresis_tracker <= 0) st->scale = fmaxf(st->scale * P.backoff_factor, P.min_scale);
+    } else {
+      st->growth_tracker += 1;
+      if (st->growth_tracker == P.growth_interval) {
+        st->growth_tracker = 0;
+        st->hysteresis_tracker = P.hysteresis;
+        st->scale = st->scale * P.growth_factor;
+      }
+    }
+  }
+  const double norm = sqrt(norm_sq);
+  st->found_inf = found_inf;
+  st->grad_norm = static_cast<float>(norm);
+  ctl->skip = found_inf;
+  if (found_inf) return;
+  // global-norm clip: g * max_norm / ||g|| when ||g|| > max_norm
+  const double coef = (P.max_norm > 0.0 && norm > P.max_norm) ? P.max_norm / norm : 1.0;
+  const int step = st->step + 1;
+  st->step = step;
+  ctl->grad_mul = static_cast<float>(grad_mul0 * coef);
+  ctl->step_size = static_cast<float>(P.lr / (1.0 - pow(P.beta1_d, step)));
+  ctl->inv_bc2 = static_cast<float>(1.0 / (1.0 - pow(P.beta2_d, step)));
+}
+
 __global__ void __launch_bounds__(kOptThreads) opt_norm_kernel(const __grid_constant__ OptParams P,
                                                                double* __restrict__ partial,
-                                                               int* __restrict__ flag) {
+                                                               int* __restrict__ flag,
+                                                               OptControl* __restrict__ ctl, int slot) {
   const float inv_scale = inv_scale_of(P);
   double acc = 0.0;
   int bad = 0;
@@ -106,66 +172,20 @@ __global__ void __launch_bounds__(kOptThreads) opt_norm_kernel(const __grid_cons
     }
     __syncthreads();
   }
+  __shared__ int last;
   if (threadIdx.x == 0) {
     partial[blockIdx.x] = red[0];
     flag[blockIdx.x] = bred[0];
+    // publish this block's partial, then count it; the block that counts
+    // last sees every partial
+    __threadfence();
+    last = atomicAdd(g_opt_done + slot, 1) == static_cast<int>(gridDim.x) - 1;
   }
-}
-
-__global__ void __launch_bounds__(kOptThreads) opt_finalize_kernel(const __grid_constant__ OptParams P,
-                                                                   const double* __restrict__ partial,
-                                                                   const int* __restrict__ flag,
-                                                                   int nparts, OptControl* ctl) {
-  __shared__ double red[kOptThreads];
-  __shared__ int bred[kOptThreads];
-  double acc = 0.0;
-  int bad = 0;
-  for (int i = threadIdx.x; i < nparts; i += kOptThreads) {
-    acc += partial[i];
-    bad |= flag[i];
-  }
-  red[threadIdx.x] = acc;
-  bred[threadIdx.x] = bad;
   __syncthreads();
-  for (int w = kOptThreads / 2; w > 0; w >>= 1) {
-    if (threadIdx.x < w) {
-      red[threadIdx.x] += red[threadIdx.x + w];
-      bred[threadIdx.x] |= bred[threadIdx.x + w];
-    }
-    __syncthreads();
-  }
-  if (threadIdx.x != 0) return;
-  tp_optimizer_state* st = P.state;
-  const double norm_sq = red[0];
-  const int found_inf = bred[0] != 0 || !isfinite(norm_sq);
-  const float grad_mul0 = inv_scale_of(P);
-  // dynamic loss scale ("Megatron" walkthrough, DynamicGradScaler.update)
-  if (P.use_scaler) {
-    if (found_inf) {
-      st->growth_tracker = 0;
-      st->hysteresis_tracker -= 1;
-      if (st->hysteresis_tracker <= 0) st->scale = fmaxf(st->scale * P.backoff_factor, P.min_scale);
-    } else {
-      st->growth_tracker += 1;
-      if (st->growth_tracker == P.growth_interval) {
-        st->growth_tracker = 0;
-        st->hysteresis_tracker = P.hysteresis;
-        st->scale = st->scale * P.growth_factor;
-      }
-    }
-  }
-  const double norm = sqrt(norm_sq);
-  st->found_inf = found_inf;
-  st->grad_norm = static_cast<float>(norm);
-  ctl->skip = found_inf;
-  if (found_inf) return;
-  // global-norm clip: g * max_norm / ||g|| when ||g|| > max_norm
-  const double coef = (P.max_norm > 0.0 && norm > P.max_norm) ? P.max_norm / norm : 1.0;
-  const int step = st->step + 1;
-  st->step = step;
-  ctl->grad_mul = static_cast<float>(grad_mul0 * coef);
-  ctl->step_size = static_cast<float>(P.lr / (1.0 - pow(P.beta1_d, step)));
-  ctl->inv_bc2 = static_cast<float>(1.0 / (1.0 - pow(P.beta2_d, step)));
+  if (!last) return;
+  __threadfence();
+  opt_finalize_block(P, partial, flag, gridDim.x, ctl, red, bred);
+  if (threadIdx.x == 0) g_opt_done[slot] = 0;  // the slot's next launch counts from zero
 }
 
 __device__ __forceinline__ float adam_elem(float p, float g, float& m, float& v, float wd,
@@ -256,10 +276,10 @@ static int* ws_flag(void* ws) { return reinterpret_cast<int*>(ws_partial(ws) + k
 
 cudaError_t launch_adam_norm(const OptParams& P, int num_sms, void* ws, cudaStream_t s) {
   const int grid = opt_grid(opt_norm_kernel, P.nchunks, num_sms);
-  opt_norm_kernel<<<grid, kOptThreads, 0, s>>>(P, ws_partial(ws), ws_flag(ws));
-  opt_finalize_kernel<<<1, kOptThreads, 0, s>>>(P, ws_partial(ws), ws_flag(ws), grid,
-                                                static_cast<OptControl*>(ws));
-  count_launches(2);
+  const int slot = static_cast<int>(g_opt_slot_seq.fetch_add(1) % kOptSlots);
+  opt_norm_kernel<<<grid, kOptThreads, 0, s>>>(P, ws_partial(ws), ws_flag(ws),
+                                               static_cast<OptControl*>(ws), slot);
+  count_launches(1);
   return cudaGetLastError();
 }
 
