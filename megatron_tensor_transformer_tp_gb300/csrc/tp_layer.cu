@@ -10,10 +10,11 @@
 //   dropout_add_kernel   out = res + x * keep / (1 - p) and its backward;
 //   pos_embed_dropout    (word + position embedding) with dropout;
 //   attn_keep_kernel     attention-dropout keep bits, 32 keys per word.
-// Dropout draws from Philox4x64-10 (Salmon et al., "Parallel random numbers:
-// as easy as 1, 2, 3", SC 2011): element e of a site with key (seed, stream)
-// takes the 16-bit field 16 (e mod 4) of word (e mod 16) / 4 at counter e / 16
-// and is kept iff the field is >= the threshold floor(p 2^16).
+// Dropout draws from Philox4x32-10 (Salmon et al., "Parallel random numbers:
+// as easy as 1, 2, 3", SC 2011): element e of a site with seed and stream
+// takes the 16-bit field 16 (e mod 2) of word (e mod 8) / 2 at counter
+// (e / 8 as two words, stream as two words) under key (seed as two words), and
+// is kept iff the field is >= the threshold floor(p 2^16).
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <math.h>
@@ -26,38 +27,42 @@ namespace {
 
 constexpr int kLnThreads = 256;  // rows up to 256 x 32 = 8192 wide
 
-__device__ __forceinline__ void philox4x64_10(uint64_t c0, uint64_t k0, uint64_t k1, uint64_t out[4]) {
-  const uint64_t M0 = 0xD2E7470EE14C6C93ull, M1 = 0xCA5A826395121157ull;
-  const uint64_t W0 = 0x9E3779B97F4A7C15ull, W1 = 0xBB67AE8584CAA73Bull;
-  uint64_t x0 = c0, x1 = 0, x2 = 0, x3 = 0;
+__device__ __forceinline__ uint4 philox4x32_10(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3,
+                                               uint32_t k0, uint32_t k1) {
+  const uint32_t M0 = 0xD2511F53u, M1 = 0xCD9E8D57u;
+  const uint32_t W0 = 0x9E3779B9u, W1 = 0xBB67AE85u;
 #pragma unroll
   for (int r = 0; r < 10; ++r) {
-    const uint64_t hi0 = __umul64hi(M0, x0), lo0 = M0 * x0;
-    const uint64_t hi1 = __umul64hi(M1, x2), lo1 = M1 * x2;
-    x0 = hi1 ^ x1 ^ k0;
-    x1 = lo1;
-    x2 = hi0 ^ x3 ^ k1;
-    x3 = lo0;
+    const uint32_t hi0 = __umulhi(M0, c0), lo0 = M0 * c0;
+    const uint32_t hi1 = __umulhi(M1, c2), lo1 = M1 * c2;
+    c0 = hi1 ^ c1 ^ k0;
+    c1 = lo1;
+    c2 = hi0 ^ c3 ^ k1;
+    c3 = lo0;
     k0 += W0;
     k1 += W1;
   }
-  out[0] = x0;
-  out[1] = x1;
-  out[2] = x2;
-  out[3] = x3;
+  return make_uint4(c0, c1, c2, c3);
 }
 
-// Keep bits of the 16 elements of Philox block `blk` (bit f = element 16 blk + f).
-__device__ __forceinline__ uint32_t keep16(uint64_t blk, uint64_t seed, uint64_t stream, uint32_t thr) {
-  uint64_t w[4];
-  philox4x64_10(blk, seed, stream, w);
+// Keep bits of the 8 elements of generator block `blk` (bit f = element 8 blk + f).
+__device__ __forceinline__ uint32_t keep8(uint64_t blk, uint64_t seed, uint64_t stream, uint32_t thr) {
+  const uint4 w = philox4x32_10(static_cast<uint32_t>(blk), static_cast<uint32_t>(blk >> 32),
+                                static_cast<uint32_t>(stream), static_cast<uint32_t>(stream >> 32),
+                                static_cast<uint32_t>(seed), static_cast<uint32_t>(seed >> 32));
+  const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
   uint32_t bits = 0;
 #pragma unroll
-  for (int f = 0; f < 16; ++f) {
-    const uint32_t field = static_cast<uint32_t>((w[f >> 2] >> (16 * (f & 3))) & 0xFFFFull);
+  for (int f = 0; f < 8; ++f) {
+    const uint32_t field = (ws[f >> 1] >> (16 * (f & 1))) & 0xFFFFu;
     bits |= (field >= thr ? 1u : 0u) << f;
   }
   return bits;
+}
+
+// Keep bits of the 16 elements 16 b .. 16 b + 15 (bit f = element 16 b + f).
+__device__ __forceinline__ uint32_t keep16(uint64_t b, uint64_t seed, uint64_t stream, uint32_t thr) {
+  return keep8(2 * b, seed, stream, thr) | (keep8(2 * b + 1, seed, stream, thr) << 8);
 }
 
 // Fixed-order block sum of one float (all threads receive it).
@@ -99,12 +104,13 @@ __device__ __forceinline__ void unpack8(const uint4& q, float* v) {
 
 // A thread owns PER values of a row in groups of eight consecutive columns:
 // group k covers columns 8 (k kLnThreads + tid) .. + 7 (h % 8 == 0).  A block
-// takes kLnFwdRows consecutive rows in order; the next row is loaded while
-// this row's sums run.
+// takes kLnFwdRows consecutive rows and issues the loads of all of them before
+// the first row's sums, so each SM has every row of its blocks in flight (one
+// row ahead left the kernel bound by DRAM latency at ~2.6 TB/s).
 constexpr int kLnFwdRows = 4;
 
 template <int PER>
-__global__ void __launch_bounds__(kLnThreads) ln_fwd_kernel(const __nv_bfloat16* __restrict__ x,
+__global__ void __launch_bounds__(kLnThreads, PER <= 16 ? 4 : 1) ln_fwd_kernel(const __nv_bfloat16* __restrict__ x,
                                                             const float* __restrict__ g,
                                                             const float* __restrict__ b, int64_t T,
                                                             int64_t h, float eps,
@@ -114,26 +120,26 @@ __global__ void __launch_bounds__(kLnThreads) ln_fwd_kernel(const __nv_bfloat16*
   constexpr int NV = PER / 8;
   __shared__ float red[kLnThreads / 32];
   const int64_t r0 = static_cast<int64_t>(blockIdx.x) * kLnFwdRows;
-  const int64_t r1 = min(T, r0 + kLnFwdRows);
+  const int nrows = static_cast<int>(min(static_cast<int64_t>(kLnFwdRows), T - r0));
   const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
-  uint4 cur[NV];
+  uint4 rows[kLnFwdRows][NV];
 #pragma unroll
-  for (int k = 0; k < NV; ++k) {
-    const int64_t c = (static_cast<int64_t>(k) * kLnThreads + threadIdx.x) * 8;
-    cur[k] = c < h ? *reinterpret_cast<const uint4*>(x + r0 * h + c) : zero;
-  }
-  for (int64_t r = r0; r < r1; ++r) {
-    uint4 nxt[NV];
+  for (int i = 0; i < kLnFwdRows; ++i) {
 #pragma unroll
     for (int k = 0; k < NV; ++k) {
       const int64_t c = (static_cast<int64_t>(k) * kLnThreads + threadIdx.x) * 8;
-      nxt[k] = (c < h && r + 1 < r1) ? *reinterpret_cast<const uint4*>(x + (r + 1) * h + c) : zero;
+      rows[i][k] = (c < h && i < nrows) ? __ldcs(reinterpret_cast<const uint4*>(x + (r0 + i) * h + c)) : zero;
     }
+  }
+#pragma unroll
+  for (int i = 0; i < kLnFwdRows; ++i) {
+    if (i >= nrows) break;  // block-uniform
+    const int64_t r = r0 + i;
     float v[PER];  // zero past h
     float s = 0.f;
 #pragma unroll
     for (int k = 0; k < NV; ++k) {
-      unpack8(cur[k], v + 8 * k);
+      unpack8(rows[i][k], v + 8 * k);
 #pragma unroll
       for (int t = 0; t < 8; ++t) s += v[8 * k + t];
     }
@@ -160,7 +166,6 @@ __global__ void __launch_bounds__(kLnThreads) ln_fwd_kernel(const __nv_bfloat16*
         for (int t = 0; t < 8; ++t) o[t] = (v[8 * k + t] - mean) * rstd * gg[t] + bb[t];
         store8(y + r * h + c, o);
       }
-      cur[k] = nxt[k];
     }
     if (threadIdx.x == 0) {
       mean_out[r] = mean;
@@ -325,7 +330,7 @@ __global__ void __launch_bounds__(32 * kLnSumSlices) ln_param_grad_sum_kernel(co
   *out = accumulate ? *out + t : t;
 }
 
-// 16 elements per thread (one Philox block): out = res + x * keep * scale, or
+// 16 elements per thread (two generator blocks): out = res + x * keep * scale, or
 // (res == null) out = x * keep * scale.  n is a multiple of 16.
 __global__ void __launch_bounds__(256) dropout_add_kernel(const __nv_bfloat16* __restrict__ x,
                                                           const __nv_bfloat16* __restrict__ res,
