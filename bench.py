@@ -117,10 +117,29 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-def kernel_source_hash():
+# The sources that define each kind of work's kernels and launches: a DRAM
+# traffic figure stays valid while these files are unchanged.
+_GEMM_SRC = ("tp_gemm_tc.cu", "tp_api.cu", "tp_internal.h", "tp_device.cuh")
+KERNEL_SOURCES = {"gemm": _GEMM_SRC, "embed": ("tp_embed.cu", "tp_internal.h"),
+                  "ce_reduce": ("tp_embed.cu", "tp_internal.h"),
+                  "attn_lse": ("tp_attn.cu", "tp_internal.h"), "attn_rowdot": ("tp_attn.cu", "tp_internal.h"),
+                  "layer": ("tp_layer.cu", "tp_internal.h"), "attn_keep": ("tp_layer.cu", "tp_internal.h"),
+                  "adam": ("tp_opt.cu", "tp_internal.h")}
+
+
+def kernel_sources(kernel: str):
+    for prefix, files in KERNEL_SOURCES.items():
+        if kernel.startswith(prefix):
+            return files
+    return None
+
+
+def kernel_source_hash(kernel: str = None):
+    """Hash of the sources of `kernel` (all library sources when None or unknown)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "megatron_tensor_transformer_tp_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    files = kernel_sources(kernel) if kernel else None
+    for name in sorted(files or os.listdir(csrc)):
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
@@ -128,16 +147,18 @@ def kernel_source_hash():
 
 def load_traffic(kernel: str, workload: str):
     """DRAM bytes per launch of `kernel` from the committed ncu summary, or
-    None when absent or taken on a different kernel source."""
+    None when absent or taken on a different source of that kernel."""
     p = os.path.join(ROOT, "profiles", "dram_traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as f:
         d = json.load(f)
-    if d.get("kernel_source_hash") != kernel_source_hash():
-        return None
     rec = d.get("kernels", {}).get(f"{workload}/{kernel}")
-    return None if rec is None else rec.get("dram_bytes_per_launch")
+    if rec is None:
+        return None
+    want = rec.get("source_hash", d.get("kernel_source_hash"))
+    have = kernel_source_hash(kernel) if "source_hash" in rec else kernel_source_hash()
+    return rec.get("dram_bytes_per_launch") if want == have else None
 
 
 class ClockSampler:
