@@ -387,8 +387,9 @@ tp_status launch_tc_groups(const Plan& pl, const bool* used, GemmGroup* groups, 
   // faster on large launches, K-major or MN-major; the one-SM kernel (128 x 256
   // tiles) on small ones, where its finer tiles balance better across SMs.
   // Causal attention outputs count the tiles that hold work: about half, plus
-  // the diagonal.  Launches of very long contractions (over 1000 k-blocks of
-  // tiles per SM, e.g. a shard sum over a whole vocabulary range) also take
+  // the diagonal.  Launches of very long contractions (over 500 k-blocks of
+  // tiles per SM, e.g. a shard sum over a whole vocabulary range or over the
+  // model-width FFN) also take
   // the two-SM kernel once they hold two one-SM tiles per SM: there the lower
   // operand traffic per SM pays and the tile count no longer sets the balance.
   bool pair = g_gemm_mode == 1;
@@ -403,7 +404,7 @@ tp_status launch_tc_groups(const Plan& pl, const bool* used, GemmGroup* groups, 
       kb_tiles += tw * kb;
     }
     const int64_t sms = dev->num_sms;
-    pair = tiles128 > 8 * sms || (tiles128 >= 2 * sms && kb_tiles > 1000 * sms);
+    pair = tiles128 > 8 * sms || (tiles128 >= 2 * sms && kb_tiles > 500 * sms);
   }
   // Tile width: 256 for every output.  (128-wide tiles for the long dependent
   // contractions of small fused launches were measured slower on GB300: a
@@ -466,6 +467,18 @@ tp_status launch_tc_groups(const Plan& pl, const bool* used, GemmGroup* groups, 
       inter_nt += g.tiles_n;
       inter_b_bytes += 2.0 * static_cast<double>(g.N) * static_cast<double>(group_k(pl, g));
     }
+  }
+  // Tile order: row blocks fastest (consecutive tiles share B's column tile),
+  // except for independent, non-causal outputs taller than wide whose A
+  // operand is far larger than B and does not stay in L2 (for example the
+  // tied gradient's dLogits range, contracted over the tokens): there
+  // consecutive tiles share A's row block, which is then read from DRAM once
+  // instead of once per column tile.
+  for (int i = 0; i < ng; ++i) {
+    GemmGroup& g = groups[i];
+    const double a_bytes = 2.0 * static_cast<double>(g.M) * static_cast<double>(group_k(pl, g));
+    g.n_fastest = i >= interleave && g.kr_mode == KR_NONE && g.dep_kind == DEP_NONE && g.prod_row < 0 &&
+                  g.prod_col < 0 && g.M > g.N && a_bytes > 128.0 * (1 << 20);
   }
   for (int i = 0; i < ng; ++i) {
     GemmGroup& g = groups[i];

@@ -63,7 +63,7 @@ constexpr int EPI_WARP_BYTES = EPI_STAGE_BYTES;
 // constant cache).
 struct GrpLite {
   int tile_begin, tiles_m, tiles_n;
-  int flags;  // bit 0: causal tiles only (tri); bits 8..15: kr_mode
+  int flags;  // bit 0: causal tiles only (tri); bit 1: column tiles fastest; bits 8..15: kr_mode
 };
 constexpr int TBL_BYTES = 1024;
 static_assert(kMaxGroups * sizeof(GrpLite) <= TBL_BYTES, "group table does not fit");
@@ -276,6 +276,12 @@ __device__ __forceinline__ TileCoord decode_tile_rows(const TcGemmParams& p, con
     c.n0 = (local - acc) * BN;
     return c;
   }
+  if (G.flags & 2) {
+    // column tiles fastest: consecutive tiles share the row block of A
+    c.m0 = (local / G.tiles_n) * ROWS;
+    c.n0 = (local % G.tiles_n) * BN;
+    return c;
+  }
   int mt = local % G.tiles_m;
   if (ATTN && ((G.flags >> 8) & 0xff) == KR_END) mt = G.tiles_m - 1 - mt;  // longest contraction first
   c.m0 = mt * ROWS;
@@ -287,7 +293,8 @@ __device__ __forceinline__ TileCoord decode_tile_rows(const TcGemmParams& p, con
 __device__ __forceinline__ void fill_group_table(const TcGemmParams& p, GrpLite* L, int tid, int nthreads) {
   for (int i = tid; i < p.num_groups; i += nthreads) {
     const GemmGroup& G = p.grp[i];
-    L[i] = GrpLite{G.tile_begin, G.tiles_m, G.tiles_n, (G.tri ? 1 : 0) | (G.kr_mode << 8)};
+    L[i] = GrpLite{G.tile_begin, G.tiles_m, G.tiles_n,
+                   (G.tri ? 1 : 0) | (G.n_fastest ? 2 : 0) | (G.kr_mode << 8)};
   }
 }
 

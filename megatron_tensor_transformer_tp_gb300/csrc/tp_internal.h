@@ -98,7 +98,10 @@ struct GemmGroup {
   float drop_scale;
   // Bulk tensor-store maps of out / out2 and the bulk-load map of aux in
   // TcGemmParams::mapO, or -1 (set by the launcher).
-  int out_map, out2_map, aux_map, pad_maps;
+  int out_map, out2_map, aux_map;
+  // Tile order (set by the launcher): column tiles fastest instead of row
+  // blocks, so consecutive tiles share the A operand's row block.
+  int n_fastest;
 };
 
 // One operand pair of the tensor-core engine.  Operands are bf16.
