@@ -384,8 +384,9 @@ tp_status launch_tc_groups(const Plan& pl, const bool* used, GemmGroup* groups, 
   if (ng == 0) return TP_OK;
   // Kernel choice (measured on GB300): the two-SM kernel (256 x 256 pair
   // tiles, 6-stage ring, 32 KB loaded per SM per k-block instead of 48 KB) is
-  // faster on large launches, K-major or MN-major; the one-SM kernel (128 x 256
-  // tiles) on small ones, where its finer tiles balance better across SMs.
+  // faster on large launches (over 6 one-SM tiles per SM), K-major or
+  // MN-major; the one-SM kernel (128 x 256 tiles) on small ones, where its
+  // finer tiles balance better across SMs.
   // Causal attention outputs count the tiles that hold work: about half, plus
   // the diagonal.  Launches of very long contractions (over 500 k-blocks of
   // tiles per SM, e.g. a shard sum over a whole vocabulary range or over the
@@ -404,7 +405,7 @@ tp_status launch_tc_groups(const Plan& pl, const bool* used, GemmGroup* groups, 
       kb_tiles += tw * kb;
     }
     const int64_t sms = dev->num_sms;
-    pair = tiles128 > 8 * sms || (tiles128 >= 2 * sms && kb_tiles > 500 * sms);
+    pair = tiles128 > 6 * sms || (tiles128 >= 2 * sms && kb_tiles > 500 * sms);
   }
   // Tile width: 256 for every output.  (128-wide tiles for the long dependent
   // contractions of small fused launches were measured slower on GB300: a
@@ -625,10 +626,14 @@ tp_status run_plan_impl(Plan& pl, tp_dtype dt, const char* name, cudaStream_t s)
   // have enough tiles per SM that the boundary costs little; there the
   // independent and the dependent outputs run as two launches, each ordered
   // longest contraction first, which keeps the long tiles out of the tail.
+  // Causal score outputs count the tiles that hold work (about half, plus the
+  // diagonal), as in the kernel choice: the attention core's P with P V then
+  // stays one launch (measured 77.5 -> 72.2 us on 8 heads of 512, s = 2048).
   int total = 0;
   bool has_dep = false;
   for (int i = 0; i < ng; ++i) {
-    total += ((groups[i].M + 127) / 128) * ((groups[i].N + 255) / 256);
+    const int rb = (groups[i].M + 127) / 128, t = rb * ((groups[i].N + 255) / 256);
+    total += groups[i].kr_mode == KR_TRI ? (t + rb) / 2 : t;
     has_dep = has_dep || groups[i].dep_kind != DEP_NONE;
   }
   if (has_dep && total > g_split_tiles_per_sm * dev->num_sms) {

@@ -104,13 +104,12 @@ __device__ __forceinline__ void unpack8(const uint4& q, float* v) {
 
 // A thread owns PER values of a row in groups of eight consecutive columns:
 // group k covers columns 8 (k kLnThreads + tid) .. + 7 (h % 8 == 0).  A block
-// takes kLnFwdRows consecutive rows and issues the loads of all of them before
-// the first row's sums, so each SM has every row of its blocks in flight (one
-// row ahead left the kernel bound by DRAM latency at ~2.6 TB/s).
+// takes kLnFwdRows consecutive rows in order; the next row is loaded while
+// this row's sums run.
 constexpr int kLnFwdRows = 4;
 
 template <int PER>
-__global__ void __launch_bounds__(kLnThreads, PER <= 16 ? 4 : 1) ln_fwd_kernel(const __nv_bfloat16* __restrict__ x,
+__global__ void __launch_bounds__(kLnThreads) ln_fwd_kernel(const __nv_bfloat16* __restrict__ x,
                                                             const float* __restrict__ g,
                                                             const float* __restrict__ b, int64_t T,
                                                             int64_t h, float eps,
@@ -120,26 +119,26 @@ __global__ void __launch_bounds__(kLnThreads, PER <= 16 ? 4 : 1) ln_fwd_kernel(c
   constexpr int NV = PER / 8;
   __shared__ float red[kLnThreads / 32];
   const int64_t r0 = static_cast<int64_t>(blockIdx.x) * kLnFwdRows;
-  const int nrows = static_cast<int>(min(static_cast<int64_t>(kLnFwdRows), T - r0));
+  const int64_t r1 = min(T, r0 + kLnFwdRows);
   const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
-  uint4 rows[kLnFwdRows][NV];
+  uint4 cur[NV];
 #pragma unroll
-  for (int i = 0; i < kLnFwdRows; ++i) {
+  for (int k = 0; k < NV; ++k) {
+    const int64_t c = (static_cast<int64_t>(k) * kLnThreads + threadIdx.x) * 8;
+    cur[k] = c < h ? *reinterpret_cast<const uint4*>(x + r0 * h + c) : zero;
+  }
+  for (int64_t r = r0; r < r1; ++r) {
+    uint4 nxt[NV];
 #pragma unroll
     for (int k = 0; k < NV; ++k) {
       const int64_t c = (static_cast<int64_t>(k) * kLnThreads + threadIdx.x) * 8;
-      rows[i][k] = (c < h && i < nrows) ? __ldcs(reinterpret_cast<const uint4*>(x + (r0 + i) * h + c)) : zero;
+      nxt[k] = (c < h && r + 1 < r1) ? *reinterpret_cast<const uint4*>(x + (r + 1) * h + c) : zero;
     }
-  }
-#pragma unroll
-  for (int i = 0; i < kLnFwdRows; ++i) {
-    if (i >= nrows) break;  // block-uniform
-    const int64_t r = r0 + i;
     float v[PER];  // zero past h
     float s = 0.f;
 #pragma unroll
     for (int k = 0; k < NV; ++k) {
-      unpack8(rows[i][k], v + 8 * k);
+      unpack8(cur[k], v + 8 * k);
 #pragma unroll
       for (int t = 0; t < 8; ++t) s += v[8 * k + t];
     }
@@ -166,6 +165,7 @@ __global__ void __launch_bounds__(kLnThreads, PER <= 16 ? 4 : 1) ln_fwd_kernel(c
         for (int t = 0; t < 8; ++t) o[t] = (v[8 * k + t] - mean) * rstd * gg[t] + bb[t];
         store8(y + r * h + c, o);
       }
+      cur[k] = nxt[k];
     }
     if (threadIdx.x == 0) {
       mean_out[r] = mean;
