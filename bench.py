@@ -880,7 +880,8 @@ def main(argv=None):
         "warmup": args.warmup, "ms_per_step": r4(ms_per_step), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": cfg.get("dtype", "bf16"),
         "data": "synthetic (seeded normals; no dataset)",
-        "config": dict(workload_config(args.workload, ws), flops_per_step=units),
+        "config": workload_config(args.workload, ws),
+        "work_per_step": units,
         "roofline": None if top is None else {
             "bound": top["bound"], "achieved": r4(top["achieved"]), "peak": top["peak"],
             "unit": top["unit"], "frac": r4(top["frac"]), "traffic": top["traffic"],
@@ -949,9 +950,9 @@ def gather_row(tp, torch, b, name, peaks, peak_src, sets=4, per_graph=16, replay
 def secondary_rows(tp, torch, flush, peaks, peak_src, main_workload):
     """The other rows of the block, each on its own workload, a few timed steps."""
     rows = {}
-    for name in ("embed_tied_V50257_h4096_T8192", "ce_V50257_h4096_T8192",
-                 "attn_b1_s2048_h4096_heads8_N8", "mlp_b2_s2048_h4096_hp16384_N2",
-                 "mlp_b4_s1024_h1024_hp4096_N4",
+    for name in ("mlp_b4_s1024_h1024_hp4096_N4", "mlp_b2_s2048_h4096_hp16384_N2",
+                 "embed_tied_V50257_h4096_T8192", "ce_V50257_h4096_T8192",
+                 "attn_b1_s2048_h4096_heads8_N8",
                  "attn_core_b1_s2048_heads8_d512_causal", "layer_b1_s2048_h4096_heads8_hp16384_N8",
                  "adam_layer_H4096"):
         if name == main_workload:
@@ -962,7 +963,7 @@ def secondary_rows(tp, torch, flush, peaks, peak_src, main_workload):
             rows["embed_gather"] = gather_row(tp, torch, b, name, peaks, peak_src)
         tp.tp_profile_reset()
         tp.tp_profile_enable(True)
-        s_ms, _ = time_steps(torch, b.step, 10, 3, flush)
+        s_ms, _ = time_steps(torch, b.step, 20, 5, flush)
         tp.tp_profile_enable(False)
         prof = tp.tp_profile_read()
         units, unit, scale = b.units()

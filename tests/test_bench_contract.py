@@ -29,6 +29,9 @@ def test_reference_arm_prints_one_complete_json_line():
     assert d["steps"] == 3 and d["warmup"] == 3 and d["n_gpus"] == 1
     assert d["higher_is_better"] is True and d["vs_baseline"] is None
     assert d["config"]["workload"] == "mlp_b2_s2048_h4096_hp16384_N2"
+    # the main arm prints the same config object (bench.workload_config)
+    import bench
+    assert d["config"] == bench.workload_config("mlp_b2_s2048_h4096_hp16384_N2", 1)
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"] and cb["sample"]
     e = d["e2e"]
