@@ -74,7 +74,8 @@ def check_full(X, Es, ranges, targets, dloss, res):
 
 
 @pytest.mark.parametrize("T,h,ranges", [(200, 256, [0, 333, 1000]), (129, 128, [0, 64, 65, 300]),
-                                        (300, 512, [0, 2048]), (1, 64, [0, 70, 140])])
+                                        (300, 512, [0, 2048]), (1, 64, [0, 70, 140]),
+                                        (150, 128, [0, 1, 9, 130, 131, 400, 512, 700, 1000])])
 def test_ce_ragged_parity(T, h, ranges):
     X, E, Es, targets, dloss = make_case(T, h, ranges, seed=T + h)
     check_full(X, Es, ranges, targets, dloss, run_ce(X, Es, ranges, targets, dloss))

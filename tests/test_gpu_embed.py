@@ -88,7 +88,9 @@ def run_logits(inp):
 
 @pytest.mark.parametrize("dtype,V,h,T,ranges", [("bf16", 1000, 136, 333, [0, 333, 1000]),
                                                 ("f32", 300, 16, 50, [0, 150, 300]),
-                                                ("bf16", 777, 256, 129, [0, 1, 300, 777])])
+                                                ("bf16", 777, 256, 129, [0, 1, 300, 777]),
+                                                # eight ranges of uneven widths, one of a single word
+                                                ("bf16", 1000, 128, 200, [0, 1, 9, 130, 131, 400, 512, 700, 1000])])
 def test_logits_small_full(dtype, V, h, T, ranges):
     cfg = dict(kind="embed", dtype=dtype, V=V, h=h, b=1, s=T, ranges=ranges, seed=11)
     inp = SI.embed_inputs(cfg)
@@ -140,7 +142,8 @@ def sort_view(ws, T, V):
 
 @pytest.mark.parametrize("dtype,V,h,T,ranges", [("bf16", 1000, 136, 777, [0, 333, 1000]),
                                                 ("f32", 300, 16, 40, [0, 150, 300]),
-                                                ("bf16", 64, 256, 300, [0, 5, 64])])
+                                                ("bf16", 64, 256, 300, [0, 5, 64]),
+                                                ("bf16", 1000, 128, 500, [0, 1, 9, 130, 131, 400, 512, 700, 1000])])
 def test_tied_grad_small_full(dtype, V, h, T, ranges):
     cfg = dict(kind="embed", dtype=dtype, V=V, h=h, b=1, s=T, ranges=ranges, seed=12)
     inp = SI.embed_inputs(cfg)

@@ -179,6 +179,21 @@ def test_layer_parity_s40_hidden_dropout_only():
     check_layer(cfg, SI.layer_inputs(dict(cfg, b=3)))
 
 
+def test_layer_parity_rows_wider_than_4096():
+    """LayerNorm's widest layout (32 values per thread) on a ragged width:
+    h = 4608 leaves the last column group partly past the row; 9 heads of 512
+    over 3 shards, one sequence of 64 tokens, both dropouts on."""
+    cfg = dict(SMALL, s=64, h=4608, hp=4608, n_heads=9, N=3, layer=4)
+    check_layer(cfg, SI.layer_inputs(dict(cfg, b=1)))
+
+
+def test_layer_parity_widest_rows_8192():
+    """The widest rows the layer accepts (h = 8192, 16 heads of 512 over 2
+    shards), one sequence of 32 tokens."""
+    cfg = dict(SMALL, s=32, h=8192, hp=8192, n_heads=16, N=2, layer=5)
+    check_layer(cfg, SI.layer_inputs(dict(cfg, b=1)))
+
+
 def test_layer_deterministic():
     cfg = dict(SMALL)
     inp = SI.layer_inputs(dict(cfg, b=1))
