@@ -33,10 +33,11 @@
  *    TP_ERR_ALIGN before anything is launched.  M (and T) may be any value >= 0.
  *  - Ownership: the caller allocates and owns every buffer, including the
  *    workspace.  The library allocates nothing: its state is static device
- *    memory (an error word, tile-scheduler and tile-completion counters, a
- *    16 x 64 block of ones) and it never frees caller memory.  Launches
- *    rotate over 64 counter slots, so at most 64 launches may be in flight
- *    at the same time across all streams of a device.  A call captured into a
+ *    memory (an error word, tile-scheduler and tile-completion counters, the
+ *    optimizer's completion counters, a 16 x 64 block of ones) and it never
+ *    frees caller memory.  Tensor-core GEMM launches and optimizer norm passes
+ *    each rotate over 64 counter slots, so at most 64 launches of each may be
+ *    in flight at the same time across all streams of a device.  A call captured into a
  *    CUDA graph keeps the slot it was given at capture: replay such a graph
  *    on one stream at a time (replays in sequence reuse the slot safely, since
  *    every launch resets its counters as it ends).
