@@ -30,7 +30,7 @@ __device__ int g_opt_done[kOptSlots];
 std::atomic<unsigned> g_opt_slot_seq{0};
 
 constexpr int kOptThreads = 256;
-constexpr int64_t kOptChunk = 8192;  // elements per chunk (a multiple of 4 x kOptThreads)
+constexpr int64_t kOptChunk = 16384;  // elements per chunk (a multiple of 4 x kOptThreads)
 static_assert(kOptChunk % (4 * kOptThreads) == 0, "chunk = whole float4 rows of the block");
 
 // Scalars the finalize kernel hands to the update kernel (workspace head).
@@ -157,7 +157,7 @@ __global__ void __launch_bounds__(kOptThreads) opt_norm_kernel(const __grid_cons
       bad |= !isfinite(a);
       part = fmaf(a, a, part);
     }
-    acc += static_cast<double>(part);  // at most 32 fp32 squares per thread per chunk
+    acc += static_cast<double>(part);  // at most 64 fp32 squares per thread per chunk
   }
   // block sum in a fixed tree
   __shared__ double red[kOptThreads];
