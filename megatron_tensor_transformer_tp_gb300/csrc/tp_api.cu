@@ -484,6 +484,30 @@ tp_status launch_tc_groups(const Plan& pl, const bool* used, GemmGroup* groups, 
     g.n_fastest = i >= interleave && g.kr_mode == KR_NONE && g.dep_kind == DEP_NONE && g.prod_row < 0 &&
                   g.prod_col < 0 && g.M > g.N && a_bytes > 128.0 * (1 << 20);
   }
+  // Stripes: in launches without dependent tiles, consecutive groups with
+  // causal contraction ranges (P V, dV, dQ, dK of the attention core: one
+  // group per head, each tile's length set by its row block) and the same
+  // tiling are enumerated together, so the longest tiles of every head come
+  // first and the launch does not end on one head's long tiles.
+  for (int i = 0; i < ng; ++i) groups[i].stripe_first = i, groups[i].stripe_n = 1;
+  bool any_dep = false;
+  for (int i = 0; i < ng; ++i) any_dep = any_dep || groups[i].dep_kind != DEP_NONE;
+  if (!any_dep) {
+    auto stripable = [&](const GemmGroup& g) {
+      return (g.kr_mode == KR_END || g.kr_mode == KR_BEGIN) && g.kr_mode != KR_TRI && !g.n_fastest &&
+             g.prod_row < 0 && g.prod_col < 0;
+    };
+    for (int i = interleave; i < ng;) {
+      int j = i + 1;
+      if (stripable(groups[i]))
+        while (j < ng && j - i < 255 && stripable(groups[j]) && groups[j].tiles_m == groups[i].tiles_m &&
+               groups[j].tiles_n == groups[i].tiles_n)
+          ++j;
+      if (j - i > 1)
+        for (int k = i; k < j; ++k) groups[k].stripe_first = i, groups[k].stripe_n = j - i;
+      i = j;
+    }
+  }
   for (int i = 0; i < ng; ++i) {
     GemmGroup& g = groups[i];
     g.tile_begin = tiles;

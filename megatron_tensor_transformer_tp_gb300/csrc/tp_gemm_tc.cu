@@ -63,7 +63,8 @@ constexpr int EPI_WARP_BYTES = EPI_STAGE_BYTES;
 // constant cache).
 struct GrpLite {
   int tile_begin, tiles_m, tiles_n;
-  int flags;  // bit 0: causal tiles only (tri); bit 1: column tiles fastest; bits 8..15: kr_mode
+  int flags;  // bit 0: causal tiles only (tri); bit 1: column tiles fastest; bit 2: striped;
+              // bits 8..15: kr_mode; bits 16..23: groups in the stripe; bits 24..31: its first group
 };
 constexpr int TBL_BYTES = 1024;
 static_assert(kMaxGroups * sizeof(GrpLite) <= TBL_BYTES, "group table does not fit");
@@ -258,8 +259,16 @@ __device__ __forceinline__ TileCoord decode_tile_rows(const TcGemmParams& p, con
   int g = p.interleave_groups;
   const int ng = p.num_groups;
   while (g + 1 < ng && tile >= L[g + 1].tile_begin) ++g;
+  int local = tile - L[g].tile_begin;
+  if (ATTN && (L[g].flags & 4)) {
+    // a stripe of identical groups: consecutive tiles cycle through the
+    // groups, each group's tiles in its own order (longest contraction first)
+    const int first = (L[g].flags >> 24) & 0xff, n = (L[g].flags >> 16) & 0xff;
+    const int t = tile - L[first].tile_begin;
+    g = first + t % n;
+    local = t / n;
+  }
   const GrpLite G = L[g];
-  const int local = tile - G.tile_begin;
   TileCoord c;
   c.g = g;
   if (ATTN && (G.flags & 1)) {
@@ -294,7 +303,8 @@ __device__ __forceinline__ void fill_group_table(const TcGemmParams& p, GrpLite*
   for (int i = tid; i < p.num_groups; i += nthreads) {
     const GemmGroup& G = p.grp[i];
     L[i] = GrpLite{G.tile_begin, G.tiles_m, G.tiles_n,
-                   (G.tri ? 1 : 0) | (G.n_fastest ? 2 : 0) | (G.kr_mode << 8)};
+                   (G.tri ? 1 : 0) | (G.n_fastest ? 2 : 0) | (G.stripe_n > 1 ? 4 : 0) | (G.kr_mode << 8) |
+                       (G.stripe_n << 16) | (G.stripe_first << 24)};
   }
 }
 

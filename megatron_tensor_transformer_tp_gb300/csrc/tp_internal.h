@@ -102,6 +102,10 @@ struct GemmGroup {
   // Tile order (set by the launcher): column tiles fastest instead of row
   // blocks, so consecutive tiles share the A operand's row block.
   int n_fastest;
+  // Stripe (set by the launcher; attention instance): stripe_n > 1 identical
+  // groups starting at group stripe_first whose tiles are enumerated cycling
+  // through the groups.
+  int stripe_first, stripe_n;
 };
 
 // One operand pair of the tensor-core engine.  Operands are bf16.
