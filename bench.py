@@ -123,7 +123,7 @@ def load_peaks():
 _GEMM_SRC = ("tp_gemm_tc.cu", "tp_api.cu", "tp_internal.h", "tp_device.cuh")
 KERNEL_SOURCES = {"gemm": _GEMM_SRC, "embed": ("tp_embed.cu", "tp_internal.h"),
                   "ce_reduce": ("tp_embed.cu", "tp_internal.h"),
-                  "attn_lse": ("tp_attn.cu", "tp_internal.h"), "attn_rowdot": ("tp_attn.cu", "tp_internal.h"),
+                  "attn_norm": ("tp_attn.cu", "tp_internal.h"), "attn_rowdot": ("tp_attn.cu", "tp_internal.h"),
                   "layer": ("tp_layer.cu", "tp_internal.h"), "attn_keep": ("tp_layer.cu", "tp_internal.h"),
                   "adam": ("tp_opt.cu", "tp_internal.h")}
 
@@ -449,12 +449,26 @@ class CEBench:
         return {"gemm_ce_fwd": ("tensor", f), "gemm_ce_bwd": ("tensor", 2 * f), "ce_reduce": ("hbm", red)}
 
 
+def attn_norm_bytes(pairs, s, causal, dropout):
+    """Algorithmic bytes of one attn_norm call: the per-part statistics its rows
+    merge (8 B per part), the lse it writes, the stored exponentials it reads
+    (the causal part of each row) and the probabilities it writes (whole rows,
+    zeros after the causal limit), plus, with dropout, the keep words of the
+    causal part and the dropped probabilities."""
+    parts = sum(r // 64 + 1 for r in range(s)) if causal else s * ((s + 63) // 64)
+    kept = s * (s + 1) / 2.0 if causal else float(s * s)
+    b = parts * 8.0 + s * 4.0 + kept * 2.0 + s * s * 2.0
+    if dropout:
+        b += kept / 8.0 + s * s * 2.0
+    return pairs * b
+
+
 class AttnCoreBench:
-    """Causal attention core per head: forward (row statistics, P and C = P V)
-    and backward (dS with dV, then dQ and dK).  The step's FLOPs are the
-    method's: 4 b H s^2 d forward and 8 b H s^2 d backward, times the causal
-    fraction (s + 1) / 2s; the forward's second score GEMM (P is recomputed
-    rather than storing fp32 scores) is not counted in the step."""
+    """Causal attention core per head: forward (scores with per-part
+    statistics and exponentials, their normalisation into P, C = P V) and
+    backward (dS with dV, then dQ and dK).  The step's FLOPs are the method's:
+    4 b H s^2 d forward and 8 b H s^2 d backward, times the causal fraction
+    (s + 1) / 2s."""
     kind = "attn_core"
 
     def __init__(self, name, tp, torch):
@@ -485,9 +499,9 @@ class AttnCoreBench:
     def kernel_work(self):
         u = 2.0 * self.b * self.H * self.s * self.s * self.d * self.frac  # one s x s x d contraction
         rows = self.b * self.H * self.s
-        return {"gemm_attn_scores": ("tensor", u), "gemm_attn_pv": ("tensor", 2 * u),
+        return {"gemm_attn_scores": ("tensor", u), "gemm_attn_pv": ("tensor", u),
                 "gemm_attn_bwd": ("tensor", 4 * u),
-                "attn_lse": ("hbm", rows * (self.s + 63) // 64 * 8.0 + rows * 4.0),
+                "attn_norm": ("hbm", attn_norm_bytes(self.b * self.H, self.s, self.causal, False)),
                 "attn_rowdot": ("hbm", 2.0 * self.T * self.h * 2 + rows * 4.0)}
 
 
@@ -553,9 +567,10 @@ class LayerBench:
                 "gemm_layer_oproj_bwd": ("tensor", 4.0 * T * h * h),
                 "gemm_layer_qkv_bwd": ("tensor", 12.0 * T * h * h),
                 "gemm_mlp_fwd": ("tensor", 4.0 * T * h * hp), "gemm_mlp_bwd": ("tensor", 8.0 * T * h * hp),
-                "gemm_attn_scores": ("tensor", u), "gemm_attn_pv": ("tensor", 2 * u),
+                "gemm_attn_scores": ("tensor", u), "gemm_attn_pv": ("tensor", u),
                 "gemm_attn_bwd": ("tensor", 4 * u),
-                "attn_lse": ("hbm", rows * (self.s + 63) // 64 * 8.0 + rows * 4.0),
+                "attn_norm": ("hbm", attn_norm_bytes(self.b * self.H, self.s, self.cfg["causal"],
+                                                     self.cfg["p_attn"] > 0)),
                 "attn_rowdot": ("hbm", 2.0 * th + rows * 4.0),
                 "attn_keep": ("hbm", rows * ((self.s + 31) // 32) * 4.0),
                 # per call: read x, write y (bf16) plus the row statistics

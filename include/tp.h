@@ -198,10 +198,14 @@ TP_API tp_status tp_attn_proj_bwd(tp_dtype dt, int64_t M, int64_t h, int n_heads
  *                 tp_attn_proj_fwd).
  *   lse out (b, n_heads, s) fp32 log-sum-exp of every score row, or NULL.
  *   workspace of tp_attn_core_workspace_size bytes, 256-byte aligned.
- * Constraints: T % s == 0 (TP_ERR_INVALID); d and s multiples of 8
- * (TP_ERR_ALIGN, TMA's 16-byte rule for head offsets and P's rows).
- * The scores are computed twice (once for the row statistics, once for P):
- * no (s x s) fp32 score matrix is stored.
+ * Constraints: T % s == 0 (TP_ERR_INVALID); d and s multiples of 8 and P
+ * 16-byte aligned (TP_ERR_ALIGN, TMA's 16-byte rule for head offsets and P's
+ * rows).
+ * Three steps: the scores launch stores, per row and 64-key part,
+ * e = exp(S - m) with m the part's max into P, and (m, sum e) into the
+ * workspace; a row kernel merges the parts into lse and rescales P in place
+ * to e exp(m - lse); then C = P V.  No (s x s) fp32 score matrix is stored,
+ * and the scores are computed once.
  */
 TP_API tp_status tp_attn_core_fwd(tp_dtype dt, int64_t T, int64_t s, int64_t h, int n_heads, int N,
                                   int causal, const void* QKV, void* P, void* C, float* lse,
@@ -240,7 +244,8 @@ TP_API size_t tp_attn_core_workspace_size(int64_t T, int64_t s, int64_t h, int n
  * stream as two words) under key (seed as two words), kept iff it is >=
  * floor(p_attn * 65536) computed from the fp32 p_attn.  The backward draws the
  * same bits again.  p_attn > 0 needs s % 16 == 0, s <= 65535 and at most 65535
- * (sequence, head) pairs (TP_ERR_INVALID otherwise) and a non-NULL Pd.
+ * (sequence, head) pairs (TP_ERR_INVALID otherwise) and a non-NULL, 16-byte
+ * aligned Pd (TP_ERR_ALIGN).
  * Other arguments as tp_attn_core_fwd / _bwd; the backward's dV is Pd^T dC
  * and its dP is (dC V^T) * keep / (1 - p_attn).
  */

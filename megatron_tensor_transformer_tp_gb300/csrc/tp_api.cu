@@ -537,6 +537,7 @@ tp_status launch_tc_groups(const Plan& pl, const bool* used, GemmGroup* groups, 
     bool ok = false;
     switch (g.epi) {
       case EPI_STORE: case EPI_BIAS_GELU: case EPI_DGELU: case EPI_CE_BWD: case EPI_SOFTMAX:
+      case EPI_SMAX_PARTS:
       case EPI_SMAX_BWD:
         ok = true;
         break;
@@ -547,7 +548,8 @@ tp_status launch_tc_groups(const Plan& pl, const bool* used, GemmGroup* groups, 
         break;
     }
     // the stores of these epilogues are bf16 whatever out_type says
-    const bool out_f32 = f32 && !(g.epi == EPI_CE_BWD || g.epi == EPI_SOFTMAX || g.epi == EPI_SMAX_BWD);
+    const bool out_f32 = f32 && !(g.epi == EPI_CE_BWD || g.epi == EPI_SOFTMAX || g.epi == EPI_SMAX_BWD ||
+                                  g.epi == EPI_SMAX_PARTS);
     // fp32 outputs keep the lanes' stores: their two 64-byte halves per chunk
     // would wait on each other's bulk read (measured slower on the backward)
     if (!ok || out_f32) continue;
@@ -570,7 +572,7 @@ tp_status launch_tc_groups(const Plan& pl, const bool* used, GemmGroup* groups, 
   p.attn = 0;
   for (int i = 0; i < ng; ++i)
     if (groups[i].kr_mode != KR_NONE || groups[i].causal || groups[i].alpha != 1.f ||
-        groups[i].epi == EPI_SOFTMAX || groups[i].epi == EPI_SMAX_BWD)
+        groups[i].epi == EPI_SOFTMAX || groups[i].epi == EPI_SMAX_BWD || groups[i].epi == EPI_SMAX_PARTS)
       p.attn = 1;
   p.num_groups = ng;
   p.num_segs = pl.ns;
@@ -993,6 +995,7 @@ tp_status attn_core_fwd_impl(tp_dtype dt, int64_t T, int64_t s, int64_t h, int n
   if (!QKV || !P || !C || (p_drop > 0.f && !Pd)) return TP_ERR_INVALID;
   if (workspace == nullptr || ws_bytes < attn_fwd_ws(a, s)) return TP_ERR_WORKSPACE;
   if (!al256(workspace)) return TP_ERR_ALIGN;
+  if (!al16(P) || (p_drop > 0.f && !al16(Pd))) return TP_ERR_ALIGN;
   cudaStream_t strm = static_cast<cudaStream_t>(stream);
   float* parts = static_cast<float*>(workspace);
   float* row_lse = lse ? lse
@@ -1002,67 +1005,45 @@ tp_status attn_core_fwd_impl(tp_dtype dt, int64_t T, int64_t s, int64_t h, int n
                             : reinterpret_cast<uint32_t*>(bb(workspace) +
                                                           round256(static_cast<size_t>(a.pairs * a.P * s) * 8) +
                                                           round256(static_cast<size_t>(a.pairs * s) * 4));
-  const int wpr = static_cast<int>((s + 31) / 32);
   const float alpha = static_cast<float>(1.0 / sqrt(static_cast<double>(a.d)));
   const int kr_s = causal ? KR_TRI : KR_NONE;
-  // 1. per row and 64-key part: (max, sum exp) of alpha q k^T, no scores stored
+  // 1. scores alpha q k^T per (sequence, head), causal tiles only: per row and
+  //    64-key part the max m and e = exp(alpha q k^T - m), e stored where P goes
+  //    and (m, sum e) to the part statistics
   const int64_t per1 = pairs_per_launch(1, 0);
   for (int64_t g0 = 0; g0 < a.pairs; g0 += per1) {
     Plan p;
     for (int64_t g = g0; g < std::min(a.pairs, g0 + per1); ++g) {
       const HeadPtrs hp = head_ptrs(QKV, g / n_heads, s, h, n_heads, N, static_cast<int>(g % n_heads));
       const int si = p.add_seg(kmajor(hp.q, s, a.d, 3 * h), kmajor(hp.k, s, a.d, 3 * h), a.d);
-      GemmGroup& gr = p.add_group(s, s, si, si + 1, EPI_CE_FWD, OUT_F32, nullptr, 0);
+      GemmGroup& gr = p.add_group(s, s, si, si + 1, EPI_SMAX_PARTS, OUT_BF16,
+                                  bb(P) + static_cast<size_t>(g * s * s) * 2, s);
       gr.alpha = alpha;
       gr.causal = causal != 0;
       gr.kr_mode = kr_s;
       gr.ce_part = parts;
       gr.ce_part0 = static_cast<int>(g * a.P);
       gr.ce_rows = static_cast<int>(s);
-      gr.tri_ok = 1;  // parts after a row's last key are never read
+      gr.tri_ok = 1;  // tiles after a row block's last key: zeros written by step 2
     }
     st = run_plan(p, dt, "gemm_attn_scores", strm);
     if (st != TP_OK) return st;
   }
-  // 2. log-sum-exp per row, parts merged in order
-  cudaError_t e = timed("attn_lse", strm, [&] {
-    return launch_attn_lse(parts, static_cast<int>(a.P), s, a.pairs * s, causal != 0, row_lse, strm);
+  // 2. log-sum-exp per row (parts merged in a fixed order), then in place
+  //    P = e exp(m - lse) (zero where masked); with attention dropout also the
+  //    keep words (drawn here) and P keep / (1 - p) to Pd
+  const cudaError_t e = timed("attn_norm", strm, [&] {
+    return launch_attn_norm(parts, static_cast<int>(a.P), s, a.pairs, causal != 0, row_lse, P,
+                            p_drop > 0.f ? Pd : nullptr, keep, p_drop, seed, stream0, n_heads, n_heads / N,
+                            strm);
   });
   if (e != cudaSuccess) return TP_ERR_CUDA;
-  if (p_drop > 0.f) {
-    e = timed("attn_keep", strm, [&] {
-      return launch_attn_keep(a.pairs, s, n_heads, n_heads / N, causal != 0, seed, stream0, p_drop, keep, strm);
-    });
-    if (e != cudaSuccess) return TP_ERR_CUDA;
-  }
-  // 3. P = exp(alpha q k^T - lse) (scores recomputed, stored in bf16), and in
-  //    the same launch C_j = P V_j, a row block once its P rows are stored
-  const int64_t rows_per_pair = (s + 255) / 256 * 2;  // 128-row blocks, pair tiles rounded up
-  const int64_t per3 = pairs_per_launch(2, rows_per_pair);
-  if (per3 < 1) return TP_ERR_INVALID;
+  // 3. C_j = P V_j (with dropout Pd V_j), the contraction stopped at the
+  //    tile's last query when causal (the keys after it have P = 0)
+  const int64_t per3 = pairs_per_launch(1, 0);
   for (int64_t g0 = 0; g0 < a.pairs; g0 += per3) {
     Plan p;
-    const int64_t g1 = std::min(a.pairs, g0 + per3);
-    int rows[kMaxGroups];
-    for (int64_t g = g0; g < g1; ++g) {
-      const HeadPtrs hp = head_ptrs(QKV, g / n_heads, s, h, n_heads, N, static_cast<int>(g % n_heads));
-      rows[g - g0] = p.counters(rows_per_pair);
-      const int si = p.add_seg(kmajor(hp.q, s, a.d, 3 * h), kmajor(hp.k, s, a.d, 3 * h), a.d);
-      GemmGroup& gr = p.add_group(s, s, si, si + 1, EPI_SOFTMAX, OUT_BF16,
-                                  bb(P) + static_cast<size_t>(g * s * s) * 2, s);
-      gr.alpha = alpha;
-      gr.causal = causal != 0;
-      gr.kr_mode = kr_s;
-      gr.row_lse = row_lse + g * s;
-      gr.prod_row = rows[g - g0];
-      if (p_drop > 0.f) {
-        gr.out2 = bb(Pd) + static_cast<size_t>(g * s * s) * 2;
-        gr.drop_mask = keep + g * s * wpr;
-        gr.drop_wpr = wpr;
-        gr.drop_scale = 1.f / (1.f - p_drop);
-      }
-    }
-    for (int64_t g = g0; g < g1; ++g) {
+    for (int64_t g = g0; g < std::min(a.pairs, g0 + per3); ++g) {
       const int64_t bi = g / n_heads;
       const HeadPtrs hp = head_ptrs(QKV, bi, s, h, n_heads, N, static_cast<int>(g % n_heads));
       const void* Pg = bb(p_drop > 0.f ? Pd : P) + static_cast<size_t>(g * s * s) * 2;
@@ -1070,8 +1051,6 @@ tp_status attn_core_fwd_impl(tp_dtype dt, int64_t T, int64_t s, int64_t h, int n
       GemmGroup& gr = p.add_group(s, a.d, si, si + 1, EPI_STORE, OUT_BF16,
                                   bb(C) + (static_cast<size_t>(bi * s) * h + hp.cc) * 2, h);
       gr.kr_mode = causal ? KR_END : KR_NONE;
-      gr.dep_kind = DEP_ROW;
-      gr.dep_base = rows[g - g0];
     }
     st = run_plan(p, dt, "gemm_attn_pv", strm);
     if (st != TP_OK) return st;

@@ -931,6 +931,60 @@ __device__ __forceinline__ void ce_fwd_epilogue_warp(const GemmGroup& G, int lan
 }
 
 // ---------------------------------------------------------------------------
+// Attention scores epilogue of one warp's region (its 32 rows and one 64-column
+// part, as above): m = the part's max of alpha acc over the columns the causal
+// mask keeps, e = exp(alpha acc - m) stored in bf16 (0 where masked), and
+// (m, sum e) per row to the part statistics.  A first pass over the part's
+// TMEM columns finds m, a second computes, sums and stores e.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void smax_parts_epilogue_warp(const GemmGroup& G, const CUtensorMap* mapO,
+                                                         uint4* st, int lane, int row0, int n0, int c_begin,
+                                                         int cpw, uint32_t taddr) {
+  const int nb = n0 + c_begin * 32;
+  if (nb >= G.N) return;  // warp-uniform: no part here
+  const int row = row0 + lane;
+  const bool row_ok = row < G.M;
+  const uint64_t map1 = G.out_map >= 0 ? reinterpret_cast<uint64_t>(mapO + G.out_map) : 0ull;
+  const float l2e = 1.4426950408889634f;
+  float m = -INFINITY;
+  for (int c = c_begin; c < c_begin + cpw; ++c) {
+    const int n = n0 + c * 32;
+    if (n >= G.N) break;  // warp-uniform
+    const int jn = G.causal ? min(min(32, G.N - n), row - n + 1) : min(32, G.N - n);
+    uint32_t rr[32];
+    tmem_ld32(taddr + static_cast<uint32_t>(c * 32), rr);
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (j < jn) m = fmaxf(m, __uint_as_float(rr[j]) * G.alpha);
+  }
+  const float base = m == -INFINITY ? 0.f : -m * l2e;  // a row with no kept column stores zeros
+  float sum = 0.f;
+  for (int c = c_begin; c < c_begin + cpw; ++c) {
+    const int n = n0 + c * 32;
+    if (n >= G.N) break;  // warp-uniform
+    const int ncols = min(32, G.N - n);
+    const int jn = G.causal ? min(ncols, row - n + 1) : ncols;
+    uint32_t rr[32];
+    tmem_ld32(taddr + static_cast<uint32_t>(c * 32), rr);
+    float v[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      v[j] = j < jn ? ex2_ftz(fmaf(__uint_as_float(rr[j]) * G.alpha, l2e, base)) : 0.f;
+      sum += v[j];
+    }
+    if (ncols == 32 && G.vec_ok) {
+      stage_store_rows(st, G.out, OUT_BF16, G.ldo, row0, G.M, n, v, lane, map1);
+    } else if (row_ok) {
+      store_chunk(G.out, OUT_BF16, G.ldo, row, n, v, ncols, false);
+    }
+  }
+  if (row_ok) {
+    const int64_t part = G.ce_part0 + nb / 64;
+    reinterpret_cast<float2*>(G.ce_part)[part * G.ce_rows + row] = make_float2(m, sum);
+  }
+}
+
+// ---------------------------------------------------------------------------
 // Dynamic tile scheduling: one (next, done) counter pair per launch slot.  The
 // last CTA to finish resets its pair, so the next launch using the slot starts
 // from zero.  Launches rotate over the slots.
@@ -1177,7 +1231,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
           tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(buf * BN);
       const bool empty = tile_empty<BM, ATTN>(p, G, tc.m0, tc.n0);
       if (G.epi == EPI_CE_FWD) ce_fwd_epilogue_warp<ATTN>(G, lane, row0, tc.n0, c_begin, cpw, taddr);
-      for (int c = c_begin; G.epi != EPI_CE_FWD && c < c_begin + cpw; ++c) {
+      if (ATTN && G.epi == EPI_SMAX_PARTS)
+        smax_parts_epilogue_warp(G, p.mapO, epi_stage, lane, row0, tc.n0, c_begin, cpw, taddr);
+      for (int c = c_begin; G.epi != EPI_CE_FWD && !(ATTN && G.epi == EPI_SMAX_PARTS) && c < c_begin + cpw;
+           ++c) {
         const int n = tc.n0 + c * 32;
         if (n >= G.N) break;  // warp-uniform
         uint32_t rr[32];
@@ -1704,7 +1761,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_pair_kernel(const __gr
           tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(buf * BN);
       const bool empty = tile_empty<BM2, ATTN>(p, G, tc.m0, tc.n0);
       if (G.epi == EPI_CE_FWD) ce_fwd_epilogue_warp<ATTN>(G, lane, row0, tc.n0, c_begin, cpw, taddr);
-      for (int c = c_begin; G.epi != EPI_CE_FWD && c < c_begin + cpw; ++c) {
+      if (ATTN && G.epi == EPI_SMAX_PARTS)
+        smax_parts_epilogue_warp(G, p.mapO, epi_stage, lane, row0, tc.n0, c_begin, cpw, taddr);
+      for (int c = c_begin; G.epi != EPI_CE_FWD && !(ATTN && G.epi == EPI_SMAX_PARTS) && c < c_begin + cpw;
+           ++c) {
         const int n = tc.n0 + c * 32;
         if (n >= G.N) break;  // warp-uniform
         uint32_t rr[32];

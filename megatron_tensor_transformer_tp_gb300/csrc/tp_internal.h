@@ -29,7 +29,10 @@ enum Epi : int {
                       // to ce_part; the logit at the row's target column to ce_target; no output
   EPI_CE_BWD = 6,     // out (bf16) = (exp(acc - row_lse[m]) - [col0 + n == row_target[m]]) * row_dloss[m]
   EPI_SOFTMAX = 7,    // out (bf16) = exp(alpha acc - row_lse[m]), 0 where causal masks (n > m)
-  EPI_SMAX_BWD = 8    // out (bf16) = aux[m, n] * (acc - row_lse[m]) * alpha  (softmax backward)
+  EPI_SMAX_BWD = 8,   // out (bf16) = aux[m, n] * (acc - row_lse[m]) * alpha  (softmax backward)
+  EPI_SMAX_PARTS = 9  // attention scores: per row and 64-column part, m = max of alpha acc over the
+                      // columns causal keeps and (m, sum e) to ce_part; out (bf16) = e =
+                      // exp(alpha acc - m), 0 where causal masks (n > m)
 };
 
 // Per-tile k-block ranges of causal attention (rows and columns of the output
@@ -165,10 +168,17 @@ struct RangeTable {
   int n;
 };
 
-// Attention core row kernels: per-part (max, sum) merge into log-sum-exp, and
-// the per-(pair, token) dot product of dC and C over a head's columns.
-cudaError_t launch_attn_lse(const void* part, int P, int64_t s, int64_t rows, int causal, float* lse,
-                            cudaStream_t st);
+// Attention core row kernels: the probabilities from the scores launch's
+// stored e = exp(alpha s - m_part) and per-part (m_part, sum e) (their
+// log-sum-exp merged in a fixed order, then P = e exp(m_part - lse) in place;
+// when Pd is given also the attention-dropout keep words, drawn as
+// launch_attn_keep draws them, and Pd = P keep / (1 - p)), and the
+// per-(pair, token) dot product of dC and C over a head's columns.  P and Pd
+// are (pairs, s, s) bf16 with 16-byte aligned rows (s % 8 == 0; s % 16 == 0
+// with dropout).
+cudaError_t launch_attn_norm(const void* part, int P, int64_t s, int64_t pairs, int causal, float* lse,
+                             void* Pm, void* Pd, uint32_t* keep, float p_drop, uint64_t seed,
+                             uint64_t stream0, int n_heads, int heads_per_shard, cudaStream_t st);
 cudaError_t launch_attn_rowdot(const void* C, const void* dC, int64_t h, int64_t s, int n_heads, int d,
                                int64_t pairs, float* D, cudaStream_t st);
 

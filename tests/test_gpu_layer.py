@@ -273,6 +273,30 @@ def test_layer_gradients_accumulate():
             assert torch.allclose(a, 2 * b, rtol=1e-5, atol=1e-6), k
 
 
+def test_layer_saved_keep_words_bit_exact():
+    """The keep words the forward saves are the oracle's attention-dropout
+    flags bit for bit: 32 keys per word, every word whose first key is at or
+    before the query drawn in full, the later words zero, and the keys past s
+    of a row's last word zero (s = 48: a half-filled last word)."""
+    cfg = dict(SMALL, s=48)
+    inp = SI.layer_inputs(dict(cfg, b=2))
+    _, saved, _, _ = run_layer(cfg, inp, keep_buffer=True)
+    s, H, N, p, seed, layer = cfg["s"], cfg["n_heads"], cfg["N"], cfg["p_attn"], cfg["seed"], cfg["layer"]
+    wpr = (s + 31) // 32
+    words = saved["attn_keep"].cpu().numpy().view(np.uint32).reshape(-1, H, s, wpr)
+    for bi in range(words.shape[0]):
+        for j in range(H):
+            keep = O.attention_keep(bi, j, s, H, N, f32p(p), seed, layer)
+            want = np.zeros((s, wpr), dtype=np.uint32)
+            for q in range(s):
+                for w in range(wpr):
+                    if 32 * w > q:
+                        continue
+                    for k in range(min(32, s - 32 * w)):
+                        want[q, w] |= np.uint32(int(keep[q, 32 * w + k]) << k)
+            assert np.array_equal(words[bi, j], want), (bi, j)
+
+
 def test_layer_saved_keep_words_match_redrawn():
     """Keeping the attention-dropout bits from the forward gives the same
     results as drawing them again in the backward."""
