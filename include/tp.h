@@ -655,6 +655,12 @@ TP_API void tp_debug_set_gemm_kernel(int mode);
  * outputs first.  Default 8; values <= 0 restore it. */
 TP_API void tp_debug_set_split_threshold(int tiles_per_sm);
 TP_API void tp_debug_set_wait_limit_ms(int ms);
+/* Programmatic dependent launch of the library's kernels: on (default), a
+ * kernel may start while the previous kernel on its stream finishes, waiting
+ * on the device for that kernel's completion before it touches memory (its
+ * set-up overlaps the previous kernel's tail); off (0), every kernel starts
+ * after the previous one has completed.  Results are identical either way. */
+TP_API void tp_debug_set_pdl(int on);
 
 #ifdef __cplusplus
 }

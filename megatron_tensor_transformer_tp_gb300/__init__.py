@@ -25,7 +25,7 @@ __all__ = [
     "tied_embed_grad_noalloc", "tp_get_status",
     "tp_status_string", "tp_num_sms", "tp_profile_enable", "tp_profile_reset", "tp_profile_read",
     "tp_debug_inject_fault", "tp_debug_set_wait_limit_ms", "tp_debug_set_gemm_kernel",
-    "tp_debug_set_split_threshold",
+    "tp_debug_set_split_threshold", "tp_debug_set_pdl",
     "tp_gelu_eval", "logits_pitch", "tp_adam_step", "tp_adam_step_workspace_size",
     "tp_optimizer_state", "tp_adam_config", "tp_param_group", "make_optimizer_state",
     "read_optimizer_state", "tp_attn_core_fwd", "tp_attn_core_bwd", "tp_attn_core_workspace_size",
@@ -126,6 +126,7 @@ _SIGNATURES = {
     "tp_debug_inject_fault": (None, [_int]),
     "tp_debug_set_gemm_kernel": (None, [_int]),
     "tp_debug_set_split_threshold": (None, [_int]),
+    "tp_debug_set_pdl": (None, [_int]),
     "tp_gelu_eval": (_int, [_c_void_p, _c_void_p, _c_void_p, _i64, _c_void_p]),
     "tp_debug_set_wait_limit_ms": (None, [_int]),
     "tp_adam_step": (_int, [ctypes.POINTER(tp_param_group), _int, ctypes.POINTER(tp_adam_config),
@@ -638,6 +639,11 @@ def tp_debug_set_gemm_kernel(mode: int):
 def tp_debug_set_split_threshold(tiles_per_sm: int):
     """Tiles per SM above which a plan with dependent outputs runs as two launches."""
     lib().tp_debug_set_split_threshold(int(tiles_per_sm))
+
+
+def tp_debug_set_pdl(on: bool):
+    """Programmatic dependent launch of the library's kernels (default on)."""
+    lib().tp_debug_set_pdl(1 if on else 0)
 
 
 def tp_debug_set_wait_limit_ms(ms: int):

@@ -48,6 +48,7 @@ int g_fault_kind = 0;
 int g_gemm_mode = 2;  // 0: one-SM kernel, 1: two-SM kernel, 2: choose per launch
 int g_split_tiles_per_sm = 8;  // plans with dependent tiles and more tiles per SM run as two launches
 unsigned long long g_wait_limit_ns = 1000ull * 1000ull * 1000ull;
+int g_pdl = 1;  // programmatic dependent launch of the library's kernels
 
 tp_status device_state(DeviceState** out) {
   int dev = 0;
@@ -146,6 +147,7 @@ void prof_flush_locked() {
 }  // namespace
 
 void tp::count_launches(int n) { g_kernel_launches.fetch_add(n); }
+bool tp::pdl_on() { return g_pdl != 0; }
 
 namespace {
 
@@ -536,9 +538,8 @@ tp_status launch_tc_groups(const Plan& pl, const bool* used, GemmGroup* groups, 
     const bool f32 = g.out_type == OUT_F32;
     bool ok = false;
     switch (g.epi) {
-      case EPI_STORE: case EPI_BIAS_GELU: case EPI_DGELU: case EPI_CE_BWD: case EPI_SOFTMAX:
+      case EPI_STORE: case EPI_BIAS_GELU: case EPI_DGELU: case EPI_CE_BWD: case EPI_SMAX_BWD:
       case EPI_SMAX_PARTS:
-      case EPI_SMAX_BWD:
         ok = true;
         break;
       case EPI_F32: case EPI_SEGSUM:
@@ -548,12 +549,11 @@ tp_status launch_tc_groups(const Plan& pl, const bool* used, GemmGroup* groups, 
         break;
     }
     // the stores of these epilogues are bf16 whatever out_type says
-    const bool out_f32 = f32 && !(g.epi == EPI_CE_BWD || g.epi == EPI_SOFTMAX || g.epi == EPI_SMAX_BWD ||
-                                  g.epi == EPI_SMAX_PARTS);
+    const bool out_f32 = f32 && !(g.epi == EPI_CE_BWD || g.epi == EPI_SMAX_BWD || g.epi == EPI_SMAX_PARTS);
     // fp32 outputs keep the lanes' stores: their two 64-byte halves per chunk
     // would wait on each other's bulk read (measured slower on the backward)
     if (!ok || out_f32) continue;
-    const bool two = g.out2 != nullptr && (g.epi == EPI_BIAS_GELU || g.epi == EPI_SOFTMAX);
+    const bool two = g.out2 != nullptr && g.epi == EPI_BIAS_GELU;
     if (nmaps + (two ? 2 : 1) > kMaxStoreMaps) break;
     if (!encode_store_map(&p.mapO[nmaps], g.out, g.M, g.N, g.ldo, out_f32)) continue;
     g.out_map = nmaps++;
@@ -572,7 +572,7 @@ tp_status launch_tc_groups(const Plan& pl, const bool* used, GemmGroup* groups, 
   p.attn = 0;
   for (int i = 0; i < ng; ++i)
     if (groups[i].kr_mode != KR_NONE || groups[i].causal || groups[i].alpha != 1.f ||
-        groups[i].epi == EPI_SOFTMAX || groups[i].epi == EPI_SMAX_BWD || groups[i].epi == EPI_SMAX_PARTS)
+        groups[i].epi == EPI_SMAX_BWD || groups[i].epi == EPI_SMAX_PARTS)
       p.attn = 1;
   p.num_groups = ng;
   p.num_segs = pl.ns;
@@ -1813,6 +1813,8 @@ extern "C" void tp_debug_set_gemm_kernel(int mode) { g_gemm_mode = (mode >= 0 &&
 extern "C" void tp_debug_set_split_threshold(int tiles_per_sm) {
   g_split_tiles_per_sm = tiles_per_sm > 0 ? tiles_per_sm : 8;
 }
+
+extern "C" void tp_debug_set_pdl(int on) { g_pdl = on != 0; }
 
 extern "C" void tp_debug_set_wait_limit_ms(int ms) {
   g_wait_limit_ns = static_cast<unsigned long long>(ms > 0 ? ms : 1000) * 1000000ull;

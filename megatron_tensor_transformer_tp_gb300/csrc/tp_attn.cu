@@ -74,6 +74,8 @@ __global__ void __launch_bounds__(32 * kNormWarps, 4) attn_norm_kernel(const flo
                                                                      __nv_bfloat16* __restrict__ Pm,
                                                                      __nv_bfloat16* __restrict__ Pd,
                                                                      NormDrop dr) {
+  pdl_wait();
+  pdl_trigger();
   const int lane = threadIdx.x & 31;
   const int64_t row = static_cast<int64_t>(blockIdx.x) * kNormWarps + (threadIdx.x >> 5);
   if (row >= s) return;  // warp-uniform
@@ -155,6 +157,8 @@ __global__ void __launch_bounds__(256) attn_rowdot_kernel(const __nv_bfloat16* _
                                                            const __nv_bfloat16* __restrict__ dC,
                                                            int64_t h, int64_t s, int n_heads, int d,
                                                            int64_t g0, int vec, float* __restrict__ D) {
+  pdl_wait();
+  pdl_trigger();
   const int64_t t = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (t >= s) return;
@@ -201,12 +205,10 @@ cudaError_t launch_attn_norm(const void* part, int P, int64_t s, int64_t pairs, 
     const dim3 grid(static_cast<unsigned>((s + kNormWarps - 1) / kNormWarps),
                     static_cast<unsigned>(pairs - g0 < kMaxGridY ? pairs - g0 : kMaxGridY));
     if (Pd != nullptr)
-      attn_norm_kernel<true><<<grid, 32 * kNormWarps, 0, st>>>(
-          static_cast<const float2*>(part), P, s, g0, causal, lse, static_cast<__nv_bfloat16*>(Pm),
+      launch_k(attn_norm_kernel<true>, grid, 32 * kNormWarps, 0, st, static_cast<const float2*>(part), P, s, g0, causal, lse, static_cast<__nv_bfloat16*>(Pm),
           static_cast<__nv_bfloat16*>(Pd), dr);
     else
-      attn_norm_kernel<false><<<grid, 32 * kNormWarps, 0, st>>>(
-          static_cast<const float2*>(part), P, s, g0, causal, lse, static_cast<__nv_bfloat16*>(Pm), nullptr, dr);
+      launch_k(attn_norm_kernel<false>, grid, 32 * kNormWarps, 0, st, static_cast<const float2*>(part), P, s, g0, causal, lse, static_cast<__nv_bfloat16*>(Pm), nullptr, dr);
     count_launches(1);
   }
   return cudaGetLastError();
@@ -219,7 +221,7 @@ cudaError_t launch_attn_rowdot(const void* C, const void* dC, int64_t h, int64_t
   for (int64_t g0 = 0; g0 < pairs; g0 += kMaxGridY) {
     const dim3 grid(static_cast<unsigned>((s + 7) / 8),
                     static_cast<unsigned>(pairs - g0 < kMaxGridY ? pairs - g0 : kMaxGridY));
-    attn_rowdot_kernel<<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(C),
+    launch_k(attn_rowdot_kernel, grid, 256, 0, st, static_cast<const __nv_bfloat16*>(C),
                                              static_cast<const __nv_bfloat16*>(dC), h, s, n_heads, d, g0, vec, D);
     count_launches(1);
   }

@@ -35,6 +35,8 @@ __global__ void __launch_bounds__(256) embed_gather_vec16(const int64_t* __restr
                                                           int64_t row_bytes,
                                                           const __grid_constant__ RangeTable rt,
                                                           uint8_t* __restrict__ out) {
+  pdl_wait();
+  pdl_trigger();
   const int lane = threadIdx.x & 31;
   const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
   const int64_t nvec = row_bytes >> 4;
@@ -62,6 +64,8 @@ __global__ void __launch_bounds__(256) embed_gather_vec16(const int64_t* __restr
 // Byte-granular fallback for rows that are not 16-byte multiples or aligned.
 __global__ void embed_gather_bytes(const int64_t* __restrict__ ids, int64_t T, int64_t row_bytes,
                                    const __grid_constant__ RangeTable rt, uint8_t* __restrict__ out) {
+  pdl_wait();
+  pdl_trigger();
   const int lane = threadIdx.x & 31;
   const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
   for (int64_t t = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; t < T;
@@ -77,6 +81,8 @@ __global__ void embed_gather_bytes(const int64_t* __restrict__ ids, int64_t T, i
 // ---------------------------------------------------------------------------
 __global__ void sort_histogram(const int64_t* __restrict__ ids, int64_t T, int64_t V,
                                int* __restrict__ counts) {
+  pdl_wait();
+  pdl_trigger();
   for (int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; t < T;
        t += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const int64_t v = ids[t];
@@ -104,6 +110,8 @@ __device__ __forceinline__ int4 scan_load4(const int* counts, int64_t V, int64_t
 
 __global__ void __launch_bounds__(SCAN_THREADS) sort_scan(int* __restrict__ counts, int64_t V,
                                                           int* __restrict__ offsets) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ int warp_sums[SCAN_THREADS / 32];
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const int64_t nch = (V + SCAN_CHUNK - 1) / SCAN_CHUNK;
@@ -162,6 +170,8 @@ __global__ void __launch_bounds__(SCAN_THREADS) sort_scan(int* __restrict__ coun
 __global__ void sort_scatter(const int64_t* __restrict__ ids, int64_t T, int64_t V,
                              const int* __restrict__ offsets, int* __restrict__ cursor,
                              int* __restrict__ perm) {
+  pdl_wait();
+  pdl_trigger();
   for (int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; t < T;
        t += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const int64_t v = ids[t];
@@ -172,6 +182,8 @@ __global__ void sort_scatter(const int64_t* __restrict__ ids, int64_t T, int64_t
 // The scatter placed each segment's tokens in arbitrary order; sorting each
 // segment by position makes the result unique (hence deterministic).
 __global__ void sort_segments(const int* __restrict__ offsets, int64_t V, int* __restrict__ perm) {
+  pdl_wait();
+  pdl_trigger();
   for (int64_t v = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; v < V;
        v += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const int b = offsets[v], e = offsets[v + 1];
@@ -194,6 +206,8 @@ __global__ void sort_segments(const int* __restrict__ offsets, int64_t V, int* _
 __global__ void segment_sum_rows(const int* __restrict__ offsets, const int* __restrict__ perm,
                                  int64_t V, const void* __restrict__ dEmb, int in_f32, int64_t h,
                                  const __grid_constant__ RangeTable dE, int accumulate) {
+  pdl_wait();
+  pdl_trigger();
   const int lane = threadIdx.x & 31;
   const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
   for (int64_t v = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; v < V;
@@ -232,9 +246,9 @@ cudaError_t launch_embed_gather(const int64_t* ids, int64_t T, int64_t row_bytes
   for (int r = 0; r < rt.n; ++r) vec = vec && (reinterpret_cast<uintptr_t>(rt.ptr[r]) % 16) == 0;
   const int blocks = blocks_for(T * 32, 256);
   if (vec)
-    embed_gather_vec16<<<blocks, 256, 0, s>>>(ids, T, row_bytes, rt, static_cast<uint8_t*>(out));
+    launch_k(embed_gather_vec16, blocks, 256, 0, s, ids, T, row_bytes, rt, static_cast<uint8_t*>(out));
   else
-    embed_gather_bytes<<<blocks, 256, 0, s>>>(ids, T, row_bytes, rt, static_cast<uint8_t*>(out));
+    launch_k(embed_gather_bytes, blocks, 256, 0, s, ids, T, row_bytes, rt, static_cast<uint8_t*>(out));
   count_launches(1);
   return cudaGetLastError();
 }
@@ -259,11 +273,11 @@ cudaError_t launch_embed_sort(const int64_t* ids, int64_t T, int64_t V, void* ws
   int* counts = sort_counts(ws, T, V);
   cudaError_t e = cudaMemsetAsync(counts, 0, static_cast<size_t>(V) * 4, s);
   if (e != cudaSuccess) return e;
-  if (T > 0) sort_histogram<<<blocks_for(T, 256), 256, 0, s>>>(ids, T, V, counts);
-  sort_scan<<<1, SCAN_THREADS, 0, s>>>(counts, V, offsets);
+  if (T > 0) launch_k(sort_histogram, blocks_for(T, 256), 256, 0, s, ids, T, V, counts);
+  launch_k(sort_scan, 1, SCAN_THREADS, 0, s, counts, V, offsets);
   if (T > 0) {
-    sort_scatter<<<blocks_for(T, 256), 256, 0, s>>>(ids, T, V, offsets, counts, perm);
-    sort_segments<<<blocks_for(V, 256), 256, 0, s>>>(offsets, V, perm);
+    launch_k(sort_scatter, blocks_for(T, 256), 256, 0, s, ids, T, V, offsets, counts, perm);
+    launch_k(sort_segments, blocks_for(V, 256), 256, 0, s, offsets, V, perm);
   }
   count_launches(T > 0 ? 4 : 1);
   return cudaGetLastError();
@@ -274,7 +288,7 @@ cudaError_t launch_segment_sum(const void* ws, int64_t V, int64_t T, const void*
   (void)T;
   const int* offsets = sort_offsets(const_cast<void*>(ws));
   const int* perm = sort_perm(const_cast<void*>(ws), V);
-  segment_sum_rows<<<blocks_for(V * 32, 256), 256, 0, s>>>(offsets, perm, V, dEmb, in_f32, h, dE,
+  launch_k(segment_sum_rows, blocks_for(V * 32, 256), 256, 0, s, offsets, perm, V, dEmb, in_f32, h, dE,
                                                            accumulate);
   count_launches(1);
   return cudaGetLastError();
@@ -305,6 +319,8 @@ __global__ void __launch_bounds__(32 * CE_SLICES) ce_reduce_kernel(const float2*
                                                         const int64_t* __restrict__ targets, int64_t V,
                                                         const float* __restrict__ target_logit,
                                                         float* __restrict__ loss, float* __restrict__ lse) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float sm[CE_SLICES][32], ss[CE_SLICES][32];
   const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
   const int64_t row = static_cast<int64_t>(blockIdx.x) * 32 + tx;
@@ -336,8 +352,7 @@ __global__ void __launch_bounds__(32 * CE_SLICES) ce_reduce_kernel(const float2*
 cudaError_t launch_ce_reduce(const void* part, int P, int64_t T, const int64_t* targets, int64_t V,
                              const float* target_logit, float* loss, float* lse, cudaStream_t s) {
   if (T <= 0) return cudaSuccess;
-  ce_reduce_kernel<<<static_cast<unsigned>((T + 31) / 32), 32 * CE_SLICES, 0, s>>>(
-      static_cast<const float2*>(part), P, T, targets, V, target_logit, loss, lse);
+  launch_k(ce_reduce_kernel, static_cast<unsigned>((T + 31) / 32), 32 * CE_SLICES, 0, s, static_cast<const float2*>(part), P, T, targets, V, target_logit, loss, lse);
   count_launches(1);
   return cudaGetLastError();
 }

@@ -53,6 +53,8 @@ __device__ __forceinline__ void epilogue_elem(const GemmGroup& G, int m, int n, 
 }
 
 __global__ void __launch_bounds__(STHREADS) simt_gemm_kernel(const __grid_constant__ SimtGemmParams p) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float As[SK][SB + 1];
   __shared__ float Bs[SK][SB + 1];
   const int tile = blockIdx.x;
@@ -105,6 +107,8 @@ __global__ void __launch_bounds__(STHREADS) simt_gemm_kernel(const __grid_consta
 // device math).
 __global__ void gelu_eval_kernel(const float* __restrict__ z, float* __restrict__ y,
                                  float* __restrict__ dy, int64_t n) {
+  pdl_wait();
+  pdl_trigger();
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const float v = z[i];
@@ -119,14 +123,14 @@ cudaError_t launch_gelu_eval(const float* z, float* y, float* dy, int64_t n, cud
   if (n <= 0) return cudaSuccess;
   int64_t blocks = (n + 255) / 256;
   if (blocks > 4096) blocks = 4096;
-  gelu_eval_kernel<<<static_cast<int>(blocks), 256, 0, s>>>(z, y, dy, n);
+  launch_k(gelu_eval_kernel, static_cast<int>(blocks), 256, 0, s, z, y, dy, n);
   count_launches(1);
   return cudaGetLastError();
 }
 
 cudaError_t launch_simt_gemm(const SimtGemmParams& p, cudaStream_t s) {
   if (p.total_tiles <= 0) return cudaSuccess;
-  simt_gemm_kernel<<<p.total_tiles, STHREADS, 0, s>>>(p);
+  launch_k(simt_gemm_kernel, p.total_tiles, STHREADS, 0, s, p);
   count_launches(1);
   return cudaGetLastError();
 }

@@ -615,32 +615,6 @@ __device__ __forceinline__ void epilogue_chunk(const GemmGroup& G, const CUtenso
   const int ncols = min(32, G.N - n);
   const bool coal = (ncols == 32) && G.vec_ok;  // warp-uniform
   if constexpr (ATTN) {
-    if (G.epi == EPI_SOFTMAX) {
-      // p = exp(alpha acc - lse) = 2^(acc alpha log2 e - lse log2 e); 0 for keys after the query
-      const float l2e = 1.4426950408889634f;
-      const float lse = row_ok ? G.row_lse[row] : 0.f;
-      const float a = G.alpha * l2e, base = -lse * l2e;
-      const int jmax = G.causal ? row - n : 31;  // columns j <= jmax are kept
-#pragma unroll
-      for (int j = 0; j < 32; ++j) v[j] = j <= jmax ? ex2_ftz(fmaf(v[j], a, base)) : 0.f;
-      if (coal) {
-        stage_store_rows(st, G.out, OUT_BF16, G.ldo, row0, G.M, n, v, lane, map1);
-      } else if (row_ok) {
-        store_chunk(G.out, OUT_BF16, G.ldo, row, n, v, ncols, false);
-      }
-      if (G.drop_mask != nullptr) {
-        // attention dropout: the kept probabilities, scaled, for the P V product
-        const uint32_t keep = row_ok ? G.drop_mask[static_cast<int64_t>(row) * G.drop_wpr + (n >> 5)] : 0u;
-#pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] = (keep >> j) & 1u ? v[j] * G.drop_scale : 0.f;
-        if (coal) {
-          stage_store_rows(st, G.out2, OUT_BF16, G.ldo, row0, G.M, n, v, lane, map2);
-        } else if (row_ok) {
-          store_chunk(G.out2, OUT_BF16, G.ldo, row, n, v, ncols, false);
-        }
-      }
-      return;
-    }
     if (G.epi == EPI_SMAX_BWD) {
       // dS = P * (dP - D) * alpha with P = aux, D = row_lse (the row's sum of P dP)
       float z[32];
@@ -1055,6 +1029,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // set-up done: wait until the previous kernel on the stream has completed
+  pdl_wait();
 
   const WaitCtx wctx{abort_flag, p.err, p.wait_limit_ns};
   const uint32_t tiles_base = smem_addr(smem);
@@ -1086,7 +1062,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_kernel(const __grid_co
       tile_ids[4 * r + 2] = tc.m0;
       tile_ids[4 * r + 3] = tc.n0;
       mbar_arrive(tile_full_bar(r));
-      if (t < 0) break;
+      if (t < 0) {
+        pdl_trigger();  // no tile left for this CTA: the next kernel may launch
+        break;
+      }
       // Next tile: the first gridDim tiles are static, the rest claimed in
       // order.  Without dependent tiles the claim is made now, so its atomic
       // round trip overlaps this tile's loads; with them it waits until this
@@ -1567,6 +1546,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_pair_kernel(const __gr
   cluster_sync_all();  // both CTAs' barriers are initialised before any remote arrive
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // set-up done: wait until the previous kernel on the stream has completed
+  pdl_wait();
 
   const WaitCtx2 wctx{abort_flag, map_to_rank(smem_addr(const_cast<int*>(abort_flag)), peer), p.err,
                       p.wait_limit_ns};
@@ -1620,7 +1601,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_pair_kernel(const __gr
         if (!take_tile(i, t, tc)) break;
         release_tile(i);
       }
-      if (t < 0) break;
+      if (t < 0) {
+        pdl_trigger();  // no tile left for this CTA: the next kernel may launch
+        break;
+      }
       // the leader claims the cluster's next tile (ahead when nothing waits; see the one-SM kernel)
       int next = -1;
       if (leader && claim_ahead) next = static_cast<int>(gridDim.x >> 1) + atomicAdd(sched, 1);
@@ -1866,27 +1850,29 @@ cudaError_t launch_tc_gemm(const TcGemmParams& p_in, int num_sms, cudaStream_t s
     if (clusters > p.total_tiles) clusters = p.total_tiles;
     if (clusters < 1) return cudaErrorInvalidConfiguration;
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = pdl_on() ? 1 : 0;
     cfg.gridDim = dim3(2 * clusters, 1, 1);
     cfg.blockDim = dim3(NUM_THREADS, 1, 1);
     cfg.dynamicSmemBytes = SMEM2_BYTES;
     cfg.stream = s;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     cudaError_t e = p.attn ? cudaLaunchKernelEx(&cfg, tc_gemm_pair_kernel<true>, p)
                            : cudaLaunchKernelEx(&cfg, tc_gemm_pair_kernel<false>, p);
     count_launches(1);
     return e != cudaSuccess ? e : cudaGetLastError();
   }
   const int grid = p.total_tiles < num_sms ? p.total_tiles : num_sms;
-  if (p.attn) tc_gemm_kernel<true><<<grid, NUM_THREADS, SMEM_BYTES, s>>>(p);
-  else tc_gemm_kernel<false><<<grid, NUM_THREADS, SMEM_BYTES, s>>>(p);
+  const cudaError_t e = p.attn ? launch_k(tc_gemm_kernel<true>, grid, NUM_THREADS, SMEM_BYTES, s, p)
+                               : launch_k(tc_gemm_kernel<false>, grid, NUM_THREADS, SMEM_BYTES, s, p);
   count_launches(1);
-  return cudaGetLastError();
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace tp

@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "tp.h"
 
 namespace tp {
@@ -28,7 +30,6 @@ enum Epi : int {
   EPI_CE_FWD = 5,     // cross-entropy partials: per row and 64-column part, (max, sum exp(acc - max))
                       // to ce_part; the logit at the row's target column to ce_target; no output
   EPI_CE_BWD = 6,     // out (bf16) = (exp(acc - row_lse[m]) - [col0 + n == row_target[m]]) * row_dloss[m]
-  EPI_SOFTMAX = 7,    // out (bf16) = exp(alpha acc - row_lse[m]), 0 where causal masks (n > m)
   EPI_SMAX_BWD = 8,   // out (bf16) = aux[m, n] * (acc - row_lse[m]) * alpha  (softmax backward)
   EPI_SMAX_PARTS = 9  // attention scores: per row and 64-column part, m = max of alpha acc over the
                       // columns causal keeps and (m, sum e) to ce_part; out (bf16) = e =
@@ -77,7 +78,8 @@ struct GemmGroup {
   // EPI_CE_FWD / EPI_CE_BWD: global column of the group's column 0 (its
   // vocabulary range start), per-row target ids; the forward writes part
   // (ce_part0 + n / 64) of row m at ce_part[2 * (part * ce_rows + m)] (max,
-  // sum); the backward reads row_lse and row_dloss.
+  // sum); the backward reads row_lse and row_dloss.  EPI_SMAX_PARTS writes
+  // its parts the same way.
   int64_t col0;
   const int64_t* row_target;
   const float* row_lse;
@@ -85,17 +87,17 @@ struct GemmGroup {
   float* ce_part;
   float* ce_target;
   int ce_part0, ce_rows;
-  // Attention: the accumulator is scaled by alpha in the CE_FWD, SOFTMAX and
-  // SMAX_BWD epilogues (CE_FWD: 1); causal masks columns n > m in CE_FWD and
-  // SOFTMAX; kr_mode selects the tile's k-block range (KRange).
+  // Attention: the accumulator is scaled by alpha in the CE_FWD, SMAX_PARTS
+  // and SMAX_BWD epilogues (CE_FWD: 1 outside attention); causal masks
+  // columns n > m in CE_FWD and SMAX_PARTS; kr_mode selects the tile's
+  // k-block range (KRange).
   float alpha;
   int causal, kr_mode;
   int tri_ok;  // KR_TRI tiles with no k-blocks need not run (their outputs are never read)
   int tri;     // set by the launcher: only the causal tiles are enumerated
   // Attention dropout: keep bits of row m, keys 32 w .. 32 w + 31, at
   // drop_mask[m * drop_wpr + w]; kept values are scaled by drop_scale.
-  // SOFTMAX then also stores the dropped probabilities to out2; SMAX_BWD
-  // scales its accumulator (dP) by the mask.
+  // SMAX_BWD scales its accumulator (dP) by the mask.
   const uint32_t* drop_mask;
   int drop_wpr;
   float drop_scale;
@@ -238,6 +240,37 @@ cudaError_t launch_adam_update(const OptParams& p, int num_sms, void* ws, cudaSt
 
 // Every kernel launch the library makes is counted (reported by the profiler).
 void count_launches(int n);
+
+// Programmatic dependent launch.  A kernel launched through launch_k may begin
+// while the previous kernel on its stream is still running, once every block
+// of that kernel has called pdl_trigger() or exited.  Before it touches global
+// memory every thread of it calls pdl_wait(), which returns once the previous
+// kernel has completed and its writes are visible (that kernel did the same,
+// so every earlier kernel has completed too).  Row kernels trigger at entry;
+// the persistent GEMMs when a CTA finds no tile left: the next kernel's launch
+// and block set-up then overlap their tail.  pdl_on() is the host switch
+// (tp_debug_set_pdl); off, launch_k launches plainly and pdl_wait returns at
+// once.
+bool pdl_on();
+#ifdef __CUDACC__
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+#endif
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                     Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = pdl_on() ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // Launchers (each returns the launch error).
 cudaError_t launch_tc_gemm(const TcGemmParams& p, int num_sms, cudaStream_t s);

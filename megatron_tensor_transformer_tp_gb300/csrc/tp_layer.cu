@@ -75,6 +75,8 @@ __global__ void __launch_bounds__(kLnThreads) ln_fwd_kernel(const __nv_bfloat16*
                                                             __nv_bfloat16* __restrict__ y,
                                                             float* __restrict__ mean_out,
                                                             float* __restrict__ rstd_out) {
+  pdl_wait();
+  pdl_trigger();
   constexpr int NV = PER / 8;
   __shared__ float red[kLnThreads / 32];
   const int64_t r0 = static_cast<int64_t>(blockIdx.x) * kLnFwdRows;
@@ -167,6 +169,8 @@ __global__ void __launch_bounds__(kLnThreads) ln_bwd_kernel(
     const float* __restrict__ g, const float* __restrict__ mean_in, const float* __restrict__ rstd_in,
     const __nv_bfloat16* __restrict__ dres, int64_t T, int64_t h, __nv_bfloat16* __restrict__ dx,
     float* __restrict__ partial) {
+  pdl_wait();
+  pdl_trigger();
   constexpr int NV = PER / 8;
   __shared__ float2 red[kLnThreads / 32];
   const int64_t r0 = static_cast<int64_t>(blockIdx.x) * kLnRows;
@@ -272,6 +276,8 @@ __global__ void __launch_bounds__(32 * kLnSumSlices) ln_param_grad_sum_kernel(co
                                                                              float* __restrict__ dg,
                                                                              float* __restrict__ db,
                                                                              int accumulate) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float red[kLnSumSlices][33];
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const int64_t c = static_cast<int64_t>(blockIdx.x) * 32 + lane;
@@ -296,6 +302,8 @@ __global__ void __launch_bounds__(256) dropout_add_kernel(const __nv_bfloat16* _
                                                           int64_t nblk, uint64_t seed, uint64_t stream,
                                                           uint32_t thr, float scale,
                                                           __nv_bfloat16* __restrict__ out) {
+  pdl_wait();
+  pdl_trigger();
   const int64_t blk = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (blk >= nblk) return;
   // the loads go out first; the Philox rounds run while they are in flight
@@ -333,6 +341,8 @@ __global__ void __launch_bounds__(256) pos_embed_dropout_kernel(
     const __nv_bfloat16* __restrict__ words, const __nv_bfloat16* __restrict__ pos_table,
     const int64_t* __restrict__ positions, int64_t h, int64_t max_pos, int64_t nblk, uint64_t seed,
     uint64_t stream, uint32_t thr, float scale, __nv_bfloat16* __restrict__ out) {
+  pdl_wait();
+  pdl_trigger();
   const int64_t blk = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (blk >= nblk) return;
   const int64_t e = blk * 16, row = e / h, col = e - row * h;
@@ -370,6 +380,8 @@ __global__ void __launch_bounds__(256) pos_embed_dropout_kernel(
 __global__ void __launch_bounds__(256) attn_keep_kernel(int64_t s, int wpr, int n_heads, int heads_per_shard,
                                                         int causal, uint64_t seed, uint64_t stream0,
                                                         uint32_t thr, uint32_t* __restrict__ words) {
+  pdl_wait();
+  pdl_trigger();
   const int w = blockIdx.x * blockDim.x + threadIdx.x;
   if (w >= wpr) return;
   const int64_t q = blockIdx.y, g = blockIdx.z;
@@ -407,9 +419,9 @@ cudaError_t launch_ln_fwd(const void* x, const float* g, const float* b, int64_t
   auto* yb = static_cast<__nv_bfloat16*>(y);
   const unsigned grid = static_cast<unsigned>((T + kLnFwdRows - 1) / kLnFwdRows);
   switch (ln_per(h)) {
-    case 8: ln_fwd_kernel<8><<<grid, kLnThreads, 0, st>>>(xb, g, b, T, h, eps, yb, mean, rstd); break;
-    case 16: ln_fwd_kernel<16><<<grid, kLnThreads, 0, st>>>(xb, g, b, T, h, eps, yb, mean, rstd); break;
-    case 32: ln_fwd_kernel<32><<<grid, kLnThreads, 0, st>>>(xb, g, b, T, h, eps, yb, mean, rstd); break;
+    case 8: launch_k(ln_fwd_kernel<8>, grid, kLnThreads, 0, st, xb, g, b, T, h, eps, yb, mean, rstd); break;
+    case 16: launch_k(ln_fwd_kernel<16>, grid, kLnThreads, 0, st, xb, g, b, T, h, eps, yb, mean, rstd); break;
+    case 32: launch_k(ln_fwd_kernel<32>, grid, kLnThreads, 0, st, xb, g, b, T, h, eps, yb, mean, rstd); break;
     default: return cudaErrorInvalidValue;
   }
   count_launches(1);
@@ -432,7 +444,7 @@ cudaError_t launch_ln_bwd(const void* dy, const void* x, const float* g, const f
   auto* dxb = static_cast<__nv_bfloat16*>(dx);
   const int ngroups = ln_bwd_blocks(T);
   const unsigned grid = static_cast<unsigned>(ngroups);
-#define TP_LNB(P) ln_bwd_kernel<P><<<grid, kLnThreads, 0, st>>>(dyb, xb, g, mean, rstd, rb, T, h, dxb, partial)
+#define TP_LNB(P) launch_k(ln_bwd_kernel<P>, grid, kLnThreads, 0, st, dyb, xb, g, mean, rstd, rb, T, h, dxb, partial)
   switch (ln_per(h)) {
     case 8: TP_LNB(8); break;
     case 16: TP_LNB(16); break;
@@ -440,8 +452,7 @@ cudaError_t launch_ln_bwd(const void* dy, const void* x, const float* g, const f
     default: return cudaErrorInvalidValue;
   }
 #undef TP_LNB
-  ln_param_grad_sum_kernel<<<static_cast<unsigned>((2 * h + 31) / 32), 32 * kLnSumSlices, 0, st>>>(
-      partial, ngroups, h, dg, db, accumulate);
+  launch_k(ln_param_grad_sum_kernel, static_cast<unsigned>((2 * h + 31) / 32), 32 * kLnSumSlices, 0, st, partial, ngroups, h, dg, db, accumulate);
   count_launches(2);
   return cudaGetLastError();
 }
@@ -450,8 +461,7 @@ cudaError_t launch_dropout_add(const void* x, const void* res, int64_t n, uint64
                                float p, void* out, cudaStream_t st) {
   const int64_t nblk = n / 16;
   if (nblk == 0) return cudaSuccess;
-  dropout_add_kernel<<<static_cast<unsigned>((nblk + 255) / 256), 256, 0, st>>>(
-      static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(res), nblk, seed, stream,
+  launch_k(dropout_add_kernel, static_cast<unsigned>((nblk + 255) / 256), 256, 0, st, static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(res), nblk, seed, stream,
       dropout_threshold(p), 1.0f / (1.0f - p), static_cast<__nv_bfloat16*>(out));
   count_launches(1);
   return cudaGetLastError();
@@ -462,8 +472,7 @@ cudaError_t launch_pos_embed_dropout(const void* words, const void* pos_table, c
                                      float p, void* out, cudaStream_t st) {
   const int64_t nblk = T * h / 16;
   if (nblk == 0) return cudaSuccess;
-  pos_embed_dropout_kernel<<<static_cast<unsigned>((nblk + 255) / 256), 256, 0, st>>>(
-      static_cast<const __nv_bfloat16*>(words), static_cast<const __nv_bfloat16*>(pos_table), positions, h,
+  launch_k(pos_embed_dropout_kernel, static_cast<unsigned>((nblk + 255) / 256), 256, 0, st, static_cast<const __nv_bfloat16*>(words), static_cast<const __nv_bfloat16*>(pos_table), positions, h,
       max_pos, nblk, seed, stream, dropout_threshold(p), 1.0f / (1.0f - p), static_cast<__nv_bfloat16*>(out));
   count_launches(1);
   return cudaGetLastError();
@@ -477,7 +486,7 @@ cudaError_t launch_attn_keep(int64_t pairs, int64_t s, int n_heads, int heads_pe
   const int bx = wpr < 256 ? wpr : 256;
   const dim3 grid(static_cast<unsigned>((wpr + bx - 1) / bx), static_cast<unsigned>(s),
                   static_cast<unsigned>(pairs));
-  attn_keep_kernel<<<grid, bx, 0, st>>>(s, wpr, n_heads, heads_per_shard, causal, seed, stream0,
+  launch_k(attn_keep_kernel, grid, bx, 0, st, s, wpr, n_heads, heads_per_shard, causal, seed, stream0,
                                         dropout_threshold(p), words);
   count_launches(1);
   return cudaGetLastError();

@@ -120,6 +120,8 @@ __global__ void __launch_bounds__(kOptThreads) opt_norm_kernel(const __grid_cons
                                                                double* __restrict__ partial,
                                                                int* __restrict__ flag,
                                                                OptControl* __restrict__ ctl, int slot) {
+  pdl_wait();
+  pdl_trigger();
   const float inv_scale = inv_scale_of(P);
   double acc = 0.0;
   int bad = 0;
@@ -199,6 +201,8 @@ __device__ __forceinline__ float adam_elem(float p, float g, float& m, float& v,
 
 __global__ void __launch_bounds__(kOptThreads) opt_adam_kernel(const __grid_constant__ OptParams P,
                                                                const OptControl* __restrict__ ctl) {
+  pdl_wait();
+  pdl_trigger();
   const OptControl c = *ctl;
   if (c.skip) return;
   for (int64_t ch = blockIdx.x; ch < P.nchunks; ch += gridDim.x) {
@@ -277,7 +281,7 @@ static int* ws_flag(void* ws) { return reinterpret_cast<int*>(ws_partial(ws) + k
 cudaError_t launch_adam_norm(const OptParams& P, int num_sms, void* ws, cudaStream_t s) {
   const int grid = opt_grid(opt_norm_kernel, P.nchunks, num_sms);
   const int slot = static_cast<int>(g_opt_slot_seq.fetch_add(1) % kOptSlots);
-  opt_norm_kernel<<<grid, kOptThreads, 0, s>>>(P, ws_partial(ws), ws_flag(ws),
+  launch_k(opt_norm_kernel, grid, kOptThreads, 0, s, P, ws_partial(ws), ws_flag(ws),
                                                static_cast<OptControl*>(ws), slot);
   count_launches(1);
   return cudaGetLastError();
@@ -285,7 +289,7 @@ cudaError_t launch_adam_norm(const OptParams& P, int num_sms, void* ws, cudaStre
 
 cudaError_t launch_adam_update(const OptParams& P, int num_sms, void* ws, cudaStream_t s) {
   const int grid = opt_grid(opt_adam_kernel, P.nchunks, num_sms);
-  opt_adam_kernel<<<grid, kOptThreads, 0, s>>>(P, static_cast<const OptControl*>(ws));
+  launch_k(opt_adam_kernel, grid, kOptThreads, 0, s, P, static_cast<const OptControl*>(ws));
   count_launches(1);
   return cudaGetLastError();
 }
