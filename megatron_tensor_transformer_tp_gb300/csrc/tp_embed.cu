@@ -35,8 +35,11 @@ __global__ void __launch_bounds__(256) embed_gather_vec16(const int64_t* __restr
                                                           int64_t row_bytes,
                                                           const __grid_constant__ RangeTable rt,
                                                           uint8_t* __restrict__ out) {
+  // No early trigger: the gather's blocks all fit in one wave, so a trigger at
+  // entry would start the next kernel's blocks at once, left waiting beside
+  // the gather's (measured 4% slower for back-to-back gathers); the next
+  // kernel launches as the gather's blocks exit.
   pdl_wait();
-  pdl_trigger();
   const int lane = threadIdx.x & 31;
   const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
   const int64_t nvec = row_bytes >> 4;
@@ -65,7 +68,6 @@ __global__ void __launch_bounds__(256) embed_gather_vec16(const int64_t* __restr
 __global__ void embed_gather_bytes(const int64_t* __restrict__ ids, int64_t T, int64_t row_bytes,
                                    const __grid_constant__ RangeTable rt, uint8_t* __restrict__ out) {
   pdl_wait();
-  pdl_trigger();
   const int lane = threadIdx.x & 31;
   const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
   for (int64_t t = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; t < T;

@@ -246,9 +246,9 @@ void count_launches(int n);
 // of that kernel has called pdl_trigger() or exited.  Before it touches global
 // memory every thread of it calls pdl_wait(), which returns once the previous
 // kernel has completed and its writes are visible (that kernel did the same,
-// so every earlier kernel has completed too).  Row kernels trigger at entry;
-// the persistent GEMMs when a CTA finds no tile left: the next kernel's launch
-// and block set-up then overlap their tail.  pdl_on() is the host switch
+// so every earlier kernel has completed too).  Row kernels trigger at entry
+// (the gather only by exiting); the persistent GEMMs when a CTA finds no tile
+// left: the next kernel's launch and block set-up then overlap their tail.  pdl_on() is the host switch
 // (tp_debug_set_pdl); off, launch_k launches plainly and pdl_wait returns at
 // once.
 bool pdl_on();
