@@ -70,3 +70,38 @@ def test_mlp_identical_with_and_without_pdl():
 def test_attention_core_identical_with_and_without_pdl():
     QKV, dC = AC.make_case(2, 256, 512, 31)
     _assert_equal(*_both(lambda: AC.run_core(QKV, dC, 256, 4, 2, True)))
+
+
+def test_tied_gradient_identical_with_and_without_pdl():
+    """The token grouping's four kernels, then the GEMM with the segment sums."""
+    from tests import test_gpu_embed as E
+    cfg = dict(kind="embed", dtype="bf16", V=5003, h=256, b=1, s=3001, ranges=[0, 1700, 5003], seed=22)
+    inp = SI.embed_inputs(cfg)
+
+    def run():
+        dE, ws = E.run_tied(inp)
+        offs, perm = E.sort_view(ws, inp["ids"].numel(), inp["V"])  # the grouping's results, not its scratch
+        return dE, torch.from_numpy(offs), torch.from_numpy(perm)
+
+    _assert_equal(*_both(run))
+
+
+def test_cross_entropy_identical_with_and_without_pdl():
+    """Statistics GEMM, the reduction kernel, then the gradient GEMM."""
+    from tests import test_gpu_ce as C
+    X, _, Es, targets, dloss = C.make_case(300, 256, [0, 700, 2048], seed=23)
+    _assert_equal(*_both(lambda: C.run_ce(X, Es, [0, 700, 2048], targets, dloss)))
+
+
+def test_adam_identical_with_and_without_pdl():
+    """The norm pass (finalized in its last block), then the update."""
+    from tests import test_gpu_opt as Op
+    groups = Op.make_groups([70001, 33, 4096])
+
+    def run():
+        d = Op.DeviceOpt(groups, Op.STATE)
+        st = d.step(Op.HYPER)
+        assert st["found_inf"] == 0
+        return [[g[k] for k in ("param", "m", "v", "model")] for g in d.g]
+
+    _assert_equal(*_both(run))
