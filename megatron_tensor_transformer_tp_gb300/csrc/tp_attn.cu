@@ -205,10 +205,11 @@ cudaError_t launch_attn_norm(const void* part, int P, int64_t s, int64_t pairs, 
     const dim3 grid(static_cast<unsigned>((s + kNormWarps - 1) / kNormWarps),
                     static_cast<unsigned>(pairs - g0 < kMaxGridY ? pairs - g0 : kMaxGridY));
     if (Pd != nullptr)
-      launch_k(attn_norm_kernel<true>, grid, 32 * kNormWarps, 0, st, static_cast<const float2*>(part), P, s, g0, causal, lse, static_cast<__nv_bfloat16*>(Pm),
-          static_cast<__nv_bfloat16*>(Pd), dr);
+      launch_k(attn_norm_kernel<true>, grid, 32 * kNormWarps, 0, st, static_cast<const float2*>(part), P, s,
+               g0, causal, lse, static_cast<__nv_bfloat16*>(Pm), static_cast<__nv_bfloat16*>(Pd), dr);
     else
-      launch_k(attn_norm_kernel<false>, grid, 32 * kNormWarps, 0, st, static_cast<const float2*>(part), P, s, g0, causal, lse, static_cast<__nv_bfloat16*>(Pm), nullptr, dr);
+      launch_k(attn_norm_kernel<false>, grid, 32 * kNormWarps, 0, st, static_cast<const float2*>(part), P, s,
+               g0, causal, lse, static_cast<__nv_bfloat16*>(Pm), nullptr, dr);
     count_launches(1);
   }
   return cudaGetLastError();
@@ -222,7 +223,7 @@ cudaError_t launch_attn_rowdot(const void* C, const void* dC, int64_t h, int64_t
     const dim3 grid(static_cast<unsigned>((s + 7) / 8),
                     static_cast<unsigned>(pairs - g0 < kMaxGridY ? pairs - g0 : kMaxGridY));
     launch_k(attn_rowdot_kernel, grid, 256, 0, st, static_cast<const __nv_bfloat16*>(C),
-                                             static_cast<const __nv_bfloat16*>(dC), h, s, n_heads, d, g0, vec, D);
+             static_cast<const __nv_bfloat16*>(dC), h, s, n_heads, d, g0, vec, D);
     count_launches(1);
   }
   return cudaGetLastError();

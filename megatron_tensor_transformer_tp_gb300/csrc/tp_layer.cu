@@ -444,7 +444,8 @@ cudaError_t launch_ln_bwd(const void* dy, const void* x, const float* g, const f
   auto* dxb = static_cast<__nv_bfloat16*>(dx);
   const int ngroups = ln_bwd_blocks(T);
   const unsigned grid = static_cast<unsigned>(ngroups);
-#define TP_LNB(P) launch_k(ln_bwd_kernel<P>, grid, kLnThreads, 0, st, dyb, xb, g, mean, rstd, rb, T, h, dxb, partial)
+#define TP_LNB(P) \
+  launch_k(ln_bwd_kernel<P>, grid, kLnThreads, 0, st, dyb, xb, g, mean, rstd, rb, T, h, dxb, partial)
   switch (ln_per(h)) {
     case 8: TP_LNB(8); break;
     case 16: TP_LNB(16); break;
@@ -452,7 +453,8 @@ cudaError_t launch_ln_bwd(const void* dy, const void* x, const float* g, const f
     default: return cudaErrorInvalidValue;
   }
 #undef TP_LNB
-  launch_k(ln_param_grad_sum_kernel, static_cast<unsigned>((2 * h + 31) / 32), 32 * kLnSumSlices, 0, st, partial, ngroups, h, dg, db, accumulate);
+  launch_k(ln_param_grad_sum_kernel, static_cast<unsigned>((2 * h + 31) / 32), 32 * kLnSumSlices, 0, st,
+           partial, ngroups, h, dg, db, accumulate);
   count_launches(2);
   return cudaGetLastError();
 }
@@ -461,8 +463,9 @@ cudaError_t launch_dropout_add(const void* x, const void* res, int64_t n, uint64
                                float p, void* out, cudaStream_t st) {
   const int64_t nblk = n / 16;
   if (nblk == 0) return cudaSuccess;
-  launch_k(dropout_add_kernel, static_cast<unsigned>((nblk + 255) / 256), 256, 0, st, static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(res), nblk, seed, stream,
-      dropout_threshold(p), 1.0f / (1.0f - p), static_cast<__nv_bfloat16*>(out));
+  launch_k(dropout_add_kernel, static_cast<unsigned>((nblk + 255) / 256), 256, 0, st,
+           static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(res), nblk, seed, stream,
+           dropout_threshold(p), 1.0f / (1.0f - p), static_cast<__nv_bfloat16*>(out));
   count_launches(1);
   return cudaGetLastError();
 }
@@ -472,8 +475,10 @@ cudaError_t launch_pos_embed_dropout(const void* words, const void* pos_table, c
                                      float p, void* out, cudaStream_t st) {
   const int64_t nblk = T * h / 16;
   if (nblk == 0) return cudaSuccess;
-  launch_k(pos_embed_dropout_kernel, static_cast<unsigned>((nblk + 255) / 256), 256, 0, st, static_cast<const __nv_bfloat16*>(words), static_cast<const __nv_bfloat16*>(pos_table), positions, h,
-      max_pos, nblk, seed, stream, dropout_threshold(p), 1.0f / (1.0f - p), static_cast<__nv_bfloat16*>(out));
+  launch_k(pos_embed_dropout_kernel, static_cast<unsigned>((nblk + 255) / 256), 256, 0, st,
+           static_cast<const __nv_bfloat16*>(words), static_cast<const __nv_bfloat16*>(pos_table), positions, h,
+           max_pos, nblk, seed, stream, dropout_threshold(p), 1.0f / (1.0f - p),
+           static_cast<__nv_bfloat16*>(out));
   count_launches(1);
   return cudaGetLastError();
 }
@@ -487,7 +492,7 @@ cudaError_t launch_attn_keep(int64_t pairs, int64_t s, int n_heads, int heads_pe
   const dim3 grid(static_cast<unsigned>((wpr + bx - 1) / bx), static_cast<unsigned>(s),
                   static_cast<unsigned>(pairs));
   launch_k(attn_keep_kernel, grid, bx, 0, st, s, wpr, n_heads, heads_per_shard, causal, seed, stream0,
-                                        dropout_threshold(p), words);
+           dropout_threshold(p), words);
   count_launches(1);
   return cudaGetLastError();
 }

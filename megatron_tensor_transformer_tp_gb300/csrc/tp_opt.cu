@@ -281,8 +281,8 @@ static int* ws_flag(void* ws) { return reinterpret_cast<int*>(ws_partial(ws) + k
 cudaError_t launch_adam_norm(const OptParams& P, int num_sms, void* ws, cudaStream_t s) {
   const int grid = opt_grid(opt_norm_kernel, P.nchunks, num_sms);
   const int slot = static_cast<int>(g_opt_slot_seq.fetch_add(1) % kOptSlots);
-  launch_k(opt_norm_kernel, grid, kOptThreads, 0, s, P, ws_partial(ws), ws_flag(ws),
-                                               static_cast<OptControl*>(ws), slot);
+  launch_k(opt_norm_kernel, grid, kOptThreads, 0, s, P, ws_partial(ws), ws_flag(ws), static_cast<OptControl*>(ws),
+           slot);
   count_launches(1);
   return cudaGetLastError();
 }
