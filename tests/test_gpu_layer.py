@@ -56,7 +56,8 @@ def test_position_embed_dropout_parity():
     assert_close(out, ref, "bf16", "embedding output")
 
 
-def test_attn_core_dropout_parity():
+@pytest.mark.parametrize("causal", [True, False])
+def test_attn_core_dropout_parity(causal):
     tp = _tp()
     b, s, h, H, N, p, seed, layer = 2, 160, 256, 4, 2, 0.25, 11, 3
     T = b * s
@@ -69,14 +70,14 @@ def test_attn_core_dropout_parity():
     dQKV = torch.empty(T, 3 * h, dtype=torch.bfloat16, device="cuda")
     ws = torch.empty(tp.tp_attn_core_workspace_size(T, s, h, H), dtype=torch.uint8, device="cuda")
     stream0 = tp.layer_stream(layer, 0)
-    tp.tp_attn_core_dropout_fwd(Q, s, H, N, True, p, seed, stream0, P, Pd, C, None, ws)
-    tp.tp_attn_core_dropout_bwd(Q, P, Pd, C, dC.cuda(), s, H, N, True, p, seed, stream0, dQKV, ws)
+    tp.tp_attn_core_dropout_fwd(Q, s, H, N, causal, p, seed, stream0, P, Pd, C, None, ws)
+    tp.tp_attn_core_dropout_bwd(Q, P, Pd, C, dC.cuda(), s, H, N, causal, p, seed, stream0, dQKV, ws)
     assert tp.tp_get_status() == tp.TP_OK
     Qn = f64(QKV)
-    rC, rP = O.attention_core(Qn, s, H, N, True, f32p(p), seed, layer)
+    rC, rP = O.attention_core(Qn, s, H, N, causal, f32p(p), seed, layer)
     assert_close(C, rC, "bf16", "C", elementwise=False)  # sums products of the bf16 P
     assert_close(P, rP, "bf16", "P")
-    lower = np.tril(np.ones((s, s), dtype=bool))
+    lower = np.tril(np.ones((s, s), dtype=bool)) if causal else np.ones((s, s), dtype=bool)
     Pdn = Pd.float().cpu().numpy()
     for bi in range(b):
         for j in range(H):
