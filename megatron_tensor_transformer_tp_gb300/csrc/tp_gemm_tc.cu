@@ -291,8 +291,17 @@ __device__ __forceinline__ TileCoord decode_tile_rows(const TcGemmParams& p, con
     c.n0 = (local % G.tiles_n) * BN;
     return c;
   }
+  const int kr = ATTN ? ((G.flags >> 8) & 0xff) : 0;
+  if (ATTN && (kr == KR_END || kr == KR_BEGIN)) {
+    // causal contraction ranges: a row block's column tiles together (they
+    // share its A rows), longest contraction first
+    int mt = local / G.tiles_n;
+    if (kr == KR_END) mt = G.tiles_m - 1 - mt;
+    c.m0 = mt * ROWS;
+    c.n0 = (local % G.tiles_n) * BN;
+    return c;
+  }
   int mt = local % G.tiles_m;
-  if (ATTN && ((G.flags >> 8) & 0xff) == KR_END) mt = G.tiles_m - 1 - mt;  // longest contraction first
   c.m0 = mt * ROWS;
   c.n0 = (local / G.tiles_m) * BN;
   return c;
