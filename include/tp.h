@@ -651,8 +651,9 @@ TP_API void tp_debug_inject_fault(int kind);
 TP_API void tp_debug_set_gemm_kernel(int mode);
 /* Plans whose outputs depend on each other run as one launch (dependent tiles
  * wait for the tiles they read) unless they have more than `tiles_per_sm`
- * 128 x 256 tiles per SM; larger plans run as two launches, independent
- * outputs first.  Default 8; values <= 0 restore it. */
+ * 128 x 256 tiles per SM (5/2 times that, rounded down, when no tile waits on
+ * a column block of another output); larger plans run as two launches,
+ * independent outputs first.  Default 8; values <= 0 restore it. */
 TP_API void tp_debug_set_split_threshold(int tiles_per_sm);
 TP_API void tp_debug_set_wait_limit_ms(int ms);
 /* Programmatic dependent launch of the library's kernels: on (default), a

@@ -658,14 +658,23 @@ tp_status run_plan_impl(Plan& pl, tp_dtype dt, const char* name, cudaStream_t s)
   // Causal score outputs count the tiles that hold work (about half, plus the
   // diagonal), as in the kernel choice: the attention core's P with P V then
   // stays one launch (measured 77.5 -> 72.2 us on 8 heads of 512, s = 2048).
+  // Outputs whose tiles wait only on row blocks of others (the MLP forward's
+  // row-parallel tiles) keep one launch up to 2.5 times as many tiles: their
+  // long tiles start as their rows complete and fill the column-parallel
+  // tiles' last rounds (the H = 4096 layer's MLP forward, 1280 tiles on 152
+  // SMs: 376 -> 338 us as one launch); a tile that waits on a column block
+  // (dW, dK) waits for the producers' last row blocks, so those plans split
+  // at the base threshold (the attention backward as one launch: 95 -> 118 us).
   int total = 0;
-  bool has_dep = false;
+  bool has_dep = false, col_dep = false;
   for (int i = 0; i < ng; ++i) {
     const int rb = (groups[i].M + 127) / 128, t = rb * ((groups[i].N + 255) / 256);
     total += groups[i].kr_mode == KR_TRI ? (t + rb) / 2 : t;
     has_dep = has_dep || groups[i].dep_kind != DEP_NONE;
+    col_dep = col_dep || groups[i].dep_kind == DEP_COL;
   }
-  if (has_dep && total > g_split_tiles_per_sm * dev->num_sms) {
+  const int split_tiles = col_dep ? g_split_tiles_per_sm : g_split_tiles_per_sm * 5 / 2;
+  if (has_dep && total > split_tiles * dev->num_sms) {
     GemmGroup first[kMaxGroups], second[kMaxGroups];
     int n1 = 0, n2 = 0;
     for (int i = 0; i < ng; ++i) {
