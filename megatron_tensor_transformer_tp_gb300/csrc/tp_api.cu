@@ -386,8 +386,9 @@ tp_status launch_tc_groups(const Plan& pl, const bool* used, GemmGroup* groups, 
   if (ng == 0) return TP_OK;
   // Kernel choice (measured on GB300): the two-SM kernel (256 x 256 pair
   // tiles, 6-stage ring, 32 KB loaded per SM per k-block instead of 48 KB) is
-  // faster on large launches (over 6 one-SM tiles per SM, or 8 when tiles of
-  // the launch wait on other tiles of it), K-major or MN-major; the one-SM
+  // faster on large launches (over 5 one-SM tiles per SM; 6 for causal
+  // ranges, whose short tiles balance better at one SM; 8 when tiles of the
+  // launch wait on other tiles of it), K-major or MN-major; the one-SM
   // kernel (128 x 256 tiles) on small ones, where its finer tiles balance
   // better across SMs.
   // Causal attention outputs count the tiles that hold work: about half, plus
@@ -399,9 +400,10 @@ tp_status launch_tc_groups(const Plan& pl, const bool* used, GemmGroup* groups, 
   bool pair = g_gemm_mode == 1;
   if (g_gemm_mode == 2) {
     int64_t tiles128 = 0, kb_tiles = 0;
-    bool deps = false;
+    bool deps = false, ranges = false;
     for (int i = 0; i < ng; ++i) {
       deps = deps || groups[i].dep_kind != DEP_NONE;
+      ranges = ranges || groups[i].kr_mode != KR_NONE;
       const int64_t rb = (groups[i].M + 127) / 128, t = rb * ((groups[i].N + 255) / 256);
       const int64_t tw = groups[i].kr_mode != KR_NONE ? (t + rb) / 2 : t;
       int64_t kb = 0;
@@ -410,7 +412,7 @@ tp_status launch_tc_groups(const Plan& pl, const bool* used, GemmGroup* groups, 
       kb_tiles += tw * kb;
     }
     const int64_t sms = dev->num_sms;
-    pair = tiles128 > (deps ? 8 : 6) * sms || (tiles128 >= 2 * sms && kb_tiles > 500 * sms);
+    pair = tiles128 > (deps ? 8 : (ranges ? 6 : 5)) * sms || (tiles128 >= 2 * sms && kb_tiles > 500 * sms);
   }
   // Tile width: 256 for every output.  (128-wide tiles for the long dependent
   // contractions of small fused launches were measured slower on GB300: a
