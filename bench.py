@@ -919,7 +919,8 @@ def main(argv=None):
             "bound": top["bound"], "achieved": r4(top["achieved"]), "peak": top["peak"],
             "unit": top["unit"], "frac": r4(top["frac"]), "traffic": top["traffic"],
             "kernel": top["kernel"], "peak_source": top["peak_source"],
-            "avg_launch_us": r4(top["avg_us"]), "launches": top["launches"]},
+            "avg_launch_us": r4(top["avg_us"]), "launches": top["launches"],
+            "launches_per_call": r4(top["kernel_launches_per_call"])},
         "kernels_frac": {k["kernel"]: r4(k["frac"]) for k in kernels},
         "embed_gather": None if gather is None else {
             "value": r4(gather["value"]), "unit": "GB/s", "frac": r4(gather["frac"]),
