@@ -43,3 +43,31 @@ def test_fewer_than_three_warmup_steps_are_refused():
     for impl in ("ours", "reference"):
         r = _run("--impl", impl, "--steps", "3", "--warmup", "2")
         assert r.returncode == 2 and "warmup" in r.stderr
+
+
+def test_roofline_achieved_recomputes_from_the_per_call_time():
+    """`achieved` is the work of one call divided by the kernel's device time
+    per call (its launches in the call summed), and the line says how many
+    launches a call holds, so a reader can recompute it from the line alone."""
+    import bench
+
+    class FakeBench:
+        name = "no_such_workload"
+
+        @staticmethod
+        def kernel_work():
+            return {"gemm_two": ("tensor", 2.0e12), "rows": ("hbm", 4.0e8)}
+
+    # 10 calls of two launches in 12.5 ms; 10 calls of one launch in 0.5 ms
+    prof = {"gemm_two": (10, 20, 12.5), "rows": (10, 10, 0.5)}
+    peaks = {"bf16_tflops": 2000.0, "bf16_tflops_sustained": 1800.0, "hbm_gbs": 8000.0}
+    top, kernels = bench.roofline_for(None, FakeBench, prof, peaks, "measured", sustained=False)
+    assert top["kernel"] == "gemm_two" and top["kernel_launches_per_call"] == 2
+    assert abs(top["avg_us"] - 1250.0) < 1e-9
+    assert abs(top["achieved"] - 2.0e12 / (top["avg_us"] * 1e-6) / 1e12) < 1e-9
+    assert abs(top["frac"] - top["achieved"] / 2000.0) < 1e-12
+    assert top["traffic"] is None  # no committed counters for this workload
+    assert "bf16_tflops" in top["peak_source"] and "sustained" not in top["peak_source"]
+    rows = {k["kernel"]: k for k in kernels}
+    assert abs(rows["rows"]["achieved"] - 4.0e8 / 50e-6 / 1e9) < 1e-9 and rows["rows"]["unit"] == "GB/s"
+    assert abs(sum(k["share"] for k in kernels) - 1.0) < 1e-12
