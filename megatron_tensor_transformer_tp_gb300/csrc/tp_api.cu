@@ -397,6 +397,11 @@ tp_status launch_tc_groups(const Plan& pl, const bool* used, GemmGroup* groups, 
   // model-width FFN) also take
   // the two-SM kernel once they hold two one-SM tiles per SM: there the lower
   // operand traffic per SM pays and the tile count no longer sets the balance.
+  // So do launches of at least one one-SM tile per SM whose tiles average 48
+  // k-blocks or more (without causal ranges): both kernels then need the same
+  // number of rounds, and the pair tiles' long main loops hide their epilogue
+  // (the H = 4096 layer's output projection, 256 one-SM tiles of 64 k-blocks:
+  // 62.4 -> 59.1 us).
   bool pair = g_gemm_mode == 1;
   if (g_gemm_mode == 2) {
     int64_t tiles128 = 0, kb_tiles = 0;
@@ -412,7 +417,8 @@ tp_status launch_tc_groups(const Plan& pl, const bool* used, GemmGroup* groups, 
       kb_tiles += tw * kb;
     }
     const int64_t sms = dev->num_sms;
-    pair = tiles128 > (deps ? 8 : (ranges ? 6 : 5)) * sms || (tiles128 >= 2 * sms && kb_tiles > 500 * sms);
+    pair = tiles128 > (deps ? 8 : (ranges ? 6 : 5)) * sms || (tiles128 >= 2 * sms && kb_tiles > 500 * sms) ||
+           (!ranges && tiles128 >= sms && kb_tiles >= 48 * tiles128);
   }
   // Tile width: 256 for every output.  (128-wide tiles for the long dependent
   // contractions of small fused launches were measured slower on GB300: a
