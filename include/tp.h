@@ -646,8 +646,12 @@ TP_API void tp_debug_inject_fault(int kind);
 /* Selects the tensor-core GEMM kernel for bf16 work: 0 the one-SM kernel
  * (128 x 256 tiles), 1 the two-SM kernel (CTA pairs computing 256 x 256 tiles
  * with tcgen05 cta_group::2), 2 (default) per launch: the two-SM kernel for
- * large launches with MN-major operands, the one-SM kernel otherwise.  All
- * give the same results up to fp32 summation order; tests run each. */
+ * launches of more than 5 one-SM tiles per SM (6 with causal contraction
+ * ranges, 8 when tiles wait on other tiles of the launch), of very long
+ * contractions (over 500 k-blocks of tiles per SM with at least 2 tiles per
+ * SM) or of long tiles (at least 1 tile per SM averaging 48 k-blocks or more,
+ * no causal ranges); the one-SM kernel otherwise.  All give the same results
+ * up to fp32 summation order; tests run each. */
 TP_API void tp_debug_set_gemm_kernel(int mode);
 /* Plans whose outputs depend on each other run as one launch (dependent tiles
  * wait for the tiles they read) unless they have more than `tiles_per_sm`
