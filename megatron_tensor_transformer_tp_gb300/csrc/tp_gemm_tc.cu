@@ -35,6 +35,7 @@
 #include <stdint.h>
 
 #include <atomic>
+#include <mutex>
 
 #include "tp_device.cuh"
 #include "tp_internal.h"
@@ -1815,42 +1816,58 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) tc_gemm_pair_kernel(const __gr
   }
 }
 
+// One-time set-up per device: the kernels' shared-memory limit is an
+// attribute of each device's copy of the kernel, and the pair grid is sized
+// by that device's occupancy.  Guarded so that threads making their first
+// calls at the same time set it up once.
+struct LaunchSetup {
+  std::once_flag once;
+  cudaError_t err = cudaSuccess;
+  int max_clusters = 0;
+};
+constexpr int kSetupDevices = 64;
+LaunchSetup g_setup[kSetupDevices];
+
+cudaError_t setup_device(LaunchSetup& st, int num_sms) {
+  cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       SMEM_BYTES);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(tc_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(tc_gemm_pair_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             SMEM2_BYTES);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(tc_gemm_pair_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             SMEM2_BYTES);
+  if (e != cudaSuccess) return e;
+  // Every cluster of the persistent grid must be resident at once (tiles
+  // may wait on tiles other clusters hold), so size the grid by occupancy.
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(2 * (num_sms / 2), 1, 1);
+  cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = SMEM2_BYTES;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaOccupancyMaxActiveClusters(&st.max_clusters, tc_gemm_pair_kernel<false>, &cfg);
+}
+
 }  // namespace
 
 cudaError_t launch_tc_gemm(const TcGemmParams& p_in, int num_sms, cudaStream_t s) {
-  static bool attr_set = false;
-  static int max_clusters = 0;
   static std::atomic<unsigned> slot_seq{0};  // launch slots rotate across all host threads
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<false>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(tc_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               SMEM_BYTES);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(tc_gemm_pair_kernel<false>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM2_BYTES);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(tc_gemm_pair_kernel<true>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM2_BYTES);
-    if (e != cudaSuccess) return e;
-    // Every cluster of the persistent grid must be resident at once (tiles
-    // may wait on tiles other clusters hold), so size the grid by occupancy.
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.gridDim = dim3(2 * (num_sms / 2), 1, 1);
-    cfg.blockDim = dim3(NUM_THREADS, 1, 1);
-    cfg.dynamicSmemBytes = SMEM2_BYTES;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    e = cudaOccupancyMaxActiveClusters(&max_clusters, tc_gemm_pair_kernel<false>, &cfg);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  int dev = 0;
+  cudaError_t de = cudaGetDevice(&dev);
+  if (de != cudaSuccess) return de;
+  if (dev < 0 || dev >= kSetupDevices) return cudaErrorInvalidDevice;
+  LaunchSetup& st = g_setup[dev];
+  std::call_once(st.once, [&] { st.err = setup_device(st, num_sms); });
+  if (st.err != cudaSuccess) return st.err;
+  const int max_clusters = st.max_clusters;
   if (p_in.total_tiles <= 0) return cudaSuccess;
   TcGemmParams& p = const_cast<TcGemmParams&>(p_in);
   p.sched_slot = static_cast<int>(slot_seq.fetch_add(1) % kSchedSlots);

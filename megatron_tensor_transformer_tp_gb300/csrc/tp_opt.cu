@@ -260,14 +260,17 @@ size_t opt_workspace_bytes() {
 // same share of chunks and no partial second wave), never more than chunks.
 template <class K>
 int opt_grid(K kernel, int64_t nchunks, int num_sms) {
-  static int per_sm = 0;  // same build, same GPU model: computed once
-  if (per_sm == 0) {
-    int b = 0;
+  // Blocks per SM depend on the kernel's resources and the architecture
+  // only (one build, one GPU model): computed on first use; threads racing on
+  // it compute the same value.
+  static std::atomic<int> per_sm{0};
+  int b = per_sm.load(std::memory_order_relaxed);
+  if (b == 0) {
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, kernel, kOptThreads, 0) != cudaSuccess || b < 1)
       b = 1;
-    per_sm = b;
+    per_sm.store(b, std::memory_order_relaxed);
   }
-  int64_t g = static_cast<int64_t>(num_sms) * per_sm;
+  int64_t g = static_cast<int64_t>(num_sms) * b;
   if (g > kMaxOptGrid) g = kMaxOptGrid;
   if (g > nchunks) g = nchunks;
   return g < 1 ? 1 : static_cast<int>(g);
