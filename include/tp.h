@@ -48,9 +48,10 @@
  *  - First call on a device: the first call of any entry point with a device
  *    current does one-time set-up (looks up the library's static device
  *    symbols, writes its block of ones, sets kernel attributes), which may
- *    load the module and synchronise the device.  Make one call per device
- *    during set-up, before any stream capture and before latency-sensitive
- *    stream work.
+ *    load the module and synchronise the device.  It runs once per device,
+ *    also when several host threads make their first calls together.  Make
+ *    one call per device during set-up, before any stream capture and before
+ *    latency-sensitive stream work.
  *  - accumulate: 0 = overwrite the gradient outputs, 1 = add into them.
  */
 #ifndef TP_H_
